@@ -1,0 +1,552 @@
+// api.cpp - the C ABI: descriptor validation, buffer sizing, weight layout,
+// and the per-call launch sequence (host orchestration, one CUDA stream).
+//
+// Forward, per layer:   pack W_ih / W_hh / biases into the 4-slot order ->
+//   input-projection GEMM over all timesteps -> h0 into the output buffer's
+//   boundary slot -> one persistent recurrent launch for all steps (both
+//   directions together when they fit) -> (last layer) copy / transpose y out.
+// Backward data, per layer from the top: pack W_hh^T and W_ih^T -> one
+//   persistent BPTT launch (writes dG and the bias-gradient sums) -> input-
+//   gradient GEMM dX = dG W_ih (feeds the layer below).
+// Backward weights, per layer and direction: dW_ih = dG^T X and
+//   dW_hh = dG^T H_prev as long-K GEMMs writing straight into the caller's gate
+//   order, and the bias gradients scattered from the sums.
+// The split mirrors cudnnRNNForwardTraining / BackwardData / BackwardWeights as
+// SystemDS LibMatrixCuDNN.java calls them in ``lstm`` / ``lstmBackward``.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "rnn.h"
+#include "rnn_internal.h"
+
+using namespace rnn;
+
+struct rnn_handle_s {
+  rnn_desc_t desc;
+  int L, D, T, B, H, I, G;
+  int lstm, ra, rb, bf16, bfirst;
+  int pos[4];          // canonical gate c sits in the caller's block pos[c]
+  int algo;            // RNN_ALGO_PERSIST_TC or RNN_ALGO_PERSIST_SIMT
+  int device, num_sms;
+  size_t es;
+  DevArea* dev;
+  uint64_t timeout_ns;
+  int skip_cta;
+  uint64_t launches;
+  bool trace;
+  // weight offsets (elements), per layer and direction
+  std::vector<size_t> off_ih, off_hh, off_b, off_bh;
+  size_t weight_elems;
+  // reserve offsets (bytes), per layer
+  std::vector<size_t> r_y, r_g, r_c, r_rh, r_dg, r_db;
+  size_t reserve_bytes;
+  // workspace offsets (bytes)
+  size_t w_p, w_xin, w_dyi, w_dx0, w_wx, w_wxt, w_wr, w_wrt, w_bx, w_bh, w_y0, w_y1, w_rh, w_g;
+  size_t workspace_bytes;
+};
+
+namespace {
+
+size_t al(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+struct Bump {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off = al(off + bytes);
+    return o;
+  }
+};
+
+int layer_in(const rnn_handle_s* h, int l) { return l == 0 ? h->I : h->D * h->H; }
+
+rnn_status_t st(int rc) { return static_cast<rnn_status_t>(rc); }
+
+#define RNN_TRY(expr)                         \
+  do {                                        \
+    int _rc = (expr);                         \
+    if (_rc) return st(_rc);                  \
+  } while (0)
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+void trace(rnn_handle_s* h, const char* what) {
+  if (h->trace) std::fprintf(stderr, "[rnn] %s\n", what);
+}
+
+void fill_layout(rnn_handle_s* h) {
+  const int L = h->L, D = h->D, T = h->T, B = h->B, H = h->H, G = h->G;
+  const size_t es = h->es;
+  // weights
+  size_t o = 0;
+  h->off_ih.assign(L * D, 0); h->off_hh.assign(L * D, 0); h->off_b.assign(L * D, 0); h->off_bh.assign(L * D, 0);
+  for (int l = 0; l < L; ++l)
+    for (int d = 0; d < D; ++d) {
+      const int i = l * D + d;
+      h->off_ih[i] = o; o += static_cast<size_t>(G) * H * layer_in(h, l);
+      h->off_hh[i] = o; o += static_cast<size_t>(G) * H * H;
+      h->off_b[i] = o; o += static_cast<size_t>(G) * H;
+      if (h->ra) { h->off_bh[i] = o; o += static_cast<size_t>(G) * H; }
+    }
+  h->weight_elems = o;
+  // reserve
+  Bump r;
+  h->r_y.assign(L, 0); h->r_g.assign(L, 0); h->r_c.assign(L, 0); h->r_rh.assign(L, 0);
+  h->r_dg.assign(L, 0); h->r_db.assign(L, 0);
+  const size_t TB = static_cast<size_t>(T) * B;
+  for (int l = 0; l < L; ++l) {
+    h->r_y[l] = r.take(static_cast<size_t>(T + 2) * B * D * H * es);
+    h->r_g[l] = r.take(static_cast<size_t>(D) * TB * 4 * H * es);
+    if (h->lstm) h->r_c[l] = r.take(static_cast<size_t>(D) * (T + 1) * B * H * 4);
+    if (h->rb) h->r_rh[l] = r.take(static_cast<size_t>(D) * TB * H * es);
+    h->r_dg[l] = r.take(TB * D * 4 * H * es);
+    h->r_db[l] = r.take(static_cast<size_t>(D) * 4 * H * 4);
+  }
+  h->reserve_bytes = r.off;
+  // workspace
+  int Imax = h->I > D * H ? h->I : D * H;
+  Bump w;
+  h->w_p = w.take(TB * D * 4 * H * es);
+  h->w_xin = h->bfirst ? w.take(TB * h->I * es) : 0;
+  h->w_dyi = w.take(TB * D * H * 4);
+  h->w_dx0 = h->bfirst ? w.take(TB * h->I * es) : 0;
+  h->w_wx = w.take(static_cast<size_t>(D) * 4 * H * Imax * es);
+  h->w_wxt = w.take(static_cast<size_t>(Imax) * D * 4 * H * es);
+  h->w_wr = w.take(static_cast<size_t>(D) * 4 * H * H * es);
+  h->w_wrt = w.take(static_cast<size_t>(D) * H * 4 * H * es);
+  h->w_bx = w.take(static_cast<size_t>(D) * 4 * H * 4);
+  h->w_bh = w.take(static_cast<size_t>(D) * 4 * H * 4);
+  // inference (reserve == NULL): two output buffers and the reset-before exchange
+  h->w_y0 = w.take(static_cast<size_t>(T + 2) * B * D * H * es);
+  h->w_y1 = w.take(static_cast<size_t>(T + 2) * B * D * H * es);
+  h->w_rh = h->rb ? w.take(static_cast<size_t>(D) * TB * H * es) : 0;
+  h->w_g = 0;
+  h->workspace_bytes = w.off;
+}
+
+// internal slot s -> caller's gate block (-1: zero / not used)
+void slots_fwd(const rnn_handle_s* h, int* m) {
+  if (h->lstm) { for (int s = 0; s < 4; ++s) m[s] = h->pos[s]; }
+  else { m[0] = h->pos[0]; m[1] = h->pos[1]; m[2] = h->pos[2]; m[3] = -1; }
+}
+void slots_bwd_rec(const rnn_handle_s* h, int* m) {
+  if (h->lstm) { for (int s = 0; s < 4; ++s) m[s] = h->pos[s]; }
+  else if (h->ra) { m[0] = h->pos[0]; m[1] = h->pos[1]; m[2] = -1; m[3] = h->pos[2]; }
+  else { m[0] = h->pos[0]; m[1] = h->pos[1]; m[2] = h->pos[2]; m[3] = -1; }
+}
+
+int count(rnn_handle_s* h, int rc, int n = 1) {
+  if (rc == 0) h->launches += n;
+  return rc;
+}
+
+int run_gemm(rnn_handle_s* h, GemmArgs g, cudaStream_t s) {
+  if (g.M <= 0 || g.N <= 0) return 0;
+  if (g.K <= 0) return 2;
+  g.in_bf16 = h->bf16;
+  if (h->bf16 && gemm_tc_supported(g)) return count(h, launch_gemm_tc(g, s, h->num_sms, h->dev, h->timeout_ns));
+  return count(h, launch_gemm_simt(g, s));
+}
+
+int reset_counters(rnn_handle_s* h, cudaStream_t s) {
+  return cudaMemsetAsync(h->dev->counters, 0, sizeof(h->dev->counters), s) == cudaSuccess ? 0 : 3;
+}
+
+// One persistent launch per layer (both directions), or one per direction
+// when both do not fit on the GPU at once.
+int run_persist(rnn_handle_s* h, PersistArgs a, bool bwd, cudaStream_t s) {
+  a.dev = h->dev;
+  a.timeout_ns = h->timeout_ns;
+  a.skip_cta = h->skip_cta;
+  auto go = [&](PersistArgs& x) -> int {
+    int rc = reset_counters(h, s);
+    if (rc) return rc;
+    if (h->algo == RNN_ALGO_PERSIST_TC)
+      rc = bwd ? launch_persist_bwd_tc(x, s, h->num_sms) : launch_persist_fwd_tc(x, s, h->num_sms);
+    else
+      rc = bwd ? launch_persist_bwd_simt(x, s, h->num_sms) : launch_persist_fwd_simt(x, s, h->num_sms);
+    return count(h, rc);
+  };
+  a.dir0 = 0;
+  a.ndir = h->D;
+  int rc = go(a);
+  if (rc != 2 || h->D == 1) return rc;
+  for (int d = 0; d < h->D; ++d) {
+    a.dir0 = d;
+    a.ndir = 1;
+    rc = go(a);
+    if (rc) return rc;
+  }
+  return 0;
+}
+
+rnn_status_t check_desc(const rnn_desc_t* d) {
+  if (!d) return RNN_BAD_PARAM;
+  if (d->mode != RNN_LSTM && d->mode != RNN_GRU) return RNN_BAD_PARAM;
+  if (d->dtype != RNN_F32 && d->dtype != RNN_BF16) return RNN_BAD_PARAM;
+  if (d->num_layers < 1 || d->num_layers > 8) return RNN_BAD_PARAM;
+  if (d->seq_len < 1 || d->batch < 1 || d->input_size < 1 || d->hidden_size < 1) return RNN_BAD_PARAM;
+  if (d->bidirectional != 0 && d->bidirectional != 1) return RNN_BAD_PARAM;
+  if (d->batch_first != 0 && d->batch_first != 1) return RNN_BAD_PARAM;
+  if (d->algo < RNN_ALGO_AUTO || d->algo > RNN_ALGO_PERSIST_SIMT) return RNN_BAD_PARAM;
+  const int G = d->mode == RNN_LSTM ? 4 : 3;
+  bool all_zero = true;
+  for (int k = 0; k < 4; ++k) all_zero = all_zero && d->gate_order[k] == 0;
+  if (!all_zero) {
+    int seen = 0;
+    for (int k = 0; k < G; ++k) {
+      const int c = d->gate_order[k];
+      if (c < 0 || c >= G || (seen >> c) & 1) return RNN_BAD_PARAM;
+      seen |= 1 << c;
+    }
+  }
+  // element counts must stay addressable with 32-bit grid dimensions
+  const long long TB = static_cast<long long>(d->seq_len) * d->batch;
+  if (TB > (1LL << 30)) return RNN_BAD_PARAM;
+  // vectorised 4-slot accesses need 16-byte aligned rows
+  if (d->dtype == RNN_BF16 && (d->hidden_size % 8 || d->input_size % 8)) return RNN_NOT_SUPPORTED;
+  if (d->dtype == RNN_F32 && (d->hidden_size % 4 || d->input_size % 4)) return RNN_NOT_SUPPORTED;
+  return RNN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rnn_status_string(rnn_status_t s) {
+  switch (s) {
+    case RNN_OK: return "RNN_OK";
+    case RNN_BAD_PARAM: return "RNN_BAD_PARAM: invalid descriptor field or pointer";
+    case RNN_NOT_SUPPORTED: return "RNN_NOT_SUPPORTED: valid but not supported on this GPU / build";
+    case RNN_CUDA_ERROR: return "RNN_CUDA_ERROR: a CUDA call failed";
+    case RNN_TIMEOUT: return "RNN_TIMEOUT: a device spin-wait ran out of time";
+    case RNN_BAD_WORKSPACE: return "RNN_BAD_WORKSPACE: workspace / reserve missing or misaligned";
+    case RNN_INTERNAL: return "RNN_INTERNAL: internal error";
+  }
+  return "unknown rnn_status_t";
+}
+
+rnn_status_t rnn_create(const rnn_desc_t* desc, rnn_handle_t* out) {
+  if (!out) return RNN_BAD_PARAM;
+  *out = nullptr;
+  rnn_status_t rs = check_desc(desc);
+  if (rs != RNN_OK) return rs;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RNN_CUDA_ERROR;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return RNN_CUDA_ERROR;
+  if (!(prop.major == 10 && prop.minor == 3)) return RNN_NOT_SUPPORTED;
+
+  rnn_handle_s* h = new (std::nothrow) rnn_handle_s();
+  if (!h) return RNN_INTERNAL;
+  h->desc = *desc;
+  h->L = desc->num_layers; h->D = desc->bidirectional ? 2 : 1;
+  h->T = desc->seq_len; h->B = desc->batch; h->H = desc->hidden_size; h->I = desc->input_size;
+  h->lstm = desc->mode == RNN_LSTM;
+  h->G = h->lstm ? 4 : 3;
+  h->ra = !h->lstm && desc->reset_after;
+  h->rb = !h->lstm && !desc->reset_after;
+  h->bf16 = desc->dtype == RNN_BF16;
+  h->bfirst = desc->batch_first;
+  h->es = h->bf16 ? 2 : 4;
+  bool all_zero = true;
+  for (int k = 0; k < 4; ++k) all_zero = all_zero && desc->gate_order[k] == 0;
+  for (int c = 0; c < 4; ++c) h->pos[c] = c;
+  if (!all_zero)
+    for (int k = 0; k < h->G; ++k) h->pos[desc->gate_order[k]] = k;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->timeout_ns = 2000000000ull;
+  h->skip_cta = -1;
+  h->launches = 0;
+  const char* tr = std::getenv("RNN_TRACE");
+  h->trace = tr && tr[0] == '1';
+  fill_layout(h);
+
+  // recurrent kernel choice
+  const bool tc_ok = h->bf16 && persist_tc_supported(desc->mode, h->ra, h->H, h->B, 1, h->num_sms);
+  PersistArgs probe;
+  probe.mode = desc->mode; probe.reset_after = h->ra; probe.is_bf16 = h->bf16;
+  probe.T = h->T; probe.B = h->B; probe.H = h->H; probe.D = h->D; probe.ndir = 1;
+  const bool simt_ok = plan_persist_simt(probe, h->num_sms, nullptr, nullptr) == 0;
+  if (desc->algo == RNN_ALGO_PERSIST_TC) h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : 0;
+  else if (desc->algo == RNN_ALGO_PERSIST_SIMT) h->algo = simt_ok ? RNN_ALGO_PERSIST_SIMT : 0;
+  else h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : (simt_ok ? RNN_ALGO_PERSIST_SIMT : 0);
+  if (h->algo == 0) { delete h; return RNN_NOT_SUPPORTED; }
+
+  if (cudaMalloc(&h->dev, sizeof(DevArea)) != cudaSuccess) { delete h; return RNN_CUDA_ERROR; }
+  if (cudaMemset(h->dev, 0, sizeof(DevArea)) != cudaSuccess) { cudaFree(h->dev); delete h; return RNN_CUDA_ERROR; }
+  *out = h;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_destroy(rnn_handle_t h) {
+  if (!h) return RNN_OK;
+  if (h->dev) cudaFree(h->dev);
+  delete h;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_get_sizes(rnn_handle_t h, size_t* wb, size_t* ws, size_t* rs) {
+  if (!h) return RNN_BAD_PARAM;
+  if (wb) *wb = h->weight_elems * h->es;
+  if (ws) *ws = h->workspace_bytes;
+  if (rs) *rs = h->reserve_bytes;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_set_timeout_ns(rnn_handle_t h, uint64_t ns) {
+  if (!h || ns == 0) return RNN_BAD_PARAM;
+  h->timeout_ns = ns;
+  return RNN_OK;
+}
+
+uint64_t rnn_launch_count(rnn_handle_t h) { return h ? h->launches : 0; }
+
+int rnn_selected_algo(rnn_handle_t h) { return h ? h->algo : 0; }
+
+rnn_status_t rnn_debug_skip_arrival(rnn_handle_t h, int cta) {
+  if (!h || cta < -1) return RNN_BAD_PARAM;
+  h->skip_cta = cta;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_sync_status(rnn_handle_t h, void* stream) {
+  if (!h) return RNN_BAD_PARAM;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RNN_CUDA_ERROR;
+  unsigned int code = 0;
+  if (cudaMemcpy(&code, &h->dev->status, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return RNN_CUDA_ERROR;
+  if (code != 0) {
+    unsigned int where[4] = {0, 0, 0, 0};
+    cudaMemcpy(where, h->dev->where, sizeof(where), cudaMemcpyDeviceToHost);
+    if (h->trace)
+      std::fprintf(stderr, "[rnn] device status %u: kernel %u block %u step %u wait %u\n", code, where[0], where[1],
+                   where[2], where[3]);
+    if (cudaMemset(h->dev, 0, sizeof(DevArea)) != cudaSuccess) return RNN_CUDA_ERROR;
+  }
+  return static_cast<rnn_status_t>(code);
+}
+
+rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const void* cx, const void* w, void* y,
+                         void* hy, void* cy, void* workspace, void* reserve, void* stream) {
+  if (!h || !x || !w || !y) return RNN_BAD_PARAM;
+  if (!workspace) return RNN_BAD_WORKSPACE;
+  const void* ptrs[] = {x, hx, cx, w, y, hy, cy, workspace, reserve};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return RNN_BAD_PARAM;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int L = h->L, D = h->D, T = h->T, B = h->B, H = h->H;
+  const size_t es = h->es;
+  const size_t TB = static_cast<size_t>(T) * B;
+  const bool train = reserve != nullptr;
+  trace(h, train ? "forward (training)" : "forward (inference)");
+  int sf[4];
+  slots_fwd(h, sf);
+  const void* layer_x = x;
+  if (h->bfirst) {
+    RNN_TRY(count(h, launch_seq_transpose(x, at<char>(workspace, h->w_xin), T, B, h->I, h->bf16, h->bf16, 1, 0,
+                                          h->I, s)));
+    layer_x = at<char>(workspace, h->w_xin);
+  }
+  void* Ybuf = nullptr;
+  for (int l = 0; l < L; ++l) {
+    const int Il = layer_in(h, l);
+    char* wb = static_cast<char*>(const_cast<void*>(w));
+    for (int d = 0; d < D; ++d) {
+      const int i = l * D + d;
+      RNN_TRY(count(h, launch_pack_rows(wb + h->off_ih[i] * es, h->G, H, Il, sf, h->bf16,
+                                        at<char>(workspace, h->w_wx) + static_cast<size_t>(d) * 4 * H * Il * es, Il, 0,
+                                        s)));
+      RNN_TRY(count(h, launch_pack_rows(wb + h->off_hh[i] * es, h->G, H, H, sf, h->bf16,
+                                        at<char>(workspace, h->w_wr) + static_cast<size_t>(d) * 4 * H * H * es, H, 0, s)));
+      RNN_TRY(count(h, launch_pack_bias(wb + h->off_b[i] * es, H, sf, h->bf16,
+                                        at<float>(workspace, h->w_bx) + static_cast<size_t>(d) * 4 * H, s)));
+      if (h->ra)
+        RNN_TRY(count(h, launch_pack_bias(wb + h->off_bh[i] * es, H, sf, h->bf16,
+                                          at<float>(workspace, h->w_bh) + static_cast<size_t>(d) * 4 * H, s)));
+    }
+    // hoisted input projection for every timestep and direction
+    GemmArgs g;
+    g.M = static_cast<int>(TB); g.N = D * 4 * H; g.K = Il;
+    g.A = layer_x; g.lda = Il; g.a_kmajor = 1;
+    g.B = at<char>(workspace, h->w_wx); g.ldb = Il; g.b_kmajor = 1;
+    g.C = at<char>(workspace, h->w_p); g.ldc = D * 4 * H; g.c_bf16 = h->bf16;
+    g.bias = at<float>(workspace, h->w_bx);
+    RNN_TRY(run_gemm(h, g, s));
+    // layer output buffer with h0 in its boundary slots
+    Ybuf = train ? at<char>(reserve, h->r_y[l]) : at<char>(workspace, (l & 1) ? h->w_y1 : h->w_y0);
+    for (int d = 0; d < D; ++d) {
+      const void* h0 = hx ? static_cast<const char*>(hx) + (static_cast<size_t>(l) * D + d) * B * H * es : nullptr;
+      RNN_TRY(count(h, launch_states_to_y(h0, Ybuf, T, B, H, D, d, h->bf16, s)));
+    }
+    PersistArgs a;
+    a.mode = h->desc.mode; a.reset_after = h->ra; a.is_bf16 = h->bf16;
+    a.T = T; a.B = B; a.H = H; a.D = D;
+    a.P = at<char>(workspace, h->w_p);
+    a.bh = h->ra ? at<float>(workspace, h->w_bh) : nullptr;
+    a.Wr = at<char>(workspace, h->w_wr);
+    a.Y = Ybuf;
+    a.gates = train ? at<char>(reserve, h->r_g[l]) : nullptr;
+    a.C = (train && h->lstm) ? at<float>(reserve, h->r_c[l]) : nullptr;
+    a.RH = h->rb ? (train ? at<char>(reserve, h->r_rh[l]) : at<char>(workspace, h->w_rh)) : nullptr;
+    a.c0 = (h->lstm && cx) ? static_cast<const char*>(cx) + static_cast<size_t>(l) * D * B * H * es : nullptr;
+    a.hy = hy ? static_cast<char*>(hy) + static_cast<size_t>(l) * D * B * H * es : nullptr;
+    a.cy = (h->lstm && cy) ? static_cast<char*>(cy) + static_cast<size_t>(l) * D * B * H * es : nullptr;
+    RNN_TRY(run_persist(h, a, false, s));
+    layer_x = static_cast<char*>(Ybuf) + static_cast<size_t>(B) * D * H * es;   // slot 1
+  }
+  // y out (rows of slots 1..T)
+  RNN_TRY(count(h, launch_seq_transpose(layer_x, y, T, B, D * H, h->bf16, h->bf16, 0, h->bfirst, D * H, s)));
+  return cudaGetLastError() == cudaSuccess ? RNN_OK : RNN_CUDA_ERROR;
+}
+
+rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, const void* dhy, const void* dcy,
+                               const void* w, const void* hx, const void* cx, void* dx, void* dhx, void* dcx,
+                               void* workspace, void* reserve, void* stream) {
+  (void)y; (void)hx; (void)cx;
+  if (!h || !dy || !w || !dx) return RNN_BAD_PARAM;
+  if (!workspace || !reserve) return RNN_BAD_WORKSPACE;
+  const void* ptrs[] = {dy, dhy, dcy, w, dx, dhx, dcx, workspace, reserve};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return RNN_BAD_PARAM;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int L = h->L, D = h->D, T = h->T, B = h->B, H = h->H;
+  const size_t es = h->es;
+  const size_t TB = static_cast<size_t>(T) * B;
+  trace(h, "backward data");
+  int sr[4], sx[4];
+  slots_bwd_rec(h, sr);
+  slots_fwd(h, sx);
+  float* dyi = at<float>(workspace, h->w_dyi);
+  RNN_TRY(count(h, launch_seq_transpose(dy, dyi, T, B, D * H, h->bf16, 0, h->bfirst, 0, D * H, s)));
+  char* wb = static_cast<char*>(const_cast<void*>(w));
+  for (int l = L - 1; l >= 0; --l) {
+    const int Il = layer_in(h, l);
+    for (int d = 0; d < D; ++d) {
+      const int i = l * D + d;
+      RNN_TRY(count(h, launch_pack_rows(wb + h->off_hh[i] * es, h->G, H, H, sr, h->bf16,
+                                        at<char>(workspace, h->w_wrt) + static_cast<size_t>(d) * H * 4 * H * es, 4 * H,
+                                        1, s)));
+      RNN_TRY(count(h, launch_pack_rows(wb + h->off_ih[i] * es, h->G, H, Il, sx, h->bf16,
+                                        at<char>(workspace, h->w_wxt) + static_cast<size_t>(d) * 4 * H * es,
+                                        static_cast<int64_t>(D) * 4 * H, 1, s)));
+    }
+    PersistArgs a;
+    a.mode = h->desc.mode; a.reset_after = h->ra; a.is_bf16 = h->bf16;
+    a.T = T; a.B = B; a.H = H; a.D = D;
+    a.Y = at<char>(reserve, h->r_y[l]);
+    a.gates = at<char>(reserve, h->r_g[l]);
+    a.C = h->lstm ? at<float>(reserve, h->r_c[l]) : nullptr;
+    a.WrT = at<char>(workspace, h->w_wrt);
+    a.dYi = dyi;
+    a.dG = at<char>(reserve, h->r_dg[l]);
+    a.db = at<float>(reserve, h->r_db[l]);
+    const size_t so = static_cast<size_t>(l) * D * B * H * es;
+    a.dhT = dhy ? static_cast<const char*>(dhy) + so : nullptr;
+    a.dcT = (h->lstm && dcy) ? static_cast<const char*>(dcy) + so : nullptr;
+    a.dh0 = dhx ? static_cast<char*>(dhx) + so : nullptr;
+    a.dc0 = (h->lstm && dcx) ? static_cast<char*>(dcx) + so : nullptr;
+    RNN_TRY(run_persist(h, a, true, s));
+    // input gradient dX = dG * W_ih (both directions summed through K)
+    GemmArgs g;
+    g.M = static_cast<int>(TB); g.N = Il; g.K = D * 4 * H;
+    g.A = at<char>(reserve, h->r_dg[l]); g.lda = D * 4 * H; g.a_kmajor = 1;
+    g.B = at<char>(workspace, h->w_wxt); g.ldb = D * 4 * H; g.b_kmajor = 1;
+    if (l > 0) {
+      g.C = dyi; g.ldc = Il; g.c_bf16 = 0;
+    } else {
+      g.C = h->bfirst ? at<char>(workspace, h->w_dx0) : dx; g.ldc = Il; g.c_bf16 = h->bf16;
+    }
+    RNN_TRY(run_gemm(h, g, s));
+  }
+  if (h->bfirst)
+    RNN_TRY(count(h, launch_seq_transpose(at<char>(workspace, h->w_dx0), dx, T, B, h->I, h->bf16, h->bf16, 0, 1,
+                                          h->I, s)));
+  return cudaGetLastError() == cudaSuccess ? RNN_OK : RNN_CUDA_ERROR;
+}
+
+rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx, const void* y, void* workspace,
+                                  const void* reserve, void* dw, void* stream) {
+  (void)hx; (void)y;
+  if (!h || !x || !dw) return RNN_BAD_PARAM;
+  if (!workspace || !reserve) return RNN_BAD_WORKSPACE;
+  const void* ptrs[] = {x, workspace, reserve, dw};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return RNN_BAD_PARAM;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int L = h->L, D = h->D, T = h->T, B = h->B, H = h->H;
+  const size_t es = h->es;
+  const size_t TB = static_cast<size_t>(T) * B;
+  trace(h, "backward weights");
+  const void* x0 = x;
+  if (h->bfirst) {
+    RNN_TRY(count(h, launch_seq_transpose(x, at<char>(workspace, h->w_xin), T, B, h->I, h->bf16, h->bf16, 1, 0,
+                                          h->I, s)));
+    x0 = at<char>(workspace, h->w_xin);
+  }
+  char* rs = static_cast<char*>(const_cast<void*>(reserve));
+  float* dwf = static_cast<float*>(dw);
+  const int* pos = h->pos;
+  int m_ih[4], m_hh[4], m_b[4], m_bh[4];
+  if (h->lstm) {
+    for (int k = 0; k < 4; ++k) m_ih[k] = m_hh[k] = m_b[k] = m_bh[k] = pos[k];
+  } else {
+    m_ih[0] = pos[0]; m_ih[1] = pos[1]; m_ih[2] = pos[2]; m_ih[3] = -1;
+    m_b[0] = pos[0]; m_b[1] = pos[1]; m_b[2] = pos[2]; m_b[3] = -1;
+    if (h->ra) {
+      m_hh[0] = pos[0]; m_hh[1] = pos[1]; m_hh[2] = -1; m_hh[3] = pos[2];
+      m_bh[0] = pos[0]; m_bh[1] = pos[1]; m_bh[2] = -1; m_bh[3] = pos[2];
+    } else {
+      m_hh[0] = pos[0]; m_hh[1] = pos[1]; m_hh[2] = -1; m_hh[3] = -1;
+    }
+  }
+  for (int l = 0; l < L; ++l) {
+    const int Il = layer_in(h, l);
+    const void* Xl = l == 0 ? x0 : rs + h->r_y[l - 1] + static_cast<size_t>(B) * D * H * es;
+    for (int d = 0; d < D; ++d) {
+      const int i = l * D + d;
+      const char* dG = rs + h->r_dg[l] + static_cast<size_t>(d) * 4 * H * es;
+      GemmArgs g;
+      g.M = 4 * H; g.K = static_cast<int>(TB);
+      g.A = dG; g.lda = D * 4 * H; g.a_kmajor = 0;
+      g.rowmap_H = H;
+      // dW_ih = sum over (t, b) of dG x^T
+      g.N = Il;
+      g.B = Xl; g.ldb = Il; g.b_kmajor = 0;
+      g.C = dwf + h->off_ih[i]; g.ldc = Il; g.c_bf16 = 0;
+      for (int k = 0; k < 4; ++k) g.perm[k] = m_ih[k];
+      RNN_TRY(run_gemm(h, g, s));
+      // dW_hh = sum over (t, b) of dG^h h_prev^T ; h_prev rows are Y slots t (forward) / t+2 (reverse)
+      const char* hp = rs + h->r_y[l] + (static_cast<size_t>(d == 0 ? 0 : 2) * B * D * H + static_cast<size_t>(d) * H) * es;
+      g.N = H;
+      g.B = hp; g.ldb = D * H; g.b_kmajor = 0;
+      g.C = dwf + h->off_hh[i]; g.ldc = H;
+      for (int k = 0; k < 4; ++k) g.perm[k] = m_hh[k];
+      RNN_TRY(run_gemm(h, g, s));
+      if (h->rb) {
+        // reset-before candidate rows: dW_hn = sum dn (r * h_prev)^T
+        g.B = rs + h->r_rh[l] + static_cast<size_t>(d) * TB * H * es; g.ldb = H;
+        g.perm[0] = -1; g.perm[1] = -1; g.perm[2] = pos[2]; g.perm[3] = -1;
+        RNN_TRY(run_gemm(h, g, s));
+      }
+      const float* db = reinterpret_cast<const float*>(rs + h->r_db[l]) + static_cast<size_t>(d) * 4 * H;
+      RNN_TRY(count(h, launch_bias_grad_scatter(db, H, m_b, 0, dwf + h->off_b[i], s)));
+      if (h->ra) RNN_TRY(count(h, launch_bias_grad_scatter(db, H, m_bh, 1, dwf + h->off_bh[i], s)));
+    }
+  }
+  return cudaGetLastError() == cudaSuccess ? RNN_OK : RNN_CUDA_ERROR;
+}
+
+}  // extern "C"

@@ -1,0 +1,196 @@
+// layout.cu - the layout / cast / pack kernels around the recurrence:
+//   * weight packing into the unit-interleaved 4-slot order the GEMMs and the
+//     persistent kernels read (plain and transposed, 32x32 shared-memory tiles
+//     so both sides stay coalesced);
+//   * bias packing and bias-gradient scatter back to the caller's gate order;
+//   * sequence copies between seq-major [T,B,F] and batch-first [B,T,F], with
+//     fp32 <-> bf16 casts, vectorised by four elements;
+//   * placing h0 into the output buffer's boundary slot.
+// SystemDS LibMatrixCuDNN.java does the same job with separate layout kernels
+// (prepare_lstm_output, prepare_lstm_backward_gradients, prepare_lstm_dinput,
+// prepare_lstm_dweight) around the cuDNN calls in ``lstm`` / ``lstmBackward``.
+#include "common.cuh"
+
+namespace rnn {
+
+namespace {
+
+template <typename T>
+__global__ void pack_rows_kernel(const T* __restrict__ W, int H, int K, int4 src,
+                                 T* __restrict__ out, int64_t ld_out) {
+  // out[(4u+s)*ld + k] = W[(src[s]*H + u)*K + k]
+  const int row = blockIdx.y;               // 4u + s
+  const int u = row >> 2, s = row & 3;
+  const int sb = s == 0 ? src.x : s == 1 ? src.y : s == 2 ? src.z : src.w;
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += gridDim.x * blockDim.x) {
+    T v = sb >= 0 ? W[(static_cast<int64_t>(sb) * H + u) * K + k] : from_f<T>(0.0f);
+    out[static_cast<int64_t>(row) * ld_out + k] = v;
+  }
+}
+
+template <typename T>
+__global__ void pack_rows_t_kernel(const T* __restrict__ W, int H, int K, int4 src,
+                                   T* __restrict__ out, int64_t ld_out) {
+  // out[k*ld + 4u+s] = W[(src[s]*H + u)*K + k], through a 32x33 tile.
+  __shared__ T tile[32][33];
+  const int r0 = blockIdx.y * 32;           // packed row block (4u+s)
+  const int k0 = blockIdx.x * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
+  for (int i = ty; i < 32; i += 8) {
+    const int row = r0 + i, k = k0 + tx;
+    T v = from_f<T>(0.0f);
+    if (row < 4 * H && k < K) {
+      const int u = row >> 2, s = row & 3;
+      const int sb = s == 0 ? src.x : s == 1 ? src.y : s == 2 ? src.z : src.w;
+      if (sb >= 0) v = W[(static_cast<int64_t>(sb) * H + u) * K + k];
+    }
+    tile[i][tx] = v;
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int k = k0 + i, row = r0 + tx;
+    if (k < K && row < 4 * H) out[static_cast<int64_t>(k) * ld_out + row] = tile[tx][i];
+  }
+}
+
+template <typename T>
+__global__ void pack_bias_kernel(const T* __restrict__ b, int H, int4 src, float* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 4 * H) return;
+  const int u = i >> 2, s = i & 3;
+  const int sb = s == 0 ? src.x : s == 1 ? src.y : s == 2 ? src.z : src.w;
+  out[i] = (sb >= 0 && b != nullptr) ? to_f<T>(b[static_cast<int64_t>(sb) * H + u]) : 0.0f;
+}
+
+__global__ void bias_grad_scatter_kernel(const float* __restrict__ db, int H, int4 dst,
+                                         float* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 4 * H) return;
+  const int u = i >> 2, s = i & 3;
+  const int d = s == 0 ? dst.x : s == 1 ? dst.y : s == 2 ? dst.z : dst.w;
+  if (d >= 0) out[static_cast<int64_t>(d) * H + u] = db[i];
+}
+
+// One output row (t, b) per blockIdx.x, features along threads.
+template <typename Ti, typename To, int V>
+__global__ void seq_copy_kernel(const Ti* __restrict__ in, To* __restrict__ out, int T, int B, int F,
+                                int in_bf, int out_bf, int64_t out_ld) {
+  const int64_t r = blockIdx.x;             // output row index in output order
+  int t, b;
+  if (out_bf) { b = static_cast<int>(r / T); t = static_cast<int>(r % T); }
+  else { t = static_cast<int>(r / B); b = static_cast<int>(r % B); }
+  const int64_t ir = in_bf ? (static_cast<int64_t>(b) * T + t) : (static_cast<int64_t>(t) * B + b);
+  const Ti* src = in + ir * F;
+  To* dst = out + r * out_ld;
+  for (int f = threadIdx.x * V; f < F; f += blockDim.x * V) {
+#pragma unroll
+    for (int v = 0; v < V; ++v) dst[f + v] = from_f<To>(to_f<Ti>(src[f + v]));
+  }
+}
+
+template <typename T>
+__global__ void states_to_y_kernel(const T* __restrict__ h0, T* __restrict__ Y, int T_, int B, int H,
+                                   int D, int dir) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * H) return;
+  const int b = i / H, u = i % H;
+  const int slot = dir == 0 ? 0 : T_ + 1;
+  Y[(static_cast<int64_t>(slot) * B + b) * D * H + dir * H + u] = h0 ? h0[i] : from_f<T>(0.0f);
+}
+
+int check_launch() {
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace
+
+int launch_pack_rows(const void* W, int G, int H, int K, const int* slot_src, int is_bf16,
+                     void* out, int64_t ld_out, int transpose, cudaStream_t s) {
+  (void)G;
+  const int4 src = make_int4(slot_src[0], slot_src[1], slot_src[2], slot_src[3]);
+  if (!transpose) {
+    dim3 grid((K + 255) / 256 > 8 ? 8 : (K + 255) / 256, 4 * H);
+    if (is_bf16)
+      pack_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(W), H, K, src, static_cast<__nv_bfloat16*>(out), ld_out);
+    else
+      pack_rows_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(W), H, K, src,
+                                                   static_cast<float*>(out), ld_out);
+  } else {
+    dim3 grid((K + 31) / 32, (4 * H + 31) / 32);
+    dim3 block(32, 8);
+    if (is_bf16)
+      pack_rows_t_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(W), H, K, src, static_cast<__nv_bfloat16*>(out), ld_out);
+    else
+      pack_rows_t_kernel<float><<<grid, block, 0, s>>>(static_cast<const float*>(W), H, K, src,
+                                                       static_cast<float*>(out), ld_out);
+  }
+  return check_launch();
+}
+
+int launch_pack_bias(const void* b, int H, const int* slot_src, int is_bf16, float* out,
+                     cudaStream_t s) {
+  const int4 src = make_int4(slot_src[0], slot_src[1], slot_src[2], slot_src[3]);
+  const int n = 4 * H;
+  if (is_bf16)
+    pack_bias_kernel<__nv_bfloat16><<<(n + 255) / 256, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(b), H, src, out);
+  else
+    pack_bias_kernel<float><<<(n + 255) / 256, 256, 0, s>>>(static_cast<const float*>(b), H, src, out);
+  return check_launch();
+}
+
+int launch_bias_grad_scatter(const float* db, int H, const int* slot_dst, int is_second, float* out,
+                             cudaStream_t s) {
+  (void)is_second;
+  const int4 dst = make_int4(slot_dst[0], slot_dst[1], slot_dst[2], slot_dst[3]);
+  bias_grad_scatter_kernel<<<(4 * H + 255) / 256, 256, 0, s>>>(db, H, dst, out);
+  return check_launch();
+}
+
+int launch_seq_transpose(const void* in, void* out, int T, int B, int F, int in_bf16, int out_bf16,
+                         int in_batch_first, int out_batch_first, int64_t out_ld, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(T) * B;
+  if (rows == 0 || F == 0) return 0;
+  if (rows > 0x7fffffffLL) return 2;
+  const int vec = (F % 4 == 0 && out_ld % 4 == 0) ? 4 : 1;
+  int threads = (F / vec + 31) / 32 * 32;
+  if (threads > 256) threads = 256;
+  if (threads < 32) threads = 32;
+  dim3 grid(static_cast<unsigned>(rows));
+#define RNN_SEQ_COPY(TI, TO)                                                                    \
+  do {                                                                                          \
+    if (vec == 4)                                                                               \
+      seq_copy_kernel<TI, TO, 4><<<grid, threads, 0, s>>>(static_cast<const TI*>(in),           \
+          static_cast<TO*>(out), T, B, F, in_batch_first, out_batch_first, out_ld);             \
+    else                                                                                        \
+      seq_copy_kernel<TI, TO, 1><<<grid, threads, 0, s>>>(static_cast<const TI*>(in),           \
+          static_cast<TO*>(out), T, B, F, in_batch_first, out_batch_first, out_ld);             \
+  } while (0)
+  if (in_bf16 && out_bf16) RNN_SEQ_COPY(__nv_bfloat16, __nv_bfloat16);
+  else if (in_bf16) RNN_SEQ_COPY(__nv_bfloat16, float);
+  else if (out_bf16) RNN_SEQ_COPY(float, __nv_bfloat16);
+  else RNN_SEQ_COPY(float, float);
+#undef RNN_SEQ_COPY
+  return check_launch();
+}
+
+int launch_states_to_y(const void* h0, void* Y, int T, int B, int H, int D, int dir, int is_bf16,
+                       cudaStream_t s) {
+  const int n = B * H;
+  if (is_bf16)
+    states_to_y_kernel<__nv_bfloat16><<<(n + 255) / 256, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(h0), static_cast<__nv_bfloat16*>(Y), T, B, H, D, dir);
+  else
+    states_to_y_kernel<float><<<(n + 255) / 256, 256, 0, s>>>(static_cast<const float*>(h0),
+                                                              static_cast<float*>(Y), T, B, H, D, dir);
+  return check_launch();
+}
+
+int launch_fill_zero(void* p, size_t bytes, cudaStream_t s) {
+  if (bytes == 0 || p == nullptr) return 0;
+  return cudaMemsetAsync(p, 0, bytes, s) == cudaSuccess ? 0 : 3;
+}
+
+}  // namespace rnn

@@ -1,0 +1,571 @@
+// persist_simt.cu - persistent recurrent kernels on fp32 FMA (SIMT).
+//
+// One launch runs every timestep of one layer (both directions when they fit
+// together).  Each CTA owns NU hidden units of one direction and keeps their
+// recurrent weights resident in shared memory for the whole sequence:
+//   forward: the 4 gate rows W_hh[gate][u][0:H] of each owned unit;
+//   backward: the column W_hh[:, u] of each owned unit over all 4H gate rows.
+// Each step a CTA stages the full previous state (h_{t-1}, or the gate
+// gradients of the step after) from L2 in chunks, forms its units'
+// contractions, applies the cell (forward) or its derivative (backward) in
+// registers, writes its slice, and arrives on a gpu-scope step counter.
+// Before the next step every CTA waits - with a time limit - until all CTAs of
+// its direction have arrived.  This is the persistent-RNN structure of the
+// persistent backward-data kernel fragment (one launch for all steps,
+// register/shared-resident weights, a per-step exchange through global memory
+// between CTAs), with acquire/release counters in place of its -0.0 sentinel
+// polling.
+//
+// This kernel serves the fp32 path (the 1e-5 bound needs fp32 FMA, not TF32),
+// GRU reset-before (two dependent contractions per step: r/z, then W_hn(r*h))
+// and any shape the tensor-core kernels do not take.
+//
+// Cell math: Lstm.cpp lstmCellForwardPassCalcUnits / basicLstmCellForwardPass
+// and backwardStepImpl; Gru.cpp gruCellForwardPassCalcUnits,
+// gruCellForwardPassCalcUnitsResetAfter, backwardStepImpl and
+// backwardStepImplResetAfter; the LSTM and GRU branches of the persistent
+// backward-data kernel fragment.
+#include "common.cuh"
+
+namespace rnn {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+
+template <typename T> __host__ __device__ inline int row_pad() { return sizeof(T) == 4 ? 1 : 2; }
+
+__device__ __forceinline__ float ldcg_f(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ float ldcg_f(const __nv_bfloat16* p) { return __bfloat162float(__ldcg(p)); }
+
+// thread 0 waits on the counter; the verdict is shared with the whole CTA.
+__device__ __forceinline__ bool cta_wait(const PersistArgs& a, const unsigned int* ctr, unsigned int target,
+                                         unsigned int kernel, int step) {
+  int ok = 1;
+  if (threadIdx.x == 0) {
+    ok = wait_counter_geq(ctr, target, a.timeout_ns) ? 1 : 0;
+    if (!ok) report_status(a.dev, 4u /* RNN_TIMEOUT */, kernel, static_cast<unsigned>(step), W_COUNTER);
+  }
+  return __syncthreads_and(ok) != 0;
+}
+
+// All stores of this phase by the CTA are ordered before the arrival.
+__device__ __forceinline__ void cta_arrive(unsigned int* ctr, bool skip) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (!skip) red_release_gpu_add(ctr, 1u);
+  }
+}
+
+// acc[p][s] += sum_k W[s][ul][k] * src[b][k] over k in [0, K), slots in MASK.
+// src row b starts at src + b * ld.
+template <typename T, int PP, int MASK>
+__device__ __forceinline__ void contract_fwd(float (&acc)[PP][4], const T* Ws, int NU, int WS,
+                                             float* hs, int KC, const T* src, int64_t ld, int K,
+                                             int B, int nu, int npairs) {
+  const int HS = KC + 1;
+  for (int k0 = 0; k0 < K; k0 += KC) {
+    const int kc = min(KC, K - k0);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < B * kc; idx += kThreads) {
+      const int b = idx / kc, kk = idx - b * kc;
+      hs[b * HS + kk] = ldcg_f(src + b * ld + k0 + kk);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      if (id >= npairs) break;
+      const int ul = id % nu, b = id / nu;
+      const float* hr = hs + b * HS;
+      const T* w0 = Ws + (0 * NU + ul) * WS + k0;
+      const T* w1 = Ws + (1 * NU + ul) * WS + k0;
+      const T* w2 = Ws + (2 * NU + ul) * WS + k0;
+      const T* w3 = Ws + (3 * NU + ul) * WS + k0;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      for (int kk = 0; kk < kc; ++kk) {
+        const float hv = hr[kk];
+        if (MASK & 1) a0 = fmaf(to_f<T>(w0[kk]), hv, a0);
+        if (MASK & 2) a1 = fmaf(to_f<T>(w1[kk]), hv, a1);
+        if (MASK & 4) a2 = fmaf(to_f<T>(w2[kk]), hv, a2);
+        if (MASK & 8) a3 = fmaf(to_f<T>(w3[kk]), hv, a3);
+      }
+      acc[p][0] += a0; acc[p][1] += a1; acc[p][2] += a2; acc[p][3] += a3;
+    }
+  }
+}
+
+// acc[p] += sum_k WT[ul][k] * src[b][k] over k in [0, K) with (k & 3) in MASK.
+template <typename T, int PP, int MASK>
+__device__ __forceinline__ void contract_bwd(float (&acc)[PP], const T* Ws, int WS, float* hs, int KC,
+                                             const T* src, int64_t ld, int K, int B, int nu, int npairs) {
+  const int HS = KC + 1;
+  for (int k0 = 0; k0 < K; k0 += KC) {
+    const int kc = min(KC, K - k0);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < B * kc; idx += kThreads) {
+      const int b = idx / kc, kk = idx - b * kc;
+      hs[b * HS + kk] = ldcg_f(src + b * ld + k0 + kk);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      if (id >= npairs) break;
+      const int ul = id % nu, b = id / nu;
+      const float* hr = hs + b * HS;
+      const T* w = Ws + ul * WS + k0;
+      float s = 0.f;
+      if (MASK == 0xF) {
+        for (int kk = 0; kk < kc; ++kk) s = fmaf(to_f<T>(w[kk]), hr[kk], s);
+      } else {
+        for (int kk = 0; kk < kc; ++kk)
+          if ((MASK >> (kk & 3)) & 1) s = fmaf(to_f<T>(w[kk]), hr[kk], s);
+      }
+      acc[p] += s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// forward
+// ---------------------------------------------------------------------------
+template <typename T, int PP>
+__global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistArgs a, int NU, int KC) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int H = a.H, B = a.B, TT = a.T, D = a.D;
+  const int dir = a.dir0 + blockIdx.y;
+  const int u0 = blockIdx.x * NU;
+  const int nu = min(NU, H - u0);
+  const int WS = H + row_pad<T>();
+  T* Ws = reinterpret_cast<T*>(smem);
+  float* hs = reinterpret_cast<float*>(smem + align16(static_cast<size_t>(4) * NU * WS * sizeof(T)));
+  const bool lstm = a.mode == 0;
+  const bool rb = !lstm && !a.reset_after;
+
+  const T* Wr = static_cast<const T*>(a.Wr) + static_cast<size_t>(dir) * 4 * H * H;
+  for (int idx = threadIdx.x; idx < 4 * nu * H; idx += kThreads) {
+    const int s = idx / (nu * H);
+    const int rem = idx - s * nu * H;
+    const int ul = rem / H, k = rem - ul * H;
+    Ws[(s * NU + ul) * WS + k] = Wr[static_cast<size_t>(4 * (u0 + ul) + s) * H + k];
+  }
+
+  T* Y = static_cast<T*>(a.Y);
+  const T* P = static_cast<const T*>(a.P);
+  T* G = static_cast<T*>(a.gates);
+  T* RH = static_cast<T*>(a.RH);
+  const int64_t ldY = static_cast<int64_t>(D) * H;
+  const int64_t ldP = static_cast<int64_t>(D) * 4 * H;
+  const int npairs = nu * B;
+  float st[PP];      // LSTM: c_{t-1}; GRU: h_{t-1} (fp32 copy)
+  float zr[PP][2];   // GRU reset-before: r, z between the two phases
+  const int slot_h0 = dir ? TT + 1 : 0;
+#pragma unroll
+  for (int p = 0; p < PP; ++p) {
+    st[p] = 0.f;
+    zr[p][0] = zr[p][1] = 0.f;
+    const int id = threadIdx.x + p * kThreads;
+    if (id >= npairs) continue;
+    const int ul = id % nu, b = id / nu, u = u0 + ul;
+    if (lstm) {
+      const T* c0 = static_cast<const T*>(a.c0);
+      st[p] = c0 ? to_f<T>(c0[(static_cast<int64_t>(dir) * B + b) * H + u]) : 0.f;
+      if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? TT : 0)) * B + b) * H + u] = st[p];
+    } else {
+      st[p] = to_f<T>(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
+    }
+  }
+
+  unsigned int* ctr = &a.dev->counters[dir];
+  const unsigned int nblk = gridDim.x;
+  const bool skip = a.skip_cta == static_cast<int>(blockIdx.x + gridDim.x * blockIdx.y);
+  unsigned int phases = 0;
+
+  for (int s = 0; s < TT; ++s) {
+    const int t = dir ? TT - 1 - s : s;
+    const int sp = dir ? t + 2 : t;     // Y slot of h_{t-1}
+    const int so = t + 1;               // Y slot of h_t
+    if (phases > 0 && !cta_wait(a, ctr, phases * nblk, K_FWD_SIMT, s)) return;
+    float acc[PP][4];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) acc[p][0] = acc[p][1] = acc[p][2] = acc[p][3] = 0.f;
+    const T* hsrc = Y + static_cast<int64_t>(sp) * B * ldY + dir * H;
+    if (rb)
+      contract_fwd<T, PP, 0x3>(acc, Ws, NU, WS, hs, KC, hsrc, ldY, H, B, nu, npairs);
+    else if (lstm)
+      contract_fwd<T, PP, 0xF>(acc, Ws, NU, WS, hs, KC, hsrc, ldY, H, B, nu, npairs);
+    else
+      contract_fwd<T, PP, 0x7>(acc, Ws, NU, WS, hs, KC, hsrc, ldY, H, B, nu, npairs);
+
+    if (rb) {
+      // phase 1: r, z and the reset state r * h_{t-1}
+#pragma unroll
+      for (int p = 0; p < PP; ++p) {
+        const int id = threadIdx.x + p * kThreads;
+        if (id >= npairs) break;
+        const int ul = id % nu, b = id / nu, u = u0 + ul;
+        float pv[4];
+        Vec4<T>::load(P + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u, pv);
+        const float r = sigm(pv[0] + acc[p][0]);
+        const float z = sigm(pv[1] + acc[p][1]);
+        zr[p][0] = r;
+        zr[p][1] = z;
+        RH[((static_cast<int64_t>(dir) * TT + t) * B + b) * H + u] = from_f<T>(r * st[p]);
+      }
+      cta_arrive(ctr, skip);
+      ++phases;
+      if (!cta_wait(a, ctr, phases * nblk, K_FWD_SIMT, s)) return;
+#pragma unroll
+      for (int p = 0; p < PP; ++p) acc[p][2] = 0.f;
+      const T* rsrc = RH + (static_cast<int64_t>(dir) * TT + t) * B * H;
+      contract_fwd<T, PP, 0x4>(acc, Ws, NU, WS, hs, KC, rsrc, H, H, B, nu, npairs);
+    }
+
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      if (id >= npairs) break;
+      const int ul = id % nu, b = id / nu, u = u0 + ul;
+      float pv[4];
+      Vec4<T>::load(P + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u, pv);
+      float gv[4];
+      float h;
+      if (lstm) {
+        const float i = sigm(pv[0] + acc[p][0]);
+        const float f = sigm(pv[1] + acc[p][1]);
+        const float g = tanhf(pv[2] + acc[p][2]);
+        const float o = sigm(pv[3] + acc[p][3]);
+        const float c = f * st[p] + i * g;
+        h = o * tanhf(c);
+        st[p] = c;
+        gv[0] = i; gv[1] = f; gv[2] = g; gv[3] = o;
+        if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = c;
+        if (s == TT - 1 && a.cy)
+          static_cast<T*>(a.cy)[(static_cast<int64_t>(dir) * B + b) * H + u] = from_f<T>(c);
+      } else if (!rb) {
+        const float* bh = a.bh + dir * 4 * H + 4 * u;
+        const float r = sigm(pv[0] + acc[p][0] + bh[0]);
+        const float z = sigm(pv[1] + acc[p][1] + bh[1]);
+        const float hn = acc[p][2] + bh[2];
+        const float n = tanhf(pv[2] + r * hn);
+        h = (1.f - z) * n + z * st[p];
+        st[p] = h;
+        gv[0] = r; gv[1] = z; gv[2] = n; gv[3] = hn;
+      } else {
+        const float r = zr[p][0], z = zr[p][1];
+        const float n = tanhf(pv[2] + acc[p][2]);
+        h = (1.f - z) * n + z * st[p];
+        st[p] = h;
+        gv[0] = r; gv[1] = z; gv[2] = n; gv[3] = 0.f;
+      }
+      Y[(static_cast<int64_t>(so) * B + b) * ldY + dir * H + u] = from_f<T>(h);
+      if (G) Vec4<T>::store(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * 4 * H + 4 * u, gv);
+      if (s == TT - 1 && a.hy)
+        static_cast<T*>(a.hy)[(static_cast<int64_t>(dir) * B + b) * H + u] = from_f<T>(h);
+    }
+    cta_arrive(ctr, skip);
+    ++phases;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// backward through time
+// ---------------------------------------------------------------------------
+template <typename T, int PP>
+__global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistArgs a, int NU, int KC) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int H = a.H, B = a.B, TT = a.T, D = a.D;
+  const int dir = a.dir0 + blockIdx.y;
+  const int u0 = blockIdx.x * NU;
+  const int nu = min(NU, H - u0);
+  const int K4 = 4 * H;
+  const int WS = K4 + row_pad<T>();
+  T* Ws = reinterpret_cast<T*>(smem);
+  float* hs = reinterpret_cast<float*>(smem + align16(static_cast<size_t>(NU) * WS * sizeof(T)));
+  __shared__ float dbs[4 * 64];
+  const bool lstm = a.mode == 0;
+  const bool rb = !lstm && !a.reset_after;
+
+  const T* WT = static_cast<const T*>(a.WrT) + static_cast<size_t>(dir) * H * K4;
+  for (int idx = threadIdx.x; idx < nu * K4; idx += kThreads) {
+    const int ul = idx / K4, k = idx - ul * K4;
+    Ws[ul * WS + k] = WT[static_cast<size_t>(u0 + ul) * K4 + k];
+  }
+
+  const T* Y = static_cast<const T*>(a.Y);
+  const T* G = static_cast<const T*>(a.gates);
+  T* dG = static_cast<T*>(a.dG);
+  const int64_t ldY = static_cast<int64_t>(D) * H;
+  const int64_t ldG = static_cast<int64_t>(D) * K4;
+  const int npairs = nu * B;
+  float carry[PP];     // LSTM dc_next; GRU resetAfter dh*z; reset-before d(rh)*r + dh*z
+  float dhv[PP];       // reset-before: dh_t between its two phases
+  float db[PP][4];
+#pragma unroll
+  for (int p = 0; p < PP; ++p) {
+    carry[p] = 0.f;
+    dhv[p] = 0.f;
+    db[p][0] = db[p][1] = db[p][2] = db[p][3] = 0.f;
+    const int id = threadIdx.x + p * kThreads;
+    if (id >= npairs) continue;
+    const int ul = id % nu, b = id / nu, u = u0 + ul;
+    if (lstm && a.dcT) carry[p] = to_f<T>(static_cast<const T*>(a.dcT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
+  }
+
+  unsigned int* ctr = &a.dev->counters[dir];
+  const unsigned int nblk = gridDim.x;
+  const bool skip = a.skip_cta == static_cast<int>(blockIdx.x + gridDim.x * blockIdx.y);
+  unsigned int phases = 0;
+
+  for (int s = 0; s <= TT; ++s) {
+    float dhr[PP];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) dhr[p] = 0.f;
+    if (s == 0) {
+      if (a.dhT) {
+#pragma unroll
+        for (int p = 0; p < PP; ++p) {
+          const int id = threadIdx.x + p * kThreads;
+          if (id >= npairs) break;
+          const int ul = id % nu, b = id / nu;
+          dhr[p] = to_f<T>(static_cast<const T*>(a.dhT)[(static_cast<int64_t>(dir) * B + b) * H + u0 + ul]);
+        }
+      }
+    } else {
+      if (!cta_wait(a, ctr, phases * nblk, K_BWD_SIMT, s)) return;
+      const int tp = dir ? s - 1 : TT - s;   // step processed just before
+      const T* src = dG + static_cast<int64_t>(tp) * B * ldG + dir * K4;
+      if (rb)
+        contract_bwd<T, PP, 0x3>(dhr, Ws, WS, hs, KC, src, ldG, K4, B, nu, npairs);
+      else
+        contract_bwd<T, PP, 0xF>(dhr, Ws, WS, hs, KC, src, ldG, K4, B, nu, npairs);
+    }
+    if (s == TT) {
+#pragma unroll
+      for (int p = 0; p < PP; ++p) {
+        const int id = threadIdx.x + p * kThreads;
+        if (id >= npairs) break;
+        const int ul = id % nu, b = id / nu, u = u0 + ul;
+        const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
+        if (a.dh0) static_cast<T*>(a.dh0)[o] = from_f<T>(lstm ? dhr[p] : dhr[p] + carry[p]);
+        if (lstm && a.dc0) static_cast<T*>(a.dc0)[o] = from_f<T>(carry[p]);
+      }
+      break;
+    }
+    const int t = dir ? s : TT - 1 - s;
+    const int sp = dir ? t + 2 : t;          // Y slot of h_{t-1}
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      if (id >= npairs) break;
+      const int ul = id % nu, b = id / nu, u = u0 + ul;
+      float gv[4];
+      Vec4<T>::load(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * K4 + 4 * u, gv);
+      const float dy = a.dYi[(static_cast<int64_t>(t) * B + b) * ldY + dir * H + u];
+      T* dg = dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u;
+      if (lstm) {
+        const float i = gv[0], f = gv[1], g = gv[2], o = gv[3];
+        const float* C = a.C + static_cast<int64_t>(dir) * (TT + 1) * B * H;
+        const float c = C[(static_cast<int64_t>(dir ? t : t + 1) * B + b) * H + u];
+        const float cp = C[(static_cast<int64_t>(dir ? t + 1 : t) * B + b) * H + u];
+        const float dh = dy + dhr[p];
+        const float tc = tanhf(c);
+        const float dc = dh * o * (1.f - tc * tc) + carry[p];
+        float da[4];
+        da[0] = dc * g * i * (1.f - i);
+        da[1] = dc * cp * f * (1.f - f);
+        da[2] = dc * i * (1.f - g * g);
+        da[3] = dh * tc * o * (1.f - o);
+        carry[p] = dc * f;
+        Vec4<T>::store(dg, da);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) db[p][q] += da[q];
+      } else if (!rb) {
+        const float r = gv[0], z = gv[1], n = gv[2], hn = gv[3];
+        const float hp = to_f<T>(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
+        const float dh = dy + dhr[p] + carry[p];
+        const float dn = dh * (1.f - z) * (1.f - n * n);
+        const float dz = dh * (hp - n) * z * (1.f - z);
+        const float dr = dn * hn * r * (1.f - r);
+        float da[4] = {dr, dz, dn, dn * r};
+        carry[p] = dh * z;
+        Vec4<T>::store(dg, da);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) db[p][q] += da[q];
+      } else {
+        // reset-before, phase A: dn, dz
+        const float z = gv[1], n = gv[2];
+        const float hp = to_f<T>(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
+        const float dh = dy + dhr[p] + carry[p];
+        const float dn = dh * (1.f - z) * (1.f - n * n);
+        const float dz = dh * (hp - n) * z * (1.f - z);
+        dhv[p] = dh;
+        dg[1] = from_f<T>(dz);
+        dg[2] = from_f<T>(dn);
+        dg[3] = from_f<T>(0.f);
+        db[p][1] += dz;
+        db[p][2] += dn;
+      }
+    }
+    cta_arrive(ctr, skip);
+    ++phases;
+    if (rb) {
+      // phase B: d(rh) = W_hn^T dn, then dr
+      if (!cta_wait(a, ctr, phases * nblk, K_BWD_SIMT, s)) return;
+      float drh[PP];
+#pragma unroll
+      for (int p = 0; p < PP; ++p) drh[p] = 0.f;
+      const T* src = dG + static_cast<int64_t>(t) * B * ldG + dir * K4;
+      contract_bwd<T, PP, 0x4>(drh, Ws, WS, hs, KC, src, ldG, K4, B, nu, npairs);
+#pragma unroll
+      for (int p = 0; p < PP; ++p) {
+        const int id = threadIdx.x + p * kThreads;
+        if (id >= npairs) break;
+        const int ul = id % nu, b = id / nu, u = u0 + ul;
+        float gv[4];
+        Vec4<T>::load(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * K4 + 4 * u, gv);
+        const float r = gv[0], z = gv[1];
+        const float hp = to_f<T>(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
+        const float dr = drh[p] * hp * r * (1.f - r);
+        dG[(static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u] = from_f<T>(dr);
+        db[p][0] += dr;
+        carry[p] = drh[p] * r + dhv[p] * z;
+      }
+      cta_arrive(ctr, skip);
+      ++phases;
+    }
+  }
+
+  // bias gradients: reduce each unit's four sums over the batch
+  for (int base = 0; base < nu; base += 64) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4 * 64; i += kThreads) dbs[i] = 0.f;
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      if (id >= npairs) break;
+      const int ul = id % nu;
+      if (ul < base || ul >= base + 64) continue;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) atomicAdd(&dbs[(ul - base) * 4 + q], db[p][q]);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4 * 64; i += kThreads) {
+      const int ul = base + i / 4;
+      if (ul < nu) a.db[static_cast<int64_t>(dir) * K4 + 4 * (u0 + ul) + (i & 3)] = dbs[i];
+    }
+  }
+}
+
+template <typename T>
+struct SimtKernels {
+  static const void* fwd(int pp) {
+    switch (pp) {
+      case 1: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 1>);
+      case 2: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 2>);
+      case 4: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 4>);
+      default: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 8>);
+    }
+  }
+  static const void* bwd(int pp) {
+    switch (pp) {
+      case 1: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 1>);
+      case 2: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 2>);
+      case 4: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 4>);
+      default: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 8>);
+    }
+  }
+};
+
+struct SimtPlan {
+  int NU = 0, nblk = 0, KC = 0, PP = 0;
+  size_t smem = 0;
+};
+
+int pp_for(int pairs) {
+  const int need = (pairs + kThreads - 1) / kThreads;
+  return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : 0;
+}
+
+// Pick units per CTA: minimise an estimated step time (a fixed cost for the
+// cross-CTA exchange when there is more than one CTA, plus the per-thread FMA
+// count) subject to shared memory, registers and co-residency of the grid.
+int make_plan(const PersistArgs& a, bool bwd, int num_sms, SimtPlan* out) {
+  const int H = a.H, B = a.B;
+  const size_t es = a.is_bf16 ? 2 : 4;
+  const size_t smem_cap = 200 * 1024;
+  int KC = (8192 / B) - 1;
+  KC = (KC / 4) * 4;
+  if (KC < 4) return 2;
+  const int Kmax = bwd ? 4 * H : H;
+  if (KC > Kmax) KC = (Kmax + 3) / 4 * 4;
+  const size_t hs_bytes = static_cast<size_t>(B) * (KC + 1) * 4;
+  double best = 1e300;
+  SimtPlan bp;
+  for (int NU = 1; NU <= H; ++NU) {
+    const int nblk = (H + NU - 1) / NU;
+    if (nblk * a.ndir > num_sms) continue;
+    const int pp = pp_for(NU * B);
+    if (pp == 0) break;
+    const size_t wbytes = bwd ? static_cast<size_t>(NU) * (4 * H + (a.is_bf16 ? 2 : 1)) * es
+                              : static_cast<size_t>(4) * NU * (H + (a.is_bf16 ? 2 : 1)) * es;
+    const size_t smem = align16(wbytes) + hs_bytes;
+    if (smem > smem_cap) break;
+    const double cost = (nblk > 1 ? 3000.0 : 0.0) + static_cast<double>(pp) * 4.0 * H * (bwd ? 1.0 : 1.0) +
+                        static_cast<double>(B) * (bwd ? 4 * H : H) / kThreads;
+    if (cost < best) {
+      best = cost;
+      bp.NU = NU; bp.nblk = nblk; bp.KC = KC; bp.PP = pp; bp.smem = smem;
+    }
+  }
+  if (bp.NU == 0) return 2;
+  *out = bp;
+  return 0;
+}
+
+int launch_simt(const PersistArgs& a, bool bwd, cudaStream_t s, int num_sms) {
+  SimtPlan pl;
+  int rc = make_plan(a, bwd, num_sms, &pl);
+  if (rc) return rc;
+  const void* fn = a.is_bf16 ? (bwd ? SimtKernels<__nv_bfloat16>::bwd(pl.PP) : SimtKernels<__nv_bfloat16>::fwd(pl.PP))
+                             : (bwd ? SimtKernels<float>::bwd(pl.PP) : SimtKernels<float>::fwd(pl.PP));
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) != cudaSuccess)
+    return 3;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, pl.smem) != cudaSuccess) return 3;
+  if (per_sm * num_sms < pl.nblk * a.ndir) return 2;
+  dim3 grid(pl.nblk, a.ndir);
+  PersistArgs args = a;
+  int NU = pl.NU, KC = pl.KC;
+  void* params[] = {&args, &NU, &KC};
+  if (cudaLaunchKernel(fn, grid, dim3(kThreads), params, pl.smem, s) != cudaSuccess) return 3;
+  return 0;
+}
+
+}  // namespace
+
+int plan_persist_simt(const PersistArgs& a, int num_sms, int* nblk, size_t* smem) {
+  SimtPlan pf, pb;
+  int rc = make_plan(a, false, num_sms, &pf);
+  if (rc) return rc;
+  rc = make_plan(a, true, num_sms, &pb);
+  if (rc) return rc;
+  if (nblk) *nblk = pf.nblk > pb.nblk ? pf.nblk : pb.nblk;
+  if (smem) *smem = pf.smem > pb.smem ? pf.smem : pb.smem;
+  return 0;
+}
+
+int launch_persist_fwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms) {
+  return launch_simt(a, false, s, num_sms);
+}
+
+int launch_persist_bwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms) {
+  return launch_simt(a, true, s, num_sms);
+}
+
+}  // namespace rnn

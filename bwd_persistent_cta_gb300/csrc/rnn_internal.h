@@ -1,0 +1,127 @@
+// rnn_internal.h - internal data layouts and kernel launch interfaces.
+//
+// Internal layouts (all seq-major; s = storage element, fp32 or bf16):
+//   * Gate slots are unit-interleaved: column 4*u + slot of a [.., 4H] array
+//     belongs to hidden unit u.  Slots (canonical gate order):
+//       LSTM            i, f, g, o
+//       GRU resetAfter  r, z, n, hn (hn = W_hn h + b_hn, forward reserve only)
+//       GRU reset-before r, z, n, (unused)
+//     GRU's fourth slot is padding in every weight matrix (zero rows).
+//   * P  [T, B, D*4H]  s    input projection W_ih x_t + b (all directions)
+//   * Y  [T+2, B, D*H] s    layer output; slot t+1 holds y_t.  Slot 0 holds
+//     the forward direction's h0 (columns [0, H)), slot T+1 the reverse
+//     direction's h0 (columns [H, 2H)), so h_{t-1} of the forward direction
+//     is slot t and h_{t+1} of the reverse direction is slot t+2.
+//   * GATES [D][T, B, 4H] s  post-activation gates (reserve).
+//   * C [D][T+1, B, H] fp32  LSTM cell state: forward c_t at slot t+1 (c0 at 0);
+//     reverse c_t at slot t (c0 at T).
+//   * RH [D][T, B, H] s      GRU reset-before r * h_{t-1} (reserve).
+//   * DG [T, B, D*4H] s      gate pre-activation gradients: LSTM (da_i, da_f,
+//     da_g, da_o); GRU resetAfter (dr, dz, dn, dn*r); reset-before (dr, dz, dn, 0).
+//   * DB [D][4H] fp32        batch- and time-summed DG, slot order (GRU
+//     resetAfter: slots r, z, n give the input-side bias gradient and slots
+//     r, z, n*r the recurrent-side one).
+//   * Packed weights: WX [D*4H, I_l] (row d*4H + 4u + s = W_ih of gate s, unit u),
+//     WXT [I_l, D*4H], WR [D][4H, H] (row 4u + s = W_hh row of gate s, unit u),
+//     WRT [D][H, 4H] (element (j, 4u+s) = W_hh[gate(s)][u][j]; for GRU
+//     resetAfter slot 2 is zero and slot 3 holds W_hn, matching the DG slots
+//     of the recurrent side), BX [D*4H] fp32, BH [D*4H] fp32.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+namespace rnn {
+
+constexpr int kSlots = 4;
+
+struct DevArea {
+  unsigned int counters[32];   // step counters of the running persistent launch
+  unsigned int status;         // 0, or the first rnn_status_t a kernel reported
+  unsigned int where[4];       // kernel id, block, step, wait kind of that report
+  unsigned int pad[27];
+};
+
+enum KernelId : unsigned int { K_FWD_SIMT = 1, K_BWD_SIMT = 2, K_FWD_TC = 3, K_BWD_TC = 4, K_GEMM_TC = 5 };
+enum WaitKind : unsigned int { W_COUNTER = 1, W_TMA = 2, W_MMA = 3, W_PEER = 4 };
+
+// C[row(m), n] = sum_k A(m, k) * B(n, k)  (+ bias[n]) (+ C_old if beta)
+//   A(m, k) = A[m*lda + k] (a_kmajor) or A[k*lda + m];  same for B with n.
+//   row(m) = m, or with rowmap_H > 0: m = 4u + s -> perm[s]*rowmap_H + u
+//   (rows whose perm[s] < 0 are not written).
+struct GemmArgs {
+  int M = 0, N = 0, K = 0;
+  const void* A = nullptr; int64_t lda = 0; int a_kmajor = 1;
+  const void* B = nullptr; int64_t ldb = 0; int b_kmajor = 1;
+  void* C = nullptr; int64_t ldc = 0; int c_bf16 = 0;
+  const float* bias = nullptr;
+  int beta = 0;
+  int rowmap_H = 0;
+  int perm[4] = {0, 1, 2, 3};
+  int in_bf16 = 1;            // operand element type (SIMT kernel takes fp32 too)
+};
+
+struct PersistArgs {
+  int mode = 0, reset_after = 0, is_bf16 = 0;
+  int T = 0, B = 0, H = 0, D = 1;   // D = directions of the layer (buffer strides)
+  int dir0 = 0, ndir = 1;            // directions handled by this launch
+  // forward
+  const void* P = nullptr;
+  const float* bh = nullptr;
+  const void* Wr = nullptr;
+  void* Y = nullptr;
+  void* gates = nullptr;
+  float* C = nullptr;
+  void* RH = nullptr;
+  const void* c0 = nullptr;          // [D][B, H] slice of cx for this layer
+  void* hy = nullptr;                // [D][B, H]
+  void* cy = nullptr;
+  // backward
+  const void* WrT = nullptr;
+  const float* dYi = nullptr;        // [T, B, D*H]
+  void* dG = nullptr;
+  float* db = nullptr;
+  const void* dhT = nullptr;         // [D][B, H] slice of dhy
+  const void* dcT = nullptr;
+  void* dh0 = nullptr;               // [D][B, H] slice of dhx
+  void* dc0 = nullptr;
+  DevArea* dev = nullptr;
+  uint64_t timeout_ns = 2000000000ull;
+  int skip_cta = -1;
+};
+
+// Host-side launch status: 0 = launched, otherwise an rnn_status_t value.
+int launch_gemm_simt(const GemmArgs& g, cudaStream_t s);
+int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns);
+bool gemm_tc_supported(const GemmArgs& g);
+
+int plan_persist_simt(const PersistArgs& a, int num_sms, int* nblk, size_t* smem);
+int launch_persist_fwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
+int launch_persist_bwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
+
+bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms);
+int launch_persist_fwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms);
+int launch_persist_bwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms);
+
+// TMA tensor map (CUtensorMap, 128 bytes) over a bf16 row-major matrix
+// ptr[j * ld + i], i < dim0, j < dim1, box box0 x box1, 128-byte swizzle.
+int make_tmap_bf16_2d(void* map, const void* ptr, uint64_t dim0, uint64_t dim1, uint64_t ld_elems,
+                      uint32_t box0, uint32_t box1);
+
+// layout / cast / pack kernels (layout.cu)
+// slot_src[s] = index of the user's gate block for internal slot s (-1 = zero)
+int launch_pack_rows(const void* W, int G, int H, int K, const int* slot_src, int is_bf16,
+                     void* out, int64_t ld_out, int transpose, cudaStream_t s);
+int launch_pack_bias(const void* b, int H, const int* slot_src, int is_bf16, float* out,
+                     cudaStream_t s);
+int launch_seq_transpose(const void* in, void* out, int T, int B, int F, int in_bf16,
+                         int out_bf16, int in_batch_first, int out_batch_first,
+                         int64_t out_ld, cudaStream_t s);
+int launch_states_to_y(const void* h0, void* Y, int T, int B, int H, int D, int dir,
+                       int is_bf16, cudaStream_t s);
+int launch_bias_grad_scatter(const float* db, int H, const int* slot_dst, int is_second,
+                             float* out, cudaStream_t s);
+int launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
+
+}  // namespace rnn

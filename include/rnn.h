@@ -1,0 +1,185 @@
+/*
+ * rnn.h - C ABI of the GB300 (sm_103a) multi-timestep LSTM / GRU library.
+ *
+ * One layer stack (1..8 layers, uni- or bidirectional) of LSTM or GRU cells,
+ * run forward over a whole sequence and back-propagated through time.  The
+ * three-phase split (forward, backward-data, backward-weights) follows the
+ * cuDNN RNN calls that SystemDS LibMatrixCuDNN.java makes in ``lstm`` and
+ * ``lstmBackward`` (cudnnRNNForwardTraining, cudnnRNNBackwardData,
+ * cudnnRNNBackwardWeights), and the Fwd / Bwd / WU entry points of poplibs
+ * Lstm.cpp (lstmFwd, lstmBwd, lstmWU) and Gru.cpp (gruFwd, gruBwd, gruWU).
+ *
+ * Cell definitions (canonical gate order; sigma = logistic sigmoid):
+ *   LSTM (Lstm.cpp lstmCellForwardPassCalcUnits / basicLstmCellForwardPass):
+ *     a = W_ih x_t + W_hh h_{t-1} + b
+ *     i = sigma(a_i), f = sigma(a_f), g = tanh(a_g), o = sigma(a_o)
+ *     c_t = f c_{t-1} + i g,  h_t = o tanh(c_t)
+ *   GRU resetAfter (Gru.cpp gruCellForwardPassCalcUnitsResetAfter):
+ *     r = sigma(W_ir x + b_ir + W_hr h + b_hr), z = sigma(W_iz x + b_iz + W_hz h + b_hz)
+ *     n = tanh(W_in x + b_in + r * (W_hn h + b_hn)),  h_t = (1 - z) n + z h_{t-1}
+ *   GRU reset-before (Gru.cpp gruCellForwardPassCalcUnits / basicGruCellForwardPass):
+ *     r, z as above with one bias b_r, b_z;  n = tanh(W_in x + b_n + W_hn (r * h_{t-1}))
+ *     h_t = (1 - z) n + z h_{t-1}
+ * Backward: the BPTT recurrences of Lstm.cpp / Gru.cpp backwardStepImpl and
+ * backwardStepImplResetAfter (identical to the LSTM and GRU branches of the
+ * persistent RNN backward-data kernel fragment), and the weight-gradient sums
+ * of basicLstmParamUpdate / basicGruParamUpdate.
+ *
+ * Conventions shared by every call
+ *   - All pointers marked "device" are device memory owned by the caller; the
+ *     library never frees them.  The handle owns only host metadata and a small
+ *     device area (status word, step counters) allocated in rnn_create.
+ *   - Calls are asynchronous on ``stream`` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).  Errors found on the host are returned;
+ *     errors found on the device (a spin-wait that ran out, RNN_TIMEOUT) are
+ *     recorded in the handle's status word and returned by rnn_sync_status.
+ *   - No call throws or aborts; every failure is a status code.
+ *   - Sequences are seq-major [T, B, F] unless desc.batch_first != 0, in which
+ *     case x, y, dy and dx are [B, T, F].  States (hx, cx, hy, cy, dhy, dcy,
+ *     dhx, dcx) are [L*D, B, H] with index l*D + d (d = 0 forward, 1 reverse).
+ *     A bidirectional layer's output row is [y_fwd (H) | y_bwd (H)].
+ *   - Element type of x, y, dy, dx, w and all states is desc.dtype (fp32 or
+ *     bf16).  Accumulation and the cell state are always fp32.  dw is fp32.
+ *   - State pointers may be NULL: NULL inputs (hx, cx, dhy, dcy) mean zero,
+ *     NULL outputs (hy, cy, dhx, dcx) are skipped - the same convention as the
+ *     ``cx == NULL`` / ``dhx != NULL`` tests of the persistent backward-data
+ *     kernel fragment and the NULL dhy that SystemDS passes.
+ *   - Every device pointer must be 16-byte aligned.
+ */
+#ifndef GB300_RNN_H
+#define GB300_RNN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RNN_OK = 0,
+  RNN_BAD_PARAM = 1,       /* a descriptor field or pointer is invalid         */
+  RNN_NOT_SUPPORTED = 2,   /* valid, but this build / GPU cannot run it        */
+  RNN_CUDA_ERROR = 3,      /* a CUDA runtime / driver call failed              */
+  RNN_TIMEOUT = 4,         /* a device spin-wait gave up (see rnn_sync_status) */
+  RNN_BAD_WORKSPACE = 5,   /* workspace / reserve pointer NULL or misaligned   */
+  RNN_INTERNAL = 6
+} rnn_status_t;
+
+typedef enum { RNN_LSTM = 0, RNN_GRU = 1 } rnn_mode_t;
+typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
+
+/* Recurrent-kernel choice.  AUTO picks the tensor-core persistent kernels
+ * (bf16 LSTM and GRU resetAfter whose W_hh slices fit on chip) and the SIMT
+ * persistent kernels otherwise (every fp32 problem, GRU reset-before, shapes
+ * the tensor-core kernels do not take).  The two explicit values force one. */
+typedef enum { RNN_ALGO_AUTO = 0, RNN_ALGO_PERSIST_TC = 1, RNN_ALGO_PERSIST_SIMT = 2 } rnn_algo_t;
+
+typedef struct {
+  int mode;            /* rnn_mode_t                                                */
+  int gate_order[4];   /* block k of every per-gate matrix holds canonical gate
+                          gate_order[k] (LSTM 0..3 = i,f,g,o; GRU 0..2 = r,z,n).
+                          All zero = canonical order.                               */
+  int reset_after;     /* GRU only: 1 = resetAfter form, 0 = reset-before           */
+  int bidirectional;   /* 0 or 1                                                    */
+  int num_layers;      /* 1..8                                                      */
+  int seq_len;         /* T >= 1                                                    */
+  int batch;           /* B >= 1                                                    */
+  int input_size;      /* I >= 1 (layer 0 input; later layers take D*H)             */
+  int hidden_size;     /* H >= 1                                                    */
+  int dtype;           /* rnn_dtype_t                                               */
+  int batch_first;     /* 0 = [T,B,F], 1 = [B,T,F] for x, y, dy, dx                 */
+  int algo;            /* rnn_algo_t                                                */
+} rnn_desc_t;
+
+typedef struct rnn_handle_s* rnn_handle_t;
+
+/* Validate ``desc`` and make a handle.  Allocates the handle's small device
+ * area on the current device (which the handle is then bound to).
+ * Returns RNN_BAD_PARAM for an invalid descriptor, RNN_NOT_SUPPORTED when the
+ * current GPU is not sm_103 or the forced algo cannot take the shape,
+ * RNN_CUDA_ERROR when the device allocation fails. */
+rnn_status_t rnn_create(const rnn_desc_t* desc, rnn_handle_t* handle);
+
+/* Free the handle and its device area.  NULL is accepted. */
+rnn_status_t rnn_destroy(rnn_handle_t handle);
+
+/* Byte sizes the caller must allocate (device memory, 256-byte aligned):
+ *   weight_bytes    - the packed weight buffer w (desc.dtype elements); dw
+ *                     has the same element count at 4 bytes per element.
+ *                     Per layer l, per direction d, in this order:
+ *                     W_ih [G*H, I_l] row-major, W_hh [G*H, H], b [G*H], and
+ *                     for GRU resetAfter b_h [G*H].  G = 4 (LSTM) or 3 (GRU);
+ *                     gate blocks in desc.gate_order.  LSTM and GRU
+ *                     reset-before have one bias vector per direction.
+ *   workspace_bytes - scratch for any one call; contents need not persist.
+ *   reserve_bytes   - state kept from rnn_forward (training) to the two
+ *                     backward calls, and from rnn_backward_data to
+ *                     rnn_backward_weights; must not be touched in between.
+ * Any output pointer may be NULL. */
+rnn_status_t rnn_get_sizes(rnn_handle_t handle, size_t* weight_bytes,
+                           size_t* workspace_bytes, size_t* reserve_bytes);
+
+/* Forward over the whole sequence.
+ *   x  [T,B,I] (device, in)         hx, cx [L*D,B,H] (device, in, may be NULL)
+ *   w  weight_bytes (device, in)    y  [T,B,D*H] (device, out)
+ *   hy, cy [L*D,B,H] (device, out, may be NULL; cy and cx are LSTM only)
+ *   workspace (device, workspace_bytes, scratch)
+ *   reserve (device, reserve_bytes, out) - NULL runs inference: nothing is
+ *     kept for a backward pass.
+ * cx is ignored for GRU. */
+rnn_status_t rnn_forward(rnn_handle_t handle, const void* x, const void* hx, const void* cx,
+                         const void* w, void* y, void* hy, void* cy,
+                         void* workspace, void* reserve, void* stream);
+
+/* Backward through time (data gradients).  Needs the reserve written by
+ * rnn_forward with the same x, hx, cx and w.
+ *   y     forward output; accepted for interface symmetry, the reserve holds
+ *         the copy the kernels read (may be NULL)
+ *   dy    [T,B,D*H] (device, in)     dhy, dcy [L*D,B,H] (device, in, may be NULL)
+ *   w     (device, in)               hx, cx: accepted for symmetry (may be NULL)
+ *   dx    [T,B,I] (device, out)      dhx, dcx [L*D,B,H] (device, out, may be NULL)
+ * Writes the gate and bias gradients into the reserve for
+ * rnn_backward_weights. */
+rnn_status_t rnn_backward_data(rnn_handle_t handle, const void* y, const void* dy,
+                               const void* dhy, const void* dcy, const void* w,
+                               const void* hx, const void* cx, void* dx, void* dhx,
+                               void* dcx, void* workspace, void* reserve, void* stream);
+
+/* Weight gradients dW_ih = sum_t dA_t x_t^T, dW_hh = sum_t dA^h_t h_{t-1}^T,
+ * db = sum_t dA_t (GRU resetAfter also db_h = sum_t dA^h_t), summed over the
+ * batch, written (overwritten, never accumulated) into dw: fp32, same layout
+ * as w.  Needs the reserve after rnn_backward_data.  x, hx, y: accepted for
+ * symmetry with cudnnRNNBackwardWeights; the reserve holds what is read. */
+rnn_status_t rnn_backward_weights(rnn_handle_t handle, const void* x, const void* hx,
+                                  const void* y, void* workspace, const void* reserve,
+                                  void* dw, void* stream);
+
+/* Synchronise ``stream`` and return (then clear) the device status word:
+ * RNN_OK, or RNN_TIMEOUT when a persistent kernel's bounded spin-wait gave up
+ * (its outputs are then invalid), or RNN_CUDA_ERROR. */
+rnn_status_t rnn_sync_status(rnn_handle_t handle, void* stream);
+
+/* Upper bound, in nanoseconds, of every device spin-wait (default 2 s). */
+rnn_status_t rnn_set_timeout_ns(rnn_handle_t handle, uint64_t ns);
+
+/* Number of kernels this handle has launched since it was created. */
+uint64_t rnn_launch_count(rnn_handle_t handle);
+
+/* Which recurrent kernel the handle runs: 1 = tensor-core persistent,
+ * 2 = SIMT persistent (rnn_algo_t values). */
+int rnn_selected_algo(rnn_handle_t handle);
+
+/* Test hook for the timeout path: CTA ``cta`` (>= 0) of the next persistent
+ * launches skips its per-step arrival, so its peers' bounded waits run out and
+ * the call ends with RNN_TIMEOUT instead of hanging.  -1 (default) = off. */
+rnn_status_t rnn_debug_skip_arrival(rnn_handle_t handle, int cta);
+
+/* Static text for a status code. */
+const char* rnn_status_string(rnn_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_RNN_H */
