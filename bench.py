@@ -1,0 +1,376 @@
+#!/usr/bin/env python
+"""Benchmark: LSTM / GRU forward + backward-through-time on GB300.
+
+One step = rnn_forward (training) + rnn_backward_data + rnn_backward_weights
+over one batch of seeded synthetic sequences, inputs resident in HBM.  The
+default workload is the single-layer GRU resetAfter, bf16 storage / fp32
+accumulation, seq 128, batch 64, input = hidden = 512.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...     (the fp64 oracle on host cores)
+
+Multi-GPU: one process per GPU under torchrun; the sequences of a step are
+independent, so each rank runs its own replica on its own batch (weak
+scaling, no data-path collective); timing takes the max over ranks.
+
+Prints one JSON line (rank 0).  ``value`` is timestep*batch per second over
+all ranks; ``roofline`` covers the kernel class with the largest share of the
+step, timed live with CUDA events on its launching stream.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "gru_ra_bf16_T128_B64_H512"
+L2_BYTES = 129 * 1024 * 1024
+METRIC = "LSTM/GRU fwd+bwd timestep*batch/s"
+UNIT = "timestep*batch/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# fp64 oracle on the host cores (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+def _oracle_sample_cols(wl, target_s: float) -> int:
+    """Batch columns per oracle sample so that one sample takes ~target_s."""
+    # fp64 numpy on the host: rough rate for sizing only
+    flops_per_col = wl.flops() / wl.batch
+    est_rate = 5e9
+    cols = max(1, min(wl.batch, int(target_s * est_rate / max(flops_per_col, 1.0))))
+    return cols
+
+
+def oracle_worker(spec: str) -> None:
+    """Internal mode, run in a fresh process: time the oracle on a bounded
+    sample and print {"seconds": ..., "units": ..., "repeats": ...}."""
+    import synth
+    from oracle import rnn_oracle
+    name, cols, budget = spec.split(":")
+    wl = synth.WORKLOADS[name]
+    cols, budget = int(cols), float(budget)
+    inp = synth.make_inputs(wl, batch_subset=list(range(cols)))
+    reps, t_total = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        rnn_oracle.run_inputs(inp, with_backward=not wl.forward_only)
+        t_total += time.perf_counter() - t0
+        reps += 1
+        if t_total >= budget:
+            break
+    print(json.dumps({"seconds": t_total, "units": reps * wl.seq_len * cols, "repeats": reps}))
+
+
+def run_oracle_subprocess(wl, budget_s: float, cols: int):
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample",
+                        f"{wl.name}:{cols}:{budget_s}"], capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle sample failed: {r.stderr[-2000:]}")
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    return out, cores
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu_index), "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic flop counts per kernel class (per whole step)
+# ---------------------------------------------------------------------------
+def class_flops(wl):
+    G, H, B, T, D = wl.gates, wl.hidden_size, wl.batch, wl.seq_len, wl.dirs
+    rec = sum(D * 2.0 * G * H * H * B * T for _ in range(wl.num_layers))
+    proj = sum(D * 2.0 * G * H * wl.layer_input(l) * B * T for l in range(wl.num_layers))
+    return {"persist_fwd": rec, "persist_bwd": rec, "gemm_proj": proj, "gemm_dx": proj,
+            "gemm_dw": proj + rec, "layout": 0.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16_tflops": d.get("bf16_tflops"), "hbm_gbs": d.get("hbm_gbs"), "src": "measured"}
+    return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "src": "fallback"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+    import synth
+    import bwd_persistent_cta_gb300 as R
+    from bwd_persistent_cta_gb300 import build as B
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0:
+        B.build()
+    if dist is not None:
+        dist.barrier()
+    B.build()
+
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    dev = torch.device("cuda", local)
+
+    def dt(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev, tdt)
+
+    rnn = R.RNN(wl.mode, wl.input_size, wl.hidden_size, wl.seq_len, wl.batch, wl.num_layers, wl.bidirectional,
+                wl.reset_after, wl.dtype, wl.gate_order, wl.batch_first, device=dev)
+    w = dt(synth.flatten_params(wl, inp.params))
+    x, dy, hx, cx = dt(inp.x), dt(inp.dy), dt(inp.h0), dt(inp.c0)
+    D = wl.dirs
+    y = torch.empty(wl.seq_len, wl.batch, D * wl.hidden_size, dtype=tdt, device=dev)
+    S = (wl.num_layers * D, wl.batch, wl.hidden_size)
+    hy = torch.empty(S, dtype=tdt, device=dev)
+    cy = torch.empty(S, dtype=tdt, device=dev) if wl.mode == "lstm" else None
+    dx = torch.empty_like(x)
+    dhx = torch.empty(S, dtype=tdt, device=dev)
+    dcx = torch.empty(S, dtype=tdt, device=dev) if wl.mode == "lstm" else None
+    dw = torch.empty(rnn.weight_count, dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        rnn.forward(x, w, hx, cx, train=not wl.forward_only, y=y, hy=hy, cy=cy)
+        if not wl.forward_only:
+            rnn.backward_data(dy, w, None, None, dx=dx, dhx=dhx, dcx=dcx)
+            rnn.backward_weights(x, dw=dw)
+
+    for _ in range(args.warmup):
+        step()
+    rnn.sync()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] or local)
+                           if os.environ.get("CUDA_VISIBLE_DEVICES") else local)
+    R.rnn_get_timing(rnn.handle)
+    R.rnn_set_timing(rnn.handle, True)
+    launches0 = rnn.launches()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    for k in range(K):
+        flush.zero_()
+        starts[k].record()
+        step()
+        ends[k].record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    rnn.sync()
+    R.rnn_set_timing(rnn.handle, False)
+    launches = rnn.launches() - launches0
+    cls_ms, cls_n = R.rnn_get_timing(rnn.handle)
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # --- end to end through the C ABI with host buffers --------------------
+    xh = x.cpu().pin_memory()
+    dyh = dy.cpu().pin_memory()
+    dwh = torch.empty(dw.shape, dtype=dw.dtype).pin_memory()
+    for _ in range(2):
+        x.copy_(xh, non_blocking=True); dy.copy_(dyh, non_blocking=True); step(); dwh.copy_(dw, non_blocking=True)
+    torch.cuda.synchronize()
+    Ke = max(3, K // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_ms = 0.0
+    for _ in range(Ke):
+        flush.zero_()
+        e0.record()
+        x.copy_(xh, non_blocking=True)
+        dy.copy_(dyh, non_blocking=True)
+        step()
+        dwh.copy_(dw, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        e_ms += e0.elapsed_time(e1)
+    e_ms /= Ke
+    if dist is not None:
+        t = torch.tensor([e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    rnn.sync()
+
+    units = wl.seq_len * wl.batch * world
+    value = units / (ms / 1e3)
+    tflops = wl.flops() * world / (ms / 1e3) / 1e12
+    peaks = load_peaks()
+    names = R.TIMING_CLASS_NAMES
+    per_step = {n: cls_ms[i] / K for i, n in enumerate(names)}
+    dom = max(range(len(names)), key=lambda i: cls_ms[i])
+    fl = class_flops(wl)
+    per_launch_ms = cls_ms[dom] / max(cls_n[dom], 1)
+    launches_per_step = cls_n[dom] / K
+    flops_per_launch = fl[names[dom]] / max(launches_per_step, 1)
+    achieved = flops_per_launch / (per_launch_ms / 1e3) / 1e12
+    roofline = {"kernel": names[dom], "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "peak_src": peaks["src"] + " bf16 burst", "share": cls_ms[dom] / max(sum(cls_ms), 1e-9),
+                "per_launch_ms": per_launch_ms, "per_class_ms_per_step": per_step}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cols = _oracle_sample_cols(wl, 3.0)
+        out, cores = run_oracle_subprocess(wl, 12.0, cols)
+        cpu = {"value": out["units"] / out["seconds"], "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{wl.name} with {cols} of {wl.batch} batch columns, fwd+bwd, "
+                         f"{out['repeats']} repeats in {out['seconds']:.1f} s (fp64 numpy)"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "mode": wl.mode, "reset_after": wl.reset_after,
+                       "layers": wl.num_layers, "bidirectional": wl.bidirectional, "seq_len": wl.seq_len,
+                       "batch_per_gpu": wl.batch, "input": wl.input_size, "hidden": wl.hidden_size,
+                       "seed": wl.seed, "parallelism": f"replicas{world}",
+                       "l2": "flushed (256 MiB write) before every timed step"},
+            "tflops": tflops, "tflops_unit": "TFLOP/s (algorithmic, sum over layers/dirs of 3*2*G*H*(I+H)*B*T)",
+            "e2e": {"value": units / (e_ms / 1e3), "unit": UNIT,
+                    "h2d_bytes_per_step": int(x.numel() * x.element_size() + dy.numel() * dy.element_size()),
+                    "d2h_bytes_per_step": int(dw.numel() * dw.element_size())},
+            "gpu_launches": int(launches), "gpu_launches_per_step": launches / K,
+            "roofline": roofline, "clocks": clocks, "cpu_baseline": cpu,
+            "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line))
+    rnn.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    cols = _oracle_sample_cols(wl, 2.0)
+    per_step = []
+    units = 0
+    cores = os.cpu_count() or 1
+    for i in range(args.warmup + args.steps):
+        out, cores = run_oracle_subprocess(wl, 0.0, cols)
+        if i >= args.warmup:
+            per_step.append(out["seconds"])
+            units += out["units"]
+    secs = sum(per_step)
+    value = units / secs
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "seq_len": wl.seq_len, "batch_per_gpu": wl.batch,
+                       "hidden": wl.hidden_size, "input": wl.input_size},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{wl.name} with {cols} of {wl.batch} batch columns per step, fwd+bwd"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.oracle_sample:
+        oracle_worker(args.oracle_sample)
+        return
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -40,6 +40,10 @@ struct rnn_handle_s {
   int skip_cta;
   uint64_t launches;
   bool trace;
+  bool timing;
+  struct Ev { cudaEvent_t a, b; int cls; };
+  std::vector<Ev> events;      // recorded, not yet read
+  std::vector<Ev> pool;        // created, free
   // weight offsets (elements), per layer and direction
   std::vector<size_t> off_ih, off_hh, off_b, off_bh;
   size_t weight_elems;
@@ -151,8 +155,34 @@ int count(rnn_handle_s* h, int rc, int n = 1) {
   return rc;
 }
 
-int run_gemm(rnn_handle_s* h, GemmArgs g, cudaStream_t s) {
+// Records an event pair around the launches made while it lives (timing on).
+struct TimeScope {
+  rnn_handle_s* h;
+  cudaStream_t s;
+  rnn_handle_s::Ev ev{};
+  bool on;
+  TimeScope(rnn_handle_s* h_, int cls, cudaStream_t s_) : h(h_), s(s_), on(h_->timing) {
+    if (!on) return;
+    if (!h->pool.empty()) {
+      ev = h->pool.back();
+      h->pool.pop_back();
+    } else if (cudaEventCreate(&ev.a) != cudaSuccess || cudaEventCreate(&ev.b) != cudaSuccess) {
+      on = false;
+      return;
+    }
+    ev.cls = cls;
+    cudaEventRecord(ev.a, s);
+  }
+  ~TimeScope() {
+    if (!on) return;
+    cudaEventRecord(ev.b, s);
+    h->events.push_back(ev);
+  }
+};
+
+int run_gemm(rnn_handle_s* h, GemmArgs g, cudaStream_t s, int cls) {
   if (g.M <= 0 || g.N <= 0) return 0;
+  TimeScope ts(h, cls, s);
   if (g.K <= 0) return 2;
   g.in_bf16 = h->bf16;
   if (h->bf16 && gemm_tc_supported(g)) return count(h, launch_gemm_tc(g, s, h->num_sms, h->dev, h->timeout_ns));
@@ -172,6 +202,7 @@ int run_persist(rnn_handle_s* h, PersistArgs a, bool bwd, cudaStream_t s) {
   auto go = [&](PersistArgs& x) -> int {
     int rc = reset_counters(h, s);
     if (rc) return rc;
+    TimeScope ts(h, bwd ? 1 : 0, s);
     if (h->algo == RNN_ALGO_PERSIST_TC)
       rc = bwd ? launch_persist_bwd_tc(x, s, h->num_sms) : launch_persist_fwd_tc(x, s, h->num_sms);
     else
@@ -272,6 +303,7 @@ rnn_status_t rnn_create(const rnn_desc_t* desc, rnn_handle_t* out) {
   h->launches = 0;
   const char* tr = std::getenv("RNN_TRACE");
   h->trace = tr && tr[0] == '1';
+  h->timing = false;
   fill_layout(h);
 
   // recurrent kernel choice
@@ -293,6 +325,8 @@ rnn_status_t rnn_create(const rnn_desc_t* desc, rnn_handle_t* out) {
 
 rnn_status_t rnn_destroy(rnn_handle_t h) {
   if (!h) return RNN_OK;
+  for (auto& e : h->events) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
+  for (auto& e : h->pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
   if (h->dev) cudaFree(h->dev);
   delete h;
   return RNN_OK;
@@ -310,6 +344,33 @@ rnn_status_t rnn_set_timeout_ns(rnn_handle_t h, uint64_t ns) {
   if (!h || ns == 0) return RNN_BAD_PARAM;
   h->timeout_ns = ns;
   return RNN_OK;
+}
+
+rnn_status_t rnn_set_timing(rnn_handle_t h, int enable) {
+  if (!h) return RNN_BAD_PARAM;
+  h->timing = enable != 0;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_get_timing(rnn_handle_t h, double* ms, uint64_t* n) {
+  if (!h) return RNN_BAD_PARAM;
+  double acc[RNN_TIMING_CLASSES] = {0};
+  uint64_t cnt[RNN_TIMING_CLASSES] = {0};
+  rnn_status_t rs = RNN_OK;
+  for (auto& e : h->events) {
+    float t = 0.f;
+    if (cudaEventSynchronize(e.b) != cudaSuccess || cudaEventElapsedTime(&t, e.a, e.b) != cudaSuccess)
+      rs = RNN_CUDA_ERROR;
+    acc[e.cls] += t;
+    cnt[e.cls] += 1;
+    h->pool.push_back(e);
+  }
+  h->events.clear();
+  for (int i = 0; i < RNN_TIMING_CLASSES; ++i) {
+    if (ms) ms[i] = acc[i];
+    if (n) n[i] = cnt[i];
+  }
+  return rs;
 }
 
 uint64_t rnn_launch_count(rnn_handle_t h) { return h ? h->launches : 0; }
@@ -384,7 +445,7 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
     g.B = at<char>(workspace, h->w_wx); g.ldb = Il; g.b_kmajor = 1;
     g.C = at<char>(workspace, h->w_p); g.ldc = D * 4 * H; g.c_bf16 = h->bf16;
     g.bias = at<float>(workspace, h->w_bx);
-    RNN_TRY(run_gemm(h, g, s));
+    RNN_TRY(run_gemm(h, g, s, 2));
     // layer output buffer with h0 in its boundary slots
     Ybuf = train ? at<char>(reserve, h->r_y[l]) : at<char>(workspace, (l & 1) ? h->w_y1 : h->w_y0);
     for (int d = 0; d < D; ++d) {
@@ -469,7 +530,7 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
     } else {
       g.C = h->bfirst ? at<char>(workspace, h->w_dx0) : dx; g.ldc = Il; g.c_bf16 = h->bf16;
     }
-    RNN_TRY(run_gemm(h, g, s));
+    RNN_TRY(run_gemm(h, g, s, 3));
   }
   if (h->bfirst)
     RNN_TRY(count(h, launch_seq_transpose(at<char>(workspace, h->w_dx0), dx, T, B, h->I, h->bf16, h->bf16, 0, 1,
@@ -527,19 +588,19 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
       g.B = Xl; g.ldb = Il; g.b_kmajor = 0;
       g.C = dwf + h->off_ih[i]; g.ldc = Il; g.c_bf16 = 0;
       for (int k = 0; k < 4; ++k) g.perm[k] = m_ih[k];
-      RNN_TRY(run_gemm(h, g, s));
+      RNN_TRY(run_gemm(h, g, s, 4));
       // dW_hh = sum over (t, b) of dG^h h_prev^T ; h_prev rows are Y slots t (forward) / t+2 (reverse)
       const char* hp = rs + h->r_y[l] + (static_cast<size_t>(d == 0 ? 0 : 2) * B * D * H + static_cast<size_t>(d) * H) * es;
       g.N = H;
       g.B = hp; g.ldb = D * H; g.b_kmajor = 0;
       g.C = dwf + h->off_hh[i]; g.ldc = H;
       for (int k = 0; k < 4; ++k) g.perm[k] = m_hh[k];
-      RNN_TRY(run_gemm(h, g, s));
+      RNN_TRY(run_gemm(h, g, s, 4));
       if (h->rb) {
         // reset-before candidate rows: dW_hn = sum dn (r * h_prev)^T
         g.B = rs + h->r_rh[l] + static_cast<size_t>(d) * TB * H * es; g.ldb = H;
         g.perm[0] = -1; g.perm[1] = -1; g.perm[2] = pos[2]; g.perm[3] = -1;
-        RNN_TRY(run_gemm(h, g, s));
+        RNN_TRY(run_gemm(h, g, s, 4));
       }
       const float* db = reinterpret_cast<const float*>(rs + h->r_db[l]) + static_cast<size_t>(d) * 4 * H;
       RNN_TRY(count(h, launch_bias_grad_scatter(db, H, m_b, 0, dwf + h->off_b[i], s)));
@@ -550,3 +611,34 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// test hook: the internal GEMM on its own (include/rnn_debug.h)
+// ---------------------------------------------------------------------------
+#include "rnn_debug.h"
+
+extern "C" rnn_status_t rnn_debug_gemm(int M, int N, int K, const void* A, int64_t lda, int a_kmajor, const void* B,
+                                       int64_t ldb, int b_kmajor, void* C, int64_t ldc, int c_bf16,
+                                       const float* bias, int beta, int rowmap_H, const int* perm, int in_bf16,
+                                       int use_tc, void* stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C) return RNN_BAD_PARAM;
+  GemmArgs g;
+  g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = lda; g.a_kmajor = a_kmajor;
+  g.B = B; g.ldb = ldb; g.b_kmajor = b_kmajor;
+  g.C = C; g.ldc = ldc; g.c_bf16 = c_bf16;
+  g.bias = bias; g.beta = beta; g.rowmap_H = rowmap_H;
+  for (int k = 0; k < 4; ++k) g.perm[k] = perm ? perm[k] : k;
+  g.in_bf16 = in_bf16;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  static DevArea* dev = nullptr;
+  if (!dev) {
+    if (cudaMalloc(&dev, sizeof(DevArea)) != cudaSuccess) return RNN_CUDA_ERROR;
+    if (cudaMemset(dev, 0, sizeof(DevArea)) != cudaSuccess) return RNN_CUDA_ERROR;
+  }
+  int nsm = 0, d = 0;
+  cudaGetDevice(&d);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, d);
+  int rc = use_tc ? launch_gemm_tc(g, s, nsm, dev, 2000000000ull) : launch_gemm_simt(g, s);
+  return static_cast<rnn_status_t>(rc);
+}

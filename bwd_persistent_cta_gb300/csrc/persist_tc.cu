@@ -45,6 +45,7 @@ constexpr int kThreads = 128;
 constexpr int kSubK = 64;                 // K columns per TMA sub-tile (128 bytes)
 constexpr int kWSub = 128 * kSubK * 2;    // bytes of one 128 x 64 weight sub-tile
 constexpr size_t kSmemCap = 227 * 1024;
+constexpr size_t kOneCtaPerSm = 120 * 1024;
 
 struct TcPersistParams {
   PersistArgs a;
@@ -542,7 +543,9 @@ bool make_plan(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out) {
     p.off_ring = static_cast<uint32_t>(a1k(wbytes));
     p.off_part = p.off_ring + static_cast<uint32_t>(a1k(R * rb));
     p.off_bar = p.off_part + static_cast<uint32_t>(a1k(part));
-    p.smem = smem;
+    // at least half an SM's shared memory: one CTA per SM, so co-resident
+    // CTAs never contend for tensor memory
+    p.smem = smem < kOneCtaPerSm ? kOneCtaPerSm : smem;
     best = p;   // later (larger) KS overwrite earlier ones
   }
   if (best.KS == 0) return false;

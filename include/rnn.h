@@ -175,6 +175,17 @@ int rnn_selected_algo(rnn_handle_t handle);
  * the call ends with RNN_TIMEOUT instead of hanging.  -1 (default) = off. */
 rnn_status_t rnn_debug_skip_arrival(rnn_handle_t handle, int cta);
 
+/* Per-kernel-class timing with CUDA events recorded on the launching stream
+ * around every launch (off by default; costs two event records per launch).
+ * Classes: 0 persistent forward, 1 persistent backward, 2 input-projection
+ * GEMM, 3 input-gradient GEMM, 4 weight-gradient GEMMs, 5 layout / pack
+ * kernels.  rnn_get_timing waits for the recorded events, writes the summed
+ * milliseconds (ms[6]) and launch counts (n[6]) since the last read, and
+ * clears them.  Either output pointer may be NULL. */
+#define RNN_TIMING_CLASSES 6
+rnn_status_t rnn_set_timing(rnn_handle_t handle, int enable);
+rnn_status_t rnn_get_timing(rnn_handle_t handle, double* ms, uint64_t* n);
+
 /* Static text for a status code. */
 const char* rnn_status_string(rnn_status_t status);
 

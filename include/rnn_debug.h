@@ -1,0 +1,33 @@
+/*
+ * rnn_debug.h - test hook of librnn.so: run the library's internal GEMM
+ * directly, so tests can check it element by element in isolation.
+ *
+ * C[row(m), n] = sum_k A(m,k) B(n,k) (+ bias[n]) (+ C if beta != 0)
+ *   A(m,k) = A[m*lda + k] when a_kmajor, else A[k*lda + m] (same for B, n)
+ *   row(m) = m, or with rowmap_H > 0: m = 4u + s -> perm[s]*rowmap_H + u
+ *   (rows with perm[s] < 0 are not written) - the gate-slot remap the weight
+ *   gradients use.
+ * A, B: device, in_bf16 ? bf16 : fp32.  C: device, c_bf16 ? bf16 : fp32.
+ * bias: device fp32 [N] or NULL.  use_tc = 1 runs the tcgen05 kernel (bf16
+ * operands, 16-byte aligned pointers and row strides), 0 the SIMT kernel.
+ * Asynchronous on ``stream``; returns an rnn_status_t.
+ */
+#ifndef GB300_RNN_DEBUG_H
+#define GB300_RNN_DEBUG_H
+
+#include <stdint.h>
+#include "rnn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+rnn_status_t rnn_debug_gemm(int M, int N, int K, const void* A, int64_t lda, int a_kmajor, const void* B,
+                            int64_t ldb, int b_kmajor, void* C, int64_t ldc, int c_bf16, const float* bias,
+                            int beta, int rowmap_H, const int* perm, int in_bf16, int use_tc, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_RNN_DEBUG_H */

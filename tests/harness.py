@@ -1,0 +1,132 @@
+"""Shared test helpers: run a synthetic workload through the C ABI on the GPU
+and through the fp64 oracle, and compare them.
+
+The GPU side goes through ``bwd_persistent_cta_gb300`` (ctypes over
+librnn.so); the oracle side through ``oracle.rnn_oracle``.  Both get the same
+seeded inputs from ``synth``.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+import synth
+
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+def max_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
+    """||gpu - ref||_inf / ||ref||_inf (0 when both vanish)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    den = float(np.max(np.abs(ref))) if ref.size else 0.0
+    num = float(np.max(np.abs(gpu - ref))) if ref.size else 0.0
+    if den == 0.0:
+        return num
+    return num / den
+
+
+def torch_dtype(wl):
+    import torch
+    return torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+
+
+def to_dev(a: Optional[np.ndarray], wl, device="cuda"):
+    import torch
+    if a is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=torch_dtype(wl))
+
+
+def to_np(t) -> Optional[np.ndarray]:
+    if t is None:
+        return None
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: int = 1) -> Dict:
+    """Forward (+ backward data + weights) through the C ABI.  Results are
+    returned seq-major and in canonical gate order (float64)."""
+    import torch
+    import bwd_persistent_cta_gb300 as R
+    from bwd_persistent_cta_gb300 import build as B
+
+    B.build()
+    wl = inp.wl
+    T, Bt, _ = inp.x.shape
+    rnn = R.RNN(wl.mode, wl.input_size, wl.hidden_size, T, Bt, wl.num_layers, wl.bidirectional, wl.reset_after,
+                wl.dtype, wl.gate_order, wl.batch_first, algo)
+    try:
+        w = to_dev(synth.flatten_params(wl, inp.params), wl)
+        xs = synth.to_batch_first(inp.x) if wl.batch_first else inp.x
+        x = to_dev(xs, wl)
+        hx, cx = to_dev(inp.h0, wl), to_dev(inp.c0, wl)
+        out = {}
+        for _ in range(repeat):
+            y, hy, cy = rnn.forward(x, w, hx, cx, train=backward)
+            if backward:
+                dys = synth.to_batch_first(inp.dy) if wl.batch_first else inp.dy
+                dy = to_dev(dys, wl)
+                dx, dhx, dcx = rnn.backward_data(dy, w, to_dev(inp.dhy, wl), to_dev(inp.dcy, wl))
+                dw = rnn.backward_weights(x)
+            rnn.sync()
+        yn = to_np(y)
+        out["y"] = np.swapaxes(yn, 0, 1) if wl.batch_first else yn
+        out["hy"] = to_np(hy)
+        if wl.mode == "lstm":
+            out["cy"] = to_np(cy)
+        if backward:
+            dxn = to_np(dx)
+            out["dx"] = np.swapaxes(dxn, 0, 1) if wl.batch_first else dxn
+            out["dhx"] = to_np(dhx)
+            if wl.mode == "lstm":
+                out["dcx"] = to_np(dcx)
+            out["dparams"] = synth.unflatten_params(wl, dw.cpu().numpy())
+        out["algo"] = rnn.algo
+        out["launches"] = rnn.launches()
+        torch.cuda.synchronize()
+        return out
+    finally:
+        rnn.close()
+
+
+def run_oracle(inp: "synth.Inputs", backward: bool = True) -> Dict:
+    from oracle import rnn_oracle
+    return rnn_oracle.run_inputs(inp, with_backward=backward)
+
+
+def compare(gpu: Dict, ref: Dict, wl, tol: Optional[float] = None, batch_idx: Optional[Sequence[int]] = None,
+            skip: Sequence[str] = ()) -> Dict[str, float]:
+    """Max relative error per output tensor; asserts each is within ``tol``.
+    ``batch_idx`` restricts the GPU's sequence and state outputs to the batch
+    columns the oracle ran."""
+    tol = TOL[wl.dtype] if tol is None else tol
+    errs = {}
+
+    def sel(a, axis):
+        return a if batch_idx is None else np.take(a, list(batch_idx), axis=axis)
+
+    for k in ("y", "dx"):
+        if k in ref and k in gpu and k not in skip:
+            errs[k] = max_rel_err(sel(gpu[k], 1), ref[k])
+    for k in ("hy", "cy", "dhx", "dcx"):
+        if k in ref and k in gpu and k not in skip:
+            errs[k] = max_rel_err(sel(gpu[k], 1), ref[k])
+    if "dparams" in ref and "dparams" in gpu and "dparams" not in skip:
+        for l, per in enumerate(ref["dparams"]):
+            for d, g in enumerate(per):
+                for name, v in g.items():
+                    errs[f"d{name}[{l},{d}]"] = max_rel_err(gpu["dparams"][l][d][name], v)
+    bad = {k: v for k, v in errs.items() if not (v <= tol)}
+    assert not bad, f"max rel err above {tol}: {bad} (all: {errs})"
+    return errs
+
+
+def masked_dy(inp: "synth.Inputs", keep: Sequence[int]) -> "synth.Inputs":
+    """Copy of ``inp`` whose dy is zero outside the batch columns ``keep``."""
+    import dataclasses
+    dy = np.zeros_like(inp.dy)
+    dy[:, list(keep)] = inp.dy[:, list(keep)]
+    return dataclasses.replace(inp, dy=dy)

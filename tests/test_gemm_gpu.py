@@ -1,0 +1,83 @@
+"""The library's internal GEMMs (tcgen05 and SIMT) checked element by element
+against an fp64 CPU product of the same (bf16-exact) inputs, through the
+rnn_debug_gemm hook: K-major and MN-major operands, ragged M / N / K tails,
+bias, accumulate-into-C, bf16 output and the gate-slot row remap."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+def _lib():
+    from bwd_persistent_cta_gb300 import build
+    build.build()
+    import bwd_persistent_cta_gb300 as R
+    return R
+
+
+def _case(M, N, K, a_kmajor, b_kmajor, use_tc, bias=False, beta=False, c_bf16=False, rowmap=None, seed=0):
+    R = _lib()
+    g = torch.Generator().manual_seed(seed)
+    dt = torch.bfloat16 if use_tc else torch.float32
+    Am = torch.randn(M, K, generator=g).to(dt)
+    Bm = torch.randn(N, K, generator=g).to(dt)
+    A_store = Am if a_kmajor else Am.t().contiguous()
+    B_store = Bm if b_kmajor else Bm.t().contiguous()
+    lda = K if a_kmajor else M
+    ldb = K if b_kmajor else N
+    ref = Am.double() @ Bm.double().t()
+    bias_t = torch.randn(N, generator=g) if bias else None
+    if bias:
+        ref = ref + bias_t.double()[None, :]
+    H = M // 4 if rowmap else 0
+    perm = rowmap or [0, 1, 2, 3]
+    out_rows = M
+    C0 = torch.randn(out_rows, N, generator=g)
+    if c_bf16:
+        C0 = C0.bfloat16().float()
+    # expected output rows
+    exp = C0.double().clone()
+    for m in range(M):
+        row = m
+        if rowmap:
+            p = perm[m & 3]
+            if p < 0:
+                continue
+            row = p * H + (m >> 2)
+        exp[row] = ref[m] + (C0.double()[row] if beta else 0.0)
+    Cd = C0.to("cuda", torch.bfloat16 if c_bf16 else torch.float32)
+    rc = R.rnn_debug_gemm(M, N, K, A_store.cuda().data_ptr(), lda, int(a_kmajor), B_store.cuda().data_ptr(), ldb,
+                          int(b_kmajor), Cd.data_ptr(), N, int(c_bf16),
+                          bias_t.cuda().data_ptr() if bias else None, int(beta), H, perm, int(use_tc), int(use_tc),
+                          torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, R.rnn_status_string(rc)
+    torch.cuda.synchronize()
+    got = Cd.double().cpu()
+    scale = float(exp.abs().max())
+    err = float((got - exp).abs().max()) / scale
+    tol = 1e-2 if c_bf16 else (2e-5 if not use_tc else 1e-5)
+    assert err < tol, (err, M, N, K, a_kmajor, b_kmajor, use_tc)
+
+
+@pytest.mark.parametrize("use_tc", [1, 0])
+@pytest.mark.parametrize("a_kmajor,b_kmajor", [(1, 1), (0, 0), (1, 0), (0, 1)])
+def test_gemm_layouts(use_tc, a_kmajor, b_kmajor):
+    _case(256, 384, 192, a_kmajor, b_kmajor, use_tc)
+
+
+@pytest.mark.parametrize("use_tc", [1, 0])
+@pytest.mark.parametrize("M,N,K", [(200, 136, 72), (128, 128, 64), (1000, 264, 520), (8, 16, 8)])
+def test_gemm_ragged(use_tc, M, N, K):
+    _case(M, N, K, 1, 1, use_tc, seed=M + N + K)
+
+
+@pytest.mark.parametrize("use_tc", [1, 0])
+def test_gemm_epilogue_bias_bf16(use_tc):
+    _case(384, 256, 128, 1, 1, use_tc, bias=True, c_bf16=True)
+
+
+@pytest.mark.parametrize("use_tc", [1, 0])
+def test_gemm_epilogue_beta_rowmap(use_tc):
+    _case(512, 200, 1000, 0, 0, use_tc, beta=True, rowmap=[2, 0, -1, 1])
