@@ -45,7 +45,7 @@ constexpr int kThreads = 128;
 constexpr int kSubK = 64;                 // K columns per TMA sub-tile (128 bytes)
 constexpr int kWSub = 128 * kSubK * 2;    // bytes of one 128 x 64 weight sub-tile
 constexpr size_t kSmemCap = 227 * 1024;
-constexpr size_t kOneCtaPerSm = 120 * 1024;
+constexpr size_t kMinSmem = 80 * 1024;
 
 struct TcPersistParams {
   PersistArgs a;
@@ -506,17 +506,17 @@ struct TcPlan {
 
 size_t a1k(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
-// Choose the K split for one direction's launch.  Candidates KS = 1..8
-// (powers of two); the largest split whose grid still fits on the GPU is
-// preferred (shorter per-CTA contraction, less shared memory per CTA).
-bool make_plan(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out) {
-  if (B < 1 || B > 256) return false;
+// Candidate K splits for one launch, preferred first: the largest split
+// whose grid fits (shorter per-CTA contraction, less shared memory per CTA).
+// Whether the clusters can all be resident at once is checked at launch.
+int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int max_out) {
+  if (B < 1 || B > 256) return 0;
   const int K = bwd ? 4 * H : H;
   const int nrg = bwd ? H / 128 : (4 * H) / 128;
-  if (bwd ? (H % 128) : (H % 32)) return false;
+  if (bwd ? (H % 128) : (H % 32)) return 0;
   const int Npad = (B + 15) / 16 * 16;
-  TcPlan best;
-  for (int KS = 1; KS <= 8; KS *= 2) {
+  int n = 0;
+  for (int KS = 8; KS >= 1 && n < max_out; KS /= 2) {
     if (K % (KS * kSubK)) continue;
     const int Kc = K / KS;
     const int nsub = Kc / kSubK;
@@ -543,19 +543,61 @@ bool make_plan(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out) {
     p.off_ring = static_cast<uint32_t>(a1k(wbytes));
     p.off_part = p.off_ring + static_cast<uint32_t>(a1k(R * rb));
     p.off_bar = p.off_part + static_cast<uint32_t>(a1k(part));
-    // at least half an SM's shared memory: one CTA per SM, so co-resident
-    // CTAs never contend for tensor memory
-    p.smem = smem < kOneCtaPerSm ? kOneCtaPerSm : smem;
-    best = p;   // later (larger) KS overwrite earlier ones
+    // at least a third of an SM's shared memory: at most two CTAs per SM, so
+    // their tensor-memory allocations (<= 256 columns each) always fit
+    p.smem = smem < kMinSmem ? kMinSmem : smem;
+    out[n++] = p;
   }
-  if (best.KS == 0) return false;
-  *out = best;
-  return true;
+  return n;
+}
+
+const void* kernel_for(int bwd, int pp) { return bwd ? bwd_fn(pp) : fwd_fn(pp); }
+
+void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPlan& pl, int ndir, cudaStream_t s) {
+  cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = dim3(pl.nrg * pl.KS, ndir, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pl.KS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+}
+
+// First candidate plan whose clusters can all be resident at once.
+bool choose_plan(int bwd, int H, int B, int ndir, int num_sms, TcPlan* chosen) {
+  TcPlan plans[4];
+  const int n = make_plans(bwd, H, B, ndir, num_sms, plans, 4);
+  for (int i = 0; i < n; ++i) {
+    const TcPlan& pl = plans[i];
+    const void* fn = kernel_for(bwd, pl.PP);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_config(cfg, attr, pl, ndir, nullptr);
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (max_clusters >= pl.nrg * ndir) {
+      *chosen = pl;
+      return true;
+    }
+  }
+  return false;
 }
 
 int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   TcPlan pl;
-  if (!make_plan(bwd, a.H, a.B, a.ndir, num_sms, &pl)) return 2;
+  if (!choose_plan(bwd, a.H, a.B, a.ndir, num_sms, &pl)) return 2;
   const int H = a.H, D = a.D;
   CUtensorMap tmW, tmX;
   int rc;
@@ -577,27 +619,10 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   P.nblk_dir = static_cast<unsigned int>(pl.nrg * pl.KS);
   P.tmem_cols = pl.tmem_cols;
   P.off_ring = pl.off_ring; P.off_part = pl.off_part; P.off_bar = pl.off_bar;
-  const void* fn = bwd ? bwd_fn(pl.PP) : fwd_fn(pl.PP);
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) != cudaSuccess)
-    return 3;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.nrg * pl.KS, a.ndir, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = pl.smem;
-  cfg.stream = s;
+  const void* fn = kernel_for(bwd, pl.PP);
+  cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = pl.KS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int max_clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 2;
-  }
-  if (max_clusters < pl.nrg * a.ndir) return 2;
+  fill_config(cfg, attr, pl, a.ndir, s);
   void* params[] = {&tmW, &tmX, &P};
   if (cudaLaunchKernelExC(&cfg, fn, params) != cudaSuccess) return 3;
   return 0;
@@ -608,7 +633,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
 bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms) {
   if (!(mode == 0 || (mode == 1 && reset_after))) return false;
   TcPlan f, b;
-  return make_plan(0, H, B, ndir, num_sms, &f) && make_plan(1, H, B, ndir, num_sms, &b);
+  return choose_plan(0, H, B, ndir, num_sms, &f) && choose_plan(1, H, B, ndir, num_sms, &b);
 }
 
 int launch_persist_fwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms) { return launch(a, 0, s, num_sms); }

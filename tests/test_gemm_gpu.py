@@ -48,9 +48,11 @@ def _case(M, N, K, a_kmajor, b_kmajor, use_tc, bias=False, beta=False, c_bf16=Fa
             row = p * H + (m >> 2)
         exp[row] = ref[m] + (C0.double()[row] if beta else 0.0)
     Cd = C0.to("cuda", torch.bfloat16 if c_bf16 else torch.float32)
-    rc = R.rnn_debug_gemm(M, N, K, A_store.cuda().data_ptr(), lda, int(a_kmajor), B_store.cuda().data_ptr(), ldb,
+    Ad, Bd = A_store.cuda(), B_store.cuda()          # kept alive until the kernel has run
+    biasd = bias_t.cuda() if bias else None
+    rc = R.rnn_debug_gemm(M, N, K, Ad.data_ptr(), lda, int(a_kmajor), Bd.data_ptr(), ldb,
                           int(b_kmajor), Cd.data_ptr(), N, int(c_bf16),
-                          bias_t.cuda().data_ptr() if bias else None, int(beta), H, perm, int(use_tc), int(use_tc),
+                          biasd.data_ptr() if bias else None, int(beta), H, perm, int(use_tc), int(use_tc),
                           torch.cuda.current_stream().cuda_stream)
     assert rc == 0, R.rnn_status_string(rc)
     torch.cuda.synchronize()

@@ -23,13 +23,14 @@ def test_skipped_arrival_times_out_and_context_survives(algo):
     try:
         w = Hn.to_dev(synth.flatten_params(wl, inp.params), wl)
         x = Hn.to_dev(inp.x, wl)
+        hx, cx = Hn.to_dev(inp.h0, wl), Hn.to_dev(inp.c0, wl)
         rnn.set_timeout_ns(200_000_000)
         rnn.debug_skip_arrival(0)
-        rnn.forward(x, w)
+        rnn.forward(x, w, hx, cx)
         rc = R.rnn_sync_status(rnn.handle, torch.cuda.current_stream().cuda_stream)
         assert rc == R.RNN_TIMEOUT, R.rnn_status_string(rc)
         rnn.debug_skip_arrival(-1)
-        y, hy, cy = rnn.forward(x, w)
+        y, hy, cy = rnn.forward(x, w, hx, cx)
         rnn.sync()
         ref = Hn.run_oracle(inp, backward=False)
         assert Hn.max_rel_err(Hn.to_np(y), ref["y"]) <= Hn.TOL["bf16"]
