@@ -55,6 +55,7 @@ _SIGS = {
     "rnn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "rnn_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "rnn_get_timing": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]),
+    "rnn_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(rnn_desc_t)] + [_P] * 7 + [ctypes.c_int, _P]),
     "rnn_debug_gemm": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int64, ctypes.c_int,
                                       _P, ctypes.c_int64, ctypes.c_int, _P, ctypes.c_int64, ctypes.c_int, _P,
                                       ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int,
@@ -122,6 +123,15 @@ def rnn_backward_data(handle, y, dy, dhy, dcy, w, hx, cx, dx, dhx, dcx, workspac
 
 def rnn_backward_weights(handle, x, hx, y, workspace, reserve, dw, stream=None) -> int:
     return lib().rnn_backward_weights(handle, x, hx, y, workspace, reserve, dw, stream)
+
+
+def rnn_forward_noalloc(desc: rnn_desc_t, x, hx, cx, w, y, hy, cy, sync: int = 1, stream=None) -> int:
+    """Inference forward with no device allocation by the library (scratch is
+    a fixed array inside librnn.so); see include/rnn.h."""
+    return lib().rnn_forward_noalloc(ctypes.byref(desc), x, hx, cx, w, y, hy, cy, int(sync), stream)
+
+
+RNN_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def rnn_sync_status(handle, stream=None) -> int:

@@ -27,33 +27,7 @@
 
 using namespace rnn;
 
-struct rnn_handle_s {
-  rnn_desc_t desc;
-  int L, D, T, B, H, I, G;
-  int lstm, ra, rb, bf16, bfirst;
-  int pos[4];          // canonical gate c sits in the caller's block pos[c]
-  int algo;            // RNN_ALGO_PERSIST_TC or RNN_ALGO_PERSIST_SIMT
-  int device, num_sms;
-  size_t es;
-  DevArea* dev;
-  uint64_t timeout_ns;
-  int skip_cta;
-  uint64_t launches;
-  bool trace;
-  bool timing;
-  struct Ev { cudaEvent_t a, b; int cls; };
-  std::vector<Ev> events;      // recorded, not yet read
-  std::vector<Ev> pool;        // created, free
-  // weight offsets (elements), per layer and direction
-  std::vector<size_t> off_ih, off_hh, off_b, off_bh;
-  size_t weight_elems;
-  // reserve offsets (bytes), per layer
-  std::vector<size_t> r_y, r_g, r_c, r_rh, r_dg, r_db;
-  size_t reserve_bytes;
-  // workspace offsets (bytes)
-  size_t w_p, w_xin, w_dyi, w_dx0, w_wx, w_wxt, w_wr, w_wrt, w_bx, w_bh, w_y0, w_y1, w_rh, w_g;
-  size_t workspace_bytes;
-};
+#include "handle.h"
 
 namespace {
 
@@ -252,6 +226,53 @@ rnn_status_t check_desc(const rnn_desc_t* d) {
 }
 
 }  // namespace
+
+namespace rnn {
+
+int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
+  rnn_status_t rs = check_desc(desc);
+  if (rs != RNN_OK) return rs;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RNN_CUDA_ERROR;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return RNN_CUDA_ERROR;
+  if (!(prop.major == 10 && prop.minor == 3)) return RNN_NOT_SUPPORTED;
+  h->desc = *desc;
+  h->L = desc->num_layers; h->D = desc->bidirectional ? 2 : 1;
+  h->T = desc->seq_len; h->B = desc->batch; h->H = desc->hidden_size; h->I = desc->input_size;
+  h->lstm = desc->mode == RNN_LSTM;
+  h->G = h->lstm ? 4 : 3;
+  h->ra = !h->lstm && desc->reset_after;
+  h->rb = !h->lstm && !desc->reset_after;
+  h->bf16 = desc->dtype == RNN_BF16;
+  h->bfirst = desc->batch_first;
+  h->es = h->bf16 ? 2 : 4;
+  bool all_zero = true;
+  for (int k = 0; k < 4; ++k) all_zero = all_zero && desc->gate_order[k] == 0;
+  for (int c = 0; c < 4; ++c) h->pos[c] = c;
+  if (!all_zero)
+    for (int k = 0; k < h->G; ++k) h->pos[desc->gate_order[k]] = k;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  h->timeout_ns = 2000000000ull;
+  h->skip_cta = -1;
+  h->launches = 0;
+  h->trace = false;
+  h->timing = false;
+  h->dev = nullptr;
+  fill_layout(h);
+  const bool tc_ok = h->bf16 && persist_tc_supported(desc->mode, h->ra, h->H, h->B, 1, h->num_sms);
+  PersistArgs probe;
+  probe.mode = desc->mode; probe.reset_after = h->ra; probe.is_bf16 = h->bf16;
+  probe.T = h->T; probe.B = h->B; probe.H = h->H; probe.D = h->D; probe.ndir = 1;
+  const bool simt_ok = plan_persist_simt(probe, h->num_sms, nullptr, nullptr) == 0;
+  if (desc->algo == RNN_ALGO_PERSIST_TC) h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : 0;
+  else if (desc->algo == RNN_ALGO_PERSIST_SIMT) h->algo = simt_ok ? RNN_ALGO_PERSIST_SIMT : 0;
+  else h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : (simt_ok ? RNN_ALGO_PERSIST_SIMT : 0);
+  return h->algo == 0 ? RNN_NOT_SUPPORTED : RNN_OK;
+}
+
+}  // namespace rnn
 
 extern "C" {
 

@@ -1,0 +1,47 @@
+// handle.h - the library handle's host-side state (shared by the C-ABI
+// translation units).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "rnn.h"
+#include "rnn_internal.h"
+
+struct rnn_handle_s {
+  using DevArea = rnn::DevArea;
+  rnn_desc_t desc;
+  int L, D, T, B, H, I, G;
+  int lstm, ra, rb, bf16, bfirst;
+  int pos[4];          // canonical gate c sits in the caller's block pos[c]
+  int algo;            // RNN_ALGO_PERSIST_TC or RNN_ALGO_PERSIST_SIMT
+  int device, num_sms;
+  size_t es;
+  DevArea* dev;
+  uint64_t timeout_ns;
+  int skip_cta;
+  uint64_t launches;
+  bool trace;
+  bool timing;
+  struct Ev { cudaEvent_t a, b; int cls; };
+  std::vector<Ev> events;      // recorded, not yet read
+  std::vector<Ev> pool;        // created, free
+  // weight offsets (elements), per layer and direction
+  std::vector<size_t> off_ih, off_hh, off_b, off_bh;
+  size_t weight_elems;
+  // reserve offsets (bytes), per layer
+  std::vector<size_t> r_y, r_g, r_c, r_rh, r_dg, r_db;
+  size_t reserve_bytes;
+  // workspace offsets (bytes)
+  size_t w_p, w_xin, w_dyi, w_dx0, w_wx, w_wxt, w_wr, w_wrt, w_bx, w_bh, w_y0, w_y1, w_rh, w_g;
+  size_t workspace_bytes;
+};
+
+
+namespace rnn {
+// Host-side initialisation of a handle for ``desc`` on the current device
+// (validation, layout, kernel choice); allocates no device memory and leaves
+// h->dev unset.  Returns an rnn_status_t.
+int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc);
+}  // namespace rnn

@@ -186,6 +186,32 @@ rnn_status_t rnn_debug_skip_arrival(rnn_handle_t handle, int cta);
 rnn_status_t rnn_set_timing(rnn_handle_t handle, int enable);
 rnn_status_t rnn_get_timing(rnn_handle_t handle, double* ms, uint64_t* n);
 
+/* Inference forward that allocates nothing on the device.
+ *
+ * The paper has no counterpart; this entry point exists for callers that
+ * cannot let a library call cudaMalloc - a process whose device memory is all
+ * pre-reserved by its own allocator or a framework's caching pool, or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device
+ * synchronisation.  It computes what rnn_forward computes with reserve == NULL
+ * (same kernels, same results) but takes no handle and no workspace: its
+ * scratch is a fixed array of RNN_NOALLOC_SCRATCH_BYTES built into the library,
+ * which every GPU that loads the library holds until the process exits.
+ *   desc                  as for rnn_create
+ *   x, hx, cx, w, y, hy, cy  as for rnn_forward (caller-owned device memory)
+ *   sync                  nonzero: synchronise ``stream`` and return the
+ *                         device status (RNN_TIMEOUT when a spin-wait gave up);
+ *                         zero: return once the work is queued
+ * Returns RNN_NOT_SUPPORTED when the problem's workspace plus 256 bytes of
+ * counters exceeds RNN_NOALLOC_SCRATCH_BYTES (nothing is launched then).
+ * The first call on each device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls share the array, which keeps the last call's contents:
+ * the counters and status are cleared by each call; calls that overlap on the
+ * GPU race on the array and must be serialised by the caller. */
+#define RNN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+rnn_status_t rnn_forward_noalloc(const rnn_desc_t* desc, const void* x, const void* hx, const void* cx,
+                                 const void* w, void* y, void* hy, void* cy, int sync, void* stream);
+
 /* Static text for a status code. */
 const char* rnn_status_string(rnn_status_t status);
 
