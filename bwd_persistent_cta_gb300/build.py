@@ -30,17 +30,17 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _flags(verbose_ptxas: bool = False):
-    f = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
+def _flags(verbose_ptxas: bool = False, extra=()):
+    f = list(extra) + ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
                 "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include"), "-I", CSRC]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]
     return f
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, src + ".o")
-    cmd = [nvcc()] + _flags(verbose_ptxas) + ["-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, build_dir: str = BUILD, extra=()) -> str:
+    obj = os.path.join(build_dir, src + ".o")
+    cmd = [nvcc()] + _flags(verbose_ptxas, extra) + ["-c", os.path.join(CSRC, src), "-o", obj]
     if src.endswith(".cpp"):
         cmd = [nvcc(), "-x", "cu"] + cmd[1:]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -51,23 +51,27 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile (if any source is newer than the library) and return its path."""
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "rnn.h")]
-    if not force and os.path.exists(LIB):
-        lib_t = os.path.getmtime(LIB)
+def build(force: bool = False, verbose_ptxas: bool = False, extra_flags=(), lib_path: str = LIB,
+          build_dir: str = BUILD) -> str:
+    """Compile (if any source is newer than the library) and return its path.
+    ``extra_flags`` / ``lib_path`` / ``build_dir`` build a variant elsewhere
+    (e.g. with -D switches for latency studies) without touching the default."""
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [
+        os.path.join(ROOT, "include", h) for h in os.listdir(os.path.join(ROOT, "include"))]
+    if not force and os.path.exists(lib_path):
+        lib_t = os.path.getmtime(lib_path)
         if all(os.path.getmtime(d) <= lib_t for d in deps):
-            return LIB
-    os.makedirs(BUILD, exist_ok=True)
+            return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, build_dir, extra_flags), SOURCES))
+    tmp = lib_path + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -8,99 +8,132 @@
 //   backward  dh^T[H, B]  = W_hh^T[H, 4H] . dG^T_{t+1}[4H, B]
 // A cluster of KS CTAs owns one 128-row block of the weight operand; CTA rank
 // ks owns the K slice [ks*K/KS, (ks+1)*K/KS) and keeps that 128 x K/KS bf16
-// tile resident in shared memory (loaded once by TMA) for the whole sequence.
+// tile resident in shared memory (loaded once by TMA) for the whole sequence,
+// and owns the 128/KS rows [ks*128/KS, (ks+1)*128/KS) of the result.
+//
 // Each step a CTA
-//   1. waits (bounded) on its direction's gpu-scope step counter until every
-//      CTA of the direction finished the previous step (acquire);
+//   1. waits (bounded) until every CTA of its direction finished the previous
+//      step: one gpu-scope counter per direction, release add / acquire poll;
 //   2. streams its K slice of the previous state (h_{t-1} rows of the layer
 //      output, or the gate gradients of the step after) with TMA through a
 //      ring of 64-column sub-tiles, issuing tcgen05.mma (M=128, N=B rounded up
 //      to 16, K=16) into a TMEM accumulator as sub-tiles land;
-//   3. moves the accumulator to shared memory (tcgen05.ld), and after a
-//      cluster barrier sums the KS partial tiles of its own units over
-//      distributed shared memory;
-//   4. applies the cell (forward) or its derivative (backward) in registers -
-//      the LSTM cell state, the GRU state and the backward carries never leave
-//      registers - and writes its units' outputs;
-//   5. arrives on the counter (release).
-// Cluster-uniform abort: a CTA whose wait ran out publishes a flag in shared
-// memory before the cluster barrier; every CTA reads all flags of its cluster
-// after it, so all of them leave together (after one more cluster barrier, so
-// no CTA exits while a peer may still read its shared memory).
+//   3. pushes each accumulator row (tcgen05.ld) straight into the shared
+//      memory of the cluster peer that owns that row (posted distributed
+//      shared-memory stores), together with its abort flag;
+//   4. after one cluster barrier sums the KS partial rows of its own units
+//      from local shared memory, applies the cell (forward) or its derivative
+//      (backward) in registers - the LSTM cell state, the GRU state and the
+//      backward carries never leave registers - stores the exchanged values,
+//      arrives on the counter, and only then stores what no CTA of this
+//      launch waits for.
+// Cluster-uniform abort: every CTA reads the same set of flags after the same
+// barrier, so all CTAs of a cluster leave at the same step (after one more
+// cluster barrier, so no CTA exits while a peer may still touch its shared
+// memory).
 //
 // This is the persistent-RNN design of the persistent backward-data kernel
 // fragment (one launch for all steps, weights resident on chip, a per-step
 // exchange between CTAs through global memory) carried to tensor cores, TMA,
-// TMEM and thread-block clusters; flag counters with acquire/release replace
-// its -0.0 sentinel polling.  Cell math: Lstm.cpp
-// lstmCellForwardPassCalcUnits / backwardStepImpl; Gru.cpp
-// gruCellForwardPassCalcUnitsResetAfter / backwardStepImplResetAfter.
+// TMEM and thread-block clusters; the fragment polls its dgates buffer for a
+// -0.0 sentinel where a release/acquire counter is used here.  Cell math:
+// Lstm.cpp lstmCellForwardPassCalcUnits / backwardStepImpl; Gru.cpp
+// gruCellForwardPassCalcUnitsResetAfter / backwardStepImplResetAfter.  The
+// sigmoid and tanh of this bf16 path use the hardware tanh.approx.f32
+// instruction (sigma(x) = 1/2 + tanh(x/2)/2); its relative error (about 2^-11)
+// is below the bf16 storage rounding of the stored states.
+#include <cstdlib>
+
 #include "common.cuh"
 
 namespace rnn {
 
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kSubK = 64;                 // K columns per TMA sub-tile (128 bytes)
+#ifdef RNN_STEP_TRACE
+// Step-phase timestamps (globaltimer, ns) of two CTAs, for latency studies;
+// compiled only with -DRNN_STEP_TRACE.
+__device__ unsigned long long g_step_trace[2][2][1100][16];
+#define RNN_TRACE_AT(slot_, kind_, step_)                                                        \
+  do {                                                                                          \
+    if (threadIdx.x == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1) && blockIdx.y == 0 && \
+        (step_) < 1100)                                                                          \
+      g_step_trace[(kind_)][blockIdx.x == 0 ? 0 : 1][(step_)][(slot_)] = globaltimer_ns();       \
+  } while (0)
+#else
+#define RNN_TRACE_AT(slot_, kind_, step_) do { } while (0)
+#endif
+
+constexpr int kThreads = 256;             // warps 0-3 read TMEM; all 8 run the cell epilogue
+constexpr int kSubK = 64;                 // K columns per 128-byte swizzled sub-tile
 constexpr int kWSub = 128 * kSubK * 2;    // bytes of one 128 x 64 weight sub-tile
+constexpr int kMaxKS = 16;
+constexpr int kMaxRing = 16;
 constexpr size_t kSmemCap = 227 * 1024;
-constexpr size_t kMinSmem = 80 * 1024;
+constexpr size_t kMinSmem = 80 * 1024;    // at most two CTAs per SM: TMEM (<= 256 cols each) fits
 
 struct TcPersistParams {
   PersistArgs a;
-  int KS, Kc, nsub, R, Npad, UPC;
+  int KS, Kc, nsub, R, Npad, UPC, RPC;
   unsigned int nblk_dir;   // CTAs per direction
   uint32_t tmem_cols;
-  uint32_t off_ring, off_part, off_bar;
+  uint32_t off_ring, off_recv, off_bar;
 };
 
 struct TcBars {
-  uint64_t wbar;
-  uint64_t mma;
-  uint64_t full[16];
-  uint64_t empty[16];
-  int abort_flag[2];
+  uint64_t wbar;                 // resident weight tile landed (TMA)
+  uint64_t mma;                  // this step's MMAs finished (tcgen05.commit)
+  uint64_t full[kMaxRing];       // exchange sub-tile landed (TMA)
+  uint64_t empty[kMaxRing];      // exchange sub-tile consumed (tcgen05.commit)
+  int flags[2][kMaxKS];          // abort flags pushed by the peers, by step parity
   uint32_t tmem;
 };
 
-__device__ __forceinline__ size_t align1k(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigm_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
+
+// Generic address of ``p`` (a shared-memory location) in CTA ``rank`` of the
+// cluster; plain loads and stores through it reach distributed shared memory.
+template <typename T>
+__device__ __forceinline__ T* peer_ptr(T* p, int rank) {
+  uint64_t g;
+  asm("mapa.u64 %0, %1, %2;" : "=l"(g) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<T*>(g);
+}
 
 // One step's contraction: stream nsub sub-tiles of the exchange operand
 // through the ring and accumulate into TMEM.  Called by thread 0 only.
 // g: running sub-tile load counter (across steps).  Returns false on timeout.
-__device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, uint8_t* wsm, uint8_t* ring,
-                              TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0, uint32_t idesc,
-                              uint32_t step_parity, bool first_use_w) {
+__device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, uint8_t* ring, TcBars& bars,
+                              uint32_t tmem, uint32_t& g, int x0, int y0, uint32_t idesc, uint64_t adesc0,
+                              bool first_use_w) {
   const int nsub = P.nsub, R = P.R;
   const uint32_t rbytes = static_cast<uint32_t>(P.Npad) * 128;
   const uint64_t to = P.a.timeout_ns;
   const uint32_t g0 = g;
-  // prologue: first min(R, nsub) loads
   for (int j = 0; j < nsub && j < R; ++j) {
     const uint32_t gg = g0 + j;
     const int slot = gg % R;
-    if (gg >= static_cast<uint32_t>(R)) {
-      if (!mbar_wait(&bars.empty[slot], ((gg / R) - 1) & 1, to)) return false;
-    }
+    if (gg >= static_cast<uint32_t>(R) && !mbar_wait(&bars.empty[slot], ((gg / R) - 1) & 1, to)) return false;
     mbar_arrive_expect_tx(&bars.full[slot], rbytes);
     tma_load_2d(ring + slot * rbytes, tmX, &bars.full[slot], x0 + j * kSubK, y0);
   }
-  if (first_use_w) {
-    if (!mbar_wait(&bars.wbar, 0, to)) return false;
-  }
+  if (first_use_w && !mbar_wait(&bars.wbar, 0, to)) return false;
+  const uint64_t bdesc0 = sdesc_sw128(smem_u32(ring), 16, 1024);
   for (int j = 0; j < nsub; ++j) {
     const uint32_t gg = g0 + j;
     const int slot = gg % R;
     if (!mbar_wait(&bars.full[slot], (gg / R) & 1, to)) return false;
     tc_fence_after();
-    const uint32_t abase = smem_u32(wsm + j * kWSub);
-    const uint32_t bbase = smem_u32(ring + slot * rbytes);
+    const uint64_t ad = adesc0 + static_cast<uint64_t>((j * kWSub) >> 4);
+    const uint64_t bd = bdesc0 + static_cast<uint64_t>((slot * rbytes) >> 4);
 #pragma unroll
-    for (int k = 0; k < kSubK / 16; ++k) {
-      mma_bf16_ss(tmem, sdesc_sw128(abase + k * 32, 16, 1024), sdesc_sw128(bbase + k * 32, 16, 1024), idesc,
-                  (j > 0 || k > 0) ? 1u : 0u);
-    }
+    for (int k = 0; k < kSubK / 16; ++k)   // +32 bytes per K=16 step inside the swizzle atom
+      mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
     mma_commit(&bars.empty[slot]);
     const int jn = j + R;
     if (jn < nsub) {
@@ -112,111 +145,108 @@ __device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, 
   }
   mma_commit(&bars.mma);
   g = g0 + nsub;
-  (void)step_parity;
   return true;
 }
 
-// TMEM accumulator (128 lanes x Npad columns) -> part[b][row] (fp32).
-__device__ __forceinline__ void tmem_to_part(uint32_t tmem, float* part, int Npad) {
+// TMEM accumulator rows -> the owning peer's receive buffer
+// recv[src = this rank][column][row within the owner], by warps 0-3
+// (warp w may only address TMEM lanes 32w .. 32w+31).
+__device__ __forceinline__ void push_partials(const TcPersistParams& P, uint32_t tmem, float* recv, int ks) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp >= 4) return;
   const int row = warp * 32 + lane;
-  for (int c = 0; c < Npad; c += 32) {
+  const int owner = row / P.RPC, lr = row - owner * P.RPC;
+  float* dst = peer_ptr(recv, owner) + static_cast<size_t>(ks) * P.Npad * P.RPC + lr;
+  for (int c = 0; c < P.Npad; c += 32) {
     float v[32];
     tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (c + j < Npad) part[(c + j) * 128 + row] = v[j];
+      if (c + j < P.Npad) dst[(c + j) * P.RPC] = v[j];
   }
 }
 
-// Common per-step front half: wait, contract, stage partials, agree on abort.
-// Returns true when the whole cluster may continue.
-__device__ bool step_front(const TcPersistParams& P, const CUtensorMap* tmX, uint8_t* wsm, uint8_t* ring,
-                           float* part, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0,
-                           uint32_t idesc, bool do_contract, unsigned int wait_target, int s, int& n_mma,
-                           bool& w_waited, unsigned int kernel) {
+// The per-step exchange and contraction, up to the point where this CTA's
+// units' summed pre-activations can be read from ``recv``.  Returns true when
+// the whole cluster may continue.
+__device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, uint8_t* ring, float* recv,
+                              TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0, uint32_t idesc,
+                              uint64_t adesc0, bool do_contract, unsigned int wait_target, int s, int ks, int& n_mma,
+                              bool& w_waited, unsigned int kernel) {
   const PersistArgs& a = P.a;
-  const int dir = a.dir0 + blockIdx.y;
-  unsigned int* ctr = &a.dev->counters[dir];
+  const int tk = kernel == K_BWD_TC ? 1 : 0;
+  (void)tk;
   int ok = 1;
   if (threadIdx.x == 0) {
-    if (wait_target > 0 && !wait_counter_geq(ctr, wait_target, a.timeout_ns)) {
+    if (wait_target > 0 && !wait_counter_geq(&a.dev->counters[a.dir0 + blockIdx.y], wait_target, a.timeout_ns)) {
       ok = 0;
       report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_COUNTER);
     }
+    RNN_TRACE_AT(7, tk, s);
     if (ok && do_contract) {
       fence_proxy_async_global();
-      if (!contract_step(P, tmX, wsm, ring, bars, tmem, g, x0, y0, idesc, 0, !w_waited)) {
+      if (!contract_step(P, tmX, ring, bars, tmem, g, x0, y0, idesc, adesc0, !w_waited)) {
         ok = 0;
         report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_TMA);
       }
       w_waited = true;
     }
+    RNN_TRACE_AT(2, tk, s);
   }
   ok = __syncthreads_and(ok);
   if (ok && do_contract) {
     const bool done = mbar_wait(&bars.mma, n_mma & 1, a.timeout_ns);
     ++n_mma;
     if (!done) report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_MMA);
+    RNN_TRACE_AT(3, tk, s);
     ok = __syncthreads_and(done ? 1 : 0);
     if (ok) {
       tc_fence_after();
-      tmem_to_part(tmem, part, P.Npad);
+      push_partials(P, tmem, recv, ks);
     }
   }
-  if (threadIdx.x == 0) bars.abort_flag[s & 1] = ok ? 0 : 1;
+  RNN_TRACE_AT(9, tk, s);
+  if (static_cast<int>(threadIdx.x) < P.KS) *peer_ptr(&bars.flags[s & 1][ks], threadIdx.x) = ok ? 0 : 1;
   tc_fence_before();
   if (P.KS > 1) cluster_sync(); else __syncthreads();
   tc_fence_after();
+  RNN_TRACE_AT(10, tk, s);
   int any = 0;
-  if (P.KS > 1) {
-    const uint32_t fa = smem_u32(&bars.abort_flag[s & 1]);
-    for (int r = 0; r < P.KS; ++r) any |= static_cast<int>(ld_shared_cluster_u32(mapa_shared(fa, r)));
-  } else {
-    any = bars.abort_flag[s & 1];
-  }
+#pragma unroll
+  for (int r = 0; r < kMaxKS; ++r)
+    if (r < P.KS) any |= bars.flags[s & 1][r];
+  RNN_TRACE_AT(4, tk, s);
   return any == 0;
 }
 
-__device__ __forceinline__ void step_arrive(const PersistArgs& a, bool skip) {
-  fence_proxy_async_global();
+// After the exchange-critical stores of a step: every thread's stores are
+// ordered before the release add by the barrier.
+__device__ __forceinline__ void step_arrive(const PersistArgs& a, bool skip, int s, int tk) {
+  (void)s; (void)tk;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (!skip) red_release_gpu_add(&a.dev->counters[a.dir0 + blockIdx.y], 1u);
-  }
+  RNN_TRACE_AT(11, tk, s);
+  if (threadIdx.x == 0 && !skip) red_release_gpu_add(&a.dev->counters[a.dir0 + blockIdx.y], 1u);
 }
 
-__device__ __forceinline__ float4 sum_partials(const TcPersistParams& P, const float* part, int b, int row4) {
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float* p = part + b * 128 + row4;
-  if (P.KS == 1) return *reinterpret_cast<const float4*>(p);
-  const uint32_t addr = smem_u32(p);
-  for (int r = 0; r < P.KS; ++r) {
-    const float4 v = ld_shared_cluster_v4(mapa_shared(addr, r));
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-  }
-  return acc;
+__device__ __forceinline__ uint2 ld_u2(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
+
+__device__ __forceinline__ void unpack4(uint2 q, float (&v)[4]) {
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&q.x);
+  __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&q.y);
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
 }
 
-__device__ __forceinline__ float sum_partial1(const TcPersistParams& P, const float* part, int b, int row) {
-  const float* p = part + b * 128 + row;
-  if (P.KS == 1) return *p;
-  const uint32_t addr = smem_u32(p);
-  float acc = 0.f;
-  for (int r = 0; r < P.KS; ++r) acc += ld_shared_cluster_f32(mapa_shared(addr, r));
-  return acc;
-}
-
-__device__ __forceinline__ void setup(const TcPersistParams& P, const CUtensorMap* tmW, uint8_t* wsm, TcBars& bars,
-                                      int wx0, int wy0) {
+__device__ __forceinline__ void setup(const TcPersistParams& P, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                      uint8_t* wsm, TcBars& bars, int wx0, int wy0) {
   if (threadIdx.x == 0) {
     mbar_init(&bars.wbar, 1);
     mbar_init(&bars.mma, 1);
     for (int i = 0; i < P.R; ++i) { mbar_init(&bars.full[i], 1); mbar_init(&bars.empty[i], 1); }
-    bars.abort_flag[0] = bars.abort_flag[1] = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
+    prefetch_tmap(tmW);
+    prefetch_tmap(tmX);
     mbar_arrive_expect_tx(&bars.wbar, static_cast<uint32_t>(P.nsub) * kWSub);
     for (int j = 0; j < P.nsub; ++j) tma_load_2d(wsm + j * kWSub, tmW, &bars.wbar, wx0 + j * kSubK, wy0);
   }
@@ -236,6 +266,15 @@ __device__ __forceinline__ void teardown(const TcPersistParams& P, TcBars& bars)
   if ((threadIdx.x >> 5) == 0) tmem_dealloc(bars.tmem, P.tmem_cols);
 }
 
+#define RNN_TC_SMEM_VIEW                                                                              \
+  extern __shared__ __align__(1024) uint8_t smem_raw[];                                              \
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &         \
+                                             ~static_cast<uintptr_t>(1023));                          \
+  uint8_t* wsm = base;                                                                                \
+  uint8_t* ring = base + P.off_ring;                                                                  \
+  float* recv = reinterpret_cast<float*>(base + P.off_recv);                                          \
+  TcBars& bars = *reinterpret_cast<TcBars*>(base + P.off_bar)
+
 // ---------------------------------------------------------------------------
 // forward
 // ---------------------------------------------------------------------------
@@ -243,13 +282,7 @@ template <int PP>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ TcPersistParams P) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* wsm = base;
-  uint8_t* ring = base + P.off_ring;
-  float* part = reinterpret_cast<float*>(base + P.off_part);
-  TcBars& bars = *reinterpret_cast<TcBars*>(base + P.off_bar);
+  RNN_TC_SMEM_VIEW;
   const PersistArgs& a = P.a;
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
   const int dir = a.dir0 + blockIdx.y;
@@ -257,9 +290,10 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int rg = static_cast<int>(blockIdx.x) / P.KS;
   const bool lstm = a.mode == 0;
 
-  setup(P, &tmW, wsm, bars, ks * P.Kc, dir * 4 * H + rg * 128);
+  setup(P, &tmW, &tmX, wsm, bars, ks * P.Kc, dir * 4 * H + rg * 128);
   const uint32_t tmem = bars.tmem;
   const uint32_t idesc = idesc_bf16(128, P.Npad, false, false);
+  const uint64_t adesc0 = sdesc_sw128(smem_u32(wsm), 16, 1024);
 
   __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.Y);
   const __nv_bfloat16* Pm = static_cast<const __nv_bfloat16*>(a.P);
@@ -270,11 +304,14 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int npairs = UPC * B;
   const int ubase = rg * 32 + ks * UPC;     // first hidden unit of this CTA's epilogue
   const int slot_h0 = dir ? TT + 1 : 0;
+  const int src_stride = P.Npad * P.RPC;    // floats per source rank in recv
 
   float st[PP];
+  float bh[PP][3];
 #pragma unroll
   for (int p = 0; p < PP; ++p) {
     st[p] = 0.f;
+    bh[p][0] = bh[p][1] = bh[p][2] = 0.f;
     const int id = threadIdx.x + p * kThreads;
     if (id >= npairs) continue;
     const int ul = id % UPC, b = id / UPC, u = ubase + ul;
@@ -284,6 +321,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? TT : 0)) * B + b) * H + u] = st[p];
     } else {
       st[p] = __bfloat162float(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
+      const float* bb = a.bh + dir * 4 * H + 4 * u;
+      bh[p][0] = bb[0]; bh[p][1] = bb[1]; bh[p][2] = bb[2];
     }
   }
 
@@ -295,46 +334,77 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     const int t = dir ? TT - 1 - s : s;
     const int sp = dir ? t + 2 : t;
     const int so = t + 1;
-    const bool ok = step_front(P, &tmX, wsm, ring, part, bars, tmem, g, dir * H + ks * P.Kc, sp * B, idesc, true,
-                               static_cast<unsigned int>(s) * P.nblk_dir, s, n_mma, w_waited, K_FWD_TC);
-    if (!ok) break;
+    RNN_TRACE_AT(0, 0, s);
+    // this step's input projections do not depend on the exchange: load them first
+    uint2 pq[PP];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      pq[p] = id < npairs ? ld_u2(Pm + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u) : make_uint2(0, 0);
+    }
+    if (!step_exchange(P, &tmX, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B, idesc, adesc0, true,
+                       static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_FWD_TC))
+      break;
+    float hv[PP];
+    float gq[PP][4];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      hv[p] = 0.f;
+      if (id >= npairs) break;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float* rp = recv + b * P.RPC + 4 * ul;
+#pragma unroll
+      for (int r = 0; r < kMaxKS; ++r) {
+        if (r < P.KS) {
+          const float4 v = *reinterpret_cast<const float4*>(rp + r * src_stride);
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+      }
+      float pv[4];
+      unpack4(pq[p], pv);
+      float h;
+      if (lstm) {
+        const float i = sigm_fast(pv[0] + acc.x);
+        const float f = sigm_fast(pv[1] + acc.y);
+        const float gg = tanh_fast(pv[2] + acc.z);
+        const float o = sigm_fast(pv[3] + acc.w);
+        const float c = f * st[p] + i * gg;
+        h = o * tanh_fast(c);
+        st[p] = c;
+        pv[0] = i; pv[1] = f; pv[2] = gg; pv[3] = o;
+      } else {
+        const float r = sigm_fast(pv[0] + acc.x + bh[p][0]);
+        const float z = sigm_fast(pv[1] + acc.y + bh[p][1]);
+        const float hn = acc.z + bh[p][2];
+        const float n = tanh_fast(pv[2] + r * hn);
+        h = (1.f - z) * n + z * st[p];
+        st[p] = h;
+        pv[0] = r; pv[1] = z; pv[2] = n; pv[3] = hn;
+      }
+      hv[p] = h;
+      gq[p][0] = pv[0]; gq[p][1] = pv[1]; gq[p][2] = pv[2]; gq[p][3] = pv[3];
+      Y[(static_cast<int64_t>(so) * B + b) * ldY + dir * H + u] = __float2bfloat16_rn(h);
+    }
+    RNN_TRACE_AT(5, 0, s);
+    step_arrive(a, skip, s, 0);
+    RNN_TRACE_AT(6, 0, s);
+    // stores nothing in this launch waits for
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
       if (id >= npairs) break;
       const int ul = id % UPC, b = id / UPC, u = ubase + ul;
-      const float4 acc = sum_partials(P, part, b, 4 * (u - rg * 32));
-      float pv[4];
-      Vec4<__nv_bfloat16>::load(Pm + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u, pv);
-      float gv[4], h;
-      if (lstm) {
-        const float i = sigm(pv[0] + acc.x);
-        const float f = sigm(pv[1] + acc.y);
-        const float gg = tanhf(pv[2] + acc.z);
-        const float o = sigm(pv[3] + acc.w);
-        const float c = f * st[p] + i * gg;
-        h = o * tanhf(c);
-        st[p] = c;
-        gv[0] = i; gv[1] = f; gv[2] = gg; gv[3] = o;
-        if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = c;
-        if (s == TT - 1 && a.cy)
-          static_cast<__nv_bfloat16*>(a.cy)[(static_cast<int64_t>(dir) * B + b) * H + u] = __float2bfloat16_rn(c);
-      } else {
-        const float* bh = a.bh + dir * 4 * H + 4 * u;
-        const float r = sigm(pv[0] + acc.x + bh[0]);
-        const float z = sigm(pv[1] + acc.y + bh[1]);
-        const float hn = acc.z + bh[2];
-        const float n = tanhf(pv[2] + r * hn);
-        h = (1.f - z) * n + z * st[p];
-        st[p] = h;
-        gv[0] = r; gv[1] = z; gv[2] = n; gv[3] = hn;
+      if (G) Vec4<__nv_bfloat16>::store(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * 4 * H + 4 * u, gq[p]);
+      if (lstm && a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = st[p];
+      if (s == TT - 1) {
+        const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
+        if (a.hy) static_cast<__nv_bfloat16*>(a.hy)[o] = __float2bfloat16_rn(hv[p]);
+        if (lstm && a.cy) static_cast<__nv_bfloat16*>(a.cy)[o] = __float2bfloat16_rn(st[p]);
       }
-      Y[(static_cast<int64_t>(so) * B + b) * ldY + dir * H + u] = __float2bfloat16_rn(h);
-      if (G) Vec4<__nv_bfloat16>::store(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * 4 * H + 4 * u, gv);
-      if (s == TT - 1 && a.hy)
-        static_cast<__nv_bfloat16*>(a.hy)[(static_cast<int64_t>(dir) * B + b) * H + u] = __float2bfloat16_rn(h);
     }
-    step_arrive(a, skip);
   }
   teardown(P, bars);
 }
@@ -346,13 +416,7 @@ template <int PP>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ TcPersistParams P) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* wsm = base;
-  uint8_t* ring = base + P.off_ring;
-  float* part = reinterpret_cast<float*>(base + P.off_part);
-  TcBars& bars = *reinterpret_cast<TcBars*>(base + P.off_bar);
+  RNN_TC_SMEM_VIEW;
   const PersistArgs& a = P.a;
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
   const int K4 = 4 * H;
@@ -361,18 +425,21 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int rg = static_cast<int>(blockIdx.x) / P.KS;
   const bool lstm = a.mode == 0;
 
-  setup(P, &tmW, wsm, bars, ks * P.Kc, dir * H + rg * 128);
+  setup(P, &tmW, &tmX, wsm, bars, ks * P.Kc, dir * H + rg * 128);
   const uint32_t tmem = bars.tmem;
   const uint32_t idesc = idesc_bf16(128, P.Npad, false, false);
+  const uint64_t adesc0 = sdesc_sw128(smem_u32(wsm), 16, 1024);
 
   const __nv_bfloat16* Y = static_cast<const __nv_bfloat16*>(a.Y);
   const __nv_bfloat16* G = static_cast<const __nv_bfloat16*>(a.gates);
   __nv_bfloat16* dG = static_cast<__nv_bfloat16*>(a.dG);
+  const float* Cb = a.C ? a.C + static_cast<int64_t>(dir) * (TT + 1) * B * H : nullptr;
   const int64_t ldY = static_cast<int64_t>(D) * H;
   const int64_t ldG = static_cast<int64_t>(D) * K4;
   const int UPC = P.UPC;
   const int npairs = UPC * B;
   const int ubase = rg * 128 + ks * UPC;
+  const int src_stride = P.Npad * P.RPC;
 
   float carry[PP], db[PP][4];
 #pragma unroll
@@ -393,23 +460,48 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   bool aborted = false;
   for (int s = 0; s <= TT; ++s) {
     const int tp = dir ? s - 1 : TT - s;     // step processed just before (s >= 1)
-    const bool ok = step_front(P, &tmX, wsm, ring, part, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B,
-                               idesc, s > 0, static_cast<unsigned int>(s) * P.nblk_dir, s, n_mma, w_waited,
-                               K_BWD_TC);
-    if (!ok) { aborted = true; break; }
     const int t = dir ? s : TT - 1 - s;
     const int sp = dir ? t + 2 : t;
+    RNN_TRACE_AT(0, 1, s);
+    // this step's saved forward values and upstream gradient: load before the exchange
+    uint2 gq[PP];
+    float e0[PP], e1[PP], dyv[PP];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      gq[p] = make_uint2(0, 0);
+      e0[p] = e1[p] = dyv[p] = 0.f;
+      if (id < npairs && s < TT) {
+        gq[p] = ld_u2(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * K4 + 4 * u);
+        dyv[p] = a.dYi[(static_cast<int64_t>(t) * B + b) * ldY + dir * H + u];
+        if (lstm) {
+          e0[p] = Cb[(static_cast<int64_t>(dir ? t : t + 1) * B + b) * H + u];
+          e1[p] = Cb[(static_cast<int64_t>(dir ? t + 1 : t) * B + b) * H + u];
+        } else {
+          e0[p] = __bfloat162float(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
+        }
+      }
+    }
+    if (!step_exchange(P, &tmX, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B, idesc,
+                       adesc0, s > 0, static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_BWD_TC)) {
+      aborted = true;
+      break;
+    }
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
       if (id >= npairs) break;
       const int ul = id % UPC, b = id / UPC, u = ubase + ul;
-      float dhr;
+      float dhr = 0.f;
       if (s == 0) {
-        dhr = a.dhT ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.dhT)[(static_cast<int64_t>(dir) * B + b) * H + u])
-                    : 0.f;
+        if (a.dhT)
+          dhr = __bfloat162float(static_cast<const __nv_bfloat16*>(a.dhT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
       } else {
-        dhr = sum_partial1(P, part, b, u - rg * 128);
+        const float* rp = recv + b * P.RPC + ul;
+#pragma unroll
+        for (int r = 0; r < kMaxKS; ++r)
+          if (r < P.KS) dhr += rp[r * src_stride];
       }
       if (s == TT) {
         const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
@@ -418,16 +510,13 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         continue;
       }
       float gv[4];
-      Vec4<__nv_bfloat16>::load(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * K4 + 4 * u, gv);
-      const float dy = a.dYi[(static_cast<int64_t>(t) * B + b) * ldY + dir * H + u];
+      unpack4(gq[p], gv);
       float da[4];
       if (lstm) {
         const float i = gv[0], f = gv[1], gg = gv[2], o = gv[3];
-        const float* C = a.C + static_cast<int64_t>(dir) * (TT + 1) * B * H;
-        const float c = C[(static_cast<int64_t>(dir ? t : t + 1) * B + b) * H + u];
-        const float cp = C[(static_cast<int64_t>(dir ? t + 1 : t) * B + b) * H + u];
-        const float dh = dy + dhr;
-        const float tc = tanhf(c);
+        const float c = e0[p], cp = e1[p];
+        const float dh = dyv[p] + dhr;
+        const float tc = tanh_fast(c);
         const float dc = dh * o * (1.f - tc * tc) + carry[p];
         da[0] = dc * gg * i * (1.f - i);
         da[1] = dc * cp * f * (1.f - f);
@@ -436,27 +525,29 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         carry[p] = dc * f;
       } else {
         const float r = gv[0], z = gv[1], n = gv[2], hn = gv[3];
-        const float hp = __bfloat162float(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
-        const float dh = dy + dhr + carry[p];
+        const float hp = e0[p];
+        const float dh = dyv[p] + dhr + carry[p];
         const float dn = dh * (1.f - z) * (1.f - n * n);
         const float dz = dh * (hp - n) * z * (1.f - z);
         const float dr = dn * hn * r * (1.f - r);
         da[0] = dr; da[1] = dz; da[2] = dn; da[3] = dn * r;
         carry[p] = dh * z;
       }
-      Vec4<__nv_bfloat16>::store(dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u, da);
 #pragma unroll
       for (int q = 0; q < 4; ++q) db[p][q] += da[q];
+      Vec4<__nv_bfloat16>::store(dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u, da);
     }
-    if (s < TT) step_arrive(a, skip);
+    RNN_TRACE_AT(5, 1, s);
+    if (s < TT) step_arrive(a, skip, s, 1);
+    RNN_TRACE_AT(6, 1, s);
   }
 
   if (!aborted) {
-    // bias gradients: reduce each unit's four sums over the batch (reuses part,
-    // after every peer has finished reading it)
+    // bias gradients: reduce each unit's four sums over the batch (reuses recv,
+    // after every peer has finished with it)
     tc_fence_before();
     if (P.KS > 1) cluster_sync(); else __syncthreads();
-    float* red = part;
+    float* red = recv;
     for (int i = threadIdx.x; i < 4 * UPC; i += kThreads) red[i] = 0.f;
     __syncthreads();
 #pragma unroll
@@ -476,7 +567,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 
 int pp_for(int pairs) {
   const int need = (pairs + kThreads - 1) / kThreads;
-  return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : need <= 16 ? 16 : 0;
+  return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : 0;
 }
 
 const void* fwd_fn(int pp) {
@@ -484,8 +575,7 @@ const void* fwd_fn(int pp) {
     case 1: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<1>);
     case 2: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<2>);
     case 4: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<4>);
-    case 8: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<8>);
-    default: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<16>);
+    default: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<8>);
   }
 }
 const void* bwd_fn(int pp) {
@@ -493,21 +583,20 @@ const void* bwd_fn(int pp) {
     case 1: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<1>);
     case 2: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<2>);
     case 4: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<4>);
-    case 8: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<8>);
-    default: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<16>);
+    default: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<8>);
   }
 }
 
 struct TcPlan {
   int KS = 0, Kc = 0, nsub = 0, R = 0, Npad = 0, UPC = 0, PP = 0, nrg = 0;
-  uint32_t tmem_cols = 0, off_ring = 0, off_part = 0, off_bar = 0;
+  uint32_t tmem_cols = 0, off_ring = 0, off_recv = 0, off_bar = 0;
   size_t smem = 0;
 };
 
 size_t a1k(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
-// Candidate K splits for one launch, preferred first: the largest split
-// whose grid fits (shorter per-CTA contraction, less shared memory per CTA).
+// Candidate K splits for one launch, preferred first: the largest split whose
+// grid fits (shorter per-CTA contraction, less shared memory per CTA).
 // Whether the clusters can all be resident at once is checked at launch.
 int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int max_out) {
   if (B < 1 || B > 256) return 0;
@@ -515,8 +604,15 @@ int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int ma
   const int nrg = bwd ? H / 128 : (4 * H) / 128;
   if (bwd ? (H % 128) : (H % 32)) return 0;
   const int Npad = (B + 15) / 16 * 16;
+  // tuning knob: RNN_TC_MAX_KS_FWD / RNN_TC_MAX_KS_BWD cap the split (1..16)
+  int cap = kMaxKS;
+  if (const char* e = std::getenv(bwd ? "RNN_TC_MAX_KS_BWD" : "RNN_TC_MAX_KS_FWD")) {
+    const int v = std::atoi(e);
+    if (v >= 1 && v <= kMaxKS) cap = v;
+  }
   int n = 0;
-  for (int KS = 8; KS >= 1 && n < max_out; KS /= 2) {
+  for (int KS = kMaxKS; KS >= 1 && n < max_out; KS /= 2) {
+    if (KS > cap) continue;
     if (K % (KS * kSubK)) continue;
     const int Kc = K / KS;
     const int nsub = Kc / kSubK;
@@ -527,11 +623,11 @@ int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int ma
     if (nrg * KS * ndir > num_sms) continue;
     const size_t wbytes = static_cast<size_t>(nsub) * kWSub;
     const size_t rb = static_cast<size_t>(Npad) * 128;
-    const size_t part = static_cast<size_t>(Npad) * 128 * 4;
-    int R = nsub < 16 ? nsub : 16;
+    const size_t recv = static_cast<size_t>(Npad) * 128 * 4;
+    int R = nsub < kMaxRing ? nsub : kMaxRing;
     size_t smem = 0;
     for (; R >= 1; --R) {
-      smem = a1k(wbytes) + a1k(R * rb) + a1k(part) + a1k(sizeof(TcBars)) + 1024;
+      smem = a1k(wbytes) + a1k(R * rb) + a1k(recv) + a1k(sizeof(TcBars)) + 1024;
       if (smem <= kSmemCap) break;
     }
     if (R < 1 || (R < nsub && R < 2)) continue;
@@ -541,10 +637,8 @@ int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int ma
     while (tc < static_cast<uint32_t>(Npad)) tc *= 2;
     p.tmem_cols = tc;
     p.off_ring = static_cast<uint32_t>(a1k(wbytes));
-    p.off_part = p.off_ring + static_cast<uint32_t>(a1k(R * rb));
-    p.off_bar = p.off_part + static_cast<uint32_t>(a1k(part));
-    // at least a third of an SM's shared memory: at most two CTAs per SM, so
-    // their tensor-memory allocations (<= 256 columns each) always fit
+    p.off_recv = p.off_ring + static_cast<uint32_t>(a1k(R * rb));
+    p.off_bar = p.off_recv + static_cast<uint32_t>(a1k(recv));
     p.smem = smem < kMinSmem ? kMinSmem : smem;
     out[n++] = p;
   }
@@ -569,13 +663,17 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPla
 
 // First candidate plan whose clusters can all be resident at once.
 bool choose_plan(int bwd, int H, int B, int ndir, int num_sms, TcPlan* chosen) {
-  TcPlan plans[4];
-  const int n = make_plans(bwd, H, B, ndir, num_sms, plans, 4);
+  TcPlan plans[5];
+  const int n = make_plans(bwd, H, B, ndir, num_sms, plans, 5);
   for (int i = 0; i < n; ++i) {
     const TcPlan& pl = plans[i];
     const void* fn = kernel_for(bwd, pl.PP);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) !=
         cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (pl.KS > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
       cudaGetLastError();
       continue;
     }
@@ -616,9 +714,10 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   TcPersistParams P;
   P.a = a;
   P.KS = pl.KS; P.Kc = pl.Kc; P.nsub = pl.nsub; P.R = pl.R; P.Npad = pl.Npad; P.UPC = pl.UPC;
+  P.RPC = 128 / pl.KS;
   P.nblk_dir = static_cast<unsigned int>(pl.nrg * pl.KS);
   P.tmem_cols = pl.tmem_cols;
-  P.off_ring = pl.off_ring; P.off_part = pl.off_part; P.off_bar = pl.off_bar;
+  P.off_ring = pl.off_ring; P.off_recv = pl.off_recv; P.off_bar = pl.off_bar;
   const void* fn = kernel_for(bwd, pl.PP);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
@@ -629,6 +728,12 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
 }
 
 }  // namespace
+
+#ifdef RNN_STEP_TRACE
+extern "C" int rnn_debug_read_step_trace(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, g_step_trace, bytes) == cudaSuccess ? 0 : 3;
+}
+#endif
 
 bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms) {
   if (!(mode == 0 || (mode == 1 && reset_after))) return false;
