@@ -16,6 +16,11 @@
 // between CTAs), with acquire/release counters in place of its -0.0 sentinel
 // polling.
 //
+// When the weights of the grid do not fit in shared memory (e.g. H = 2048), the
+// kernels stream them instead: each step reads the owned rows / columns
+// through the read-only data cache from L2 (the packed recurrent weights of a
+// layer, at most 32 MiB in bf16, stay L2-resident across steps).
+//
 // This kernel serves the fp32 path (the 1e-5 bound needs fp32 FMA, not TF32),
 // GRU reset-before (two dependent contractions per step: r/z, then W_hn(r*h))
 // and any shape the tensor-core kernels do not take.
@@ -32,6 +37,20 @@ namespace rnn {
 namespace {
 
 constexpr int kThreads = 256;
+
+#ifdef RNN_STEP_TRACE
+// Step-phase timestamps (globaltimer, ns) of CTA 0 and the last CTA of the
+// latency-mode forward, for latency studies; compiled only with -DRNN_STEP_TRACE.
+__device__ unsigned long long g_lat_trace[2][1100][8];
+#define RNN_LAT_TRACE(slot_, step_)                                                              \
+  do {                                                                                          \
+    if (threadIdx.x == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1) && blockIdx.y == 0 && \
+        (step_) < 1100)                                                                          \
+      g_lat_trace[blockIdx.x == 0 ? 0 : 1][(step_)][(slot_)] = globaltimer_ns();                 \
+  } while (0)
+#else
+#define RNN_LAT_TRACE(slot_, step_) do { } while (0)
+#endif
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 
@@ -51,56 +70,36 @@ __device__ __forceinline__ bool cta_wait(const PersistArgs& a, const unsigned in
   return __syncthreads_and(ok) != 0;
 }
 
-// All stores of this phase by the CTA are ordered before the arrival.
+// All stores of this phase by the CTA are ordered before the arrival (the
+// barrier, then the release add).
 __device__ __forceinline__ void cta_arrive(unsigned int* ctr, bool skip) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (!skip) red_release_gpu_add(ctr, 1u);
+  if (threadIdx.x == 0 && !skip) red_release_gpu_add(ctr, 1u);
+}
+
+// The recurrent weights as seen by one CTA: resident in shared memory
+// (row stride WS), or streamed from the packed global copy.
+template <typename T, bool STREAM>
+struct WView {
+  const T* base;   // smem tile, or this direction's packed global matrix
+  int NU, WS, u0, H;
+  __device__ __forceinline__ const T* fwd_row(int s, int ul, int k0) const {
+    return STREAM ? base + static_cast<size_t>(4 * (u0 + ul) + s) * H + k0 : base + (s * NU + ul) * WS + k0;
   }
+  __device__ __forceinline__ const T* bwd_row(int ul, int k0) const {
+    return STREAM ? base + static_cast<size_t>(u0 + ul) * 4 * H + k0 : base + ul * WS + k0;
+  }
+};
+template <typename T, bool STREAM>
+__device__ __forceinline__ float ldw(const T* p) {
+  if (STREAM) return to_f<T>(__ldg(p));
+  return to_f<T>(*p);
 }
 
 // acc[p][s] += sum_k W[s][ul][k] * src[b][k] over k in [0, K), slots in MASK.
 // src row b starts at src + b * ld.
-template <typename T, int PP, int MASK>
-__device__ __forceinline__ void contract_fwd(float (&acc)[PP][4], const T* Ws, int NU, int WS,
-                                             float* hs, int KC, const T* src, int64_t ld, int K,
-                                             int B, int nu, int npairs) {
-  const int HS = KC + 1;
-  for (int k0 = 0; k0 < K; k0 += KC) {
-    const int kc = min(KC, K - k0);
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < B * kc; idx += kThreads) {
-      const int b = idx / kc, kk = idx - b * kc;
-      hs[b * HS + kk] = ldcg_f(src + b * ld + k0 + kk);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int p = 0; p < PP; ++p) {
-      const int id = threadIdx.x + p * kThreads;
-      if (id >= npairs) break;
-      const int ul = id % nu, b = id / nu;
-      const float* hr = hs + b * HS;
-      const T* w0 = Ws + (0 * NU + ul) * WS + k0;
-      const T* w1 = Ws + (1 * NU + ul) * WS + k0;
-      const T* w2 = Ws + (2 * NU + ul) * WS + k0;
-      const T* w3 = Ws + (3 * NU + ul) * WS + k0;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-      for (int kk = 0; kk < kc; ++kk) {
-        const float hv = hr[kk];
-        if (MASK & 1) a0 = fmaf(to_f<T>(w0[kk]), hv, a0);
-        if (MASK & 2) a1 = fmaf(to_f<T>(w1[kk]), hv, a1);
-        if (MASK & 4) a2 = fmaf(to_f<T>(w2[kk]), hv, a2);
-        if (MASK & 8) a3 = fmaf(to_f<T>(w3[kk]), hv, a3);
-      }
-      acc[p][0] += a0; acc[p][1] += a1; acc[p][2] += a2; acc[p][3] += a3;
-    }
-  }
-}
-
-// acc[p] += sum_k WT[ul][k] * src[b][k] over k in [0, K) with (k & 3) in MASK.
-template <typename T, int PP, int MASK>
-__device__ __forceinline__ void contract_bwd(float (&acc)[PP], const T* Ws, int WS, float* hs, int KC,
+template <typename T, bool STREAM, int PP, int MASK>
+__device__ __forceinline__ void contract_fwd(float (&acc)[PP][4], const WView<T, STREAM>& W, float* hs, int KC,
                                              const T* src, int64_t ld, int K, int B, int nu, int npairs) {
   const int HS = KC + 1;
   for (int k0 = 0; k0 < K; k0 += KC) {
@@ -117,15 +116,51 @@ __device__ __forceinline__ void contract_bwd(float (&acc)[PP], const T* Ws, int 
       if (id >= npairs) break;
       const int ul = id % nu, b = id / nu;
       const float* hr = hs + b * HS;
-      const T* w = Ws + ul * WS + k0;
-      float s = 0.f;
+      const T* w0 = W.fwd_row(0, ul, k0);
+      const T* w1 = W.fwd_row(1, ul, k0);
+      const T* w2 = W.fwd_row(2, ul, k0);
+      const T* w3 = W.fwd_row(3, ul, k0);
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      for (int kk = 0; kk < kc; ++kk) {
+        const float hv = hr[kk];
+        if (MASK & 1) a0 = fmaf(ldw<T, STREAM>(w0 + kk), hv, a0);
+        if (MASK & 2) a1 = fmaf(ldw<T, STREAM>(w1 + kk), hv, a1);
+        if (MASK & 4) a2 = fmaf(ldw<T, STREAM>(w2 + kk), hv, a2);
+        if (MASK & 8) a3 = fmaf(ldw<T, STREAM>(w3 + kk), hv, a3);
+      }
+      acc[p][0] += a0; acc[p][1] += a1; acc[p][2] += a2; acc[p][3] += a3;
+    }
+  }
+}
+
+// acc[p] += sum_k WT[ul][k] * src[b][k] over k in [0, K) with (k & 3) in MASK.
+template <typename T, bool STREAM, int PP, int MASK>
+__device__ __forceinline__ void contract_bwd(float (&acc)[PP], const WView<T, STREAM>& W, float* hs, int KC,
+                                             const T* src, int64_t ld, int K, int B, int nu, int npairs) {
+  const int HS = KC + 1;
+  for (int k0 = 0; k0 < K; k0 += KC) {
+    const int kc = min(KC, K - k0);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < B * kc; idx += kThreads) {
+      const int b = idx / kc, kk = idx - b * kc;
+      hs[b * HS + kk] = ldcg_f(src + b * ld + k0 + kk);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      if (id >= npairs) break;
+      const int ul = id % nu, b = id / nu;
+      const float* hr = hs + b * HS;
+      const T* w = W.bwd_row(ul, k0);
+      float sacc = 0.f;
       if (MASK == 0xF) {
-        for (int kk = 0; kk < kc; ++kk) s = fmaf(to_f<T>(w[kk]), hr[kk], s);
+        for (int kk = 0; kk < kc; ++kk) sacc = fmaf(ldw<T, STREAM>(w + kk), hr[kk], sacc);
       } else {
         for (int kk = 0; kk < kc; ++kk)
-          if ((MASK >> (kk & 3)) & 1) s = fmaf(to_f<T>(w[kk]), hr[kk], s);
+          if ((MASK >> (kk & 3)) & 1) sacc = fmaf(ldw<T, STREAM>(w + kk), hr[kk], sacc);
       }
-      acc[p] += s;
+      acc[p] += sacc;
     }
   }
 }
@@ -133,7 +168,7 @@ __device__ __forceinline__ void contract_bwd(float (&acc)[PP], const T* Ws, int 
 // ---------------------------------------------------------------------------
 // forward
 // ---------------------------------------------------------------------------
-template <typename T, int PP>
+template <typename T, int PP, bool STREAM>
 __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistArgs a, int NU, int KC) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
@@ -142,17 +177,20 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
   const int nu = min(NU, H - u0);
   const int WS = H + row_pad<T>();
   T* Ws = reinterpret_cast<T*>(smem);
-  float* hs = reinterpret_cast<float*>(smem + align16(static_cast<size_t>(4) * NU * WS * sizeof(T)));
+  float* hs = reinterpret_cast<float*>(STREAM ? smem : smem + align16(static_cast<size_t>(4) * NU * WS * sizeof(T)));
   const bool lstm = a.mode == 0;
   const bool rb = !lstm && !a.reset_after;
 
   const T* Wr = static_cast<const T*>(a.Wr) + static_cast<size_t>(dir) * 4 * H * H;
-  for (int idx = threadIdx.x; idx < 4 * nu * H; idx += kThreads) {
-    const int s = idx / (nu * H);
-    const int rem = idx - s * nu * H;
-    const int ul = rem / H, k = rem - ul * H;
-    Ws[(s * NU + ul) * WS + k] = Wr[static_cast<size_t>(4 * (u0 + ul) + s) * H + k];
+  if (!STREAM) {
+    for (int idx = threadIdx.x; idx < 4 * nu * H; idx += kThreads) {
+      const int s = idx / (nu * H);
+      const int rem = idx - s * nu * H;
+      const int ul = rem / H, k = rem - ul * H;
+      Ws[(s * NU + ul) * WS + k] = Wr[static_cast<size_t>(4 * (u0 + ul) + s) * H + k];
+    }
   }
+  const WView<T, STREAM> W{STREAM ? Wr : Ws, NU, WS, u0, H};
 
   T* Y = static_cast<T*>(a.Y);
   const T* P = static_cast<const T*>(a.P);
@@ -195,11 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
     for (int p = 0; p < PP; ++p) acc[p][0] = acc[p][1] = acc[p][2] = acc[p][3] = 0.f;
     const T* hsrc = Y + static_cast<int64_t>(sp) * B * ldY + dir * H;
     if (rb)
-      contract_fwd<T, PP, 0x3>(acc, Ws, NU, WS, hs, KC, hsrc, ldY, H, B, nu, npairs);
+      contract_fwd<T, STREAM, PP, 0x3>(acc, W, hs, KC, hsrc, ldY, H, B, nu, npairs);
     else if (lstm)
-      contract_fwd<T, PP, 0xF>(acc, Ws, NU, WS, hs, KC, hsrc, ldY, H, B, nu, npairs);
+      contract_fwd<T, STREAM, PP, 0xF>(acc, W, hs, KC, hsrc, ldY, H, B, nu, npairs);
     else
-      contract_fwd<T, PP, 0x7>(acc, Ws, NU, WS, hs, KC, hsrc, ldY, H, B, nu, npairs);
+      contract_fwd<T, STREAM, PP, 0x7>(acc, W, hs, KC, hsrc, ldY, H, B, nu, npairs);
 
     if (rb) {
       // phase 1: r, z and the reset state r * h_{t-1}
@@ -222,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
 #pragma unroll
       for (int p = 0; p < PP; ++p) acc[p][2] = 0.f;
       const T* rsrc = RH + (static_cast<int64_t>(dir) * TT + t) * B * H;
-      contract_fwd<T, PP, 0x4>(acc, Ws, NU, WS, hs, KC, rsrc, H, H, B, nu, npairs);
+      contract_fwd<T, STREAM, PP, 0x4>(acc, W, hs, KC, rsrc, H, H, B, nu, npairs);
     }
 
 #pragma unroll
@@ -275,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
 // ---------------------------------------------------------------------------
 // backward through time
 // ---------------------------------------------------------------------------
-template <typename T, int PP>
+template <typename T, int PP, bool STREAM>
 __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistArgs a, int NU, int KC) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
@@ -285,16 +323,19 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
   const int K4 = 4 * H;
   const int WS = K4 + row_pad<T>();
   T* Ws = reinterpret_cast<T*>(smem);
-  float* hs = reinterpret_cast<float*>(smem + align16(static_cast<size_t>(NU) * WS * sizeof(T)));
+  float* hs = reinterpret_cast<float*>(STREAM ? smem : smem + align16(static_cast<size_t>(NU) * WS * sizeof(T)));
   __shared__ float dbs[4 * 64];
   const bool lstm = a.mode == 0;
   const bool rb = !lstm && !a.reset_after;
 
   const T* WT = static_cast<const T*>(a.WrT) + static_cast<size_t>(dir) * H * K4;
-  for (int idx = threadIdx.x; idx < nu * K4; idx += kThreads) {
-    const int ul = idx / K4, k = idx - ul * K4;
-    Ws[ul * WS + k] = WT[static_cast<size_t>(u0 + ul) * K4 + k];
+  if (!STREAM) {
+    for (int idx = threadIdx.x; idx < nu * K4; idx += kThreads) {
+      const int ul = idx / K4, k = idx - ul * K4;
+      Ws[ul * WS + k] = WT[static_cast<size_t>(u0 + ul) * K4 + k];
+    }
   }
+  const WView<T, STREAM> W{STREAM ? WT : Ws, NU, WS, u0, H};
 
   const T* Y = static_cast<const T*>(a.Y);
   const T* G = static_cast<const T*>(a.gates);
@@ -340,9 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
       const int tp = dir ? s - 1 : TT - s;   // step processed just before
       const T* src = dG + static_cast<int64_t>(tp) * B * ldG + dir * K4;
       if (rb)
-        contract_bwd<T, PP, 0x3>(dhr, Ws, WS, hs, KC, src, ldG, K4, B, nu, npairs);
+        contract_bwd<T, STREAM, PP, 0x3>(dhr, W, hs, KC, src, ldG, K4, B, nu, npairs);
       else
-        contract_bwd<T, PP, 0xF>(dhr, Ws, WS, hs, KC, src, ldG, K4, B, nu, npairs);
+        contract_bwd<T, STREAM, PP, 0xF>(dhr, W, hs, KC, src, ldG, K4, B, nu, npairs);
     }
     if (s == TT) {
 #pragma unroll
@@ -420,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
 #pragma unroll
       for (int p = 0; p < PP; ++p) drh[p] = 0.f;
       const T* src = dG + static_cast<int64_t>(t) * B * ldG + dir * K4;
-      contract_bwd<T, PP, 0x4>(drh, Ws, WS, hs, KC, src, ldG, K4, B, nu, npairs);
+      contract_bwd<T, STREAM, PP, 0x4>(drh, W, hs, KC, src, ldG, K4, B, nu, npairs);
 #pragma unroll
       for (int p = 0; p < PP; ++p) {
         const int id = threadIdx.x + p * kThreads;
@@ -462,28 +503,273 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
   }
 }
 
+// ---------------------------------------------------------------------------
+// forward, large weights, small batch (latency mode)
+// ---------------------------------------------------------------------------
+// For layers whose recurrent weights do not fit the per-unit layout above
+// (e.g. H = 2048) and batch <= 8.  Each CTA owns NU units; as many of their
+// weight rows as fit stay resident in shared memory for the whole sequence,
+// the remaining rows are streamed from L2 each step (read-only path).  Each
+// warp owns rows r = warp, warp + 8, ...; its lanes split K in 16-byte
+// vectors.  Per K vector a lane loads its slice of h_{t-1} for every batch
+// column once (from shared memory, staged per step) and reuses it across its
+// rows; the per-row partial sums are combined with warp shuffles.  At batch 8
+// the step is FP32-issue bound, at batch 1 bound by the exchange.
+constexpr int kLatRows = 8;    // max rows per warp (4 * NU <= 64)
+
+template <typename T, int BB>
+__device__ __forceinline__ void latency_rows(const T* Ws, int WSR, int Rs, const T* Wg, int H, const int* rowmap,
+                                             int row0, int nrows, const T* hs, int B, float* out) {
+  constexpr int VE = 16 / sizeof(T);           // elements per 16-byte vector
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nv = H / (32 * VE);
+  float acc[kLatRows][BB];
+#pragma unroll
+  for (int j = 0; j < kLatRows; ++j)
+#pragma unroll
+    for (int b = 0; b < BB; ++b) acc[j][b] = 0.f;
+  for (int v = 0; v < nv; ++v) {
+    const int k = (v * 32 + lane) * VE;
+    float hv[BB][VE];
+#pragma unroll
+    for (int b = 0; b < BB; ++b) {
+      if (b < B) {
+        const uint4 q = *reinterpret_cast<const uint4*>(hs + static_cast<size_t>(b) * H + k);
+        if (sizeof(T) == 2) {
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+          for (int e = 0; e < VE / 2; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            hv[b][2 * e] = f.x; hv[b][2 * e + 1] = f.y;
+          }
+        } else {
+          const float* f = reinterpret_cast<const float*>(&q);
+#pragma unroll
+          for (int e = 0; e < VE; ++e) hv[b][e] = f[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VE; ++e) hv[b][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kLatRows; ++j) {
+      const int r = row0 + warp + 8 * j;
+      if (r < nrows) {
+        const uint4 q = r < Rs ? *reinterpret_cast<const uint4*>(Ws + static_cast<size_t>(r) * WSR + k)
+                               : __ldg(reinterpret_cast<const uint4*>(Wg + static_cast<size_t>(rowmap[r]) * H + k));
+        float w[VE];
+        if (sizeof(T) == 2) {
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+          for (int e = 0; e < VE / 2; ++e) {
+            const float2 f = __bfloat1622float2(h2[e]);
+            w[2 * e] = f.x; w[2 * e + 1] = f.y;
+          }
+        } else {
+          const float* f = reinterpret_cast<const float*>(&q);
+#pragma unroll
+          for (int e = 0; e < VE; ++e) w[e] = f[e];
+        }
+#pragma unroll
+        for (int b = 0; b < BB; ++b)
+#pragma unroll
+          for (int e = 0; e < VE; ++e) acc[j][b] = fmaf(w[e], hv[b][e], acc[j][b]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kLatRows; ++j) {
+    const int r = row0 + warp + 8 * j;
+#pragma unroll
+    for (int b = 0; b < BB; ++b) {
+      float x = acc[j][b];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+      if (lane == 0 && r < nrows && b < B) out[r * BB + b] = x;
+    }
+  }
+}
+
+// B rows of a state (storage type, row stride ld) -> hs[b][k] in shared memory.
 template <typename T>
+__device__ __forceinline__ void stage_state(const T* src, int64_t ld, int H, int B, T* hs) {
+  constexpr int VE = 16 / sizeof(T);
+  const int per_row = H / VE;
+  for (int i = threadIdx.x; i < B * per_row; i += kThreads) {
+    const int b = i / per_row, c = i - b * per_row;
+    const uint4 q = __ldcg(reinterpret_cast<const uint4*>(src + b * ld) + c);
+    *reinterpret_cast<uint4*>(hs + static_cast<size_t>(b) * H + c * VE) = q;
+  }
+}
+
+template <typename T, int BB>
+__global__ void __launch_bounds__(kThreads, 1) persist_fwd_latency_kernel(PersistArgs a, int NU, int Rs) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int H = a.H, B = a.B, TT = a.T, D = a.D;
+  const int dir = a.dir0 + blockIdx.y;
+  const int u0 = blockIdx.x * NU;
+  const int nu = min(NU, H - u0);
+  const bool lstm = a.mode == 0;
+  const bool rb = !lstm && !a.reset_after;
+  const int na = lstm ? 4 : (rb ? 2 : 3);     // phase-A rows per unit
+  const int WSR = H + 16 / static_cast<int>(sizeof(T));   // resident row stride (16-byte aligned)
+  T* hs = reinterpret_cast<T*>(smem);                                   // [BB][H]
+  float* out = reinterpret_cast<float*>(smem + static_cast<size_t>(BB) * H * sizeof(T));   // [4*NU][BB]
+  int* rows = reinterpret_cast<int*>(out + 4 * NU * BB);                // local row -> packed row
+  T* Ws = reinterpret_cast<T*>(rows + 4 * NU);                          // [Rs][WSR]
+  int nA = 0, nAB = 0;
+  {
+    // phase A rows: LSTM i,f,g,o; GRU resetAfter r,z,n; reset-before r,z.  Phase B (reset-before): n.
+    for (int ul = 0; ul < nu; ++ul)
+      for (int sl = 0; sl < na; ++sl) {
+        if (threadIdx.x == 0) rows[nA] = 4 * (u0 + ul) + sl;
+        ++nA;
+      }
+    nAB = nA;
+    if (rb)
+      for (int ul = 0; ul < nu; ++ul) {
+        if (threadIdx.x == 0) rows[nAB] = 4 * (u0 + ul) + 2;
+        ++nAB;
+      }
+  }
+  __syncthreads();
+  const T* Wr = static_cast<const T*>(a.Wr) + static_cast<size_t>(dir) * 4 * H * H;
+  const int rs = min(Rs, nAB);
+  {
+    constexpr int VE = 16 / sizeof(T);
+    const int per_row = H / VE;
+    for (int i = threadIdx.x; i < rs * per_row; i += kThreads) {
+      const int r = i / per_row, c = i - r * per_row;
+      *reinterpret_cast<uint4*>(Ws + static_cast<size_t>(r) * WSR + c * VE) =
+          __ldg(reinterpret_cast<const uint4*>(Wr + static_cast<size_t>(rows[r]) * H) + c);
+    }
+  }
+
+  T* Y = static_cast<T*>(a.Y);
+  const T* P = static_cast<const T*>(a.P);
+  T* G = static_cast<T*>(a.gates);
+  T* RH = static_cast<T*>(a.RH);
+  const int64_t ldY = static_cast<int64_t>(D) * H;
+  const int64_t ldP = static_cast<int64_t>(D) * 4 * H;
+  const int npairs = nu * B;          // <= kThreads: one pair per thread
+  const int id = threadIdx.x;
+  const bool has = id < npairs;
+  const int ul = has ? id % nu : 0, b = has ? id / nu : 0, u = u0 + ul;
+  const int slot_h0 = dir ? TT + 1 : 0;
+  float st = 0.f;
+  if (has) {
+    if (lstm) {
+      const T* c0 = static_cast<const T*>(a.c0);
+      st = c0 ? to_f<T>(c0[(static_cast<int64_t>(dir) * B + b) * H + u]) : 0.f;
+      if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? TT : 0)) * B + b) * H + u] = st;
+    } else {
+      st = to_f<T>(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
+    }
+  }
+  unsigned int* ctr = &a.dev->counters[dir];
+  const unsigned int nblk = gridDim.x;
+  const bool skip = a.skip_cta == static_cast<int>(blockIdx.x + gridDim.x * blockIdx.y);
+  unsigned int phases = 0;
+
+  for (int s = 0; s < TT; ++s) {
+    const int t = dir ? TT - 1 - s : s;
+    const int sp = dir ? t + 2 : t;
+    float pv[4] = {0.f, 0.f, 0.f, 0.f};
+    RNN_LAT_TRACE(0, s);
+    if (has) Vec4<T>::load(P + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u, pv);
+    if (phases > 0 && !cta_wait(a, ctr, phases * nblk, K_FWD_SIMT, s)) return;
+    RNN_LAT_TRACE(1, s);
+    stage_state<T>(Y + static_cast<int64_t>(sp) * B * ldY + dir * H, ldY, H, B, hs);
+    __syncthreads();
+    RNN_LAT_TRACE(2, s);
+    latency_rows<T, BB>(Ws, WSR, rs, Wr, H, rows, 0, nA, hs, B, out);
+    __syncthreads();
+    RNN_LAT_TRACE(3, s);
+    float gv[4] = {0.f, 0.f, 0.f, 0.f}, h = 0.f;
+    float r = 0.f, z = 0.f;
+    if (has) {
+      const float* o = out + (ul * na) * BB + b;   // this unit's rows in phase-A order
+      if (lstm) {
+        const float i = sigm(pv[0] + o[0]);
+        const float f = sigm(pv[1] + o[BB]);
+        const float g = tanhf(pv[2] + o[2 * BB]);
+        const float oo = sigm(pv[3] + o[3 * BB]);
+        const float c = f * st + i * g;
+        h = oo * tanhf(c);
+        st = c;
+        gv[0] = i; gv[1] = f; gv[2] = g; gv[3] = oo;
+      } else if (!rb) {
+        const float* bh = a.bh + dir * 4 * H + 4 * u;
+        r = sigm(pv[0] + o[0] + bh[0]);
+        z = sigm(pv[1] + o[BB] + bh[1]);
+        const float hn = o[2 * BB] + bh[2];
+        const float n = tanhf(pv[2] + r * hn);
+        h = (1.f - z) * n + z * st;
+        gv[0] = r; gv[1] = z; gv[2] = n; gv[3] = hn;
+      } else {
+        r = sigm(pv[0] + o[0]);
+        z = sigm(pv[1] + o[BB]);
+        RH[((static_cast<int64_t>(dir) * TT + t) * B + b) * H + u] = from_f<T>(r * st);
+      }
+    }
+    if (rb) {
+      cta_arrive(ctr, skip);
+      ++phases;
+      if (!cta_wait(a, ctr, phases * nblk, K_FWD_SIMT, s)) return;
+      stage_state<T>(RH + (static_cast<int64_t>(dir) * TT + t) * B * H, H, H, B, hs);
+      __syncthreads();
+      latency_rows<T, BB>(Ws, WSR, rs, Wr, H, rows, nA, nAB, hs, B, out);
+      __syncthreads();
+      if (has) {
+        const float n = tanhf(pv[2] + out[(nA + ul) * BB + b]);
+        h = (1.f - z) * n + z * st;
+        gv[0] = r; gv[1] = z; gv[2] = n; gv[3] = 0.f;
+      }
+    }
+    if (has) {
+      if (!lstm) st = h;
+      Y[(static_cast<int64_t>(t + 1) * B + b) * ldY + dir * H + u] = from_f<T>(h);
+    }
+    RNN_LAT_TRACE(4, s);
+    cta_arrive(ctr, skip);
+    RNN_LAT_TRACE(5, s);
+    ++phases;
+    if (has) {
+      if (G) Vec4<T>::store(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * 4 * H + 4 * u, gv);
+      if (lstm && a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = st;
+      if (s == TT - 1) {
+        const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
+        if (a.hy) static_cast<T*>(a.hy)[o] = from_f<T>(h);
+        if (lstm && a.cy) static_cast<T*>(a.cy)[o] = from_f<T>(st);
+      }
+    }
+  }
+}
+
+template <typename T, bool STREAM>
 struct SimtKernels {
   static const void* fwd(int pp) {
     switch (pp) {
-      case 1: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 1>);
-      case 2: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 2>);
-      case 4: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 4>);
-      default: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 8>);
+      case 1: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 1, STREAM>);
+      case 2: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 2, STREAM>);
+      case 4: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 4, STREAM>);
+      default: return reinterpret_cast<const void*>(&persist_fwd_simt_kernel<T, 8, STREAM>);
     }
   }
   static const void* bwd(int pp) {
     switch (pp) {
-      case 1: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 1>);
-      case 2: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 2>);
-      case 4: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 4>);
-      default: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 8>);
+      case 1: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 1, STREAM>);
+      case 2: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 2, STREAM>);
+      case 4: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 4, STREAM>);
+      default: return reinterpret_cast<const void*>(&persist_bwd_simt_kernel<T, 8, STREAM>);
     }
   }
 };
 
 struct SimtPlan {
   int NU = 0, nblk = 0, KC = 0, PP = 0;
+  bool stream = false;
   size_t smem = 0;
 };
 
@@ -492,9 +778,19 @@ int pp_for(int pairs) {
   return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : 0;
 }
 
+const void* kernel_for(const PersistArgs& a, bool bwd, const SimtPlan& pl) {
+  if (a.is_bf16)
+    return pl.stream ? (bwd ? SimtKernels<__nv_bfloat16, true>::bwd(pl.PP) : SimtKernels<__nv_bfloat16, true>::fwd(pl.PP))
+                     : (bwd ? SimtKernels<__nv_bfloat16, false>::bwd(pl.PP) : SimtKernels<__nv_bfloat16, false>::fwd(pl.PP));
+  return pl.stream ? (bwd ? SimtKernels<float, true>::bwd(pl.PP) : SimtKernels<float, true>::fwd(pl.PP))
+                   : (bwd ? SimtKernels<float, false>::bwd(pl.PP) : SimtKernels<float, false>::fwd(pl.PP));
+}
+
 // Pick units per CTA: minimise an estimated step time (a fixed cost for the
 // cross-CTA exchange when there is more than one CTA, plus the per-thread FMA
 // count) subject to shared memory, registers and co-residency of the grid.
+// Without a resident fit, stream the weights and spread them over the most
+// CTAs that fit (more read bandwidth).
 int make_plan(const PersistArgs& a, bool bwd, int num_sms, SimtPlan* out) {
   const int H = a.H, B = a.B;
   const size_t es = a.is_bf16 ? 2 : 4;
@@ -516,15 +812,69 @@ int make_plan(const PersistArgs& a, bool bwd, int num_sms, SimtPlan* out) {
                               : static_cast<size_t>(4) * NU * (H + (a.is_bf16 ? 2 : 1)) * es;
     const size_t smem = align16(wbytes) + hs_bytes;
     if (smem > smem_cap) break;
-    const double cost = (nblk > 1 ? 3000.0 : 0.0) + static_cast<double>(pp) * 4.0 * H * (bwd ? 1.0 : 1.0) +
+    const double cost = (nblk > 1 ? 3000.0 : 0.0) + static_cast<double>(pp) * 4.0 * H +
                         static_cast<double>(B) * (bwd ? 4 * H : H) / kThreads;
     if (cost < best) {
       best = cost;
-      bp.NU = NU; bp.nblk = nblk; bp.KC = KC; bp.PP = pp; bp.smem = smem;
+      bp.NU = NU; bp.nblk = nblk; bp.KC = KC; bp.PP = pp; bp.smem = smem; bp.stream = false;
     }
   }
-  if (bp.NU == 0) return 2;
+  if (bp.NU == 0) {
+    const int max_ctas = num_sms / a.ndir;
+    if (max_ctas < 1) return 2;
+    const int NU = (H + max_ctas - 1) / max_ctas;
+    const int pp = pp_for(NU * B);
+    if (pp == 0) return 2;
+    bp.NU = NU; bp.nblk = (H + NU - 1) / NU; bp.KC = KC; bp.PP = pp; bp.smem = hs_bytes; bp.stream = true;
+  }
   *out = bp;
+  return 0;
+}
+
+const void* latency_fwd_fn(const PersistArgs& a) {
+  const int bb = a.B <= 1 ? 1 : a.B <= 2 ? 2 : a.B <= 4 ? 4 : 8;
+  if (a.is_bf16) {
+    switch (bb) {
+      case 1: return reinterpret_cast<const void*>(&persist_fwd_latency_kernel<__nv_bfloat16, 1>);
+      case 2: return reinterpret_cast<const void*>(&persist_fwd_latency_kernel<__nv_bfloat16, 2>);
+      case 4: return reinterpret_cast<const void*>(&persist_fwd_latency_kernel<__nv_bfloat16, 4>);
+      default: return reinterpret_cast<const void*>(&persist_fwd_latency_kernel<__nv_bfloat16, 8>);
+    }
+  }
+  switch (bb) {
+    case 1: return reinterpret_cast<const void*>(&persist_fwd_latency_kernel<float, 1>);
+    case 2: return reinterpret_cast<const void*>(&persist_fwd_latency_kernel<float, 2>);
+    case 4: return reinterpret_cast<const void*>(&persist_fwd_latency_kernel<float, 4>);
+    default: return reinterpret_cast<const void*>(&persist_fwd_latency_kernel<float, 8>);
+  }
+}
+
+// Latency-mode forward (large weights, batch <= 8): one pair per thread, as
+// many weight rows resident in shared memory as fit.
+int launch_latency_fwd(const PersistArgs& a, cudaStream_t s, int num_sms) {
+  const int max_ctas = num_sms / a.ndir;
+  const int NU = (a.H + max_ctas - 1) / max_ctas;
+  if (NU * a.B > kThreads || 4 * NU > 8 * kLatRows) return 2;
+  const int nblk = (a.H + NU - 1) / NU;
+  const int bb = a.B <= 1 ? 1 : a.B <= 2 ? 2 : a.B <= 4 ? 4 : 8;
+  const size_t es = a.is_bf16 ? 2 : 4;
+  const size_t fixed = static_cast<size_t>(bb) * a.H * es + static_cast<size_t>(4) * NU * bb * 4 + 4 * NU * 4;
+  const size_t row_bytes = (static_cast<size_t>(a.H) + 16 / es) * es;
+  const size_t cap = 220 * 1024;
+  if (fixed > cap) return 2;
+  int Rs = static_cast<int>((cap - fixed) / row_bytes);
+  if (Rs > 4 * NU) Rs = 4 * NU;
+  const size_t smem = fixed + static_cast<size_t>(Rs) * row_bytes;
+  const void* fn = latency_fwd_fn(a);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return 3;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) return 3;
+  if (per_sm * num_sms < nblk * a.ndir) return 2;
+  PersistArgs args = a;
+  int nu = NU, rs = Rs;
+  void* params[] = {&args, &nu, &rs};
+  if (cudaLaunchKernel(fn, dim3(nblk, a.ndir), dim3(kThreads), params, smem, s) != cudaSuccess) return 3;
   return 0;
 }
 
@@ -532,8 +882,12 @@ int launch_simt(const PersistArgs& a, bool bwd, cudaStream_t s, int num_sms) {
   SimtPlan pl;
   int rc = make_plan(a, bwd, num_sms, &pl);
   if (rc) return rc;
-  const void* fn = a.is_bf16 ? (bwd ? SimtKernels<__nv_bfloat16>::bwd(pl.PP) : SimtKernels<__nv_bfloat16>::fwd(pl.PP))
-                             : (bwd ? SimtKernels<float>::bwd(pl.PP) : SimtKernels<float>::fwd(pl.PP));
+  const int span = 32 * (a.is_bf16 ? 8 : 4);
+  if (pl.stream && !bwd && a.B <= 8 && a.H % span == 0) {
+    rc = launch_latency_fwd(a, s, num_sms);
+    if (rc != 2) return rc;
+  }
+  const void* fn = kernel_for(a, bwd, pl);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) != cudaSuccess)
     return 3;
   int per_sm = 0;
@@ -548,6 +902,12 @@ int launch_simt(const PersistArgs& a, bool bwd, cudaStream_t s, int num_sms) {
 }
 
 }  // namespace
+
+#ifdef RNN_STEP_TRACE
+extern "C" int rnn_debug_read_lat_trace(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, g_lat_trace, bytes) == cudaSuccess ? 0 : 3;
+}
+#endif
 
 int plan_persist_simt(const PersistArgs& a, int num_sms, int* nblk, size_t* smem) {
   SimtPlan pf, pb;

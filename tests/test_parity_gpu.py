@@ -132,3 +132,22 @@ def test_full_lstm2bi_bf16_T512_B128_H1024_sampled():
     gpu = Hn.run_gpu(full)
     ref = Hn.run_oracle(synth.make_inputs(wl, batch_subset=keep))
     Hn.compare(gpu, ref, wl, batch_idx=keep)
+
+
+# ---------------------------------------------------------------------------
+# weights that do not fit on chip: the SIMT kernels stream them from L2
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("mode,ra", [("lstm", False), ("gru", False), ("gru", True)])
+def test_streamed_weights_fp32(mode, ra):
+    wl = _wl(mode, ra, 1, False, 4, 3, 16, 2048, "f32", 101, state_std=0.5)
+    inp = synth.make_inputs(wl)
+    Hn.compare(Hn.run_gpu(inp), Hn.run_oracle(inp), wl, tol=1e-5)
+
+
+@pytest.mark.parametrize("name,keep", [("gru_rb_bf16_T1024_B1_H2048", [0]), ("gru_rb_bf16_T1024_B8_H2048", [0, 7]),
+                                       ("lstm_bf16_T1024_B1_H2048", [0]), ("lstm_bf16_T1024_B8_H2048", [3, 6])])
+def test_full_latency_workloads_forward(name, keep):
+    wl = synth.WORKLOADS[name]
+    gpu = Hn.run_gpu(synth.make_inputs(wl), backward=False)
+    ref = Hn.run_oracle(synth.make_inputs(wl, batch_subset=keep), backward=False)
+    Hn.compare(gpu, ref, wl, batch_idx=keep)
