@@ -63,32 +63,30 @@ def _oracle_sample_cols(wl, target_s: float) -> int:
 
 def oracle_worker(spec: str) -> None:
     """Internal mode, run in a fresh process: time the oracle on a bounded
-    sample and print {"seconds": ..., "units": ..., "repeats": ...}."""
+    sample, at least ``reps`` times and until ``budget`` seconds have passed;
+    print {"times": [seconds per repeat], "units_per_rep": ...}."""
     import synth
     from oracle import rnn_oracle
-    name, cols, budget = spec.split(":")
+    name, cols, budget, reps = spec.split(":")
     wl = synth.WORKLOADS[name]
-    cols, budget = int(cols), float(budget)
+    cols, budget, reps = int(cols), float(budget), int(reps)
     inp = synth.make_inputs(wl, batch_subset=list(range(cols)))
-    reps, t_total = 0, 0.0
-    while True:
+    times = []
+    while len(times) < reps or sum(times) < budget:
         t0 = time.perf_counter()
         rnn_oracle.run_inputs(inp, with_backward=not wl.forward_only)
-        t_total += time.perf_counter() - t0
-        reps += 1
-        if t_total >= budget:
-            break
-    print(json.dumps({"seconds": t_total, "units": reps * wl.seq_len * cols, "repeats": reps}))
+        times.append(time.perf_counter() - t0)
+    print(json.dumps({"times": times, "units_per_rep": wl.seq_len * cols}))
 
 
-def run_oracle_subprocess(wl, budget_s: float, cols: int):
+def run_oracle_subprocess(wl, budget_s: float, cols: int, reps: int = 1):
     cores = os.cpu_count() or 1
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = str(cores)
     env["CUDA_VISIBLE_DEVICES"] = ""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample",
-                        f"{wl.name}:{cols}:{budget_s}"], capture_output=True, text=True, env=env, cwd=ROOT)
+                        f"{wl.name}:{cols}:{budget_s}:{reps}"], capture_output=True, text=True, env=env, cwd=ROOT)
     if r.returncode != 0:
         raise RuntimeError(f"oracle sample failed: {r.stderr[-2000:]}")
     out = json.loads(r.stdout.strip().splitlines()[-1])
@@ -147,6 +145,24 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (replicas: one per GPU, no data-path collective)
+# ---------------------------------------------------------------------------
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's time: the job is done when every replica is."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the max-over-ranks time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # algorithmic flop counts per kernel class (per whole step)
 # ---------------------------------------------------------------------------
 def class_flops(wl):
@@ -155,6 +171,41 @@ def class_flops(wl):
     proj = sum(D * 2.0 * G * H * wl.layer_input(l) * B * T for l in range(wl.num_layers))
     return {"persist_fwd": rec, "persist_bwd": rec, "gemm_proj": proj, "gemm_dx": proj,
             "gemm_dw": proj + rec, "layout": 0.0}
+
+
+PROFILE_FOR_CLASS = {
+    "persist_bwd": "profiles/persist_bwd_tc_{workload}.md",
+    "persist_fwd": "profiles/persist_fwd_tc_{workload}.md",
+}
+KERNEL_SOURCES = ["bwd_persistent_cta_gb300/csrc/persist_tc.cu", "bwd_persistent_cta_gb300/csrc/common.cuh"]
+
+
+def profiled_traffic(cls: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel source has changed since
+    the counters were taken."""
+    import hashlib
+    path = PROFILE_FOR_CLASS.get(cls)
+    if not path:
+        return None
+    path = os.path.join(ROOT, path.format(workload=workload))
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    sha = h.hexdigest()[:16]
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.split(":", 1)[0].strip() in ("traffic-bytes-per-launch", "kernel-source-sha256"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel-source-sha256") != sha:
+        return None
+    try:
+        return int(fields["traffic-bytes-per-launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def load_peaks():
@@ -249,11 +300,7 @@ def run_ours(args):
     R.rnn_set_timing(rnn.handle, False)
     launches = rnn.launches() - launches0
     cls_ms, cls_n = R.rnn_get_timing(rnn.handle)
-    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K, dist, dev)
 
     # --- end to end through the C ABI with host buffers --------------------
     xh = x.cpu().pin_memory()
@@ -275,15 +322,11 @@ def run_ours(args):
         e1.record()
         torch.cuda.synchronize()
         e_ms += e0.elapsed_time(e1)
-    e_ms /= Ke
-    if dist is not None:
-        t = torch.tensor([e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(e_ms / Ke, dist, dev)
     rnn.sync()
 
     units = wl.seq_len * wl.batch * world
-    value = units / (ms / 1e3)
+    value = job_throughput(wl.seq_len * wl.batch, world, ms)
     tflops = wl.flops() * world / (ms / 1e3) / 1e12
     peaks = load_peaks()
     names = R.TIMING_CLASS_NAMES
@@ -295,17 +338,21 @@ def run_ours(args):
     flops_per_launch = fl[names[dom]] / max(launches_per_step, 1)
     achieved = flops_per_launch / (per_launch_ms / 1e3) / 1e12
     roofline = {"kernel": names[dom], "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "traffic": profiled_traffic(names[dom], wl.name),
                 "peak_src": peaks["src"] + " bf16 burst", "share": cls_ms[dom] / max(sum(cls_ms), 1e-9),
                 "per_launch_ms": per_launch_ms, "per_class_ms_per_step": per_step}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cols = _oracle_sample_cols(wl, 3.0)
-        out, cores = run_oracle_subprocess(wl, 12.0, cols)
-        cpu = {"value": out["units"] / out["seconds"], "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{wl.name} with {cols} of {wl.batch} batch columns, fwd+bwd, "
-                         f"{out['repeats']} repeats in {out['seconds']:.1f} s (fp64 numpy)"}
+        out, cores = run_oracle_subprocess(wl, 12.0, cols, reps=2)
+        times = out["times"][1:]          # the first repeat warms the process up
+        cpu = {"value": out["units_per_rep"] * len(times) / sum(times), "unit": UNIT, "cores": cores,
+               "kind": "oracle",
+               "sample": f"{wl.name} with {cols} of {wl.batch} batch columns, "
+                         f"{'fwd' if wl.forward_only else 'fwd+bwd'}, {len(times)} timed repeats in "
+                         f"{sum(times):.1f} s after one warm-up (fp64 numpy, all host cores)"}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -317,7 +364,7 @@ def run_ours(args):
                        "seed": wl.seed, "parallelism": f"replicas{world}",
                        "l2": "flushed (256 MiB write) before every timed step"},
             "tflops": tflops, "tflops_unit": "TFLOP/s (algorithmic, sum over layers/dirs of 3*2*G*H*(I+H)*B*T)",
-            "e2e": {"value": units / (e_ms / 1e3), "unit": UNIT,
+            "e2e": {"value": job_throughput(wl.seq_len * wl.batch, world, e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": int(x.numel() * x.element_size() + dy.numel() * dy.element_size()),
                     "d2h_bytes_per_step": int(dw.numel() * dw.element_size())},
             "gpu_launches": int(launches), "gpu_launches_per_step": launches / K,
@@ -340,14 +387,9 @@ def run_reference(args):
         return
     wl = synth.WORKLOADS[args.workload]
     cols = _oracle_sample_cols(wl, 2.0)
-    per_step = []
-    units = 0
-    cores = os.cpu_count() or 1
-    for i in range(args.warmup + args.steps):
-        out, cores = run_oracle_subprocess(wl, 0.0, cols)
-        if i >= args.warmup:
-            per_step.append(out["seconds"])
-            units += out["units"]
+    out, cores = run_oracle_subprocess(wl, 0.0, cols, reps=args.warmup + args.steps)
+    per_step = out["times"][args.warmup:args.warmup + args.steps]
+    units = out["units_per_rep"] * len(per_step)
     secs = sum(per_step)
     value = units / secs
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
