@@ -149,17 +149,17 @@ __device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, 
 }
 
 // TMEM accumulator rows -> the owning peer's receive buffer
-// recv[src = this rank][column][row within the owner], by warps 0-3
-// (warp w may only address TMEM lanes 32w .. 32w+31).
+// recv[src = this rank][column][row within the owner].  Warps w and w + 4 read
+// the same TMEM lane quarter (32 * (w % 4) ..) and split the 32-column chunks.
 __device__ __forceinline__ void push_partials(const TcPersistParams& P, uint32_t tmem, float* recv, int ks) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp >= 4) return;
-  const int row = warp * 32 + lane;
+  const int q = warp & 3, half = warp >> 2;
+  const int row = q * 32 + lane;
   const int owner = row / P.RPC, lr = row - owner * P.RPC;
   float* dst = peer_ptr(recv, owner) + static_cast<size_t>(ks) * P.Npad * P.RPC + lr;
-  for (int c = 0; c < P.Npad; c += 32) {
+  for (int c = half * 32; c < P.Npad; c += 64) {
     float v[32];
-    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, v);
+    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (c + j < P.Npad) dst[(c + j) * P.RPC] = v[j];
@@ -230,6 +230,20 @@ __device__ __forceinline__ void step_arrive(const PersistArgs& a, bool skip, int
 
 __device__ __forceinline__ uint2 ld_u2(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
 
+// Explicit shared-memory loads: the compiler cannot mistake them for global
+// accesses that might alias the epilogue's stores, so they issue together.
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float lds_f1(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void unpack4(uint2 q, float (&v)[4]) {
   __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&q.x);
   __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&q.y);
@@ -278,7 +292,7 @@ __device__ __forceinline__ void teardown(const TcPersistParams& P, TcBars& bars)
 // ---------------------------------------------------------------------------
 // forward
 // ---------------------------------------------------------------------------
-template <int PP>
+template <int PP, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ TcPersistParams P) {
@@ -286,9 +300,10 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const PersistArgs& a = P.a;
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
   const int dir = a.dir0 + blockIdx.y;
-  const int ks = static_cast<int>(blockIdx.x) % P.KS;
-  const int rg = static_cast<int>(blockIdx.x) / P.KS;
+  const int ks = static_cast<int>(blockIdx.x) % KS;
+  const int rg = static_cast<int>(blockIdx.x) / KS;
   const bool lstm = a.mode == 0;
+  constexpr int RPC = 128 / KS;
 
   setup(P, &tmW, &tmX, wsm, bars, ks * P.Kc, dir * 4 * H + rg * 128);
   const uint32_t tmem = bars.tmem;
@@ -304,7 +319,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int npairs = UPC * B;
   const int ubase = rg * 32 + ks * UPC;     // first hidden unit of this CTA's epilogue
   const int slot_h0 = dir ? TT + 1 : 0;
-  const int src_stride = P.Npad * P.RPC;    // floats per source rank in recv
+  const uint32_t recv_s = smem_u32(recv);
+  const uint32_t src_bytes = static_cast<uint32_t>(P.Npad) * RPC * 4;   // bytes per source rank in recv
 
   float st[PP];
   float bh[PP][3];
@@ -346,6 +362,25 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     if (!step_exchange(P, &tmX, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B, idesc, adesc0, true,
                        static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_FWD_TC))
       break;
+    // partial sums of every pair first (all shared loads in flight), then the cell
+    float4 acc[PP];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      const int ul = id % UPC, b = id / UPC;
+      acc[p] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (id < npairs) {
+        const uint32_t ra = recv_s + static_cast<uint32_t>((b * RPC + 4 * ul) * 4);
+        float4 v[KS];
+#pragma unroll
+        for (int r = 0; r < KS; ++r) v[r] = lds_f4(ra + r * src_bytes);
+#pragma unroll
+        for (int r = 0; r < KS; ++r) {
+          acc[p].x += v[r].x; acc[p].y += v[r].y; acc[p].z += v[r].z; acc[p].w += v[r].w;
+        }
+      }
+    }
+    RNN_TRACE_AT(12, 0, s);
     float hv[PP];
     float gq[PP][4];
 #pragma unroll
@@ -354,31 +389,22 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       hv[p] = 0.f;
       if (id >= npairs) break;
       const int ul = id % UPC, b = id / UPC, u = ubase + ul;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float* rp = recv + b * P.RPC + 4 * ul;
-#pragma unroll
-      for (int r = 0; r < kMaxKS; ++r) {
-        if (r < P.KS) {
-          const float4 v = *reinterpret_cast<const float4*>(rp + r * src_stride);
-          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-        }
-      }
       float pv[4];
       unpack4(pq[p], pv);
       float h;
       if (lstm) {
-        const float i = sigm_fast(pv[0] + acc.x);
-        const float f = sigm_fast(pv[1] + acc.y);
-        const float gg = tanh_fast(pv[2] + acc.z);
-        const float o = sigm_fast(pv[3] + acc.w);
+        const float i = sigm_fast(pv[0] + acc[p].x);
+        const float f = sigm_fast(pv[1] + acc[p].y);
+        const float gg = tanh_fast(pv[2] + acc[p].z);
+        const float o = sigm_fast(pv[3] + acc[p].w);
         const float c = f * st[p] + i * gg;
         h = o * tanh_fast(c);
         st[p] = c;
         pv[0] = i; pv[1] = f; pv[2] = gg; pv[3] = o;
       } else {
-        const float r = sigm_fast(pv[0] + acc.x + bh[p][0]);
-        const float z = sigm_fast(pv[1] + acc.y + bh[p][1]);
-        const float hn = acc.z + bh[p][2];
+        const float r = sigm_fast(pv[0] + acc[p].x + bh[p][0]);
+        const float z = sigm_fast(pv[1] + acc[p].y + bh[p][1]);
+        const float hn = acc[p].z + bh[p][2];
         const float n = tanh_fast(pv[2] + r * hn);
         h = (1.f - z) * n + z * st[p];
         st[p] = h;
@@ -388,6 +414,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       gq[p][0] = pv[0]; gq[p][1] = pv[1]; gq[p][2] = pv[2]; gq[p][3] = pv[3];
       Y[(static_cast<int64_t>(so) * B + b) * ldY + dir * H + u] = __float2bfloat16_rn(h);
     }
+    RNN_TRACE_AT(13, 0, s);
     RNN_TRACE_AT(5, 0, s);
     step_arrive(a, skip, s, 0);
     RNN_TRACE_AT(6, 0, s);
@@ -412,7 +439,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 // ---------------------------------------------------------------------------
 // backward through time
 // ---------------------------------------------------------------------------
-template <int PP>
+template <int PP, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ TcPersistParams P) {
@@ -421,9 +448,10 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
   const int K4 = 4 * H;
   const int dir = a.dir0 + blockIdx.y;
-  const int ks = static_cast<int>(blockIdx.x) % P.KS;
-  const int rg = static_cast<int>(blockIdx.x) / P.KS;
+  const int ks = static_cast<int>(blockIdx.x) % KS;
+  const int rg = static_cast<int>(blockIdx.x) / KS;
   const bool lstm = a.mode == 0;
+  constexpr int RPC = 128 / KS;
 
   setup(P, &tmW, &tmX, wsm, bars, ks * P.Kc, dir * H + rg * 128);
   const uint32_t tmem = bars.tmem;
@@ -439,7 +467,8 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int UPC = P.UPC;
   const int npairs = UPC * B;
   const int ubase = rg * 128 + ks * UPC;
-  const int src_stride = P.Npad * P.RPC;
+  const uint32_t recv_s = smem_u32(recv);
+  const uint32_t src_bytes = static_cast<uint32_t>(P.Npad) * RPC * 4;
 
   float carry[PP], db[PP][4];
 #pragma unroll
@@ -488,21 +517,34 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       aborted = true;
       break;
     }
+    // recurrent gradient of every pair first (all shared loads in flight)
+    float dhs[PP];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      dhs[p] = 0.f;
+      if (id < npairs) {
+        if (s == 0) {
+          if (a.dhT)
+            dhs[p] = __bfloat162float(
+                static_cast<const __nv_bfloat16*>(a.dhT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
+        } else {
+          const uint32_t ra = recv_s + static_cast<uint32_t>((b * RPC + ul) * 4);
+          float v[KS];
+#pragma unroll
+          for (int r = 0; r < KS; ++r) v[r] = lds_f1(ra + r * src_bytes);
+#pragma unroll
+          for (int r = 0; r < KS; ++r) dhs[p] += v[r];
+        }
+      }
+    }
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
       if (id >= npairs) break;
       const int ul = id % UPC, b = id / UPC, u = ubase + ul;
-      float dhr = 0.f;
-      if (s == 0) {
-        if (a.dhT)
-          dhr = __bfloat162float(static_cast<const __nv_bfloat16*>(a.dhT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
-      } else {
-        const float* rp = recv + b * P.RPC + ul;
-#pragma unroll
-        for (int r = 0; r < kMaxKS; ++r)
-          if (r < P.KS) dhr += rp[r * src_stride];
-      }
+      const float dhr = dhs[p];
       if (s == TT) {
         const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
         if (a.dh0) static_cast<__nv_bfloat16*>(a.dh0)[o] = __float2bfloat16_rn(lstm ? dhr : dhr + carry[p]);
@@ -546,7 +588,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     // bias gradients: reduce each unit's four sums over the batch (reuses recv,
     // after every peer has finished with it)
     tc_fence_before();
-    if (P.KS > 1) cluster_sync(); else __syncthreads();
+    if (KS > 1) cluster_sync(); else __syncthreads();
     float* red = recv;
     for (int i = threadIdx.x; i < 4 * UPC; i += kThreads) red[i] = 0.f;
     __syncthreads();
@@ -570,20 +612,40 @@ int pp_for(int pairs) {
   return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : 0;
 }
 
-const void* fwd_fn(int pp) {
+template <int KS>
+const void* fwd_fn_ks(int pp) {
   switch (pp) {
-    case 1: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<1>);
-    case 2: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<2>);
-    case 4: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<4>);
-    default: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<8>);
+    case 1: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<1, KS>);
+    case 2: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<2, KS>);
+    case 4: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<4, KS>);
+    default: return reinterpret_cast<const void*>(&persist_fwd_tc_kernel<8, KS>);
   }
 }
-const void* bwd_fn(int pp) {
+template <int KS>
+const void* bwd_fn_ks(int pp) {
   switch (pp) {
-    case 1: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<1>);
-    case 2: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<2>);
-    case 4: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<4>);
-    default: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<8>);
+    case 1: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<1, KS>);
+    case 2: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<2, KS>);
+    case 4: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<4, KS>);
+    default: return reinterpret_cast<const void*>(&persist_bwd_tc_kernel<8, KS>);
+  }
+}
+const void* fwd_fn(int pp, int ks) {
+  switch (ks) {
+    case 1: return fwd_fn_ks<1>(pp);
+    case 2: return fwd_fn_ks<2>(pp);
+    case 4: return fwd_fn_ks<4>(pp);
+    case 8: return fwd_fn_ks<8>(pp);
+    default: return fwd_fn_ks<16>(pp);
+  }
+}
+const void* bwd_fn(int pp, int ks) {
+  switch (ks) {
+    case 1: return bwd_fn_ks<1>(pp);
+    case 2: return bwd_fn_ks<2>(pp);
+    case 4: return bwd_fn_ks<4>(pp);
+    case 8: return bwd_fn_ks<8>(pp);
+    default: return bwd_fn_ks<16>(pp);
   }
 }
 
@@ -645,7 +707,7 @@ int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int ma
   return n;
 }
 
-const void* kernel_for(int bwd, int pp) { return bwd ? bwd_fn(pp) : fwd_fn(pp); }
+const void* kernel_for(int bwd, int pp, int ks) { return bwd ? bwd_fn(pp, ks) : fwd_fn(pp, ks); }
 
 void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPlan& pl, int ndir, cudaStream_t s) {
   cfg = cudaLaunchConfig_t{};
@@ -667,7 +729,7 @@ bool choose_plan(int bwd, int H, int B, int ndir, int num_sms, TcPlan* chosen) {
   const int n = make_plans(bwd, H, B, ndir, num_sms, plans, 5);
   for (int i = 0; i < n; ++i) {
     const TcPlan& pl = plans[i];
-    const void* fn = kernel_for(bwd, pl.PP);
+    const void* fn = kernel_for(bwd, pl.PP, pl.KS);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -718,7 +780,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   P.nblk_dir = static_cast<unsigned int>(pl.nrg * pl.KS);
   P.tmem_cols = pl.tmem_cols;
   P.off_ring = pl.off_ring; P.off_recv = pl.off_recv; P.off_bar = pl.off_bar;
-  const void* fn = kernel_for(bwd, pl.PP);
+  const void* fn = kernel_for(bwd, pl.PP, pl.KS);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   fill_config(cfg, attr, pl, a.ndir, s);
