@@ -71,10 +71,14 @@ constexpr int kMaxKS = 16;
 constexpr int kMaxRing = 16;
 constexpr size_t kSmemCap = 227 * 1024;
 constexpr size_t kMinSmem = 80 * 1024;    // at most two CTAs per SM: TMEM (<= 256 cols each) fits
+constexpr size_t kOneCtaSmem = 116 * 1024; // one CTA per SM (it holds all 512 TMEM columns)
 
 struct TcPersistParams {
   PersistArgs a;
   int KS, Kc, nsub, R, Npad, UPC, RPC;
+  int w_tmem;              // weight tile in tensor memory (A operand from TMEM) instead of shared memory
+  int single;              // the whole K slice arrives with one 4-D TMA per step (R == nsub)
+  uint32_t wcol;           // first TMEM column of the weight tile (w_tmem)
   unsigned int nblk_dir;   // CTAs per direction
   uint32_t tmem_cols;
   uint32_t off_ring, off_recv, off_bar;
@@ -105,15 +109,54 @@ __device__ __forceinline__ T* peer_ptr(T* p, int rank) {
   return reinterpret_cast<T*>(g);
 }
 
-// One step's contraction: stream nsub sub-tiles of the exchange operand
-// through the ring and accumulate into TMEM.  Called by thread 0 only.
-// g: running sub-tile load counter (across steps).  Returns false on timeout.
-__device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, uint8_t* ring, TcBars& bars,
-                              uint32_t tmem, uint32_t& g, int x0, int y0, uint32_t idesc, uint64_t adesc0,
-                              bool first_use_w) {
+// The MMAs of sub-tile j (64 K columns) of the K slice, exchange operand in
+// ring slot ``slot``.
+__device__ __forceinline__ void mma_subtile(const TcPersistParams& P, uint32_t tmem, uint64_t adesc0,
+                                            uint64_t bdesc0, uint32_t rbytes, uint32_t idesc, int j, int slot) {
+  const uint64_t bd = bdesc0 + static_cast<uint64_t>((slot * rbytes) >> 4);
+  if (P.w_tmem) {
+    // K=16 bf16 = 8 TMEM columns
+    const uint32_t at = tmem + P.wcol + static_cast<uint32_t>(j * (kSubK / 2));
+#pragma unroll
+    for (int k = 0; k < kSubK / 16; ++k) mma_bf16_ts(tmem, at + 8 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
+  } else {
+    const uint64_t ad = adesc0 + static_cast<uint64_t>((j * kWSub) >> 4);
+#pragma unroll
+    for (int k = 0; k < kSubK / 16; ++k)   // +32 bytes per K=16 step inside the swizzle atom
+      mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
+  }
+}
+
+// One step's contraction: bring the exchange operand's K slice into shared
+// memory and accumulate into TMEM.  Called by thread 0 only.  Either one 4-D
+// TMA brings the whole slice (chunk j at ring + j * rbytes), or nsub 2-D loads
+// stream through a ring of R slots.  g: running load counter (across steps).
+// (x0, y0): 2-D coordinates of the slice; (c2, dir): its chunk and direction
+// coordinates in the 4-D view.  Returns false on timeout.
+__device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, const CUtensorMap* tmX4,
+                              uint8_t* ring, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0, int c2,
+                              int dir, uint32_t idesc, uint64_t adesc0, bool first_use_w, int tk, int s) {
+  (void)tk; (void)s;
   const int nsub = P.nsub, R = P.R;
   const uint32_t rbytes = static_cast<uint32_t>(P.Npad) * 128;
   const uint64_t to = P.a.timeout_ns;
+  const uint64_t bdesc0 = sdesc_sw128(smem_u32(ring), 16, 1024);
+  if (P.single) {
+    // the previous step's MMAs on the ring finished before this CTA released
+    // that step, and every CTA's did before the counter let this load start
+    mbar_arrive_expect_tx(&bars.full[0], static_cast<uint32_t>(nsub) * rbytes);
+    tma_load_4d(ring, tmX4, &bars.full[0], 0, y0, c2, dir);
+    RNN_TRACE_AT(1, tk, s);
+    if (first_use_w && !P.w_tmem && !mbar_wait(&bars.wbar, 0, to)) return false;
+    if (!mbar_wait(&bars.full[0], g & 1, to)) return false;
+    RNN_TRACE_AT(8, tk, s);
+    RNN_TRACE_AT(14, tk, s);
+    tc_fence_after();
+    for (int j = 0; j < nsub; ++j) mma_subtile(P, tmem, adesc0, bdesc0, rbytes, idesc, j, j);
+    mma_commit(&bars.mma);
+    g += 1;
+    return true;
+  }
   const uint32_t g0 = g;
   for (int j = 0; j < nsub && j < R; ++j) {
     const uint32_t gg = g0 + j;
@@ -122,18 +165,16 @@ __device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, 
     mbar_arrive_expect_tx(&bars.full[slot], rbytes);
     tma_load_2d(ring + slot * rbytes, tmX, &bars.full[slot], x0 + j * kSubK, y0);
   }
-  if (first_use_w && !mbar_wait(&bars.wbar, 0, to)) return false;
-  const uint64_t bdesc0 = sdesc_sw128(smem_u32(ring), 16, 1024);
+  RNN_TRACE_AT(1, tk, s);
+  if (first_use_w && !P.w_tmem && !mbar_wait(&bars.wbar, 0, to)) return false;
   for (int j = 0; j < nsub; ++j) {
     const uint32_t gg = g0 + j;
     const int slot = gg % R;
     if (!mbar_wait(&bars.full[slot], (gg / R) & 1, to)) return false;
+    if (j == 0) RNN_TRACE_AT(8, tk, s);
+    if (j == nsub - 1) RNN_TRACE_AT(14, tk, s);
     tc_fence_after();
-    const uint64_t ad = adesc0 + static_cast<uint64_t>((j * kWSub) >> 4);
-    const uint64_t bd = bdesc0 + static_cast<uint64_t>((slot * rbytes) >> 4);
-#pragma unroll
-    for (int k = 0; k < kSubK / 16; ++k)   // +32 bytes per K=16 step inside the swizzle atom
-      mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
+    mma_subtile(P, tmem, adesc0, bdesc0, rbytes, idesc, j, slot);
     mma_commit(&bars.empty[slot]);
     const int jn = j + R;
     if (jn < nsub) {
@@ -169,8 +210,9 @@ __device__ __forceinline__ void push_partials(const TcPersistParams& P, uint32_t
 // The per-step exchange and contraction, up to the point where this CTA's
 // units' summed pre-activations can be read from ``recv``.  Returns true when
 // the whole cluster may continue.
-__device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, uint8_t* ring, float* recv,
-                              TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0, uint32_t idesc,
+__device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, const CUtensorMap* tmX4,
+                              uint8_t* ring, float* recv, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0,
+                              int c2, int dir, uint32_t idesc,
                               uint64_t adesc0, bool do_contract, unsigned int wait_target, int s, int ks, int& n_mma,
                               bool& w_waited, unsigned int kernel) {
   const PersistArgs& a = P.a;
@@ -184,8 +226,7 @@ __device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, 
     }
     RNN_TRACE_AT(7, tk, s);
     if (ok && do_contract) {
-      fence_proxy_async_global();
-      if (!contract_step(P, tmX, ring, bars, tmem, g, x0, y0, idesc, adesc0, !w_waited)) {
+      if (!contract_step(P, tmX, tmX4, ring, bars, tmem, g, x0, y0, c2, dir, idesc, adesc0, !w_waited, tk, s)) {
         ok = 0;
         report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_TMA);
       }
@@ -219,10 +260,15 @@ __device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, 
   return any == 0;
 }
 
-// After the exchange-critical stores of a step: every thread's stores are
-// ordered before the release add by the barrier.
+// After the exchange-critical stores of a step.  Each thread orders its own
+// generic-proxy stores before the TMA (async-proxy) reads that other CTAs issue
+// once they observe the counter; the barrier orders every thread's stores
+// before the release add.  Fencing here, on the writer side, keeps the fence
+// off the reader's critical path, where it would also wait for the reader's
+// own outstanding prefetch loads.
 __device__ __forceinline__ void step_arrive(const PersistArgs& a, bool skip, int s, int tk) {
   (void)s; (void)tk;
+  fence_proxy_async_global();
   __syncthreads();
   RNN_TRACE_AT(11, tk, s);
   if (threadIdx.x == 0 && !skip) red_release_gpu_add(&a.dev->counters[a.dir0 + blockIdx.y], 1u);
@@ -251,18 +297,25 @@ __device__ __forceinline__ void unpack4(uint2 q, float (&v)[4]) {
   v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
 }
 
+// Barriers, TMEM, and the resident weight tile: 128 rows from row wy0, K
+// columns from column wx0 of the packed weight matrix w (leading dimension
+// ldw), either by TMA into shared memory or, with w_tmem, by every thread
+// through registers into TMEM columns [wcol, wcol + Kc/2) (lane = row).
 __device__ __forceinline__ void setup(const TcPersistParams& P, const CUtensorMap* tmW, const CUtensorMap* tmX,
-                                      uint8_t* wsm, TcBars& bars, int wx0, int wy0) {
+                                      const CUtensorMap* tmX4, uint8_t* wsm, TcBars& bars, int wx0, int wy0,
+                                      const __nv_bfloat16* w, int64_t ldw) {
   if (threadIdx.x == 0) {
     mbar_init(&bars.wbar, 1);
     mbar_init(&bars.mma, 1);
     for (int i = 0; i < P.R; ++i) { mbar_init(&bars.full[i], 1); mbar_init(&bars.empty[i], 1); }
     fence_mbar_init();
     fence_proxy_async_smem();
-    prefetch_tmap(tmW);
-    prefetch_tmap(tmX);
-    mbar_arrive_expect_tx(&bars.wbar, static_cast<uint32_t>(P.nsub) * kWSub);
-    for (int j = 0; j < P.nsub; ++j) tma_load_2d(wsm + j * kWSub, tmW, &bars.wbar, wx0 + j * kSubK, wy0);
+    if (P.single) prefetch_tmap(tmX4); else prefetch_tmap(tmX);
+    if (!P.w_tmem) {
+      prefetch_tmap(tmW);
+      mbar_arrive_expect_tx(&bars.wbar, static_cast<uint32_t>(P.nsub) * kWSub);
+      for (int j = 0; j < P.nsub; ++j) tma_load_2d(wsm + j * kWSub, tmW, &bars.wbar, wx0 + j * kSubK, wy0);
+    }
   }
   if ((threadIdx.x >> 5) == 0) {
     tmem_alloc(&bars.tmem, P.tmem_cols);
@@ -271,6 +324,26 @@ __device__ __forceinline__ void setup(const TcPersistParams& P, const CUtensorMa
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (P.w_tmem) {
+    // warps w and w + 4 share lane quarter w % 4 and split the K columns
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, half = warp >> 2;
+    const int ncol = P.Kc / 4;   // 32-bit columns per half
+    const __nv_bfloat16* src = w + (static_cast<int64_t>(wy0) + q * 32 + lane) * ldw + wx0 + half * (P.Kc / 2);
+    const uint32_t trow = bars.tmem + (static_cast<uint32_t>(q * 32) << 16) + P.wcol + static_cast<uint32_t>(half * ncol);
+    for (int c = 0; c < ncol; c += 32) {
+      const uint4* p4 = reinterpret_cast<const uint4*>(src + 2 * c);
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = p4[i];
+        r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+      }
+      tmem_st_32x32b_x32(trow + c, r);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
 }
 
 __device__ __forceinline__ void teardown(const TcPersistParams& P, TcBars& bars) {
@@ -295,7 +368,7 @@ __device__ __forceinline__ void teardown(const TcPersistParams& P, TcBars& bars)
 template <int PP, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                      const __grid_constant__ TcPersistParams P) {
+                      const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ TcPersistParams P) {
   RNN_TC_SMEM_VIEW;
   const PersistArgs& a = P.a;
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
@@ -305,7 +378,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const bool lstm = a.mode == 0;
   constexpr int RPC = 128 / KS;
 
-  setup(P, &tmW, &tmX, wsm, bars, ks * P.Kc, dir * 4 * H + rg * 128);
+  setup(P, &tmW, &tmX, &tmX4, wsm, bars, ks * P.Kc, dir * 4 * H + rg * 128, static_cast<const __nv_bfloat16*>(a.Wr),
+        H);
   const uint32_t tmem = bars.tmem;
   const uint32_t idesc = idesc_bf16(128, P.Npad, false, false);
   const uint64_t adesc0 = sdesc_sw128(smem_u32(wsm), 16, 1024);
@@ -359,7 +433,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       const int ul = id % UPC, b = id / UPC, u = ubase + ul;
       pq[p] = id < npairs ? ld_u2(Pm + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u) : make_uint2(0, 0);
     }
-    if (!step_exchange(P, &tmX, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B, idesc, adesc0, true,
+    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B, ks * P.nsub, dir, idesc,
+                       adesc0, true,
                        static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_FWD_TC))
       break;
     // partial sums of every pair first (all shared loads in flight), then the cell
@@ -442,7 +517,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 template <int PP, int KS>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                      const __grid_constant__ TcPersistParams P) {
+                      const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ TcPersistParams P) {
   RNN_TC_SMEM_VIEW;
   const PersistArgs& a = P.a;
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
@@ -453,7 +528,8 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const bool lstm = a.mode == 0;
   constexpr int RPC = 128 / KS;
 
-  setup(P, &tmW, &tmX, wsm, bars, ks * P.Kc, dir * H + rg * 128);
+  setup(P, &tmW, &tmX, &tmX4, wsm, bars, ks * P.Kc, dir * H + rg * 128, static_cast<const __nv_bfloat16*>(a.WrT),
+        4 * H);
   const uint32_t tmem = bars.tmem;
   const uint32_t idesc = idesc_bf16(128, P.Npad, false, false);
   const uint64_t adesc0 = sdesc_sw128(smem_u32(wsm), 16, 1024);
@@ -512,8 +588,8 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         }
       }
     }
-    if (!step_exchange(P, &tmX, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B, idesc,
-                       adesc0, s > 0, static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_BWD_TC)) {
+    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B,
+                       ks * P.nsub, dir, idesc, adesc0, s > 0, static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_BWD_TC)) {
       aborted = true;
       break;
     }
@@ -650,7 +726,7 @@ const void* bwd_fn(int pp, int ks) {
 }
 
 struct TcPlan {
-  int KS = 0, Kc = 0, nsub = 0, R = 0, Npad = 0, UPC = 0, PP = 0, nrg = 0;
+  int KS = 0, Kc = 0, nsub = 0, R = 0, Npad = 0, UPC = 0, PP = 0, nrg = 0, w_tmem = 0;
   uint32_t tmem_cols = 0, off_ring = 0, off_recv = 0, off_bar = 0;
   size_t smem = 0;
 };
@@ -686,22 +762,38 @@ int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int ma
     const size_t wbytes = static_cast<size_t>(nsub) * kWSub;
     const size_t rb = static_cast<size_t>(Npad) * 128;
     const size_t recv = static_cast<size_t>(Npad) * 128 * 4;
+    // weight tile in shared memory, with the deepest exchange ring that fits
     int R = nsub < kMaxRing ? nsub : kMaxRing;
     size_t smem = 0;
     for (; R >= 1; --R) {
       smem = a1k(wbytes) + a1k(R * rb) + a1k(recv) + a1k(sizeof(TcBars)) + 1024;
       if (smem <= kSmemCap) break;
     }
-    if (R < 1 || (R < nsub && R < 2)) continue;
+    bool w_tmem = false;
+    if (R < nsub && Kc % 128 == 0 && Kc / 2 <= 256 && Npad <= 256) {
+      // weight tile in TMEM columns [256, 256 + Kc/2) instead: the whole K
+      // slice of the exchange operand then fits in flight at once
+      const size_t sm2 = a1k(static_cast<size_t>(nsub) * rb) + a1k(recv) + a1k(sizeof(TcBars)) + 1024;
+      if (sm2 <= kSmemCap) {
+        w_tmem = true;
+        R = nsub;
+        smem = sm2;
+      }
+    }
+    if (!w_tmem && (R < 1 || (R < nsub && R < 2))) continue;
     TcPlan p;
     p.KS = KS; p.Kc = Kc; p.nsub = nsub; p.R = R; p.Npad = Npad; p.UPC = UPC; p.PP = PP; p.nrg = nrg;
+    p.w_tmem = w_tmem ? 1 : 0;
     uint32_t tc = 32;
     while (tc < static_cast<uint32_t>(Npad)) tc *= 2;
-    p.tmem_cols = tc;
-    p.off_ring = static_cast<uint32_t>(a1k(wbytes));
+    p.tmem_cols = w_tmem ? 512 : tc;
+    p.off_ring = w_tmem ? 0 : static_cast<uint32_t>(a1k(wbytes));
     p.off_recv = p.off_ring + static_cast<uint32_t>(a1k(R * rb));
     p.off_bar = p.off_recv + static_cast<uint32_t>(a1k(recv));
-    p.smem = smem < kMinSmem ? kMinSmem : smem;
+    // all 512 TMEM columns: the shared-memory request alone must keep a
+    // second CTA off the SM
+    const size_t floor = w_tmem ? kOneCtaSmem : kMinSmem;
+    p.smem = smem < floor ? floor : smem;
     out[n++] = p;
   }
   return n;
@@ -759,7 +851,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   TcPlan pl;
   if (!choose_plan(bwd, a.H, a.B, a.ndir, num_sms, &pl)) return 2;
   const int H = a.H, D = a.D;
-  CUtensorMap tmW, tmX;
+  CUtensorMap tmW, tmX, tmX4;
   int rc;
   if (!bwd) {
     rc = make_tmap_bf16_2d(&tmW, a.Wr, H, static_cast<uint64_t>(D) * 4 * H, H, kSubK, 128);
@@ -773,6 +865,20 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
                            static_cast<uint64_t>(D) * 4 * H, kSubK, pl.Npad);
   }
   if (rc) return rc;
+  // 4-D view of the exchange operand: (64 columns, row, 64-column chunk,
+  // direction), so that one box {64, Npad, nsub, 1} lands as nsub consecutive
+  // swizzled 64-column sub-tiles
+  int single = pl.R >= pl.nsub ? 1 : 0;
+  if (single) {
+    const uint64_t Kd = bwd ? 4ull * H : static_cast<uint64_t>(H);
+    const uint64_t rows = bwd ? static_cast<uint64_t>(a.T) * a.B : static_cast<uint64_t>(a.T + 2) * a.B;
+    const uint64_t dims[4] = {static_cast<uint64_t>(kSubK), rows, Kd / kSubK, static_cast<uint64_t>(D)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(D) * Kd * 2, static_cast<uint64_t>(kSubK) * 2, Kd * 2};
+    const uint32_t box[4] = {static_cast<uint32_t>(kSubK), static_cast<uint32_t>(pl.Npad),
+                             static_cast<uint32_t>(pl.nsub), 1u};
+    if (make_tmap_bf16_4d(&tmX4, bwd ? a.dG : a.Y, dims, strides, box) != 0) single = 0;
+  }
+  if (!single) tmX4 = tmX;
   TcPersistParams P;
   P.a = a;
   P.KS = pl.KS; P.Kc = pl.Kc; P.nsub = pl.nsub; P.R = pl.R; P.Npad = pl.Npad; P.UPC = pl.UPC;
@@ -780,11 +886,14 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   P.nblk_dir = static_cast<unsigned int>(pl.nrg * pl.KS);
   P.tmem_cols = pl.tmem_cols;
   P.off_ring = pl.off_ring; P.off_recv = pl.off_recv; P.off_bar = pl.off_bar;
+  P.w_tmem = pl.w_tmem;
+  P.single = single;
+  P.wcol = 256;
   const void* fn = kernel_for(bwd, pl.PP, pl.KS);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   fill_config(cfg, attr, pl, a.ndir, s);
-  void* params[] = {&tmW, &tmX, &P};
+  void* params[] = {&tmW, &tmX, &tmX4, &P};
   if (cudaLaunchKernelExC(&cfg, fn, params) != cudaSuccess) return 3;
   return 0;
 }

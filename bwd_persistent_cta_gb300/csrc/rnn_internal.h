@@ -108,6 +108,10 @@ int launch_persist_bwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms);
 // ptr[j * ld + i], i < dim0, j < dim1, box box0 x box1, 128-byte swizzle.
 int make_tmap_bf16_2d(void* map, const void* ptr, uint64_t dim0, uint64_t dim1, uint64_t ld_elems,
                       uint32_t box0, uint32_t box1);
+// 4-D view: element (i0..i3) at 2*i0 + i1*strides[0] + i2*strides[1] + i3*strides[2]
+// bytes; box[0] * 2 == 128 (the swizzle span).
+int make_tmap_bf16_4d(void* map, const void* ptr, const uint64_t* dims, const uint64_t* strides_bytes,
+                      const uint32_t* box);
 
 // layout / cast / pack kernels (layout.cu)
 // slot_src[s] = index of the user's gate block for internal slot s (-1 = zero)

@@ -1,4 +1,4 @@
-// tmap.cpp - host-side TMA tensor-map encoding (bf16, 2-D, 128-byte swizzle).
+// tmap.cpp - host-side TMA tensor-map encoding (bf16, 2-D and 4-D, 128-byte swizzle).
 // The driver entry point is looked up at run time through the CUDA runtime,
 // so the library has no link-time dependency on the driver library.
 #include <cuda.h>
@@ -39,6 +39,29 @@ int make_tmap_bf16_2d(void* map, const void* ptr, uint64_t dim0, uint64_t dim1, 
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : 2;
+}
+
+// Four-dimensional view of bf16 data: element (i0, i1, i2, i3) at byte
+// offset 2*i0 + i1*stride1 + i2*stride2 + i3*stride3 (strides in bytes, any
+// order, multiples of 16); the box is box[0..3] elements with box[0]*2 == 128.
+int make_tmap_bf16_4d(void* map, const void* ptr, const uint64_t* dims, const uint64_t* strides_bytes,
+                      const uint32_t* box) {
+  std::call_once(g_once, lookup);
+  if (!g_encode) return 3;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0) return 2;
+  cuuint64_t d[4];
+  cuuint64_t st[3];
+  cuuint32_t b[4];
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 4; ++i) { d[i] = dims[i]; b[i] = box[i]; }
+  for (int i = 0; i < 3; ++i) {
+    if (strides_bytes[i] % 16 != 0) return 2;
+    st[i] = strides_bytes[i];
+  }
+  CUresult r = g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), d,
+                        st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : 2;
 }
