@@ -159,7 +159,11 @@ int run_gemm(rnn_handle_s* h, GemmArgs g, cudaStream_t s, int cls) {
   TimeScope ts(h, cls, s);
   if (g.K <= 0) return 2;
   g.in_bf16 = h->bf16;
-  if (h->bf16 && gemm_tc_supported(g)) return count(h, launch_gemm_tc(g, s, h->num_sms, h->dev, h->timeout_ns));
+  if (h->bf16 && gemm_tc_supported(g)) {
+    int n = 1;
+    const int rc = launch_gemm_tc(g, s, h->num_sms, h->dev, h->timeout_ns, &n);
+    return count(h, rc, n);
+  }
   return count(h, launch_gemm_simt(g, s));
 }
 
@@ -604,6 +608,9 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
       g.M = 4 * H; g.K = static_cast<int>(TB);
       g.A = dG; g.lda = D * 4 * H; g.a_kmajor = 0;
       g.rowmap_H = H;
+      // long K = T*B: the projection buffer (idle here) holds split-K partials
+      g.split_ws = at<char>(workspace, h->w_p);
+      g.split_ws_bytes = TB * D * 4 * H * es;
       // dW_ih = sum over (t, b) of dG x^T
       g.N = Il;
       g.B = Xl; g.ldb = Il; g.b_kmajor = 0;
@@ -652,6 +659,22 @@ extern "C" rnn_status_t rnn_debug_gemm(int M, int N, int K, const void* A, int64
   for (int k = 0; k < 4; ++k) g.perm[k] = perm ? perm[k] : k;
   g.in_bf16 = in_bf16;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // scratch for a K split of fp32 outputs, as the weight gradients get (kept
+  // across calls, grown on demand; only this test hook allocates it)
+  static void* ws = nullptr;
+  static size_t ws_bytes = 0;
+  if (!c_bf16 && use_tc) {
+    const size_t need = static_cast<size_t>(16) * M * N * sizeof(float);
+    if (need > ws_bytes) {
+      if (ws) cudaFree(ws);
+      ws = nullptr;
+      ws_bytes = 0;
+      if (cudaMalloc(&ws, need) != cudaSuccess) return RNN_CUDA_ERROR;
+      ws_bytes = need;
+    }
+    g.split_ws = ws;
+    g.split_ws_bytes = ws_bytes;
+  }
   static DevArea* dev = nullptr;
   if (!dev) {
     if (cudaMalloc(&dev, sizeof(DevArea)) != cudaSuccess) return RNN_CUDA_ERROR;

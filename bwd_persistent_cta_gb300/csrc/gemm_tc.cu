@@ -7,36 +7,52 @@
 //   weight gradients  dW = dG^T * [X | H_prev] (basicLstmParamUpdate /
 //                                              basicGruParamUpdate, one long-K GEMM)
 //
-// Structure: a persistent kernel, one CTA per SM, 128 x 128 output tiles,
-// 64-deep K slices in a 4-stage shared-memory ring.
+// Structure: a persistent kernel, one CTA per SM, 128 x BN output tiles
+// (BN = 256, or 128 when 256-wide tiles would leave most SMs idle), 64-deep K
+// slices in a shared-memory ring (4 x 48 KB or 6 x 32 KB).
 //   warp 0       TMA producer (one elected thread)
-//   warp 1       TMEM owner and MMA issuer (one elected thread); M=128, N=128,
+//   warp 1       TMEM owner and MMA issuer (one elected thread); M=128, N=BN,
 //                K=16 per tcgen05.mma, 128-byte swizzled operands
 //   warps 2..5   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //                lanes 32*(w%4) .. +31 = tile rows), bias / accumulate / cast,
 //                global stores with the gate-slot row remap
-// Two TMEM accumulators (2 x 128 columns) let the epilogue of one tile overlap
+// Two TMEM accumulators (2 x BN columns) let the epilogue of one tile overlap
 // the main loop of the next.  Operands may be K-major (row = M or N index, K
 // contiguous) or MN-major (K = row index, M or N contiguous); the descriptor
-// major-ness bits select which.  Every wait is bounded; on timeout the kernel
-// records RNN_TIMEOUT in the status word and leaves its loops.
+// major-ness bits select which.
+//
+// Split K (a long K with too few tiles to fill the GPU, i.e. the weight
+// gradients): work item (tile, s) covers K slice s of S and stores its raw
+// fp32 partial product to scratch; a second kernel sums the S partials of
+// every element in split order (deterministic) and applies the epilogue.
+// Every wait is bounded; on timeout the kernel records RNN_TIMEOUT in the
+// status word and leaves its loops.
+#include <cstdlib>
+
 #include "common.cuh"
 
 namespace rnn {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;          // 16 KB
-constexpr int B_BYTES = BN * BK * 2;          // 16 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BM = 128, BK = 64;
 constexpr int kThreads = 192;
-constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int kMaxSplits = 16;
 
+template <int BN>
+struct GemmCfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+};
+
+template <int BN>
 struct alignas(1024) GemmSmem {
-  uint8_t stage[STAGES][STAGE_BYTES];
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint8_t stage[GemmCfg<BN>::STAGES][GemmCfg<BN>::STAGE_BYTES];
+  uint64_t full[GemmCfg<BN>::STAGES];
+  uint64_t empty[GemmCfg<BN>::STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_base;
@@ -53,31 +69,39 @@ struct TcGemmParams {
   int perm[4];
   DevArea* dev;
   uint64_t timeout_ns;
+  int splits;                 // S >= 1
+  float* ws;                  // S > 1: partial products, [S][M][N] fp32
 };
 
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kmajor, int kstep) {
-  // base: 1024-aligned start of a 128 x 64 (rows x K) operand tile.
+  // base: 1024-aligned start of a rows x 64 (rows x K) operand tile.
   if (kmajor) return sdesc_sw128(base + kstep * 32, 16, 1024);
-  // MN-major: two 64-element MN chunks of 64 K-rows (8 KB each).
+  // MN-major: 64-element MN chunks of 64 K-rows (8 KB each).
   return sdesc_sw128(base + kstep * 2048, 8192, 1024);
 }
 
+// One rows x 64 operand tile: a single box (K-major, the map's box is
+// 64 x rows) or rows/64 boxes of 64 x 64 (MN-major).
+template <int ROWS>
 __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int kmajor,
                                              int row0, int k0) {
   if (kmajor) {
     tma_load_2d(dst, map, bar, k0, row0);
   } else {
-    tma_load_2d(dst, map, bar, row0, k0);
-    tma_load_2d(dst + 8192, map, bar, row0 + 64, k0);
+#pragma unroll
+    for (int c = 0; c < ROWS / 64; ++c) tma_load_2d(dst + 8192 * c, map, bar, row0 + 64 * c, k0);
   }
 }
 
-__device__ __forceinline__ void store_chunk(const TcGemmParams& p, int64_t row, int n0, const float (&v)[32]) {
-  // 32 consecutive columns n0 .. n0+31 of one output row.
+// 32 consecutive columns n0 .. n0+31 of one output row.  bias: added when
+// non-null; beta: C's previous value is added (read through L2: another SM may
+// have written it during this launch).
+__device__ __forceinline__ void store_chunk(const TcGemmParams& p, int64_t row, int n0, const float (&v)[32],
+                                            const float* bias, int beta) {
   const bool full = n0 + 32 <= p.N;
   if (p.c_bf16) {
     __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + n0;
-    if (full && (p.ldc % 8 == 0) && !p.beta) {
+    if (full && (p.ldc % 8 == 0) && !beta) {
 #pragma unroll
       for (int j = 0; j < 32; j += 8) {
         uint4 q;
@@ -85,7 +109,7 @@ __device__ __forceinline__ void store_chunk(const TcGemmParams& p, int64_t row, 
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           float a0 = v[j + 2 * e], a1 = v[j + 2 * e + 1];
-          if (p.bias) { a0 += p.bias[n0 + j + 2 * e]; a1 += p.bias[n0 + j + 2 * e + 1]; }
+          if (bias) { a0 += bias[n0 + j + 2 * e]; a1 += bias[n0 + j + 2 * e + 1]; }
           __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
           w[e] = *reinterpret_cast<uint32_t*>(&h);
         }
@@ -94,8 +118,8 @@ __device__ __forceinline__ void store_chunk(const TcGemmParams& p, int64_t row, 
     } else {
       for (int j = 0; j < 32 && n0 + j < p.N; ++j) {
         float a = v[j];
-        if (p.bias) a += p.bias[n0 + j];
-        if (p.beta) a += __bfloat162float(C[j]);
+        if (bias) a += bias[n0 + j];
+        if (beta) a += __bfloat162float(__ldcg(C + j));
         C[j] = __float2bfloat16_rn(a);
       }
     }
@@ -105,9 +129,9 @@ __device__ __forceinline__ void store_chunk(const TcGemmParams& p, int64_t row, 
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {
         float4 q = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-        if (p.bias) { q.x += p.bias[n0 + j]; q.y += p.bias[n0 + j + 1]; q.z += p.bias[n0 + j + 2]; q.w += p.bias[n0 + j + 3]; }
-        if (p.beta) {
-          const float4 o = *reinterpret_cast<const float4*>(C + j);
+        if (bias) { q.x += bias[n0 + j]; q.y += bias[n0 + j + 1]; q.z += bias[n0 + j + 2]; q.w += bias[n0 + j + 3]; }
+        if (beta) {
+          const float4 o = __ldcg(reinterpret_cast<const float4*>(C + j));
           q.x += o.x; q.y += o.y; q.z += o.z; q.w += o.w;
         }
         *reinterpret_cast<float4*>(C + j) = q;
@@ -115,23 +139,40 @@ __device__ __forceinline__ void store_chunk(const TcGemmParams& p, int64_t row, 
     } else {
       for (int j = 0; j < 32 && n0 + j < p.N; ++j) {
         float a = v[j];
-        if (p.bias) a += p.bias[n0 + j];
-        if (p.beta) a += C[j];
+        if (bias) a += bias[n0 + j];
+        if (beta) a += __ldcg(C + j);
         C[j] = a;
       }
     }
   }
 }
 
+// Raw fp32 partial product: 32 consecutive columns n0.. of row m of split s.
+__device__ __forceinline__ void store_partial(const TcGemmParams& p, int s, int m, int n0, const float (&v)[32]) {
+  float* W = p.ws + (static_cast<int64_t>(s) * p.M + m) * p.N + n0;
+  if (n0 + 32 <= p.N && p.N % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(W + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+  } else {
+    for (int j = 0; j < 32 && n0 + j < p.N; ++j) W[j] = v[j];
+  }
+}
+
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcGemmParams p) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int STAGES = Cfg::STAGES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  GemmSmem& sm = *reinterpret_cast<GemmSmem*>(
+  GemmSmem<BN>& sm = *reinterpret_cast<GemmSmem<BN>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = (p.M + BM - 1) / BM, nt = (p.N + BN - 1) / BN;
   const int ntiles = mt * nt;
+  const int nitems = ntiles * p.splits;
   const int nk = (p.K + BK - 1) / BK;
+  // K blocks [kb_lo(s), kb_lo(s + 1)) belong to split s
+  auto kb_lo = [&](int s) { return static_cast<int>((static_cast<int64_t>(nk) * s) / p.splits); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], 1); }
@@ -142,7 +183,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     prefetch_tmap(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    tmem_alloc(&sm.tmem_base, Cfg::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -154,9 +195,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t it = 0;
-      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+        const int tile = item % ntiles, sp = item / ntiles;
         const int m0 = (tile / nt) * BM, n0 = (tile % nt) * BN;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        for (int kb = kb_lo(sp); kb < kb_lo(sp + 1); ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait(&sm.empty[s], ph ^ 1, p.timeout_ns) || *(volatile int*)&sm.abort_flag) {
@@ -164,9 +206,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             sm.abort_flag = 1;
             goto producer_done;
           }
-          mbar_arrive_expect_tx(&sm.full[s], STAGE_BYTES);
-          load_operand(sm.stage[s], &tmA, &sm.full[s], p.a_kmajor, m0, kb * BK);
-          load_operand(sm.stage[s] + A_BYTES, &tmB, &sm.full[s], p.b_kmajor, n0, kb * BK);
+          mbar_arrive_expect_tx(&sm.full[s], Cfg::STAGE_BYTES);
+          load_operand<BM>(sm.stage[s], &tmA, &sm.full[s], p.a_kmajor, m0, kb * BK);
+          load_operand<BN>(sm.stage[s] + A_BYTES, &tmB, &sm.full[s], p.b_kmajor, n0, kb * BK);
         }
       }
     producer_done:;
@@ -174,7 +216,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     if (lane == 0) {
       uint32_t it = 0, acc = 0;
-      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++acc) {
+      for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++acc) {
+        const int sp = item / ntiles;
         const int buf = acc & 1;
         const uint32_t aph = (acc >> 1) & 1;
         if (!mbar_wait(&sm.tempty[buf], aph ^ 1, p.timeout_ns) || *(volatile int*)&sm.abort_flag) {
@@ -185,7 +228,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc_fence_after();
         const uint32_t dt = tmem + buf * BN;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int k0 = kb_lo(sp), k1 = kb_lo(sp + 1);
+        for (int kb = k0; kb < k1; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
           if (!mbar_wait(&sm.full[s], ph, p.timeout_ns) || *(volatile int*)&sm.abort_flag) {
@@ -200,7 +244,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             mma_bf16_ss(dt, operand_desc(abase, p.a_kmajor, k), operand_desc(bbase, p.b_kmajor, k), idesc,
-                        (kb > 0 || k > 0) ? 1u : 0u);
+                        (kb > k0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&sm.empty[s]);
         }
@@ -211,7 +255,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else {
     const int q = warp & 3;              // TMEM lane quarter of this warp
     uint32_t acc = 0;
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++acc) {
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++acc) {
+      const int tile = item % ntiles, sp = item / ntiles;
       const int buf = acc & 1;
       const uint32_t aph = (acc >> 1) & 1;
       int ok = 1;
@@ -226,7 +271,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int m = m0 + q * 32 + lane;
       int64_t row = m;
       bool write = m < p.M;
-      if (write && p.rowmap_H > 0) {
+      if (write && p.splits == 1 && p.rowmap_H > 0) {
         const int pm = p.perm[m & 3];
         if (pm < 0) write = false;
         row = static_cast<int64_t>(pm) * p.rowmap_H + (m >> 2);
@@ -234,7 +279,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int c = 0; c < BN; c += 32) {
         float v[32];
         tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c, v);
-        if (write && n0 + c < p.N) store_chunk(p, row, n0 + c, v);
+        if (write && n0 + c < p.N) {
+          if (p.splits > 1) store_partial(p, sp, m, n0 + c, v);
+          else store_chunk(p, row, n0 + c, v, p.bias, p.beta);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -245,22 +293,82 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
 }
 
-constexpr size_t kSmemBytes = sizeof(GemmSmem) + 1024;
+template <int BN>
+constexpr size_t smem_bytes() { return sizeof(GemmSmem<BN>) + 1024; }
 
-}  // namespace
-
-bool gemm_tc_supported(const GemmArgs& g) {
-  if (!g.in_bf16 || g.K <= 0 || g.M <= 0 || g.N <= 0) return false;
-  if ((reinterpret_cast<uintptr_t>(g.A) & 15) || (reinterpret_cast<uintptr_t>(g.B) & 15)) return false;
-  if ((g.lda * 2) % 16 || (g.ldb * 2) % 16) return false;
-  return true;
+// C[row(m), n] = sum over s in order of ws[s][m][n] (+ bias[n]) (+ C if beta),
+// four consecutive columns per thread.
+__global__ void __launch_bounds__(256)
+gemm_split_reduce_kernel(const float* __restrict__ ws, int S, int M, int N, TcGemmParams p) {
+  const int nq = (N + 3) / 4;
+  const int64_t total = static_cast<int64_t>(M) * nq;
+  const int64_t plane = static_cast<int64_t>(M) * N;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(i / nq), n0 = static_cast<int>(i % nq) * 4;
+    int64_t row = m;
+    if (p.rowmap_H > 0) {
+      const int pm = p.perm[m & 3];
+      if (pm < 0) continue;
+      row = static_cast<int64_t>(pm) * p.rowmap_H + (m >> 2);
+    }
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    const float* w = ws + static_cast<int64_t>(m) * N + n0;
+    if (n0 + 4 <= N && N % 4 == 0) {
+      for (int s = 0; s < S; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(w + s * plane);
+        a[0] += v.x; a[1] += v.y; a[2] += v.z; a[3] += v.w;
+      }
+    } else {
+      for (int s = 0; s < S; ++s)
+        for (int j = 0; j < 4 && n0 + j < N; ++j) a[j] += w[s * plane + j];
+    }
+    for (int j = 0; j < 4 && n0 + j < N; ++j) {
+      float x = a[j];
+      if (p.bias) x += p.bias[n0 + j];
+      if (p.c_bf16) {
+        __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + n0 + j;
+        if (p.beta) x += __bfloat162float(*C);
+        *C = __float2bfloat16_rn(x);
+      } else {
+        float* C = static_cast<float*>(p.C) + row * p.ldc + n0 + j;
+        if (p.beta) x += *C;
+        *C = x;
+      }
+    }
+  }
 }
 
-int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns) {
-  if (!gemm_tc_supported(g)) return 2;
+struct GemmPlan { int BN, S; };
+
+// Tile width and K split.  Items run in waves of num_sms.  128 x 256 tiles
+// unless they would leave most SMs idle; then a long K is split when the
+// scratch allows and that saves at least a sixth of the waves per unit of
+// work, and otherwise 128-wide tiles double the tile count.
+GemmPlan plan_gemm(const GemmArgs& g, int num_sms) {
+  const int mt = (g.M + BM - 1) / BM;
+  const int t256 = mt * ((g.N + 255) / 256), t128 = mt * ((g.N + 127) / 128);
+  const int nk = (g.K + BK - 1) / BK;
+  if (t256 >= num_sms) return {256, 1};
+  const size_t plane = static_cast<size_t>(g.M) * g.N * 4;
+  if (g.split_ws && nk >= 32) {
+    int best = 1;
+    double best_cost = 1.0;
+    for (int S = 2; S <= kMaxSplits && nk / S >= 16 && S * plane <= g.split_ws_bytes; ++S) {
+      const double cost = static_cast<double>((t256 * S + num_sms - 1) / num_sms) / S;
+      if (cost < best_cost - 1e-9) { best_cost = cost; best = S; }
+    }
+    if (best > 1 && best_cost <= 5.0 / 6.0) return {256, best};
+  }
+  if (2 * t256 < num_sms && t128 > t256) return {128, 1};
+  return {256, 1};
+}
+
+template <int BN>
+int launch_bn(const GemmArgs& g, int S, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns) {
   CUtensorMap ta, tb;
   int rc;
   // A: rows = M; B: rows = N.
@@ -278,17 +386,47 @@ int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev,
   for (int i = 0; i < 4; ++i) p.perm[i] = g.perm[i];
   p.dev = dev;
   p.timeout_ns = timeout_ns;
+  p.splits = S;
+  p.ws = static_cast<float*>(g.split_ws);
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<BN>())) != cudaSuccess)
       return 3;
     attr_set = true;
   }
-  const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(ta, tb, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+  const int items = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * S;
+  const int grid = items < num_sms ? items : num_sms;
+  gemm_tc_kernel<BN><<<grid, kThreads, smem_bytes<BN>(), s>>>(ta, tb, p);
+  if (cudaGetLastError() != cudaSuccess) return 3;
+  if (S > 1) {
+    gemm_split_reduce_kernel<<<4 * num_sms, 256, 0, s>>>(p.ws, S, g.M, g.N, p);
+    if (cudaGetLastError() != cudaSuccess) return 3;
+  }
+  return 0;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(const GemmArgs& g) {
+  if (!g.in_bf16 || g.K <= 0 || g.M <= 0 || g.N <= 0) return false;
+  if ((reinterpret_cast<uintptr_t>(g.A) & 15) || (reinterpret_cast<uintptr_t>(g.B) & 15)) return false;
+  if ((g.lda * 2) % 16 || (g.ldb * 2) % 16) return false;
+  return true;
+}
+
+int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns,
+                   int* launches) {
+  if (!gemm_tc_supported(g)) return 2;
+  GemmPlan pl = plan_gemm(g, num_sms);
+  // tuning knob: RNN_GEMM_BN=128|256 forces the tile width (no K split)
+  if (const char* e = std::getenv("RNN_GEMM_BN")) {
+    const int v = std::atoi(e);
+    if (v == 128 || v == 256) pl = {v, 1};
+  }
+  if (launches) *launches = pl.S > 1 ? 2 : 1;
+  return pl.BN == 256 ? launch_bn<256>(g, pl.S, s, num_sms, dev, timeout_ns)
+                      : launch_bn<128>(g, pl.S, s, num_sms, dev, timeout_ns);
 }
 
 }  // namespace rnn

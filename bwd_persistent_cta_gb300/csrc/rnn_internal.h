@@ -60,6 +60,10 @@ struct GemmArgs {
   int rowmap_H = 0;
   int perm[4] = {0, 1, 2, 3};
   int in_bf16 = 1;            // operand element type (SIMT kernel takes fp32 too)
+  // scratch the tcgen05 kernel may use to split K across CTAs (fp32 partial
+  // products, reduced in a fixed order by a second kernel); null: no split
+  void* split_ws = nullptr;
+  size_t split_ws_bytes = 0;
 };
 
 struct PersistArgs {
@@ -93,7 +97,9 @@ struct PersistArgs {
 
 // Host-side launch status: 0 = launched, otherwise an rnn_status_t value.
 int launch_gemm_simt(const GemmArgs& g, cudaStream_t s);
-int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns);
+// *launches (optional) receives the number of kernels launched (2 with a K split).
+int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns,
+                   int* launches = nullptr);
 bool gemm_tc_supported(const GemmArgs& g);
 
 int plan_persist_simt(const PersistArgs& a, int num_sms, int* nblk, size_t* smem);

@@ -83,3 +83,32 @@ def test_gemm_epilogue_bias_bf16(use_tc):
 @pytest.mark.parametrize("use_tc", [1, 0])
 def test_gemm_epilogue_beta_rowmap(use_tc):
     _case(512, 200, 1000, 0, 0, use_tc, beta=True, rowmap=[2, 0, -1, 1])
+
+
+def test_gemm_split_k_rowmap_beta_bias():
+    # long K, few tiles: K is split across CTAs; the partials are summed in split order
+    _case(512, 512, 8192, 0, 0, 1, bias=True, beta=True, rowmap=[1, -1, 0, 2], seed=11)
+
+
+def test_gemm_split_k_multiwave():
+    # more (tile, split) items than SMs: the split items run in several waves
+    _case(6400, 512, 3072, 1, 1, 1, seed=12)
+
+
+def test_gemm_split_k_deterministic():
+    R = _lib()
+    g = torch.Generator().manual_seed(13)
+    M, N, K = 1024, 512, 16384
+    A = torch.randn(M, K, generator=g).bfloat16().cuda()
+    B = torch.randn(N, K, generator=g).bfloat16().cuda()
+    outs = []
+    for _ in range(2):
+        C = torch.zeros(M, N, device="cuda")
+        rc = R.rnn_debug_gemm(M, N, K, A.data_ptr(), K, 1, B.data_ptr(), K, 1, C.data_ptr(), N, 0, None, 0, 0,
+                              [0, 1, 2, 3], 1, 1, torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, R.rnn_status_string(rc)
+        torch.cuda.synchronize()
+        outs.append(C.cpu())
+    assert torch.equal(outs[0], outs[1])
+    ref = A.double().cpu() @ B.double().cpu().t()
+    assert float((outs[0].double() - ref).abs().max()) / float(ref.abs().max()) < 1e-5
