@@ -37,6 +37,15 @@ Readings where the pages are silent (each is listed in the design doc):
     n = tanh(W_in x + b_n + W_hn (r * h));
   * dhy / dcy default to zero; weight gradients overwrite (never accumulate
     across calls).
+  * variable sequence lengths (poplibs Gru.cpp / Lstm.cpp, the batchwise
+    time-step mask of the forward and backward loops): sequence b has
+    len_b <= T valid steps; at a step t >= len_b the mask m = 0 holds the
+    state (h, c carried unchanged, the latched final state) and zeroes the
+    output, h_t = m h' + (1 - m) h_{t-1}, c_t = m c' + (1 - m) c_{t-1},
+    y_t = m h'.  The backward is the exact derivative of that: the gate
+    gradients of a masked step are zero and the state gradients pass through
+    it unchanged.  The reverse direction therefore starts from h0 at
+    t = len_b - 1.
 """
 from __future__ import annotations
 
@@ -57,19 +66,33 @@ def _time_order(T: int, reverse: bool):
     return range(T - 1, -1, -1) if reverse else range(T)
 
 
+def _masks(T: int, B: int, lengths) -> np.ndarray:
+    """m[t, b, 0] = 1 when step t is inside sequence b (t < len_b), else 0;
+    all ones without lengths (the batchwise time-step mask)."""
+    m = np.ones((T, B, 1))
+    if lengths is not None:
+        for b, n in enumerate(lengths):
+            m[int(n):, b, 0] = 0.0
+    return m
+
+
 # ----------------------------------------------------------------------------
 # LSTM, one direction of one layer
 # ----------------------------------------------------------------------------
-def lstm_forward_dir(x, p, h0, c0, reverse=False):
+def lstm_forward_dir(x, p, h0, c0, reverse=False, lengths=None):
     """Lstm.cpp, lstmCellForwardPassCalcUnits / basicLstmCellForwardPass:
     a = W_ih x_t + W_hh h_{t-1} + b; i, f, o = sigmoid; g = tanh;
-    c_t = f c_{t-1} + i g; h_t = o tanh(c_t)."""
+    c' = f c_{t-1} + i g; h' = o tanh(c').  With the step mask m:
+    c_t = m c' + (1-m) c_{t-1}; h_t = m h' + (1-m) h_{t-1}; y_t = m h'."""
     T, B, _ = x.shape
     H = p["W_hh"].shape[1]
+    M = _masks(T, B, lengths)
     h, c = h0, c0
     y = np.zeros((T, B, H))
     keep = {k: np.zeros((T, B, H)) for k in ("i", "f", "g", "o", "c", "c_prev", "h_prev")}
+    keep["m"] = M
     for t in _time_order(T, reverse):
+        m = M[t]
         a = x[t] @ p["W_ih"].T + h @ p["W_hh"].T + p["b"]
         i = sigmoid(a[:, 0 * H:1 * H])
         f = sigmoid(a[:, 1 * H:2 * H])
@@ -80,8 +103,8 @@ def lstm_forward_dir(x, p, h0, c0, reverse=False):
         for k, v in (("i", i), ("f", f), ("g", g), ("o", o), ("c", c_new),
                      ("c_prev", c), ("h_prev", h)):
             keep[k][t] = v
-        y[t] = h_new
-        h, c = h_new, c_new
+        y[t] = m * h_new
+        h, c = m * h_new + (1.0 - m) * h, m * c_new + (1.0 - m) * c
     return y, h, c, keep
 
 
@@ -94,22 +117,26 @@ def lstm_backward_dir(x, p, keep, dy, dhT, dcT, reverse=False):
       da_o = dh tanh(c_t) o(1-o)
       dh_rec <- W_hh^T da; dc_next <- dc f
     Weight gradients (basicLstmParamUpdate): dW_ih = sum da x^T,
-    dW_hh = sum da h_{t-1}^T, db = sum da."""
+    dW_hh = sum da h_{t-1}^T, db = sum da.
+    Masked step (m = 0): the gate gradients are zero and dh_rec, dc_next pass
+    through unchanged; dy_t does not reach the state."""
     T, B, I = x.shape
     H = p["W_hh"].shape[1]
+    M = keep["m"]
     dA = np.zeros((T, B, 4 * H))
     dh_rec, dc_next = dhT, dcT
     for t in reversed(list(_time_order(T, reverse))):
+        m = M[t]
         i, f, g, o = keep["i"][t], keep["f"][t], keep["g"][t], keep["o"][t]
         tc = np.tanh(keep["c"][t])
-        dh = dy[t] + dh_rec
-        dc = dh * o * (1.0 - tc * tc) + dc_next
+        dh = m * (dy[t] + dh_rec)
+        dc = dh * o * (1.0 - tc * tc) + m * dc_next
         dA[t, :, 0 * H:1 * H] = dc * g * i * (1.0 - i)
         dA[t, :, 1 * H:2 * H] = dc * keep["c_prev"][t] * f * (1.0 - f)
         dA[t, :, 2 * H:3 * H] = dc * i * (1.0 - g * g)
         dA[t, :, 3 * H:4 * H] = dh * tc * o * (1.0 - o)
-        dh_rec = dA[t] @ p["W_hh"]
-        dc_next = dc * f
+        dh_rec = dA[t] @ p["W_hh"] + (1.0 - m) * dh_rec
+        dc_next = dc * f + (1.0 - m) * dc_next
     dx = dA @ p["W_ih"]
     flat = dA.reshape(T * B, 4 * H)
     grads = {"W_ih": flat.T @ x.reshape(T * B, I),
@@ -121,16 +148,20 @@ def lstm_backward_dir(x, p, keep, dy, dhT, dcT, reverse=False):
 # ----------------------------------------------------------------------------
 # GRU resetAfter, one direction of one layer
 # ----------------------------------------------------------------------------
-def gru_ra_forward_dir(x, p, h0, reverse=False):
+def gru_ra_forward_dir(x, p, h0, reverse=False, lengths=None):
     """Gru.cpp, gruCellForwardPassCalcUnitsResetAfter:
     a^x = W_ih x + b_i; a^h = W_hh h + b_h; r = s(a^x_r + a^h_r);
-    z = s(a^x_z + a^h_z); n = tanh(a^x_n + r a^h_n); h' = (1-z) n + z h."""
+    z = s(a^x_z + a^h_z); n = tanh(a^x_n + r a^h_n); h' = (1-z) n + z h.
+    With the step mask m: h_t = m h' + (1-m) h_{t-1}; y_t = m h'."""
     T, B, _ = x.shape
     H = p["W_hh"].shape[1]
+    M = _masks(T, B, lengths)
     h = h0
     y = np.zeros((T, B, H))
     keep = {k: np.zeros((T, B, H)) for k in ("r", "z", "n", "hn", "h_prev")}
+    keep["m"] = M
     for t in _time_order(T, reverse):
+        m = M[t]
         ax = x[t] @ p["W_ih"].T + p["b"]
         ah = h @ p["W_hh"].T + p["b_h"]
         r = sigmoid(ax[:, 0:H] + ah[:, 0:H])
@@ -140,8 +171,8 @@ def gru_ra_forward_dir(x, p, h0, reverse=False):
         h_new = (1.0 - z) * n + z * h
         for k, v in (("r", r), ("z", z), ("n", n), ("hn", hn), ("h_prev", h)):
             keep[k][t] = v
-        y[t] = h_new
-        h = h_new
+        y[t] = m * h_new
+        h = m * h_new + (1.0 - m) * h
     return y, h, keep
 
 
@@ -153,21 +184,24 @@ def gru_ra_backward_dir(x, p, keep, dy, dhT, reverse=False):
       input side dA^x = [dr, dz, dn]; recurrent side dA^h = [dr, dz, dn r]
       dh_rec <- W_hh^T dA^h + dh z
     Weight gradients: dW_ih = sum dA^x x^T, dW_hh = sum dA^h h^T,
-    db_i = sum dA^x, db_h = sum dA^h."""
+    db_i = sum dA^x, db_h = sum dA^h.
+    Masked step (m = 0): zero gate gradients, dh_rec passes through."""
     T, B, I = x.shape
     H = p["W_hh"].shape[1]
+    M = keep["m"]
     dAx = np.zeros((T, B, 3 * H))
     dAh = np.zeros((T, B, 3 * H))
     dh_rec = dhT
     for t in reversed(list(_time_order(T, reverse))):
+        m = M[t]
         r, z, n, hn, hp = (keep[k][t] for k in ("r", "z", "n", "hn", "h_prev"))
-        dh = dy[t] + dh_rec
+        dh = m * (dy[t] + dh_rec)
         dn = dh * (1.0 - z) * (1.0 - n * n)
         dz = dh * (hp - n) * z * (1.0 - z)
         dr = dn * hn * r * (1.0 - r)
         dAx[t] = np.concatenate([dr, dz, dn], axis=1)
         dAh[t] = np.concatenate([dr, dz, dn * r], axis=1)
-        dh_rec = dAh[t] @ p["W_hh"] + dh * z
+        dh_rec = dAh[t] @ p["W_hh"] + dh * z + (1.0 - m) * dh_rec
     dx = dAx @ p["W_ih"]
     fx = dAx.reshape(T * B, 3 * H)
     fh = dAh.reshape(T * B, 3 * H)
@@ -180,17 +214,21 @@ def gru_ra_backward_dir(x, p, keep, dy, dhT, reverse=False):
 # ----------------------------------------------------------------------------
 # GRU reset-before, one direction of one layer
 # ----------------------------------------------------------------------------
-def gru_rb_forward_dir(x, p, h0, reverse=False):
+def gru_rb_forward_dir(x, p, h0, reverse=False, lengths=None):
     """Gru.cpp, gruCellForwardPassCalcUnits / basicGruCellForwardPass:
     [r, z] = s(W_{ih,rz} x + W_{hh,rz} h + b_rz);
-    n = tanh(W_in x + W_hn (r * h) + b_n); h' = (1-z) n + z h."""
+    n = tanh(W_in x + W_hn (r * h) + b_n); h' = (1-z) n + z h.
+    With the step mask m: h_t = m h' + (1-m) h_{t-1}; y_t = m h'."""
     T, B, _ = x.shape
     H = p["W_hh"].shape[1]
+    M = _masks(T, B, lengths)
     h = h0
     y = np.zeros((T, B, H))
     keep = {k: np.zeros((T, B, H)) for k in ("r", "z", "n", "rh", "h_prev")}
+    keep["m"] = M
     Wi, Wh, b = p["W_ih"], p["W_hh"], p["b"]
     for t in _time_order(T, reverse):
+        m = M[t]
         a_rz = x[t] @ Wi[0:2 * H].T + h @ Wh[0:2 * H].T + b[0:2 * H]
         r = sigmoid(a_rz[:, 0:H])
         z = sigmoid(a_rz[:, H:2 * H])
@@ -199,8 +237,8 @@ def gru_rb_forward_dir(x, p, h0, reverse=False):
         h_new = (1.0 - z) * n + z * h
         for k, v in (("r", r), ("z", z), ("n", n), ("rh", rh), ("h_prev", h)):
             keep[k][t] = v
-        y[t] = h_new
-        h = h_new
+        y[t] = m * h_new
+        h = m * h_new + (1.0 - m) * h
     return y, h, keep
 
 
@@ -212,21 +250,24 @@ def gru_rb_backward_dir(x, p, keep, dy, dhT, reverse=False):
       dh_rec <- d(rh) * r + W_{hh,rz}^T [dr, dz] + dh z
     Weight gradients (basicGruParamUpdate): dW_ih = sum [dr,dz,dn] x^T,
     dW_{hh,rz} = sum [dr,dz] h_{t-1}^T, dW_hn = sum dn (r*h_{t-1})^T,
-    db = sum [dr, dz, dn]."""
+    db = sum [dr, dz, dn].
+    Masked step (m = 0): zero gate gradients, dh_rec passes through."""
     T, B, I = x.shape
     H = p["W_hh"].shape[1]
     Wh = p["W_hh"]
+    M = keep["m"]
     dA = np.zeros((T, B, 3 * H))
     dh_rec = dhT
     for t in reversed(list(_time_order(T, reverse))):
+        m = M[t]
         r, z, n, hp = (keep[k][t] for k in ("r", "z", "n", "h_prev"))
-        dh = dy[t] + dh_rec
+        dh = m * (dy[t] + dh_rec)
         dn = dh * (1.0 - z) * (1.0 - n * n)
         dz = dh * (hp - n) * z * (1.0 - z)
         drh = dn @ Wh[2 * H:3 * H]
         dr = drh * hp * r * (1.0 - r)
         dA[t] = np.concatenate([dr, dz, dn], axis=1)
-        dh_rec = drh * r + dA[t, :, 0:2 * H] @ Wh[0:2 * H] + dh * z
+        dh_rec = drh * r + dA[t, :, 0:2 * H] @ Wh[0:2 * H] + dh * z + (1.0 - m) * dh_rec
     dx = dA @ p["W_ih"]
     f = dA.reshape(T * B, 3 * H)
     dW_hh = np.concatenate([
@@ -240,9 +281,11 @@ def gru_rb_backward_dir(x, p, keep, dy, dhT, reverse=False):
 # Stacked, optionally bidirectional layer
 # ----------------------------------------------------------------------------
 def rnn_forward(mode: str, reset_after: bool, params, x, h0=None, c0=None,
-                bidirectional: bool = False) -> Dict:
+                bidirectional: bool = False, lengths=None) -> Dict:
     """Layer l+1 reads layer l's output; a bidirectional layer's output is
     [y_fwd | y_bwd] on the feature axis; NULL initial states are zero.
+    ``lengths`` (optional, [B] ints <= T): valid steps per sequence, the same
+    for every layer and direction.
     Returns y [T,B,D*H], hy [L*D,B,H], cy (LSTM) and a cache for rnn_backward."""
     L, D = len(params), (2 if bidirectional else 1)
     T, B, _ = x.shape
@@ -258,12 +301,13 @@ def rnn_forward(mode: str, reset_after: bool, params, x, h0=None, c0=None,
             s = l * D + d
             p = params[l][d]
             if mode == LSTM:
-                y, hT, cT, keep = lstm_forward_dir(layer_in, p, h0[s], c0[s], reverse=(d == 1))
+                y, hT, cT, keep = lstm_forward_dir(layer_in, p, h0[s], c0[s], reverse=(d == 1),
+                                                   lengths=lengths)
                 cy[s] = cT
             elif reset_after:
-                y, hT, keep = gru_ra_forward_dir(layer_in, p, h0[s], reverse=(d == 1))
+                y, hT, keep = gru_ra_forward_dir(layer_in, p, h0[s], reverse=(d == 1), lengths=lengths)
             else:
-                y, hT, keep = gru_rb_forward_dir(layer_in, p, h0[s], reverse=(d == 1))
+                y, hT, keep = gru_rb_forward_dir(layer_in, p, h0[s], reverse=(d == 1), lengths=lengths)
             hy[s] = hT
             outs.append(y)
             per_dir.append(keep)
@@ -336,7 +380,8 @@ def run_inputs(inp, with_backward: bool = True) -> Dict:
     """Convenience: run a ``synth.Inputs`` bundle (duck-typed: .wl, .params,
     .x, .h0, .c0, .dy, .dhy, .dcy) through forward (+ backward)."""
     wl = inp.wl
-    f = rnn_forward(wl.mode, wl.reset_after, inp.params, inp.x, inp.h0, inp.c0, wl.bidirectional)
+    f = rnn_forward(wl.mode, wl.reset_after, inp.params, inp.x, inp.h0, inp.c0, wl.bidirectional,
+                    lengths=getattr(inp, "lengths", None))
     out = {"y": f["y"], "hy": f["hy"]}
     if wl.mode == LSTM:
         out["cy"] = f["cy"]

@@ -9,7 +9,10 @@
   otherwise;
 * central finite differences of the loss sum <dy, y> + <dhy, h_T> + <dcy, c_T>;
 * structural invariants: reverse direction = forward on the time-reversed input;
-  stacked layers = sequential single-layer calls.
+  stacked layers = sequential single-layer calls;
+* variable sequence lengths: a masked batch equals each sequence run alone on
+  its own truncated length (outputs, final states, all gradients), full lengths
+  equal no lengths, and the masked backward matches finite differences.
 A final group plants mistakes in a copy of the oracle and checks that the pins
 catch each one.
 """
@@ -276,7 +279,7 @@ def test_gru_reset_before_equals_reset_after_for_diagonal_Whn():
 # ---------------------------------------------------------------------------
 # central finite differences
 # ---------------------------------------------------------------------------
-def _fd_check(mode, reset_after, L, bidir, oracle=O, seed=13, T=3, B=2, I=3, H=2, rtol=1e-7):
+def _fd_check(mode, reset_after, L, bidir, oracle=O, seed=13, T=3, B=2, I=3, H=2, rtol=1e-7, lengths=None):
     rng = np.random.default_rng(seed)
     D = 2 if bidir else 1
     params = _rand_params(rng, mode, reset_after, L, D, I, H, 0.8)
@@ -288,10 +291,10 @@ def _fd_check(mode, reset_after, L, bidir, oracle=O, seed=13, T=3, B=2, I=3, H=2
     dcy = rng.normal(size=(L * D, B, H)) if mode == "lstm" else None
 
     def loss():
-        f = oracle.rnn_forward(mode, reset_after, params, x, h0, c0, bidir)
+        f = oracle.rnn_forward(mode, reset_after, params, x, h0, c0, bidir, lengths=lengths)
         return oracle.rnn_loss(mode, f, dy, dhy, dcy)
 
-    f = oracle.rnn_forward(mode, reset_after, params, x, h0, c0, bidir)
+    f = oracle.rnn_forward(mode, reset_after, params, x, h0, c0, bidir, lengths=lengths)
     g = oracle.rnn_backward(mode, reset_after, params, f, dy, dhy, dcy, bidir)
     checks = [(x, g["dx"]), (h0, g["dhx"])]
     if mode == "lstm":
@@ -386,7 +389,7 @@ def _mutant(old, new):
 
 MUTATIONS = [
     # (mode, reset_after, old text, new text)
-    ("lstm", False, "dc = dh * o * (1.0 - tc * tc) + dc_next", "dc = dh * o * (1.0 - tc * tc)"),
+    ("lstm", False, "dc = dh * o * (1.0 - tc * tc) + m * dc_next", "dc = dh * o * (1.0 - tc * tc)"),
     ("lstm", False, "dc_next = dc * f", "dc_next = dc * i"),
     ("lstm", False, "dA[t, :, 3 * H:4 * H] = dh * tc * o * (1.0 - o)",
      "dA[t, :, 3 * H:4 * H] = dc * tc * o * (1.0 - o)"),
@@ -419,3 +422,120 @@ def test_planted_forward_mistakes_fail_golden_or_torch(old, new):
     x = np.array(case["x"], float).reshape(-1, 1, 1)
     f = mut.rnn_forward("gru", True, [[_scalar_params(case)]], x, np.full((1, 1, 1), case["h0"]))
     assert abs(f["y"][0, 0, 0] - case["expect_h"][0]) > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# variable sequence lengths
+# ---------------------------------------------------------------------------
+def _len_case(mode, reset_after, L, bidir, seed, T=6, B=4, I=3, H=4):
+    rng = np.random.default_rng(seed)
+    D = 2 if bidir else 1
+    params = _rand_params(rng, mode, reset_after, L, D, I, H)
+    x = rng.normal(size=(T, B, I))
+    h0 = rng.normal(size=(L * D, B, H))
+    c0 = rng.normal(size=(L * D, B, H)) if mode == "lstm" else None
+    dy = rng.normal(size=(T, B, D * H))
+    dhy = rng.normal(size=(L * D, B, H))
+    dcy = rng.normal(size=(L * D, B, H)) if mode == "lstm" else None
+    return params, x, h0, c0, dy, dhy, dcy
+
+
+CELLS = [("lstm", False), ("gru", True), ("gru", False)]
+
+
+@pytest.mark.parametrize("mode,reset_after", CELLS)
+def test_lengths_all_full_equal_no_lengths(mode, reset_after):
+    params, x, h0, c0, dy, dhy, dcy = _len_case(mode, reset_after, 2, True, 31)
+    T, B = x.shape[:2]
+    a = O.rnn_forward(mode, reset_after, params, x, h0, c0, True)
+    b = O.rnn_forward(mode, reset_after, params, x, h0, c0, True, lengths=[T] * B)
+    ga = O.rnn_backward(mode, reset_after, params, a, dy, dhy, dcy, True)
+    gb = O.rnn_backward(mode, reset_after, params, b, dy, dhy, dcy, True)
+    assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["hy"], b["hy"])
+    assert np.array_equal(ga["dx"], gb["dx"]) and np.array_equal(ga["dhx"], gb["dhx"])
+    for l in range(2):
+        for d in range(2):
+            for k in ga["dparams"][l][d]:
+                assert np.array_equal(ga["dparams"][l][d][k], gb["dparams"][l][d][k])
+
+
+@pytest.mark.parametrize("mode,reset_after", CELLS)
+@pytest.mark.parametrize("L,bidir", [(1, False), (2, True)])
+def test_lengths_equal_truncated_sequences(mode, reset_after, L, bidir):
+    """Each sequence of a masked batch behaves as if run alone on its first
+    len_b steps: outputs (zero beyond len_b), final states, input and state
+    gradients; weight gradients are the sum over sequences of those runs."""
+    params, x, h0, c0, dy, dhy, dcy = _len_case(mode, reset_after, L, bidir, 32 + L)
+    T, B = x.shape[:2]
+    D = 2 if bidir else 1
+    lengths = [4, 6, 0, 1]
+    f = O.rnn_forward(mode, reset_after, params, x, h0, c0, bidir, lengths=lengths)
+    g = O.rnn_backward(mode, reset_after, params, f, dy, dhy, dcy, bidir)
+    dw_sum = [[{k: np.zeros_like(v) for k, v in params[l][d].items()} for d in range(D)] for l in range(L)]
+    for b, n in enumerate(lengths):
+        assert np.all(f["y"][n:, b] == 0.0) and np.all(g["dx"][n:, b] == 0.0)
+        if n == 0:
+            assert np.array_equal(f["hy"][:, b], h0[:, b])
+            assert np.array_equal(g["dhx"][:, b], dhy[:, b])
+            if mode == "lstm":
+                assert np.array_equal(f["cy"][:, b], c0[:, b])
+                assert np.array_equal(g["dcx"][:, b], dcy[:, b])
+            continue
+        sl = slice(b, b + 1)
+        c0b = c0[:, sl] if mode == "lstm" else None
+        dcyb = dcy[:, sl] if mode == "lstm" else None
+        fb = O.rnn_forward(mode, reset_after, params, x[:n, sl], h0[:, sl], c0b, bidir)
+        gb = O.rnn_backward(mode, reset_after, params, fb, dy[:n, sl], dhy[:, sl], dcyb, bidir)
+        assert np.allclose(f["y"][:n, sl], fb["y"], rtol=1e-12, atol=1e-13)
+        assert np.allclose(f["hy"][:, sl], fb["hy"], rtol=1e-12, atol=1e-13)
+        assert np.allclose(g["dx"][:n, sl], gb["dx"], rtol=1e-11, atol=1e-12)
+        assert np.allclose(g["dhx"][:, sl], gb["dhx"], rtol=1e-11, atol=1e-12)
+        if mode == "lstm":
+            assert np.allclose(f["cy"][:, sl], fb["cy"], rtol=1e-12, atol=1e-13)
+            assert np.allclose(g["dcx"][:, sl], gb["dcx"], rtol=1e-11, atol=1e-12)
+        for l in range(L):
+            for d in range(D):
+                for k in dw_sum[l][d]:
+                    dw_sum[l][d][k] += gb["dparams"][l][d][k]
+    for l in range(L):
+        for d in range(D):
+            for k in dw_sum[l][d]:
+                assert np.allclose(g["dparams"][l][d][k], dw_sum[l][d][k], rtol=1e-10, atol=1e-11), (l, d, k)
+
+
+@pytest.mark.parametrize("mode,reset_after", CELLS)
+def test_lengths_finite_differences(mode, reset_after):
+    assert _fd_check(mode, reset_after, 2, True, seed=33, T=4, B=3, lengths=[4, 2, 0]) < 1e-7
+
+
+@pytest.mark.parametrize("mode,reset_after,old,new", [
+    ("lstm", False, "dh = m * (dy[t] + dh_rec)", "dh = dy[t] + dh_rec"),
+    ("lstm", False, "dc_next = dc * f + (1.0 - m) * dc_next", "dc_next = dc * f"),
+    ("gru", True, "dh_rec = dAh[t] @ p[\"W_hh\"] + dh * z + (1.0 - m) * dh_rec",
+     "dh_rec = dAh[t] @ p[\"W_hh\"] + dh * z"),
+    ("gru", False, "Wh[0:2 * H] + dh * z + (1.0 - m) * dh_rec", "Wh[0:2 * H] + dh * z + dh_rec"),
+])
+def test_planted_mask_mistakes_fail_finite_differences(mode, reset_after, old, new):
+    mut = _mutant(old, new)
+    assert _fd_check(mode, reset_after, 1, False, oracle=mut, seed=34, T=4, B=3, lengths=[4, 2, 0]) > 1e-4
+
+
+@pytest.mark.parametrize("old,new", [
+    ("        y[t] = m * h_new\n        h, c = m * h_new", "        y[t] = h_new\n        h, c = m * h_new"),
+    ("h, c = m * h_new + (1.0 - m) * h, m * c_new + (1.0 - m) * c", "h, c = m * h_new, m * c_new"),
+])
+def test_planted_mask_forward_mistakes_fail_truncation(old, new):
+    mut = _mutant(old, new)
+    params, x, h0, c0, dy, dhy, dcy = _len_case("lstm", False, 1, True, 35)
+    lengths = [4, 6, 0, 1]
+    f = mut.rnn_forward("lstm", False, params, x, h0, c0, True, lengths=lengths)
+    ok = True
+    for b, n in enumerate(lengths):
+        if n == 0:
+            ok = ok and np.array_equal(f["hy"][:, b], h0[:, b]) and np.all(f["y"][:, b] == 0)
+            continue
+        fb = O.rnn_forward("lstm", False, params, x[:n, b:b + 1], h0[:, b:b + 1], c0[:, b:b + 1], True)
+        ok = ok and np.allclose(f["y"][:, b:b + 1], np.concatenate(
+            [fb["y"], np.zeros((x.shape[0] - n, 1, fb["y"].shape[2]))], axis=0)) and np.allclose(
+            f["hy"][:, b:b + 1], fb["hy"])
+    assert not ok
