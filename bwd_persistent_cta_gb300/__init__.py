@@ -49,6 +49,7 @@ _SIGS = {
     "rnn_backward_weights": (ctypes.c_int, [_P] * 8),
     "rnn_sync_status": (ctypes.c_int, [_P, _P]),
     "rnn_set_timeout_ns": (ctypes.c_int, [_P, ctypes.c_uint64]),
+    "rnn_set_seq_lengths": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int)]),
     "rnn_launch_count": (ctypes.c_uint64, [_P]),
     "rnn_selected_algo": (ctypes.c_int, [_P]),
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
@@ -140,6 +141,14 @@ def rnn_sync_status(handle, stream=None) -> int:
 
 def rnn_set_timeout_ns(handle, ns: int) -> int:
     return lib().rnn_set_timeout_ns(handle, int(ns))
+
+
+def rnn_set_seq_lengths(handle, lengths) -> int:
+    """lengths: a sequence of batch ints in [0, seq_len], or None for full length."""
+    if lengths is None:
+        return lib().rnn_set_seq_lengths(handle, None)
+    arr = (ctypes.c_int * len(lengths))(*[int(v) for v in lengths])
+    return lib().rnn_set_seq_lengths(handle, arr)
 
 
 def rnn_launch_count(handle) -> int:
@@ -282,6 +291,12 @@ class RNN:
 
     def set_timeout_ns(self, ns: int):
         self._check(rnn_set_timeout_ns(self.handle, ns), "rnn_set_timeout_ns")
+
+    def set_seq_lengths(self, lengths):
+        """Valid steps per sequence (batch ints), or None for full length."""
+        if lengths is not None and len(lengths) != self.desc.batch:
+            raise ValueError("one length per sequence of the batch")
+        self._check(rnn_set_seq_lengths(self.handle, lengths), "rnn_set_seq_lengths")
 
     def debug_skip_arrival(self, cta: int):
         self._check(rnn_debug_skip_arrival(self.handle, cta), "rnn_debug_skip_arrival")

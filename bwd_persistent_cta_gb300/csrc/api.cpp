@@ -261,6 +261,8 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
   h->timeout_ns = 2000000000ull;
   h->skip_cta = -1;
   h->launches = 0;
+  h->d_len = nullptr;
+  h->has_len = 0;
   h->trace = false;
   h->timing = false;
   h->dev = nullptr;
@@ -326,6 +328,8 @@ rnn_status_t rnn_create(const rnn_desc_t* desc, rnn_handle_t* out) {
   h->timeout_ns = 2000000000ull;
   h->skip_cta = -1;
   h->launches = 0;
+  h->d_len = nullptr;
+  h->has_len = 0;
   const char* tr = std::getenv("RNN_TRACE");
   h->trace = tr && tr[0] == '1';
   h->timing = false;
@@ -353,6 +357,7 @@ rnn_status_t rnn_destroy(rnn_handle_t h) {
   for (auto& e : h->events) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
   for (auto& e : h->pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
   if (h->dev) cudaFree(h->dev);
+  if (h->d_len) cudaFree(h->d_len);
   delete h;
   return RNN_OK;
 }
@@ -368,6 +373,24 @@ rnn_status_t rnn_get_sizes(rnn_handle_t h, size_t* wb, size_t* ws, size_t* rs) {
 rnn_status_t rnn_set_timeout_ns(rnn_handle_t h, uint64_t ns) {
   if (!h || ns == 0) return RNN_BAD_PARAM;
   h->timeout_ns = ns;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_set_seq_lengths(rnn_handle_t h, const int* lengths) {
+  if (!h) return RNN_BAD_PARAM;
+  if (!lengths) {
+    h->has_len = 0;
+    return RNN_OK;
+  }
+  for (int b = 0; b < h->B; ++b)
+    if (lengths[b] < 0 || lengths[b] > h->T) return RNN_BAD_PARAM;
+  if (!h->d_len && cudaMalloc(&h->d_len, sizeof(int) * h->B) != cudaSuccess) {
+    h->d_len = nullptr;
+    return RNN_CUDA_ERROR;
+  }
+  if (cudaMemcpy(h->d_len, lengths, sizeof(int) * h->B, cudaMemcpyHostToDevice) != cudaSuccess)
+    return RNN_CUDA_ERROR;
+  h->has_len = 1;
   return RNN_OK;
 }
 
@@ -490,11 +513,13 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
     a.c0 = (h->lstm && cx) ? static_cast<const char*>(cx) + static_cast<size_t>(l) * D * B * H * es : nullptr;
     a.hy = hy ? static_cast<char*>(hy) + static_cast<size_t>(l) * D * B * H * es : nullptr;
     a.cy = (h->lstm && cy) ? static_cast<char*>(cy) + static_cast<size_t>(l) * D * B * H * es : nullptr;
+    a.len = h->has_len ? h->d_len : nullptr;
     RNN_TRY(run_persist(h, a, false, s));
     layer_x = static_cast<char*>(Ybuf) + static_cast<size_t>(B) * D * H * es;   // slot 1
   }
   // y out (rows of slots 1..T)
-  RNN_TRY(count(h, launch_seq_transpose(layer_x, y, T, B, D * H, h->bf16, h->bf16, 0, h->bfirst, D * H, s)));
+  RNN_TRY(count(h, launch_seq_transpose(layer_x, y, T, B, D * H, h->bf16, h->bf16, 0, h->bfirst, D * H, s,
+                                        h->has_len ? h->d_len : nullptr)));
   return cudaGetLastError() == cudaSuccess ? RNN_OK : RNN_CUDA_ERROR;
 }
 
@@ -542,6 +567,7 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
     const size_t so = static_cast<size_t>(l) * D * B * H * es;
     a.dhT = dhy ? static_cast<const char*>(dhy) + so : nullptr;
     a.dcT = (h->lstm && dcy) ? static_cast<const char*>(dcy) + so : nullptr;
+    a.len = h->has_len ? h->d_len : nullptr;
     a.dh0 = dhx ? static_cast<char*>(dhx) + so : nullptr;
     a.dc0 = (h->lstm && dcx) ? static_cast<char*>(dcx) + so : nullptr;
     RNN_TRY(run_persist(h, a, true, s));

@@ -22,6 +22,8 @@ struct rnn_handle_s {
   uint64_t timeout_ns;
   int skip_cta;
   uint64_t launches;
+  int* d_len;                  // device copy of the sequence lengths (B ints), or null
+  int has_len;                 // 1: the lengths in d_len apply
   bool trace;
   bool timing;
   struct Ev { cudaEvent_t a, b; int cls; };

@@ -72,9 +72,10 @@ __global__ void bias_grad_scatter_kernel(const float* __restrict__ db, int H, in
 }
 
 // One output row (t, b) per blockIdx.x, features along threads.
+// Rows (t, b) with t >= len[b] (len non-null) are written as zeros.
 template <typename Ti, typename To, int V>
 __global__ void seq_copy_kernel(const Ti* __restrict__ in, To* __restrict__ out, int T, int B, int F,
-                                int in_bf, int out_bf, int64_t out_ld) {
+                                int in_bf, int out_bf, int64_t out_ld, const int* __restrict__ len) {
   const int64_t r = blockIdx.x;             // output row index in output order
   int t, b;
   if (out_bf) { b = static_cast<int>(r / T); t = static_cast<int>(r % T); }
@@ -82,9 +83,10 @@ __global__ void seq_copy_kernel(const Ti* __restrict__ in, To* __restrict__ out,
   const int64_t ir = in_bf ? (static_cast<int64_t>(b) * T + t) : (static_cast<int64_t>(t) * B + b);
   const Ti* src = in + ir * F;
   To* dst = out + r * out_ld;
+  const bool live = !len || t < len[b];
   for (int f = threadIdx.x * V; f < F; f += blockDim.x * V) {
 #pragma unroll
-    for (int v = 0; v < V; ++v) dst[f + v] = from_f<To>(to_f<Ti>(src[f + v]));
+    for (int v = 0; v < V; ++v) dst[f + v] = from_f<To>(live ? to_f<Ti>(src[f + v]) : 0.0f);
   }
 }
 
@@ -150,7 +152,7 @@ int launch_bias_grad_scatter(const float* db, int H, const int* slot_dst, int is
 }
 
 int launch_seq_transpose(const void* in, void* out, int T, int B, int F, int in_bf16, int out_bf16,
-                         int in_batch_first, int out_batch_first, int64_t out_ld, cudaStream_t s) {
+                         int in_batch_first, int out_batch_first, int64_t out_ld, cudaStream_t s, const int* len) {
   const int64_t rows = static_cast<int64_t>(T) * B;
   if (rows == 0 || F == 0) return 0;
   if (rows > 0x7fffffffLL) return 2;
@@ -163,10 +165,10 @@ int launch_seq_transpose(const void* in, void* out, int T, int B, int F, int in_
   do {                                                                                          \
     if (vec == 4)                                                                               \
       seq_copy_kernel<TI, TO, 4><<<grid, threads, 0, s>>>(static_cast<const TI*>(in),           \
-          static_cast<TO*>(out), T, B, F, in_batch_first, out_batch_first, out_ld);             \
+          static_cast<TO*>(out), T, B, F, in_batch_first, out_batch_first, out_ld, len);        \
     else                                                                                        \
       seq_copy_kernel<TI, TO, 1><<<grid, threads, 0, s>>>(static_cast<const TI*>(in),           \
-          static_cast<TO*>(out), T, B, F, in_batch_first, out_batch_first, out_ld);             \
+          static_cast<TO*>(out), T, B, F, in_batch_first, out_batch_first, out_ld, len);        \
   } while (0)
   if (in_bf16 && out_bf16) RNN_SEQ_COPY(__nv_bfloat16, __nv_bfloat16);
   else if (in_bf16) RNN_SEQ_COPY(__nv_bfloat16, float);

@@ -200,21 +200,27 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
   const int64_t ldP = static_cast<int64_t>(D) * 4 * H;
   const int npairs = nu * B;
   float st[PP];      // LSTM: c_{t-1}; GRU: h_{t-1} (fp32 copy)
+  float hl[PP];      // LSTM: h_{t-1}, held over masked steps
+  int lenp[PP];      // valid steps of the pair's sequence (later steps are masked)
   float zr[PP][2];   // GRU reset-before: r, z between the two phases
   const int slot_h0 = dir ? TT + 1 : 0;
 #pragma unroll
   for (int p = 0; p < PP; ++p) {
-    st[p] = 0.f;
+    st[p] = hl[p] = 0.f;
+    lenp[p] = TT;
     zr[p][0] = zr[p][1] = 0.f;
     const int id = threadIdx.x + p * kThreads;
     if (id >= npairs) continue;
     const int ul = id % nu, b = id / nu, u = u0 + ul;
+    if (a.len) lenp[p] = a.len[b];
+    const float h0 = to_f<T>(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
     if (lstm) {
       const T* c0 = static_cast<const T*>(a.c0);
       st[p] = c0 ? to_f<T>(c0[(static_cast<int64_t>(dir) * B + b) * H + u]) : 0.f;
+      hl[p] = h0;
       if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? TT : 0)) * B + b) * H + u] = st[p];
     } else {
-      st[p] = to_f<T>(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
+      st[p] = h0;
     }
   }
 
@@ -272,14 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
       Vec4<T>::load(P + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u, pv);
       float gv[4];
       float h;
+      const bool live = t < lenp[p];
       if (lstm) {
         const float i = sigm(pv[0] + acc[p][0]);
         const float f = sigm(pv[1] + acc[p][1]);
         const float g = tanhf(pv[2] + acc[p][2]);
         const float o = sigm(pv[3] + acc[p][3]);
-        const float c = f * st[p] + i * g;
+        float c = f * st[p] + i * g;
         h = o * tanhf(c);
+        if (!live) { c = st[p]; h = hl[p]; }
         st[p] = c;
+        hl[p] = h;
         gv[0] = i; gv[1] = f; gv[2] = g; gv[3] = o;
         if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = c;
         if (s == TT - 1 && a.cy)
@@ -290,13 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
         const float z = sigm(pv[1] + acc[p][1] + bh[1]);
         const float hn = acc[p][2] + bh[2];
         const float n = tanhf(pv[2] + r * hn);
-        h = (1.f - z) * n + z * st[p];
+        h = live ? (1.f - z) * n + z * st[p] : st[p];
         st[p] = h;
         gv[0] = r; gv[1] = z; gv[2] = n; gv[3] = hn;
       } else {
         const float r = zr[p][0], z = zr[p][1];
         const float n = tanhf(pv[2] + acc[p][2]);
-        h = (1.f - z) * n + z * st[p];
+        h = live ? (1.f - z) * n + z * st[p] : st[p];
         st[p] = h;
         gv[0] = r; gv[1] = z; gv[2] = n; gv[3] = 0.f;
       }
@@ -344,16 +353,21 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
   const int64_t ldG = static_cast<int64_t>(D) * K4;
   const int npairs = nu * B;
   float carry[PP];     // LSTM dc_next; GRU resetAfter dh*z; reset-before d(rh)*r + dh*z
-  float dhv[PP];       // reset-before: dh_t between its two phases
+                       // (GRU: the whole state gradient over a masked step)
+  float carry_h[PP];   // LSTM: dh passed over masked steps
+  float dhv[PP];       // reset-before: dh_t (masked: the passed gradient) between its two phases
+  int lenp[PP];
   float db[PP][4];
 #pragma unroll
   for (int p = 0; p < PP; ++p) {
-    carry[p] = 0.f;
+    carry[p] = carry_h[p] = 0.f;
     dhv[p] = 0.f;
+    lenp[p] = TT;
     db[p][0] = db[p][1] = db[p][2] = db[p][3] = 0.f;
     const int id = threadIdx.x + p * kThreads;
     if (id >= npairs) continue;
     const int ul = id % nu, b = id / nu, u = u0 + ul;
+    if (a.len) lenp[p] = a.len[b];
     if (lstm && a.dcT) carry[p] = to_f<T>(static_cast<const T*>(a.dcT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
   }
 
@@ -392,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
         if (id >= npairs) break;
         const int ul = id % nu, b = id / nu, u = u0 + ul;
         const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
-        if (a.dh0) static_cast<T*>(a.dh0)[o] = from_f<T>(lstm ? dhr[p] : dhr[p] + carry[p]);
+        if (a.dh0) static_cast<T*>(a.dh0)[o] = from_f<T>(lstm ? dhr[p] + carry_h[p] : dhr[p] + carry[p]);
         if (lstm && a.dc0) static_cast<T*>(a.dc0)[o] = from_f<T>(carry[p]);
       }
       break;
@@ -408,43 +422,62 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
       Vec4<T>::load(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * K4 + 4 * u, gv);
       const float dy = a.dYi[(static_cast<int64_t>(t) * B + b) * ldY + dir * H + u];
       T* dg = dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u;
+      const bool live = t < lenp[p];
       if (lstm) {
-        const float i = gv[0], f = gv[1], g = gv[2], o = gv[3];
-        const float* C = a.C + static_cast<int64_t>(dir) * (TT + 1) * B * H;
-        const float c = C[(static_cast<int64_t>(dir ? t : t + 1) * B + b) * H + u];
-        const float cp = C[(static_cast<int64_t>(dir ? t + 1 : t) * B + b) * H + u];
-        const float dh = dy + dhr[p];
-        const float tc = tanhf(c);
-        const float dc = dh * o * (1.f - tc * tc) + carry[p];
-        float da[4];
-        da[0] = dc * g * i * (1.f - i);
-        da[1] = dc * cp * f * (1.f - f);
-        da[2] = dc * i * (1.f - g * g);
-        da[3] = dh * tc * o * (1.f - o);
-        carry[p] = dc * f;
+        const float gh = dhr[p] + carry_h[p];
+        float da[4] = {0.f, 0.f, 0.f, 0.f};
+        if (live) {
+          const float i = gv[0], f = gv[1], g = gv[2], o = gv[3];
+          const float* C = a.C + static_cast<int64_t>(dir) * (TT + 1) * B * H;
+          const float c = C[(static_cast<int64_t>(dir ? t : t + 1) * B + b) * H + u];
+          const float cp = C[(static_cast<int64_t>(dir ? t + 1 : t) * B + b) * H + u];
+          const float dh = dy + gh;
+          const float tc = tanhf(c);
+          const float dc = dh * o * (1.f - tc * tc) + carry[p];
+          da[0] = dc * g * i * (1.f - i);
+          da[1] = dc * cp * f * (1.f - f);
+          da[2] = dc * i * (1.f - g * g);
+          da[3] = dh * tc * o * (1.f - o);
+          carry[p] = dc * f;
+          carry_h[p] = 0.f;
+        } else {
+          carry_h[p] = gh;
+        }
         Vec4<T>::store(dg, da);
 #pragma unroll
         for (int q = 0; q < 4; ++q) db[p][q] += da[q];
       } else if (!rb) {
-        const float r = gv[0], z = gv[1], n = gv[2], hn = gv[3];
-        const float hp = to_f<T>(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
-        const float dh = dy + dhr[p] + carry[p];
-        const float dn = dh * (1.f - z) * (1.f - n * n);
-        const float dz = dh * (hp - n) * z * (1.f - z);
-        const float dr = dn * hn * r * (1.f - r);
-        float da[4] = {dr, dz, dn, dn * r};
-        carry[p] = dh * z;
+        const float gh = dhr[p] + carry[p];
+        float da[4] = {0.f, 0.f, 0.f, 0.f};
+        if (live) {
+          const float r = gv[0], z = gv[1], n = gv[2], hn = gv[3];
+          const float hp = to_f<T>(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
+          const float dh = dy + gh;
+          const float dn = dh * (1.f - z) * (1.f - n * n);
+          const float dz = dh * (hp - n) * z * (1.f - z);
+          const float dr = dn * hn * r * (1.f - r);
+          da[0] = dr; da[1] = dz; da[2] = dn; da[3] = dn * r;
+          carry[p] = dh * z;
+        } else {
+          carry[p] = gh;
+        }
         Vec4<T>::store(dg, da);
 #pragma unroll
         for (int q = 0; q < 4; ++q) db[p][q] += da[q];
       } else {
         // reset-before, phase A: dn, dz
-        const float z = gv[1], n = gv[2];
-        const float hp = to_f<T>(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
-        const float dh = dy + dhr[p] + carry[p];
-        const float dn = dh * (1.f - z) * (1.f - n * n);
-        const float dz = dh * (hp - n) * z * (1.f - z);
-        dhv[p] = dh;
+        const float gh = dhr[p] + carry[p];
+        float dn = 0.f, dz = 0.f;
+        if (live) {
+          const float z = gv[1], n = gv[2];
+          const float hp = to_f<T>(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
+          const float dh = dy + gh;
+          dn = dh * (1.f - z) * (1.f - n * n);
+          dz = dh * (hp - n) * z * (1.f - z);
+          dhv[p] = dh;
+        } else {
+          dhv[p] = gh;
+        }
         dg[1] = from_f<T>(dz);
         dg[2] = from_f<T>(dn);
         dg[3] = from_f<T>(0.f);
@@ -471,10 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
         Vec4<T>::load(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * K4 + 4 * u, gv);
         const float r = gv[0], z = gv[1];
         const float hp = to_f<T>(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
-        const float dr = drh[p] * hp * r * (1.f - r);
+        const bool live = t < lenp[p];
+        const float dr = live ? drh[p] * hp * r * (1.f - r) : 0.f;
         dG[(static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u] = from_f<T>(dr);
         db[p][0] += dr;
-        carry[p] = drh[p] * r + dhv[p] * z;
+        carry[p] = live ? drh[p] * r + dhv[p] * z : dhv[p];
       }
       cta_arrive(ctr, skip);
       ++phases;
@@ -657,14 +691,19 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_latency_kernel(Persis
   const bool has = id < npairs;
   const int ul = has ? id % nu : 0, b = has ? id / nu : 0, u = u0 + ul;
   const int slot_h0 = dir ? TT + 1 : 0;
-  float st = 0.f;
+  float st = 0.f;     // LSTM: c_{t-1}; GRU: h_{t-1}
+  float hl = 0.f;     // LSTM: h_{t-1}, held over masked steps
+  int lenb = TT;      // valid steps of the pair's sequence
   if (has) {
+    if (a.len) lenb = a.len[b];
+    const float h0 = to_f<T>(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
     if (lstm) {
       const T* c0 = static_cast<const T*>(a.c0);
       st = c0 ? to_f<T>(c0[(static_cast<int64_t>(dir) * B + b) * H + u]) : 0.f;
+      hl = h0;
       if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? TT : 0)) * B + b) * H + u] = st;
     } else {
-      st = to_f<T>(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
+      st = h0;
     }
   }
   unsigned int* ctr = &a.dev->counters[dir];
@@ -695,9 +734,11 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_latency_kernel(Persis
         const float f = sigm(pv[1] + o[BB]);
         const float g = tanhf(pv[2] + o[2 * BB]);
         const float oo = sigm(pv[3] + o[3 * BB]);
-        const float c = f * st + i * g;
+        float c = f * st + i * g;
         h = oo * tanhf(c);
+        if (t >= lenb) { c = st; h = hl; }
         st = c;
+        hl = h;
         gv[0] = i; gv[1] = f; gv[2] = g; gv[3] = oo;
       } else if (!rb) {
         const float* bh = a.bh + dir * 4 * H + 4 * u;
@@ -705,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_latency_kernel(Persis
         z = sigm(pv[1] + o[BB] + bh[1]);
         const float hn = o[2 * BB] + bh[2];
         const float n = tanhf(pv[2] + r * hn);
-        h = (1.f - z) * n + z * st;
+        h = t < lenb ? (1.f - z) * n + z * st : st;
         gv[0] = r; gv[1] = z; gv[2] = n; gv[3] = hn;
       } else {
         r = sigm(pv[0] + o[0]);
@@ -723,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_latency_kernel(Persis
       __syncthreads();
       if (has) {
         const float n = tanhf(pv[2] + out[(nA + ul) * BB + b]);
-        h = (1.f - z) * n + z * st;
+        h = t < lenb ? (1.f - z) * n + z * st : st;
         gv[0] = r; gv[1] = z; gv[2] = n; gv[3] = 0.f;
       }
     }

@@ -27,6 +27,10 @@
 //      backward carries never leave registers - stores the exchanged values,
 //      arrives on the counter, and only then stores what no CTA of this
 //      launch waits for.
+// Variable sequence lengths: at a step t >= len[b] the pair (u, b) keeps its
+// state (h, c) and stores it unchanged, and the backward step writes zero gate
+// gradients and passes the state gradients on (LSTM: an extra register carries
+// dh past such steps).
 // Cluster-uniform abort: every CTA reads the same set of flags after the same
 // barrier, so all CTAs of a cluster leave at the same step (after one more
 // cluster barrier, so no CTA exits while a peer may still touch its shared
@@ -396,21 +400,27 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const uint32_t recv_s = smem_u32(recv);
   const uint32_t src_bytes = static_cast<uint32_t>(P.Npad) * RPC * 4;   // bytes per source rank in recv
 
-  float st[PP];
+  float st[PP];      // LSTM: c_{t-1}; GRU: h_{t-1}
+  float hl[PP];      // LSTM: h_{t-1} (held over masked steps)
+  int lenp[PP];      // valid steps of the pair's sequence
   float bh[PP][3];
 #pragma unroll
   for (int p = 0; p < PP; ++p) {
-    st[p] = 0.f;
+    st[p] = hl[p] = 0.f;
+    lenp[p] = TT;
     bh[p][0] = bh[p][1] = bh[p][2] = 0.f;
     const int id = threadIdx.x + p * kThreads;
     if (id >= npairs) continue;
     const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+    if (a.len) lenp[p] = a.len[b];
+    const float h0 = __bfloat162float(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
     if (lstm) {
       const __nv_bfloat16* c0 = static_cast<const __nv_bfloat16*>(a.c0);
       st[p] = c0 ? __bfloat162float(c0[(static_cast<int64_t>(dir) * B + b) * H + u]) : 0.f;
+      hl[p] = h0;
       if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? TT : 0)) * B + b) * H + u] = st[p];
     } else {
-      st[p] = __bfloat162float(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
+      st[p] = h0;
       const float* bb = a.bh + dir * 4 * H + 4 * u;
       bh[p][0] = bb[0]; bh[p][1] = bb[1]; bh[p][2] = bb[2];
     }
@@ -467,21 +477,24 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       float pv[4];
       unpack4(pq[p], pv);
       float h;
+      const bool live = t < lenp[p];
       if (lstm) {
         const float i = sigm_fast(pv[0] + acc[p].x);
         const float f = sigm_fast(pv[1] + acc[p].y);
         const float gg = tanh_fast(pv[2] + acc[p].z);
         const float o = sigm_fast(pv[3] + acc[p].w);
-        const float c = f * st[p] + i * gg;
+        float c = f * st[p] + i * gg;
         h = o * tanh_fast(c);
+        if (!live) { c = st[p]; h = hl[p]; }
         st[p] = c;
+        hl[p] = h;
         pv[0] = i; pv[1] = f; pv[2] = gg; pv[3] = o;
       } else {
         const float r = sigm_fast(pv[0] + acc[p].x + bh[p][0]);
         const float z = sigm_fast(pv[1] + acc[p].y + bh[p][1]);
         const float hn = acc[p].z + bh[p][2];
         const float n = tanh_fast(pv[2] + r * hn);
-        h = (1.f - z) * n + z * st[p];
+        h = live ? (1.f - z) * n + z * st[p] : st[p];
         st[p] = h;
         pv[0] = r; pv[1] = z; pv[2] = n; pv[3] = hn;
       }
@@ -546,14 +559,19 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const uint32_t recv_s = smem_u32(recv);
   const uint32_t src_bytes = static_cast<uint32_t>(P.Npad) * RPC * 4;
 
-  float carry[PP], db[PP][4];
+  // carry: LSTM dc_next, GRU dh*z (or the whole dh over a masked step);
+  // carry_h: LSTM dh passed over masked steps
+  float carry[PP], carry_h[PP], db[PP][4];
+  int lenp[PP];
 #pragma unroll
   for (int p = 0; p < PP; ++p) {
-    carry[p] = 0.f;
+    carry[p] = carry_h[p] = 0.f;
+    lenp[p] = TT;
     db[p][0] = db[p][1] = db[p][2] = db[p][3] = 0.f;
     const int id = threadIdx.x + p * kThreads;
     if (id >= npairs) continue;
     const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+    if (a.len) lenp[p] = a.len[b];
     if (lstm && a.dcT)
       carry[p] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.dcT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
   }
@@ -623,33 +641,45 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       const float dhr = dhs[p];
       if (s == TT) {
         const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
-        if (a.dh0) static_cast<__nv_bfloat16*>(a.dh0)[o] = __float2bfloat16_rn(lstm ? dhr : dhr + carry[p]);
+        if (a.dh0) static_cast<__nv_bfloat16*>(a.dh0)[o] = __float2bfloat16_rn(lstm ? dhr + carry_h[p] : dhr + carry[p]);
         if (lstm && a.dc0) static_cast<__nv_bfloat16*>(a.dc0)[o] = __float2bfloat16_rn(carry[p]);
         continue;
       }
       float gv[4];
       unpack4(gq[p], gv);
-      float da[4];
+      float da[4] = {0.f, 0.f, 0.f, 0.f};
+      const bool live = t < lenp[p];
       if (lstm) {
-        const float i = gv[0], f = gv[1], gg = gv[2], o = gv[3];
-        const float c = e0[p], cp = e1[p];
-        const float dh = dyv[p] + dhr;
-        const float tc = tanh_fast(c);
-        const float dc = dh * o * (1.f - tc * tc) + carry[p];
-        da[0] = dc * gg * i * (1.f - i);
-        da[1] = dc * cp * f * (1.f - f);
-        da[2] = dc * i * (1.f - gg * gg);
-        da[3] = dh * tc * o * (1.f - o);
-        carry[p] = dc * f;
+        const float gh = dhr + carry_h[p];
+        if (live) {
+          const float i = gv[0], f = gv[1], gg = gv[2], o = gv[3];
+          const float c = e0[p], cp = e1[p];
+          const float dh = dyv[p] + gh;
+          const float tc = tanh_fast(c);
+          const float dc = dh * o * (1.f - tc * tc) + carry[p];
+          da[0] = dc * gg * i * (1.f - i);
+          da[1] = dc * cp * f * (1.f - f);
+          da[2] = dc * i * (1.f - gg * gg);
+          da[3] = dh * tc * o * (1.f - o);
+          carry[p] = dc * f;
+          carry_h[p] = 0.f;
+        } else {
+          carry_h[p] = gh;
+        }
       } else {
-        const float r = gv[0], z = gv[1], n = gv[2], hn = gv[3];
-        const float hp = e0[p];
-        const float dh = dyv[p] + dhr + carry[p];
-        const float dn = dh * (1.f - z) * (1.f - n * n);
-        const float dz = dh * (hp - n) * z * (1.f - z);
-        const float dr = dn * hn * r * (1.f - r);
-        da[0] = dr; da[1] = dz; da[2] = dn; da[3] = dn * r;
-        carry[p] = dh * z;
+        const float gh = dhr + carry[p];
+        if (live) {
+          const float r = gv[0], z = gv[1], n = gv[2], hn = gv[3];
+          const float hp = e0[p];
+          const float dh = dyv[p] + gh;
+          const float dn = dh * (1.f - z) * (1.f - n * n);
+          const float dz = dh * (hp - n) * z * (1.f - z);
+          const float dr = dn * hn * r * (1.f - r);
+          da[0] = dr; da[1] = dz; da[2] = dn; da[3] = dn * r;
+          carry[p] = dh * z;
+        } else {
+          carry[p] = gh;
+        }
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) db[p][q] += da[q];

@@ -68,6 +68,9 @@ struct GemmArgs {
 
 struct PersistArgs {
   int mode = 0, reset_after = 0, is_bf16 = 0;
+  // valid steps per sequence ([B], device) or null = all T; step t of
+  // sequence b is masked when t >= len[b] (state held, zero gate gradients)
+  const int* len = nullptr;
   int T = 0, B = 0, H = 0, D = 1;   // D = directions of the layer (buffer strides)
   int dir0 = 0, ndir = 1;            // directions handled by this launch
   // forward
@@ -125,9 +128,10 @@ int launch_pack_rows(const void* W, int G, int H, int K, const int* slot_src, in
                      void* out, int64_t ld_out, int transpose, cudaStream_t s);
 int launch_pack_bias(const void* b, int H, const int* slot_src, int is_bf16, float* out,
                      cudaStream_t s);
+// len (optional, device [B]): output rows (t, b) with t >= len[b] are zero.
 int launch_seq_transpose(const void* in, void* out, int T, int B, int F, int in_bf16,
                          int out_bf16, int in_batch_first, int out_batch_first,
-                         int64_t out_ld, cudaStream_t s);
+                         int64_t out_ld, cudaStream_t s, const int* len = nullptr);
 int launch_states_to_y(const void* h0, void* Y, int T, int B, int H, int D, int dir,
                        int is_bf16, cudaStream_t s);
 int launch_bias_grad_scatter(const float* db, int H, const int* slot_dst, int is_second,

@@ -163,6 +163,23 @@ rnn_status_t rnn_sync_status(rnn_handle_t handle, void* stream);
 /* Upper bound, in nanoseconds, of every device spin-wait (default 2 s). */
 rnn_status_t rnn_set_timeout_ns(rnn_handle_t handle, uint64_t ns);
 
+/* Variable sequence lengths (poplibs Gru.cpp / Lstm.cpp: the batchwise
+ * time-step limit of the forward and backward loops).  ``lengths``: host
+ * array of desc.batch ints, each in [0, seq_len]; sequence b then has
+ * lengths[b] valid steps, and at every later step t >= lengths[b] (in time
+ * order, for both directions) the step is masked: the state h (and c) is
+ * carried unchanged, the output y_t is zero, and in the backward calls the
+ * state gradients pass through the step while its gate gradients are zero
+ * (so padded positions contribute nothing to dx, dW and db, and dy there is
+ * ignored).  hy / cy are the states after each sequence's last valid step;
+ * the reverse direction starts from hx at t = lengths[b] - 1.
+ * NULL restores full length for every sequence.  The lengths apply to the
+ * following rnn_forward / rnn_backward_data calls (which must see the same
+ * lengths) and are copied synchronously to the handle's device memory, so
+ * call this between uses of the handle.  Returns RNN_BAD_PARAM for a length
+ * outside [0, seq_len], RNN_CUDA_ERROR if the copy fails. */
+rnn_status_t rnn_set_seq_lengths(rnn_handle_t handle, const int* lengths);
+
 /* Number of kernels this handle has launched since it was created. */
 uint64_t rnn_launch_count(rnn_handle_t handle);
 

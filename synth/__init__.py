@@ -52,6 +52,9 @@ class Workload:
     gate_order: Tuple[int, ...] = ()   # empty -> canonical
     forward_only: bool = False
     batch_first: bool = False
+    # variable sequence lengths: None = every sequence has T steps; else the
+    # lengths are drawn uniformly from [ceil(min_len_frac * T), T]
+    min_len_frac: Optional[float] = None
 
     @property
     def gates(self) -> int:
@@ -80,7 +83,8 @@ class Workload:
         return f if self.forward_only else 3.0 * f
 
 
-# The five workloads of the problem statement (sizes, seeds, distributions).
+# The five workloads of the problem statement (sizes, seeds, distributions),
+# and variable-length versions of two of them.
 WORKLOADS: Dict[str, Workload] = {
     "lstm_f32_T16_B4_I32_H32": Workload(
         "lstm_f32_T16_B4_I32_H32", LSTM, False, 1, False, 16, 4, 32, 32, "f32", 0,
@@ -106,6 +110,13 @@ WORKLOADS: Dict[str, Workload] = {
     "lstm_bf16_T1024_B8_H2048": Workload(
         "lstm_bf16_T1024_B8_H2048", LSTM, False, 1, False, 1024, 8, 2048, 2048, "bf16", 4,
         state_std=None, forward_only=True),
+    # variable sequence lengths (lengths uniform in [T/2, T]) on two of the shapes above
+    "gru_ra_bf16_T128_B64_H512_varlen": Workload(
+        "gru_ra_bf16_T128_B64_H512_varlen", GRU, True, 1, False, 128, 64, 512, 512, "bf16", 1,
+        state_std=None, min_len_frac=0.5),
+    "lstm2bi_bf16_T512_B128_H1024_varlen": Workload(
+        "lstm2bi_bf16_T512_B128_H1024_varlen", LSTM, False, 2, True, 512, 128, 1024, 1024, "bf16", 3,
+        state_std=None, min_len_frac=0.5),
 }
 
 
@@ -130,6 +141,7 @@ class Inputs:
     dy: np.ndarray
     dhy: Optional[np.ndarray] = None
     dcy: Optional[np.ndarray] = None
+    lengths: Optional[np.ndarray] = None   # [B] valid steps per sequence, or None (all T)
 
 
 def make_inputs(wl: Workload, batch_subset: Optional[Sequence[int]] = None) -> Inputs:
@@ -165,13 +177,20 @@ def make_inputs(wl: Workload, batch_subset: Optional[Sequence[int]] = None) -> I
         h0 = nrm(wl.state_std, S, B, H).numpy()
         c0 = nrm(wl.state_std, S, B, H).numpy() if wl.mode == LSTM else None
     dy = nrm(wl.dy_std, T, B, wl.dirs * H).numpy()
+    lengths = None
+    if wl.min_len_frac is not None:
+        # a generator of its own, so the draws above do not depend on it
+        gl = torch.Generator(device="cpu").manual_seed(wl.seed + 7919)
+        lo = min(T, int(math.ceil(wl.min_len_frac * T)))
+        lengths = torch.randint(lo, T + 1, (B,), generator=gl).numpy().astype(np.int64)
     if batch_subset is not None:
         idx = np.asarray(list(batch_subset))
         x, dy = x[:, idx], dy[:, idx]
         h0 = None if h0 is None else h0[:, idx]
         c0 = None if c0 is None else c0[:, idx]
+        lengths = None if lengths is None else lengths[idx]
     return Inputs(wl, params, rnd(x), None if h0 is None else rnd(h0),
-                  None if c0 is None else rnd(c0), rnd(dy))
+                  None if c0 is None else rnd(c0), rnd(dy), lengths=lengths)
 
 
 # ----------------------------------------------------------------------------

@@ -59,6 +59,8 @@ def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: i
     rnn = R.RNN(wl.mode, wl.input_size, wl.hidden_size, T, Bt, wl.num_layers, wl.bidirectional, wl.reset_after,
                 wl.dtype, wl.gate_order, wl.batch_first, algo)
     try:
+        if inp.lengths is not None:
+            rnn.set_seq_lengths([int(v) for v in inp.lengths])
         w = to_dev(synth.flatten_params(wl, inp.params), wl)
         xs = synth.to_batch_first(inp.x) if wl.batch_first else inp.x
         x = to_dev(xs, wl)
