@@ -65,6 +65,7 @@ def oracle_worker(spec: str) -> None:
     """Internal mode, run in a fresh process: time the oracle on a bounded
     sample, at least ``reps`` times and until ``budget`` seconds have passed;
     print {"times": [seconds per repeat], "units_per_rep": ...}."""
+    import numpy as np
     import synth
     from oracle import rnn_oracle
     name, cols, budget, reps = spec.split(":")
@@ -76,7 +77,8 @@ def oracle_worker(spec: str) -> None:
         t0 = time.perf_counter()
         rnn_oracle.run_inputs(inp, with_backward=not wl.forward_only)
         times.append(time.perf_counter() - t0)
-    print(json.dumps({"times": times, "units_per_rep": wl.seq_len * cols}))
+    units = wl.seq_len * cols if inp.lengths is None else int(np.sum(inp.lengths))
+    print(json.dumps({"times": times, "units_per_rep": units}))
 
 
 def run_oracle_subprocess(wl, budget_s: float, cols: int, reps: int = 1):
@@ -177,7 +179,8 @@ PROFILE_FOR_CLASS = {
     "persist_bwd": "profiles/persist_bwd_tc_{workload}.md",
     "persist_fwd": "profiles/persist_fwd_tc_{workload}.md",
 }
-KERNEL_SOURCES = ["bwd_persistent_cta_gb300/csrc/persist_tc.cu", "bwd_persistent_cta_gb300/csrc/common.cuh"]
+KERNEL_SOURCES = ["bwd_persistent_cta_gb300/csrc/persist_tc_kernels.cuh", "bwd_persistent_cta_gb300/csrc/persist_tc.cu",
+                  "bwd_persistent_cta_gb300/csrc/common.cuh"]
 
 
 def profiled_traffic(cls: str, workload: str):
@@ -250,6 +253,11 @@ def run_ours(args):
 
     rnn = R.RNN(wl.mode, wl.input_size, wl.hidden_size, wl.seq_len, wl.batch, wl.num_layers, wl.bidirectional,
                 wl.reset_after, wl.dtype, wl.gate_order, wl.batch_first, device=dev)
+    # variable-length workloads: the work is the valid steps (sum of lengths)
+    valid_frac = 1.0
+    if inp.lengths is not None:
+        rnn.set_seq_lengths([int(v) for v in inp.lengths])
+        valid_frac = float(np.sum(inp.lengths)) / (wl.seq_len * wl.batch)
     w = dt(synth.flatten_params(wl, inp.params))
     x, dy, hx, cx = dt(inp.x), dt(inp.dy), dt(inp.h0), dt(inp.c0)
     D = wl.dirs
@@ -325,9 +333,9 @@ def run_ours(args):
     e_ms = max_over_ranks(e_ms / Ke, dist, dev)
     rnn.sync()
 
-    units = wl.seq_len * wl.batch * world
-    value = job_throughput(wl.seq_len * wl.batch, world, ms)
-    tflops = wl.flops() * world / (ms / 1e3) / 1e12
+    units = wl.seq_len * wl.batch * world * valid_frac
+    value = job_throughput(wl.seq_len * wl.batch * valid_frac, world, ms)
+    tflops = wl.flops() * valid_frac * world / (ms / 1e3) / 1e12
     peaks = load_peaks()
     names = R.TIMING_CLASS_NAMES
     per_step = {n: cls_ms[i] / K for i, n in enumerate(names)}
@@ -362,9 +370,13 @@ def run_ours(args):
                        "layers": wl.num_layers, "bidirectional": wl.bidirectional, "seq_len": wl.seq_len,
                        "batch_per_gpu": wl.batch, "input": wl.input_size, "hidden": wl.hidden_size,
                        "seed": wl.seed, "parallelism": f"replicas{world}",
-                       "l2": "flushed (256 MiB write) before every timed step"},
+                       "l2": "flushed (256 MiB write) before every timed step",
+                       **({} if inp.lengths is None else {
+                           "seq_lengths": {"min": int(np.min(inp.lengths)), "max": int(np.max(inp.lengths)),
+                                           "valid_frac": valid_frac,
+                                           "units": "valid timesteps (sum of sequence lengths) x 1"}})},
             "tflops": tflops, "tflops_unit": "TFLOP/s (algorithmic, sum over layers/dirs of 3*2*G*H*(I+H)*B*T)",
-            "e2e": {"value": job_throughput(wl.seq_len * wl.batch, world, e_ms), "unit": UNIT,
+            "e2e": {"value": job_throughput(wl.seq_len * wl.batch * valid_frac, world, e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": int(x.numel() * x.element_size() + dy.numel() * dy.element_size()),
                     "d2h_bytes_per_step": int(dw.numel() * dw.element_size())},
             "gpu_launches": int(launches), "gpu_launches_per_step": launches / K,

@@ -1,0 +1,734 @@
+// persist_tc_kernels.cuh - persistent recurrent kernels on the tcgen05 tensor cores
+// (bf16 operands, fp32 accumulation in tensor memory), forward and backward
+// through time, for LSTM and GRU resetAfter.
+//
+// Work split.  The per-step recurrent contraction is swapped so that the
+// weights are the M=128 operand and the batch is N:
+//   forward   S^T[4H, B]  = W_hh[4H, H] . h_{t-1}^T[H, B]
+//   backward  dh^T[H, B]  = W_hh^T[H, 4H] . dG^T_{t+1}[4H, B]
+// A cluster of KS CTAs owns one 128-row block of the weight operand; CTA rank
+// ks owns the K slice [ks*K/KS, (ks+1)*K/KS) and keeps that 128 x K/KS bf16
+// tile resident in shared memory (loaded once by TMA) for the whole sequence,
+// and owns the 128/KS rows [ks*128/KS, (ks+1)*128/KS) of the result.
+//
+// Each step a CTA
+//   1. waits (bounded) until every CTA of its direction finished the previous
+//      step: one gpu-scope counter per direction, release add / acquire poll;
+//   2. streams its K slice of the previous state (h_{t-1} rows of the layer
+//      output, or the gate gradients of the step after) with TMA through a
+//      ring of 64-column sub-tiles, issuing tcgen05.mma (M=128, N=B rounded up
+//      to 16, K=16) into a TMEM accumulator as sub-tiles land;
+//   3. pushes each accumulator row (tcgen05.ld) straight into the shared
+//      memory of the cluster peer that owns that row (posted distributed
+//      shared-memory stores), together with its abort flag;
+//   4. after one cluster barrier sums the KS partial rows of its own units
+//      from local shared memory, applies the cell (forward) or its derivative
+//      (backward) in registers - the LSTM cell state, the GRU state and the
+//      backward carries never leave registers - stores the exchanged values,
+//      arrives on the counter, and only then stores what no CTA of this
+//      launch waits for.
+// Variable sequence lengths: at a step t >= len[b] the pair (u, b) keeps its
+// state (h, c) and stores it unchanged, and the backward step writes zero gate
+// gradients and passes the state gradients on (LSTM: an extra register carries
+// dh past such steps).
+// Cluster-uniform abort: every CTA reads the same set of flags after the same
+// barrier, so all CTAs of a cluster leave at the same step (after one more
+// cluster barrier, so no CTA exits while a peer may still touch its shared
+// memory).
+//
+// This is the persistent-RNN design of the persistent backward-data kernel
+// fragment (one launch for all steps, weights resident on chip, a per-step
+// exchange between CTAs through global memory) carried to tensor cores, TMA,
+// TMEM and thread-block clusters; the fragment polls its dgates buffer for a
+// -0.0 sentinel where a release/acquire counter is used here.  Cell math:
+// Lstm.cpp lstmCellForwardPassCalcUnits / backwardStepImpl; Gru.cpp
+// gruCellForwardPassCalcUnitsResetAfter / backwardStepImplResetAfter.  The
+// sigmoid and tanh of this bf16 path use the hardware tanh.approx.f32
+// instruction (sigma(x) = 1/2 + tanh(x/2)/2); its relative error (about 2^-11)
+// is below the bf16 storage rounding of the stored states.
+#pragma once
+
+#include <cstdlib>
+
+#include "common.cuh"
+
+namespace rnn {
+
+namespace {
+
+#ifdef RNN_STEP_TRACE
+// Step-phase timestamps (globaltimer, ns) of two CTAs, for latency studies;
+// compiled only with -DRNN_STEP_TRACE.
+__device__ unsigned long long g_step_trace[2][2][1100][16];
+#define RNN_TRACE_AT(slot_, kind_, step_)                                                        \
+  do {                                                                                          \
+    if (threadIdx.x == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1) && blockIdx.y == 0 && \
+        (step_) < 1100)                                                                          \
+      g_step_trace[(kind_)][blockIdx.x == 0 ? 0 : 1][(step_)][(slot_)] = globaltimer_ns();       \
+  } while (0)
+#else
+#define RNN_TRACE_AT(slot_, kind_, step_) do { } while (0)
+#endif
+
+constexpr int kThreads = 256;             // warps 0-3 read TMEM; all 8 run the cell epilogue
+constexpr int kSubK = 64;                 // K columns per 128-byte swizzled sub-tile
+constexpr int kWSub = 128 * kSubK * 2;    // bytes of one 128 x 64 weight sub-tile
+constexpr int kMaxKS = 16;
+constexpr int kMaxRing = 16;
+constexpr size_t kSmemCap = 227 * 1024;
+constexpr size_t kMinSmem = 80 * 1024;    // at most two CTAs per SM: TMEM (<= 256 cols each) fits
+constexpr size_t kOneCtaSmem = 116 * 1024; // one CTA per SM (it holds all 512 TMEM columns)
+
+struct TcPersistParams {
+  PersistArgs a;
+  int KS, Kc, nsub, R, Npad, UPC, RPC;
+  int w_tmem;              // weight tile in tensor memory (A operand from TMEM) instead of shared memory
+  int single;              // the whole K slice arrives with one 4-D TMA per step (R == nsub)
+  uint32_t wcol;           // first TMEM column of the weight tile (w_tmem)
+  unsigned int nblk_dir;   // CTAs per direction
+  uint32_t tmem_cols;
+  uint32_t off_ring, off_recv, off_bar;
+};
+
+struct TcBars {
+  uint64_t wbar;                 // resident weight tile landed (TMA)
+  uint64_t mma;                  // this step's MMAs finished (tcgen05.commit)
+  uint64_t full[kMaxRing];       // exchange sub-tile landed (TMA)
+  uint64_t empty[kMaxRing];      // exchange sub-tile consumed (tcgen05.commit)
+  int flags[2][kMaxKS];          // abort flags pushed by the peers, by step parity
+  uint32_t tmem;
+};
+
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigm_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
+
+// Generic address of ``p`` (a shared-memory location) in CTA ``rank`` of the
+// cluster; plain loads and stores through it reach distributed shared memory.
+template <typename T>
+__device__ __forceinline__ T* peer_ptr(T* p, int rank) {
+  uint64_t g;
+  asm("mapa.u64 %0, %1, %2;" : "=l"(g) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<T*>(g);
+}
+
+// The MMAs of sub-tile j (64 K columns) of the K slice, exchange operand in
+// ring slot ``slot``.
+__device__ __forceinline__ void mma_subtile(const TcPersistParams& P, uint32_t tmem, uint64_t adesc0,
+                                            uint64_t bdesc0, uint32_t rbytes, uint32_t idesc, int j, int slot) {
+  const uint64_t bd = bdesc0 + static_cast<uint64_t>((slot * rbytes) >> 4);
+  if (P.w_tmem) {
+    // K=16 bf16 = 8 TMEM columns
+    const uint32_t at = tmem + P.wcol + static_cast<uint32_t>(j * (kSubK / 2));
+#pragma unroll
+    for (int k = 0; k < kSubK / 16; ++k) mma_bf16_ts(tmem, at + 8 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
+  } else {
+    const uint64_t ad = adesc0 + static_cast<uint64_t>((j * kWSub) >> 4);
+#pragma unroll
+    for (int k = 0; k < kSubK / 16; ++k)   // +32 bytes per K=16 step inside the swizzle atom
+      mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
+  }
+}
+
+// One step's contraction: bring the exchange operand's K slice into shared
+// memory and accumulate into TMEM.  Called by thread 0 only.  Either one 4-D
+// TMA brings the whole slice (chunk j at ring + j * rbytes), or nsub 2-D loads
+// stream through a ring of R slots.  g: running load counter (across steps).
+// (x0, y0): 2-D coordinates of the slice; (c2, dir): its chunk and direction
+// coordinates in the 4-D view.  Returns false on timeout.
+__device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, const CUtensorMap* tmX4,
+                              uint8_t* ring, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0, int c2,
+                              int dir, uint32_t idesc, uint64_t adesc0, bool first_use_w, int tk, int s) {
+  (void)tk; (void)s;
+  const int nsub = P.nsub, R = P.R;
+  const uint32_t rbytes = static_cast<uint32_t>(P.Npad) * 128;
+  const uint64_t to = P.a.timeout_ns;
+  const uint64_t bdesc0 = sdesc_sw128(smem_u32(ring), 16, 1024);
+  if (P.single) {
+    // the previous step's MMAs on the ring finished before this CTA released
+    // that step, and every CTA's did before the counter let this load start
+    mbar_arrive_expect_tx(&bars.full[0], static_cast<uint32_t>(nsub) * rbytes);
+    tma_load_4d(ring, tmX4, &bars.full[0], 0, y0, c2, dir);
+    RNN_TRACE_AT(1, tk, s);
+    if (first_use_w && !P.w_tmem && !mbar_wait(&bars.wbar, 0, to)) return false;
+    if (!mbar_wait(&bars.full[0], g & 1, to)) return false;
+    RNN_TRACE_AT(8, tk, s);
+    RNN_TRACE_AT(14, tk, s);
+    tc_fence_after();
+    for (int j = 0; j < nsub; ++j) mma_subtile(P, tmem, adesc0, bdesc0, rbytes, idesc, j, j);
+    mma_commit(&bars.mma);
+    g += 1;
+    return true;
+  }
+  const uint32_t g0 = g;
+  for (int j = 0; j < nsub && j < R; ++j) {
+    const uint32_t gg = g0 + j;
+    const int slot = gg % R;
+    if (gg >= static_cast<uint32_t>(R) && !mbar_wait(&bars.empty[slot], ((gg / R) - 1) & 1, to)) return false;
+    mbar_arrive_expect_tx(&bars.full[slot], rbytes);
+    tma_load_2d(ring + slot * rbytes, tmX, &bars.full[slot], x0 + j * kSubK, y0);
+  }
+  RNN_TRACE_AT(1, tk, s);
+  if (first_use_w && !P.w_tmem && !mbar_wait(&bars.wbar, 0, to)) return false;
+  for (int j = 0; j < nsub; ++j) {
+    const uint32_t gg = g0 + j;
+    const int slot = gg % R;
+    if (!mbar_wait(&bars.full[slot], (gg / R) & 1, to)) return false;
+    if (j == 0) RNN_TRACE_AT(8, tk, s);
+    if (j == nsub - 1) RNN_TRACE_AT(14, tk, s);
+    tc_fence_after();
+    mma_subtile(P, tmem, adesc0, bdesc0, rbytes, idesc, j, slot);
+    mma_commit(&bars.empty[slot]);
+    const int jn = j + R;
+    if (jn < nsub) {
+      const uint32_t gn = g0 + jn;
+      if (!mbar_wait(&bars.empty[slot], ((gn / R) - 1) & 1, to)) return false;
+      mbar_arrive_expect_tx(&bars.full[slot], rbytes);
+      tma_load_2d(ring + slot * rbytes, tmX, &bars.full[slot], x0 + jn * kSubK, y0);
+    }
+  }
+  mma_commit(&bars.mma);
+  g = g0 + nsub;
+  return true;
+}
+
+// TMEM accumulator rows -> the owning peer's receive buffer
+// recv[src = this rank][column][row within the owner].  Warps w and w + 4 read
+// the same TMEM lane quarter (32 * (w % 4) ..) and split the 32-column chunks.
+__device__ __forceinline__ void push_partials(const TcPersistParams& P, uint32_t tmem, float* recv, int ks) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3, half = warp >> 2;
+  const int row = q * 32 + lane;
+  const int owner = row / P.RPC, lr = row - owner * P.RPC;
+  float* dst = peer_ptr(recv, owner) + static_cast<size_t>(ks) * P.Npad * P.RPC + lr;
+  for (int c = half * 32; c < P.Npad; c += 64) {
+    float v[32];
+    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (c + j < P.Npad) dst[(c + j) * P.RPC] = v[j];
+  }
+}
+
+// The per-step exchange and contraction, up to the point where this CTA's
+// units' summed pre-activations can be read from ``recv``.  Returns true when
+// the whole cluster may continue.
+__device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, const CUtensorMap* tmX4,
+                              uint8_t* ring, float* recv, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0,
+                              int c2, int dir, uint32_t idesc,
+                              uint64_t adesc0, bool do_contract, unsigned int wait_target, int s, int ks, int& n_mma,
+                              bool& w_waited, unsigned int kernel) {
+  const PersistArgs& a = P.a;
+  const int tk = kernel == K_BWD_TC ? 1 : 0;
+  (void)tk;
+  int ok = 1;
+  if (threadIdx.x == 0) {
+    if (wait_target > 0 && !wait_counter_geq(&a.dev->counters[a.dir0 + blockIdx.y], wait_target, a.timeout_ns)) {
+      ok = 0;
+      report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_COUNTER);
+    }
+    RNN_TRACE_AT(7, tk, s);
+    if (ok && do_contract) {
+      if (!contract_step(P, tmX, tmX4, ring, bars, tmem, g, x0, y0, c2, dir, idesc, adesc0, !w_waited, tk, s)) {
+        ok = 0;
+        report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_TMA);
+      }
+      w_waited = true;
+    }
+    RNN_TRACE_AT(2, tk, s);
+  }
+  ok = __syncthreads_and(ok);
+  if (ok && do_contract) {
+    const bool done = mbar_wait(&bars.mma, n_mma & 1, a.timeout_ns);
+    ++n_mma;
+    if (!done) report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_MMA);
+    RNN_TRACE_AT(3, tk, s);
+    ok = __syncthreads_and(done ? 1 : 0);
+    if (ok) {
+      tc_fence_after();
+      push_partials(P, tmem, recv, ks);
+    }
+  }
+  RNN_TRACE_AT(9, tk, s);
+  if (static_cast<int>(threadIdx.x) < P.KS) *peer_ptr(&bars.flags[s & 1][ks], threadIdx.x) = ok ? 0 : 1;
+  tc_fence_before();
+  if (P.KS > 1) cluster_sync(); else __syncthreads();
+  tc_fence_after();
+  RNN_TRACE_AT(10, tk, s);
+  int any = 0;
+#pragma unroll
+  for (int r = 0; r < kMaxKS; ++r)
+    if (r < P.KS) any |= bars.flags[s & 1][r];
+  RNN_TRACE_AT(4, tk, s);
+  return any == 0;
+}
+
+// After the exchange-critical stores of a step.  Each thread orders its own
+// generic-proxy stores before the TMA (async-proxy) reads that other CTAs issue
+// once they observe the counter; the barrier orders every thread's stores
+// before the release add.  Fencing here, on the writer side, keeps the fence
+// off the reader's critical path, where it would also wait for the reader's
+// own outstanding prefetch loads.
+__device__ __forceinline__ void step_arrive(const PersistArgs& a, bool skip, int s, int tk) {
+  (void)s; (void)tk;
+  fence_proxy_async_global();
+  __syncthreads();
+  RNN_TRACE_AT(11, tk, s);
+  if (threadIdx.x == 0 && !skip) red_release_gpu_add(&a.dev->counters[a.dir0 + blockIdx.y], 1u);
+}
+
+__device__ __forceinline__ uint2 ld_u2(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
+
+// Explicit shared-memory loads: the compiler cannot mistake them for global
+// accesses that might alias the epilogue's stores, so they issue together.
+__device__ __forceinline__ float4 lds_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float lds_f1(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void unpack4(uint2 q, float (&v)[4]) {
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&q.x);
+  __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&q.y);
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+}
+
+// Barriers, TMEM, and the resident weight tile: 128 rows from row wy0, K
+// columns from column wx0 of the packed weight matrix w (leading dimension
+// ldw), either by TMA into shared memory or, with w_tmem, by every thread
+// through registers into TMEM columns [wcol, wcol + Kc/2) (lane = row).
+__device__ __forceinline__ void setup(const TcPersistParams& P, const CUtensorMap* tmW, const CUtensorMap* tmX,
+                                      const CUtensorMap* tmX4, uint8_t* wsm, TcBars& bars, int wx0, int wy0,
+                                      const __nv_bfloat16* w, int64_t ldw) {
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.wbar, 1);
+    mbar_init(&bars.mma, 1);
+    for (int i = 0; i < P.R; ++i) { mbar_init(&bars.full[i], 1); mbar_init(&bars.empty[i], 1); }
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    if (P.single) prefetch_tmap(tmX4); else prefetch_tmap(tmX);
+    if (!P.w_tmem) {
+      prefetch_tmap(tmW);
+      mbar_arrive_expect_tx(&bars.wbar, static_cast<uint32_t>(P.nsub) * kWSub);
+      for (int j = 0; j < P.nsub; ++j) tma_load_2d(wsm + j * kWSub, tmW, &bars.wbar, wx0 + j * kSubK, wy0);
+    }
+  }
+  if ((threadIdx.x >> 5) == 0) {
+    tmem_alloc(&bars.tmem, P.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (P.w_tmem) {
+    // warps w and w + 4 share lane quarter w % 4 and split the K columns
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, half = warp >> 2;
+    const int ncol = P.Kc / 4;   // 32-bit columns per half
+    const __nv_bfloat16* src = w + (static_cast<int64_t>(wy0) + q * 32 + lane) * ldw + wx0 + half * (P.Kc / 2);
+    const uint32_t trow = bars.tmem + (static_cast<uint32_t>(q * 32) << 16) + P.wcol + static_cast<uint32_t>(half * ncol);
+    for (int c = 0; c < ncol; c += 32) {
+      const uint4* p4 = reinterpret_cast<const uint4*>(src + 2 * c);
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = p4[i];
+        r[4 * i] = v.x; r[4 * i + 1] = v.y; r[4 * i + 2] = v.z; r[4 * i + 3] = v.w;
+      }
+      tmem_st_32x32b_x32(trow + c, r);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+}
+
+__device__ __forceinline__ void teardown(const TcPersistParams& P, TcBars& bars) {
+  tc_fence_before();
+  if (P.KS > 1) cluster_sync(); else __syncthreads();
+  tc_fence_after();
+  if ((threadIdx.x >> 5) == 0) tmem_dealloc(bars.tmem, P.tmem_cols);
+}
+
+#define RNN_TC_SMEM_VIEW                                                                              \
+  extern __shared__ __align__(1024) uint8_t smem_raw[];                                              \
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &         \
+                                             ~static_cast<uintptr_t>(1023));                          \
+  uint8_t* wsm = base;                                                                                \
+  uint8_t* ring = base + P.off_ring;                                                                  \
+  float* recv = reinterpret_cast<float*>(base + P.off_recv);                                          \
+  TcBars& bars = *reinterpret_cast<TcBars*>(base + P.off_bar)
+
+// ---------------------------------------------------------------------------
+// forward
+// ---------------------------------------------------------------------------
+template <int PP, int KS, bool MASK>
+__global__ void __launch_bounds__(kThreads, 1)
+persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                      const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ TcPersistParams P) {
+  RNN_TC_SMEM_VIEW;
+  const PersistArgs& a = P.a;
+  const int H = a.H, B = a.B, TT = a.T, D = a.D;
+  const int dir = a.dir0 + blockIdx.y;
+  const int ks = static_cast<int>(blockIdx.x) % KS;
+  const int rg = static_cast<int>(blockIdx.x) / KS;
+  const bool lstm = a.mode == 0;
+  constexpr int RPC = 128 / KS;
+
+  setup(P, &tmW, &tmX, &tmX4, wsm, bars, ks * P.Kc, dir * 4 * H + rg * 128, static_cast<const __nv_bfloat16*>(a.Wr),
+        H);
+  const uint32_t tmem = bars.tmem;
+  const uint32_t idesc = idesc_bf16(128, P.Npad, false, false);
+  const uint64_t adesc0 = sdesc_sw128(smem_u32(wsm), 16, 1024);
+
+  __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.Y);
+  const __nv_bfloat16* Pm = static_cast<const __nv_bfloat16*>(a.P);
+  __nv_bfloat16* G = static_cast<__nv_bfloat16*>(a.gates);
+  const int64_t ldY = static_cast<int64_t>(D) * H;
+  const int64_t ldP = static_cast<int64_t>(D) * 4 * H;
+  const int UPC = P.UPC;
+  const int npairs = UPC * B;
+  const int ubase = rg * 32 + ks * UPC;     // first hidden unit of this CTA's epilogue
+  const int slot_h0 = dir ? TT + 1 : 0;
+  const uint32_t recv_s = smem_u32(recv);
+  const uint32_t src_bytes = static_cast<uint32_t>(P.Npad) * RPC * 4;   // bytes per source rank in recv
+
+  float st[PP];      // LSTM: c_{t-1}; GRU: h_{t-1}
+  float hl[PP];      // MASK, LSTM: h_{t-1} (held over masked steps)
+  int lenp[PP];      // MASK: valid steps of the pair's sequence
+  float bh[PP][3];
+#pragma unroll
+  for (int p = 0; p < PP; ++p) {
+    st[p] = hl[p] = 0.f;
+    lenp[p] = TT;
+    bh[p][0] = bh[p][1] = bh[p][2] = 0.f;
+    const int id = threadIdx.x + p * kThreads;
+    if (id >= npairs) continue;
+    const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+    if constexpr (MASK) lenp[p] = a.len[b];
+    if (lstm) {
+      const __nv_bfloat16* c0 = static_cast<const __nv_bfloat16*>(a.c0);
+      st[p] = c0 ? __bfloat162float(c0[(static_cast<int64_t>(dir) * B + b) * H + u]) : 0.f;
+      if constexpr (MASK) hl[p] = __bfloat162float(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
+      if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? TT : 0)) * B + b) * H + u] = st[p];
+    } else {
+      st[p] = __bfloat162float(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
+      const float* bb = a.bh + dir * 4 * H + 4 * u;
+      bh[p][0] = bb[0]; bh[p][1] = bb[1]; bh[p][2] = bb[2];
+    }
+  }
+
+  const bool skip = a.skip_cta == static_cast<int>(blockIdx.x + gridDim.x * blockIdx.y);
+  uint32_t g = 0;
+  int n_mma = 0;
+  bool w_waited = false;
+  for (int s = 0; s < TT; ++s) {
+    const int t = dir ? TT - 1 - s : s;
+    const int sp = dir ? t + 2 : t;
+    const int so = t + 1;
+    RNN_TRACE_AT(0, 0, s);
+    // this step's input projections do not depend on the exchange: load them first
+    uint2 pq[PP];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      pq[p] = id < npairs ? ld_u2(Pm + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u) : make_uint2(0, 0);
+    }
+    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B, ks * P.nsub, dir, idesc,
+                       adesc0, true,
+                       static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_FWD_TC))
+      break;
+    // partial sums of every pair first (all shared loads in flight), then the cell
+    float4 acc[PP];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      const int ul = id % UPC, b = id / UPC;
+      acc[p] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (id < npairs) {
+        const uint32_t ra = recv_s + static_cast<uint32_t>((b * RPC + 4 * ul) * 4);
+        float4 v[KS];
+#pragma unroll
+        for (int r = 0; r < KS; ++r) v[r] = lds_f4(ra + r * src_bytes);
+#pragma unroll
+        for (int r = 0; r < KS; ++r) {
+          acc[p].x += v[r].x; acc[p].y += v[r].y; acc[p].z += v[r].z; acc[p].w += v[r].w;
+        }
+      }
+    }
+    RNN_TRACE_AT(12, 0, s);
+    float hv[PP];
+    float gq[PP][4];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      hv[p] = 0.f;
+      if (id >= npairs) break;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      float pv[4];
+      unpack4(pq[p], pv);
+      float h;
+      if (lstm) {
+        const float i = sigm_fast(pv[0] + acc[p].x);
+        const float f = sigm_fast(pv[1] + acc[p].y);
+        const float gg = tanh_fast(pv[2] + acc[p].z);
+        const float o = sigm_fast(pv[3] + acc[p].w);
+        float c = f * st[p] + i * gg;
+        h = o * tanh_fast(c);
+        if constexpr (MASK) {
+          if (t >= lenp[p]) { c = st[p]; h = hl[p]; }
+          hl[p] = h;
+        }
+        st[p] = c;
+        pv[0] = i; pv[1] = f; pv[2] = gg; pv[3] = o;
+      } else {
+        const float r = sigm_fast(pv[0] + acc[p].x + bh[p][0]);
+        const float z = sigm_fast(pv[1] + acc[p].y + bh[p][1]);
+        const float hn = acc[p].z + bh[p][2];
+        const float n = tanh_fast(pv[2] + r * hn);
+        h = (1.f - z) * n + z * st[p];
+        if constexpr (MASK) {
+          if (t >= lenp[p]) h = st[p];
+        }
+        st[p] = h;
+        pv[0] = r; pv[1] = z; pv[2] = n; pv[3] = hn;
+      }
+      hv[p] = h;
+      gq[p][0] = pv[0]; gq[p][1] = pv[1]; gq[p][2] = pv[2]; gq[p][3] = pv[3];
+      Y[(static_cast<int64_t>(so) * B + b) * ldY + dir * H + u] = __float2bfloat16_rn(h);
+    }
+    RNN_TRACE_AT(13, 0, s);
+    RNN_TRACE_AT(5, 0, s);
+    step_arrive(a, skip, s, 0);
+    RNN_TRACE_AT(6, 0, s);
+    // stores nothing in this launch waits for
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      if (id >= npairs) break;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      if (G) Vec4<__nv_bfloat16>::store(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * 4 * H + 4 * u, gq[p]);
+      if (lstm && a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = st[p];
+      if (s == TT - 1) {
+        const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
+        if (a.hy) static_cast<__nv_bfloat16*>(a.hy)[o] = __float2bfloat16_rn(hv[p]);
+        if (lstm && a.cy) static_cast<__nv_bfloat16*>(a.cy)[o] = __float2bfloat16_rn(st[p]);
+      }
+    }
+  }
+  teardown(P, bars);
+}
+
+// ---------------------------------------------------------------------------
+// backward through time
+// ---------------------------------------------------------------------------
+template <int PP, int KS, bool MASK>
+__global__ void __launch_bounds__(kThreads, 1)
+persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                      const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ TcPersistParams P) {
+  RNN_TC_SMEM_VIEW;
+  const PersistArgs& a = P.a;
+  const int H = a.H, B = a.B, TT = a.T, D = a.D;
+  const int K4 = 4 * H;
+  const int dir = a.dir0 + blockIdx.y;
+  const int ks = static_cast<int>(blockIdx.x) % KS;
+  const int rg = static_cast<int>(blockIdx.x) / KS;
+  const bool lstm = a.mode == 0;
+  constexpr int RPC = 128 / KS;
+
+  setup(P, &tmW, &tmX, &tmX4, wsm, bars, ks * P.Kc, dir * H + rg * 128, static_cast<const __nv_bfloat16*>(a.WrT),
+        4 * H);
+  const uint32_t tmem = bars.tmem;
+  const uint32_t idesc = idesc_bf16(128, P.Npad, false, false);
+  const uint64_t adesc0 = sdesc_sw128(smem_u32(wsm), 16, 1024);
+
+  const __nv_bfloat16* Y = static_cast<const __nv_bfloat16*>(a.Y);
+  const __nv_bfloat16* G = static_cast<const __nv_bfloat16*>(a.gates);
+  __nv_bfloat16* dG = static_cast<__nv_bfloat16*>(a.dG);
+  const float* Cb = a.C ? a.C + static_cast<int64_t>(dir) * (TT + 1) * B * H : nullptr;
+  const int64_t ldY = static_cast<int64_t>(D) * H;
+  const int64_t ldG = static_cast<int64_t>(D) * K4;
+  const int UPC = P.UPC;
+  const int npairs = UPC * B;
+  const int ubase = rg * 128 + ks * UPC;
+  const uint32_t recv_s = smem_u32(recv);
+  const uint32_t src_bytes = static_cast<uint32_t>(P.Npad) * RPC * 4;
+
+  // carry: LSTM dc_next, GRU dh*z (or the whole dh over a masked step);
+  // carry_h: LSTM dh passed over masked steps
+  float carry[PP], carry_h[PP], db[PP][4];
+  float cnext[PP];   // LSTM: the cell state the next step needs as c_t
+  int lenp[PP];
+#pragma unroll
+  for (int p = 0; p < PP; ++p) {
+    carry[p] = carry_h[p] = cnext[p] = 0.f;
+    lenp[p] = TT;
+    db[p][0] = db[p][1] = db[p][2] = db[p][3] = 0.f;
+    const int id = threadIdx.x + p * kThreads;
+    if (id >= npairs) continue;
+    const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+    if constexpr (MASK) lenp[p] = a.len[b];
+    if (lstm && a.dcT)
+      carry[p] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.dcT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
+  }
+
+  const bool skip = a.skip_cta == static_cast<int>(blockIdx.x + gridDim.x * blockIdx.y);
+  uint32_t g = 0;
+  int n_mma = 0;
+  bool w_waited = false;
+  bool aborted = false;
+  for (int s = 0; s <= TT; ++s) {
+    const int tp = dir ? s - 1 : TT - s;     // step processed just before (s >= 1)
+    const int t = dir ? s : TT - 1 - s;
+    const int sp = dir ? t + 2 : t;
+    RNN_TRACE_AT(0, 1, s);
+    // this step's saved forward values and upstream gradient: load before the exchange
+    // (LSTM: c_t is the c_{t-1} the previous step loaded, only c_{t-1} is read)
+    uint2 gq[PP];
+    float e0[PP], e1[PP], dyv[PP];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      gq[p] = make_uint2(0, 0);
+      e0[p] = e1[p] = dyv[p] = 0.f;
+      if (id < npairs && s < TT) {
+        gq[p] = ld_u2(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * K4 + 4 * u);
+        dyv[p] = a.dYi[(static_cast<int64_t>(t) * B + b) * ldY + dir * H + u];
+        if (lstm) {
+          e0[p] = s == 0 ? Cb[(static_cast<int64_t>(dir ? t : t + 1) * B + b) * H + u] : cnext[p];
+          e1[p] = Cb[(static_cast<int64_t>(dir ? t + 1 : t) * B + b) * H + u];
+        } else {
+          e0[p] = __bfloat162float(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
+        }
+      }
+    }
+    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B,
+                       ks * P.nsub, dir, idesc, adesc0, s > 0, static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_BWD_TC)) {
+      aborted = true;
+      break;
+    }
+    // recurrent gradient of every pair first (all shared loads in flight)
+    float dhs[PP];
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      dhs[p] = 0.f;
+      if (id < npairs) {
+        if (s == 0) {
+          if (a.dhT)
+            dhs[p] = __bfloat162float(
+                static_cast<const __nv_bfloat16*>(a.dhT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
+        } else {
+          const uint32_t ra = recv_s + static_cast<uint32_t>((b * RPC + ul) * 4);
+          float v[KS];
+#pragma unroll
+          for (int r = 0; r < KS; ++r) v[r] = lds_f1(ra + r * src_bytes);
+#pragma unroll
+          for (int r = 0; r < KS; ++r) dhs[p] += v[r];
+        }
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      if (id >= npairs) break;
+      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      const float dhr = dhs[p];
+      if (s == TT) {
+        const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
+        if (a.dh0) static_cast<__nv_bfloat16*>(a.dh0)[o] = __float2bfloat16_rn(lstm ? dhr + (MASK ? carry_h[p] : 0.f)
+                                                                                   : dhr + carry[p]);
+        if (lstm && a.dc0) static_cast<__nv_bfloat16*>(a.dc0)[o] = __float2bfloat16_rn(carry[p]);
+        continue;
+      }
+      float gv[4];
+      unpack4(gq[p], gv);
+      float da[4] = {0.f, 0.f, 0.f, 0.f};
+      bool live = true;
+      if constexpr (MASK) live = t < lenp[p];
+      if (lstm) {
+        const float gh = MASK ? dhr + carry_h[p] : dhr;
+        if (live) {
+          const float i = gv[0], f = gv[1], gg = gv[2], o = gv[3];
+          const float c = e0[p], cp = e1[p];
+          const float dh = dyv[p] + gh;
+          const float tc = tanh_fast(c);
+          const float dc = dh * o * (1.f - tc * tc) + carry[p];
+          da[0] = dc * gg * i * (1.f - i);
+          da[1] = dc * cp * f * (1.f - f);
+          da[2] = dc * i * (1.f - gg * gg);
+          da[3] = dh * tc * o * (1.f - o);
+          carry[p] = dc * f;
+          if constexpr (MASK) carry_h[p] = 0.f;
+        } else {
+          carry_h[p] = gh;
+        }
+        cnext[p] = e1[p];
+      } else {
+        const float gh = dhr + carry[p];
+        if (live) {
+          const float r = gv[0], z = gv[1], n = gv[2], hn = gv[3];
+          const float hp = e0[p];
+          const float dh = dyv[p] + gh;
+          const float dn = dh * (1.f - z) * (1.f - n * n);
+          const float dz = dh * (hp - n) * z * (1.f - z);
+          const float dr = dn * hn * r * (1.f - r);
+          da[0] = dr; da[1] = dz; da[2] = dn; da[3] = dn * r;
+          carry[p] = dh * z;
+        } else {
+          carry[p] = gh;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) db[p][q] += da[q];
+      Vec4<__nv_bfloat16>::store(dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u, da);
+    }
+    RNN_TRACE_AT(5, 1, s);
+    if (s < TT) step_arrive(a, skip, s, 1);
+    RNN_TRACE_AT(6, 1, s);
+  }
+
+  if (!aborted) {
+    // bias gradients: reduce each unit's four sums over the batch (reuses recv,
+    // after every peer has finished with it)
+    tc_fence_before();
+    if (KS > 1) cluster_sync(); else __syncthreads();
+    float* red = recv;
+    for (int i = threadIdx.x; i < 4 * UPC; i += kThreads) red[i] = 0.f;
+    __syncthreads();
+#pragma unroll
+    for (int p = 0; p < PP; ++p) {
+      const int id = threadIdx.x + p * kThreads;
+      if (id >= npairs) break;
+      const int ul = id % UPC;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) atomicAdd(&red[ul * 4 + q], db[p][q]);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 4 * UPC; i += kThreads)
+      a.db[static_cast<int64_t>(dir) * K4 + 4 * ubase + i] = red[i];
+  }
+  teardown(P, bars);
+}
+
+}  // namespace
+
+// Kernel entry points by template arguments (PP pairs per thread in 1, 2, 4, 8;
+// K split KS in 1, 2, 4, 8, 16; mask = variable sequence lengths), defined in
+// persist_tc_fwd.cu / persist_tc_bwd.cu so the instances compile in parallel.
+const void* persist_tc_fwd_kernel_ptr(int pp, int ks, int mask);
+const void* persist_tc_bwd_kernel_ptr(int pp, int ks, int mask);
+
+}  // namespace rnn
