@@ -26,9 +26,17 @@ Sources (titles and sections of the pages the method is taken from):
   * SystemDS ``LibMatrixCuDNN.java``: ``lstm`` / ``lstmBackward`` (the
     forward / backward-data / backward-weights split, NULL final-state
     gradient).
+  * Plain RNN cells (the fragment's CUDNN_RNN_RELU / CUDNN_RNN_TANH branch):
+    h' = act(W_ih x + W_hh h + b) with one gate; its backward step multiplies
+    the state gradient by the activation's derivative (ReLU: zero where the
+    output is not positive; tanh: 1 - h'^2).
 
 Readings where the pages are silent (each is listed in the design doc):
-  * cell clipping is off (identity);
+  * LSTM cell clipping (the fragment's clip / dclip on the cell state), when
+    enabled with bounds lo < hi: the state is the raw c, and every use of it
+    goes through clip(x) = min(max(x, lo), hi) (a NaN stays NaN):
+    c_t = f clip(c_{t-1}) + i g, h_t = o tanh(clip(c_t)); cy is the raw c_T;
+    dclip(x) = 1 on [lo, hi], else 0; off by default (identity);
   * LSTM has one bias vector per direction (the sum of cuDNN's two);
   * the GRU update is h' = (1 - z) * n + z * h (both GRU sources agree);
   * resetAfter keeps separate input / recurrent biases, with the recurrent
@@ -54,6 +62,7 @@ from typing import Dict, List, Optional
 import numpy as np
 
 LSTM, GRU = "lstm", "gru"
+RNN_RELU, RNN_TANH = "rnn_relu", "rnn_tanh"   # plain RNN: h' = act(W_ih x + W_hh h + b)
 
 
 def sigmoid(a: np.ndarray) -> np.ndarray:
@@ -64,6 +73,22 @@ def _time_order(T: int, reverse: bool):
     """The reverse direction walks t = T-1 .. 0 over the same inputs
     (direction mapping of the persistent kernel's step loop)."""
     return range(T - 1, -1, -1) if reverse else range(T)
+
+
+def _clip(x, clip):
+    """clip(x) = min(max(x, lo), hi); identity when ``clip`` is None."""
+    if clip is None:
+        return x
+    lo, hi = clip
+    return np.where(x < lo, lo, np.where(x > hi, hi, x))
+
+
+def _dclip(x, clip):
+    """Derivative of _clip: 1 on [lo, hi], 0 outside."""
+    if clip is None:
+        return np.ones_like(x)
+    lo, hi = clip
+    return ((x >= lo) & (x <= hi)).astype(float)
 
 
 def _masks(T: int, B: int, lengths) -> np.ndarray:
@@ -79,11 +104,13 @@ def _masks(T: int, B: int, lengths) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # LSTM, one direction of one layer
 # ----------------------------------------------------------------------------
-def lstm_forward_dir(x, p, h0, c0, reverse=False, lengths=None):
+def lstm_forward_dir(x, p, h0, c0, reverse=False, lengths=None, clip=None):
     """Lstm.cpp, lstmCellForwardPassCalcUnits / basicLstmCellForwardPass:
     a = W_ih x_t + W_hh h_{t-1} + b; i, f, o = sigmoid; g = tanh;
     c' = f c_{t-1} + i g; h' = o tanh(c').  With the step mask m:
-    c_t = m c' + (1-m) c_{t-1}; h_t = m h' + (1-m) h_{t-1}; y_t = m h'."""
+    c_t = m c' + (1-m) c_{t-1}; h_t = m h' + (1-m) h_{t-1}; y_t = m h'.
+    With cell clipping (bounds ``clip``): c' = f clip(c_{t-1}) + i g and
+    h' = o tanh(clip(c'))."""
     T, B, _ = x.shape
     H = p["W_hh"].shape[1]
     M = _masks(T, B, lengths)
@@ -91,6 +118,7 @@ def lstm_forward_dir(x, p, h0, c0, reverse=False, lengths=None):
     y = np.zeros((T, B, H))
     keep = {k: np.zeros((T, B, H)) for k in ("i", "f", "g", "o", "c", "c_prev", "h_prev")}
     keep["m"] = M
+    keep["clip"] = clip
     for t in _time_order(T, reverse):
         m = M[t]
         a = x[t] @ p["W_ih"].T + h @ p["W_hh"].T + p["b"]
@@ -98,8 +126,8 @@ def lstm_forward_dir(x, p, h0, c0, reverse=False, lengths=None):
         f = sigmoid(a[:, 1 * H:2 * H])
         g = np.tanh(a[:, 2 * H:3 * H])
         o = sigmoid(a[:, 3 * H:4 * H])
-        c_new = f * c + i * g
-        h_new = o * np.tanh(c_new)
+        c_new = f * _clip(c, clip) + i * g
+        h_new = o * np.tanh(_clip(c_new, clip))
         for k, v in (("i", i), ("f", f), ("g", g), ("o", o), ("c", c_new),
                      ("c_prev", c), ("h_prev", h)):
             keep[k][t] = v
@@ -119,24 +147,29 @@ def lstm_backward_dir(x, p, keep, dy, dhT, dcT, reverse=False):
     Weight gradients (basicLstmParamUpdate): dW_ih = sum da x^T,
     dW_hh = sum da h_{t-1}^T, db = sum da.
     Masked step (m = 0): the gate gradients are zero and dh_rec, dc_next pass
-    through unchanged; dy_t does not reach the state."""
+    through unchanged; dy_t does not reach the state.  With cell clipping
+    (the fragment's LSTM branch): dc = dh o (1 - tanh^2 clip(c_t)) dclip(c_t)
+    + dc_next, da_f uses clip(c_{t-1}), da_o uses tanh(clip(c_t)), and
+    dc_next <- dc f dclip(c_{t-1})."""
     T, B, I = x.shape
     H = p["W_hh"].shape[1]
     M = keep["m"]
+    clip = keep.get("clip")
     dA = np.zeros((T, B, 4 * H))
     dh_rec, dc_next = dhT, dcT
     for t in reversed(list(_time_order(T, reverse))):
         m = M[t]
         i, f, g, o = keep["i"][t], keep["f"][t], keep["g"][t], keep["o"][t]
-        tc = np.tanh(keep["c"][t])
+        ct, cp = keep["c"][t], keep["c_prev"][t]
+        tc = np.tanh(_clip(ct, clip))
         dh = m * (dy[t] + dh_rec)
-        dc = dh * o * (1.0 - tc * tc) + m * dc_next
+        dc = dh * o * (1.0 - tc * tc) * _dclip(ct, clip) + m * dc_next
         dA[t, :, 0 * H:1 * H] = dc * g * i * (1.0 - i)
-        dA[t, :, 1 * H:2 * H] = dc * keep["c_prev"][t] * f * (1.0 - f)
+        dA[t, :, 1 * H:2 * H] = dc * _clip(cp, clip) * f * (1.0 - f)
         dA[t, :, 2 * H:3 * H] = dc * i * (1.0 - g * g)
         dA[t, :, 3 * H:4 * H] = dh * tc * o * (1.0 - o)
         dh_rec = dA[t] @ p["W_hh"] + (1.0 - m) * dh_rec
-        dc_next = dc * f + (1.0 - m) * dc_next
+        dc_next = dc * f * _dclip(cp, clip) + (1.0 - m) * dc_next
     dx = dA @ p["W_ih"]
     flat = dA.reshape(T * B, 4 * H)
     grads = {"W_ih": flat.T @ x.reshape(T * B, I),
@@ -278,14 +311,69 @@ def gru_rb_backward_dir(x, p, keep, dy, dhT, reverse=False):
 
 
 # ----------------------------------------------------------------------------
+# plain RNN (ReLU / tanh), one direction of one layer
+# ----------------------------------------------------------------------------
+def _act(mode, a):
+    return np.maximum(a, 0.0) if mode == RNN_RELU else np.tanh(a)
+
+
+def _dact_from_out(mode, h):
+    """Activation derivative expressed through its output, as the fragment's
+    backward branch does: ReLU 1 where h > 0 else 0; tanh 1 - h^2."""
+    return (h > 0.0).astype(float) if mode == RNN_RELU else 1.0 - h * h
+
+
+def rnn_plain_forward_dir(mode, x, p, h0, reverse=False, lengths=None):
+    """h' = act(W_ih x_t + W_hh h_{t-1} + b); with the step mask m:
+    h_t = m h' + (1-m) h_{t-1}; y_t = m h'."""
+    T, B, _ = x.shape
+    H = p["W_hh"].shape[1]
+    M = _masks(T, B, lengths)
+    h = h0
+    y = np.zeros((T, B, H))
+    keep = {k: np.zeros((T, B, H)) for k in ("h", "h_prev")}
+    keep["m"] = M
+    for t in _time_order(T, reverse):
+        m = M[t]
+        h_new = _act(mode, x[t] @ p["W_ih"].T + h @ p["W_hh"].T + p["b"])
+        keep["h"][t], keep["h_prev"][t] = h_new, h
+        y[t] = m * h_new
+        h = m * h_new + (1.0 - m) * h
+    return y, h, keep
+
+
+def rnn_plain_backward_dir(mode, x, p, keep, dy, dhT, reverse=False):
+    """The fragment's plain-RNN branch: da = (dy_t + dh_rec) act'(h'),
+    dh_rec <- W_hh^T da (masked steps: da = 0, dh_rec passes through).
+    Weight gradients dW_ih = sum da x^T, dW_hh = sum da h_{t-1}^T,
+    db = sum da."""
+    T, B, I = x.shape
+    H = p["W_hh"].shape[1]
+    M = keep["m"]
+    dA = np.zeros((T, B, H))
+    dh_rec = dhT
+    for t in reversed(list(_time_order(T, reverse))):
+        m = M[t]
+        dA[t] = m * (dy[t] + dh_rec) * _dact_from_out(mode, keep["h"][t])
+        dh_rec = dA[t] @ p["W_hh"] + (1.0 - m) * dh_rec
+    dx = dA @ p["W_ih"]
+    flat = dA.reshape(T * B, H)
+    grads = {"W_ih": flat.T @ x.reshape(T * B, I),
+             "W_hh": flat.T @ keep["h_prev"].reshape(T * B, H),
+             "b": flat.sum(axis=0)}
+    return dx, dh_rec, grads, dA
+
+
+# ----------------------------------------------------------------------------
 # Stacked, optionally bidirectional layer
 # ----------------------------------------------------------------------------
 def rnn_forward(mode: str, reset_after: bool, params, x, h0=None, c0=None,
-                bidirectional: bool = False, lengths=None) -> Dict:
+                bidirectional: bool = False, lengths=None, clip=None) -> Dict:
     """Layer l+1 reads layer l's output; a bidirectional layer's output is
     [y_fwd | y_bwd] on the feature axis; NULL initial states are zero.
     ``lengths`` (optional, [B] ints <= T): valid steps per sequence, the same
-    for every layer and direction.
+    for every layer and direction.  ``clip`` (optional, (lo, hi)): LSTM cell
+    clipping bounds.
     Returns y [T,B,D*H], hy [L*D,B,H], cy (LSTM) and a cache for rnn_backward."""
     L, D = len(params), (2 if bidirectional else 1)
     T, B, _ = x.shape
@@ -302,8 +390,10 @@ def rnn_forward(mode: str, reset_after: bool, params, x, h0=None, c0=None,
             p = params[l][d]
             if mode == LSTM:
                 y, hT, cT, keep = lstm_forward_dir(layer_in, p, h0[s], c0[s], reverse=(d == 1),
-                                                   lengths=lengths)
+                                                   lengths=lengths, clip=clip)
                 cy[s] = cT
+            elif mode in (RNN_RELU, RNN_TANH):
+                y, hT, keep = rnn_plain_forward_dir(mode, layer_in, p, h0[s], reverse=(d == 1), lengths=lengths)
             elif reset_after:
                 y, hT, keep = gru_ra_forward_dir(layer_in, p, h0[s], reverse=(d == 1), lengths=lengths)
             else:
@@ -348,6 +438,9 @@ def rnn_backward(mode: str, reset_after: bool, params, fwd: Dict, dy,
                 dxd, dh0, dc0, g, dg = lstm_backward_dir(layer_in, p, per_dir[d], dyd,
                                                          dhy[s], dcy[s], reverse=(d == 1))
                 dcx[s] = dc0
+            elif mode in (RNN_RELU, RNN_TANH):
+                dxd, dh0, g, dg = rnn_plain_backward_dir(mode, layer_in, p, per_dir[d], dyd,
+                                                         dhy[s], reverse=(d == 1))
             elif reset_after:
                 dxd, dh0, g, dg = gru_ra_backward_dir(layer_in, p, per_dir[d], dyd,
                                                       dhy[s], reverse=(d == 1))
@@ -381,7 +474,7 @@ def run_inputs(inp, with_backward: bool = True) -> Dict:
     .x, .h0, .c0, .dy, .dhy, .dcy) through forward (+ backward)."""
     wl = inp.wl
     f = rnn_forward(wl.mode, wl.reset_after, inp.params, inp.x, inp.h0, inp.c0, wl.bidirectional,
-                    lengths=getattr(inp, "lengths", None))
+                    lengths=getattr(inp, "lengths", None), clip=getattr(inp, "clip", None))
     out = {"y": f["y"], "hy": f["hy"]}
     if wl.mode == LSTM:
         out["cy"] = f["cy"]

@@ -65,7 +65,8 @@ def test_golden_scalar_cases(name):
     p = _scalar_params(case)
     h0 = np.full((1, 1, 1), case["h0"])
     c0 = np.full((1, 1, 1), case["c0"])
-    f = O.rnn_forward(case["mode"], case["reset_after"], [[p]], x, h0, c0)
+    clip = tuple(case["clip"]) if "clip" in case else None
+    f = O.rnn_forward(case["mode"], case["reset_after"], [[p]], x, h0, c0, clip=clip)
     np.testing.assert_allclose(f["y"][:, 0, 0], case["expect_h"], rtol=0, atol=1e-14)
     if "expect_c" in case:
         keep = f["cache"][0][1][0]
@@ -76,7 +77,7 @@ def test_golden_scalar_cases(name):
 
 
 def _rand_params(rng, mode, reset_after, L, D, I, H, scale=0.5):
-    G = 4 if mode == "lstm" else 3
+    G = 4 if mode == "lstm" else (3 if mode == "gru" else 1)
     params = []
     for l in range(L):
         per = []
@@ -162,8 +163,12 @@ def _torch_run(mode, params, x, h0, c0, dy, dhy, dcy, bidirectional):
     L, D = len(params), len(params[0])
     T, B, I = x.shape
     H = params[0][0]["W_hh"].shape[1]
-    cls = torch.nn.LSTM if mode == "lstm" else torch.nn.GRU
-    m = cls(I, H, num_layers=L, bidirectional=bidirectional, dtype=torch.float64)
+    if mode in ("rnn_relu", "rnn_tanh"):
+        m = torch.nn.RNN(I, H, num_layers=L, nonlinearity=mode[4:], bidirectional=bidirectional,
+                         dtype=torch.float64)
+    else:
+        cls = torch.nn.LSTM if mode == "lstm" else torch.nn.GRU
+        m = cls(I, H, num_layers=L, bidirectional=bidirectional, dtype=torch.float64)
     with torch.no_grad():
         for l in range(L):
             for d in range(D):
@@ -195,7 +200,9 @@ def _torch_run(mode, params, x, h0, c0, dy, dhy, dcy, bidirectional):
 
 
 @pytest.mark.parametrize("mode,L,bidir", [("lstm", 1, False), ("lstm", 2, True),
-                                          ("gru", 1, False), ("gru", 2, True)])
+                                          ("gru", 1, False), ("gru", 2, True),
+                                          ("rnn_relu", 1, False), ("rnn_relu", 2, True),
+                                          ("rnn_tanh", 1, False), ("rnn_tanh", 2, True)])
 def test_matches_torch_fp64(mode, L, bidir):
     rng = np.random.default_rng(11)
     T, B, I, H = 6, 3, 5, 4
@@ -228,7 +235,7 @@ def test_matches_torch_fp64(mode, L, bidir):
             np.testing.assert_allclose(g["b"], getattr(m, "bias_ih" + sfx).grad.numpy(), **tol)
             if mode == "gru":
                 np.testing.assert_allclose(g["b_h"], getattr(m, "bias_hh" + sfx).grad.numpy(), **tol)
-            else:  # one LSTM bias: its gradient equals both of torch's
+            else:  # one LSTM / plain-RNN bias: its gradient equals both of torch's
                 np.testing.assert_allclose(g["b"], getattr(m, "bias_hh" + sfx).grad.numpy(), **tol)
 
 
@@ -279,22 +286,23 @@ def test_gru_reset_before_equals_reset_after_for_diagonal_Whn():
 # ---------------------------------------------------------------------------
 # central finite differences
 # ---------------------------------------------------------------------------
-def _fd_check(mode, reset_after, L, bidir, oracle=O, seed=13, T=3, B=2, I=3, H=2, rtol=1e-7, lengths=None):
+def _fd_check(mode, reset_after, L, bidir, oracle=O, seed=13, T=3, B=2, I=3, H=2, rtol=1e-7, lengths=None,
+              clip=None, state_scale=1.0):
     rng = np.random.default_rng(seed)
     D = 2 if bidir else 1
     params = _rand_params(rng, mode, reset_after, L, D, I, H, 0.8)
     x = rng.normal(size=(T, B, I))
     h0 = rng.normal(size=(L * D, B, H))
-    c0 = rng.normal(size=(L * D, B, H)) if mode == "lstm" else None
+    c0 = rng.normal(size=(L * D, B, H)) * state_scale if mode == "lstm" else None
     dy = rng.normal(size=(T, B, D * H))
     dhy = rng.normal(size=(L * D, B, H))
     dcy = rng.normal(size=(L * D, B, H)) if mode == "lstm" else None
 
     def loss():
-        f = oracle.rnn_forward(mode, reset_after, params, x, h0, c0, bidir, lengths=lengths)
+        f = oracle.rnn_forward(mode, reset_after, params, x, h0, c0, bidir, lengths=lengths, clip=clip)
         return oracle.rnn_loss(mode, f, dy, dhy, dcy)
 
-    f = oracle.rnn_forward(mode, reset_after, params, x, h0, c0, bidir, lengths=lengths)
+    f = oracle.rnn_forward(mode, reset_after, params, x, h0, c0, bidir, lengths=lengths, clip=clip)
     g = oracle.rnn_backward(mode, reset_after, params, f, dy, dhy, dcy, bidir)
     checks = [(x, g["dx"]), (h0, g["dhx"])]
     if mode == "lstm":
@@ -322,7 +330,7 @@ def _fd_check(mode, reset_after, L, bidir, oracle=O, seed=13, T=3, B=2, I=3, H=2
     return worst
 
 
-@pytest.mark.parametrize("mode,reset_after", [("lstm", False), ("gru", True), ("gru", False)])
+@pytest.mark.parametrize("mode,reset_after", [("lstm", False), ("gru", True), ("gru", False), ("rnn_tanh", False)])
 @pytest.mark.parametrize("L,bidir", [(1, False), (2, True)])
 def test_finite_differences(mode, reset_after, L, bidir):
     assert _fd_check(mode, reset_after, L, bidir) < 1e-7
@@ -389,7 +397,8 @@ def _mutant(old, new):
 
 MUTATIONS = [
     # (mode, reset_after, old text, new text)
-    ("lstm", False, "dc = dh * o * (1.0 - tc * tc) + m * dc_next", "dc = dh * o * (1.0 - tc * tc)"),
+    ("lstm", False, "dc = dh * o * (1.0 - tc * tc) * _dclip(ct, clip) + m * dc_next",
+     "dc = dh * o * (1.0 - tc * tc) * _dclip(ct, clip)"),
     ("lstm", False, "dc_next = dc * f", "dc_next = dc * i"),
     ("lstm", False, "dA[t, :, 3 * H:4 * H] = dh * tc * o * (1.0 - o)",
      "dA[t, :, 3 * H:4 * H] = dc * tc * o * (1.0 - o)"),
@@ -402,6 +411,9 @@ MUTATIONS = [
      "dh_rec = drh + dA[t, :, 0:2 * H] @ Wh[0:2 * H] + dh * z"),
     ("gru", False, "f[:, 2 * H:3 * H].T @ keep[\"rh\"].reshape(T * B, H)",
      "f[:, 2 * H:3 * H].T @ keep[\"h_prev\"].reshape(T * B, H)"),
+    ("rnn_tanh", False, "else 1.0 - h * h", "else 1.0 - h"),
+    ("rnn_tanh", False, "dh_rec = dA[t] @ p[\"W_hh\"] + (1.0 - m) * dh_rec\n    dx = dA @ p[\"W_ih\"]\n    flat = dA.reshape(T * B, H)",
+     "dh_rec = dA[t] @ p[\"W_ih\"][:, :H] + (1.0 - m) * dh_rec\n    dx = dA @ p[\"W_ih\"]\n    flat = dA.reshape(T * B, H)"),
 ]
 
 
@@ -440,7 +452,7 @@ def _len_case(mode, reset_after, L, bidir, seed, T=6, B=4, I=3, H=4):
     return params, x, h0, c0, dy, dhy, dcy
 
 
-CELLS = [("lstm", False), ("gru", True), ("gru", False)]
+CELLS = [("lstm", False), ("gru", True), ("gru", False), ("rnn_relu", False), ("rnn_tanh", False)]
 
 
 @pytest.mark.parametrize("mode,reset_after", CELLS)
@@ -510,7 +522,7 @@ def test_lengths_finite_differences(mode, reset_after):
 
 @pytest.mark.parametrize("mode,reset_after,old,new", [
     ("lstm", False, "dh = m * (dy[t] + dh_rec)", "dh = dy[t] + dh_rec"),
-    ("lstm", False, "dc_next = dc * f + (1.0 - m) * dc_next", "dc_next = dc * f"),
+    ("lstm", False, "dc_next = dc * f * _dclip(cp, clip) + (1.0 - m) * dc_next", "dc_next = dc * f * _dclip(cp, clip)"),
     ("gru", True, "dh_rec = dAh[t] @ p[\"W_hh\"] + dh * z + (1.0 - m) * dh_rec",
      "dh_rec = dAh[t] @ p[\"W_hh\"] + dh * z"),
     ("gru", False, "Wh[0:2 * H] + dh * z + (1.0 - m) * dh_rec", "Wh[0:2 * H] + dh * z + dh_rec"),
@@ -539,3 +551,50 @@ def test_planted_mask_forward_mistakes_fail_truncation(old, new):
             [fb["y"], np.zeros((x.shape[0] - n, 1, fb["y"].shape[2]))], axis=0)) and np.allclose(
             f["hy"][:, b:b + 1], fb["hy"])
     assert not ok
+
+
+# ---------------------------------------------------------------------------
+# LSTM cell clipping
+# ---------------------------------------------------------------------------
+def test_clip_with_unreached_bounds_is_identity():
+    params, x, h0, c0, dy, dhy, dcy = _len_case("lstm", False, 2, True, 41)
+    a = O.rnn_forward("lstm", False, params, x, h0, c0, True)
+    b = O.rnn_forward("lstm", False, params, x, h0, c0, True, clip=(-1e9, 1e9))
+    ga = O.rnn_backward("lstm", False, params, a, dy, dhy, dcy, True)
+    gb = O.rnn_backward("lstm", False, params, b, dy, dhy, dcy, True)
+    for k in ("y", "hy", "cy"):
+        assert np.array_equal(a[k], b[k])
+    for k in ("dx", "dhx", "dcx"):
+        assert np.array_equal(ga[k], gb[k])
+
+
+def _clip_case_is_active(seed, clip):
+    """The clipped run differs from the unclipped one, and no cell value sits
+    within the finite-difference step of a bound."""
+    rng = np.random.default_rng(seed)
+    params = _rand_params(rng, "lstm", False, 2, 2, 3, 2, 0.8)
+    x = rng.normal(size=(4, 3, 3))
+    f = O.rnn_forward("lstm", False, params, x, rng.normal(size=(4, 3, 2)), 3.0 * rng.normal(size=(4, 3, 2)), True,
+                      clip=clip)
+    cs = np.concatenate([k["c"].ravel() for _, per in f["cache"] for k in per] +
+                        [k["c_prev"].ravel() for _, per in f["cache"] for k in per])
+    outside = np.sum((cs < clip[0]) | (cs > clip[1]))
+    margin = np.min(np.minimum(np.abs(cs - clip[0]), np.abs(cs - clip[1])))
+    return outside, margin
+
+
+def test_clip_finite_differences():
+    clip = (-0.6, 0.7)
+    outside, margin = _clip_case_is_active(42, clip)
+    assert outside >= 5 and margin > 1e-4
+    assert _fd_check("lstm", False, 2, True, seed=42, T=4, B=3, clip=clip, state_scale=3.0) < 1e-7
+
+
+@pytest.mark.parametrize("old,new", [
+    ("dc = dh * o * (1.0 - tc * tc) * _dclip(ct, clip) + m * dc_next", "dc = dh * o * (1.0 - tc * tc) + m * dc_next"),
+    ("dc_next = dc * f * _dclip(cp, clip) + (1.0 - m) * dc_next", "dc_next = dc * f + (1.0 - m) * dc_next"),
+    ("dc * _clip(cp, clip) * f * (1.0 - f)", "dc * cp * f * (1.0 - f)"),
+])
+def test_planted_clip_mistakes_fail_finite_differences(old, new):
+    mut = _mutant(old, new)
+    assert _fd_check("lstm", False, 2, True, oracle=mut, seed=42, T=4, B=3, clip=(-0.6, 0.7), state_scale=3.0) > 1e-4
