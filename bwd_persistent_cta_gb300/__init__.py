@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librnn.so")
 
 RNN_OK, RNN_BAD_PARAM, RNN_NOT_SUPPORTED, RNN_CUDA_ERROR, RNN_TIMEOUT, RNN_BAD_WORKSPACE, RNN_INTERNAL = range(7)
-RNN_LSTM, RNN_GRU = 0, 1
+RNN_LSTM, RNN_GRU, RNN_RNN_RELU, RNN_RNN_TANH = 0, 1, 2, 3
 RNN_F32, RNN_BF16 = 0, 1
 RNN_ALGO_AUTO, RNN_ALGO_PERSIST_TC, RNN_ALGO_PERSIST_SIMT = 0, 1, 2
 
@@ -50,6 +50,7 @@ _SIGS = {
     "rnn_sync_status": (ctypes.c_int, [_P, _P]),
     "rnn_set_timeout_ns": (ctypes.c_int, [_P, ctypes.c_uint64]),
     "rnn_set_seq_lengths": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int)]),
+    "rnn_set_cell_clip": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_double, ctypes.c_double]),
     "rnn_launch_count": (ctypes.c_uint64, [_P]),
     "rnn_selected_algo": (ctypes.c_int, [_P]),
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
@@ -151,6 +152,10 @@ def rnn_set_seq_lengths(handle, lengths) -> int:
     return lib().rnn_set_seq_lengths(handle, arr)
 
 
+def rnn_set_cell_clip(handle, enable: int, lo: float = 0.0, hi: float = 0.0) -> int:
+    return lib().rnn_set_cell_clip(handle, int(enable), float(lo), float(hi))
+
+
 def rnn_launch_count(handle) -> int:
     return int(lib().rnn_launch_count(handle))
 
@@ -205,7 +210,7 @@ class RNN:
         self.torch = torch
         self.device = torch.device(device if device is not None else "cuda")
         d = rnn_desc_t()
-        d.mode = RNN_LSTM if mode == "lstm" else RNN_GRU
+        d.mode = {"lstm": RNN_LSTM, "gru": RNN_GRU, "rnn_relu": RNN_RNN_RELU, "rnn_tanh": RNN_RNN_TANH}[mode]
         for k, v in enumerate(gate_order):
             d.gate_order[k] = int(v)
         d.reset_after = int(bool(reset_after))
@@ -291,6 +296,13 @@ class RNN:
 
     def set_timeout_ns(self, ns: int):
         self._check(rnn_set_timeout_ns(self.handle, ns), "rnn_set_timeout_ns")
+
+    def set_cell_clip(self, bounds):
+        """LSTM cell clipping to (lo, hi), or None to turn it off."""
+        if bounds is None:
+            self._check(rnn_set_cell_clip(self.handle, 0), "rnn_set_cell_clip")
+        else:
+            self._check(rnn_set_cell_clip(self.handle, 1, bounds[0], bounds[1]), "rnn_set_cell_clip")
 
     def set_seq_lengths(self, lengths):
         """Valid steps per sequence (batch ints), or None for full length."""

@@ -115,11 +115,13 @@ void fill_layout(rnn_handle_s* h) {
 
 // internal slot s -> caller's gate block (-1: zero / not used)
 void slots_fwd(const rnn_handle_s* h, int* m) {
-  if (h->lstm) { for (int s = 0; s < 4; ++s) m[s] = h->pos[s]; }
+  if (h->plain) { m[0] = 0; m[1] = m[2] = m[3] = -1; }
+  else if (h->lstm) { for (int s = 0; s < 4; ++s) m[s] = h->pos[s]; }
   else { m[0] = h->pos[0]; m[1] = h->pos[1]; m[2] = h->pos[2]; m[3] = -1; }
 }
 void slots_bwd_rec(const rnn_handle_s* h, int* m) {
-  if (h->lstm) { for (int s = 0; s < 4; ++s) m[s] = h->pos[s]; }
+  if (h->plain) { m[0] = 0; m[1] = m[2] = m[3] = -1; }
+  else if (h->lstm) { for (int s = 0; s < 4; ++s) m[s] = h->pos[s]; }
   else if (h->ra) { m[0] = h->pos[0]; m[1] = h->pos[1]; m[2] = -1; m[3] = h->pos[2]; }
   else { m[0] = h->pos[0]; m[1] = h->pos[1]; m[2] = h->pos[2]; m[3] = -1; }
 }
@@ -202,14 +204,15 @@ int run_persist(rnn_handle_s* h, PersistArgs a, bool bwd, cudaStream_t s) {
 
 rnn_status_t check_desc(const rnn_desc_t* d) {
   if (!d) return RNN_BAD_PARAM;
-  if (d->mode != RNN_LSTM && d->mode != RNN_GRU) return RNN_BAD_PARAM;
+  if (d->mode != RNN_LSTM && d->mode != RNN_GRU && d->mode != RNN_RNN_RELU && d->mode != RNN_RNN_TANH)
+    return RNN_BAD_PARAM;
   if (d->dtype != RNN_F32 && d->dtype != RNN_BF16) return RNN_BAD_PARAM;
   if (d->num_layers < 1 || d->num_layers > 8) return RNN_BAD_PARAM;
   if (d->seq_len < 1 || d->batch < 1 || d->input_size < 1 || d->hidden_size < 1) return RNN_BAD_PARAM;
   if (d->bidirectional != 0 && d->bidirectional != 1) return RNN_BAD_PARAM;
   if (d->batch_first != 0 && d->batch_first != 1) return RNN_BAD_PARAM;
   if (d->algo < RNN_ALGO_AUTO || d->algo > RNN_ALGO_PERSIST_SIMT) return RNN_BAD_PARAM;
-  const int G = d->mode == RNN_LSTM ? 4 : 3;
+  const int G = d->mode == RNN_LSTM ? 4 : (d->mode == RNN_GRU ? 3 : 1);
   bool all_zero = true;
   for (int k = 0; k < 4; ++k) all_zero = all_zero && d->gate_order[k] == 0;
   if (!all_zero) {
@@ -245,9 +248,10 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
   h->L = desc->num_layers; h->D = desc->bidirectional ? 2 : 1;
   h->T = desc->seq_len; h->B = desc->batch; h->H = desc->hidden_size; h->I = desc->input_size;
   h->lstm = desc->mode == RNN_LSTM;
-  h->G = h->lstm ? 4 : 3;
-  h->ra = !h->lstm && desc->reset_after;
-  h->rb = !h->lstm && !desc->reset_after;
+  h->plain = desc->mode == RNN_RNN_RELU || desc->mode == RNN_RNN_TANH;
+  h->G = h->lstm ? 4 : (h->plain ? 1 : 3);
+  h->ra = desc->mode == RNN_GRU && desc->reset_after;
+  h->rb = desc->mode == RNN_GRU && !desc->reset_after;
   h->bf16 = desc->dtype == RNN_BF16;
   h->bfirst = desc->batch_first;
   h->es = h->bf16 ? 2 : 4;
@@ -263,6 +267,8 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
   h->launches = 0;
   h->d_len = nullptr;
   h->has_len = 0;
+  h->clip = 0;
+  h->clip_lo = h->clip_hi = 0.f;
   h->trace = false;
   h->timing = false;
   h->dev = nullptr;
@@ -298,53 +304,12 @@ const char* rnn_status_string(rnn_status_t s) {
 rnn_status_t rnn_create(const rnn_desc_t* desc, rnn_handle_t* out) {
   if (!out) return RNN_BAD_PARAM;
   *out = nullptr;
-  rnn_status_t rs = check_desc(desc);
-  if (rs != RNN_OK) return rs;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return RNN_CUDA_ERROR;
-  cudaDeviceProp prop;
-  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return RNN_CUDA_ERROR;
-  if (!(prop.major == 10 && prop.minor == 3)) return RNN_NOT_SUPPORTED;
-
   rnn_handle_s* h = new (std::nothrow) rnn_handle_s();
   if (!h) return RNN_INTERNAL;
-  h->desc = *desc;
-  h->L = desc->num_layers; h->D = desc->bidirectional ? 2 : 1;
-  h->T = desc->seq_len; h->B = desc->batch; h->H = desc->hidden_size; h->I = desc->input_size;
-  h->lstm = desc->mode == RNN_LSTM;
-  h->G = h->lstm ? 4 : 3;
-  h->ra = !h->lstm && desc->reset_after;
-  h->rb = !h->lstm && !desc->reset_after;
-  h->bf16 = desc->dtype == RNN_BF16;
-  h->bfirst = desc->batch_first;
-  h->es = h->bf16 ? 2 : 4;
-  bool all_zero = true;
-  for (int k = 0; k < 4; ++k) all_zero = all_zero && desc->gate_order[k] == 0;
-  for (int c = 0; c < 4; ++c) h->pos[c] = c;
-  if (!all_zero)
-    for (int k = 0; k < h->G; ++k) h->pos[desc->gate_order[k]] = k;
-  h->device = dev;
-  h->num_sms = prop.multiProcessorCount;
-  h->timeout_ns = 2000000000ull;
-  h->skip_cta = -1;
-  h->launches = 0;
-  h->d_len = nullptr;
-  h->has_len = 0;
+  const int rc = rnn::init_handle_host(h, desc);
+  if (rc != RNN_OK) { delete h; return static_cast<rnn_status_t>(rc); }
   const char* tr = std::getenv("RNN_TRACE");
   h->trace = tr && tr[0] == '1';
-  h->timing = false;
-  fill_layout(h);
-
-  // recurrent kernel choice
-  const bool tc_ok = h->bf16 && persist_tc_supported(desc->mode, h->ra, h->H, h->B, 1, h->num_sms);
-  PersistArgs probe;
-  probe.mode = desc->mode; probe.reset_after = h->ra; probe.is_bf16 = h->bf16;
-  probe.T = h->T; probe.B = h->B; probe.H = h->H; probe.D = h->D; probe.ndir = 1;
-  const bool simt_ok = plan_persist_simt(probe, h->num_sms, nullptr, nullptr) == 0;
-  if (desc->algo == RNN_ALGO_PERSIST_TC) h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : 0;
-  else if (desc->algo == RNN_ALGO_PERSIST_SIMT) h->algo = simt_ok ? RNN_ALGO_PERSIST_SIMT : 0;
-  else h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : (simt_ok ? RNN_ALGO_PERSIST_SIMT : 0);
-  if (h->algo == 0) { delete h; return RNN_NOT_SUPPORTED; }
 
   if (cudaMalloc(&h->dev, sizeof(DevArea)) != cudaSuccess) { delete h; return RNN_CUDA_ERROR; }
   if (cudaMemset(h->dev, 0, sizeof(DevArea)) != cudaSuccess) { cudaFree(h->dev); delete h; return RNN_CUDA_ERROR; }
@@ -391,6 +356,19 @@ rnn_status_t rnn_set_seq_lengths(rnn_handle_t h, const int* lengths) {
   if (cudaMemcpy(h->d_len, lengths, sizeof(int) * h->B, cudaMemcpyHostToDevice) != cudaSuccess)
     return RNN_CUDA_ERROR;
   h->has_len = 1;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_set_cell_clip(rnn_handle_t h, int enable, double lo, double hi) {
+  if (!h) return RNN_BAD_PARAM;
+  if (!enable) {
+    h->clip = 0;
+    return RNN_OK;
+  }
+  if (!h->lstm || !(lo < hi)) return RNN_BAD_PARAM;
+  h->clip = 1;
+  h->clip_lo = static_cast<float>(lo);
+  h->clip_hi = static_cast<float>(hi);
   return RNN_OK;
 }
 
@@ -514,6 +492,7 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
     a.hy = hy ? static_cast<char*>(hy) + static_cast<size_t>(l) * D * B * H * es : nullptr;
     a.cy = (h->lstm && cy) ? static_cast<char*>(cy) + static_cast<size_t>(l) * D * B * H * es : nullptr;
     a.len = h->has_len ? h->d_len : nullptr;
+    a.clip = h->clip; a.clip_lo = h->clip_lo; a.clip_hi = h->clip_hi;
     RNN_TRY(run_persist(h, a, false, s));
     layer_x = static_cast<char*>(Ybuf) + static_cast<size_t>(B) * D * H * es;   // slot 1
   }
@@ -568,6 +547,7 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
     a.dhT = dhy ? static_cast<const char*>(dhy) + so : nullptr;
     a.dcT = (h->lstm && dcy) ? static_cast<const char*>(dcy) + so : nullptr;
     a.len = h->has_len ? h->d_len : nullptr;
+    a.clip = h->clip; a.clip_lo = h->clip_lo; a.clip_hi = h->clip_hi;
     a.dh0 = dhx ? static_cast<char*>(dhx) + so : nullptr;
     a.dc0 = (h->lstm && dcx) ? static_cast<char*>(dcx) + so : nullptr;
     RNN_TRY(run_persist(h, a, true, s));
@@ -612,7 +592,9 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
   float* dwf = static_cast<float*>(dw);
   const int* pos = h->pos;
   int m_ih[4], m_hh[4], m_b[4], m_bh[4];
-  if (h->lstm) {
+  if (h->plain) {
+    for (int k = 0; k < 4; ++k) m_ih[k] = m_hh[k] = m_b[k] = m_bh[k] = k == 0 ? 0 : -1;
+  } else if (h->lstm) {
     for (int k = 0; k < 4; ++k) m_ih[k] = m_hh[k] = m_b[k] = m_bh[k] = pos[k];
   } else {
     m_ih[0] = pos[0]; m_ih[1] = pos[1]; m_ih[2] = pos[2]; m_ih[3] = -1;

@@ -56,6 +56,16 @@ template <> struct Vec4<__nv_bfloat16> {
 
 __device__ __forceinline__ float sigm(float a) { return 1.0f / (1.0f + expf(-a)); }
 
+// LSTM cell clipping: clip(x) = min(max(x, lo), hi), a NaN stays NaN; with
+// lo = -inf, hi = +inf it is the identity.  dclip = 1 on [lo, hi], else 0.
+__device__ __forceinline__ float clipv(float x, float lo, float hi) { return x < lo ? lo : (x > hi ? hi : x); }
+__device__ __forceinline__ float dclipv(float x, float lo, float hi) { return (x >= lo && x <= hi) ? 1.f : 0.f; }
+
+// Plain RNN activation (mode 2 = ReLU, 3 = tanh) and its derivative through
+// the output h' (ReLU: 1 where h' > 0; tanh: 1 - h'^2).
+__device__ __forceinline__ float plain_act(int mode, float a) { return mode == 2 ? fmaxf(a, 0.f) : tanhf(a); }
+__device__ __forceinline__ float plain_dact(int mode, float h) { return mode == 2 ? (h > 0.f ? 1.f : 0.f) : 1.f - h * h; }
+
 // ---------------------------------------------------------------------------
 // time, status, flags
 // ---------------------------------------------------------------------------

@@ -13,7 +13,7 @@ struct rnn_handle_s {
   using DevArea = rnn::DevArea;
   rnn_desc_t desc;
   int L, D, T, B, H, I, G;
-  int lstm, ra, rb, bf16, bfirst;
+  int lstm, ra, rb, plain, bf16, bfirst;   // plain: RNN_RNN_RELU / RNN_RNN_TANH (one gate)
   int pos[4];          // canonical gate c sits in the caller's block pos[c]
   int algo;            // RNN_ALGO_PERSIST_TC or RNN_ALGO_PERSIST_SIMT
   int device, num_sms;
@@ -24,6 +24,8 @@ struct rnn_handle_s {
   uint64_t launches;
   int* d_len;                  // device copy of the sequence lengths (B ints), or null
   int has_len;                 // 1: the lengths in d_len apply
+  int clip;                    // LSTM cell clipping on, bounds [clip_lo, clip_hi]
+  float clip_lo, clip_hi;
   bool trace;
   bool timing;
   struct Ev { cudaEvent_t a, b; int cls; };

@@ -179,7 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
   T* Ws = reinterpret_cast<T*>(smem);
   float* hs = reinterpret_cast<float*>(STREAM ? smem : smem + align16(static_cast<size_t>(4) * NU * WS * sizeof(T)));
   const bool lstm = a.mode == 0;
-  const bool rb = !lstm && !a.reset_after;
+  const bool plain = a.mode >= 2;
+  const bool rb = a.mode == 1 && !a.reset_after;
+  const float clo = a.clip ? a.clip_lo : -INFINITY, chi = a.clip ? a.clip_hi : INFINITY;
 
   const T* Wr = static_cast<const T*>(a.Wr) + static_cast<size_t>(dir) * 4 * H * H;
   if (!STREAM) {
@@ -242,6 +244,8 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
       contract_fwd<T, STREAM, PP, 0x3>(acc, W, hs, KC, hsrc, ldY, H, B, nu, npairs);
     else if (lstm)
       contract_fwd<T, STREAM, PP, 0xF>(acc, W, hs, KC, hsrc, ldY, H, B, nu, npairs);
+    else if (plain)
+      contract_fwd<T, STREAM, PP, 0x1>(acc, W, hs, KC, hsrc, ldY, H, B, nu, npairs);
     else
       contract_fwd<T, STREAM, PP, 0x7>(acc, W, hs, KC, hsrc, ldY, H, B, nu, npairs);
 
@@ -284,8 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
         const float f = sigm(pv[1] + acc[p][1]);
         const float g = tanhf(pv[2] + acc[p][2]);
         const float o = sigm(pv[3] + acc[p][3]);
-        float c = f * st[p] + i * g;
-        h = o * tanhf(c);
+        float c = f * clipv(st[p], clo, chi) + i * g;
+        h = o * tanhf(clipv(c, clo, chi));
         if (!live) { c = st[p]; h = hl[p]; }
         st[p] = c;
         hl[p] = h;
@@ -293,6 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
         if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = c;
         if (s == TT - 1 && a.cy)
           static_cast<T*>(a.cy)[(static_cast<int64_t>(dir) * B + b) * H + u] = from_f<T>(c);
+      } else if (plain) {
+        const float hn = plain_act(a.mode, pv[0] + acc[p][0]);
+        h = live ? hn : st[p];
+        st[p] = h;
+        gv[0] = hn; gv[1] = gv[2] = gv[3] = 0.f;
       } else if (!rb) {
         const float* bh = a.bh + dir * 4 * H + 4 * u;
         const float r = sigm(pv[0] + acc[p][0] + bh[0]);
@@ -335,7 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
   float* hs = reinterpret_cast<float*>(STREAM ? smem : smem + align16(static_cast<size_t>(NU) * WS * sizeof(T)));
   __shared__ float dbs[4 * 64];
   const bool lstm = a.mode == 0;
-  const bool rb = !lstm && !a.reset_after;
+  const bool plain = a.mode >= 2;
+  const bool rb = a.mode == 1 && !a.reset_after;
+  const float clo = a.clip ? a.clip_lo : -INFINITY, chi = a.clip ? a.clip_hi : INFINITY;
 
   const T* WT = static_cast<const T*>(a.WrT) + static_cast<size_t>(dir) * H * K4;
   if (!STREAM) {
@@ -396,6 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
       const T* src = dG + static_cast<int64_t>(tp) * B * ldG + dir * K4;
       if (rb)
         contract_bwd<T, STREAM, PP, 0x3>(dhr, W, hs, KC, src, ldG, K4, B, nu, npairs);
+      else if (plain)
+        contract_bwd<T, STREAM, PP, 0x1>(dhr, W, hs, KC, src, ldG, K4, B, nu, npairs);
       else
         contract_bwd<T, STREAM, PP, 0xF>(dhr, W, hs, KC, src, ldG, K4, B, nu, npairs);
     }
@@ -432,13 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
           const float c = C[(static_cast<int64_t>(dir ? t : t + 1) * B + b) * H + u];
           const float cp = C[(static_cast<int64_t>(dir ? t + 1 : t) * B + b) * H + u];
           const float dh = dy + gh;
-          const float tc = tanhf(c);
-          const float dc = dh * o * (1.f - tc * tc) + carry[p];
+          const float tc = tanhf(clipv(c, clo, chi));
+          const float dc = dh * o * (1.f - tc * tc) * (a.clip ? dclipv(c, clo, chi) : 1.f) + carry[p];
           da[0] = dc * g * i * (1.f - i);
-          da[1] = dc * cp * f * (1.f - f);
+          da[1] = dc * clipv(cp, clo, chi) * f * (1.f - f);
           da[2] = dc * i * (1.f - g * g);
           da[3] = dh * tc * o * (1.f - o);
-          carry[p] = dc * f;
+          carry[p] = dc * f * (a.clip ? dclipv(cp, clo, chi) : 1.f);
           carry_h[p] = 0.f;
         } else {
           carry_h[p] = gh;
@@ -446,6 +459,17 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
         Vec4<T>::store(dg, da);
 #pragma unroll
         for (int q = 0; q < 4; ++q) db[p][q] += da[q];
+      } else if (plain) {
+        const float gh = dhr[p] + carry[p];
+        float da[4] = {0.f, 0.f, 0.f, 0.f};
+        if (live) {
+          da[0] = (dy + gh) * plain_dact(a.mode, gv[0]);
+          carry[p] = 0.f;
+        } else {
+          carry[p] = gh;
+        }
+        Vec4<T>::store(dg, da);
+        db[p][0] += da[0];
       } else if (!rb) {
         const float gh = dhr[p] + carry[p];
         float da[4] = {0.f, 0.f, 0.f, 0.f};
@@ -645,8 +669,10 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_latency_kernel(Persis
   const int u0 = blockIdx.x * NU;
   const int nu = min(NU, H - u0);
   const bool lstm = a.mode == 0;
-  const bool rb = !lstm && !a.reset_after;
-  const int na = lstm ? 4 : (rb ? 2 : 3);     // phase-A rows per unit
+  const bool plain = a.mode >= 2;
+  const bool rb = a.mode == 1 && !a.reset_after;
+  const int na = lstm ? 4 : (rb ? 2 : (plain ? 1 : 3));     // phase-A rows per unit
+  const float clo = a.clip ? a.clip_lo : -INFINITY, chi = a.clip ? a.clip_hi : INFINITY;
   const int WSR = H + 16 / static_cast<int>(sizeof(T));   // resident row stride (16-byte aligned)
   T* hs = reinterpret_cast<T*>(smem);                                   // [BB][H]
   float* out = reinterpret_cast<float*>(smem + static_cast<size_t>(BB) * H * sizeof(T));   // [4*NU][BB]
@@ -734,12 +760,16 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_latency_kernel(Persis
         const float f = sigm(pv[1] + o[BB]);
         const float g = tanhf(pv[2] + o[2 * BB]);
         const float oo = sigm(pv[3] + o[3 * BB]);
-        float c = f * st + i * g;
-        h = oo * tanhf(c);
+        float c = f * clipv(st, clo, chi) + i * g;
+        h = oo * tanhf(clipv(c, clo, chi));
         if (t >= lenb) { c = st; h = hl; }
         st = c;
         hl = h;
         gv[0] = i; gv[1] = f; gv[2] = g; gv[3] = oo;
+      } else if (plain) {
+        const float hn = plain_act(a.mode, pv[0] + o[0]);
+        h = t < lenb ? hn : st;
+        gv[0] = hn;
       } else if (!rb) {
         const float* bh = a.bh + dir * 4 * H + 4 * u;
         r = sigm(pv[0] + o[0] + bh[0]);

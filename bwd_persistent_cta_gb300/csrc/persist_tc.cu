@@ -86,8 +86,8 @@ int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int ma
   return n;
 }
 
-const void* kernel_for(int bwd, int pp, int ks, int mask) {
-  return bwd ? persist_tc_bwd_kernel_ptr(pp, ks, mask) : persist_tc_fwd_kernel_ptr(pp, ks, mask);
+const void* kernel_for(int bwd, int pp, int ks, int ext) {
+  return bwd ? persist_tc_bwd_kernel_ptr(pp, ks, ext) : persist_tc_fwd_kernel_ptr(pp, ks, ext);
 }
 
 void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPlan& pl, int ndir, cudaStream_t s) {
@@ -105,12 +105,12 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPla
 }
 
 // First candidate plan whose clusters can all be resident at once.
-bool choose_plan(int bwd, int H, int B, int ndir, int num_sms, int mask, TcPlan* chosen) {
+bool choose_plan(int bwd, int H, int B, int ndir, int num_sms, int ext, TcPlan* chosen) {
   TcPlan plans[5];
   const int n = make_plans(bwd, H, B, ndir, num_sms, plans, 5);
   for (int i = 0; i < n; ++i) {
     const TcPlan& pl = plans[i];
-    const void* fn = kernel_for(bwd, pl.PP, pl.KS, mask);
+    const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) !=
         cudaSuccess) {
       cudaGetLastError();
@@ -138,8 +138,9 @@ bool choose_plan(int bwd, int H, int B, int ndir, int num_sms, int mask, TcPlan*
 
 int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   TcPlan pl;
-  const int mask = a.len != nullptr ? 1 : 0;
-  if (!choose_plan(bwd, a.H, a.B, a.ndir, num_sms, mask, &pl)) return 2;
+  // the extended kernel variant takes sequence lengths and cell clipping
+  const int ext = (a.len != nullptr || a.clip) ? 1 : 0;
+  if (!choose_plan(bwd, a.H, a.B, a.ndir, num_sms, ext, &pl)) return 2;
   const int H = a.H, D = a.D;
   CUtensorMap tmW, tmX, tmX4;
   int rc;
@@ -179,7 +180,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   P.w_tmem = pl.w_tmem;
   P.single = single;
   P.wcol = 256;
-  const void* fn = kernel_for(bwd, pl.PP, pl.KS, mask);
+  const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   fill_config(cfg, attr, pl, a.ndir, s);

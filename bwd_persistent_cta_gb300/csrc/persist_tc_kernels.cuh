@@ -27,10 +27,14 @@
 //      backward carries never leave registers - stores the exchanged values,
 //      arrives on the counter, and only then stores what no CTA of this
 //      launch waits for.
-// Variable sequence lengths: at a step t >= len[b] the pair (u, b) keeps its
-// state (h, c) and stores it unchanged, and the backward step writes zero gate
-// gradients and passes the state gradients on (LSTM: an extra register carries
-// dh past such steps).
+// Extended variant (template flag EXT, used when sequence lengths or LSTM cell
+// clipping are set; the plain variant compiles without either):
+//  * variable sequence lengths: at a step t >= len[b] the pair (u, b) keeps
+//    its state (h, c) and stores it unchanged, and the backward step writes
+//    zero gate gradients and passes the state gradients on (LSTM: an extra
+//    register carries dh past such steps);
+//  * LSTM cell clipping: every use of the raw cell state goes through
+//    clip = min(max(c, lo), hi), and the backward multiplies by dclip.
 // Cluster-uniform abort: every CTA reads the same set of flags after the same
 // barrier, so all CTAs of a cluster leave at the same step (after one more
 // cluster barrier, so no CTA exits while a peer may still touch its shared
@@ -371,7 +375,7 @@ __device__ __forceinline__ void teardown(const TcPersistParams& P, TcBars& bars)
 // ---------------------------------------------------------------------------
 // forward
 // ---------------------------------------------------------------------------
-template <int PP, int KS, bool MASK>
+template <int PP, int KS, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ TcPersistParams P) {
@@ -383,6 +387,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int rg = static_cast<int>(blockIdx.x) / KS;
   const bool lstm = a.mode == 0;
   constexpr int RPC = 128 / KS;
+  const bool clip = EXT && a.clip;
+  const float clo = a.clip_lo, chi = a.clip_hi;
 
   setup(P, &tmW, &tmX, &tmX4, wsm, bars, ks * P.Kc, dir * 4 * H + rg * 128, static_cast<const __nv_bfloat16*>(a.Wr),
         H);
@@ -403,8 +409,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const uint32_t src_bytes = static_cast<uint32_t>(P.Npad) * RPC * 4;   // bytes per source rank in recv
 
   float st[PP];      // LSTM: c_{t-1}; GRU: h_{t-1}
-  float hl[PP];      // MASK, LSTM: h_{t-1} (held over masked steps)
-  int lenp[PP];      // MASK: valid steps of the pair's sequence
+  float hl[PP];      // EXT, LSTM: h_{t-1} (held over masked steps)
+  int lenp[PP];      // EXT: valid steps of the pair's sequence
   float bh[PP][3];
 #pragma unroll
   for (int p = 0; p < PP; ++p) {
@@ -414,11 +420,11 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     const int id = threadIdx.x + p * kThreads;
     if (id >= npairs) continue;
     const int ul = id % UPC, b = id / UPC, u = ubase + ul;
-    if constexpr (MASK) lenp[p] = a.len[b];
+    if constexpr (EXT) lenp[p] = a.len ? a.len[b] : TT;   // clipping alone: no lengths
     if (lstm) {
       const __nv_bfloat16* c0 = static_cast<const __nv_bfloat16*>(a.c0);
       st[p] = c0 ? __bfloat162float(c0[(static_cast<int64_t>(dir) * B + b) * H + u]) : 0.f;
-      if constexpr (MASK) hl[p] = __bfloat162float(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
+      if constexpr (EXT) hl[p] = __bfloat162float(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
       if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? TT : 0)) * B + b) * H + u] = st[p];
     } else {
       st[p] = __bfloat162float(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
@@ -483,9 +489,15 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         const float f = sigm_fast(pv[1] + acc[p].y);
         const float gg = tanh_fast(pv[2] + acc[p].z);
         const float o = sigm_fast(pv[3] + acc[p].w);
-        float c = f * st[p] + i * gg;
-        h = o * tanh_fast(c);
-        if constexpr (MASK) {
+        float c;
+        if (clip) {
+          c = f * clipv(st[p], clo, chi) + i * gg;
+          h = o * tanh_fast(clipv(c, clo, chi));
+        } else {
+          c = f * st[p] + i * gg;
+          h = o * tanh_fast(c);
+        }
+        if constexpr (EXT) {
           if (t >= lenp[p]) { c = st[p]; h = hl[p]; }
           hl[p] = h;
         }
@@ -497,7 +509,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         const float hn = acc[p].z + bh[p][2];
         const float n = tanh_fast(pv[2] + r * hn);
         h = (1.f - z) * n + z * st[p];
-        if constexpr (MASK) {
+        if constexpr (EXT) {
           if (t >= lenp[p]) h = st[p];
         }
         st[p] = h;
@@ -532,7 +544,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 // ---------------------------------------------------------------------------
 // backward through time
 // ---------------------------------------------------------------------------
-template <int PP, int KS, bool MASK>
+template <int PP, int KS, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ TcPersistParams P) {
@@ -545,6 +557,8 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int rg = static_cast<int>(blockIdx.x) / KS;
   const bool lstm = a.mode == 0;
   constexpr int RPC = 128 / KS;
+  const bool clip = EXT && a.clip;
+  const float clo = a.clip_lo, chi = a.clip_hi;
 
   setup(P, &tmW, &tmX, &tmX4, wsm, bars, ks * P.Kc, dir * H + rg * 128, static_cast<const __nv_bfloat16*>(a.WrT),
         4 * H);
@@ -577,7 +591,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     const int id = threadIdx.x + p * kThreads;
     if (id >= npairs) continue;
     const int ul = id % UPC, b = id / UPC, u = ubase + ul;
-    if constexpr (MASK) lenp[p] = a.len[b];
+    if constexpr (EXT) lenp[p] = a.len ? a.len[b] : TT;   // clipping alone: no lengths
     if (lstm && a.dcT)
       carry[p] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.dcT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
   }
@@ -648,7 +662,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       const float dhr = dhs[p];
       if (s == TT) {
         const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
-        if (a.dh0) static_cast<__nv_bfloat16*>(a.dh0)[o] = __float2bfloat16_rn(lstm ? dhr + (MASK ? carry_h[p] : 0.f)
+        if (a.dh0) static_cast<__nv_bfloat16*>(a.dh0)[o] = __float2bfloat16_rn(lstm ? dhr + (EXT ? carry_h[p] : 0.f)
                                                                                    : dhr + carry[p]);
         if (lstm && a.dc0) static_cast<__nv_bfloat16*>(a.dc0)[o] = __float2bfloat16_rn(carry[p]);
         continue;
@@ -657,21 +671,31 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       unpack4(gq[p], gv);
       float da[4] = {0.f, 0.f, 0.f, 0.f};
       bool live = true;
-      if constexpr (MASK) live = t < lenp[p];
+      if constexpr (EXT) live = t < lenp[p];
       if (lstm) {
-        const float gh = MASK ? dhr + carry_h[p] : dhr;
+        const float gh = EXT ? dhr + carry_h[p] : dhr;
         if (live) {
           const float i = gv[0], f = gv[1], gg = gv[2], o = gv[3];
           const float c = e0[p], cp = e1[p];
           const float dh = dyv[p] + gh;
-          const float tc = tanh_fast(c);
-          const float dc = dh * o * (1.f - tc * tc) + carry[p];
-          da[0] = dc * gg * i * (1.f - i);
-          da[1] = dc * cp * f * (1.f - f);
-          da[2] = dc * i * (1.f - gg * gg);
-          da[3] = dh * tc * o * (1.f - o);
-          carry[p] = dc * f;
-          if constexpr (MASK) carry_h[p] = 0.f;
+          if (clip) {
+            const float tc = tanh_fast(clipv(c, clo, chi));
+            const float dc = dh * o * (1.f - tc * tc) * dclipv(c, clo, chi) + carry[p];
+            da[0] = dc * gg * i * (1.f - i);
+            da[1] = dc * clipv(cp, clo, chi) * f * (1.f - f);
+            da[2] = dc * i * (1.f - gg * gg);
+            da[3] = dh * tc * o * (1.f - o);
+            carry[p] = dc * f * dclipv(cp, clo, chi);
+          } else {
+            const float tc = tanh_fast(c);
+            const float dc = dh * o * (1.f - tc * tc) + carry[p];
+            da[0] = dc * gg * i * (1.f - i);
+            da[1] = dc * cp * f * (1.f - f);
+            da[2] = dc * i * (1.f - gg * gg);
+            da[3] = dh * tc * o * (1.f - o);
+            carry[p] = dc * f;
+          }
+          if constexpr (EXT) carry_h[p] = 0.f;
         } else {
           carry_h[p] = gh;
         }
@@ -726,9 +750,9 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 }  // namespace
 
 // Kernel entry points by template arguments (PP pairs per thread in 1, 2, 4, 8;
-// K split KS in 1, 2, 4, 8, 16; mask = variable sequence lengths), defined in
+// K split KS in 1, 2, 4, 8, 16; ext = the extended variant), defined in
 // persist_tc_fwd.cu / persist_tc_bwd.cu so the instances compile in parallel.
-const void* persist_tc_fwd_kernel_ptr(int pp, int ks, int mask);
-const void* persist_tc_bwd_kernel_ptr(int pp, int ks, int mask);
+const void* persist_tc_fwd_kernel_ptr(int pp, int ks, int ext);
+const void* persist_tc_bwd_kernel_ptr(int pp, int ks, int ext);
 
 }  // namespace rnn

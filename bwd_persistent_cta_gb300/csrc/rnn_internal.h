@@ -67,7 +67,11 @@ struct GemmArgs {
 };
 
 struct PersistArgs {
-  int mode = 0, reset_after = 0, is_bf16 = 0;
+  int mode = 0, reset_after = 0, is_bf16 = 0;   // mode: rnn_mode_t (0 LSTM, 1 GRU, 2 / 3 plain ReLU / tanh)
+  // LSTM cell clipping: every use of the (raw) cell state goes through
+  // clip(x) = min(max(x, clip_lo), clip_hi)
+  int clip = 0;
+  float clip_lo = 0.f, clip_hi = 0.f;
   // valid steps per sequence ([B], device) or null = all T; step t of
   // sequence b is masked when t >= len[b] (state held, zero gate gradients)
   const int* len = nullptr;

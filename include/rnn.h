@@ -66,7 +66,10 @@ typedef enum {
   RNN_INTERNAL = 6
 } rnn_status_t;
 
-typedef enum { RNN_LSTM = 0, RNN_GRU = 1 } rnn_mode_t;
+/* RNN_RNN_RELU / RNN_RNN_TANH: the plain recurrent cell h' = act(W_ih x +
+ * W_hh h + b) of the persistent backward-data kernel fragment's
+ * CUDNN_RNN_RELU / CUDNN_RNN_TANH branch (one gate, G = 1). */
+typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_RNN_RELU = 2, RNN_RNN_TANH = 3 } rnn_mode_t;
 typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
 
 /* Recurrent-kernel choice.  AUTO picks the tensor-core persistent kernels
@@ -78,8 +81,8 @@ typedef enum { RNN_ALGO_AUTO = 0, RNN_ALGO_PERSIST_TC = 1, RNN_ALGO_PERSIST_SIMT
 typedef struct {
   int mode;            /* rnn_mode_t                                                */
   int gate_order[4];   /* block k of every per-gate matrix holds canonical gate
-                          gate_order[k] (LSTM 0..3 = i,f,g,o; GRU 0..2 = r,z,n).
-                          All zero = canonical order.                               */
+                          gate_order[k] (LSTM 0..3 = i,f,g,o; GRU 0..2 = r,z,n;
+                          plain RNN: one gate, only 0).  All zero = canonical.      */
   int reset_after;     /* GRU only: 1 = resetAfter form, 0 = reset-before           */
   int bidirectional;   /* 0 or 1                                                    */
   int num_layers;      /* 1..8                                                      */
@@ -109,7 +112,8 @@ rnn_status_t rnn_destroy(rnn_handle_t handle);
  *                     has the same element count at 4 bytes per element.
  *                     Per layer l, per direction d, in this order:
  *                     W_ih [G*H, I_l] row-major, W_hh [G*H, H], b [G*H], and
- *                     for GRU resetAfter b_h [G*H].  G = 4 (LSTM) or 3 (GRU);
+ *                     for GRU resetAfter b_h [G*H].  G = 4 (LSTM), 3 (GRU) or
+ *                     1 (plain RNN);
  *                     gate blocks in desc.gate_order.  LSTM and GRU
  *                     reset-before have one bias vector per direction.
  *   workspace_bytes - scratch for any one call; contents need not persist.
@@ -179,6 +183,16 @@ rnn_status_t rnn_set_timeout_ns(rnn_handle_t handle, uint64_t ns);
  * call this between uses of the handle.  Returns RNN_BAD_PARAM for a length
  * outside [0, seq_len], RNN_CUDA_ERROR if the copy fails. */
 rnn_status_t rnn_set_seq_lengths(rnn_handle_t handle, const int* lengths);
+
+/* LSTM cell clipping (the clip / dclip of the persistent backward-data kernel
+ * fragment's LSTM branch).  With enable != 0 and lo < hi the cell state stays
+ * the raw value c, and every use of it goes through clip(x) = min(max(x, lo),
+ * hi) (a NaN stays NaN): c_t = f * clip(c_{t-1}) + i * g and
+ * h_t = o * tanh(clip(c_t)); cy is the raw c_T; the backward uses
+ * dclip(x) = 1 on [lo, hi], 0 outside.  enable = 0 turns it off (the
+ * default).  Applies to the following forward / backward calls, which must
+ * agree.  RNN_BAD_PARAM for a non-LSTM handle or lo >= hi. */
+rnn_status_t rnn_set_cell_clip(rnn_handle_t handle, int enable, double lo, double hi);
 
 /* Number of kernels this handle has launched since it was created. */
 uint64_t rnn_launch_count(rnn_handle_t handle);

@@ -58,7 +58,7 @@ class Workload:
 
     @property
     def gates(self) -> int:
-        return 4 if self.mode == LSTM else 3
+        return 4 if self.mode == LSTM else (3 if self.mode == GRU else 1)
 
     @property
     def dirs(self) -> int:
@@ -142,6 +142,7 @@ class Inputs:
     dhy: Optional[np.ndarray] = None
     dcy: Optional[np.ndarray] = None
     lengths: Optional[np.ndarray] = None   # [B] valid steps per sequence, or None (all T)
+    clip: Optional[Tuple[float, float]] = None   # LSTM cell clipping bounds, or None
 
 
 def make_inputs(wl: Workload, batch_subset: Optional[Sequence[int]] = None) -> Inputs:

@@ -61,6 +61,8 @@ def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: i
     try:
         if inp.lengths is not None:
             rnn.set_seq_lengths([int(v) for v in inp.lengths])
+        if inp.clip is not None:
+            rnn.set_cell_clip(inp.clip)
         w = to_dev(synth.flatten_params(wl, inp.params), wl)
         xs = synth.to_batch_first(inp.x) if wl.batch_first else inp.x
         x = to_dev(xs, wl)
