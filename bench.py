@@ -252,7 +252,7 @@ def run_ours(args):
         return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev, tdt)
 
     rnn = R.RNN(wl.mode, wl.input_size, wl.hidden_size, wl.seq_len, wl.batch, wl.num_layers, wl.bidirectional,
-                wl.reset_after, wl.dtype, wl.gate_order, wl.batch_first, device=dev)
+                wl.reset_after, wl.dtype, wl.gate_order, wl.batch_first, device=dev, recompute=wl.recompute)
     # variable-length workloads: the work is the valid steps (sum of lengths)
     valid_frac = 1.0
     if inp.lengths is not None:
@@ -274,7 +274,7 @@ def run_ours(args):
     def step():
         rnn.forward(x, w, hx, cx, train=not wl.forward_only, y=y, hy=hy, cy=cy)
         if not wl.forward_only:
-            rnn.backward_data(dy, w, None, None, dx=dx, dhx=dhx, dcx=dcx)
+            rnn.backward_data(dy, w, None, None, dx=dx, dhx=dhx, dcx=dcx, cx=cx)
             rnn.backward_weights(x, dw=dw)
 
     for _ in range(args.warmup):
@@ -371,6 +371,7 @@ def run_ours(args):
                        "batch_per_gpu": wl.batch, "input": wl.input_size, "hidden": wl.hidden_size,
                        "seed": wl.seed, "parallelism": f"replicas{world}",
                        "l2": "flushed (256 MiB write) before every timed step",
+                       "reserve_bytes": rnn.reserve_bytes, "recompute_cell_states": wl.recompute,
                        **({} if inp.lengths is None else {
                            "seq_lengths": {"min": int(np.min(inp.lengths)), "max": int(np.max(inp.lengths)),
                                            "valid_frac": valid_frac,

@@ -51,6 +51,7 @@ _SIGS = {
     "rnn_set_timeout_ns": (ctypes.c_int, [_P, ctypes.c_uint64]),
     "rnn_set_seq_lengths": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int)]),
     "rnn_set_cell_clip": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_double, ctypes.c_double]),
+    "rnn_set_recomputation": (ctypes.c_int, [_P, ctypes.c_int]),
     "rnn_launch_count": (ctypes.c_uint64, [_P]),
     "rnn_selected_algo": (ctypes.c_int, [_P]),
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
@@ -152,6 +153,10 @@ def rnn_set_seq_lengths(handle, lengths) -> int:
     return lib().rnn_set_seq_lengths(handle, arr)
 
 
+def rnn_set_recomputation(handle, mode: int) -> int:
+    return lib().rnn_set_recomputation(handle, int(mode))
+
+
 def rnn_set_cell_clip(handle, enable: int, lo: float = 0.0, hi: float = 0.0) -> int:
     return lib().rnn_set_cell_clip(handle, int(enable), float(lo), float(hi))
 
@@ -205,7 +210,7 @@ class RNN:
     def __init__(self, mode: str, input_size: int, hidden_size: int, seq_len: int, batch: int,
                  num_layers: int = 1, bidirectional: bool = False, reset_after: bool = True,
                  dtype: str = "bf16", gate_order: Sequence[int] = (), batch_first: bool = False,
-                 algo: int = RNN_ALGO_AUTO, device=None):
+                 algo: int = RNN_ALGO_AUTO, device=None, recompute: bool = False):
         import torch
         self.torch = torch
         self.device = torch.device(device if device is not None else "cuda")
@@ -224,6 +229,8 @@ class RNN:
         self.tdtype = torch.bfloat16 if dtype == "bf16" else torch.float32
         with torch.cuda.device(self.device):
             self.handle = rnn_create(d)
+        if recompute:
+            self._check(rnn_set_recomputation(self.handle, 1), "rnn_set_recomputation")
         self.weight_bytes, self.workspace_bytes, self.reserve_bytes = rnn_get_sizes(self.handle)
         self.weight_count = self.weight_bytes // (2 if dtype == "bf16" else 4)
         self.workspace = torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=self.device)
@@ -269,7 +276,7 @@ class RNN:
         self._check(rc, "rnn_forward")
         return y, hy, cy
 
-    def backward_data(self, dy, w, dhy=None, dcy=None, dx=None, dhx=None, dcx=None, stream=None):
+    def backward_data(self, dy, w, dhy=None, dcy=None, dx=None, dhx=None, dcx=None, stream=None, cx=None):
         torch = self.torch
         d = self.desc
         shp = (d.batch, d.seq_len, d.input_size) if d.batch_first else (d.seq_len, d.batch, d.input_size)
@@ -277,7 +284,7 @@ class RNN:
         dhx = torch.empty(self._state_shape(), dtype=self.tdtype, device=self.device) if dhx is None else dhx
         if d.mode == RNN_LSTM and dcx is None:
             dcx = torch.empty(self._state_shape(), dtype=self.tdtype, device=self.device)
-        rc = rnn_backward_data(self.handle, None, _p(dy), _p(dhy), _p(dcy), _p(w), None, None, _p(dx), _p(dhx),
+        rc = rnn_backward_data(self.handle, None, _p(dy), _p(dhy), _p(dcy), _p(w), None, _p(cx), _p(dx), _p(dhx),
                                _p(dcx), _p(self.workspace), _p(self.reserve), _stream(stream))
         self._check(rc, "rnn_backward_data")
         return dx, dhx, dcx

@@ -86,7 +86,7 @@ void fill_layout(rnn_handle_s* h) {
   for (int l = 0; l < L; ++l) {
     h->r_y[l] = r.take(static_cast<size_t>(T + 2) * B * D * H * es);
     h->r_g[l] = r.take(static_cast<size_t>(D) * TB * 4 * H * es);
-    if (h->lstm) h->r_c[l] = r.take(static_cast<size_t>(D) * (T + 1) * B * H * 4);
+    if (h->lstm && !h->recompute) h->r_c[l] = r.take(static_cast<size_t>(D) * (T + 1) * B * H * 4);
     if (h->rb) h->r_rh[l] = r.take(static_cast<size_t>(D) * TB * H * es);
     h->r_dg[l] = r.take(TB * D * 4 * H * es);
     h->r_db[l] = r.take(static_cast<size_t>(D) * 4 * H * 4);
@@ -267,6 +267,7 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
   h->launches = 0;
   h->d_len = nullptr;
   h->has_len = 0;
+  h->recompute = 0;
   h->clip = 0;
   h->clip_lo = h->clip_hi = 0.f;
   h->trace = false;
@@ -356,6 +357,13 @@ rnn_status_t rnn_set_seq_lengths(rnn_handle_t h, const int* lengths) {
   if (cudaMemcpy(h->d_len, lengths, sizeof(int) * h->B, cudaMemcpyHostToDevice) != cudaSuccess)
     return RNN_CUDA_ERROR;
   h->has_len = 1;
+  return RNN_OK;
+}
+
+rnn_status_t rnn_set_recomputation(rnn_handle_t h, int mode) {
+  if (!h || mode < 0 || mode > 1) return RNN_BAD_PARAM;
+  h->recompute = h->lstm ? mode : 0;
+  fill_layout(h);
   return RNN_OK;
 }
 
@@ -486,7 +494,7 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
     a.Wr = at<char>(workspace, h->w_wr);
     a.Y = Ybuf;
     a.gates = train ? at<char>(reserve, h->r_g[l]) : nullptr;
-    a.C = (train && h->lstm) ? at<float>(reserve, h->r_c[l]) : nullptr;
+    a.C = (train && h->lstm && !h->recompute) ? at<float>(reserve, h->r_c[l]) : nullptr;
     a.RH = h->rb ? (train ? at<char>(reserve, h->r_rh[l]) : at<char>(workspace, h->w_rh)) : nullptr;
     a.c0 = (h->lstm && cx) ? static_cast<const char*>(cx) + static_cast<size_t>(l) * D * B * H * es : nullptr;
     a.hy = hy ? static_cast<char*>(hy) + static_cast<size_t>(l) * D * B * H * es : nullptr;
@@ -505,10 +513,10 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
 rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, const void* dhy, const void* dcy,
                                const void* w, const void* hx, const void* cx, void* dx, void* dhx, void* dcx,
                                void* workspace, void* reserve, void* stream) {
-  (void)y; (void)hx; (void)cx;
+  (void)y; (void)hx;   // cx: read only with recomputation (the cell states' initial value)
   if (!h || !dy || !w || !dx) return RNN_BAD_PARAM;
   if (!workspace || !reserve) return RNN_BAD_WORKSPACE;
-  const void* ptrs[] = {dy, dhy, dcy, w, dx, dhx, dcx, workspace, reserve};
+  const void* ptrs[] = {dy, dhy, dcy, w, cx, dx, dhx, dcx, workspace, reserve};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return RNN_BAD_PARAM;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -539,6 +547,15 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
     a.Y = at<char>(reserve, h->r_y[l]);
     a.gates = at<char>(reserve, h->r_g[l]);
     a.C = h->lstm ? at<float>(reserve, h->r_c[l]) : nullptr;
+    if (h->lstm && h->recompute) {
+      // cell states recomputed from the saved gates into the projection
+      // buffer, idle in the backward pass (D*(T+1)*B*H*4 <= T*B*D*4H*es bytes)
+      float* Cw = at<float>(workspace, h->w_p);
+      const void* c0 = cx ? static_cast<const char*>(cx) + static_cast<size_t>(l) * D * B * H * es : nullptr;
+      RNN_TRY(count(h, launch_recompute_cells(a.gates, c0, Cw, T, B, H, D, h->bf16, h->has_len ? h->d_len : nullptr,
+                                              h->clip, h->clip_lo, h->clip_hi, s)));
+      a.C = Cw;
+    }
     a.WrT = at<char>(workspace, h->w_wrt);
     a.dYi = dyi;
     a.dG = at<char>(reserve, h->r_dg[l]);

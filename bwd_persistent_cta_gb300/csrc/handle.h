@@ -24,6 +24,7 @@ struct rnn_handle_s {
   uint64_t launches;
   int* d_len;                  // device copy of the sequence lengths (B ints), or null
   int has_len;                 // 1: the lengths in d_len apply
+  int recompute;               // LSTM: no cell states in the reserve; the backward recomputes them
   int clip;                    // LSTM cell clipping on, bounds [clip_lo, clip_hi]
   float clip_lo, clip_hi;
   bool trace;

@@ -100,6 +100,50 @@ __global__ void states_to_y_kernel(const T* __restrict__ h0, T* __restrict__ Y, 
   Y[(static_cast<int64_t>(slot) * B + b) * D * H + dir * H + u] = h0 ? h0[i] : from_f<T>(0.0f);
 }
 
+// Recomputation of the LSTM cell states from the saved gate activations
+// (poplibs Lstm.cpp recomputeCellAndTanhImpl: prevCellState * forgetGate +
+// inputGate * candidate, before the backward pass): one thread per (direction,
+// sequence, unit) walks the direction's time order, c_t = f * clip(c_{t-1}) +
+// i * g (clip = identity without cell clipping; a masked step t >= len[b]
+// keeps c), and writes every c_t in the layout the forward kernels use,
+// C[d][slot][b][u] with slot t + 1 (forward direction) or t (reverse) and the
+// initial state in slot 0 / T.  Gate loads of four steps are issued before
+// their arithmetic.
+template <typename T>
+__global__ void recompute_cells_kernel(const T* __restrict__ gates, const T* __restrict__ c0, float* __restrict__ C,
+                                       int TT, int B, int H, int D, const int* __restrict__ len, int clip, float lo,
+                                       float hi) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(D) * B * H) return;
+  const int u = static_cast<int>(i % H);
+  const int b = static_cast<int>((i / H) % B);
+  const int d = static_cast<int>(i / (static_cast<int64_t>(H) * B));
+  const int lenb = len ? len[b] : TT;
+  float* Cd = C + static_cast<int64_t>(d) * (TT + 1) * B * H;
+  float c = c0 ? to_f<T>(c0[(static_cast<int64_t>(d) * B + b) * H + u]) : 0.f;
+  Cd[(static_cast<int64_t>(d ? TT : 0) * B + b) * H + u] = c;
+  const T* G = gates + (static_cast<int64_t>(d) * TT * B + b) * 4 * H + 4 * u;
+  const int64_t gstep = static_cast<int64_t>(B) * 4 * H;
+  for (int s0 = 0; s0 < TT; s0 += 4) {
+    float g4[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int s = s0 + j;
+      const int t = d ? TT - 1 - s : s;
+      if (s < TT) Vec4<T>::load(G + static_cast<int64_t>(t) * gstep, g4[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int s = s0 + j;
+      if (s >= TT) break;
+      const int t = d ? TT - 1 - s : s;
+      const float cc = clip ? (c < lo ? lo : (c > hi ? hi : c)) : c;
+      if (t < lenb) c = g4[j][1] * cc + g4[j][0] * g4[j][2];
+      Cd[(static_cast<int64_t>(d ? t : t + 1) * B + b) * H + u] = c;
+    }
+  }
+}
+
 int check_launch() {
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
@@ -187,6 +231,21 @@ int launch_states_to_y(const void* h0, void* Y, int T, int B, int H, int D, int 
   else
     states_to_y_kernel<float><<<(n + 255) / 256, 256, 0, s>>>(static_cast<const float*>(h0),
                                                               static_cast<float*>(Y), T, B, H, D, dir);
+  return check_launch();
+}
+
+int launch_recompute_cells(const void* gates, const void* c0, float* C, int T, int B, int H, int D, int is_bf16,
+                           const int* len, int clip, float lo, float hi, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(D) * B * H;
+  const unsigned grid = static_cast<unsigned>((n + 255) / 256);
+  if (is_bf16)
+    recompute_cells_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(gates),
+                                                               static_cast<const __nv_bfloat16*>(c0), C, T, B, H,
+                                                               D, len, clip, lo, hi);
+  else
+    recompute_cells_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(gates),
+                                                       static_cast<const float*>(c0), C, T, B, H, D, len, clip, lo,
+                                                       hi);
   return check_launch();
 }
 

@@ -141,5 +141,11 @@ int launch_states_to_y(const void* h0, void* Y, int T, int B, int H, int D, int 
 int launch_bias_grad_scatter(const float* db, int H, const int* slot_dst, int is_second,
                              float* out, cudaStream_t s);
 int launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
+// LSTM cell states c_t of every step from the saved gate activations
+// ([D][T, B, 4H], slots i, f, g, o) and c0 ([D, B, H] or null = zero) into C
+// ([D][T+1, B, H] fp32, the forward kernels' layout); len / clip as in
+// PersistArgs.
+int launch_recompute_cells(const void* gates, const void* c0, float* C, int T, int B, int H, int D, int is_bf16,
+                           const int* len, int clip, float lo, float hi, cudaStream_t s);
 
 }  // namespace rnn

@@ -184,6 +184,19 @@ rnn_status_t rnn_set_timeout_ns(rnn_handle_t handle, uint64_t ns);
  * outside [0, seq_len], RNN_CUDA_ERROR if the copy fails. */
 rnn_status_t rnn_set_seq_lengths(rnn_handle_t handle, const int* lengths);
 
+/* Recomputation (poplibs Lstm.cpp LstmRecomputationMode::CellAndTanh).
+ * mode 1: the LSTM forward keeps no cell states in the reserve (smaller by
+ * num_layers * D * (seq_len+1) * batch * hidden * 4 bytes); rnn_backward_data
+ * recomputes them from the saved gate activations (c_t = f * c_{t-1} + i * g,
+ * with the cell clipping and sequence lengths in force) before each layer's
+ * backward pass, into its workspace, and tanh(c_t) is recomputed in the
+ * backward step as always.  rnn_backward_data must then receive the same cx
+ * as rnn_forward.  mode 0 (the default) stores the cell states.  A GRU or
+ * plain-RNN handle has no cell state and ignores the mode.  Changes the sizes
+ * rnn_get_sizes reports: set it before allocating.  RNN_BAD_PARAM for other
+ * modes. */
+rnn_status_t rnn_set_recomputation(rnn_handle_t handle, int mode);
+
 /* LSTM cell clipping (the clip / dclip of the persistent backward-data kernel
  * fragment's LSTM branch).  With enable != 0 and lo < hi the cell state stays
  * the raw value c, and every use of it goes through clip(x) = min(max(x, lo),

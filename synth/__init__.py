@@ -55,6 +55,8 @@ class Workload:
     # variable sequence lengths: None = every sequence has T steps; else the
     # lengths are drawn uniformly from [ceil(min_len_frac * T), T]
     min_len_frac: Optional[float] = None
+    # LSTM recomputation mode: the backward pass recomputes the cell states
+    recompute: bool = False
 
     @property
     def gates(self) -> int:
@@ -117,6 +119,10 @@ WORKLOADS: Dict[str, Workload] = {
     "lstm2bi_bf16_T512_B128_H1024_varlen": Workload(
         "lstm2bi_bf16_T512_B128_H1024_varlen", LSTM, False, 2, True, 512, 128, 1024, 1024, "bf16", 3,
         state_std=None, min_len_frac=0.5),
+    # the 2-layer bidirectional LSTM with the cell states recomputed in the backward pass
+    "lstm2bi_bf16_T512_B128_H1024_recompute": Workload(
+        "lstm2bi_bf16_T512_B128_H1024_recompute", LSTM, False, 2, True, 512, 128, 1024, 1024, "bf16", 3,
+        state_std=None, recompute=True),
 }
 
 

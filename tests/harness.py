@@ -57,7 +57,7 @@ def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: i
     wl = inp.wl
     T, Bt, _ = inp.x.shape
     rnn = R.RNN(wl.mode, wl.input_size, wl.hidden_size, T, Bt, wl.num_layers, wl.bidirectional, wl.reset_after,
-                wl.dtype, wl.gate_order, wl.batch_first, algo)
+                wl.dtype, wl.gate_order, wl.batch_first, algo, recompute=wl.recompute)
     try:
         if inp.lengths is not None:
             rnn.set_seq_lengths([int(v) for v in inp.lengths])
@@ -73,7 +73,7 @@ def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: i
             if backward:
                 dys = synth.to_batch_first(inp.dy) if wl.batch_first else inp.dy
                 dy = to_dev(dys, wl)
-                dx, dhx, dcx = rnn.backward_data(dy, w, to_dev(inp.dhy, wl), to_dev(inp.dcy, wl))
+                dx, dhx, dcx = rnn.backward_data(dy, w, to_dev(inp.dhy, wl), to_dev(inp.dcy, wl), cx=cx)
                 dw = rnn.backward_weights(x)
             rnn.sync()
         yn = to_np(y)
