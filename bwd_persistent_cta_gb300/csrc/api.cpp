@@ -183,8 +183,11 @@ int run_persist(rnn_handle_s* h, PersistArgs a, bool bwd, cudaStream_t s) {
     int rc = reset_counters(h, s);
     if (rc) return rc;
     TimeScope ts(h, bwd ? 1 : 0, s);
-    if (h->algo == RNN_ALGO_PERSIST_TC)
-      rc = bwd ? launch_persist_bwd_tc(x, s, h->num_sms) : launch_persist_fwd_tc(x, s, h->num_sms);
+    if (h->algo == RNN_ALGO_PERSIST_TC) {
+      // forward: the cluster-resident kernel when the layer fits one cluster
+      rc = bwd ? 2 : launch_persist_fwd_cl(x, s, h->num_sms);
+      if (rc == 2) rc = bwd ? launch_persist_bwd_tc(x, s, h->num_sms) : launch_persist_fwd_tc(x, s, h->num_sms);
+    }
     else
       rc = bwd ? launch_persist_bwd_simt(x, s, h->num_sms) : launch_persist_fwd_simt(x, s, h->num_sms);
     return count(h, rc);

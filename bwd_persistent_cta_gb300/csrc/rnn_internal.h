@@ -43,7 +43,8 @@ struct DevArea {
   unsigned int pad[27];
 };
 
-enum KernelId : unsigned int { K_FWD_SIMT = 1, K_BWD_SIMT = 2, K_FWD_TC = 3, K_BWD_TC = 4, K_GEMM_TC = 5 };
+enum KernelId : unsigned int { K_FWD_SIMT = 1, K_BWD_SIMT = 2, K_FWD_TC = 3, K_BWD_TC = 4, K_GEMM_TC = 5,
+                                K_FWD_CL = 6 };
 enum WaitKind : unsigned int { W_COUNTER = 1, W_TMA = 2, W_MMA = 3, W_PEER = 4 };
 
 // C[row(m), n] = sum_k A(m, k) * B(n, k)  (+ bias[n]) (+ C_old if beta)
@@ -114,13 +115,16 @@ int launch_persist_fwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
 int launch_persist_bwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
 
 bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms);
+// Cluster-resident forward (persist_cl.cu): returns 2 when the shape or the
+// options do not fit it (the caller then uses the tcgen05 persistent kernel).
+int launch_persist_fwd_cl(const PersistArgs& a, cudaStream_t s, int num_sms);
 int launch_persist_fwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms);
 int launch_persist_bwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms);
 
 // TMA tensor map (CUtensorMap, 128 bytes) over a bf16 row-major matrix
 // ptr[j * ld + i], i < dim0, j < dim1, box box0 x box1, 128-byte swizzle.
 int make_tmap_bf16_2d(void* map, const void* ptr, uint64_t dim0, uint64_t dim1, uint64_t ld_elems,
-                      uint32_t box0, uint32_t box1);
+                      uint32_t box0, uint32_t box1, int swizzle_bytes = 128);
 // 4-D view: element (i0..i3) at 2*i0 + i1*strides[0] + i2*strides[1] + i3*strides[2]
 // bytes; box[0] * 2 == 128 (the swizzle span).
 int make_tmap_bf16_4d(void* map, const void* ptr, const uint64_t* dims, const uint64_t* strides_bytes,

@@ -27,9 +27,10 @@ void lookup() {
 }  // namespace
 
 // Row-major matrix ptr[j * ld + i], i < dim0 (contiguous), j < dim1; the box is
-// box0 x box1 elements with box0 * 2 == 128 bytes (the swizzle span).
+// box0 x box1 elements with box0 * 2 == swizzle_bytes (the swizzle span, 128
+// or 64).
 int make_tmap_bf16_2d(void* map, const void* ptr, uint64_t dim0, uint64_t dim1, uint64_t ld_elems,
-                      uint32_t box0, uint32_t box1) {
+                      uint32_t box0, uint32_t box1, int swizzle_bytes) {
   std::call_once(g_once, lookup);
   if (!g_encode) return 3;
   if ((reinterpret_cast<uintptr_t>(ptr) & 15) != 0 || (ld_elems * 2) % 16 != 0) return 2;
@@ -37,8 +38,10 @@ int make_tmap_bf16_2d(void* map, const void* ptr, uint64_t dim0, uint64_t dim1, 
   cuuint64_t strides[1] = {ld_elems * 2};
   cuuint32_t box[2] = {box0, box1};
   cuuint32_t estr[2] = {1, 1};
+  if (swizzle_bytes != 128 && swizzle_bytes != 64) return 2;
   CUresult r = g_encode(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
-                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : 2;
 }
