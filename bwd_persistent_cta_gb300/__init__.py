@@ -52,6 +52,8 @@ _SIGS = {
     "rnn_set_seq_lengths": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int)]),
     "rnn_set_cell_clip": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_double, ctypes.c_double]),
     "rnn_set_recomputation": (ctypes.c_int, [_P, ctypes.c_int]),
+    "rnn_set_interleaved_dw": (ctypes.c_int, [_P, ctypes.c_int]),
+    "rnn_interleaved_dw_active": (ctypes.c_int, [_P]),
     "rnn_launch_count": (ctypes.c_uint64, [_P]),
     "rnn_selected_algo": (ctypes.c_int, [_P]),
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
@@ -157,6 +159,14 @@ def rnn_set_recomputation(handle, mode: int) -> int:
     return lib().rnn_set_recomputation(handle, int(mode))
 
 
+def rnn_set_interleaved_dw(handle, mode: int) -> int:
+    return lib().rnn_set_interleaved_dw(handle, int(mode))
+
+
+def rnn_interleaved_dw_active(handle) -> int:
+    return int(lib().rnn_interleaved_dw_active(handle))
+
+
 def rnn_set_cell_clip(handle, enable: int, lo: float = 0.0, hi: float = 0.0) -> int:
     return lib().rnn_set_cell_clip(handle, int(enable), float(lo), float(hi))
 
@@ -210,7 +220,7 @@ class RNN:
     def __init__(self, mode: str, input_size: int, hidden_size: int, seq_len: int, batch: int,
                  num_layers: int = 1, bidirectional: bool = False, reset_after: bool = True,
                  dtype: str = "bf16", gate_order: Sequence[int] = (), batch_first: bool = False,
-                 algo: int = RNN_ALGO_AUTO, device=None, recompute: bool = False):
+                 algo: int = RNN_ALGO_AUTO, device=None, recompute: bool = False, interleaved_dw: int = 1):
         import torch
         self.torch = torch
         self.device = torch.device(device if device is not None else "cuda")
@@ -231,6 +241,8 @@ class RNN:
             self.handle = rnn_create(d)
         if recompute:
             self._check(rnn_set_recomputation(self.handle, 1), "rnn_set_recomputation")
+        if int(interleaved_dw) != 1:
+            self._check(rnn_set_interleaved_dw(self.handle, int(interleaved_dw)), "rnn_set_interleaved_dw")
         self.weight_bytes, self.workspace_bytes, self.reserve_bytes = rnn_get_sizes(self.handle)
         self.weight_count = self.weight_bytes // (2 if dtype == "bf16" else 4)
         self.workspace = torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=self.device)
@@ -250,6 +262,10 @@ class RNN:
     @property
     def algo(self) -> int:
         return rnn_selected_algo(self.handle)
+
+    @property
+    def interleaved_dw(self) -> bool:
+        return bool(rnn_interleaved_dw_active(self.handle))
 
     def launches(self) -> int:
         return rnn_launch_count(self.handle)

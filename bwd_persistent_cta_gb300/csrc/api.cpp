@@ -81,7 +81,7 @@ void fill_layout(rnn_handle_s* h) {
   // reserve
   Bump r;
   h->r_y.assign(L, 0); h->r_g.assign(L, 0); h->r_c.assign(L, 0); h->r_rh.assign(L, 0);
-  h->r_dg.assign(L, 0); h->r_db.assign(L, 0);
+  h->r_dg.assign(L, 0); h->r_db.assign(L, 0); h->r_dwhh.assign(L, 0);
   const size_t TB = static_cast<size_t>(T) * B;
   for (int l = 0; l < L; ++l) {
     h->r_y[l] = r.take(static_cast<size_t>(T + 2) * B * D * H * es);
@@ -90,6 +90,7 @@ void fill_layout(rnn_handle_s* h) {
     if (h->rb) h->r_rh[l] = r.take(static_cast<size_t>(D) * TB * H * es);
     h->r_dg[l] = r.take(TB * D * 4 * H * es);
     h->r_db[l] = r.take(static_cast<size_t>(D) * 4 * H * 4);
+    if (h->dw_bptt) h->r_dwhh[l] = r.take(static_cast<size_t>(D) * G * H * H * 4);
   }
   h->reserve_bytes = r.off;
   // workspace
@@ -124,6 +125,17 @@ void slots_bwd_rec(const rnn_handle_s* h, int* m) {
   else if (h->lstm) { for (int s = 0; s < 4; ++s) m[s] = h->pos[s]; }
   else if (h->ra) { m[0] = h->pos[0]; m[1] = h->pos[1]; m[2] = -1; m[3] = h->pos[2]; }
   else { m[0] = h->pos[0]; m[1] = h->pos[1]; m[2] = h->pos[2]; m[3] = -1; }
+}
+
+// Interleaved dW_hh (the weight update inside the backward pass) where the
+// SIMT backward kernel runs the layer and can hide the per-step work; the
+// reserve then holds the accumulated gradient between the backward calls.
+void update_dw_bptt(rnn_handle_s* h) {
+  PersistArgs probe;
+  probe.mode = h->desc.mode; probe.reset_after = h->ra; probe.is_bf16 = h->bf16;
+  probe.T = h->T; probe.B = h->B; probe.H = h->H; probe.D = h->D;
+  h->dw_bptt = h->dw_mode && h->algo == RNN_ALGO_PERSIST_SIMT &&
+                persist_simt_dwhh_ok(probe, h->num_sms, h->dw_mode == 1);
 }
 
 int count(rnn_handle_s* h, int rc, int n = 1) {
@@ -271,6 +283,8 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
   h->d_len = nullptr;
   h->has_len = 0;
   h->recompute = 0;
+  h->dw_mode = 1;
+  h->dw_bptt = 0;
   h->clip = 0;
   h->clip_lo = h->clip_hi = 0.f;
   h->trace = false;
@@ -285,6 +299,8 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
   if (desc->algo == RNN_ALGO_PERSIST_TC) h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : 0;
   else if (desc->algo == RNN_ALGO_PERSIST_SIMT) h->algo = simt_ok ? RNN_ALGO_PERSIST_SIMT : 0;
   else h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : (simt_ok ? RNN_ALGO_PERSIST_SIMT : 0);
+  update_dw_bptt(h);
+  fill_layout(h);
   return h->algo == 0 ? RNN_NOT_SUPPORTED : RNN_OK;
 }
 
@@ -369,6 +385,16 @@ rnn_status_t rnn_set_recomputation(rnn_handle_t h, int mode) {
   fill_layout(h);
   return RNN_OK;
 }
+
+rnn_status_t rnn_set_interleaved_dw(rnn_handle_t h, int mode) {
+  if (!h || mode < 0 || mode > 2) return RNN_BAD_PARAM;
+  h->dw_mode = mode;
+  update_dw_bptt(h);
+  fill_layout(h);
+  return RNN_OK;
+}
+
+int rnn_interleaved_dw_active(rnn_handle_t h) { return h ? h->dw_bptt : 0; }
 
 rnn_status_t rnn_set_cell_clip(rnn_handle_t h, int enable, double lo, double hi) {
   if (!h) return RNN_BAD_PARAM;
@@ -570,6 +596,11 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
     a.clip = h->clip; a.clip_lo = h->clip_lo; a.clip_hi = h->clip_hi;
     a.dh0 = dhx ? static_cast<char*>(dhx) + so : nullptr;
     a.dc0 = (h->lstm && dcx) ? static_cast<char*>(dcx) + so : nullptr;
+    if (h->dw_bptt) {
+      a.dwhh = at<float>(reserve, h->r_dwhh[l]);
+      for (int k = 0; k < 4; ++k) a.whh_map[k] = sr[k];
+      a.RH = h->rb ? at<char>(reserve, h->r_rh[l]) : nullptr;
+    }
     RNN_TRY(run_persist(h, a, true, s));
     // input gradient dX = dG * W_ih (both directions summed through K)
     GemmArgs g;
@@ -645,18 +676,27 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
       g.C = dwf + h->off_ih[i]; g.ldc = Il; g.c_bf16 = 0;
       for (int k = 0; k < 4; ++k) g.perm[k] = m_ih[k];
       RNN_TRY(run_gemm(h, g, s, 4));
-      // dW_hh = sum over (t, b) of dG^h h_prev^T ; h_prev rows are Y slots t (forward) / t+2 (reverse)
-      const char* hp = rs + h->r_y[l] + (static_cast<size_t>(d == 0 ? 0 : 2) * B * D * H + static_cast<size_t>(d) * H) * es;
-      g.N = H;
-      g.B = hp; g.ldb = D * H; g.b_kmajor = 0;
-      g.C = dwf + h->off_hh[i]; g.ldc = H;
-      for (int k = 0; k < 4; ++k) g.perm[k] = m_hh[k];
-      RNN_TRY(run_gemm(h, g, s, 4));
-      if (h->rb) {
-        // reset-before candidate rows: dW_hn = sum dn (r * h_prev)^T
-        g.B = rs + h->r_rh[l] + static_cast<size_t>(d) * TB * H * es; g.ldb = H;
-        g.perm[0] = -1; g.perm[1] = -1; g.perm[2] = pos[2]; g.perm[3] = -1;
+      if (h->dw_bptt) {
+        // accumulated by the backward-data pass, already in the caller's rows
+        const size_t bytes = static_cast<size_t>(h->G) * H * H * 4;
+        if (cudaMemcpyAsync(dwf + h->off_hh[i], rs + h->r_dwhh[l] + d * bytes, bytes, cudaMemcpyDeviceToDevice,
+                            s) != cudaSuccess)
+          return RNN_CUDA_ERROR;
+      } else {
+        // dW_hh = sum over (t, b) of dG^h h_prev^T ; h_prev rows are Y slots t (forward) / t+2 (reverse)
+        const char* hp =
+            rs + h->r_y[l] + (static_cast<size_t>(d == 0 ? 0 : 2) * B * D * H + static_cast<size_t>(d) * H) * es;
+        g.N = H;
+        g.B = hp; g.ldb = D * H; g.b_kmajor = 0;
+        g.C = dwf + h->off_hh[i]; g.ldc = H;
+        for (int k = 0; k < 4; ++k) g.perm[k] = m_hh[k];
         RNN_TRY(run_gemm(h, g, s, 4));
+        if (h->rb) {
+          // reset-before candidate rows: dW_hn = sum dn (r * h_prev)^T
+          g.B = rs + h->r_rh[l] + static_cast<size_t>(d) * TB * H * es; g.ldb = H;
+          g.perm[0] = -1; g.perm[1] = -1; g.perm[2] = pos[2]; g.perm[3] = -1;
+          RNN_TRY(run_gemm(h, g, s, 4));
+        }
       }
       const float* db = reinterpret_cast<const float*>(rs + h->r_db[l]) + static_cast<size_t>(d) * 4 * H;
       RNN_TRY(count(h, launch_bias_grad_scatter(db, H, m_b, 0, dwf + h->off_b[i], s)));

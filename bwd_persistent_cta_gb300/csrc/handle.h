@@ -25,6 +25,8 @@ struct rnn_handle_s {
   int* d_len;                  // device copy of the sequence lengths (B ints), or null
   int has_len;                 // 1: the lengths in d_len apply
   int recompute;               // LSTM: no cell states in the reserve; the backward recomputes them
+  int dw_mode;                 // interleaved dW_hh: 0 never, 1 where the SIMT backward kernel hides it, 2 where it fits
+  int dw_bptt;                 // 1: rnn_backward_data accumulates dW_hh into the reserve
   int clip;                    // LSTM cell clipping on, bounds [clip_lo, clip_hi]
   float clip_lo, clip_hi;
   bool trace;
@@ -36,7 +38,7 @@ struct rnn_handle_s {
   std::vector<size_t> off_ih, off_hh, off_b, off_bh;
   size_t weight_elems;
   // reserve offsets (bytes), per layer
-  std::vector<size_t> r_y, r_g, r_c, r_rh, r_dg, r_db;
+  std::vector<size_t> r_y, r_g, r_c, r_rh, r_dg, r_db, r_dwhh;
   size_t reserve_bytes;
   // workspace offsets (bytes)
   size_t w_p, w_xin, w_dyi, w_dx0, w_wx, w_wxt, w_wr, w_wrt, w_bx, w_bh, w_y0, w_y1, w_rh, w_g;

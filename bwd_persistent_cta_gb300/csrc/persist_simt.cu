@@ -60,10 +60,12 @@ __device__ __forceinline__ float ldcg_f(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ float ldcg_f(const __nv_bfloat16* p) { return __bfloat162float(__ldcg(p)); }
 
 // thread 0 waits on the counter; the verdict is shared with the whole CTA.
+// A direction run by one CTA needs no counter: the block barrier orders its
+// own global writes before its reads.
 __device__ __forceinline__ bool cta_wait(const PersistArgs& a, const unsigned int* ctr, unsigned int target,
                                          unsigned int kernel, int step) {
   int ok = 1;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && gridDim.x > 1) {
     ok = wait_counter_geq(ctr, target, a.timeout_ns) ? 1 : 0;
     if (!ok) report_status(a.dev, 4u /* RNN_TIMEOUT */, kernel, static_cast<unsigned>(step), W_COUNTER);
   }
@@ -74,7 +76,7 @@ __device__ __forceinline__ bool cta_wait(const PersistArgs& a, const unsigned in
 // barrier, then the release add).
 __device__ __forceinline__ void cta_arrive(unsigned int* ctr, bool skip) {
   __syncthreads();
-  if (threadIdx.x == 0 && !skip) red_release_gpu_add(ctr, 1u);
+  if (threadIdx.x == 0 && !skip && gridDim.x > 1) red_release_gpu_add(ctr, 1u);
 }
 
 // The recurrent weights as seen by one CTA: resident in shared memory
@@ -331,6 +333,82 @@ __global__ void __launch_bounds__(kThreads, 1) persist_fwd_simt_kernel(PersistAr
 // ---------------------------------------------------------------------------
 // backward through time
 // ---------------------------------------------------------------------------
+// Floats of the staging tile hs (B rows of KC + 1), rounded up to 16 bytes.
+__host__ __device__ inline int hs_floats(int B, int KC) { return (B * (KC + 1) + 3) & ~3; }
+
+// Per-step work bounds for accumulating dW_hh inside the backward kernel.
+// Anywhere (mode 2): NU * H * B <= kDwhhWork, at most 4 * kDwhhWork / 256 =
+// 256 multiply-adds per thread.  By default (mode 1) only where the work
+// hides behind the wait for the step exchange: each thread's share of the
+// (unit, column) items times the batch at most kDwhhIters (measured on
+// GB300: GRU resetAfter fp32 H128 B16, 1 x 16, and GRU reset-before bf16
+// H128 B8, 1 x 8, gained 30 and 13 us per step; LSTM fp32 H256 B8, 4 x 8,
+// lost 20 us).
+constexpr int kDwhhWork = 16384;
+constexpr int kDwhhIters = 16;
+
+// 4-byte asynchronous global -> shared copy (completes at cp_async_wait_all)
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc) {
+  const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Stages the step's second operand of the dW_hh accumulation into shared
+// memory, vs[b][k] = h_{t-1}[b][k] (Y slot sp), and for the reset-before
+// candidate vs[B + b][k] = (r * h_{t-1})[b][k] (RH), in 4-byte copies (H even
+// for bf16) issued early in the step so that they land during the contraction.
+template <typename T>
+__device__ __forceinline__ void dwhh_stage(const PersistArgs& a, T* vs, int dir, int t, int sp, bool rb) {
+  const int H = a.H, B = a.B;
+  const int64_t ldY = static_cast<int64_t>(a.D) * H;
+  constexpr int E = 4 / static_cast<int>(sizeof(T));
+  const int HW = H / E;
+  const T* hp = static_cast<const T*>(a.Y) + static_cast<int64_t>(sp) * B * ldY + dir * H;
+  for (int i = threadIdx.x; i < B * HW; i += kThreads) {
+    const int b = i / HW, kw = i - b * HW;
+    cp_async_4(vs + b * H + kw * E, hp + b * ldY + kw * E);
+  }
+  if (rb) {
+    const T* rh = static_cast<const T*>(a.RH) + (static_cast<int64_t>(dir) * a.T + t) * B * H;
+    for (int i = threadIdx.x; i < B * HW; i += kThreads) cp_async_4(vs + B * H + i * E, rh + i * E);
+  }
+}
+
+// dW_hh accumulation of one step (the weight update interleaved with the
+// backward pass: poplibs Lstm.cpp / Gru.cpp accumulate the weight gradients
+// inside the backward loop, "Interleaved weight update").  The CTA's rows are
+// its units' 4 gate slots, row j = 4 * ul + slot; for column k
+//   acc[j][k] += sum_b dG_t[b][j] * v_b[k],
+// v = h_{t-1}, or r * h_{t-1} for the reset-before candidate (both staged in
+// vs).  Work items are (unit, column) pairs, k fastest, spread over all
+// threads; a warp reads one unit's four gate gradients as a broadcast float4
+// from dgs[b][4 * NU], and the four sums of an item stay in registers over
+// the batch.
+template <typename T>
+__device__ __forceinline__ void dwhh_step(float* accs, const float* dgs, const T* vs, int NU, int nu, int H, int B,
+                                          bool rb) {
+  const int ld = 4 * NU;
+  for (int item = threadIdx.x; item < nu * H; item += kThreads) {
+    const int ul = item / H, k = item - ul * H;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll 4
+    for (int b = 0; b < B; ++b) {
+      const float4 g = *reinterpret_cast<const float4*>(dgs + b * ld + 4 * ul);
+      const float v = to_f<T>(vs[b * H + k]);
+      s0 = fmaf(g.x, v, s0);
+      s1 = fmaf(g.y, v, s1);
+      s2 = fmaf(g.z, rb ? to_f<T>(vs[(B + b) * H + k]) : v, s2);
+      s3 = fmaf(g.w, v, s3);
+    }
+    float* acc = accs + 4 * ul * H + k;
+    acc[0] += s0;
+    acc[H] += s1;
+    acc[2 * H] += s2;
+    acc[3 * H] += s3;
+  }
+}
+
 template <typename T, int PP, bool STREAM>
 __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistArgs a, int NU, int KC) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -356,6 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
     }
   }
   const WView<T, STREAM> W{STREAM ? WT : Ws, NU, WS, u0, H};
+  // interleaved dW_hh: accumulator [4 * NU][H] and the step's gate gradients
+  // [B][4 * NU] after the staging tile
+  const bool dw = a.dwhh != nullptr;
+  float* accs = hs + hs_floats(B, KC);
+  float* dgs = accs + 4 * NU * H;
+  T* vs = reinterpret_cast<T*>(dgs + 4 * NU * B);
+  if (dw)
+    for (int i = threadIdx.x; i < 4 * nu * H; i += kThreads) accs[i] = 0.f;
 
   const T* Y = static_cast<const T*>(a.Y);
   const T* G = static_cast<const T*>(a.gates);
@@ -391,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
     float dhr[PP];
 #pragma unroll
     for (int p = 0; p < PP; ++p) dhr[p] = 0.f;
+    if (dw && s == 0) dwhh_stage<T>(a, vs, dir, dir ? 0 : TT - 1, dir ? 2 : TT - 1, rb);
     if (s == 0) {
       if (a.dhT) {
 #pragma unroll
@@ -403,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
       }
     } else {
       if (!cta_wait(a, ctr, phases * nblk, K_BWD_SIMT, s)) return;
+      if (dw && s < TT) dwhh_stage<T>(a, vs, dir, dir ? s : TT - 1 - s, dir ? s + 2 : TT - 1 - s, rb);
       const int tp = dir ? s - 1 : TT - s;   // step processed just before
       const T* src = dG + static_cast<int64_t>(tp) * B * ldG + dir * K4;
       if (rb)
@@ -457,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
           carry_h[p] = gh;
         }
         Vec4<T>::store(dg, da);
+        if (dw) *reinterpret_cast<float4*>(dgs + b * 4 * NU + 4 * ul) = make_float4(da[0], da[1], da[2], da[3]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) db[p][q] += da[q];
       } else if (plain) {
@@ -469,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
           carry[p] = gh;
         }
         Vec4<T>::store(dg, da);
+        if (dw) *reinterpret_cast<float4*>(dgs + b * 4 * NU + 4 * ul) = make_float4(da[0], 0.f, 0.f, 0.f);
         db[p][0] += da[0];
       } else if (!rb) {
         const float gh = dhr[p] + carry[p];
@@ -486,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
           carry[p] = gh;
         }
         Vec4<T>::store(dg, da);
+        if (dw) *reinterpret_cast<float4*>(dgs + b * 4 * NU + 4 * ul) = make_float4(da[0], da[1], da[2], da[3]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) db[p][q] += da[q];
       } else {
@@ -505,12 +596,22 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
         dg[1] = from_f<T>(dz);
         dg[2] = from_f<T>(dn);
         dg[3] = from_f<T>(0.f);
+        if (dw) {
+          dgs[b * 4 * NU + 4 * ul + 1] = dz;
+          dgs[b * 4 * NU + 4 * ul + 2] = dn;
+          dgs[b * 4 * NU + 4 * ul + 3] = 0.f;
+        }
         db[p][1] += dz;
         db[p][2] += dn;
       }
     }
+    if (dw) cp_async_wait_all();
     cta_arrive(ctr, skip);
     ++phases;
+    // the weight-gradient work of the step overlaps the wait for the other CTAs
+    // (cta_arrive's barrier made dgs and vs complete; the next cta_wait's
+    // barrier orders these reads before the next step's writes)
+    if (dw && !rb) dwhh_step<T>(accs, dgs, vs, NU, nu, H, B, false);
     if (rb) {
       // phase B: d(rh) = W_hn^T dn, then dr
       if (!cta_wait(a, ctr, phases * nblk, K_BWD_SIMT, s)) return;
@@ -531,11 +632,13 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
         const bool live = t < lenp[p];
         const float dr = live ? drh[p] * hp * r * (1.f - r) : 0.f;
         dG[(static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u] = from_f<T>(dr);
+        if (dw) dgs[b * 4 * NU + 4 * ul] = dr;
         db[p][0] += dr;
         carry[p] = live ? drh[p] * r + dhv[p] * z : dhv[p];
       }
       cta_arrive(ctr, skip);
       ++phases;
+      if (dw) dwhh_step<T>(accs, dgs, vs, NU, nu, H, B, true);
     }
   }
 
@@ -557,6 +660,18 @@ __global__ void __launch_bounds__(kThreads, 1) persist_bwd_simt_kernel(PersistAr
     for (int i = threadIdx.x; i < 4 * 64; i += kThreads) {
       const int ul = base + i / 4;
       if (ul < nu) a.db[static_cast<int64_t>(dir) * K4 + 4 * (u0 + ul) + (i & 3)] = dbs[i];
+    }
+  }
+
+  // interleaved dW_hh: each row of the CTA to its caller gate block
+  if (dw) {
+    __syncthreads();
+    const int G = lstm ? 4 : (plain ? 1 : 3);
+    float* dst = a.dwhh + static_cast<int64_t>(dir) * G * H * H;
+    for (int i = threadIdx.x; i < 4 * nu * H; i += kThreads) {
+      const int j = i / H, k = i - j * H;
+      const int m = a.whh_map[j & 3];
+      if (m >= 0) dst[(static_cast<int64_t>(m) * H + u0 + (j >> 2)) * H + k] = accs[i];
     }
   }
 }
@@ -860,6 +975,11 @@ const void* kernel_for(const PersistArgs& a, bool bwd, const SimtPlan& pl) {
 // Pick units per CTA: minimise an estimated step time (a fixed cost for the
 // cross-CTA exchange when there is more than one CTA, plus the per-thread FMA
 // count) subject to shared memory, registers and co-residency of the grid.
+// The exchange weight (500 serial FMAs per thread) is from GB300 timings: a
+// step exchange costs about 2-3 us, one serial FMA per thread (weights and
+// state from shared memory) about 6 ns; e.g. GRU reset-before bf16, H = 128,
+// batch 8: one CTA with 4 pairs per thread took 30 us per backward step,
+// 8 CTAs with one pair each 12 us.
 // Without a resident fit, stream the weights and spread them over the most
 // CTAs that fit (more read bandwidth).
 int make_plan(const PersistArgs& a, bool bwd, int num_sms, SimtPlan* out) {
@@ -872,6 +992,7 @@ int make_plan(const PersistArgs& a, bool bwd, int num_sms, SimtPlan* out) {
   const int Kmax = bwd ? 4 * H : H;
   if (KC > Kmax) KC = (Kmax + 3) / 4 * 4;
   const size_t hs_bytes = static_cast<size_t>(B) * (KC + 1) * 4;
+  const bool dw = bwd && a.dwhh != nullptr;
   double best = 1e300;
   SimtPlan bp;
   for (int NU = 1; NU <= H; ++NU) {
@@ -879,11 +1000,18 @@ int make_plan(const PersistArgs& a, bool bwd, int num_sms, SimtPlan* out) {
     if (nblk * a.ndir > num_sms) continue;
     const int pp = pp_for(NU * B);
     if (pp == 0) break;
+    if (dw && (static_cast<int64_t>(NU) * H * B > kDwhhWork || (a.is_bf16 && (H & 1)))) break;
     const size_t wbytes = bwd ? static_cast<size_t>(NU) * (4 * H + (a.is_bf16 ? 2 : 1)) * es
                               : static_cast<size_t>(4) * NU * (H + (a.is_bf16 ? 2 : 1)) * es;
-    const size_t smem = align16(wbytes) + hs_bytes;
+    // interleaved dW_hh: accumulator [4 NU][H] and gate gradients [B][4 NU],
+    // fp32, then the staged h_{t-1} (and r * h_{t-1}) tiles [B][H]
+    const bool rb = a.mode == 1 && !a.reset_after;
+    const size_t smem = dw ? align16(wbytes) + static_cast<size_t>(hs_floats(B, KC)) * 4 +
+                                 static_cast<size_t>(4) * NU * (H + B) * 4 +
+                                 static_cast<size_t>(rb ? 2 : 1) * B * H * es
+                           : align16(wbytes) + hs_bytes;
     if (smem > smem_cap) break;
-    const double cost = (nblk > 1 ? 3000.0 : 0.0) + static_cast<double>(pp) * 4.0 * H +
+    const double cost = (nblk > 1 ? 500.0 : 0.0) + static_cast<double>(pp) * 4.0 * H +
                         static_cast<double>(B) * (bwd ? 4 * H : H) / kThreads;
     if (cost < best) {
       best = cost;
@@ -891,6 +1019,7 @@ int make_plan(const PersistArgs& a, bool bwd, int num_sms, SimtPlan* out) {
     }
   }
   if (bp.NU == 0) {
+    if (dw) return 2;   // streamed weights: no interleaved dW_hh
     const int max_ctas = num_sms / a.ndir;
     if (max_ctas < 1) return 2;
     const int NU = (H + max_ctas - 1) / max_ctas;
@@ -989,6 +1118,33 @@ int plan_persist_simt(const PersistArgs& a, int num_sms, int* nblk, size_t* smem
   if (nblk) *nblk = pf.nblk > pb.nblk ? pf.nblk : pb.nblk;
   if (smem) *smem = pf.smem > pb.smem ? pf.smem : pb.smem;
   return 0;
+}
+
+// hidden_only (mode 1): the backward kernel's own plan must stay as without
+// the accumulation, span several CTAs per direction (a lone CTA has no wait
+// to hide the work behind: LSTM fp32 T16 B4 H32 measured +20 us in the
+// backward kernel against 10 us for the dW_hh GEMM) and give each thread at
+// most kDwhhIters item-batch iterations per step.  The launch tries both
+// directions at once first, then one at a time.
+bool persist_simt_dwhh_ok(const PersistArgs& a, int num_sms, bool hidden_only) {
+  PersistArgs b = a;
+  float probe = 0.f;
+  for (int nd : {a.D, 1}) {
+    b.ndir = nd;
+    SimtPlan nat, dwp;
+    b.dwhh = nullptr;
+    const int rn = make_plan(b, true, num_sms, &nat);
+    b.dwhh = &probe;   // only tested for null by the planner
+    const int rd = make_plan(b, true, num_sms, &dwp);
+    if (!hidden_only) {
+      if (rd == 0) return true;
+      continue;
+    }
+    if (rn != 0) continue;
+    return rd == 0 && dwp.NU == nat.NU && nat.nblk > 1 && !nat.stream &&
+           (nat.NU * a.H + kThreads - 1) / kThreads * a.B <= kDwhhIters;
+  }
+  return false;
 }
 
 int launch_persist_fwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms) {

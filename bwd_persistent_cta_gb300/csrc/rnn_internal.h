@@ -98,6 +98,13 @@ struct PersistArgs {
   const void* dcT = nullptr;
   void* dh0 = nullptr;               // [D][B, H] slice of dhx
   void* dc0 = nullptr;
+  // recurrent weight gradient accumulated inside the backward kernel (SIMT
+  // kernel only): [D][G*H][H] fp32 in the caller's gate blocks, internal slot s
+  // of unit u -> row whh_map[s] * H + u (-1: the slot is no W_hh row); the
+  // reset-before candidate rows take r * h_{t-1} from RH.  null = the weight
+  // gradient is left to the GEMM of the backward-weights call
+  float* dwhh = nullptr;
+  int whh_map[4] = {-1, -1, -1, -1};
   DevArea* dev = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int skip_cta = -1;
@@ -111,6 +118,10 @@ int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev,
 bool gemm_tc_supported(const GemmArgs& g);
 
 int plan_persist_simt(const PersistArgs& a, int num_sms, int* nblk, size_t* smem);
+// Whether the SIMT backward kernel can accumulate dW_hh in its step loop for
+// this shape (the per-step work small, the accumulator within shared memory);
+// with hidden_only, also that the work hides behind the step exchange.
+bool persist_simt_dwhh_ok(const PersistArgs& a, int num_sms, bool hidden_only);
 int launch_persist_fwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
 int launch_persist_bwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
 

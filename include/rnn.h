@@ -207,6 +207,31 @@ rnn_status_t rnn_set_recomputation(rnn_handle_t handle, int mode);
  * agree.  RNN_BAD_PARAM for a non-LSTM handle or lo >= hi. */
 rnn_status_t rnn_set_cell_clip(rnn_handle_t handle, int enable, double lo, double hi);
 
+/* Interleaved weight update (poplibs Lstm.cpp / Gru.cpp "Interleaved weight
+ * update": the weight gradients accumulated inside the backward loop).
+ * Where the SIMT persistent backward kernel runs the layers and its per-step
+ * share of the recurrent weight gradient is small (units per CTA x hidden x
+ * batch <= 16384 multiply-adds; small layers and batches), rnn_backward_data
+ * can accumulate dW_hh in fp32 step by step inside that kernel into the
+ * reserve, and rnn_backward_weights then copies it to dw instead of running
+ * the dW_hh GEMM; dW_ih and the biases are unchanged.  The result is the same
+ * sum in another summation order.
+ *   mode 0: always the GEMM;
+ *   mode 1 (the default): interleaved where, in addition, the work hides
+ *     behind the wait for the step exchange: each direction spans several
+ *     CTAs (a lone CTA has nothing to hide it behind) and each thread's
+ *     per-step share is at most 16 batch-length passes over its (unit,
+ *     column) items;
+ *   mode 2: interleaved wherever the kernel can.
+ * Changes the reserve size rnn_get_sizes reports (by num_layers * D * G *
+ * hidden^2 * 4 bytes when active): set it before allocating.  RNN_BAD_PARAM
+ * for other modes. */
+rnn_status_t rnn_set_interleaved_dw(rnn_handle_t handle, int mode);
+
+/* 1 when rnn_backward_data accumulates dW_hh (see rnn_set_interleaved_dw),
+ * else 0. */
+int rnn_interleaved_dw_active(rnn_handle_t handle);
+
 /* Number of kernels this handle has launched since it was created. */
 uint64_t rnn_launch_count(rnn_handle_t handle);
 

@@ -46,7 +46,8 @@ def to_np(t) -> Optional[np.ndarray]:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
-def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: int = 1) -> Dict:
+def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: int = 1,
+            interleaved_dw: int = 1) -> Dict:
     """Forward (+ backward data + weights) through the C ABI.  Results are
     returned seq-major and in canonical gate order (float64)."""
     import torch
@@ -57,7 +58,8 @@ def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: i
     wl = inp.wl
     T, Bt, _ = inp.x.shape
     rnn = R.RNN(wl.mode, wl.input_size, wl.hidden_size, T, Bt, wl.num_layers, wl.bidirectional, wl.reset_after,
-                wl.dtype, wl.gate_order, wl.batch_first, algo, recompute=wl.recompute)
+                wl.dtype, wl.gate_order, wl.batch_first, algo, recompute=wl.recompute,
+                interleaved_dw=interleaved_dw)
     try:
         if inp.lengths is not None:
             rnn.set_seq_lengths([int(v) for v in inp.lengths])
@@ -90,6 +92,8 @@ def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: i
             out["dparams"] = synth.unflatten_params(wl, dw.cpu().numpy())
         out["algo"] = rnn.algo
         out["launches"] = rnn.launches()
+        out["interleaved_dw"] = rnn.interleaved_dw
+        out["reserve_bytes"] = rnn.reserve_bytes
         torch.cuda.synchronize()
         return out
     finally:
