@@ -21,9 +21,16 @@ struct TcPlan {
 size_t a1k(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
 // Candidate K splits for one launch, preferred first: the largest split whose
-// grid fits (shorter per-CTA contraction, less shared memory per CTA).
+// grid fits (shorter per-CTA contraction, less shared memory per CTA), except
+// that the backward takes a cluster of 8 before one of 16.  Measured on GB300
+// (backward kernel, T=128): 16 -> 8 changed GRU resetAfter B64 H512 from 868
+// to 803 us, B64 H256 761 -> 672, B32 H512 584 -> 563, LSTM B64 H512 804 ->
+// 693, B32 H256 533 -> 454, B128 H512 1080 -> 1012, B64 H768 794 -> 783: the
+// partial-sum push and the cluster barrier shrink with the cluster while the
+// per-CTA MMAs double.  GRU above batch 64 keeps 16 (B128 H512: 1251 at 16,
+// 1353 at 8), its heavier per-row backward step being split over more CTAs.
 // Whether the clusters can all be resident at once is checked at launch.
-int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int max_out) {
+int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int max_out) {
   if (B < 1 || B > 256) return 0;
   const int K = bwd ? 4 * H : H;
   const int nrg = bwd ? H / 128 : (4 * H) / 128;
@@ -83,6 +90,11 @@ int make_plans(int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int ma
     p.smem = smem < floor ? floor : smem;
     out[n++] = p;
   }
+  if (bwd && n >= 2 && out[0].KS == 16 && out[1].KS == 8 && !(mode == 1 && Npad > 64)) {
+    const TcPlan t = out[0];
+    out[0] = out[1];
+    out[1] = t;
+  }
   return n;
 }
 
@@ -105,9 +117,9 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPla
 }
 
 // First candidate plan whose clusters can all be resident at once.
-bool choose_plan(int bwd, int H, int B, int ndir, int num_sms, int ext, TcPlan* chosen) {
+bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext, TcPlan* chosen) {
   TcPlan plans[5];
-  const int n = make_plans(bwd, H, B, ndir, num_sms, plans, 5);
+  const int n = make_plans(mode, bwd, H, B, ndir, num_sms, plans, 5);
   for (int i = 0; i < n; ++i) {
     const TcPlan& pl = plans[i];
     const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
@@ -140,7 +152,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   TcPlan pl;
   // the extended kernel variant takes sequence lengths and cell clipping
   const int ext = (a.len != nullptr || a.clip) ? 1 : 0;
-  if (!choose_plan(bwd, a.H, a.B, a.ndir, num_sms, ext, &pl)) return 2;
+  if (!choose_plan(a.mode, bwd, a.H, a.B, a.ndir, num_sms, ext, &pl)) return 2;
   const int H = a.H, D = a.D;
   CUtensorMap tmW, tmX, tmX4;
   int rc;
@@ -195,7 +207,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
 bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms) {
   if (!(mode == 0 || (mode == 1 && reset_after))) return false;
   TcPlan f, b;
-  return choose_plan(0, H, B, ndir, num_sms, 0, &f) && choose_plan(1, H, B, ndir, num_sms, 0, &b);
+  return choose_plan(mode, 0, H, B, ndir, num_sms, 0, &f) && choose_plan(mode, 1, H, B, ndir, num_sms, 0, &b);
 }
 
 int launch_persist_fwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms) { return launch(a, 0, s, num_sms); }
