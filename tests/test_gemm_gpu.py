@@ -85,6 +85,17 @@ def test_gemm_epilogue_beta_rowmap(use_tc):
     _case(512, 200, 1000, 0, 0, use_tc, beta=True, rowmap=[2, 0, -1, 1])
 
 
+@pytest.mark.parametrize("use_tc", [1, 0])
+def test_gemm_epilogue_bf16_beta_bias_rowmap_ragged(use_tc):
+    # bf16 output with accumulate, bias and the row remap; N = 8 full 32-column chunks + 8
+    _case(384, 264, 200, 1, 1, use_tc, bias=True, beta=True, c_bf16=True, rowmap=[3, -1, 0, 1], seed=14)
+
+
+@pytest.mark.parametrize("use_tc", [1, 0])
+def test_gemm_epilogue_f32_bias(use_tc):
+    _case(200, 96, 64, 1, 0, use_tc, bias=True, seed=15)
+
+
 def test_gemm_split_k_rowmap_beta_bias():
     # long K, few tiles: K is split across CTAs; the partials are summed in split order
     _case(512, 512, 8192, 0, 0, 1, bias=True, beta=True, rowmap=[1, -1, 0, 2], seed=11)
