@@ -485,22 +485,37 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
     layer_x = at<char>(workspace, h->w_xin);
   }
   void* Ybuf = nullptr;
+  const bool y_direct = h->algo == RNN_ALGO_PERSIST_TC && !h->bfirst;
   for (int l = 0; l < L; ++l) {
     const int Il = layer_in(h, l);
     char* wb = static_cast<char*>(const_cast<void*>(w));
+    // layer output buffer (h0 goes into its boundary slots)
+    Ybuf = train ? at<char>(reserve, h->r_y[l]) : at<char>(workspace, (l & 1) ? h->w_y1 : h->w_y0);
+    // one launch: packed W_ih, W_hh, biases of both directions, h0 into Ybuf
+    PackBatch pb;
     for (int d = 0; d < D; ++d) {
       const int i = l * D + d;
-      RNN_TRY(count(h, launch_pack_rows(wb + h->off_ih[i] * es, h->G, H, Il, sf, h->bf16,
-                                        at<char>(workspace, h->w_wx) + static_cast<size_t>(d) * 4 * H * Il * es, Il, 0,
-                                        s)));
-      RNN_TRY(count(h, launch_pack_rows(wb + h->off_hh[i] * es, h->G, H, H, sf, h->bf16,
-                                        at<char>(workspace, h->w_wr) + static_cast<size_t>(d) * 4 * H * H * es, H, 0, s)));
-      RNN_TRY(count(h, launch_pack_bias(wb + h->off_b[i] * es, H, sf, h->bf16,
-                                        at<float>(workspace, h->w_bx) + static_cast<size_t>(d) * 4 * H, s)));
-      if (h->ra)
-        RNN_TRY(count(h, launch_pack_bias(wb + h->off_bh[i] * es, H, sf, h->bf16,
-                                          at<float>(workspace, h->w_bh) + static_cast<size_t>(d) * 4 * H, s)));
+      PackJob j;
+      for (int k = 0; k < 4; ++k) j.map[k] = sf[k];
+      j.H = H;
+      j.kind = PACK_ROWS; j.K = Il; j.in = wb + h->off_ih[i] * es; j.ld_out = Il;
+      j.out = at<char>(workspace, h->w_wx) + static_cast<size_t>(d) * 4 * H * Il * es;
+      pb.add(j);
+      j.K = H; j.in = wb + h->off_hh[i] * es; j.ld_out = H;
+      j.out = at<char>(workspace, h->w_wr) + static_cast<size_t>(d) * 4 * H * H * es;
+      pb.add(j);
+      j.kind = PACK_BIAS; j.in = wb + h->off_b[i] * es; j.out = at<float>(workspace, h->w_bx) + static_cast<size_t>(d) * 4 * H;
+      pb.add(j);
+      if (h->ra) {
+        j.in = wb + h->off_bh[i] * es; j.out = at<float>(workspace, h->w_bh) + static_cast<size_t>(d) * 4 * H;
+        pb.add(j);
+      }
+      PackJob y;
+      y.kind = H0_TO_Y; y.H = H; y.T = T; y.B = B; y.D = D; y.dir = d; y.out = Ybuf;
+      y.in = hx ? static_cast<const char*>(hx) + (static_cast<size_t>(l) * D + d) * B * H * es : nullptr;
+      pb.add(y);
     }
+    RNN_TRY(count(h, launch_pack_batch(pb, h->bf16, s)));
     // hoisted input projection for every timestep and direction
     GemmArgs g;
     g.M = static_cast<int>(TB); g.N = D * 4 * H; g.K = Il;
@@ -509,12 +524,6 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
     g.C = at<char>(workspace, h->w_p); g.ldc = D * 4 * H; g.c_bf16 = h->bf16;
     g.bias = at<float>(workspace, h->w_bx);
     RNN_TRY(run_gemm(h, g, s, 2));
-    // layer output buffer with h0 in its boundary slots
-    Ybuf = train ? at<char>(reserve, h->r_y[l]) : at<char>(workspace, (l & 1) ? h->w_y1 : h->w_y0);
-    for (int d = 0; d < D; ++d) {
-      const void* h0 = hx ? static_cast<const char*>(hx) + (static_cast<size_t>(l) * D + d) * B * H * es : nullptr;
-      RNN_TRY(count(h, launch_states_to_y(h0, Ybuf, T, B, H, D, d, h->bf16, s)));
-    }
     PersistArgs a;
     a.mode = h->desc.mode; a.reset_after = h->ra; a.is_bf16 = h->bf16;
     a.T = T; a.B = B; a.H = H; a.D = D;
@@ -530,12 +539,15 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
     a.cy = (h->lstm && cy) ? static_cast<char*>(cy) + static_cast<size_t>(l) * D * B * H * es : nullptr;
     a.len = h->has_len ? h->d_len : nullptr;
     a.clip = h->clip; a.clip_lo = h->clip_lo; a.clip_hi = h->clip_hi;
+    // the tensor-core kernels write the caller's seq-major y themselves
+    if (l == L - 1 && y_direct) a.y_out = y;
     RNN_TRY(run_persist(h, a, false, s));
     layer_x = static_cast<char*>(Ybuf) + static_cast<size_t>(B) * D * H * es;   // slot 1
   }
   // y out (rows of slots 1..T)
-  RNN_TRY(count(h, launch_seq_transpose(layer_x, y, T, B, D * H, h->bf16, h->bf16, 0, h->bfirst, D * H, s,
-                                        h->has_len ? h->d_len : nullptr)));
+  if (!y_direct)
+    RNN_TRY(count(h, launch_seq_transpose(layer_x, y, T, B, D * H, h->bf16, h->bf16, 0, h->bfirst, D * H, s,
+                                          h->has_len ? h->d_len : nullptr)));
   return cudaGetLastError() == cudaSuccess ? RNN_OK : RNN_CUDA_ERROR;
 }
 
@@ -561,15 +573,22 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
   char* wb = static_cast<char*>(const_cast<void*>(w));
   for (int l = L - 1; l >= 0; --l) {
     const int Il = layer_in(h, l);
+    // one launch: W_hh^T and W_ih^T of both directions
+    PackBatch pb;
     for (int d = 0; d < D; ++d) {
       const int i = l * D + d;
-      RNN_TRY(count(h, launch_pack_rows(wb + h->off_hh[i] * es, h->G, H, H, sr, h->bf16,
-                                        at<char>(workspace, h->w_wrt) + static_cast<size_t>(d) * H * 4 * H * es, 4 * H,
-                                        1, s)));
-      RNN_TRY(count(h, launch_pack_rows(wb + h->off_ih[i] * es, h->G, H, Il, sx, h->bf16,
-                                        at<char>(workspace, h->w_wxt) + static_cast<size_t>(d) * 4 * H * es,
-                                        static_cast<int64_t>(D) * 4 * H, 1, s)));
+      PackJob j;
+      j.kind = PACK_ROWS_T; j.H = H;
+      for (int k = 0; k < 4; ++k) j.map[k] = sr[k];
+      j.K = H; j.in = wb + h->off_hh[i] * es; j.ld_out = 4 * H;
+      j.out = at<char>(workspace, h->w_wrt) + static_cast<size_t>(d) * H * 4 * H * es;
+      pb.add(j);
+      for (int k = 0; k < 4; ++k) j.map[k] = sx[k];
+      j.K = Il; j.in = wb + h->off_ih[i] * es; j.ld_out = static_cast<int64_t>(D) * 4 * H;
+      j.out = at<char>(workspace, h->w_wxt) + static_cast<size_t>(d) * 4 * H * es;
+      pb.add(j);
     }
+    RNN_TRY(count(h, launch_pack_batch(pb, h->bf16, s)));
     PersistArgs a;
     a.mode = h->desc.mode; a.reset_after = h->ra; a.is_bf16 = h->bf16;
     a.T = T; a.B = B; a.H = H; a.D = D;
@@ -657,6 +676,7 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
       m_hh[0] = pos[0]; m_hh[1] = pos[1]; m_hh[2] = -1; m_hh[3] = -1;
     }
   }
+  PackBatch scatter;
   for (int l = 0; l < L; ++l) {
     const int Il = layer_in(h, l);
     const void* Xl = l == 0 ? x0 : rs + h->r_y[l - 1] + static_cast<size_t>(B) * D * H * es;
@@ -698,11 +718,29 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
           RNN_TRY(run_gemm(h, g, s, 4));
         }
       }
-      const float* db = reinterpret_cast<const float*>(rs + h->r_db[l]) + static_cast<size_t>(d) * 4 * H;
-      RNN_TRY(count(h, launch_bias_grad_scatter(db, H, m_b, 0, dwf + h->off_b[i], s)));
-      if (h->ra) RNN_TRY(count(h, launch_bias_grad_scatter(db, H, m_bh, 1, dwf + h->off_bh[i], s)));
+      // bias gradients back to the caller's gate blocks (batched below)
+      PackJob j;
+      j.kind = SCATTER_DB; j.H = H;
+      j.in = reinterpret_cast<const float*>(rs + h->r_db[l]) + static_cast<size_t>(d) * 4 * H;
+      for (int k = 0; k < 4; ++k) j.map[k] = m_b[k];
+      j.out = dwf + h->off_b[i];
+      if (!scatter.add(j)) {
+        RNN_TRY(count(h, launch_pack_batch(scatter, 0, s)));
+        scatter.n = 0;
+        scatter.add(j);
+      }
+      if (h->ra) {
+        for (int k = 0; k < 4; ++k) j.map[k] = m_bh[k];
+        j.out = dwf + h->off_bh[i];
+        if (!scatter.add(j)) {
+          RNN_TRY(count(h, launch_pack_batch(scatter, 0, s)));
+          scatter.n = 0;
+          scatter.add(j);
+        }
+      }
     }
   }
+  RNN_TRY(count(h, launch_pack_batch(scatter, 0, s)));
   return cudaGetLastError() == cudaSuccess ? RNN_OK : RNN_CUDA_ERROR;
 }
 

@@ -71,6 +71,91 @@ __global__ void bias_grad_scatter_kernel(const float* __restrict__ db, int H, in
   if (d >= 0) out[static_cast<int64_t>(d) * H + u] = db[i];
 }
 
+// Several layout jobs in one launch: job j takes blocks [start[j], start[j+1])
+// and walks its elements with a stride of its block count.  The bodies are the
+// ones of the single-job kernels above (same index maps).
+struct PackBatchArgs {
+  int n;
+  int start[kMaxPackJobs + 1];
+  PackJob job[kMaxPackJobs];
+};
+
+template <typename T>
+__device__ __forceinline__ void pack_job_rows(const PackJob& J, int blk, int nblk) {
+  const T* W = static_cast<const T*>(J.in);
+  T* out = static_cast<T*>(J.out);
+  const int64_t total = static_cast<int64_t>(4) * J.H * J.K;
+  for (int64_t i = static_cast<int64_t>(blk) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(nblk) * blockDim.x) {
+    const int row = static_cast<int>(i / J.K), k = static_cast<int>(i - static_cast<int64_t>(row) * J.K);
+    const int u = row >> 2, sb = J.map[row & 3];
+    out[static_cast<int64_t>(row) * J.ld_out + k] =
+        sb >= 0 ? W[(static_cast<int64_t>(sb) * J.H + u) * J.K + k] : from_f<T>(0.0f);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void pack_job_rows_t(const PackJob& J, int blk, int nblk, float (*tile)[33]) {
+  const T* W = static_cast<const T*>(J.in);
+  T* out = static_cast<T*>(J.out);
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
+  const int tk = (J.K + 31) / 32, tr = (4 * J.H + 31) / 32;
+  for (int tile_i = blk; tile_i < tk * tr; tile_i += nblk) {
+    const int k0 = (tile_i % tk) * 32, r0 = (tile_i / tk) * 32;
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+      const int row = r0 + i, k = k0 + tx;
+      float v = 0.f;
+      if (row < 4 * J.H && k < J.K) {
+        const int sb = J.map[row & 3];
+        if (sb >= 0) v = to_f<T>(W[(static_cast<int64_t>(sb) * J.H + (row >> 2)) * J.K + k]);
+      }
+      tile[i][tx] = v;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+      const int k = k0 + i, row = r0 + tx;
+      if (k < J.K && row < 4 * J.H) out[static_cast<int64_t>(k) * J.ld_out + row] = from_f<T>(tile[tx][i]);
+    }
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) pack_batch_kernel(PackBatchArgs P) {
+  __shared__ float tile[32][33];
+  int j = 0;
+  while (j < P.n - 1 && static_cast<int>(blockIdx.x) >= P.start[j + 1]) ++j;
+  const PackJob& J = P.job[j];
+  const int blk = blockIdx.x - P.start[j], nblk = P.start[j + 1] - P.start[j];
+  const int tid = blk * blockDim.x + threadIdx.x, nthr = nblk * blockDim.x;
+  switch (J.kind) {
+    case PACK_ROWS: pack_job_rows<T>(J, blk, nblk); break;
+    case PACK_ROWS_T: pack_job_rows_t<T>(J, blk, nblk, tile); break;
+    case PACK_BIAS:
+      for (int i = tid; i < 4 * J.H; i += nthr) {
+        const int sb = J.map[i & 3];
+        static_cast<float*>(J.out)[i] =
+            (sb >= 0 && J.in) ? to_f<T>(static_cast<const T*>(J.in)[static_cast<int64_t>(sb) * J.H + (i >> 2)]) : 0.f;
+      }
+      break;
+    case SCATTER_DB:
+      for (int i = tid; i < 4 * J.H; i += nthr) {
+        const int d = J.map[i & 3];
+        if (d >= 0) static_cast<float*>(J.out)[static_cast<int64_t>(d) * J.H + (i >> 2)] =
+            static_cast<const float*>(J.in)[i];
+      }
+      break;
+    default: {   // H0_TO_Y
+      const int slot = J.dir == 0 ? 0 : J.T + 1;
+      for (int i = tid; i < J.B * J.H; i += nthr) {
+        const int b = i / J.H, u = i - b * J.H;
+        static_cast<T*>(J.out)[(static_cast<int64_t>(slot) * J.B + b) * J.D * J.H + J.dir * J.H + u] =
+            J.in ? static_cast<const T*>(J.in)[i] : from_f<T>(0.0f);
+      }
+    }
+  }
+}
+
 // One output row (t, b) per blockIdx.x, features along threads.
 // Rows (t, b) with t >= len[b] (len non-null) are written as zeros.
 template <typename Ti, typename To, int V>
@@ -246,6 +331,30 @@ int launch_recompute_cells(const void* gates, const void* c0, float* C, int T, i
     recompute_cells_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(gates),
                                                        static_cast<const float*>(c0), C, T, B, H, D, len, clip, lo,
                                                        hi);
+  return check_launch();
+}
+
+int launch_pack_batch(const PackBatch& pb, int is_bf16, cudaStream_t s) {
+  if (pb.n <= 0) return 0;
+  if (pb.n > kMaxPackJobs) return 2;
+  PackBatchArgs P;
+  P.n = pb.n;
+  P.start[0] = 0;
+  for (int j = 0; j < pb.n; ++j) {
+    const PackJob& J = pb.job[j];
+    P.job[j] = J;
+    int64_t work;
+    switch (J.kind) {
+      case PACK_ROWS: work = (static_cast<int64_t>(4) * J.H * J.K + 1023) / 1024; break;
+      case PACK_ROWS_T: work = static_cast<int64_t>((J.K + 31) / 32) * ((4 * J.H + 31) / 32); break;
+      case H0_TO_Y: work = (static_cast<int64_t>(J.B) * J.H + 255) / 256; break;
+      default: work = (4 * J.H + 255) / 256;
+    }
+    const int nb = static_cast<int>(work < 1 ? 1 : work > 512 ? 512 : work);
+    P.start[j + 1] = P.start[j] + nb;
+  }
+  if (is_bf16) pack_batch_kernel<__nv_bfloat16><<<P.start[pb.n], 256, 0, s>>>(P);
+  else pack_batch_kernel<float><<<P.start[pb.n], 256, 0, s>>>(P);
   return check_launch();
 }
 

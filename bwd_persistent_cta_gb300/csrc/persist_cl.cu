@@ -325,7 +325,7 @@ int launch_persist_fwd_cl(const PersistArgs& a, cudaStream_t s, int num_sms) {
   // the cell for 4x the pairs, which outweighs the cheaper exchange
   const char* e = std::getenv("RNN_CLUSTER_FWD");
   if (!e || e[0] != '1') return 2;
-  if (!a.is_bf16 || !(a.mode == 0 || (a.mode == 1 && a.reset_after)) || a.len || a.clip) return 2;
+  if (!a.is_bf16 || !(a.mode == 0 || (a.mode == 1 && a.reset_after)) || a.len || a.clip || a.y_out) return 2;
   const int H = a.H, B = a.B;
   if (H % 128 != 0 || 4 * H / 128 > kMaxChunks || B < 1 || B > 64) return 2;
   const int nm = 4 * H / 128;

@@ -30,6 +30,11 @@
 // gruCellForwardPassCalcUnitsResetAfter, backwardStepImpl and
 // backwardStepImplResetAfter; the LSTM and GRU branches of the persistent
 // backward-data kernel fragment.
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "common.cuh"
 
 namespace rnn {
@@ -1049,9 +1054,40 @@ const void* latency_fwd_fn(const PersistArgs& a) {
   }
 }
 
+// Host-side plan cache: the occupancy queries behind a launch cost host time
+// that the GPU would wait for at every persistent launch.  Dynamic shared
+// memory limits only ever rise, so a cached plan never meets a lower limit set
+// for another shape.
+struct SimtKey {
+  int v[11];
+  bool operator<(const SimtKey& o) const { return std::lexicographical_compare(v, v + 11, o.v, o.v + 11); }
+};
+struct SimtEntry {
+  int rc = 0;
+  SimtPlan pl;
+  int lat = 0;          // latency-mode forward chosen
+  int lat_NU = 0, lat_Rs = 0, lat_nblk = 0;
+  size_t lat_smem = 0;
+};
+std::mutex g_simt_mu;
+std::map<SimtKey, SimtEntry> g_simt;
+std::map<std::pair<const void*, int>, int> g_simt_smem;
+
+bool raise_smem(const void* fn, int dev, size_t bytes) {
+  int& cur = g_simt_smem[{fn, dev}];
+  if (static_cast<int>(bytes) <= cur) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cur = static_cast<int>(bytes);
+  return true;
+}
+
 // Latency-mode forward (large weights, batch <= 8): one pair per thread, as
-// many weight rows resident in shared memory as fit.
-int launch_latency_fwd(const PersistArgs& a, cudaStream_t s, int num_sms) {
+// many weight rows resident in shared memory as fit.  Plans only (0, or 2 when
+// it does not apply); the caller launches.
+int plan_latency_fwd(const PersistArgs& a, int num_sms, int dev, SimtEntry* e) {
   const int max_ctas = num_sms / a.ndir;
   const int NU = (a.H + max_ctas - 1) / max_ctas;
   if (NU * a.B > kThreads || 4 * NU > 8 * kLatRows) return 2;
@@ -1066,33 +1102,60 @@ int launch_latency_fwd(const PersistArgs& a, cudaStream_t s, int num_sms) {
   if (Rs > 4 * NU) Rs = 4 * NU;
   const size_t smem = fixed + static_cast<size_t>(Rs) * row_bytes;
   const void* fn = latency_fwd_fn(a);
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-    return 3;
+  if (!raise_smem(fn, dev, smem)) return 3;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess) return 3;
   if (per_sm * num_sms < nblk * a.ndir) return 2;
-  PersistArgs args = a;
-  int nu = NU, rs = Rs;
-  void* params[] = {&args, &nu, &rs};
-  if (cudaLaunchKernel(fn, dim3(nblk, a.ndir), dim3(kThreads), params, smem, s) != cudaSuccess) return 3;
+  e->lat = 1;
+  e->lat_NU = NU; e->lat_Rs = Rs; e->lat_nblk = nblk; e->lat_smem = smem;
   return 0;
 }
 
-int launch_simt(const PersistArgs& a, bool bwd, cudaStream_t s, int num_sms) {
-  SimtPlan pl;
-  int rc = make_plan(a, bwd, num_sms, &pl);
-  if (rc) return rc;
-  const int span = 32 * (a.is_bf16 ? 8 : 4);
-  if (pl.stream && !bwd && a.B <= 8 && a.H % span == 0) {
-    rc = launch_latency_fwd(a, s, num_sms);
-    if (rc != 2) return rc;
+// The plan of one launch (cached per shape and device).
+SimtEntry simt_entry(const PersistArgs& a, bool bwd, int num_sms) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const SimtKey key{{bwd ? 1 : 0, a.mode, a.reset_after, a.is_bf16, a.H, a.B, a.ndir, a.dwhh ? 1 : 0, num_sms, dev,
+                     a.D}};
+  std::lock_guard<std::mutex> lock(g_simt_mu);
+  const auto hit = g_simt.find(key);
+  if (hit != g_simt.end()) return hit->second;
+  SimtEntry e;
+  e.rc = make_plan(a, bwd, num_sms, &e.pl);
+  if (e.rc == 0) {
+    const int span = 32 * (a.is_bf16 ? 8 : 4);
+    int lrc = 2;
+    if (e.pl.stream && !bwd && a.B <= 8 && a.H % span == 0) lrc = plan_latency_fwd(a, num_sms, dev, &e);
+    if (lrc == 3) {
+      e.rc = 3;
+    } else if (!e.lat) {
+      const void* fn = kernel_for(a, bwd, e.pl);
+      int per_sm = 0;
+      if (!raise_smem(fn, dev, e.pl.smem) ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, e.pl.smem) != cudaSuccess)
+        e.rc = 3;
+      else if (per_sm * num_sms < e.pl.nblk * a.ndir)
+        e.rc = 2;
+    }
   }
+  if (e.rc != 3) g_simt[key] = e;   // a CUDA error is not cached
+  return e;
+}
+
+int launch_simt(const PersistArgs& a, bool bwd, cudaStream_t s, int num_sms) {
+  const SimtEntry e = simt_entry(a, bwd, num_sms);
+  if (e.rc) return e.rc;
+  if (e.lat) {
+    PersistArgs args = a;
+    int nu = e.lat_NU, rs = e.lat_Rs;
+    void* params[] = {&args, &nu, &rs};
+    if (cudaLaunchKernel(latency_fwd_fn(a), dim3(e.lat_nblk, a.ndir), dim3(kThreads), params, e.lat_smem, s) !=
+        cudaSuccess)
+      return 3;
+    return 0;
+  }
+  const SimtPlan& pl = e.pl;
   const void* fn = kernel_for(a, bwd, pl);
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) != cudaSuccess)
-    return 3;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, pl.smem) != cudaSuccess) return 3;
-  if (per_sm * num_sms < pl.nblk * a.ndir) return 2;
   dim3 grid(pl.nblk, a.ndir);
   PersistArgs args = a;
   int NU = pl.NU, KC = pl.KC;

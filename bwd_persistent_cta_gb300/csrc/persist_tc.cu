@@ -1,6 +1,11 @@
 // persist_tc.cu - plans and launches of the persistent tensor-core kernels
 // (the kernels themselves: persist_tc_kernels.cuh; their instances:
 // persist_tc_fwd.cu, persist_tc_bwd.cu).
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "persist_tc_kernels.cuh"
 
 namespace rnn {
@@ -116,18 +121,47 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPla
   cfg.numAttrs = 1;
 }
 
+// Chosen plans per shape and device, and the dynamic shared-memory limit set
+// on each kernel (only ever raised, so that a cached plan never meets a lower
+// limit set for another shape).  The occupancy query behind a plan costs tens
+// of microseconds of host time, which the GPU would otherwise wait for at the
+// start of every persistent launch.
+struct PlanKey {
+  int v[8];
+  bool operator<(const PlanKey& o) const { return std::lexicographical_compare(v, v + 8, o.v, o.v + 8); }
+};
+std::mutex g_plan_mu;
+std::map<PlanKey, std::pair<bool, TcPlan>> g_plans;
+std::map<std::pair<const void*, int>, int> g_smem_limit;
+
+bool raise_smem_limit(const void* fn, int dev, int bytes) {
+  int& cur = g_smem_limit[{fn, dev}];
+  if (bytes <= cur) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cur = bytes;
+  return true;
+}
+
 // First candidate plan whose clusters can all be resident at once.
 bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext, TcPlan* chosen) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const PlanKey key{{mode, bwd, H, B, ndir, num_sms, ext, dev}};
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  const auto hit = g_plans.find(key);
+  if (hit != g_plans.end()) {
+    *chosen = hit->second.second;
+    return hit->second.first;
+  }
   TcPlan plans[5];
   const int n = make_plans(mode, bwd, H, B, ndir, num_sms, plans, 5);
   for (int i = 0; i < n; ++i) {
     const TcPlan& pl = plans[i];
     const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem)) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      continue;
-    }
+    if (!raise_smem_limit(fn, dev, static_cast<int>(pl.smem))) continue;
     if (pl.KS > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
       cudaGetLastError();
       continue;
@@ -142,9 +176,11 @@ bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext
     }
     if (max_clusters >= pl.nrg * ndir) {
       *chosen = pl;
+      g_plans[key] = {true, pl};
       return true;
     }
   }
+  g_plans[key] = {false, TcPlan()};
   return false;
 }
 
@@ -191,6 +227,8 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   P.off_ring = pl.off_ring; P.off_recv = pl.off_recv; P.off_bar = pl.off_bar;
   P.w_tmem = pl.w_tmem;
   P.single = single;
+  const uint64_t proj_bytes = static_cast<uint64_t>(a.T) * a.B * D * 4 * H * 2;
+  P.prefetch = !bwd && proj_bytes > (32ull << 20);
   P.wcol = 256;
   const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
   cudaLaunchConfig_t cfg;

@@ -88,6 +88,7 @@ struct TcPersistParams {
   int KS, Kc, nsub, R, Npad, UPC, RPC;
   int w_tmem;              // weight tile in tensor memory (A operand from TMEM) instead of shared memory
   int single;              // the whole K slice arrives with one 4-D TMA per step (R == nsub)
+  int prefetch;            // forward: request later steps' projections into L2 (kPrefetchSteps)
   uint32_t wcol;           // first TMEM column of the weight tile (w_tmem)
   unsigned int nblk_dir;   // CTAs per direction
   uint32_t tmem_cols;
@@ -102,6 +103,19 @@ struct TcBars {
   int flags[2][kMaxKS];          // abort flags pushed by the peers, by step parity
   uint32_t tmem;
 };
+
+// The forward requests the input projections of the step this many steps
+// ahead into L2 when they are too large to stay there after the projection
+// GEMM (more than a quarter of L2): the step's own loads would otherwise wait
+// on HBM inside the chain (GB300: LSTM T256 B32 H1024, 67 MB of projections,
+// forward 1.09 -> 1.06 ms; 2-layer bidirectional T512 B128 H1024 8.77 ->
+// 8.29 ms; GRU T128 B64 H512, 17 MB, still in L2: 0.57 -> 0.59 ms, so off).
+// The same prefetch of the backward's saved gates, states and dy measured
+// slower (17.4 -> 18.2 ms on the 2-layer LSTM) and is not done.
+constexpr int kPrefetchSteps = 4;
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 __device__ __forceinline__ float tanh_fast(float x) {
   float y;
@@ -523,7 +537,17 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     RNN_TRACE_AT(5, 0, s);
     step_arrive(a, skip, s, 0);
     RNN_TRACE_AT(6, 0, s);
-    // stores nothing in this launch waits for
+    // stores nothing in this launch waits for, and the prefetch of later projections
+    if (P.prefetch && s + kPrefetchSteps < TT) {
+      const int tf = dir ? TT - 1 - (s + kPrefetchSteps) : s + kPrefetchSteps;
+#pragma unroll
+      for (int p = 0; p < PP; ++p) {
+        const int id = threadIdx.x + p * kThreads;
+        if (id >= npairs) break;
+        const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+        prefetch_l2(Pm + (static_cast<int64_t>(tf) * B + b) * ldP + dir * 4 * H + 4 * u);
+      }
+    }
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
@@ -531,6 +555,14 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       const int ul = id % UPC, b = id / UPC, u = ubase + ul;
       if (G) Vec4<__nv_bfloat16>::store(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * 4 * H + 4 * u, gq[p]);
       if (lstm && a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = st[p];
+      if (a.y_out) {
+        float yv = hv[p];
+        if constexpr (EXT) {
+          if (t >= lenp[p]) yv = 0.f;
+        }
+        static_cast<__nv_bfloat16*>(a.y_out)[(static_cast<int64_t>(t) * B + b) * ldY + dir * H + u] =
+            __float2bfloat16_rn(yv);
+      }
       if (s == TT - 1) {
         const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
         if (a.hy) static_cast<__nv_bfloat16*>(a.hy)[o] = __float2bfloat16_rn(hv[p]);

@@ -89,6 +89,7 @@ struct PersistArgs {
   const void* c0 = nullptr;          // [D][B, H] slice of cx for this layer
   void* hy = nullptr;                // [D][B, H]
   void* cy = nullptr;
+  void* y_out = nullptr;             // tensor-core forward: also writes y_t to [T, B, D*H] (zero at masked steps)
   // backward
   const void* WrT = nullptr;
   const float* dYi = nullptr;        // [T, B, D*H]
@@ -151,6 +152,31 @@ int launch_pack_bias(const void* b, int H, const int* slot_src, int is_bf16, flo
 int launch_seq_transpose(const void* in, void* out, int T, int B, int F, int in_bf16,
                          int out_bf16, int in_batch_first, int out_batch_first,
                          int64_t out_ld, cudaStream_t s, const int* len = nullptr);
+// Several layout jobs in one launch (the forward's weight / bias packing and
+// h0 placement, the backward's transposed packing, the bias-gradient scatter).
+enum PackKind { PACK_ROWS = 0, PACK_ROWS_T = 1, PACK_BIAS = 2, SCATTER_DB = 3, H0_TO_Y = 4 };
+struct PackJob {
+  int kind = PACK_ROWS;
+  int H = 0, K = 0;
+  // PACK_*: internal slot -> caller gate block to read; SCATTER_DB: slot ->
+  // caller block to write; -1: zero / skipped
+  int map[4] = {-1, -1, -1, -1};
+  const void* in = nullptr;   // may be null for PACK_BIAS (zeros) and H0_TO_Y (zero state)
+  void* out = nullptr;
+  int64_t ld_out = 0;         // PACK_ROWS / PACK_ROWS_T row stride of out
+  int T = 0, B = 0, D = 1, dir = 0;   // H0_TO_Y
+};
+constexpr int kMaxPackJobs = 12;
+struct PackBatch {
+  int n = 0;
+  PackJob job[kMaxPackJobs];
+  bool add(const PackJob& j) {
+    if (n >= kMaxPackJobs) return false;
+    job[n++] = j;
+    return true;
+  }
+};
+int launch_pack_batch(const PackBatch& pb, int is_bf16, cudaStream_t s);
 int launch_states_to_y(const void* h0, void* Y, int T, int B, int H, int D, int dir,
                        int is_bf16, cudaStream_t s);
 int launch_bias_grad_scatter(const float* db, int H, const int* slot_dst, int is_second,
