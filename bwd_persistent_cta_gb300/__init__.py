@@ -56,6 +56,7 @@ _SIGS = {
     "rnn_interleaved_dw_active": (ctypes.c_int, [_P]),
     "rnn_launch_count": (ctypes.c_uint64, [_P]),
     "rnn_selected_algo": (ctypes.c_int, [_P]),
+    "rnn_selected_fwd_algo": (ctypes.c_int, [_P]),
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
     "rnn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "rnn_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
@@ -179,6 +180,10 @@ def rnn_selected_algo(handle) -> int:
     return int(lib().rnn_selected_algo(handle))
 
 
+def rnn_selected_fwd_algo(handle) -> int:
+    return int(lib().rnn_selected_fwd_algo(handle))
+
+
 RNN_TIMING_CLASSES = 6
 TIMING_CLASS_NAMES = ("persist_fwd", "persist_bwd", "gemm_proj", "gemm_dx", "gemm_dw", "layout")
 
@@ -262,6 +267,10 @@ class RNN:
     @property
     def algo(self) -> int:
         return rnn_selected_algo(self.handle)
+
+    @property
+    def fwd_algo(self) -> int:
+        return rnn_selected_fwd_algo(self.handle)
 
     @property
     def interleaved_dw(self) -> bool:

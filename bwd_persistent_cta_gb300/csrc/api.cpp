@@ -195,7 +195,7 @@ int run_persist(rnn_handle_s* h, PersistArgs a, bool bwd, cudaStream_t s) {
     int rc = reset_counters(h, s);
     if (rc) return rc;
     TimeScope ts(h, bwd ? 1 : 0, s);
-    if (h->algo == RNN_ALGO_PERSIST_TC) {
+    if (bwd ? h->algo == RNN_ALGO_PERSIST_TC : h->fwd_tc != 0) {
       // forward: the cluster-resident kernel when the layer fits one cluster
       rc = bwd ? 2 : launch_persist_fwd_cl(x, s, h->num_sms);
       if (rc == 2) rc = bwd ? launch_persist_bwd_tc(x, s, h->num_sms) : launch_persist_fwd_tc(x, s, h->num_sms);
@@ -299,6 +299,12 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
   if (desc->algo == RNN_ALGO_PERSIST_TC) h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : 0;
   else if (desc->algo == RNN_ALGO_PERSIST_SIMT) h->algo = simt_ok ? RNN_ALGO_PERSIST_SIMT : 0;
   else h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : (simt_ok ? RNN_ALGO_PERSIST_SIMT : 0);
+  // automatic choice: a tensor-core forward even where only the backward
+  // lacks a tensor-core plan (e.g. hidden 2048: the forward splits its weight
+  // tile between tensor and shared memory)
+  h->fwd_tc = h->algo == RNN_ALGO_PERSIST_TC ||
+              (desc->algo == RNN_ALGO_AUTO && h->algo == RNN_ALGO_PERSIST_SIMT && h->bf16 &&
+               persist_tc_fwd_supported(desc->mode, h->ra, h->H, h->B, 1, h->num_sms));
   update_dw_bptt(h);
   fill_layout(h);
   return h->algo == 0 ? RNN_NOT_SUPPORTED : RNN_OK;
@@ -440,6 +446,10 @@ uint64_t rnn_launch_count(rnn_handle_t h) { return h ? h->launches : 0; }
 
 int rnn_selected_algo(rnn_handle_t h) { return h ? h->algo : 0; }
 
+int rnn_selected_fwd_algo(rnn_handle_t h) {
+  return h ? (h->fwd_tc ? RNN_ALGO_PERSIST_TC : h->algo) : 0;
+}
+
 rnn_status_t rnn_debug_skip_arrival(rnn_handle_t h, int cta) {
   if (!h || cta < -1) return RNN_BAD_PARAM;
   h->skip_cta = cta;
@@ -485,7 +495,7 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
     layer_x = at<char>(workspace, h->w_xin);
   }
   void* Ybuf = nullptr;
-  const bool y_direct = h->algo == RNN_ALGO_PERSIST_TC && !h->bfirst;
+  const bool y_direct = h->fwd_tc && !h->bfirst;
   for (int l = 0; l < L; ++l) {
     const int Il = layer_in(h, l);
     char* wb = static_cast<char*>(const_cast<void*>(w));

@@ -16,6 +16,8 @@ struct rnn_handle_s {
   int lstm, ra, rb, plain, bf16, bfirst;   // plain: RNN_RNN_RELU / RNN_RNN_TANH (one gate)
   int pos[4];          // canonical gate c sits in the caller's block pos[c]
   int algo;            // RNN_ALGO_PERSIST_TC or RNN_ALGO_PERSIST_SIMT
+  int fwd_tc;          // the forward runs the tensor-core kernel (also when algo is SIMT: a
+                       // shape whose backward has no tensor-core plan)
   int device, num_sms;
   size_t es;
   DevArea* dev;

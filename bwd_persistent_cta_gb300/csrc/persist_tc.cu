@@ -2,6 +2,7 @@
 // (the kernels themselves: persist_tc_kernels.cuh; their instances:
 // persist_tc_fwd.cu, persist_tc_bwd.cu).
 #include <algorithm>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -68,30 +69,33 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
       smem = a1k(wbytes) + a1k(R * rb) + a1k(recv) + a1k(sizeof(TcBars)) + 1024;
       if (smem <= kSmemCap) break;
     }
-    bool w_tmem = false;
-    if (R < nsub && Kc % 128 == 0 && Kc / 2 <= 256 && Npad <= 256) {
-      // weight tile in TMEM columns [256, 256 + Kc/2) instead: the whole K
-      // slice of the exchange operand then fits in flight at once
-      const size_t sm2 = a1k(static_cast<size_t>(nsub) * rb) + a1k(recv) + a1k(sizeof(TcBars)) + 1024;
-      if (sm2 <= kSmemCap) {
-        w_tmem = true;
+    // else weight sub-tiles in TMEM columns [256, 512) (an even count, at most
+    // 8), the others in shared memory, and the whole K slice of the exchange
+    // operand in flight at once
+    int wt = 0;
+    if (R < nsub && Npad <= 256) {
+      const int t = (nsub < 8 ? nsub : 8) & ~1;
+      const size_t sm2 = a1k(static_cast<size_t>(nsub - t) * kWSub) + a1k(static_cast<size_t>(nsub) * rb) +
+                         a1k(recv) + a1k(sizeof(TcBars)) + 1024;
+      if (t >= 2 && sm2 <= kSmemCap) {
+        wt = t;
         R = nsub;
         smem = sm2;
       }
     }
-    if (!w_tmem && (R < 1 || (R < nsub && R < 2))) continue;
+    if (!wt && (R < 1 || (R < nsub && R < 2))) continue;
     TcPlan p;
     p.KS = KS; p.Kc = Kc; p.nsub = nsub; p.R = R; p.Npad = Npad; p.UPC = UPC; p.PP = PP; p.nrg = nrg;
-    p.w_tmem = w_tmem ? 1 : 0;
+    p.w_tmem = wt;
     uint32_t tc = 32;
     while (tc < static_cast<uint32_t>(Npad)) tc *= 2;
-    p.tmem_cols = w_tmem ? 512 : tc;
-    p.off_ring = w_tmem ? 0 : static_cast<uint32_t>(a1k(wbytes));
+    p.tmem_cols = wt ? 512 : tc;
+    p.off_ring = static_cast<uint32_t>(a1k(static_cast<size_t>(nsub - wt) * kWSub));
     p.off_recv = p.off_ring + static_cast<uint32_t>(a1k(R * rb));
     p.off_bar = p.off_recv + static_cast<uint32_t>(a1k(recv));
     // all 512 TMEM columns: the shared-memory request alone must keep a
     // second CTA off the SM
-    const size_t floor = w_tmem ? kOneCtaSmem : kMinSmem;
+    const size_t floor = wt ? kOneCtaSmem : kMinSmem;
     p.smem = smem < floor ? floor : smem;
     out[n++] = p;
   }
@@ -127,9 +131,14 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPla
 // of microseconds of host time, which the GPU would otherwise wait for at the
 // start of every persistent launch.
 struct PlanKey {
-  int v[8];
-  bool operator<(const PlanKey& o) const { return std::lexicographical_compare(v, v + 8, o.v, o.v + 8); }
+  int v[10];
+  bool operator<(const PlanKey& o) const { return std::lexicographical_compare(v, v + 10, o.v, o.v + 10); }
 };
+
+int env_cap(const char* name) {
+  const char* e = std::getenv(name);
+  return e ? std::atoi(e) : 0;
+}
 std::mutex g_plan_mu;
 std::map<PlanKey, std::pair<bool, TcPlan>> g_plans;
 std::map<std::pair<const void*, int>, int> g_smem_limit;
@@ -149,7 +158,8 @@ bool raise_smem_limit(const void* fn, int dev, int bytes) {
 bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext, TcPlan* chosen) {
   int dev = 0;
   cudaGetDevice(&dev);
-  const PlanKey key{{mode, bwd, H, B, ndir, num_sms, ext, dev}};
+  const PlanKey key{{mode, bwd, H, B, ndir, num_sms, ext, dev, env_cap("RNN_TC_MAX_KS_FWD"),
+                     env_cap("RNN_TC_MAX_KS_BWD")}};
   std::lock_guard<std::mutex> lock(g_plan_mu);
   const auto hit = g_plans.find(key);
   if (hit != g_plans.end()) {
@@ -246,6 +256,12 @@ bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int
   if (!(mode == 0 || (mode == 1 && reset_after))) return false;
   TcPlan f, b;
   return choose_plan(mode, 0, H, B, ndir, num_sms, 0, &f) && choose_plan(mode, 1, H, B, ndir, num_sms, 0, &b);
+}
+
+bool persist_tc_fwd_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms) {
+  if (!(mode == 0 || (mode == 1 && reset_after))) return false;
+  TcPlan f;
+  return choose_plan(mode, 0, H, B, ndir, num_sms, 0, &f);
 }
 
 int launch_persist_fwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms) { return launch(a, 0, s, num_sms); }

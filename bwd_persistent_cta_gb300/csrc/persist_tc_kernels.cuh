@@ -86,7 +86,8 @@ constexpr size_t kOneCtaSmem = 116 * 1024; // one CTA per SM (it holds all 512 T
 struct TcPersistParams {
   PersistArgs a;
   int KS, Kc, nsub, R, Npad, UPC, RPC;
-  int w_tmem;              // weight tile in tensor memory (A operand from TMEM) instead of shared memory
+  int w_tmem;              // 64-column weight sub-tiles held in tensor memory (the A operand from TMEM):
+                           // sub-tiles [0, w_tmem) there, [w_tmem, nsub) in shared memory
   int single;              // the whole K slice arrives with one 4-D TMA per step (R == nsub)
   int prefetch;            // forward: request later steps' projections into L2 (kPrefetchSteps)
   uint32_t wcol;           // first TMEM column of the weight tile (w_tmem)
@@ -138,13 +139,13 @@ __device__ __forceinline__ T* peer_ptr(T* p, int rank) {
 __device__ __forceinline__ void mma_subtile(const TcPersistParams& P, uint32_t tmem, uint64_t adesc0,
                                             uint64_t bdesc0, uint32_t rbytes, uint32_t idesc, int j, int slot) {
   const uint64_t bd = bdesc0 + static_cast<uint64_t>((slot * rbytes) >> 4);
-  if (P.w_tmem) {
+  if (j < P.w_tmem) {
     // K=16 bf16 = 8 TMEM columns
     const uint32_t at = tmem + P.wcol + static_cast<uint32_t>(j * (kSubK / 2));
 #pragma unroll
     for (int k = 0; k < kSubK / 16; ++k) mma_bf16_ts(tmem, at + 8 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
   } else {
-    const uint64_t ad = adesc0 + static_cast<uint64_t>((j * kWSub) >> 4);
+    const uint64_t ad = adesc0 + static_cast<uint64_t>(((j - P.w_tmem) * kWSub) >> 4);
 #pragma unroll
     for (int k = 0; k < kSubK / 16; ++k)   // +32 bytes per K=16 step inside the swizzle atom
       mma_bf16_ss(tmem, ad + 2 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
@@ -171,7 +172,7 @@ __device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, 
     mbar_arrive_expect_tx(&bars.full[0], static_cast<uint32_t>(nsub) * rbytes);
     tma_load_4d(ring, tmX4, &bars.full[0], 0, y0, c2, dir);
     RNN_TRACE_AT(1, tk, s);
-    if (first_use_w && !P.w_tmem && !mbar_wait(&bars.wbar, 0, to)) return false;
+    if (first_use_w && P.w_tmem < P.nsub && !mbar_wait(&bars.wbar, 0, to)) return false;
     if (!mbar_wait(&bars.full[0], g & 1, to)) return false;
     RNN_TRACE_AT(8, tk, s);
     RNN_TRACE_AT(14, tk, s);
@@ -190,7 +191,7 @@ __device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, 
     tma_load_2d(ring + slot * rbytes, tmX, &bars.full[slot], x0 + j * kSubK, y0);
   }
   RNN_TRACE_AT(1, tk, s);
-  if (first_use_w && !P.w_tmem && !mbar_wait(&bars.wbar, 0, to)) return false;
+  if (first_use_w && P.w_tmem < P.nsub && !mbar_wait(&bars.wbar, 0, to)) return false;
   for (int j = 0; j < nsub; ++j) {
     const uint32_t gg = g0 + j;
     const int slot = gg % R;
@@ -323,8 +324,9 @@ __device__ __forceinline__ void unpack4(uint2 q, float (&v)[4]) {
 
 // Barriers, TMEM, and the resident weight tile: 128 rows from row wy0, K
 // columns from column wx0 of the packed weight matrix w (leading dimension
-// ldw), either by TMA into shared memory or, with w_tmem, by every thread
-// through registers into TMEM columns [wcol, wcol + Kc/2) (lane = row).
+// ldw).  Its first w_tmem sub-tiles go by every thread through registers into
+// TMEM columns [wcol, wcol + 32 * w_tmem) (lane = row), the others by TMA into
+// shared memory.
 __device__ __forceinline__ void setup(const TcPersistParams& P, const CUtensorMap* tmW, const CUtensorMap* tmX,
                                       const CUtensorMap* tmX4, uint8_t* wsm, TcBars& bars, int wx0, int wy0,
                                       const __nv_bfloat16* w, int64_t ldw) {
@@ -335,10 +337,11 @@ __device__ __forceinline__ void setup(const TcPersistParams& P, const CUtensorMa
     fence_mbar_init();
     fence_proxy_async_smem();
     if (P.single) prefetch_tmap(tmX4); else prefetch_tmap(tmX);
-    if (!P.w_tmem) {
+    if (P.w_tmem < P.nsub) {
       prefetch_tmap(tmW);
-      mbar_arrive_expect_tx(&bars.wbar, static_cast<uint32_t>(P.nsub) * kWSub);
-      for (int j = 0; j < P.nsub; ++j) tma_load_2d(wsm + j * kWSub, tmW, &bars.wbar, wx0 + j * kSubK, wy0);
+      mbar_arrive_expect_tx(&bars.wbar, static_cast<uint32_t>(P.nsub - P.w_tmem) * kWSub);
+      for (int j = P.w_tmem; j < P.nsub; ++j)
+        tma_load_2d(wsm + (j - P.w_tmem) * kWSub, tmW, &bars.wbar, wx0 + j * kSubK, wy0);
     }
   }
   if ((threadIdx.x >> 5) == 0) {
@@ -351,8 +354,9 @@ __device__ __forceinline__ void setup(const TcPersistParams& P, const CUtensorMa
   if (P.w_tmem) {
     // warps w and w + 4 share lane quarter w % 4 and split the K columns
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, half = warp >> 2;
-    const int ncol = P.Kc / 4;   // 32-bit columns per half
-    const __nv_bfloat16* src = w + (static_cast<int64_t>(wy0) + q * 32 + lane) * ldw + wx0 + half * (P.Kc / 2);
+    const int kt = P.w_tmem * kSubK;   // K columns held in TMEM (w_tmem even)
+    const int ncol = kt / 4;           // 32-bit columns per half
+    const __nv_bfloat16* src = w + (static_cast<int64_t>(wy0) + q * 32 + lane) * ldw + wx0 + half * (kt / 2);
     const uint32_t trow = bars.tmem + (static_cast<uint32_t>(q * 32) << 16) + P.wcol + static_cast<uint32_t>(half * ncol);
     for (int c = 0; c < ncol; c += 32) {
       const uint4* p4 = reinterpret_cast<const uint4*>(src + 2 * c);

@@ -127,6 +127,8 @@ int launch_persist_fwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
 int launch_persist_bwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
 
 bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms);
+// The forward kernel alone (a layer whose backward has no tensor-core plan).
+bool persist_tc_fwd_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms);
 // Cluster-resident forward (persist_cl.cu): returns 2 when the shape or the
 // options do not fit it (the caller then uses the tcgen05 persistent kernel).
 int launch_persist_fwd_cl(const PersistArgs& a, cudaStream_t s, int num_sms);

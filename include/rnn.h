@@ -239,6 +239,14 @@ uint64_t rnn_launch_count(rnn_handle_t handle);
  * 2 = SIMT persistent (rnn_algo_t values). */
 int rnn_selected_algo(rnn_handle_t handle);
 
+/* Which recurrent kernel the forward runs (rnn_algo_t values).  Equal to
+ * rnn_selected_algo except where the automatic choice runs the forward on the
+ * tensor-core kernel and the backward on the SIMT kernel: a bf16 LSTM or GRU
+ * resetAfter layer whose backward has no tensor-core plan (e.g. hidden 2048,
+ * where the forward keeps part of its weight tile in tensor memory and the
+ * rest in shared memory). */
+int rnn_selected_fwd_algo(rnn_handle_t handle);
+
 /* Test hook for the timeout path: CTA ``cta`` (>= 0) of the next persistent
  * launches skips its per-step arrival, so its peers' bounded waits run out and
  * the call ends with RNN_TIMEOUT instead of hanging.  -1 (default) = off. */

@@ -91,6 +91,7 @@ def run_gpu(inp: "synth.Inputs", algo: int = 0, backward: bool = True, repeat: i
                 out["dcx"] = to_np(dcx)
             out["dparams"] = synth.unflatten_params(wl, dw.cpu().numpy())
         out["algo"] = rnn.algo
+        out["fwd_algo"] = rnn.fwd_algo
         out["launches"] = rnn.launches()
         out["interleaved_dw"] = rnn.interleaved_dw
         out["reserve_bytes"] = rnn.reserve_bytes
