@@ -217,6 +217,9 @@ int run_persist(rnn_handle_s* h, PersistArgs a, bool bwd, cudaStream_t s) {
   return 0;
 }
 
+// GRU reset-before forward on the tensor-core kernel from this batch on.
+constexpr int kRbTcMinBatch = 4;
+
 rnn_status_t check_desc(const rnn_desc_t* d) {
   if (!d) return RNN_BAD_PARAM;
   if (d->mode != RNN_LSTM && d->mode != RNN_GRU && d->mode != RNN_RNN_RELU && d->mode != RNN_RNN_TANH)
@@ -301,9 +304,11 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
   else h->algo = tc_ok ? RNN_ALGO_PERSIST_TC : (simt_ok ? RNN_ALGO_PERSIST_SIMT : 0);
   // automatic choice: a tensor-core forward even where only the backward
   // lacks a tensor-core plan (e.g. hidden 2048: the forward splits its weight
-  // tile between tensor and shared memory)
+  // tile between tensor and shared memory; GRU reset-before, whose forward
+  // exchanges twice per step, from batch kRbTcMinBatch on)
   h->fwd_tc = h->algo == RNN_ALGO_PERSIST_TC ||
               (desc->algo == RNN_ALGO_AUTO && h->algo == RNN_ALGO_PERSIST_SIMT && h->bf16 &&
+               (!h->rb || h->B >= kRbTcMinBatch) &&
                persist_tc_fwd_supported(desc->mode, h->ra, h->H, h->B, 1, h->num_sms));
   update_dw_bptt(h);
   fill_layout(h);

@@ -196,8 +196,11 @@ bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext
 
 int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   TcPlan pl;
-  // the extended kernel variant takes sequence lengths and cell clipping
-  const int ext = (a.len != nullptr || a.clip) ? 1 : 0;
+  // the extended kernel variant takes sequence lengths, cell clipping and the
+  // GRU reset-before forward
+  const bool rb = a.mode == 1 && !a.reset_after;
+  if (rb && (bwd || !a.RH)) return 2;
+  const int ext = (a.len != nullptr || a.clip || rb) ? 1 : 0;
   if (!choose_plan(a.mode, bwd, a.H, a.B, a.ndir, num_sms, ext, &pl)) return 2;
   const int H = a.H, D = a.D;
   CUtensorMap tmW, tmX, tmX4;
@@ -228,6 +231,20 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
     if (make_tmap_bf16_4d(&tmX4, bwd ? a.dG : a.Y, dims, strides, box) != 0) single = 0;
   }
   if (!single) tmX4 = tmX;
+  // reset-before: views of RH [D][T*B][H] for the second exchange of a step
+  // (whole K slice per TMA only)
+  CUtensorMap tmR = tmX, tmR4 = tmX4;
+  if (rb) {
+    if (!single) return 2;
+    const uint64_t TB = static_cast<uint64_t>(a.T) * a.B;
+    if (make_tmap_bf16_2d(&tmR, a.RH, H, D * TB, H, kSubK, pl.Npad) != 0) return 2;
+    const uint64_t dims[4] = {static_cast<uint64_t>(kSubK), TB, static_cast<uint64_t>(H) / kSubK,
+                              static_cast<uint64_t>(D)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(H) * 2, static_cast<uint64_t>(kSubK) * 2, TB * H * 2};
+    const uint32_t box[4] = {static_cast<uint32_t>(kSubK), static_cast<uint32_t>(pl.Npad),
+                             static_cast<uint32_t>(pl.nsub), 1u};
+    if (make_tmap_bf16_4d(&tmR4, a.RH, dims, strides, box) != 0) return 2;
+  }
   TcPersistParams P;
   P.a = a;
   P.KS = pl.KS; P.Kc = pl.Kc; P.nsub = pl.nsub; P.R = pl.R; P.Npad = pl.Npad; P.UPC = pl.UPC;
@@ -244,8 +261,9 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   fill_config(cfg, attr, pl, a.ndir, s);
-  void* params[] = {&tmW, &tmX, &tmX4, &P};
-  if (cudaLaunchKernelExC(&cfg, fn, params) != cudaSuccess) return 3;
+  void* params_fwd[] = {&tmW, &tmX, &tmX4, &tmR, &tmR4, &P};
+  void* params_bwd[] = {&tmW, &tmX, &tmX4, &P};
+  if (cudaLaunchKernelExC(&cfg, fn, bwd ? params_bwd : params_fwd) != cudaSuccess) return 3;
   return 0;
 }
 
@@ -259,9 +277,12 @@ bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int
 }
 
 bool persist_tc_fwd_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms) {
-  if (!(mode == 0 || (mode == 1 && reset_after))) return false;
+  if (mode != 0 && mode != 1) return false;
+  const bool rb = mode == 1 && !reset_after;
   TcPlan f;
-  return choose_plan(mode, 0, H, B, ndir, num_sms, 0, &f);
+  if (!choose_plan(mode, 0, H, B, ndir, num_sms, rb ? 1 : 0, &f)) return false;
+  // reset-before exchanges r * h_{t-1} as one whole K slice per step
+  return !rb || f.R >= f.nsub;
 }
 
 int launch_persist_fwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms) { return launch(a, 0, s, num_sms); }

@@ -156,10 +156,10 @@ __device__ __forceinline__ void mma_subtile(const TcPersistParams& P, uint32_t t
 // memory and accumulate into TMEM.  Called by thread 0 only.  Either one 4-D
 // TMA brings the whole slice (chunk j at ring + j * rbytes), or nsub 2-D loads
 // stream through a ring of R slots.  g: running load counter (across steps).
-// (x0, y0): 2-D coordinates of the slice; (c2, dir): its chunk and direction
-// coordinates in the 4-D view.  Returns false on timeout.
+// (x0, y0): 2-D coordinates of the slice; (y4, c2, dir): its row, chunk and
+// direction coordinates in the 4-D view.  Returns false on timeout.
 __device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, const CUtensorMap* tmX4,
-                              uint8_t* ring, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0, int c2,
+                              uint8_t* ring, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0, int y4, int c2,
                               int dir, uint32_t idesc, uint64_t adesc0, bool first_use_w, int tk, int s) {
   (void)tk; (void)s;
   const int nsub = P.nsub, R = P.R;
@@ -170,7 +170,7 @@ __device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, 
     // the previous step's MMAs on the ring finished before this CTA released
     // that step, and every CTA's did before the counter let this load start
     mbar_arrive_expect_tx(&bars.full[0], static_cast<uint32_t>(nsub) * rbytes);
-    tma_load_4d(ring, tmX4, &bars.full[0], 0, y0, c2, dir);
+    tma_load_4d(ring, tmX4, &bars.full[0], 0, y4, c2, dir);
     RNN_TRACE_AT(1, tk, s);
     if (first_use_w && P.w_tmem < P.nsub && !mbar_wait(&bars.wbar, 0, to)) return false;
     if (!mbar_wait(&bars.full[0], g & 1, to)) return false;
@@ -237,7 +237,7 @@ __device__ __forceinline__ void push_partials(const TcPersistParams& P, uint32_t
 // the whole cluster may continue.
 __device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, const CUtensorMap* tmX4,
                               uint8_t* ring, float* recv, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0,
-                              int c2, int dir, uint32_t idesc,
+                              int y4, int c2, int dir, uint32_t idesc,
                               uint64_t adesc0, bool do_contract, unsigned int wait_target, int s, int ks, int& n_mma,
                               bool& w_waited, unsigned int kernel) {
   const PersistArgs& a = P.a;
@@ -251,7 +251,7 @@ __device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, 
     }
     RNN_TRACE_AT(7, tk, s);
     if (ok && do_contract) {
-      if (!contract_step(P, tmX, tmX4, ring, bars, tmem, g, x0, y0, c2, dir, idesc, adesc0, !w_waited, tk, s)) {
+      if (!contract_step(P, tmX, tmX4, ring, bars, tmem, g, x0, y0, y4, c2, dir, idesc, adesc0, !w_waited, tk, s)) {
         ok = 0;
         report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_TMA);
       }
@@ -396,7 +396,8 @@ __device__ __forceinline__ void teardown(const TcPersistParams& P, TcBars& bars)
 template <int PP, int KS, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                      const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ TcPersistParams P) {
+                      const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ CUtensorMap tmR,
+                      const __grid_constant__ CUtensorMap tmR4, const __grid_constant__ TcPersistParams P) {
   RNN_TC_SMEM_VIEW;
   const PersistArgs& a = P.a;
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
@@ -404,6 +405,10 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int ks = static_cast<int>(blockIdx.x) % KS;
   const int rg = static_cast<int>(blockIdx.x) / KS;
   const bool lstm = a.mode == 0;
+  // GRU reset-before (extended variant only): two exchanges per step, the
+  // second over r * h_{t-1} (tmR / tmR4: a view of RH [D][T*B][H])
+  const bool rbm = EXT && a.mode == 1 && !a.reset_after;
+  __nv_bfloat16* RHp = static_cast<__nv_bfloat16*>(a.RH);
   constexpr int RPC = 128 / KS;
   const bool clip = EXT && a.clip;
   const float clo = a.clip_lo, chi = a.clip_hi;
@@ -446,8 +451,10 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       if (a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? TT : 0)) * B + b) * H + u] = st[p];
     } else {
       st[p] = __bfloat162float(Y[(static_cast<int64_t>(slot_h0) * B + b) * ldY + dir * H + u]);
-      const float* bb = a.bh + dir * 4 * H + 4 * u;
-      bh[p][0] = bb[0]; bh[p][1] = bb[1]; bh[p][2] = bb[2];
+      if (a.bh) {   // resetAfter's recurrent biases (reset-before has its biases in P)
+        const float* bb = a.bh + dir * 4 * H + 4 * u;
+        bh[p][0] = bb[0]; bh[p][1] = bb[1]; bh[p][2] = bb[2];
+      }
     }
   }
 
@@ -468,9 +475,10 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       const int ul = id % UPC, b = id / UPC, u = ubase + ul;
       pq[p] = id < npairs ? ld_u2(Pm + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u) : make_uint2(0, 0);
     }
-    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B, ks * P.nsub, dir, idesc,
-                       adesc0, true,
-                       static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_FWD_TC))
+    const int ex = rbm ? 2 * s : s;   // exchanges (counter phases) before this step's first
+    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B, sp * B, ks * P.nsub,
+                       dir, idesc, adesc0, true, static_cast<unsigned int>(ex) * P.nblk_dir, ex, ks, n_mma, w_waited,
+                       K_FWD_TC))
       break;
     // partial sums of every pair first (all shared loads in flight), then the cell
     float4 acc[PP];
@@ -497,6 +505,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
       hv[p] = 0.f;
+      gq[p][0] = gq[p][1] = gq[p][2] = gq[p][3] = 0.f;
       if (id >= npairs) break;
       const int ul = id % UPC, b = id / UPC, u = ubase + ul;
       float pv[4];
@@ -521,6 +530,13 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         }
         st[p] = c;
         pv[0] = i; pv[1] = f; pv[2] = gg; pv[3] = o;
+      } else if (rbm) {
+        // reset-before, phase A: r, z and the reset state the second contraction reads
+        const float r = sigm_fast(pv[0] + acc[p].x);
+        const float z = sigm_fast(pv[1] + acc[p].y);
+        gq[p][0] = r; gq[p][1] = z;
+        RHp[((static_cast<int64_t>(dir) * TT + t) * B + b) * H + u] = __float2bfloat16_rn(r * st[p]);
+        continue;
       } else {
         const float r = sigm_fast(pv[0] + acc[p].x + bh[p][0]);
         const float z = sigm_fast(pv[1] + acc[p].y + bh[p][1]);
@@ -536,6 +552,36 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       hv[p] = h;
       gq[p][0] = pv[0]; gq[p][1] = pv[1]; gq[p][2] = pv[2]; gq[p][3] = pv[3];
       Y[(static_cast<int64_t>(so) * B + b) * ldY + dir * H + u] = __float2bfloat16_rn(h);
+    }
+    if constexpr (EXT) {
+      if (rbm) {
+        // reset-before, phase B: publish r * h_{t-1}, then n = tanh(W_in x + b_n + W_hn (r * h_{t-1}))
+        step_arrive(a, skip, s, 0);
+        if (!step_exchange(P, &tmR, &tmR4, ring, recv, bars, tmem, g, ks * P.Kc, (dir * TT + t) * B, t * B,
+                           ks * P.nsub, dir, idesc, adesc0, true, static_cast<unsigned int>(ex + 1) * P.nblk_dir,
+                           ex + 1, ks, n_mma, w_waited, K_FWD_TC))
+          break;
+#pragma unroll
+        for (int p = 0; p < PP; ++p) {
+          const int id = threadIdx.x + p * kThreads;
+          if (id >= npairs) break;
+          const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+          const uint32_t ra = recv_s + static_cast<uint32_t>((b * RPC + 4 * ul + 2) * 4);
+          float sn = 0.f;
+#pragma unroll
+          for (int r = 0; r < KS; ++r) sn += lds_f1(ra + r * src_bytes);
+          float pv[4];
+          unpack4(pq[p], pv);
+          const float n = tanh_fast(pv[2] + sn);
+          const float z = gq[p][1];
+          float h = (1.f - z) * n + z * st[p];
+          if (t >= lenp[p]) h = st[p];
+          st[p] = h;
+          hv[p] = h;
+          gq[p][2] = n; gq[p][3] = 0.f;
+          Y[(static_cast<int64_t>(so) * B + b) * ldY + dir * H + u] = __float2bfloat16_rn(h);
+        }
+      }
     }
     RNN_TRACE_AT(13, 0, s);
     RNN_TRACE_AT(5, 0, s);
@@ -664,6 +710,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       }
     }
     if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B,
+                       (s > 0 ? tp : 0) * B,
                        ks * P.nsub, dir, idesc, adesc0, s > 0, static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_BWD_TC)) {
       aborted = true;
       break;

@@ -1,0 +1,71 @@
+"""GRU reset-before forward on the tensor-core kernel (two exchanges per step:
+r, z from W_hh h_{t-1}, then n from W_hn (r * h_{t-1})), chosen automatically
+from batch 4 on, with the SIMT backward reading the gates and r * h_{t-1} it
+stored.  Against the fp64 oracle, tolerance 2e-2 (bf16): forward and backward,
+one and two layers, both directions, sequence lengths, hidden sizes that take
+one or several K slices, and the small-batch case that stays on the SIMT
+forward."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import synth
+from tests import harness as Hn
+
+pytestmark = pytest.mark.gpu
+
+TC, SIMT = 1, 2
+
+
+def _wl(L, bidir, T, B, I, H, seed):
+    return synth.Workload(f"rb_tc_T{T}_B{B}_I{I}_H{H}_L{L}{'bi' if bidir else ''}", "gru", False, L, bidir, T, B, I,
+                          H, "bf16", seed, state_std=0.5)
+
+
+@pytest.mark.parametrize("L,bidir,T,B,H", [(1, False, 10, 8, 128), (1, True, 9, 16, 256), (2, True, 7, 4, 192),
+                                           (1, False, 6, 8, 1024), (1, False, 5, 33, 512)])
+def test_reset_before_tc_forward(L, bidir, T, B, H):
+    wl = _wl(L, bidir, T, B, 64, H, 700 + H + B)
+    inp = synth.make_inputs(wl)
+    gpu = Hn.run_gpu(inp)
+    assert gpu["fwd_algo"] == TC and gpu["algo"] == SIMT
+    Hn.compare(gpu, Hn.run_oracle(inp), wl)
+
+
+def test_reset_before_tc_forward_with_lengths():
+    wl = _wl(2, True, 9, 8, 32, 128, 711)
+    inp = dataclasses.replace(synth.make_inputs(wl), lengths=np.array([9, 0, 1, 5, 8, 3, 9, 7]))
+    gpu = Hn.run_gpu(inp)
+    assert gpu["fwd_algo"] == TC
+    Hn.compare(gpu, Hn.run_oracle(inp), wl)
+    for b, n in enumerate(inp.lengths):
+        assert np.all(gpu["y"][n:, b] == 0.0)
+
+
+def test_reset_before_small_batch_stays_simt():
+    wl = _wl(1, False, 6, 2, 32, 128, 712)
+    inp = synth.make_inputs(wl)
+    gpu = Hn.run_gpu(inp)
+    assert gpu["fwd_algo"] == SIMT
+    Hn.compare(gpu, Hn.run_oracle(inp), wl)
+
+
+def test_reset_before_tc_inference_matches_training():
+    import torch
+    import bwd_persistent_cta_gb300 as R
+    wl = _wl(1, True, 8, 8, 32, 128, 713)
+    inp = synth.make_inputs(wl)
+    rnn = R.RNN("gru", 32, 128, 8, 8, 1, True, False, "bf16")
+    try:
+        assert rnn.fwd_algo == TC
+        w = Hn.to_dev(synth.flatten_params(wl, inp.params), wl)
+        x, hx = Hn.to_dev(inp.x, wl), Hn.to_dev(inp.h0, wl)
+        y1, h1, _ = rnn.forward(x, w, hx, None, train=True)
+        y0, h0, _ = rnn.forward(x, w, hx, None, train=False)
+        rnn.sync()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(Hn.to_np(y0), Hn.to_np(y1))
+        np.testing.assert_array_equal(Hn.to_np(h0), Hn.to_np(h1))
+    finally:
+        rnn.close()
