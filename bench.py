@@ -15,7 +15,10 @@ scaling, no data-path collective); timing takes the max over ranks.
 
 Prints one JSON line (rank 0).  ``value`` is timestep*batch per second over
 all ranks; ``roofline`` covers the kernel class with the largest share of the
-step, timed live with CUDA events on its launching stream.
+step, timed live with CUDA events on its launching stream.  ``e2e`` is the
+same step through the C ABI with the inputs uploaded from pinned host memory
+and the result (dw; y for forward-only workloads) read back inside the timed
+region; dy's upload runs on a copy stream during the forward.
 """
 from __future__ import annotations
 
@@ -313,20 +316,36 @@ def run_ours(args):
     # --- end to end through the C ABI with host buffers --------------------
     xh = x.cpu().pin_memory()
     dyh = dy.cpu().pin_memory()
-    dwh = torch.empty(dw.shape, dtype=dw.dtype).pin_memory()
+    res = y if wl.forward_only else dw            # the step's result read back to the host
+    resh = torch.empty(res.shape, dtype=res.dtype).pin_memory()
     for _ in range(2):
-        x.copy_(xh, non_blocking=True); dy.copy_(dyh, non_blocking=True); step(); dwh.copy_(dw, non_blocking=True)
+        x.copy_(xh, non_blocking=True); dy.copy_(dyh, non_blocking=True); step(); resh.copy_(res, non_blocking=True)
     torch.cuda.synchronize()
     Ke = max(3, K // 2)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # dy is needed only by the backward: its upload runs on a copy stream
+    # during the forward (started after e0, waited for before the backward)
+    copy_stream = torch.cuda.Stream(device=dev)
+    started, dy_in = torch.cuda.Event(), torch.cuda.Event()
+    main = torch.cuda.current_stream()
     e_ms = 0.0
     for _ in range(Ke):
         flush.zero_()
         e0.record()
+        started.record()
         x.copy_(xh, non_blocking=True)
-        dy.copy_(dyh, non_blocking=True)
-        step()
-        dwh.copy_(dw, non_blocking=True)
+        if wl.forward_only:
+            step()
+        else:
+            copy_stream.wait_event(started)
+            with torch.cuda.stream(copy_stream):
+                dy.copy_(dyh, non_blocking=True)
+                dy_in.record()
+            rnn.forward(x, w, hx, cx, train=True, y=y, hy=hy, cy=cy)
+            main.wait_event(dy_in)
+            rnn.backward_data(dy, w, None, None, dx=dx, dhx=dhx, dcx=dcx, cx=cx)
+            rnn.backward_weights(x, dw=dw)
+        resh.copy_(res, non_blocking=True)
         e1.record()
         torch.cuda.synchronize()
         e_ms += e0.elapsed_time(e1)
@@ -378,8 +397,9 @@ def run_ours(args):
                                            "units": "valid timesteps (sum of sequence lengths) x 1"}})},
             "tflops": tflops, "tflops_unit": "TFLOP/s (algorithmic, sum over layers/dirs of 3*2*G*H*(I+H)*B*T)",
             "e2e": {"value": job_throughput(wl.seq_len * wl.batch * valid_frac, world, e_ms), "unit": UNIT,
-                    "h2d_bytes_per_step": int(x.numel() * x.element_size() + dy.numel() * dy.element_size()),
-                    "d2h_bytes_per_step": int(dw.numel() * dw.element_size())},
+                    "h2d_bytes_per_step": int(x.numel() * x.element_size() +
+                                              (0 if wl.forward_only else dy.numel() * dy.element_size())),
+                    "d2h_bytes_per_step": int(res.numel() * res.element_size())},
             "gpu_launches": int(launches), "gpu_launches_per_step": launches / K,
             "roofline": roofline, "clocks": clocks, "cpu_baseline": cpu,
             "wall_s_timed_region": t_wall,
