@@ -89,7 +89,9 @@ void fill_layout(rnn_handle_s* h) {
     if (h->lstm && !h->recompute) h->r_c[l] = r.take(static_cast<size_t>(D) * (T + 1) * B * H * 4);
     if (h->rb) h->r_rh[l] = r.take(static_cast<size_t>(D) * TB * H * es);
     h->r_dg[l] = r.take(TB * D * 4 * H * es);
-    h->r_db[l] = r.take(static_cast<size_t>(D) * 4 * H * 4);
+    // bias-gradient sums, one plane per batch part of the tensor-core backward
+    // (plane 0 holds the total when it returns)
+    h->r_db[l] = r.take(static_cast<size_t>(kMaxBatchParts) * D * 4 * H * 4);
     if (h->dw_bptt) h->r_dwhh[l] = r.take(static_cast<size_t>(D) * G * H * H * 4);
   }
   h->reserve_bytes = r.off;

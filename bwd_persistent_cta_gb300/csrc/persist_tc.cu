@@ -6,6 +6,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "persist_tc_kernels.cuh"
 
@@ -20,89 +21,124 @@ int pp_for(int pairs) {
 
 struct TcPlan {
   int KS = 0, Kc = 0, nsub = 0, R = 0, Npad = 0, UPC = 0, PP = 0, nrg = 0, w_tmem = 0;
+  int NB = 1, Bp = 0;   // batch parts per row group, batch rows per part
   uint32_t tmem_cols = 0, off_ring = 0, off_recv = 0, off_bar = 0;
   size_t smem = 0;
 };
 
 size_t a1k(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
-// Candidate K splits for one launch, preferred first: the largest split whose
-// grid fits (shorter per-CTA contraction, less shared memory per CTA), except
-// that the backward takes a cluster of 8 before one of 16.  Measured on GB300
-// (backward kernel, T=128): 16 -> 8 changed GRU resetAfter B64 H512 from 868
-// to 803 us, B64 H256 761 -> 672, B32 H512 584 -> 563, LSTM B64 H512 804 ->
-// 693, B32 H256 533 -> 454, B128 H512 1080 -> 1012, B64 H768 794 -> 783: the
-// partial-sum push and the cluster barrier shrink with the cluster while the
-// per-CTA MMAs double.  GRU above batch 64 keeps 16 (B128 H512: 1251 at 16,
-// 1353 at 8), its heavier per-row backward step being split over more CTAs.
-// Whether the clusters can all be resident at once is checked at launch.
+// Estimated per-step cost (us) of a plan's parts that differ between plans,
+// fitted to GB300 step traces and sweeps (T=128..512, B 32..128, H 512..1024):
+// MMA issue ~55 ns per K=16 instruction (issue-bound at N <= 128), the
+// DSMEM partial push ~33 ns per KB (51 in clusters of 16), the epilogue
+// ~0.35 us (forward) / 0.5 us (backward) per pair per thread, and the cluster
+// barrier by cluster size.  The counter exchange and TMA are about equal
+// across plans.  Examples it ranks as measured: GRU resetAfter B64 H512 takes
+// K split 4 / 2 batch parts forward (0.586 -> 0.477 ms) and 8 / 2 backward
+// (0.819 -> 0.606 ms); LSTM B32 H1024 keeps 4 / 1 and 8 / 1 (2 parts: 1.08 ->
+// 1.18 ms forward, 1.30 -> 1.56 ms backward); the 2-layer bidirectional LSTM
+// B128 H1024 backward takes 4 / 4 (17.8 -> 14.0 ms); GRU B128 H512 without
+// parts keeps a split of 16 over 8 (1.25 vs 1.35 ms).
+double plan_cost(int bwd, int KS, int Kc, int Npad, int pairs) {
+  const double mma = 0.055 * (Kc / 16);
+  const double push_kb = 128.0 * Npad * 4 * (KS - 1) / KS / 1024.0;
+  const double push = push_kb * (KS >= 16 ? 0.051 : 0.033);
+  const double per_thread = (pairs + kThreads - 1) / kThreads;
+  const double epi = (bwd ? 0.5 : 0.35) * per_thread;
+  const double cl = KS >= 16 ? 1.6 : KS >= 8 ? 0.8 : KS >= 4 ? 0.7 : KS >= 2 ? 0.6 : 0.2;
+  return mma + push + epi + cl;
+}
+
+// Candidate plans for one launch (K split x batch parts), cheapest first by
+// plan_cost.  Whether their clusters can all be resident at once is checked
+// at launch.
 int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int max_out) {
+  (void)mode;
   if (B < 1 || B > 256) return 0;
   const int K = bwd ? 4 * H : H;
   const int nrg = bwd ? H / 128 : (4 * H) / 128;
   if (bwd ? (H % 128) : (H % 32)) return 0;
-  const int Npad = (B + 15) / 16 * 16;
-  // tuning knob: RNN_TC_MAX_KS_FWD / RNN_TC_MAX_KS_BWD cap the split (1..16)
+  // tuning knobs: RNN_TC_MAX_KS_FWD / RNN_TC_MAX_KS_BWD cap the K split
+  // (1..16); RNN_TC_NB_FWD / RNN_TC_NB_BWD fix the batch parts (1, 2, 4)
   int cap = kMaxKS;
   if (const char* e = std::getenv(bwd ? "RNN_TC_MAX_KS_BWD" : "RNN_TC_MAX_KS_FWD")) {
     const int v = std::atoi(e);
     if (v >= 1 && v <= kMaxKS) cap = v;
   }
-  int n = 0;
-  for (int KS = kMaxKS; KS >= 1 && n < max_out; KS /= 2) {
-    if (KS > cap) continue;
-    if (K % (KS * kSubK)) continue;
-    const int Kc = K / KS;
-    const int nsub = Kc / kSubK;
-    const int UPC = (bwd ? 128 : 32) / KS;
-    if (UPC < 1) continue;
-    const int PP = pp_for(UPC * B);
-    if (PP == 0) continue;
-    if (nrg * KS * ndir > num_sms) continue;
-    const size_t wbytes = static_cast<size_t>(nsub) * kWSub;
-    const size_t rb = static_cast<size_t>(Npad) * 128;
-    const size_t recv = static_cast<size_t>(Npad) * 128 * 4;
-    // weight tile in shared memory, with the deepest exchange ring that fits
-    int R = nsub < kMaxRing ? nsub : kMaxRing;
-    size_t smem = 0;
-    for (; R >= 1; --R) {
-      smem = a1k(wbytes) + a1k(R * rb) + a1k(recv) + a1k(sizeof(TcBars)) + 1024;
-      if (smem <= kSmemCap) break;
-    }
-    // else weight sub-tiles in TMEM columns [256, 512) (an even count, at most
-    // 8), the others in shared memory, and the whole K slice of the exchange
-    // operand in flight at once
-    int wt = 0;
-    if (R < nsub && Npad <= 256) {
-      const int t = (nsub < 8 ? nsub : 8) & ~1;
-      const size_t sm2 = a1k(static_cast<size_t>(nsub - t) * kWSub) + a1k(static_cast<size_t>(nsub) * rb) +
-                         a1k(recv) + a1k(sizeof(TcBars)) + 1024;
-      if (t >= 2 && sm2 <= kSmemCap) {
-        wt = t;
-        R = nsub;
-        smem = sm2;
-      }
-    }
-    if (!wt && (R < 1 || (R < nsub && R < 2))) continue;
-    TcPlan p;
-    p.KS = KS; p.Kc = Kc; p.nsub = nsub; p.R = R; p.Npad = Npad; p.UPC = UPC; p.PP = PP; p.nrg = nrg;
-    p.w_tmem = wt;
-    uint32_t tc = 32;
-    while (tc < static_cast<uint32_t>(Npad)) tc *= 2;
-    p.tmem_cols = wt ? 512 : tc;
-    p.off_ring = static_cast<uint32_t>(a1k(static_cast<size_t>(nsub - wt) * kWSub));
-    p.off_recv = p.off_ring + static_cast<uint32_t>(a1k(R * rb));
-    p.off_bar = p.off_recv + static_cast<uint32_t>(a1k(recv));
-    // all 512 TMEM columns: the shared-memory request alone must keep a
-    // second CTA off the SM
-    const size_t floor = wt ? kOneCtaSmem : kMinSmem;
-    p.smem = smem < floor ? floor : smem;
-    out[n++] = p;
+  int nb_only = 0;
+  if (const char* e = std::getenv(bwd ? "RNN_TC_NB_BWD" : "RNN_TC_NB_FWD")) {
+    const int v = std::atoi(e);
+    if (v == 1 || v == 2 || v == 4) nb_only = v;
   }
-  if (bwd && n >= 2 && out[0].KS == 16 && out[1].KS == 8 && !(mode == 1 && Npad > 64)) {
-    const TcPlan t = out[0];
-    out[0] = out[1];
-    out[1] = t;
+  std::vector<std::pair<double, TcPlan>> cands;
+  for (int NB = 1; NB <= kMaxBatchParts; NB *= 2) {
+    // each batch part: Bp rows (at least 8; every part non-empty), the MMA N
+    // dimension padded to 16
+    const int Bp = (B + NB - 1) / NB;
+    if (NB > 1 && (Bp < 8 || (NB - 1) * Bp >= B)) continue;
+    if (nb_only && NB != nb_only && !(NB == 1 && (B + nb_only - 1) / nb_only < 8)) continue;
+    const int Npad = (Bp + 15) / 16 * 16;
+    for (int KS = kMaxKS; KS >= 1; KS /= 2) {
+      if (KS > cap) continue;
+      if (K % (KS * kSubK)) continue;
+      const int Kc = K / KS;
+      const int nsub = Kc / kSubK;
+      const int UPC = (bwd ? 128 : 32) / KS;
+      if (UPC < 1) continue;
+      const int PP = pp_for(UPC * Bp);
+      if (PP == 0) continue;
+      if (nrg * KS * NB * ndir > num_sms) continue;
+      const size_t wbytes = static_cast<size_t>(nsub) * kWSub;
+      const size_t rb = static_cast<size_t>(Npad) * 128;
+      const size_t recv = static_cast<size_t>(Npad) * 128 * 4;
+      // weight tile in shared memory, with the deepest exchange ring that fits
+      int R = nsub < kMaxRing ? nsub : kMaxRing;
+      size_t smem = 0;
+      for (; R >= 1; --R) {
+        smem = a1k(wbytes) + a1k(R * rb) + a1k(recv) + a1k(sizeof(TcBars)) + 1024;
+        if (smem <= kSmemCap) break;
+      }
+      // else weight sub-tiles in TMEM columns [256, 512) (an even count, at
+      // most 8), the others in shared memory, and the whole K slice of the
+      // exchange operand in flight at once
+      int wt = 0;
+      if (R < nsub && Npad <= 256) {
+        const int t = (nsub < 8 ? nsub : 8) & ~1;
+        const size_t sm2 = a1k(static_cast<size_t>(nsub - t) * kWSub) + a1k(static_cast<size_t>(nsub) * rb) +
+                           a1k(recv) + a1k(sizeof(TcBars)) + 1024;
+        if (t >= 2 && sm2 <= kSmemCap) {
+          wt = t;
+          R = nsub;
+          smem = sm2;
+        }
+      }
+      if (!wt && (R < 1 || (R < nsub && R < 2))) continue;
+      TcPlan p;
+      p.KS = KS; p.Kc = Kc; p.nsub = nsub; p.R = R; p.Npad = Npad; p.UPC = UPC; p.PP = PP; p.nrg = nrg;
+      p.NB = NB; p.Bp = Bp;
+      p.w_tmem = wt;
+      uint32_t tc = 32;
+      while (tc < static_cast<uint32_t>(Npad)) tc *= 2;
+      p.tmem_cols = wt ? 512 : tc;
+      p.off_ring = static_cast<uint32_t>(a1k(static_cast<size_t>(nsub - wt) * kWSub));
+      p.off_recv = p.off_ring + static_cast<uint32_t>(a1k(R * rb));
+      p.off_bar = p.off_recv + static_cast<uint32_t>(a1k(recv));
+      // all 512 TMEM columns: the shared-memory request alone must keep a
+      // second CTA off the SM
+      const size_t floor = wt ? kOneCtaSmem : kMinSmem;
+      p.smem = smem < floor ? floor : smem;
+      cands.emplace_back(plan_cost(bwd, KS, Kc, Npad, UPC * Bp), p);
+    }
+  }
+  std::stable_sort(cands.begin(), cands.end(),
+                   [](const std::pair<double, TcPlan>& x, const std::pair<double, TcPlan>& y) {
+                     return x.first < y.first;
+                   });
+  int n = 0;
+  for (const auto& c : cands) {
+    if (n >= max_out) break;
+    out[n++] = c.second;
   }
   return n;
 }
@@ -113,7 +149,7 @@ const void* kernel_for(int bwd, int pp, int ks, int ext) {
 
 void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPlan& pl, int ndir, cudaStream_t s) {
   cfg = cudaLaunchConfig_t{};
-  cfg.gridDim = dim3(pl.nrg * pl.KS, ndir, 1);
+  cfg.gridDim = dim3(pl.nrg * pl.KS * pl.NB, ndir, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
@@ -131,8 +167,8 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPla
 // of microseconds of host time, which the GPU would otherwise wait for at the
 // start of every persistent launch.
 struct PlanKey {
-  int v[10];
-  bool operator<(const PlanKey& o) const { return std::lexicographical_compare(v, v + 10, o.v, o.v + 10); }
+  int v[12];
+  bool operator<(const PlanKey& o) const { return std::lexicographical_compare(v, v + 12, o.v, o.v + 12); }
 };
 
 int env_cap(const char* name) {
@@ -159,15 +195,15 @@ bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext
   int dev = 0;
   cudaGetDevice(&dev);
   const PlanKey key{{mode, bwd, H, B, ndir, num_sms, ext, dev, env_cap("RNN_TC_MAX_KS_FWD"),
-                     env_cap("RNN_TC_MAX_KS_BWD")}};
+                     env_cap("RNN_TC_MAX_KS_BWD"), env_cap("RNN_TC_NB_FWD"), env_cap("RNN_TC_NB_BWD")}};
   std::lock_guard<std::mutex> lock(g_plan_mu);
   const auto hit = g_plans.find(key);
   if (hit != g_plans.end()) {
     *chosen = hit->second.second;
     return hit->second.first;
   }
-  TcPlan plans[5];
-  const int n = make_plans(mode, bwd, H, B, ndir, num_sms, plans, 5);
+  TcPlan plans[12];
+  const int n = make_plans(mode, bwd, H, B, ndir, num_sms, plans, 12);
   for (int i = 0; i < n; ++i) {
     const TcPlan& pl = plans[i];
     const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
@@ -184,7 +220,7 @@ bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext
       cudaGetLastError();
       continue;
     }
-    if (max_clusters >= pl.nrg * ndir) {
+    if (max_clusters >= pl.nrg * pl.NB * ndir) {
       *chosen = pl;
       g_plans[key] = {true, pl};
       return true;
@@ -249,7 +285,10 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   P.a = a;
   P.KS = pl.KS; P.Kc = pl.Kc; P.nsub = pl.nsub; P.R = pl.R; P.Npad = pl.Npad; P.UPC = pl.UPC;
   P.RPC = 128 / pl.KS;
-  P.nblk_dir = static_cast<unsigned int>(pl.nrg * pl.KS);
+  P.nblk_dir = static_cast<unsigned int>(pl.nrg * pl.KS * pl.NB);
+  P.nrg = pl.nrg;
+  P.NB = pl.NB;
+  P.Bp = pl.Bp;
   P.tmem_cols = pl.tmem_cols;
   P.off_ring = pl.off_ring; P.off_recv = pl.off_recv; P.off_bar = pl.off_bar;
   P.w_tmem = pl.w_tmem;

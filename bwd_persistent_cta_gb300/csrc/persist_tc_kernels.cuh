@@ -90,6 +90,8 @@ struct TcPersistParams {
                            // sub-tiles [0, w_tmem) there, [w_tmem, nsub) in shared memory
   int single;              // the whole K slice arrives with one 4-D TMA per step (R == nsub)
   int prefetch;            // forward: request later steps' projections into L2 (kPrefetchSteps)
+  int nrg;                 // 128-row groups per direction
+  int NB, Bp;              // batch parts per row group and batch rows per part (Npad = Bp rounded up to 16)
   uint32_t wcol;           // first TMEM column of the weight tile (w_tmem)
   unsigned int nblk_dir;   // CTAs per direction
   uint32_t tmem_cols;
@@ -402,8 +404,12 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const PersistArgs& a = P.a;
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
   const int dir = a.dir0 + blockIdx.y;
+  // blockIdx.x = (batch part * row groups + row group) * KS + K slice; a
+  // cluster is the KS K slices of one row group and batch part
   const int ks = static_cast<int>(blockIdx.x) % KS;
-  const int rg = static_cast<int>(blockIdx.x) / KS;
+  const int rg = (static_cast<int>(blockIdx.x) / KS) % P.nrg;
+  const int b0 = (static_cast<int>(blockIdx.x) / KS / P.nrg) * P.Bp;   // first batch row of this part
+  const int Bn = min(P.Bp, B - b0);
   const bool lstm = a.mode == 0;
   // GRU reset-before (extended variant only): two exchanges per step, the
   // second over r * h_{t-1} (tmR / tmR4: a view of RH [D][T*B][H])
@@ -425,7 +431,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int64_t ldY = static_cast<int64_t>(D) * H;
   const int64_t ldP = static_cast<int64_t>(D) * 4 * H;
   const int UPC = P.UPC;
-  const int npairs = UPC * B;
+  const int npairs = UPC * Bn;
   const int ubase = rg * 32 + ks * UPC;     // first hidden unit of this CTA's epilogue
   const int slot_h0 = dir ? TT + 1 : 0;
   const uint32_t recv_s = smem_u32(recv);
@@ -442,7 +448,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     bh[p][0] = bh[p][1] = bh[p][2] = 0.f;
     const int id = threadIdx.x + p * kThreads;
     if (id >= npairs) continue;
-    const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+    const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
     if constexpr (EXT) lenp[p] = a.len ? a.len[b] : TT;   // clipping alone: no lengths
     if (lstm) {
       const __nv_bfloat16* c0 = static_cast<const __nv_bfloat16*>(a.c0);
@@ -472,11 +478,12 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
-      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
       pq[p] = id < npairs ? ld_u2(Pm + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u) : make_uint2(0, 0);
     }
     const int ex = rbm ? 2 * s : s;   // exchanges (counter phases) before this step's first
-    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B, sp * B, ks * P.nsub,
+    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B + b0, sp * B + b0,
+                       ks * P.nsub,
                        dir, idesc, adesc0, true, static_cast<unsigned int>(ex) * P.nblk_dir, ex, ks, n_mma, w_waited,
                        K_FWD_TC))
       break;
@@ -485,10 +492,10 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
-      const int ul = id % UPC, b = id / UPC;
+      const int ul = id % UPC, bl = id / UPC;
       acc[p] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (id < npairs) {
-        const uint32_t ra = recv_s + static_cast<uint32_t>((b * RPC + 4 * ul) * 4);
+        const uint32_t ra = recv_s + static_cast<uint32_t>((bl * RPC + 4 * ul) * 4);
         float4 v[KS];
 #pragma unroll
         for (int r = 0; r < KS; ++r) v[r] = lds_f4(ra + r * src_bytes);
@@ -507,7 +514,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       hv[p] = 0.f;
       gq[p][0] = gq[p][1] = gq[p][2] = gq[p][3] = 0.f;
       if (id >= npairs) break;
-      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
       float pv[4];
       unpack4(pq[p], pv);
       float h;
@@ -557,7 +564,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       if (rbm) {
         // reset-before, phase B: publish r * h_{t-1}, then n = tanh(W_in x + b_n + W_hn (r * h_{t-1}))
         step_arrive(a, skip, s, 0);
-        if (!step_exchange(P, &tmR, &tmR4, ring, recv, bars, tmem, g, ks * P.Kc, (dir * TT + t) * B, t * B,
+        if (!step_exchange(P, &tmR, &tmR4, ring, recv, bars, tmem, g, ks * P.Kc, (dir * TT + t) * B + b0, t * B + b0,
                            ks * P.nsub, dir, idesc, adesc0, true, static_cast<unsigned int>(ex + 1) * P.nblk_dir,
                            ex + 1, ks, n_mma, w_waited, K_FWD_TC))
           break;
@@ -565,8 +572,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         for (int p = 0; p < PP; ++p) {
           const int id = threadIdx.x + p * kThreads;
           if (id >= npairs) break;
-          const int ul = id % UPC, b = id / UPC, u = ubase + ul;
-          const uint32_t ra = recv_s + static_cast<uint32_t>((b * RPC + 4 * ul + 2) * 4);
+          const int ul = id % UPC, bl = id / UPC, b = b0 + bl, u = ubase + ul;
+          const uint32_t ra = recv_s + static_cast<uint32_t>((bl * RPC + 4 * ul + 2) * 4);
           float sn = 0.f;
 #pragma unroll
           for (int r = 0; r < KS; ++r) sn += lds_f1(ra + r * src_bytes);
@@ -594,7 +601,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       for (int p = 0; p < PP; ++p) {
         const int id = threadIdx.x + p * kThreads;
         if (id >= npairs) break;
-        const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+        const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
         prefetch_l2(Pm + (static_cast<int64_t>(tf) * B + b) * ldP + dir * 4 * H + 4 * u);
       }
     }
@@ -602,7 +609,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
       if (id >= npairs) break;
-      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
       if (G) Vec4<__nv_bfloat16>::store(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * 4 * H + 4 * u, gq[p]);
       if (lstm && a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = st[p];
       if (a.y_out) {
@@ -636,7 +643,10 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int K4 = 4 * H;
   const int dir = a.dir0 + blockIdx.y;
   const int ks = static_cast<int>(blockIdx.x) % KS;
-  const int rg = static_cast<int>(blockIdx.x) / KS;
+  const int rg = (static_cast<int>(blockIdx.x) / KS) % P.nrg;
+  const int nb = static_cast<int>(blockIdx.x) / KS / P.nrg;   // batch part
+  const int b0 = nb * P.Bp;
+  const int Bn = min(P.Bp, B - b0);
   const bool lstm = a.mode == 0;
   constexpr int RPC = 128 / KS;
   const bool clip = EXT && a.clip;
@@ -655,7 +665,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int64_t ldY = static_cast<int64_t>(D) * H;
   const int64_t ldG = static_cast<int64_t>(D) * K4;
   const int UPC = P.UPC;
-  const int npairs = UPC * B;
+  const int npairs = UPC * Bn;
   const int ubase = rg * 128 + ks * UPC;
   const uint32_t recv_s = smem_u32(recv);
   const uint32_t src_bytes = static_cast<uint32_t>(P.Npad) * RPC * 4;
@@ -672,7 +682,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     db[p][0] = db[p][1] = db[p][2] = db[p][3] = 0.f;
     const int id = threadIdx.x + p * kThreads;
     if (id >= npairs) continue;
-    const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+    const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
     if constexpr (EXT) lenp[p] = a.len ? a.len[b] : TT;   // clipping alone: no lengths
     if (lstm && a.dcT)
       carry[p] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.dcT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
@@ -695,7 +705,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
-      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
       gq[p] = make_uint2(0, 0);
       e0[p] = e1[p] = dyv[p] = 0.f;
       if (id < npairs && s < TT) {
@@ -709,8 +719,8 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         }
       }
     }
-    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B,
-                       (s > 0 ? tp : 0) * B,
+    if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B + b0,
+                       (s > 0 ? tp : 0) * B + b0,
                        ks * P.nsub, dir, idesc, adesc0, s > 0, static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_BWD_TC)) {
       aborted = true;
       break;
@@ -720,7 +730,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
-      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
       dhs[p] = 0.f;
       if (id < npairs) {
         if (s == 0) {
@@ -728,7 +738,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
             dhs[p] = __bfloat162float(
                 static_cast<const __nv_bfloat16*>(a.dhT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
         } else {
-          const uint32_t ra = recv_s + static_cast<uint32_t>((b * RPC + ul) * 4);
+          const uint32_t ra = recv_s + static_cast<uint32_t>(((b - b0) * RPC + ul) * 4);
           float v[KS];
 #pragma unroll
           for (int r = 0; r < KS; ++r) v[r] = lds_f1(ra + r * src_bytes);
@@ -741,7 +751,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
       if (id >= npairs) break;
-      const int ul = id % UPC, b = id / UPC, u = ubase + ul;
+      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
       const float dhr = dhs[p];
       if (s == TT) {
         const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
@@ -824,8 +834,29 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       for (int q = 0; q < 4; ++q) atomicAdd(&red[ul * 4 + q], db[p][q]);
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < 4 * UPC; i += kThreads)
-      a.db[static_cast<int64_t>(dir) * K4 + 4 * ubase + i] = red[i];
+    // this batch part's sums to plane nb of db [NB][D][4H]; with several
+    // parts, part 0 then adds planes 1.. in order (deterministic) once every
+    // CTA of the direction has arrived once more
+    float* plane = a.db + (static_cast<int64_t>(nb) * D + dir) * K4 + 4 * ubase;
+    for (int i = threadIdx.x; i < 4 * UPC; i += kThreads) plane[i] = red[i];
+    if (P.NB > 1) {
+      step_arrive(a, skip, TT, 1);
+      if (nb == 0) {
+        int ok = 1;
+        if (threadIdx.x == 0) {
+          ok = wait_counter_geq(&a.dev->counters[a.dir0 + blockIdx.y],
+                                static_cast<unsigned int>(TT + 1) * P.nblk_dir, a.timeout_ns) ? 1 : 0;
+          if (!ok) report_status(a.dev, 4u, K_BWD_TC, static_cast<unsigned>(TT), W_COUNTER);
+        }
+        if (__syncthreads_and(ok)) {
+          for (int i = threadIdx.x; i < 4 * UPC; i += kThreads) {
+            float v = red[i];
+            for (int q = 1; q < P.NB; ++q) v += __ldcg(a.db + (static_cast<int64_t>(q) * D + dir) * K4 + 4 * ubase + i);
+            plane[i] = v;
+          }
+        }
+      }
+    }
   }
   teardown(P, bars);
 }

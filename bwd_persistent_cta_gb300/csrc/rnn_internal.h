@@ -126,6 +126,9 @@ bool persist_simt_dwhh_ok(const PersistArgs& a, int num_sms, bool hidden_only);
 int launch_persist_fwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
 int launch_persist_bwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms);
 
+// Batch parts the tensor-core backward may split a row group into; its bias
+// gradients take one [D][4H] fp32 plane per part (the sum lands in plane 0).
+constexpr int kMaxBatchParts = 4;
 bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms);
 // The forward kernel alone (a layer whose backward has no tensor-core plan).
 bool persist_tc_fwd_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms);
