@@ -822,23 +822,38 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     // after every peer has finished with it)
     tc_fence_before();
     if (KS > 1) cluster_sync(); else __syncthreads();
+    // Deterministic order throughout: UPC divides kThreads, so all pairs of
+    // thread t belong to unit t % UPC; each thread sums its pairs in order,
+    // then unit ul adds threads ul, ul + UPC, ... in index order.
     float* red = recv;
-    for (int i = threadIdx.x; i < 4 * UPC; i += kThreads) red[i] = 0.f;
-    __syncthreads();
+    {
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int p = 0; p < PP; ++p) {
-      const int id = threadIdx.x + p * kThreads;
-      if (id >= npairs) break;
-      const int ul = id % UPC;
+      for (int p = 0; p < PP; ++p) {
+        const int id = threadIdx.x + p * kThreads;
+        if (id >= npairs) break;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) atomicAdd(&red[ul * 4 + q], db[p][q]);
+        for (int q = 0; q < 4; ++q) part[q] += db[p][q];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) red[threadIdx.x * 4 + q] = part[q];
     }
     __syncthreads();
     // this batch part's sums to plane nb of db [NB][D][4H]; with several
-    // parts, part 0 then adds planes 1.. in order (deterministic) once every
-    // CTA of the direction has arrived once more
+    // parts, part 0 then adds planes 1.. in order once every CTA of the
+    // direction has arrived once more
     float* plane = a.db + (static_cast<int64_t>(nb) * D + dir) * K4 + 4 * ubase;
-    for (int i = threadIdx.x; i < 4 * UPC; i += kThreads) plane[i] = red[i];
+    float sums[2] = {0.f, 0.f};   // 4 * UPC <= 2 * kThreads values
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = threadIdx.x + k * kThreads;
+      if (i >= 4 * UPC) break;
+      const int ul = i >> 2, q = i & 3;
+      float v = 0.f;
+      for (int t2 = ul; t2 < kThreads; t2 += UPC) v += red[t2 * 4 + q];
+      sums[k] = v;
+      plane[i] = v;
+    }
     if (P.NB > 1) {
       step_arrive(a, skip, TT, 1);
       if (nb == 0) {
@@ -849,8 +864,11 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
           if (!ok) report_status(a.dev, 4u, K_BWD_TC, static_cast<unsigned>(TT), W_COUNTER);
         }
         if (__syncthreads_and(ok)) {
-          for (int i = threadIdx.x; i < 4 * UPC; i += kThreads) {
-            float v = red[i];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int i = threadIdx.x + k * kThreads;
+            if (i >= 4 * UPC) break;
+            float v = sums[k];
             for (int q = 1; q < P.NB; ++q) v += __ldcg(a.db + (static_cast<int64_t>(q) * D + dir) * K4 + 4 * ubase + i);
             plane[i] = v;
           }

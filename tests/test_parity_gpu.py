@@ -104,6 +104,9 @@ def test_repeated_calls_are_deterministic():
     b = Hn.run_gpu(inp, repeat=3)
     for k in ("y", "hy", "dx", "dhx"):
         np.testing.assert_array_equal(a[k], b[k])
+    # weight and bias gradients too: split-K and bias sums run in a fixed order
+    for name, v in a["dparams"][0][0].items():
+        np.testing.assert_array_equal(v, b["dparams"][0][0][name])
 
 
 # ---------------------------------------------------------------------------
