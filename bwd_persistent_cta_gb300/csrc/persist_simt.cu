@@ -21,8 +21,9 @@
 // through the read-only data cache from L2 (the packed recurrent weights of a
 // layer, at most 32 MiB in bf16, stay L2-resident across steps).
 //
-// This kernel serves the fp32 path (the 1e-5 bound needs fp32 FMA, not TF32),
-// GRU reset-before (two dependent contractions per step: r/z, then W_hn(r*h))
+// These kernels serve the fp32 path (the 1e-5 bound needs fp32 FMA, not
+// TF32), the plain RNN cells, the GRU reset-before backward (two dependent
+// contractions per step: r/z, then W_hn(r*h)) and its forward below batch 4,
 // and any shape the tensor-core kernels do not take.
 //
 // Cell math: Lstm.cpp lstmCellForwardPassCalcUnits / basicLstmCellForwardPass

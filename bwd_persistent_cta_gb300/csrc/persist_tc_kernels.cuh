@@ -1,15 +1,18 @@
 // persist_tc_kernels.cuh - persistent recurrent kernels on the tcgen05 tensor cores
 // (bf16 operands, fp32 accumulation in tensor memory), forward and backward
-// through time, for LSTM and GRU resetAfter.
+// through time, for LSTM and GRU resetAfter (and the GRU reset-before
+// forward, in the extended variant).
 //
 // Work split.  The per-step recurrent contraction is swapped so that the
 // weights are the M=128 operand and the batch is N:
 //   forward   S^T[4H, B]  = W_hh[4H, H] . h_{t-1}^T[H, B]
 //   backward  dh^T[H, B]  = W_hh^T[H, 4H] . dG^T_{t+1}[4H, B]
-// A cluster of KS CTAs owns one 128-row block of the weight operand; CTA rank
-// ks owns the K slice [ks*K/KS, (ks+1)*K/KS) and keeps that 128 x K/KS bf16
-// tile resident in shared memory (loaded once by TMA) for the whole sequence,
-// and owns the 128/KS rows [ks*128/KS, (ks+1)*128/KS) of the result.
+// A cluster of KS CTAs owns one 128-row block of the weight operand and one
+// batch part (NB parts of Bp rows split the batch); CTA rank ks owns the K
+// slice [ks*K/KS, (ks+1)*K/KS) and keeps that 128 x K/KS bf16 tile resident
+// for the whole sequence - in shared memory (loaded once by TMA), in tensor
+// memory as the MMA A operand, or split between the two - and owns the
+// 128/KS rows [ks*128/KS, (ks+1)*128/KS) of the result for its batch part.
 //
 // Each step a CTA
 //   1. waits (bounded) until every CTA of its direction finished the previous
@@ -28,13 +31,16 @@
 //      arrives on the counter, and only then stores what no CTA of this
 //      launch waits for.
 // Extended variant (template flag EXT, used when sequence lengths or LSTM cell
-// clipping are set; the plain variant compiles without either):
+// clipping are set, and for the GRU reset-before forward; the plain variant
+// compiles without them):
 //  * variable sequence lengths: at a step t >= len[b] the pair (u, b) keeps
 //    its state (h, c) and stores it unchanged, and the backward step writes
 //    zero gate gradients and passes the state gradients on (LSTM: an extra
 //    register carries dh past such steps);
 //  * LSTM cell clipping: every use of the raw cell state goes through
-//    clip = min(max(c, lo), hi), and the backward multiplies by dclip.
+//    clip = min(max(c, lo), hi), and the backward multiplies by dclip;
+//  * GRU reset-before forward: two exchanges per step, the second over
+//    r * h_{t-1}, which each CTA stores for its units in between.
 // Cluster-uniform abort: every CTA reads the same set of flags after the same
 // barrier, so all CTAs of a cluster leave at the same step (after one more
 // cluster barrier, so no CTA exits while a peer may still touch its shared

@@ -74,8 +74,11 @@ typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
 
 /* Recurrent-kernel choice.  AUTO picks the tensor-core persistent kernels
  * (bf16 LSTM and GRU resetAfter whose W_hh slices fit on chip) and the SIMT
- * persistent kernels otherwise (every fp32 problem, GRU reset-before, shapes
- * the tensor-core kernels do not take).  The two explicit values force one. */
+ * persistent kernels otherwise (every fp32 problem, plain RNN cells, GRU
+ * reset-before, shapes the tensor-core kernels do not take); with AUTO the
+ * forward alone may still run on the tensor cores (see
+ * rnn_selected_fwd_algo).  The two explicit values force one kernel family
+ * for both passes. */
 typedef enum { RNN_ALGO_AUTO = 0, RNN_ALGO_PERSIST_TC = 1, RNN_ALGO_PERSIST_SIMT = 2 } rnn_algo_t;
 
 typedef struct {
