@@ -58,6 +58,8 @@ _SIGS = {
     "rnn_selected_algo": (ctypes.c_int, [_P]),
     "rnn_selected_fwd_algo": (ctypes.c_int, [_P]),
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
+    "rnn_debug_tc_plans": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "rnn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "rnn_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "rnn_get_timing": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]),
@@ -200,6 +202,15 @@ def rnn_get_timing(handle):
     if rc != RNN_OK:
         raise RnnError(rc, "rnn_get_timing")
     return list(ms), [int(v) for v in n]
+
+
+def rnn_debug_tc_plans(mode: int, bwd: int, hidden: int, batch: int, ndir: int, num_sms: int, max_out: int = 16):
+    """Candidate tensor-core plans, cheapest first: a list of dicts."""
+    buf = (ctypes.c_int * (7 * max_out))()
+    n = lib().rnn_debug_tc_plans(int(mode), int(bwd), int(hidden), int(batch), int(ndir), int(num_sms), buf,
+                                 int(max_out))
+    keys = ("ks", "nb", "ctas", "npad", "pp", "w_tmem", "smem")
+    return [dict(zip(keys, buf[7 * i:7 * i + 7])) for i in range(n)]
 
 
 def rnn_debug_skip_arrival(handle, cta: int) -> int:

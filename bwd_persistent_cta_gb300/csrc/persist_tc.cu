@@ -324,6 +324,20 @@ bool persist_tc_fwd_supported(int mode, int reset_after, int H, int B, int ndir,
   return !rb || f.R >= f.nsub;
 }
 
+extern "C" int rnn_debug_tc_plans(int mode, int bwd, int hidden, int batch, int ndir, int num_sms, int* out,
+                                  int max_out) {
+  if (!out || max_out <= 0) return 0;
+  TcPlan plans[32];
+  const int n = make_plans(mode, bwd ? 1 : 0, hidden, batch, ndir, num_sms, plans, max_out < 32 ? max_out : 32);
+  for (int i = 0; i < n; ++i) {
+    const TcPlan& p = plans[i];
+    int* o = out + 7 * i;
+    o[0] = p.KS; o[1] = p.NB; o[2] = p.nrg * p.KS * p.NB * ndir; o[3] = p.Npad; o[4] = p.PP; o[5] = p.w_tmem;
+    o[6] = static_cast<int>(p.smem);
+  }
+  return n;
+}
+
 int launch_persist_fwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms) { return launch(a, 0, s, num_sms); }
 int launch_persist_bwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms) { return launch(a, 1, s, num_sms); }
 

@@ -1,6 +1,7 @@
 /*
- * rnn_debug.h - test hook of librnn.so: run the library's internal GEMM
- * directly, so tests can check it element by element in isolation.
+ * rnn_debug.h - test hooks of librnn.so: the library's internal GEMM, run
+ * directly so tests can check it element by element in isolation, and the
+ * tensor-core planner's candidate ranking.
  *
  * C[row(m), n] = sum_k A(m,k) B(n,k) (+ bias[n]) (+ C if beta != 0)
  *   A(m,k) = A[m*lda + k] when a_kmajor, else A[k*lda + m] (same for B, n)
@@ -25,6 +26,17 @@ extern "C" {
 rnn_status_t rnn_debug_gemm(int M, int N, int K, const void* A, int64_t lda, int a_kmajor, const void* B,
                             int64_t ldb, int b_kmajor, void* C, int64_t ldc, int c_bf16, const float* bias,
                             int beta, int rowmap_H, const int* perm, int in_bf16, int use_tc, void* stream);
+
+/* Planner hook: the candidate plans of the tensor-core persistent kernel for
+ * one launch shape, cheapest first by the per-step cost estimate, before the
+ * launch-time check that their clusters can all be resident (host arithmetic
+ * only; needs no GPU).  mode: rnn_mode_t; bwd: 0 forward, 1 backward; ndir:
+ * directions in the launch; num_sms: SMs of the device.  For candidate i,
+ * out[7*i ...] = {K split (CTAs per cluster), batch parts, CTAs, padded
+ * batch rows per part, pairs per thread (1/2/4/8), weight sub-tiles held in
+ * tensor memory, shared memory bytes}.  Returns the number of candidates
+ * written (at most max_out). */
+int rnn_debug_tc_plans(int mode, int bwd, int hidden, int batch, int ndir, int num_sms, int* out, int max_out);
 
 #ifdef __cplusplus
 }

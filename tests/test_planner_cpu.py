@@ -1,0 +1,65 @@
+"""Host logic of the tensor-core planner (no GPU): the candidate ranking by the
+per-step cost estimate, followed by the co-residency filter the launch applies
+(emulated here with the limits measured on the 152-SM GB300: 7 clusters of 16
+CTAs, 15 of 8, 36 of 4 at one CTA per SM).  Each pinned choice is the plan
+measured fastest for that shape."""
+import os
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+LSTM, GRU = 0, 1
+SMS = 152
+MAX_CLUSTERS = {16: 7, 8: 15, 4: 36, 2: 76, 1: 152}
+
+
+@pytest.fixture(scope="module")
+def R():
+    from bwd_persistent_cta_gb300 import build as B
+    B.build()
+    import bwd_persistent_cta_gb300 as mod
+    return mod
+
+
+def chosen(R, mode, bwd, H, B, ndir):
+    """First candidate whose clusters can all be resident, as the launch picks it."""
+    for p in R.rnn_debug_tc_plans(mode, bwd, H, B, ndir, SMS):
+        if p["ctas"] // p["ks"] <= MAX_CLUSTERS[p["ks"]]:
+            return p["ks"], p["nb"]
+    return None
+
+
+@pytest.mark.parametrize("mode,bwd,H,B,ndir,expect", [
+    (GRU, 0, 512, 64, 1, (4, 2)),      # 0.586 -> 0.477 ms against (4, 1)
+    (GRU, 1, 512, 64, 1, (8, 2)),      # 0.819 -> 0.606 ms against (8, 1)
+    (LSTM, 0, 1024, 32, 1, (4, 1)),    # (2, 2): 1.08 -> 1.18 ms
+    (LSTM, 1, 1024, 32, 1, (8, 1)),    # (4, 2): 1.30 -> 1.56 ms
+    (LSTM, 0, 1024, 128, 2, (2, 1)),   # both directions in one launch
+    (LSTM, 1, 1024, 128, 2, None),     # no plan for both directions at once ...
+    (LSTM, 1, 1024, 128, 1, (4, 4)),   # ... one at a time: 17.8 -> 14.0 ms against (8, 1)
+    (LSTM, 0, 2048, 8, 1, (2, 1)),     # split weight tile, 128 CTAs
+])
+def test_planner_choice(R, mode, bwd, H, B, ndir, expect):
+    assert chosen(R, mode, bwd, H, B, ndir) == expect
+
+
+def test_candidates_respect_resources(R):
+    for mode, bwd, H, B in [(LSTM, 0, 1024, 128), (GRU, 1, 512, 64), (LSTM, 0, 2048, 8), (GRU, 1, 256, 200)]:
+        plans = R.rnn_debug_tc_plans(mode, bwd, H, B, 1, SMS)
+        assert plans
+        for p in plans:
+            assert p["ctas"] <= SMS
+            assert p["smem"] <= 227 * 1024
+            assert p["npad"] % 16 == 0 and p["npad"] <= 256
+            assert p["pp"] in (1, 2, 4, 8)
+            assert p["w_tmem"] % 2 == 0 and p["w_tmem"] <= 8
+            # every batch part non-empty, at least 8 rows when split
+            bp = -(-B // p["nb"])
+            assert p["nb"] == 1 or (bp >= 8 and (p["nb"] - 1) * bp < B)
+
+
+def test_no_plan_for_unsupported_shapes(R):
+    assert R.rnn_debug_tc_plans(LSTM, 1, 96, 16, 1, SMS) == []    # backward needs H % 128 == 0
+    assert R.rnn_debug_tc_plans(LSTM, 0, 512, 300, 1, SMS) == []  # batch above 256
