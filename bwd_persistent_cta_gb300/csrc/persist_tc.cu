@@ -55,7 +55,7 @@ double plan_cost(int bwd, int KS, int Kc, int Npad, int pairs) {
 // at launch.
 int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int max_out) {
   (void)mode;
-  if (B < 1 || B > 256) return 0;
+  if (B < 1 || B > 256 * kMaxBatchParts) return 0;
   const int K = bwd ? 4 * H : H;
   const int nrg = bwd ? H / 128 : (4 * H) / 128;
   if (bwd ? (H % 128) : (H % 32)) return 0;
@@ -76,6 +76,7 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
     // each batch part: Bp rows (at least 8; every part non-empty), the MMA N
     // dimension padded to 16
     const int Bp = (B + NB - 1) / NB;
+    if (Bp > 256) continue;   // one part's MMA N stays within 256
     if (NB > 1 && (Bp < 8 || (NB - 1) * Bp >= B)) continue;
     if (nb_only && NB != nb_only && !(NB == 1 && (B + nb_only - 1) / nb_only < 8)) continue;
     const int Npad = (Bp + 15) / 16 * 16;

@@ -69,3 +69,13 @@ def test_batch_parts_repeatable(monkeypatch):
         np.testing.assert_array_equal(a[k], b[k])
     for name, v in a["dparams"][0][0].items():
         np.testing.assert_array_equal(v, b["dparams"][0][0][name])
+
+
+@pytest.mark.parametrize("mode,ra", [("lstm", False), ("gru", True)])
+def test_batch_above_256_on_tensor_cores(mode, ra):
+    # 300 sequences: the MMA N limit of 256 needs 2 batch parts of 150 (N 160)
+    wl = _wl(mode, ra, 1, False, 6, 300, 64, 128, 840)
+    inp = synth.make_inputs(wl)
+    gpu = Hn.run_gpu(inp)
+    assert gpu["algo"] == TC
+    Hn.compare(gpu, Hn.run_oracle(inp), wl)

@@ -62,4 +62,14 @@ def test_candidates_respect_resources(R):
 
 def test_no_plan_for_unsupported_shapes(R):
     assert R.rnn_debug_tc_plans(LSTM, 1, 96, 16, 1, SMS) == []    # backward needs H % 128 == 0
-    assert R.rnn_debug_tc_plans(LSTM, 0, 512, 300, 1, SMS) == []  # batch above 256
+    assert R.rnn_debug_tc_plans(LSTM, 0, 512, 1100, 1, SMS) == []  # batch above 4 parts of 256
+
+
+def test_large_batch_takes_batch_parts(R):
+    # above 256 rows the MMA N limit needs 2 or 4 batch parts
+    for H, B, nb_min in [(512, 300, 2), (512, 512, 2), (256, 600, 4)]:
+        plans = R.rnn_debug_tc_plans(LSTM, 0, H, B, 1, SMS)
+        assert plans and all(p["nb"] >= nb_min and p["npad"] <= 256 for p in plans)
+    # hidden 512, batch 1000: 4 parts of 250 rows leave at most a K split of 2
+    # on the 152 SMs, i.e. 16 pairs per thread: no tensor-core plan
+    assert R.rnn_debug_tc_plans(LSTM, 0, 512, 1000, 1, SMS) == []
