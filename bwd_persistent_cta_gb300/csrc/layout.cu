@@ -84,13 +84,25 @@ template <typename T>
 __device__ __forceinline__ void pack_job_rows(const PackJob& J, int blk, int nblk) {
   const T* W = static_cast<const T*>(J.in);
   T* out = static_cast<T*>(J.out);
-  const int64_t total = static_cast<int64_t>(4) * J.H * J.K;
+  // 16-byte vectors when the rows allow it (K and ld_out multiples of the
+  // vector, 16-byte aligned bases), else one element at a time
+  constexpr int V = 16 / static_cast<int>(sizeof(T));
+  const bool vec = J.K % V == 0 && J.ld_out % V == 0 && (reinterpret_cast<uintptr_t>(W) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+  const int per_row = vec ? J.K / V : J.K;
+  const int64_t total = static_cast<int64_t>(4) * J.H * per_row;
   for (int64_t i = static_cast<int64_t>(blk) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(nblk) * blockDim.x) {
-    const int row = static_cast<int>(i / J.K), k = static_cast<int>(i - static_cast<int64_t>(row) * J.K);
+    const int row = static_cast<int>(i / per_row), c = static_cast<int>(i - static_cast<int64_t>(row) * per_row);
     const int u = row >> 2, sb = J.map[row & 3];
-    out[static_cast<int64_t>(row) * J.ld_out + k] =
-        sb >= 0 ? W[(static_cast<int64_t>(sb) * J.H + u) * J.K + k] : from_f<T>(0.0f);
+    if (vec) {
+      const uint4 v = sb >= 0 ? *reinterpret_cast<const uint4*>(W + (static_cast<int64_t>(sb) * J.H + u) * J.K + c * V)
+                              : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(out + static_cast<int64_t>(row) * J.ld_out + c * V) = v;
+    } else {
+      out[static_cast<int64_t>(row) * J.ld_out + c] =
+          sb >= 0 ? W[(static_cast<int64_t>(sb) * J.H + u) * J.K + c] : from_f<T>(0.0f);
+    }
   }
 }
 
