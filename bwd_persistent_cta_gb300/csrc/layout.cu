@@ -15,65 +15,13 @@ namespace rnn {
 
 namespace {
 
-template <typename T>
-__global__ void pack_rows_kernel(const T* __restrict__ W, int H, int K, int4 src,
-                                 T* __restrict__ out, int64_t ld_out) {
-  // out[(4u+s)*ld + k] = W[(src[s]*H + u)*K + k]
-  const int row = blockIdx.y;               // 4u + s
-  const int u = row >> 2, s = row & 3;
-  const int sb = s == 0 ? src.x : s == 1 ? src.y : s == 2 ? src.z : src.w;
-  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < K; k += gridDim.x * blockDim.x) {
-    T v = sb >= 0 ? W[(static_cast<int64_t>(sb) * H + u) * K + k] : from_f<T>(0.0f);
-    out[static_cast<int64_t>(row) * ld_out + k] = v;
-  }
-}
-
-template <typename T>
-__global__ void pack_rows_t_kernel(const T* __restrict__ W, int H, int K, int4 src,
-                                   T* __restrict__ out, int64_t ld_out) {
-  // out[k*ld + 4u+s] = W[(src[s]*H + u)*K + k], through a 32x33 tile.
-  __shared__ T tile[32][33];
-  const int r0 = blockIdx.y * 32;           // packed row block (4u+s)
-  const int k0 = blockIdx.x * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
-  for (int i = ty; i < 32; i += 8) {
-    const int row = r0 + i, k = k0 + tx;
-    T v = from_f<T>(0.0f);
-    if (row < 4 * H && k < K) {
-      const int u = row >> 2, s = row & 3;
-      const int sb = s == 0 ? src.x : s == 1 ? src.y : s == 2 ? src.z : src.w;
-      if (sb >= 0) v = W[(static_cast<int64_t>(sb) * H + u) * K + k];
-    }
-    tile[i][tx] = v;
-  }
-  __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int k = k0 + i, row = r0 + tx;
-    if (k < K && row < 4 * H) out[static_cast<int64_t>(k) * ld_out + row] = tile[tx][i];
-  }
-}
-
-template <typename T>
-__global__ void pack_bias_kernel(const T* __restrict__ b, int H, int4 src, float* __restrict__ out) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= 4 * H) return;
-  const int u = i >> 2, s = i & 3;
-  const int sb = s == 0 ? src.x : s == 1 ? src.y : s == 2 ? src.z : src.w;
-  out[i] = (sb >= 0 && b != nullptr) ? to_f<T>(b[static_cast<int64_t>(sb) * H + u]) : 0.0f;
-}
-
-__global__ void bias_grad_scatter_kernel(const float* __restrict__ db, int H, int4 dst,
-                                         float* __restrict__ out) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= 4 * H) return;
-  const int u = i >> 2, s = i & 3;
-  const int d = s == 0 ? dst.x : s == 1 ? dst.y : s == 2 ? dst.z : dst.w;
-  if (d >= 0) out[static_cast<int64_t>(d) * H + u] = db[i];
-}
-
 // Several layout jobs in one launch: job j takes blocks [start[j], start[j+1])
-// and walks its elements with a stride of its block count.  The bodies are the
-// ones of the single-job kernels above (same index maps).
+// and walks its elements with a stride of its block count.
+//   PACK_ROWS    out[(4u+s)*ld + k] = W[(map[s]*H + u)*K + k]   (zero for map -1)
+//   PACK_ROWS_T  out[k*ld + 4u+s]   = the same, through a 32x33 tile
+//   PACK_BIAS    out[4u+s] = b[map[s]*H + u]                     (fp32 out)
+//   SCATTER_DB   out[map[s]*H + u] = db[4u+s]                    (fp32)
+//   H0_TO_Y      Y[slot][b][dir*H + u] = h0[b][u], slot 0 (forward) / T+1 (reverse)
 struct PackBatchArgs {
   int n;
   int start[kMaxPackJobs + 1];
@@ -187,16 +135,6 @@ __global__ void seq_copy_kernel(const Ti* __restrict__ in, To* __restrict__ out,
   }
 }
 
-template <typename T>
-__global__ void states_to_y_kernel(const T* __restrict__ h0, T* __restrict__ Y, int T_, int B, int H,
-                                   int D, int dir) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= B * H) return;
-  const int b = i / H, u = i % H;
-  const int slot = dir == 0 ? 0 : T_ + 1;
-  Y[(static_cast<int64_t>(slot) * B + b) * D * H + dir * H + u] = h0 ? h0[i] : from_f<T>(0.0f);
-}
-
 // Recomputation of the LSTM cell states from the saved gate activations
 // (poplibs Lstm.cpp recomputeCellAndTanhImpl: prevCellState * forgetGate +
 // inputGate * candidate, before the backward pass): one thread per (direction,
@@ -247,51 +185,6 @@ int check_launch() {
 
 }  // namespace
 
-int launch_pack_rows(const void* W, int G, int H, int K, const int* slot_src, int is_bf16,
-                     void* out, int64_t ld_out, int transpose, cudaStream_t s) {
-  (void)G;
-  const int4 src = make_int4(slot_src[0], slot_src[1], slot_src[2], slot_src[3]);
-  if (!transpose) {
-    dim3 grid((K + 255) / 256 > 8 ? 8 : (K + 255) / 256, 4 * H);
-    if (is_bf16)
-      pack_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(W), H, K, src, static_cast<__nv_bfloat16*>(out), ld_out);
-    else
-      pack_rows_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(W), H, K, src,
-                                                   static_cast<float*>(out), ld_out);
-  } else {
-    dim3 grid((K + 31) / 32, (4 * H + 31) / 32);
-    dim3 block(32, 8);
-    if (is_bf16)
-      pack_rows_t_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(W), H, K, src, static_cast<__nv_bfloat16*>(out), ld_out);
-    else
-      pack_rows_t_kernel<float><<<grid, block, 0, s>>>(static_cast<const float*>(W), H, K, src,
-                                                       static_cast<float*>(out), ld_out);
-  }
-  return check_launch();
-}
-
-int launch_pack_bias(const void* b, int H, const int* slot_src, int is_bf16, float* out,
-                     cudaStream_t s) {
-  const int4 src = make_int4(slot_src[0], slot_src[1], slot_src[2], slot_src[3]);
-  const int n = 4 * H;
-  if (is_bf16)
-    pack_bias_kernel<__nv_bfloat16><<<(n + 255) / 256, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(b), H, src, out);
-  else
-    pack_bias_kernel<float><<<(n + 255) / 256, 256, 0, s>>>(static_cast<const float*>(b), H, src, out);
-  return check_launch();
-}
-
-int launch_bias_grad_scatter(const float* db, int H, const int* slot_dst, int is_second, float* out,
-                             cudaStream_t s) {
-  (void)is_second;
-  const int4 dst = make_int4(slot_dst[0], slot_dst[1], slot_dst[2], slot_dst[3]);
-  bias_grad_scatter_kernel<<<(4 * H + 255) / 256, 256, 0, s>>>(db, H, dst, out);
-  return check_launch();
-}
-
 int launch_seq_transpose(const void* in, void* out, int T, int B, int F, int in_bf16, int out_bf16,
                          int in_batch_first, int out_batch_first, int64_t out_ld, cudaStream_t s, const int* len) {
   const int64_t rows = static_cast<int64_t>(T) * B;
@@ -316,18 +209,6 @@ int launch_seq_transpose(const void* in, void* out, int T, int B, int F, int in_
   else if (out_bf16) RNN_SEQ_COPY(float, __nv_bfloat16);
   else RNN_SEQ_COPY(float, float);
 #undef RNN_SEQ_COPY
-  return check_launch();
-}
-
-int launch_states_to_y(const void* h0, void* Y, int T, int B, int H, int D, int dir, int is_bf16,
-                       cudaStream_t s) {
-  const int n = B * H;
-  if (is_bf16)
-    states_to_y_kernel<__nv_bfloat16><<<(n + 255) / 256, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(h0), static_cast<__nv_bfloat16*>(Y), T, B, H, D, dir);
-  else
-    states_to_y_kernel<float><<<(n + 255) / 256, 256, 0, s>>>(static_cast<const float*>(h0),
-                                                              static_cast<float*>(Y), T, B, H, D, dir);
   return check_launch();
 }
 

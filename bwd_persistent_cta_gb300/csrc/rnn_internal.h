@@ -148,12 +148,8 @@ int make_tmap_bf16_4d(void* map, const void* ptr, const uint64_t* dims, const ui
                       const uint32_t* box);
 
 // layout / cast / pack kernels (layout.cu)
-// slot_src[s] = index of the user's gate block for internal slot s (-1 = zero)
-int launch_pack_rows(const void* W, int G, int H, int K, const int* slot_src, int is_bf16,
-                     void* out, int64_t ld_out, int transpose, cudaStream_t s);
-int launch_pack_bias(const void* b, int H, const int* slot_src, int is_bf16, float* out,
-                     cudaStream_t s);
-// len (optional, device [B]): output rows (t, b) with t >= len[b] are zero.
+// Sequence copy [T,B,F] <-> [B,T,F] with casts; len (optional, device [B]):
+// output rows (t, b) with t >= len[b] are zero.
 int launch_seq_transpose(const void* in, void* out, int T, int B, int F, int in_bf16,
                          int out_bf16, int in_batch_first, int out_batch_first,
                          int64_t out_ld, cudaStream_t s, const int* len = nullptr);
@@ -182,10 +178,6 @@ struct PackBatch {
   }
 };
 int launch_pack_batch(const PackBatch& pb, int is_bf16, cudaStream_t s);
-int launch_states_to_y(const void* h0, void* Y, int T, int B, int H, int D, int dir,
-                       int is_bf16, cudaStream_t s);
-int launch_bias_grad_scatter(const float* db, int H, const int* slot_dst, int is_second,
-                             float* out, cudaStream_t s);
 int launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
 // LSTM cell states c_t of every step from the saved gate activations
 // ([D][T, B, 4H], slots i, f, g, o) and c0 ([D, B, H] or null = zero) into C
