@@ -60,6 +60,7 @@ _SIGS = {
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
     "rnn_debug_tc_plans": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+    "rnn_debug_simt_plan": (ctypes.c_int, [ctypes.c_int] * 9 + [ctypes.POINTER(ctypes.c_int)]),
     "rnn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "rnn_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "rnn_get_timing": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]),
@@ -211,6 +212,16 @@ def rnn_debug_tc_plans(mode: int, bwd: int, hidden: int, batch: int, ndir: int, 
                                  int(max_out))
     keys = ("ks", "nb", "ctas", "npad", "pp", "w_tmem", "smem")
     return [dict(zip(keys, buf[7 * i:7 * i + 7])) for i in range(n)]
+
+
+def rnn_debug_simt_plan(mode: int, reset_after: int, is_bf16: int, bwd: int, hidden: int, batch: int, ndir: int,
+                        num_sms: int, dwhh: int = 0):
+    """The SIMT persistent kernel's plan for one launch shape (a dict), or None."""
+    buf = (ctypes.c_int * 7)()
+    ok = lib().rnn_debug_simt_plan(int(mode), int(reset_after), int(is_bf16), int(bwd), int(hidden), int(batch),
+                                   int(ndir), int(num_sms), int(dwhh), buf)
+    keys = ("nu", "nblk", "pp", "stream", "smem", "dwhh_default", "dwhh_possible")
+    return dict(zip(keys, buf[:7])) if ok else None
 
 
 def rnn_debug_skip_arrival(handle, cta: int) -> int:

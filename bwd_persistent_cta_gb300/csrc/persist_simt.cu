@@ -1211,6 +1211,24 @@ bool persist_simt_dwhh_ok(const PersistArgs& a, int num_sms, bool hidden_only) {
   return false;
 }
 
+extern "C" int rnn_debug_simt_plan(int mode, int reset_after, int is_bf16, int bwd, int hidden, int batch,
+                                   int ndir, int num_sms, int dwhh, int* out) {
+  if (!out) return 0;
+  PersistArgs a;
+  a.mode = mode; a.reset_after = reset_after; a.is_bf16 = is_bf16;
+  a.H = hidden; a.B = batch; a.D = ndir; a.ndir = ndir;
+  float probe = 0.f;
+  if (dwhh) a.dwhh = &probe;   // only tested for null by the planner
+  SimtPlan pl;
+  if (make_plan(a, bwd != 0, num_sms, &pl) != 0) return 0;
+  out[0] = pl.NU; out[1] = pl.nblk; out[2] = pl.PP; out[3] = pl.stream ? 1 : 0;
+  out[4] = static_cast<int>(pl.smem);
+  a.dwhh = nullptr;
+  out[5] = persist_simt_dwhh_ok(a, num_sms, true) ? 1 : 0;
+  out[6] = persist_simt_dwhh_ok(a, num_sms, false) ? 1 : 0;
+  return 1;
+}
+
 int launch_persist_fwd_simt(const PersistArgs& a, cudaStream_t s, int num_sms) {
   return launch_simt(a, false, s, num_sms);
 }

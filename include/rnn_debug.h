@@ -38,6 +38,15 @@ rnn_status_t rnn_debug_gemm(int M, int N, int K, const void* A, int64_t lda, int
  * written (at most max_out). */
 int rnn_debug_tc_plans(int mode, int bwd, int hidden, int batch, int ndir, int num_sms, int* out, int max_out);
 
+/* Planner hook: the SIMT persistent kernel's plan for one launch shape (host
+ * arithmetic only).  dwhh != 0 plans with the interleaved dW_hh accumulator.
+ * out[0..6] = {units per CTA, CTAs per direction, pairs per thread, weights
+ * streamed (1) or resident (0), shared memory bytes, interleaved dW_hh taken
+ * by default (mode 1), interleaved dW_hh possible at all (mode 2)}.  Returns 1,
+ * or 0 when the kernel cannot take the shape. */
+int rnn_debug_simt_plan(int mode, int reset_after, int is_bf16, int bwd, int hidden, int batch, int ndir,
+                        int num_sms, int dwhh, int* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -73,3 +73,27 @@ def test_large_batch_takes_batch_parts(R):
     # hidden 512, batch 1000: 4 parts of 250 rows leave at most a K split of 2
     # on the 152 SMs, i.e. 16 pairs per thread: no tensor-core plan
     assert R.rnn_debug_tc_plans(LSTM, 0, 512, 1000, 1, SMS) == []
+
+
+# SIMT persistent kernels: units per CTA from the cost model (exchange weighted
+# as 500 serial FMAs, calibrated on GB300), and where the interleaved weight
+# update is taken by default (several CTAs per direction and at most 16
+# item-batch passes per thread per step).
+@pytest.mark.parametrize("args,nblk_gt1,dw_default", [
+    ((LSTM, 0, 0, 1, 32, 4, 1), False, False),     # fp32 T16 B4 H32: one CTA (148 vs 165 us with it)
+    ((GRU, 0, 1, 1, 128, 8, 1), True, True),       # reset-before bf16: 8+ CTAs (30 -> 12 us per step)
+    ((GRU, 1, 0, 1, 128, 16, 1), True, True),      # 1172 -> 1143 us per step with the interleave
+    ((LSTM, 0, 0, 1, 256, 8, 2), True, False),     # 4 units x 8 rows = 32 passes: 974 vs 994 us
+])
+def test_simt_plan_choice(R, args, nblk_gt1, dw_default):
+    p = R.rnn_debug_simt_plan(*args, num_sms=SMS)
+    assert p is not None and not p["stream"]
+    assert (p["nblk"] > 1) == nblk_gt1
+    assert bool(p["dwhh_default"]) == dw_default
+    assert p["dwhh_possible"]
+
+
+def test_simt_streams_weights_that_do_not_fit(R):
+    p = R.rnn_debug_simt_plan(LSTM, 0, 1, 0, 2048, 8, 1, SMS)
+    assert p is not None and p["stream"] and p["nblk"] <= SMS
+    assert not R.rnn_debug_simt_plan(LSTM, 0, 1, 1, 2048, 8, 1, SMS)["dwhh_possible"]
