@@ -1,8 +1,9 @@
 /*
  * rnn.h - C ABI of the GB300 (sm_103a) multi-timestep LSTM / GRU library.
  *
- * One layer stack (1..8 layers, uni- or bidirectional) of LSTM or GRU cells,
- * run forward over a whole sequence and back-propagated through time.  The
+ * One layer stack (1..8 layers, uni- or bidirectional) of LSTM, GRU or plain
+ * RNN cells, run forward over a whole sequence and back-propagated through
+ * time.  The
  * three-phase split (forward, backward-data, backward-weights) follows the
  * cuDNN RNN calls that SystemDS LibMatrixCuDNN.java makes in ``lstm`` and
  * ``lstmBackward`` (cudnnRNNForwardTraining, cudnnRNNBackwardData,
@@ -144,7 +145,9 @@ rnn_status_t rnn_forward(rnn_handle_t handle, const void* x, const void* hx, con
  *   y     forward output; accepted for interface symmetry, the reserve holds
  *         the copy the kernels read (may be NULL)
  *   dy    [T,B,D*H] (device, in)     dhy, dcy [L*D,B,H] (device, in, may be NULL)
- *   w     (device, in)               hx, cx: accepted for symmetry (may be NULL)
+ *   w     (device, in)               hx: accepted for symmetry (may be NULL)
+ *   cx    (device, in, may be NULL = zero) read only with recomputation
+ *         (rnn_set_recomputation): it must then be the cx of rnn_forward
  *   dx    [T,B,I] (device, out)      dhx, dcx [L*D,B,H] (device, out, may be NULL)
  * Writes the gate and bias gradients into the reserve for
  * rnn_backward_weights. */
@@ -156,8 +159,10 @@ rnn_status_t rnn_backward_data(rnn_handle_t handle, const void* y, const void* d
 /* Weight gradients dW_ih = sum_t dA_t x_t^T, dW_hh = sum_t dA^h_t h_{t-1}^T,
  * db = sum_t dA_t (GRU resetAfter also db_h = sum_t dA^h_t), summed over the
  * batch, written (overwritten, never accumulated) into dw: fp32, same layout
- * as w.  Needs the reserve after rnn_backward_data.  x, hx, y: accepted for
- * symmetry with cudnnRNNBackwardWeights; the reserve holds what is read. */
+ * as w.  Needs the reserve after rnn_backward_data.  x (device, in, not NULL)
+ * is read: it is the input operand of layer 0's dW_ih, and must be the x of
+ * rnn_forward.  hx, y: accepted for symmetry with cudnnRNNBackwardWeights (may
+ * be NULL); the reserve holds the states and gate gradients that are read. */
 rnn_status_t rnn_backward_weights(rnn_handle_t handle, const void* x, const void* hx,
                                   const void* y, void* workspace, const void* reserve,
                                   void* dw, void* stream);
