@@ -252,7 +252,8 @@ int rnn_selected_algo(rnn_handle_t handle);
  * tensor-core kernel and the backward on the SIMT kernel: a bf16 LSTM or GRU
  * resetAfter layer whose backward has no tensor-core plan (e.g. hidden 2048,
  * where the forward keeps part of its weight tile in tensor memory and the
- * rest in shared memory). */
+ * rest in shared memory), and bf16 GRU reset-before from batch 4 (its
+ * forward's two exchanges per step on the tensor cores). */
 int rnn_selected_fwd_algo(rnn_handle_t handle);
 
 /* Test hook for the timeout path: CTA ``cta`` (>= 0) of the next persistent
@@ -263,8 +264,9 @@ rnn_status_t rnn_debug_skip_arrival(rnn_handle_t handle, int cta);
 /* Per-kernel-class timing with CUDA events recorded on the launching stream
  * around every launch (off by default; costs two event records per launch).
  * Classes: 0 persistent forward, 1 persistent backward, 2 input-projection
- * GEMM, 3 input-gradient GEMM, 4 weight-gradient GEMMs, 5 layout / pack
- * kernels.  rnn_get_timing waits for the recorded events, writes the summed
+ * GEMM, 3 input-gradient GEMM, 4 weight-gradient GEMMs (with their split-K
+ * reduction), 5 reserved for the layout / pack kernels, which are not timed
+ * (it reads 0).  rnn_get_timing waits for the recorded events, writes the summed
  * milliseconds (ms[6]) and launch counts (n[6]) since the last read, and
  * clears them.  Either output pointer may be NULL. */
 #define RNN_TIMING_CLASSES 6
