@@ -230,6 +230,7 @@ rnn_status_t check_desc(const rnn_desc_t* d) {
   if (d->num_layers < 1 || d->num_layers > 8) return RNN_BAD_PARAM;
   if (d->seq_len < 1 || d->batch < 1 || d->input_size < 1 || d->hidden_size < 1) return RNN_BAD_PARAM;
   if (d->bidirectional != 0 && d->bidirectional != 1) return RNN_BAD_PARAM;
+  if (d->reset_after != 0 && d->reset_after != 1) return RNN_BAD_PARAM;
   if (d->batch_first != 0 && d->batch_first != 1) return RNN_BAD_PARAM;
   if (d->algo < RNN_ALGO_AUTO || d->algo > RNN_ALGO_PERSIST_SIMT) return RNN_BAD_PARAM;
   const int G = d->mode == RNN_LSTM ? 4 : (d->mode == RNN_GRU ? 3 : 1);

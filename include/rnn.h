@@ -87,7 +87,7 @@ typedef struct {
   int gate_order[4];   /* block k of every per-gate matrix holds canonical gate
                           gate_order[k] (LSTM 0..3 = i,f,g,o; GRU 0..2 = r,z,n;
                           plain RNN: one gate, only 0).  All zero = canonical.      */
-  int reset_after;     /* GRU only: 1 = resetAfter form, 0 = reset-before           */
+  int reset_after;     /* 0 or 1; GRU only: 1 = resetAfter form, 0 = reset-before */
   int bidirectional;   /* 0 or 1                                                    */
   int num_layers;      /* 1..8                                                      */
   int seq_len;         /* T >= 1                                                    */
@@ -103,9 +103,14 @@ typedef struct rnn_handle_s* rnn_handle_t;
 
 /* Validate ``desc`` and make a handle.  Allocates the handle's small device
  * area on the current device (which the handle is then bound to).
- * Returns RNN_BAD_PARAM for an invalid descriptor, RNN_NOT_SUPPORTED when the
- * current GPU is not sm_103 or the forced algo cannot take the shape,
- * RNN_CUDA_ERROR when the device allocation fails. */
+ * Returns RNN_BAD_PARAM for an invalid descriptor (a field outside the range
+ * given above, a gate_order that is not a permutation of 0..G-1, or
+ * seq_len * batch above 2^30), checked before any device call;
+ * RNN_NOT_SUPPORTED when input_size or hidden_size is not a multiple of 8
+ * (bf16) or 4 (fp32) - rows are moved in 16-byte vectors - when the current
+ * GPU is not sm_103, or when the forced algo cannot take the shape;
+ * RNN_CUDA_ERROR when the device allocation fails (no device included).
+ * ``*handle`` is NULL after any failure. */
 rnn_status_t rnn_create(const rnn_desc_t* desc, rnn_handle_t* handle);
 
 /* Free the handle and its device area.  NULL is accepted. */

@@ -72,3 +72,128 @@ def test_bad_descriptor_rejected_before_any_device_call(lib):
     d.num_layers = 1
     d.gate_order[0], d.gate_order[1], d.gate_order[2], d.gate_order[3] = 0, 0, 1, 2
     assert lib.rnn_create(ctypes.byref(d), ctypes.byref(h)) == R.RNN_BAD_PARAM
+
+
+# ---------------------------------------------------------------------------
+# the header and the binding agree (a drift here is a silent ABI mismatch)
+# ---------------------------------------------------------------------------
+def _header_text():
+    txt = ""
+    for h in ("rnn.h", "rnn_debug.h"):
+        txt += open(os.path.join(ROOT, "include", h)).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return re.sub(r"//[^\n]*", "", txt)
+
+
+def test_binding_argument_counts_match_header():
+    import bwd_persistent_cta_gb300 as R
+    protos = re.findall(r"\b(rnn_[a-z_]+)\s*\(([^()]*)\)\s*;", _header_text())
+    assert len(protos) >= 20
+    for name, args in protos:
+        args = args.strip()
+        n = 0 if args in ("", "void") else args.count(",") + 1
+        assert name in R._SIGS, name
+        assert len(R._SIGS[name][1]) == n, (name, n, len(R._SIGS[name][1]))
+
+
+def test_descriptor_struct_matches_header():
+    import bwd_persistent_cta_gb300 as R
+    body = re.search(r"typedef struct\s*\{(.*?)\}\s*rnn_desc_t\s*;", _header_text(), flags=re.S).group(1)
+    fields = re.findall(r"\bint\s+([a-z_]+)\s*(?:\[(\d+)\])?\s*;", body)
+    assert [f for f, _ in fields] == [f for f, _ in R.rnn_desc_t._fields_]
+    assert ctypes.sizeof(R.rnn_desc_t) == 4 * sum(int(n) if n else 1 for _, n in fields)
+    for (name, n), (_, ct) in zip(fields, R.rnn_desc_t._fields_):
+        assert ctypes.sizeof(ct) == 4 * (int(n) if n else 1), name
+
+
+def test_enum_values_match_header():
+    import bwd_persistent_cta_gb300 as R
+    vals = dict(re.findall(r"\b(RNN_[A-Z0-9_]+)\s*=\s*(\d+)", _header_text()))
+    assert {"RNN_OK", "RNN_BF16", "RNN_GRU", "RNN_ALGO_PERSIST_SIMT"} <= set(vals)
+    for name, v in vals.items():
+        assert getattr(R, name) == int(v), name
+
+
+# ---------------------------------------------------------------------------
+# descriptor validation: every rule of rnn_create is checked on the host
+# before any device call, so each answer is the same with or without a GPU
+# ---------------------------------------------------------------------------
+def _desc(R, **kw):
+    d = R.rnn_desc_t()
+    base = dict(mode=R.RNN_LSTM, reset_after=0, bidirectional=0, num_layers=1, seq_len=4, batch=2, input_size=8,
+                hidden_size=8, dtype=R.RNN_BF16, batch_first=0, algo=R.RNN_ALGO_AUTO)
+    base.update(kw)
+    order = base.pop("gate_order", (0, 0, 0, 0))
+    for k, v in base.items():
+        setattr(d, k, v)
+    for k in range(4):
+        d.gate_order[k] = order[k]
+    return d
+
+
+BAD = [
+    dict(mode=4), dict(mode=-1), dict(dtype=2), dict(num_layers=0), dict(num_layers=9), dict(seq_len=0),
+    dict(batch=0), dict(input_size=0), dict(hidden_size=-8), dict(bidirectional=2), dict(reset_after=2),
+    dict(batch_first=-1), dict(algo=3), dict(algo=-1),
+    dict(gate_order=(1, 0, 3, 3)), dict(gate_order=(0, 1, 2, 4)),
+    dict(mode=1, gate_order=(0, 1, 3, 0)), dict(mode=1, gate_order=(2, 2, 1, 0)),
+    dict(mode=2, gate_order=(1, 0, 0, 0)),
+    dict(seq_len=1 << 16, batch=1 << 15),          # T * B = 2^31 rows
+]
+UNSUPPORTED = [dict(hidden_size=12), dict(input_size=4), dict(dtype=0, hidden_size=6), dict(dtype=0, input_size=2)]
+VALID = [dict(), dict(mode=1, gate_order=(2, 0, 1, 0)), dict(gate_order=(3, 2, 1, 0)), dict(dtype=0, hidden_size=4,
+         input_size=4), dict(mode=3, num_layers=8, bidirectional=1, batch_first=1, algo=2),
+         dict(seq_len=1 << 15, batch=1 << 15)]
+
+
+@pytest.mark.parametrize("kw", BAD, ids=[str(k) for k in BAD])
+def test_invalid_descriptor_is_bad_param(lib, kw):
+    import bwd_persistent_cta_gb300 as R
+    h = ctypes.c_void_p(16)
+    assert lib.rnn_create(ctypes.byref(_desc(R, **kw)), ctypes.byref(h)) == R.RNN_BAD_PARAM
+    assert not h.value
+    # the allocation-free forward validates the same descriptor first
+    assert lib.rnn_forward_noalloc(ctypes.byref(_desc(R, **kw)), 16, None, None, 16, 16, None, None, 0,
+                                   None) == R.RNN_BAD_PARAM
+
+
+@pytest.mark.parametrize("kw", UNSUPPORTED, ids=[str(k) for k in UNSUPPORTED])
+def test_unaligned_rows_not_supported(lib, kw):
+    import bwd_persistent_cta_gb300 as R
+    h = ctypes.c_void_p(16)
+    assert lib.rnn_create(ctypes.byref(_desc(R, **kw)), ctypes.byref(h)) == R.RNN_NOT_SUPPORTED
+    assert not h.value
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-device path")
+@pytest.mark.parametrize("kw", VALID, ids=[str(k) for k in VALID])
+def test_valid_descriptor_reaches_the_device_query(lib, kw):
+    import bwd_persistent_cta_gb300 as R
+    h = ctypes.c_void_p(16)
+    assert lib.rnn_create(ctypes.byref(_desc(R, **kw)), ctypes.byref(h)) in (R.RNN_CUDA_ERROR, R.RNN_NOT_SUPPORTED)
+    assert not h.value
+
+
+def test_null_arguments(lib):
+    import bwd_persistent_cta_gb300 as R
+    h = ctypes.c_void_p()
+    assert lib.rnn_create(None, ctypes.byref(h)) == R.RNN_BAD_PARAM
+    assert lib.rnn_create(ctypes.byref(_desc(R)), None) == R.RNN_BAD_PARAM
+    assert lib.rnn_forward_noalloc(None, 16, None, None, 16, 16, None, None, 0, None) == R.RNN_BAD_PARAM
+    assert lib.rnn_destroy(None) == R.RNN_OK
+    bad = R.RNN_BAD_PARAM
+    assert lib.rnn_get_sizes(None, None, None, None) == bad
+    assert lib.rnn_forward(None, *([None] * 10)) == bad
+    assert lib.rnn_backward_data(None, *([None] * 13)) == bad
+    assert lib.rnn_backward_weights(None, *([None] * 7)) == bad
+    assert lib.rnn_sync_status(None, None) == bad
+    assert lib.rnn_set_timeout_ns(None, 1) == bad
+    assert lib.rnn_set_seq_lengths(None, None) == bad
+    assert lib.rnn_set_cell_clip(None, 1, -1.0, 1.0) == bad
+    assert lib.rnn_set_recomputation(None, 0) == bad
+    assert lib.rnn_set_interleaved_dw(None, 1) == bad
+    assert lib.rnn_set_timing(None, 1) == bad
+    assert lib.rnn_get_timing(None, None, None) == bad
+    assert lib.rnn_debug_skip_arrival(None, 0) == bad
+    for q in ("rnn_interleaved_dw_active", "rnn_launch_count", "rnn_selected_algo", "rnn_selected_fwd_algo"):
+        assert getattr(lib, q)(None) == 0, q
