@@ -130,23 +130,32 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
+        with open(self.path) as f:
+            out = parse_clock_lines(f)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return out
+
+
+def parse_clock_lines(lines):
+    """Summarise nvidia-smi samples of ClockSampler.QUERY (csv, no header, no
+    units): median SM clock, the highest max clock, and every throttle reason
+    seen active in any sample."""
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            smax.append(float(f[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ---------------------------------------------------------------------------
@@ -220,6 +229,19 @@ def load_peaks():
         d = json.load(open(p))
         return {"bf16_tflops": d.get("bf16_tflops"), "hbm_gbs": d.get("hbm_gbs"), "src": "measured"}
     return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "src": "fallback"}
+
+
+def workload_config(wl, lengths, world: int) -> dict:
+    """The ``config`` keys that name the workload; both arms report them."""
+    cfg = {"workload": wl.name, "mode": wl.mode, "reset_after": wl.reset_after, "layers": wl.num_layers,
+           "bidirectional": wl.bidirectional, "seq_len": wl.seq_len, "batch_per_gpu": wl.batch,
+           "input": wl.input_size, "hidden": wl.hidden_size, "seed": wl.seed, "parallelism": f"replicas{world}",
+           "recompute_cell_states": wl.recompute}
+    if lengths is not None:
+        cfg["seq_lengths"] = {"min": int(min(lengths)), "max": int(max(lengths)),
+                              "valid_frac": float(sum(int(v) for v in lengths)) / (wl.seq_len * wl.batch),
+                              "units": "valid timesteps (sum of sequence lengths) x 1"}
+    return cfg
 
 
 # ---------------------------------------------------------------------------
@@ -385,16 +407,9 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "mode": wl.mode, "reset_after": wl.reset_after,
-                       "layers": wl.num_layers, "bidirectional": wl.bidirectional, "seq_len": wl.seq_len,
-                       "batch_per_gpu": wl.batch, "input": wl.input_size, "hidden": wl.hidden_size,
-                       "seed": wl.seed, "parallelism": f"replicas{world}",
+            "config": {**workload_config(wl, inp.lengths, world),
                        "l2": "flushed (256 MiB write) before every timed step",
-                       "reserve_bytes": rnn.reserve_bytes, "recompute_cell_states": wl.recompute,
-                       **({} if inp.lengths is None else {
-                           "seq_lengths": {"min": int(np.min(inp.lengths)), "max": int(np.max(inp.lengths)),
-                                           "valid_frac": valid_frac,
-                                           "units": "valid timesteps (sum of sequence lengths) x 1"}})},
+                       "reserve_bytes": rnn.reserve_bytes},
             "tflops": tflops, "tflops_unit": "TFLOP/s (algorithmic, sum over layers/dirs of 3*2*G*H*(I+H)*B*T)",
             "e2e": {"value": job_throughput(wl.seq_len * wl.batch * valid_frac, world, e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": int(x.numel() * x.element_size() +
@@ -428,10 +443,10 @@ def run_reference(args):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(args.steps, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": wl.name, "seq_len": wl.seq_len, "batch_per_gpu": wl.batch,
-                       "hidden": wl.hidden_size, "input": wl.input_size},
+            "config": workload_config(wl, synth.make_lengths(wl), args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{wl.name} with {cols} of {wl.batch} batch columns per step, fwd+bwd"},
+                             "sample": f"{wl.name} with {cols} of {wl.batch} batch columns per step, "
+                                       f"{'fwd' if wl.forward_only else 'fwd+bwd'}"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

@@ -151,6 +151,17 @@ class Inputs:
     clip: Optional[Tuple[float, float]] = None   # LSTM cell clipping bounds, or None
 
 
+def make_lengths(wl: Workload) -> Optional[np.ndarray]:
+    """The workload's [B] sequence lengths (None: every sequence has T steps),
+    drawn from a generator of their own so that no other draw depends on them."""
+    if wl.min_len_frac is None:
+        return None
+    T = wl.seq_len
+    gl = torch.Generator(device="cpu").manual_seed(wl.seed + 7919)
+    lo = min(T, int(math.ceil(wl.min_len_frac * T)))
+    return torch.randint(lo, T + 1, (wl.batch,), generator=gl).numpy().astype(np.int64)
+
+
 def make_inputs(wl: Workload, batch_subset: Optional[Sequence[int]] = None) -> Inputs:
     """Draw the workload's inputs.  ``batch_subset`` keeps only those batch
     columns of x, h0, c0 and dy (the draws themselves are unchanged)."""
@@ -184,12 +195,7 @@ def make_inputs(wl: Workload, batch_subset: Optional[Sequence[int]] = None) -> I
         h0 = nrm(wl.state_std, S, B, H).numpy()
         c0 = nrm(wl.state_std, S, B, H).numpy() if wl.mode == LSTM else None
     dy = nrm(wl.dy_std, T, B, wl.dirs * H).numpy()
-    lengths = None
-    if wl.min_len_frac is not None:
-        # a generator of its own, so the draws above do not depend on it
-        gl = torch.Generator(device="cpu").manual_seed(wl.seed + 7919)
-        lo = min(T, int(math.ceil(wl.min_len_frac * T)))
-        lengths = torch.randint(lo, T + 1, (B,), generator=gl).numpy().astype(np.int64)
+    lengths = make_lengths(wl)
     if batch_subset is not None:
         idx = np.asarray(list(batch_subset))
         x, dy = x[:, idx], dy[:, idx]
