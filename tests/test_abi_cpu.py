@@ -197,3 +197,38 @@ def test_null_arguments(lib):
     assert lib.rnn_debug_skip_arrival(None, 0) == bad
     for q in ("rnn_interleaved_dw_active", "rnn_launch_count", "rnn_selected_algo", "rnn_selected_fwd_algo"):
         assert getattr(lib, q)(None) == 0, q
+
+
+C_CALLER = r"""
+#include "rnn.h"
+#include "rnn_debug.h"
+#include <stdio.h>
+int main(void) {
+  rnn_desc_t d = {0};
+  rnn_handle_t h = 0;
+  rnn_status_t rc;
+  d.mode = RNN_GRU; d.reset_after = 1; d.num_layers = 1; d.seq_len = 4; d.batch = 2;
+  d.input_size = 8; d.hidden_size = 8; d.dtype = RNN_BF16; d.algo = RNN_ALGO_AUTO;
+  d.gate_order[0] = 2; d.gate_order[1] = 2;            /* not a permutation */
+  rc = rnn_create(&d, &h);
+  printf("%d %d %s\n", (int)rc, h == 0, rnn_status_string(rc));
+  return rc == RNN_BAD_PARAM && h == 0 && rnn_destroy(0) == RNN_OK ? 0 : 1;
+}
+"""
+
+
+def test_headers_are_plain_c_and_the_library_links_from_c(lib, tmp_path):
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    import bwd_persistent_cta_gb300 as R
+    src, exe = tmp_path / "caller.c", tmp_path / "caller"
+    src.write_text(C_CALLER)
+    libdir = os.path.dirname(R.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-L", libdir, "-lrnn", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.startswith("1 1 RNN_BAD_PARAM")
