@@ -27,6 +27,7 @@
 // every element in split order (deterministic) and applies the epilogue.
 // Every wait is bounded; on timeout the kernel records RNN_TIMEOUT in the
 // status word and leaves its loops.
+#include <atomic>
 #include <cstdlib>
 
 #include "common.cuh"
@@ -388,12 +389,17 @@ int launch_bn(const GemmArgs& g, int S, cudaStream_t s, int num_sms, DevArea* de
   p.timeout_ns = timeout_ns;
   p.splits = S;
   p.ws = static_cast<float*>(g.split_ws);
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory limit is a per-device attribute: set it once on each
+  // device this instantiation launches on (any thread may get here first)
+  static std::atomic<uint64_t> attr_set{0};
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return 3;
+  const uint64_t bit = cur < 64 ? (1ull << cur) : 0ull;
+  if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
     if (cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes<BN>())) != cudaSuccess)
       return 3;
-    attr_set = true;
+    attr_set.fetch_or(bit, std::memory_order_release);
   }
   const int items = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * S;
   const int grid = items < num_sms ? items : num_sms;

@@ -11,7 +11,10 @@
  * A, B: device, in_bf16 ? bf16 : fp32.  C: device, c_bf16 ? bf16 : fp32.
  * bias: device fp32 [N] or NULL.  use_tc = 1 runs the tcgen05 kernel (bf16
  * operands, 16-byte aligned pointers and row strides), 0 the SIMT kernel.
- * Asynchronous on ``stream``; returns an rnn_status_t.
+ * Asynchronous on ``stream``; returns an rnn_status_t.  A test hook: its
+ * split-K scratch and status area are allocated on first use on the device
+ * current then and kept for the process, so call it from one thread and on
+ * one device only.
  */
 #ifndef GB300_RNN_DEBUG_H
 #define GB300_RNN_DEBUG_H
