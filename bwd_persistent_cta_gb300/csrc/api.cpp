@@ -320,6 +320,29 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
 
 }  // namespace rnn
 
+namespace {
+
+// Makes the handle's device current for one call and puts the caller's
+// current device back afterwards (nothing to do when it already is current).
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) { ok = false; return; }
+    if (cur == dev) return;
+    if (cudaSetDevice(dev) != cudaSuccess) { ok = false; return; }
+    prev = cur;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+  DeviceGuard(const DeviceGuard&) = delete;
+  DeviceGuard& operator=(const DeviceGuard&) = delete;
+};
+
+}  // namespace
+
 extern "C" {
 
 const char* rnn_status_string(rnn_status_t s) {
@@ -353,6 +376,7 @@ rnn_status_t rnn_create(const rnn_desc_t* desc, rnn_handle_t* out) {
 
 rnn_status_t rnn_destroy(rnn_handle_t h) {
   if (!h) return RNN_OK;
+  DeviceGuard dg(h->device);
   for (auto& e : h->events) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
   for (auto& e : h->pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
   if (h->dev) cudaFree(h->dev);
@@ -377,6 +401,8 @@ rnn_status_t rnn_set_timeout_ns(rnn_handle_t h, uint64_t ns) {
 
 rnn_status_t rnn_set_seq_lengths(rnn_handle_t h, const int* lengths) {
   if (!h) return RNN_BAD_PARAM;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return RNN_CUDA_ERROR;
   if (!lengths) {
     h->has_len = 0;
     return RNN_OK;
@@ -395,6 +421,8 @@ rnn_status_t rnn_set_seq_lengths(rnn_handle_t h, const int* lengths) {
 
 rnn_status_t rnn_set_recomputation(rnn_handle_t h, int mode) {
   if (!h || mode < 0 || mode > 1) return RNN_BAD_PARAM;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return RNN_CUDA_ERROR;
   h->recompute = h->lstm ? mode : 0;
   fill_layout(h);
   return RNN_OK;
@@ -402,6 +430,8 @@ rnn_status_t rnn_set_recomputation(rnn_handle_t h, int mode) {
 
 rnn_status_t rnn_set_interleaved_dw(rnn_handle_t h, int mode) {
   if (!h || mode < 0 || mode > 2) return RNN_BAD_PARAM;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return RNN_CUDA_ERROR;
   h->dw_mode = mode;
   update_dw_bptt(h);
   fill_layout(h);
@@ -466,6 +496,8 @@ rnn_status_t rnn_debug_skip_arrival(rnn_handle_t h, int cta) {
 
 rnn_status_t rnn_sync_status(rnn_handle_t h, void* stream) {
   if (!h) return RNN_BAD_PARAM;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return RNN_CUDA_ERROR;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return RNN_CUDA_ERROR;
   unsigned int code = 0;
@@ -485,6 +517,8 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
                          void* hy, void* cy, void* workspace, void* reserve, void* stream) {
   if (!h || !x || !w || !y) return RNN_BAD_PARAM;
   if (!workspace) return RNN_BAD_WORKSPACE;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return RNN_CUDA_ERROR;
   const void* ptrs[] = {x, hx, cx, w, y, hy, cy, workspace, reserve};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return RNN_BAD_PARAM;
@@ -575,6 +609,8 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
   (void)y; (void)hx;   // cx: read only with recomputation (the cell states' initial value)
   if (!h || !dy || !w || !dx) return RNN_BAD_PARAM;
   if (!workspace || !reserve) return RNN_BAD_WORKSPACE;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return RNN_CUDA_ERROR;
   const void* ptrs[] = {dy, dhy, dcy, w, cx, dx, dhx, dcx, workspace, reserve};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return RNN_BAD_PARAM;
@@ -662,6 +698,8 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
   (void)hx; (void)y;
   if (!h || !x || !dw) return RNN_BAD_PARAM;
   if (!workspace || !reserve) return RNN_BAD_WORKSPACE;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return RNN_CUDA_ERROR;
   const void* ptrs[] = {x, workspace, reserve, dw};
   for (const void* p : ptrs)
     if (!aligned16(p)) return RNN_BAD_PARAM;

@@ -30,6 +30,10 @@
  *   - All pointers marked "device" are device memory owned by the caller; the
  *     library never frees them.  The handle owns only host metadata and a small
  *     device area (status word, step counters) allocated in rnn_create.
+ *   - A handle belongs to the device that was current in rnn_create.  Each
+ *     call that touches the GPU makes that device current for its duration
+ *     and restores the caller's current device before it returns; ``stream``
+ *     and every device pointer must belong to that device.
  *   - Calls are asynchronous on ``stream`` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream).  Errors found on the host are returned;
  *     errors found on the device (a spin-wait that ran out, RNN_TIMEOUT) are
