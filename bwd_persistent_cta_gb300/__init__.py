@@ -92,9 +92,11 @@ def _p(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream=None) -> int:
+def _stream(stream=None, device=None) -> int:
+    """cudaStream_t of ``stream``, else of the current stream of ``device``
+    (default: the current device)."""
     import torch
-    return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+    return (stream if stream is not None else torch.cuda.current_stream(device)).cuda_stream
 
 
 # --- the C entry points, same names -----------------------------------------
@@ -251,6 +253,8 @@ class RNN:
         import torch
         self.torch = torch
         self.device = torch.device(device if device is not None else "cuda")
+        if self.device.index is None:     # pin the device current now: the handle is bound to it
+            self.device = torch.device("cuda", torch.cuda.current_device())
         d = rnn_desc_t()
         d.mode = {"lstm": RNN_LSTM, "gru": RNN_GRU, "rnn_relu": RNN_RNN_RELU, "rnn_tanh": RNN_RNN_TANH}[mode]
         for k, v in enumerate(gate_order):
@@ -319,7 +323,7 @@ class RNN:
         if d.mode == RNN_LSTM and cy is None:
             cy = torch.empty(self._state_shape(), dtype=self.tdtype, device=self.device)
         rc = rnn_forward(self.handle, _p(x), _p(hx), _p(cx), _p(w), _p(y), _p(hy), _p(cy),
-                         _p(self.workspace), _p(self.reserve) if train else None, _stream(stream))
+                         _p(self.workspace), _p(self.reserve) if train else None, _stream(stream, self.device))
         self._check(rc, "rnn_forward")
         return y, hy, cy
 
@@ -332,7 +336,7 @@ class RNN:
         if d.mode == RNN_LSTM and dcx is None:
             dcx = torch.empty(self._state_shape(), dtype=self.tdtype, device=self.device)
         rc = rnn_backward_data(self.handle, None, _p(dy), _p(dhy), _p(dcy), _p(w), None, _p(cx), _p(dx), _p(dhx),
-                               _p(dcx), _p(self.workspace), _p(self.reserve), _stream(stream))
+                               _p(dcx), _p(self.workspace), _p(self.reserve), _stream(stream, self.device))
         self._check(rc, "rnn_backward_data")
         return dx, dhx, dcx
 
@@ -340,12 +344,12 @@ class RNN:
         torch = self.torch
         dw = torch.empty(self.weight_count, dtype=torch.float32, device=self.device) if dw is None else dw
         rc = rnn_backward_weights(self.handle, _p(x), None, None, _p(self.workspace), _p(self.reserve), _p(dw),
-                                  _stream(stream))
+                                  _stream(stream, self.device))
         self._check(rc, "rnn_backward_weights")
         return dw
 
     def sync(self, stream=None):
-        rc = rnn_sync_status(self.handle, _stream(stream))
+        rc = rnn_sync_status(self.handle, _stream(stream, self.device))
         self._check(rc, "rnn_sync_status")
 
     def set_timeout_ns(self, ns: int):
