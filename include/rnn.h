@@ -39,6 +39,14 @@
  *     errors found on the device (a spin-wait that ran out, RNN_TIMEOUT) are
  *     recorded in the handle's status word and returned by rnn_sync_status.
  *   - No call throws or aborts; every failure is a status code.
+ *   - One handle serves one host thread at a time; different handles may be
+ *     used from different threads (the library's shared plan caches are
+ *     locked).  The recurrent kernels are persistent grids sized to be
+ *     resident at once on an otherwise idle GPU: a call that overlaps other
+ *     kernels holding SMs (another handle's calls on a concurrent stream,
+ *     another client under MPS) may find some of its CTAs not resident, and
+ *     its waits then end in RNN_TIMEOUT rather than a hang.  Order such
+ *     calls on one stream.
  *   - Sequences are seq-major [T, B, F] unless desc.batch_first != 0, in which
  *     case x, y, dy and dx are [B, T, F].  States (hx, cx, hy, cy, dhy, dcy,
  *     dhx, dcx) are [L*D, B, H] with index l*D + d (d = 0 forward, 1 reverse).
