@@ -84,8 +84,9 @@ def oracle_worker(spec: str) -> None:
     print(json.dumps({"times": times, "units_per_rep": units}))
 
 
-def run_oracle_subprocess(wl, budget_s: float, cols: int, reps: int = 1):
-    cores = os.cpu_count() or 1
+def run_oracle_subprocess(wl, budget_s: float, cols: int, reps: int = 1, threads: int = 0):
+    """Time the oracle in a fresh process on ``threads`` host threads (0: all cores)."""
+    cores = threads or os.cpu_count() or 1
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = str(cores)
@@ -402,6 +403,11 @@ def run_ours(args):
                "sample": f"{wl.name} with {cols} of {wl.batch} batch columns, "
                          f"{'fwd' if wl.forward_only else 'fwd+bwd'}, {len(times)} timed repeats in "
                          f"{sum(times):.1f} s after one warm-up (fp64 numpy, all host cores)"}
+        # the same sample on one host thread
+        out1, _ = run_oracle_subprocess(wl, 6.0, cols, reps=2, threads=1)
+        t1 = out1["times"][1:]
+        cpu["single_thread"] = {"value": out1["units_per_rep"] * len(t1) / sum(t1), "cores": 1,
+                                "timed_s": sum(t1)}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,

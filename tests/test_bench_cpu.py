@@ -145,3 +145,12 @@ def test_reference_arm_other_ranks_print_nothing():
     r = _run_reference({"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("threads", [1, 0])
+def test_oracle_timing_subprocess(threads):
+    wl = synth.WORKLOADS["lstm_f32_T16_B4_I32_H32"]
+    out, cores = bench.run_oracle_subprocess(wl, 0.0, 3, reps=2, threads=threads)
+    assert cores == (1 if threads == 1 else (os.cpu_count() or 1))
+    assert len(out["times"]) == 2 and all(t > 0 for t in out["times"])
+    assert out["units_per_rep"] == wl.seq_len * 3
