@@ -19,6 +19,8 @@ step, timed live with CUDA events on its launching stream.  ``e2e`` is the
 same step through the C ABI with the inputs uploaded from pinned host memory
 and the result (dw; y for forward-only workloads) read back inside the timed
 region; dy's upload runs on a copy stream during the forward.
+``us_per_timestep`` is the step time over the sequence length (the per-step
+latency of the forward-only workloads).
 """
 from __future__ import annotations
 
@@ -411,7 +413,8 @@ def run_ours(args):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "ms_per_step": ms, "us_per_timestep": ms * 1e3 / wl.seq_len, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {**workload_config(wl, inp.lengths, world),
                        "l2": "flushed (256 MiB write) before every timed step",
