@@ -31,7 +31,7 @@ Sources (titles and sections of the pages the method is taken from):
     the state gradient by the activation's derivative (ReLU: zero where the
     output is not positive; tanh: 1 - h'^2).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   * LSTM cell clipping (the fragment's clip / dclip on the cell state), when
     enabled with bounds lo < hi: the state is the raw c, and every use of it
     goes through clip(x) = min(max(x, lo), hi) (a NaN stays NaN):
