@@ -349,7 +349,7 @@ const char* rnn_status_string(rnn_status_t s) {
   switch (s) {
     case RNN_OK: return "RNN_OK";
     case RNN_BAD_PARAM: return "RNN_BAD_PARAM: invalid descriptor field or pointer";
-    case RNN_NOT_SUPPORTED: return "RNN_NOT_SUPPORTED: valid but not supported on this GPU / build";
+    case RNN_NOT_SUPPORTED: return "RNN_NOT_SUPPORTED: valid, but the library or GPU cannot run it";
     case RNN_CUDA_ERROR: return "RNN_CUDA_ERROR: a CUDA call failed";
     case RNN_TIMEOUT: return "RNN_TIMEOUT: a device spin-wait ran out of time";
     case RNN_BAD_WORKSPACE: return "RNN_BAD_WORKSPACE: workspace / reserve missing or misaligned";

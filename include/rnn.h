@@ -72,7 +72,7 @@ extern "C" {
 typedef enum {
   RNN_OK = 0,
   RNN_BAD_PARAM = 1,       /* a descriptor field or pointer is invalid         */
-  RNN_NOT_SUPPORTED = 2,   /* valid, but this build / GPU cannot run it        */
+  RNN_NOT_SUPPORTED = 2,   /* valid, but the library or GPU cannot run it      */
   RNN_CUDA_ERROR = 3,      /* a CUDA runtime / driver call failed              */
   RNN_TIMEOUT = 4,         /* a device spin-wait gave up (see rnn_sync_status) */
   RNN_BAD_WORKSPACE = 5,   /* workspace / reserve pointer NULL or misaligned   */
