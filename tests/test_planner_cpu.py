@@ -97,3 +97,43 @@ def test_simt_streams_weights_that_do_not_fit(R):
     p = R.rnn_debug_simt_plan(LSTM, 0, 1, 0, 2048, 8, 1, SMS)
     assert p is not None and p["stream"] and p["nblk"] <= SMS
     assert not R.rnn_debug_simt_plan(LSTM, 0, 1, 1, 2048, 8, 1, SMS)["dwhh_possible"]
+
+
+# Structural invariants over a sweep of shapes: what the kernel itself needs of
+# a plan, independent of the cost ranking.  Each CTA owns 128 output rows of
+# one direction (forward: 32 units x 4 gate slots of h W_hh^T; backward: 128
+# units of dG W_hh), one 1/KS slice of the contraction dimension (forward H,
+# backward 4H, in 64-column sub-tiles) and one batch part; its 256 threads
+# cover the part's (unit, row) pairs of the epilogue PP at a time.
+@pytest.mark.parametrize("mode", [LSTM, GRU])
+@pytest.mark.parametrize("bwd", [0, 1])
+@pytest.mark.parametrize("ndir", [1, 2])
+def test_plan_invariants_sweep(R, mode, bwd, ndir):
+    n_shapes = n_planned = 0
+    for H in (32, 64, 96, 128, 192, 256, 384, 512, 768, 1024, 1536, 2048):
+        for B in (1, 3, 8, 16, 33, 64, 100, 128, 200, 256, 300, 512, 600, 1024):
+            n_shapes += 1
+            plans = R.rnn_debug_tc_plans(mode, bwd, H, B, ndir, SMS, max_out=32)
+            if bwd and H % 128:
+                assert plans == []
+                continue
+            n_planned += bool(plans)
+            rows, K = (H, 4 * H) if bwd else (4 * H, H)
+            seen = set()
+            for p in plans:
+                ks, nb, npad, pp = p["ks"], p["nb"], p["npad"], p["pp"]
+                assert (ks, nb) not in seen
+                seen.add((ks, nb))
+                assert ks in (1, 2, 4, 8, 16) and nb in (1, 2, 4) and pp in (1, 2, 4, 8)
+                assert K % (ks * 64) == 0
+                assert p["ctas"] == (rows // 128) * ks * nb * ndir <= SMS
+                bp = -(-B // nb)
+                assert bp <= 256 and npad == -(-bp // 16) * 16
+                assert nb == 1 or (bp >= 8 and (nb - 1) * bp < B)
+                units = (128 if bwd else 32) // ks
+                assert units >= 1 and units * bp <= 256 * pp
+                assert p["smem"] <= 227 * 1024
+                assert p["w_tmem"] % 2 == 0 and 0 <= p["w_tmem"] <= min(8, K // ks // 64)
+            if ndir == 2 and plans:
+                assert R.rnn_debug_tc_plans(mode, bwd, H, B, 1, SMS, max_out=32)
+    assert n_planned > n_shapes // 4
