@@ -137,3 +137,35 @@ def test_plan_invariants_sweep(R, mode, bwd, ndir):
             if ndir == 2 and plans:
                 assert R.rnn_debug_tc_plans(mode, bwd, H, B, 1, SMS, max_out=32)
     assert n_planned > n_shapes // 4
+
+
+# The SIMT planner over a sweep: units per CTA cover the hidden size with no
+# empty CTA, every CTA of the launch fits on its own SM, the 256 threads cover
+# the (unit, row) pairs PP at a time, a resident weight slice stays within the
+# shared-memory budget, and the interleaved weight update is only offered where
+# the kernel can hold its accumulator (at most 16384 unit x hidden x batch
+# products per CTA) and only taken by default with several CTAs per direction.
+@pytest.mark.parametrize("mode,ra,bf16", [(LSTM, 0, 0), (LSTM, 0, 1), (GRU, 1, 1), (GRU, 0, 0), (GRU, 0, 1),
+                                          (2, 0, 0), (3, 0, 1)])
+@pytest.mark.parametrize("bwd", [0, 1])
+def test_simt_plan_invariants_sweep(R, mode, ra, bf16, bwd):
+    planned = 0
+    for H in (8, 32, 40, 64, 128, 256, 512, 1024, 2048):
+        for B in (1, 2, 5, 8, 16, 32, 64, 128):
+            for ndir in (1, 2):
+                p = R.rnn_debug_simt_plan(mode, ra, bf16, bwd, H, B, ndir, SMS)
+                if p is None:
+                    continue
+                planned += 1
+                nu, nblk, pp = p["nu"], p["nblk"], p["pp"]
+                assert nblk == -(-H // nu) and (nblk - 1) * nu < H
+                assert nblk * ndir <= SMS
+                assert pp in (1, 2, 4, 8) and nu * B <= 256 * pp
+                if not p["stream"]:
+                    assert p["smem"] <= 200 * 1024
+                if p["dwhh_default"]:
+                    assert p["dwhh_possible"] and nblk > 1 and not p["stream"]
+                q = R.rnn_debug_simt_plan(mode, ra, bf16, bwd, H, B, ndir, SMS, dwhh=1)
+                if bwd and q is not None:
+                    assert q["nu"] * H * B <= 16384 and not q["stream"] and q["smem"] <= 200 * 1024
+    assert planned > 0
