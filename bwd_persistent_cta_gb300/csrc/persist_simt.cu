@@ -32,6 +32,8 @@
 // backwardStepImplResetAfter; the LSTM and GRU branches of the persistent
 // backward-data kernel fragment.
 #include <algorithm>
+#include <cstdio>
+#include <cstdlib>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -1112,6 +1114,28 @@ int plan_latency_fwd(const PersistArgs& a, int num_sms, int dev, SimtEntry* e) {
   return 0;
 }
 
+// RNN_TRACE=1: one stderr line per launch shape, when its plan is chosen.
+void trace_entry(const PersistArgs& a, bool bwd, const SimtEntry& e) {
+  const char* env = std::getenv("RNN_TRACE");
+  if (!env || env[0] != '1') return;
+  const char* pass = bwd ? "backward" : "forward";
+  if (e.rc) {
+    std::fprintf(stderr, "[rnn] SIMT %s H=%d B=%d dirs=%d: no plan fits\n", pass, a.H, a.B, a.ndir);
+  } else if (e.lat) {
+    std::fprintf(stderr,
+                 "[rnn] SIMT %s H=%d B=%d dirs=%d: latency mode, %d CTAs of %d units, %d weight rows resident, "
+                 "%zu B shared memory\n",
+                 pass, a.H, a.B, a.ndir, e.lat_nblk * a.ndir, e.lat_NU, e.lat_Rs, e.lat_smem);
+  } else {
+    std::fprintf(stderr,
+                 "[rnn] SIMT %s H=%d B=%d dirs=%d: %d CTAs of %d units, %d pair(s) per thread, weights %s, "
+                 "%zu B shared memory%s\n",
+                 pass, a.H, a.B, a.ndir, e.pl.nblk * a.ndir, e.pl.NU, e.pl.PP,
+                 e.pl.stream ? "streamed from L2" : "resident", e.pl.smem,
+                 a.dwhh ? ", dW_hh accumulated per step" : "");
+  }
+}
+
 // The plan of one launch (cached per shape and device).
 SimtEntry simt_entry(const PersistArgs& a, bool bwd, int num_sms) {
   int dev = 0;
@@ -1139,7 +1163,10 @@ SimtEntry simt_entry(const PersistArgs& a, bool bwd, int num_sms) {
         e.rc = 2;
     }
   }
-  if (e.rc != 3) g_simt[key] = e;   // a CUDA error is not cached
+  if (e.rc != 3) {   // a CUDA error is not cached
+    g_simt[key] = e;
+    trace_entry(a, bwd, e);
+  }
   return e;
 }
 

@@ -2,6 +2,7 @@
 // (the kernels themselves: persist_tc_kernels.cuh; their instances:
 // persist_tc_fwd.cu, persist_tc_bwd.cu).
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 #include <map>
 #include <mutex>
@@ -192,6 +193,22 @@ bool raise_smem_limit(const void* fn, int dev, int bytes) {
 }
 
 // First candidate plan whose clusters can all be resident at once.
+// RNN_TRACE=1: one stderr line per launch shape, when its plan is chosen.
+void trace_plan(int bwd, int H, int B, int ndir, int ext, const TcPlan* p) {
+  const char* e = std::getenv("RNN_TRACE");
+  if (!e || e[0] != '1') return;
+  const char* pass = bwd ? "backward" : "forward";
+  if (!p) {
+    std::fprintf(stderr, "[rnn] tensor-core %s H=%d B=%d dirs=%d: no plan fits\n", pass, H, B, ndir);
+    return;
+  }
+  std::fprintf(stderr,
+               "[rnn] tensor-core %s H=%d B=%d dirs=%d%s: K split %d, %d batch part(s) of %d rows, %d CTAs, "
+               "%d pair(s) per thread, %d weight sub-tiles in tensor memory, %zu B shared memory\n",
+               pass, H, B, ndir, ext ? " (extended)" : "", p->KS, p->NB, p->Bp, p->nrg * p->KS * p->NB * ndir, p->PP,
+               p->w_tmem, p->smem);
+}
+
 bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext, TcPlan* chosen) {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -224,10 +241,12 @@ bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext
     if (max_clusters >= pl.nrg * pl.NB * ndir) {
       *chosen = pl;
       g_plans[key] = {true, pl};
+      trace_plan(bwd, H, B, ndir, ext, &pl);
       return true;
     }
   }
   g_plans[key] = {false, TcPlan()};
+  trace_plan(bwd, H, B, ndir, ext, nullptr);
   return false;
 }
 

@@ -58,6 +58,25 @@
  *     ``cx == NULL`` / ``dhx != NULL`` tests of the persistent backward-data
  *     kernel fragment and the NULL dhy that SystemDS passes.
  *   - Every device pointer must be 16-byte aligned.
+ *
+ * Environment variables (read by the library; none is needed in normal use)
+ *   RNN_TRACE=1            stderr: each recurrent-kernel plan when it is first
+ *                          chosen for a shape (grid, K split, batch parts,
+ *                          shared memory), and the device status record
+ *                          (kernel, block, step, wait) when rnn_sync_status
+ *                          finds an error.
+ *   RNN_TC_MAX_KS_FWD / RNN_TC_MAX_KS_BWD = 1..16
+ *                          cap the tensor-core kernels' K split (CTAs per
+ *                          cluster) in the forward / backward.
+ *   RNN_TC_NB_FWD / RNN_TC_NB_BWD = 1, 2 or 4
+ *                          fix their number of batch parts.
+ *   RNN_GEMM_BN=128|256    force the tensor-core GEMM's tile width (no K split).
+ *   RNN_CLUSTER_FWD=1      allow the cluster-resident forward for layers whose
+ *                          gate rows fit one cluster (slower at the measured
+ *                          shapes; off by default).
+ * The status-record part of RNN_TRACE is fixed at rnn_create; the others are
+ * read at every call (tensor-core plans are cached per shape and per value of
+ * the four RNN_TC_ variables).
  */
 #ifndef GB300_RNN_H
 #define GB300_RNN_H
