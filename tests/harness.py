@@ -113,6 +113,10 @@ def compare(gpu: Dict, ref: Dict, wl, tol: Optional[float] = None, batch_idx: Op
     columns the oracle ran."""
     tol = TOL[wl.dtype] if tol is None else tol
     errs = {}
+    # every output the oracle produced must be there to compare
+    missing = [k for k in ("y", "hy", "cy", "dx", "dhx", "dcx", "dparams") if k in ref and k not in skip
+               and k not in gpu]
+    assert not missing, f"GPU result lacks {missing}"
 
     def sel(a, axis):
         return a if batch_idx is None else np.take(a, list(batch_idx), axis=axis)
@@ -128,6 +132,7 @@ def compare(gpu: Dict, ref: Dict, wl, tol: Optional[float] = None, batch_idx: Op
             for d, g in enumerate(per):
                 for name, v in g.items():
                     errs[f"d{name}[{l},{d}]"] = max_rel_err(gpu["dparams"][l][d][name], v)
+    assert "y" in errs or "y" in skip, "nothing compared"
     bad = {k: v for k, v in errs.items() if not (v <= tol)}
     assert not bad, f"max rel err above {tol}: {bad} (all: {errs})"
     return errs
