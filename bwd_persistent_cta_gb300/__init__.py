@@ -250,13 +250,20 @@ class RNN:
                  num_layers: int = 1, bidirectional: bool = False, reset_after: bool = True,
                  dtype: str = "bf16", gate_order: Sequence[int] = (), batch_first: bool = False,
                  algo: int = RNN_ALGO_AUTO, device=None, recompute: bool = False, interleaved_dw: int = 1):
+        modes = {"lstm": RNN_LSTM, "gru": RNN_GRU, "rnn_relu": RNN_RNN_RELU, "rnn_tanh": RNN_RNN_TANH}
+        if mode not in modes:
+            raise ValueError(f"mode must be one of {sorted(modes)}, not {mode!r}")
+        if dtype not in ("bf16", "f32"):
+            raise ValueError(f"dtype must be 'bf16' or 'f32', not {dtype!r}")
+        if len(gate_order) > 4:
+            raise ValueError(f"gate_order has at most 4 entries, not {len(gate_order)}")
         import torch
         self.torch = torch
         self.device = torch.device(device if device is not None else "cuda")
         if self.device.index is None:     # pin the device current now: the handle is bound to it
             self.device = torch.device("cuda", torch.cuda.current_device())
         d = rnn_desc_t()
-        d.mode = {"lstm": RNN_LSTM, "gru": RNN_GRU, "rnn_relu": RNN_RNN_RELU, "rnn_tanh": RNN_RNN_TANH}[mode]
+        d.mode = modes[mode]
         for k, v in enumerate(gate_order):
             d.gate_order[k] = int(v)
         d.reset_after = int(bool(reset_after))

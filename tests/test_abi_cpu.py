@@ -232,3 +232,13 @@ def test_headers_are_plain_c_and_the_library_links_from_c(lib, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.startswith("1 1 RNN_BAD_PARAM")
+
+
+@pytest.mark.parametrize("kw", [dict(mode="lstm2"), dict(dtype="fp16"), dict(dtype="bfloat16"),
+                                dict(gate_order=(0, 1, 2, 3, 0))])
+def test_binding_rejects_bad_arguments_before_any_device_call(kw):
+    import bwd_persistent_cta_gb300 as R
+    args = dict(mode="lstm", input_size=8, hidden_size=8, seq_len=4, batch=2)
+    args.update(kw)
+    with pytest.raises(ValueError):
+        R.RNN(**args)
