@@ -320,6 +320,57 @@ class RNN:
         d = self.desc
         return (d.num_layers * (2 if d.bidirectional else 1), d.batch, d.hidden_size)
 
+    def _seq_shape(self, features: int):
+        d = self.desc
+        return (d.batch, d.seq_len, features) if d.batch_first else (d.seq_len, d.batch, features)
+
+    def _want(self, t, name: str, shape=None, numel=None, dtype=None):
+        """Raise unless ``t`` (None passes) can be handed to the C ABI as
+        ``name``: a tensor on this handle's device, of the given shape (or
+        element count) and dtype, contiguous and 16-byte aligned.  The library
+        sees only pointers, so a wrong shape here would be an out-of-bounds
+        access there."""
+        if t is None:
+            return
+        torch = self.torch
+        dtype = self.tdtype if dtype is None else dtype
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor, not {type(t).__name__}")
+        if t.device != self.device:
+            raise ValueError(f"{name} is on {t.device}; the handle is on {self.device}")
+        if t.dtype != dtype:
+            raise ValueError(f"{name} has dtype {t.dtype}; expected {dtype}")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}; expected {tuple(shape)}")
+        if numel is not None and t.numel() != numel:
+            raise ValueError(f"{name} has {t.numel()} elements; expected {numel}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.data_ptr() % 16:
+            raise ValueError(f"{name} must start on a 16-byte boundary")
+
+    def _check_forward(self, x, w, hx, cx, y, hy, cy):
+        d = self.desc
+        S = self._state_shape()
+        self._want(x, "x", self._seq_shape(d.input_size))
+        self._want(w, "w", numel=self.weight_count)
+        for t, n in ((hx, "hx"), (cx, "cx"), (hy, "hy"), (cy, "cy")):
+            self._want(t, n, S)
+        self._want(y, "y", self._seq_shape((2 if d.bidirectional else 1) * d.hidden_size))
+
+    def _check_backward_data(self, dy, w, dhy, dcy, dx, dhx, dcx, cx):
+        d = self.desc
+        S = self._state_shape()
+        self._want(dy, "dy", self._seq_shape((2 if d.bidirectional else 1) * d.hidden_size))
+        self._want(w, "w", numel=self.weight_count)
+        for t, n in ((dhy, "dhy"), (dcy, "dcy"), (dhx, "dhx"), (dcx, "dcx"), (cx, "cx")):
+            self._want(t, n, S)
+        self._want(dx, "dx", self._seq_shape(d.input_size))
+
+    def _check_backward_weights(self, x, dw):
+        self._want(x, "x", self._seq_shape(self.desc.input_size))
+        self._want(dw, "dw", numel=self.weight_count, dtype=self.torch.float32)
+
     def forward(self, x, w, hx=None, cx=None, train=True, y=None, hy=None, cy=None, stream=None):
         torch = self.torch
         d = self.desc
@@ -329,6 +380,9 @@ class RNN:
         hy = torch.empty(self._state_shape(), dtype=self.tdtype, device=self.device) if hy is None else hy
         if d.mode == RNN_LSTM and cy is None:
             cy = torch.empty(self._state_shape(), dtype=self.tdtype, device=self.device)
+        if x is None or w is None:
+            raise ValueError("x and w are required")
+        self._check_forward(x, w, hx, cx, y, hy, cy)
         rc = rnn_forward(self.handle, _p(x), _p(hx), _p(cx), _p(w), _p(y), _p(hy), _p(cy),
                          _p(self.workspace), _p(self.reserve) if train else None, _stream(stream, self.device))
         self._check(rc, "rnn_forward")
@@ -342,6 +396,9 @@ class RNN:
         dhx = torch.empty(self._state_shape(), dtype=self.tdtype, device=self.device) if dhx is None else dhx
         if d.mode == RNN_LSTM and dcx is None:
             dcx = torch.empty(self._state_shape(), dtype=self.tdtype, device=self.device)
+        if dy is None or w is None:
+            raise ValueError("dy and w are required")
+        self._check_backward_data(dy, w, dhy, dcy, dx, dhx, dcx, cx)
         rc = rnn_backward_data(self.handle, None, _p(dy), _p(dhy), _p(dcy), _p(w), None, _p(cx), _p(dx), _p(dhx),
                                _p(dcx), _p(self.workspace), _p(self.reserve), _stream(stream, self.device))
         self._check(rc, "rnn_backward_data")
@@ -350,6 +407,9 @@ class RNN:
     def backward_weights(self, x, dw=None, stream=None):
         torch = self.torch
         dw = torch.empty(self.weight_count, dtype=torch.float32, device=self.device) if dw is None else dw
+        if x is None:
+            raise ValueError("x is required")
+        self._check_backward_weights(x, dw)
         rc = rnn_backward_weights(self.handle, _p(x), None, None, _p(self.workspace), _p(self.reserve), _p(dw),
                                   _stream(stream, self.device))
         self._check(rc, "rnn_backward_weights")

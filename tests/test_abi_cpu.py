@@ -242,3 +242,64 @@ def test_binding_rejects_bad_arguments_before_any_device_call(kw):
     args.update(kw)
     with pytest.raises(ValueError):
         R.RNN(**args)
+
+
+def _unbound_rnn(mode="lstm", bidirectional=True, batch_first=False, dtype="bf16"):
+    """An RNN wrapper without a handle, on the CPU device: enough to exercise
+    its argument checks, which run before any library call."""
+    import torch
+    import bwd_persistent_cta_gb300 as R
+    r = object.__new__(R.RNN)
+    r.torch = torch
+    r.device = torch.device("cpu")
+    r.tdtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+    d = R.rnn_desc_t()
+    d.mode = R.RNN_LSTM if mode == "lstm" else R.RNN_GRU
+    d.num_layers, d.seq_len, d.batch, d.input_size, d.hidden_size = 2, 5, 3, 8, 16
+    d.bidirectional, d.batch_first = int(bidirectional), int(batch_first)
+    r.desc = d
+    r.weight_count = 1000
+    r.handle = None
+    return r
+
+
+@pytest.mark.parametrize("batch_first", [False, True])
+def test_wrapper_checks_tensors_before_calling_the_library(batch_first):
+    import torch
+    r = _unbound_rnn(batch_first=batch_first)
+    bf = torch.bfloat16
+    seq = (lambda F: (3, 5, F)) if batch_first else (lambda F: (5, 3, F))
+    x, y, w = torch.zeros(seq(8), dtype=bf), torch.zeros(seq(32), dtype=bf), torch.zeros(1000, dtype=bf)
+    S = torch.zeros(4, 3, 16, dtype=bf)
+    r._check_forward(x, w, S, S, y, S, S)                       # all consistent
+    r._check_forward(x, w, None, None, y, None, None)
+    r._check_backward_data(y, w, S, None, x, S, S, None)
+    r._check_backward_weights(x, torch.zeros(1000, dtype=torch.float32))
+    bad = [
+        lambda: r._check_forward(torch.zeros(seq(9), dtype=bf), w, None, None, y, None, None),    # input size
+        lambda: r._check_forward(x.transpose(0, 1), w, None, None, y, None, None),                # layout
+        lambda: r._check_forward(x, torch.zeros(999, dtype=bf), None, None, y, None, None),       # weights
+        lambda: r._check_forward(x, w, torch.zeros(2, 3, 16, dtype=bf), None, y, None, None),     # state layers
+        lambda: r._check_forward(x, w, None, None, torch.zeros(seq(16), dtype=bf), None, None),   # y width (D*H)
+        lambda: r._check_forward(x.float(), w, None, None, y, None, None),                        # dtype
+        lambda: r._check_forward(torch.zeros(seq(16), dtype=bf)[..., ::2], w, None, None, y, None, None),
+        lambda: r._check_backward_data(y, w, None, None, torch.zeros(seq(4), dtype=bf), None, None, None),
+        lambda: r._check_backward_data(y, w, None, torch.zeros(4, 2, 16, dtype=bf), x, None, None, None),
+        lambda: r._check_backward_weights(x, torch.zeros(1000, dtype=bf)),                        # dw is fp32
+        lambda: r._check_backward_weights(x, torch.zeros(1001, dtype=torch.float32)),
+        lambda: r._check_forward([0.0], w, None, None, y, None, None),                            # not a tensor
+    ]
+    for f in bad:
+        with pytest.raises((ValueError, TypeError)):
+            f()
+
+
+def test_wrapper_checks_alignment_and_device():
+    import torch
+    r = _unbound_rnn(bidirectional=False)
+    bf = torch.bfloat16
+    x = torch.zeros(5 * 3 * 8 + 1, dtype=bf)[1:].view(5, 3, 8)           # 2-byte offset
+    with pytest.raises(ValueError, match="16-byte"):
+        r._want(x, "x", (5, 3, 8))
+    with pytest.raises(ValueError, match="handle is on"):
+        r._want(torch.zeros(5, 3, 8, dtype=bf, device="meta"), "x", (5, 3, 8))
