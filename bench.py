@@ -230,8 +230,15 @@ def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"bf16_tflops": d.get("bf16_tflops"), "hbm_gbs": d.get("hbm_gbs"), "src": "measured"}
-    return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "src": "fallback"}
+        return {"bf16_tflops": d.get("bf16_tflops"), "hbm_gbs": d.get("hbm_gbs"), "sm_max_mhz": d.get("sm_max_mhz"),
+                "src": "measured"}
+    return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "sm_max_mhz": 2070.0, "src": "fallback"}
+
+
+def fp32_fma_tflops(sms: int, sm_mhz: float) -> float:
+    """FP32 peak of the SIMT pipes: 128 FP32 lanes per SM, one FMA (2 flops)
+    per lane per clock."""
+    return sms * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 def workload_config(wl, lengths, world: int) -> dict:
@@ -389,10 +396,17 @@ def run_ours(args):
     launches_per_step = cls_n[dom] / K
     flops_per_launch = fl[names[dom]] / max(launches_per_step, 1)
     achieved = flops_per_launch / (per_launch_ms / 1e3) / 1e12
-    roofline = {"kernel": names[dom], "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+    if wl.dtype == "bf16":
+        bound, peak, peak_src = "tensor", peaks["bf16_tflops"], peaks["src"] + " bf16 burst"
+    else:
+        # the fp32 path runs on the FP32 pipes (FMA), not the tensor cores
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        peak = fp32_fma_tflops(sms, peaks.get("sm_max_mhz") or 2070.0)
+        bound, peak_src = "alu", f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x {peaks.get('sm_max_mhz') or 2070.0:.0f} MHz"
+    roofline = {"kernel": names[dom], "bound": bound, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": profiled_traffic(names[dom], wl.name),
-                "peak_src": peaks["src"] + " bf16 burst", "share": cls_ms[dom] / max(sum(cls_ms), 1e-9),
+                "peak_src": peak_src, "share": cls_ms[dom] / max(sum(cls_ms), 1e-9),
                 "per_launch_ms": per_launch_ms, "per_class_ms_per_step": per_step}
 
     cpu = None

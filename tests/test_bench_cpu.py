@@ -154,3 +154,9 @@ def test_oracle_timing_subprocess(threads):
     assert cores == (1 if threads == 1 else (os.cpu_count() or 1))
     assert len(out["times"]) == 2 and all(t > 0 for t in out["times"])
     assert out["units_per_rep"] == wl.seq_len * 3
+
+
+def test_fp32_peak_derivation():
+    # 152 SMs x 128 FP32 lanes x 2 flops per FMA x 2070 MHz
+    assert bench.fp32_fma_tflops(152, 2070.0) == pytest.approx(80.54784)
+    assert bench.load_peaks()["sm_max_mhz"] > 0
