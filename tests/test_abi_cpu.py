@@ -303,3 +303,57 @@ def test_wrapper_checks_alignment_and_device():
         r._want(x, "x", (5, 3, 8))
     with pytest.raises(ValueError, match="handle is on"):
         r._want(torch.zeros(5, 3, 8, dtype=bf, device="meta"), "x", (5, 3, 8))
+
+
+def test_wrapper_marshals_the_calls(monkeypatch):
+    """forward / backward_data / backward_weights of the wrapper, with the C
+    entry points replaced by recorders: outputs are allocated with the right
+    shapes, the arguments reach the library in its order, inference passes no
+    reserve, and a library error becomes RnnError."""
+    import torch
+    import bwd_persistent_cta_gb300 as R
+    r = _unbound_rnn(bidirectional=True)
+    r.handle = 1234
+    try:
+        r.workspace = torch.zeros(256, dtype=torch.uint8)
+        r.reserve = torch.zeros(256, dtype=torch.uint8)
+        calls = []
+
+        def rec(name, rc=R.RNN_OK):
+            def f(*args):
+                calls.append((name, args))
+                return rc
+            return f
+
+        monkeypatch.setattr(R, "_stream", lambda stream=None, device=None: 77)
+        monkeypatch.setattr(R, "rnn_forward", rec("fwd"))
+        monkeypatch.setattr(R, "rnn_backward_data", rec("bwd"))
+        monkeypatch.setattr(R, "rnn_backward_weights", rec("wu"))
+        bf = torch.bfloat16
+        x, w = torch.zeros(5, 3, 8, dtype=bf), torch.zeros(1000, dtype=bf)
+        hx = torch.zeros(4, 3, 16, dtype=bf)
+        y, hy, cy = r.forward(x, w, hx, None)
+        assert y.shape == (5, 3, 32) and hy.shape == cy.shape == (4, 3, 16)
+        name, a = calls[-1]
+        assert a[0] == 1234 and a[1] == x.data_ptr() and a[2] == hx.data_ptr() and a[3] is None
+        assert a[4] == w.data_ptr() and a[5] == y.data_ptr() and a[6] == hy.data_ptr() and a[7] == cy.data_ptr()
+        assert a[8] == r.workspace.data_ptr() and a[9] == r.reserve.data_ptr() and a[10] == 77
+        r.forward(x, w, train=False)
+        assert calls[-1][1][9] is None                                   # inference: no reserve
+        dy = torch.zeros(5, 3, 32, dtype=bf)
+        dx, dhx, dcx = r.backward_data(dy, w)
+        assert dx.shape == (5, 3, 8) and dhx.shape == dcx.shape == (4, 3, 16)
+        a = calls[-1][1]
+        assert a[2] == dy.data_ptr() and a[5] == w.data_ptr() and a[8] == dx.data_ptr() and a[9] == dhx.data_ptr()
+        assert a[10] == dcx.data_ptr() and a[12] == r.reserve.data_ptr()
+        dw = r.backward_weights(x)
+        assert dw.dtype == torch.float32 and dw.numel() == 1000
+        a = calls[-1][1]
+        assert a[1] == x.data_ptr() and a[5] == r.reserve.data_ptr() and a[6] == dw.data_ptr()
+        with pytest.raises(ValueError):
+            r.forward(x, torch.zeros(10, dtype=bf))
+        monkeypatch.setattr(R, "rnn_forward", rec("fwd", R.RNN_NOT_SUPPORTED))
+        with pytest.raises(R.RnnError):
+            r.forward(x, w)
+    finally:
+        r.handle = None      # a fake handle must never reach rnn_destroy
