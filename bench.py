@@ -433,7 +433,9 @@ def run_ours(args):
             "config": {**workload_config(wl, inp.lengths, world),
                        "l2": "flushed (256 MiB write) before every timed step",
                        "reserve_bytes": rnn.reserve_bytes},
-            "tflops": tflops, "tflops_unit": "TFLOP/s (algorithmic, sum over layers/dirs of 3*2*G*H*(I+H)*B*T)",
+            "tflops": tflops,
+            "tflops_unit": "TFLOP/s (algorithmic, sum over layers/dirs of "
+                           f"{'' if wl.forward_only else '3*'}2*G*H*(I+H)*B*T)",
             "e2e": {"value": job_throughput(wl.seq_len * wl.batch * valid_frac, world, e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": int(x.numel() * x.element_size() +
                                               (0 if wl.forward_only else dy.numel() * dy.element_size())),
