@@ -3,15 +3,22 @@
 
 One step = rnn_forward (training) + rnn_backward_data + rnn_backward_weights
 over one batch of seeded synthetic sequences, inputs resident in HBM.  The
-default workload is the single-layer GRU resetAfter, bf16 storage / fp32
-accumulation, seq 128, batch 64, input = hidden = 512.
+default workload is the largest configuration of the problem statement that
+fits one GPU: the 2-layer bidirectional LSTM, bf16 storage / fp32
+accumulation, seq 512, batch 128, input 1024 (layer 2: 2048), hidden 1024 per
+direction.  The other workloads run with --workload NAME.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...     (the fp64 oracle on host cores)
 
+Without --steps the number of timed steps is chosen after the warm-up so that
+the timed region lasts at least 2.5 s (at least 10 steps).
+
 Multi-GPU: one process per GPU under torchrun; the sequences of a step are
 independent, so each rank runs its own replica on its own batch (weak
-scaling, no data-path collective); timing takes the max over ranks.
+scaling, no data-path collective); timing takes the max over ranks.  A plain
+``python bench.py --gpus N`` (no WORLD_SIZE in the environment) starts its N
+ranks itself through torch.distributed.run on 127.0.0.1.
 
 Prints one JSON line (rank 0).  ``value`` is timestep*batch per second over
 all ranks; ``roofline`` covers the kernel class with the largest share of the
@@ -36,7 +43,9 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "gru_ra_bf16_T128_B64_H512"
+DEFAULT_WORKLOAD = "lstm2bi_bf16_T512_B128_H1024"
+MIN_TIMED_S = 2.5
+L2_POLICY = "flushed (256 MiB write) before every timed GPU step"
 L2_BYTES = 129 * 1024 * 1024
 METRIC = "LSTM/GRU fwd+bwd timestep*batch/s"
 UNIT = "timestep*batch/s"
@@ -45,12 +54,16 @@ UNIT = "timestep*batch/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--probe-ranks", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="run the workload on a shorter sequence (profiling captures of a smaller case); "
+                         "the workload name then carries the length")
     return ap.parse_args()
 
 
@@ -74,7 +87,11 @@ def oracle_worker(spec: str) -> None:
     import synth
     from oracle import rnn_oracle
     name, cols, budget, reps = spec.split(":")
-    wl = synth.WORKLOADS[name]
+    base, _, tlen = name.partition("@T")
+    wl = synth.WORKLOADS[base]
+    if tlen:
+        import dataclasses
+        wl = dataclasses.replace(wl, name=name, seq_len=int(tlen))
     cols, budget, reps = int(cols), float(budget), int(reps)
     inp = synth.make_inputs(wl, batch_subset=list(range(cols)))
     times = []
@@ -187,7 +204,24 @@ def class_flops(wl):
     rec = sum(D * 2.0 * G * H * H * B * T for _ in range(wl.num_layers))
     proj = sum(D * 2.0 * G * H * wl.layer_input(l) * B * T for l in range(wl.num_layers))
     return {"persist_fwd": rec, "persist_bwd": rec, "gemm_proj": proj, "gemm_dx": proj,
-            "gemm_dw": proj + rec, "layout": 0.0}
+            "gemm_dw": proj + rec, "layout_seq": 0.0, "layout_pack": 0.0, "recompute_cells": 0.0}
+
+
+LAYOUT_CLASSES = ("layout_seq", "layout_pack", "recompute_cells")
+
+
+def layout_report(names, cls_ms, cls_n, cls_bytes, steps: int, hbm_gbs: float):
+    """Per layout class: time, launches and algorithmic bytes per step, and
+    the achieved bandwidth against the measured HBM copy rate."""
+    out = {}
+    for i, n in enumerate(names):
+        if n not in LAYOUT_CLASSES or cls_n[i] == 0:
+            continue
+        gbs = cls_bytes[i] / (cls_ms[i] / 1e3) / 1e9 if cls_ms[i] > 0 else None
+        out[n] = {"ms_per_step": cls_ms[i] / steps, "launches_per_step": cls_n[i] / steps,
+                  "bytes_per_step": cls_bytes[i] / steps, "achieved_gbs": gbs,
+                  "frac_of_hbm": gbs / hbm_gbs if gbs is not None else None}
+    return out
 
 
 PROFILE_FOR_CLASS = {
@@ -246,7 +280,7 @@ def workload_config(wl, lengths, world: int) -> dict:
     cfg = {"workload": wl.name, "mode": wl.mode, "reset_after": wl.reset_after, "layers": wl.num_layers,
            "bidirectional": wl.bidirectional, "seq_len": wl.seq_len, "batch_per_gpu": wl.batch,
            "input": wl.input_size, "hidden": wl.hidden_size, "seed": wl.seed, "parallelism": f"replicas{world}",
-           "recompute_cell_states": wl.recompute}
+           "recompute_cell_states": wl.recompute, "l2": L2_POLICY}
     if lengths is not None:
         cfg["seq_lengths"] = {"min": int(min(lengths)), "max": int(max(lengths)),
                               "valid_frac": float(sum(int(v) for v in lengths)) / (wl.seq_len * wl.batch),
@@ -257,6 +291,17 @@ def workload_config(wl, lengths, world: int) -> dict:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def pick_workload(args):
+    """The named workload, or a copy of it on --seq-len timesteps (same seed,
+    shapes and draws otherwise; the name records the length)."""
+    import dataclasses
+    import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.seq_len is not None and args.seq_len != wl.seq_len:
+        wl = dataclasses.replace(wl, name=f"{wl.name}@T{args.seq_len}", seq_len=int(args.seq_len))
+    return wl
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -278,7 +323,7 @@ def run_ours(args):
         dist.barrier()
     B.build()
 
-    wl = synth.WORKLOADS[args.workload]
+    wl = pick_workload(args)
     inp = synth.make_inputs(wl)
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     dev = torch.device("cuda", local)
@@ -317,6 +362,16 @@ def run_ours(args):
     rnn.sync()
 
     K = args.steps
+    if K is None:
+        # enough steps for a timed region of at least MIN_TIMED_S (the same K on every rank)
+        t0 = time.perf_counter()
+        step()
+        rnn.sync()
+        K = max(10, int(MIN_TIMED_S / max(time.perf_counter() - t0, 1e-4)) + 1)
+        if dist is not None:
+            kt = torch.tensor([K], dtype=torch.int64, device=dev)
+            dist.all_reduce(kt, op=dist.ReduceOp.MAX)
+            K = int(kt.item())
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] or local)
@@ -342,7 +397,7 @@ def run_ours(args):
     rnn.sync()
     R.rnn_set_timing(rnn.handle, False)
     launches = rnn.launches() - launches0
-    cls_ms, cls_n = R.rnn_get_timing(rnn.handle)
+    cls_ms, cls_n, cls_bytes = R.rnn_get_timing_ex(rnn.handle)
     ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K, dist, dev)
 
     # --- end to end through the C ABI with host buffers --------------------
@@ -403,6 +458,7 @@ def run_ours(args):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         peak = fp32_fma_tflops(sms, peaks.get("sm_max_mhz") or 2070.0)
         bound, peak_src = "alu", f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x {peaks.get('sm_max_mhz') or 2070.0:.0f} MHz"
+    layout = layout_report(names, cls_ms, cls_n, cls_bytes, K, peaks["hbm_gbs"])
     roofline = {"kernel": names[dom], "bound": bound, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": profiled_traffic(names[dom], wl.name),
@@ -430,9 +486,8 @@ def run_ours(args):
             "ms_per_step": ms, "us_per_timestep": ms * 1e3 / wl.seq_len, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-            "config": {**workload_config(wl, inp.lengths, world),
-                       "l2": "flushed (256 MiB write) before every timed step",
-                       "reserve_bytes": rnn.reserve_bytes},
+            "config": workload_config(wl, inp.lengths, world),
+            "reserve_bytes": rnn.reserve_bytes,
             "tflops": tflops,
             "tflops_unit": "TFLOP/s (algorithmic, sum over layers/dirs of "
                            f"{'' if wl.forward_only else '3*'}2*G*H*(I+H)*B*T)",
@@ -441,7 +496,8 @@ def run_ours(args):
                                               (0 if wl.forward_only else dy.numel() * dy.element_size())),
                     "d2h_bytes_per_step": int(res.numel() * res.element_size())},
             "gpu_launches": int(launches), "gpu_launches_per_step": launches / K,
-            "roofline": roofline, "clocks": clocks, "cpu_baseline": cpu,
+            "roofline": roofline, "layout": layout, "layout_peak_src": peaks["src"] + " HBM copy",
+            "clocks": clocks, "cpu_baseline": cpu,
             "wall_s_timed_region": t_wall,
         }
         print(json.dumps(line))
@@ -458,15 +514,16 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    wl = synth.WORKLOADS[args.workload]
+    wl = pick_workload(args)
     cols = _oracle_sample_cols(wl, 2.0)
-    out, cores = run_oracle_subprocess(wl, 0.0, cols, reps=args.warmup + args.steps)
-    per_step = out["times"][args.warmup:args.warmup + args.steps]
+    steps = args.steps if args.steps is not None else 10
+    out, cores = run_oracle_subprocess(wl, 0.0, cols, reps=args.warmup + steps)
+    per_step = out["times"][args.warmup:args.warmup + steps]
     units = out["units_per_rep"] * len(per_step)
     secs = sum(per_step)
     value = units / secs
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(args.steps, 1), "higher_is_better": True,
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(steps, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": workload_config(wl, synth.make_lengths(wl), args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -476,10 +533,50 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def self_launch(args) -> int:
+    """``--gpus N`` without WORLD_SIZE in the environment: run this script as
+    N ranks under torch.distributed.run (one node, rendezvous on 127.0.0.1)
+    and return its exit code."""
+    import socket
+    sock = socket.socket()
+    sock.bind(("127.0.0.1", 0))
+    port = sock.getsockname()[1]
+    sock.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.run(cmd, cwd=ROOT).returncode
+
+
+def probe_ranks(args) -> None:
+    """The launch and aggregation path alone, without a kernel: every rank
+    joins the process group (nccl with GPUs, else gloo), the ranks' numbers
+    are summed, and rank 0 prints how many ranks took part."""
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    t = torch.tensor([1.0 + rank], dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t)
+    slowest = max_over_ranks(float(rank), dist if world > 1 else None, "cpu")
+    if rank == 0:
+        print(json.dumps({"probe": "ranks", "n_gpus": world, "gpus_requested": args.gpus,
+                          "rank_sum": float(t.item()), "max_rank": slowest}))
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main():
     args = parse()
     if args.oracle_sample:
         oracle_worker(args.oracle_sample)
+        return
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(self_launch(args))
+    if args.probe_ranks:
+        probe_ranks(args)
         return
     if args.impl == "reference":
         run_reference(args)

@@ -58,12 +58,15 @@ _SIGS = {
     "rnn_selected_algo": (ctypes.c_int, [_P]),
     "rnn_selected_fwd_algo": (ctypes.c_int, [_P]),
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
+    "rnn_debug_set_plan_overrides": (ctypes.c_int, [ctypes.c_int] * 5),
     "rnn_debug_tc_plans": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "rnn_debug_simt_plan": (ctypes.c_int, [ctypes.c_int] * 9 + [ctypes.POINTER(ctypes.c_int)]),
     "rnn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "rnn_set_timing": (ctypes.c_int, [_P, ctypes.c_int]),
     "rnn_get_timing": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]),
+    "rnn_get_timing_ex": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64),
+                                         ctypes.POINTER(ctypes.c_double)]),
     "rnn_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(rnn_desc_t)] + [_P] * 7 + [ctypes.c_int, _P]),
     "rnn_debug_gemm": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int64, ctypes.c_int,
                                       _P, ctypes.c_int64, ctypes.c_int, _P, ctypes.c_int64, ctypes.c_int, _P,
@@ -189,8 +192,9 @@ def rnn_selected_fwd_algo(handle) -> int:
     return int(lib().rnn_selected_fwd_algo(handle))
 
 
-RNN_TIMING_CLASSES = 6
-TIMING_CLASS_NAMES = ("persist_fwd", "persist_bwd", "gemm_proj", "gemm_dx", "gemm_dw", "layout")
+RNN_TIMING_CLASSES = 8
+TIMING_CLASS_NAMES = ("persist_fwd", "persist_bwd", "gemm_proj", "gemm_dx", "gemm_dw", "layout_seq", "layout_pack",
+                      "recompute_cells")
 
 
 def rnn_set_timing(handle, enable: bool) -> int:
@@ -198,13 +202,24 @@ def rnn_set_timing(handle, enable: bool) -> int:
 
 
 def rnn_get_timing(handle):
-    """(ms[6], counts[6]) since the last read; waits for the recorded events."""
+    """(ms[8], counts[8]) since the last read; waits for the recorded events."""
     ms = (ctypes.c_double * RNN_TIMING_CLASSES)()
     n = (ctypes.c_uint64 * RNN_TIMING_CLASSES)()
     rc = lib().rnn_get_timing(handle, ms, n)
     if rc != RNN_OK:
         raise RnnError(rc, "rnn_get_timing")
     return list(ms), [int(v) for v in n]
+
+
+def rnn_get_timing_ex(handle):
+    """(ms[8], counts[8], algorithmic bytes[8]) since the last read."""
+    ms = (ctypes.c_double * RNN_TIMING_CLASSES)()
+    n = (ctypes.c_uint64 * RNN_TIMING_CLASSES)()
+    by = (ctypes.c_double * RNN_TIMING_CLASSES)()
+    rc = lib().rnn_get_timing_ex(handle, ms, n, by)
+    if rc != RNN_OK:
+        raise RnnError(rc, "rnn_get_timing_ex")
+    return list(ms), [int(v) for v in n], list(by)
 
 
 def rnn_debug_tc_plans(mode: int, bwd: int, hidden: int, batch: int, ndir: int, num_sms: int, max_out: int = 16):
@@ -228,6 +243,12 @@ def rnn_debug_simt_plan(mode: int, reset_after: int, is_bf16: int, bwd: int, hid
 
 def rnn_debug_skip_arrival(handle, cta: int) -> int:
     return lib().rnn_debug_skip_arrival(handle, int(cta))
+
+
+def rnn_debug_set_plan_overrides(max_ks_fwd: int = 0, max_ks_bwd: int = 0, nb_fwd: int = 0, nb_bwd: int = 0,
+                                 gemm_bn: int = 0) -> int:
+    return lib().rnn_debug_set_plan_overrides(int(max_ks_fwd), int(max_ks_bwd), int(nb_fwd), int(nb_bwd),
+                                              int(gemm_bn))
 
 
 def rnn_debug_gemm(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, C, ldc, c_bf16, bias, beta, rowmap_H, perm,

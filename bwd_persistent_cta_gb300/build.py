@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librnn.so")
 SOURCES = ["api.cpp", "tmap.cpp", "layout.cu", "gemm_simt.cu", "gemm_tc.cu",
-           "persist_simt.cu", "persist_tc.cu", "persist_tc_fwd.cu", "persist_tc_bwd.cu", "persist_cl.cu",
+           "persist_simt.cu", "persist_tc.cu", "persist_tc_fwd.cu", "persist_tc_bwd.cu",
            "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

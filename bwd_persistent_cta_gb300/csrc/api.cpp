@@ -19,6 +19,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -48,6 +49,13 @@ int layer_in(const rnn_handle_s* h, int l) { return l == 0 ? h->I : h->D * h->H;
 
 rnn_status_t st(int rc) { return static_cast<rnn_status_t>(rc); }
 
+// A layout launch, timed in its class with its algorithmic bytes.
+#define RNN_LAYOUT(cls, bytes, expr)          \
+  do {                                        \
+    TimeScope _ts(h, (cls), s, (bytes));      \
+    int _rc = (expr);                         \
+    if (_rc) return st(_rc);                  \
+  } while (0)
 #define RNN_TRY(expr)                         \
   do {                                        \
     int _rc = (expr);                         \
@@ -151,7 +159,7 @@ struct TimeScope {
   cudaStream_t s;
   rnn_handle_s::Ev ev{};
   bool on;
-  TimeScope(rnn_handle_s* h_, int cls, cudaStream_t s_) : h(h_), s(s_), on(h_->timing) {
+  TimeScope(rnn_handle_s* h_, int cls, cudaStream_t s_, double bytes = 0.0) : h(h_), s(s_), on(h_->timing) {
     if (!on) return;
     if (!h->pool.empty()) {
       ev = h->pool.back();
@@ -161,6 +169,7 @@ struct TimeScope {
       return;
     }
     ev.cls = cls;
+    ev.bytes = bytes;
     cudaEventRecord(ev.a, s);
   }
   ~TimeScope() {
@@ -169,6 +178,30 @@ struct TimeScope {
     h->events.push_back(ev);
   }
 };
+
+// Timing classes of the layout kernels and their algorithmic bytes (every
+// element read once and written once at its storage size).
+constexpr int kClsSeq = 5, kClsPack = 6, kClsRecompute = 7;
+double seq_bytes(int T, int B, int F, int in_bf16, int out_bf16) {
+  return static_cast<double>(T) * B * F * ((in_bf16 ? 2 : 4) + (out_bf16 ? 2 : 4));
+}
+double pack_bytes(const PackBatch& pb, int es) {
+  double b = 0.0;
+  for (int i = 0; i < pb.n; ++i) {
+    const PackJob& j = pb.job[i];
+    int mapped = 0;
+    for (int k = 0; k < 4; ++k) mapped += j.map[k] >= 0;
+    const double HK = static_cast<double>(j.H) * j.K;
+    switch (j.kind) {
+      case PACK_ROWS:
+      case PACK_ROWS_T: b += (mapped + 4.0) * HK * es; break;
+      case PACK_BIAS: b += (j.in ? mapped * es : 0) * static_cast<double>(j.H) + 16.0 * j.H; break;
+      case SCATTER_DB: b += 16.0 * j.H + 4.0 * mapped * j.H; break;
+      default: b += (j.in ? 2.0 : 1.0) * j.B * j.H * es;   // H0_TO_Y
+    }
+  }
+  return b;
+}
 
 int run_gemm(rnn_handle_s* h, GemmArgs g, cudaStream_t s, int cls) {
   if (g.M <= 0 || g.N <= 0) return 0;
@@ -197,11 +230,8 @@ int run_persist(rnn_handle_s* h, PersistArgs a, bool bwd, cudaStream_t s) {
     int rc = reset_counters(h, s);
     if (rc) return rc;
     TimeScope ts(h, bwd ? 1 : 0, s);
-    if (bwd ? h->algo == RNN_ALGO_PERSIST_TC : h->fwd_tc != 0) {
-      // forward: the cluster-resident kernel when the layer fits one cluster
-      rc = bwd ? 2 : launch_persist_fwd_cl(x, s, h->num_sms);
-      if (rc == 2) rc = bwd ? launch_persist_bwd_tc(x, s, h->num_sms) : launch_persist_fwd_tc(x, s, h->num_sms);
-    }
+    if (bwd ? h->algo == RNN_ALGO_PERSIST_TC : h->fwd_tc != 0)
+      rc = bwd ? launch_persist_bwd_tc(x, s, h->num_sms) : launch_persist_fwd_tc(x, s, h->num_sms);
     else
       rc = bwd ? launch_persist_bwd_simt(x, s, h->num_sms) : launch_persist_fwd_simt(x, s, h->num_sms);
     return count(h, rc);
@@ -343,6 +373,17 @@ struct DeviceGuard {
 
 }  // namespace
 
+namespace rnn {
+namespace {
+std::mutex g_override_mu;
+PlanOverrides g_override{0, 0, 0, 0, 0};
+}  // namespace
+PlanOverrides plan_overrides() {
+  std::lock_guard<std::mutex> lock(g_override_mu);
+  return g_override;
+}
+}  // namespace rnn
+
 extern "C" {
 
 const char* rnn_status_string(rnn_status_t s) {
@@ -459,9 +500,9 @@ rnn_status_t rnn_set_timing(rnn_handle_t h, int enable) {
   return RNN_OK;
 }
 
-rnn_status_t rnn_get_timing(rnn_handle_t h, double* ms, uint64_t* n) {
+rnn_status_t rnn_get_timing_ex(rnn_handle_t h, double* ms, uint64_t* n, double* bytes) {
   if (!h) return RNN_BAD_PARAM;
-  double acc[RNN_TIMING_CLASSES] = {0};
+  double acc[RNN_TIMING_CLASSES] = {0}, by[RNN_TIMING_CLASSES] = {0};
   uint64_t cnt[RNN_TIMING_CLASSES] = {0};
   rnn_status_t rs = RNN_OK;
   for (auto& e : h->events) {
@@ -470,15 +511,19 @@ rnn_status_t rnn_get_timing(rnn_handle_t h, double* ms, uint64_t* n) {
       rs = RNN_CUDA_ERROR;
     acc[e.cls] += t;
     cnt[e.cls] += 1;
+    by[e.cls] += e.bytes;
     h->pool.push_back(e);
   }
   h->events.clear();
   for (int i = 0; i < RNN_TIMING_CLASSES; ++i) {
     if (ms) ms[i] = acc[i];
     if (n) n[i] = cnt[i];
+    if (bytes) bytes[i] = by[i];
   }
   return rs;
 }
+
+rnn_status_t rnn_get_timing(rnn_handle_t h, double* ms, uint64_t* n) { return rnn_get_timing_ex(h, ms, n, nullptr); }
 
 uint64_t rnn_launch_count(rnn_handle_t h) { return h ? h->launches : 0; }
 
@@ -486,6 +531,17 @@ int rnn_selected_algo(rnn_handle_t h) { return h ? h->algo : 0; }
 
 int rnn_selected_fwd_algo(rnn_handle_t h) {
   return h ? (h->fwd_tc ? RNN_ALGO_PERSIST_TC : h->algo) : 0;
+}
+
+rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn) {
+  auto ks_ok = [](int v) { return v >= 0 && v <= 16; };
+  auto nb_ok = [](int v) { return v == 0 || v == 1 || v == 2 || v == 4; };
+  if (!ks_ok(max_ks_fwd) || !ks_ok(max_ks_bwd) || !nb_ok(nb_fwd) || !nb_ok(nb_bwd) ||
+      !(gemm_bn == 0 || gemm_bn == 128 || gemm_bn == 256))
+    return RNN_BAD_PARAM;
+  std::lock_guard<std::mutex> lock(rnn::g_override_mu);
+  rnn::g_override = {max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn};
+  return RNN_OK;
 }
 
 rnn_status_t rnn_debug_skip_arrival(rnn_handle_t h, int cta) {
@@ -532,8 +588,9 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
   slots_fwd(h, sf);
   const void* layer_x = x;
   if (h->bfirst) {
-    RNN_TRY(count(h, launch_seq_transpose(x, at<char>(workspace, h->w_xin), T, B, h->I, h->bf16, h->bf16, 1, 0,
-                                          h->I, s)));
+    RNN_LAYOUT(kClsSeq, seq_bytes(T, B, h->I, h->bf16, h->bf16),
+               count(h, launch_seq_transpose(x, at<char>(workspace, h->w_xin), T, B, h->I, h->bf16, h->bf16, 1, 0,
+                                             h->I, s)));
     layer_x = at<char>(workspace, h->w_xin);
   }
   void* Ybuf = nullptr;
@@ -567,7 +624,7 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
       y.in = hx ? static_cast<const char*>(hx) + (static_cast<size_t>(l) * D + d) * B * H * es : nullptr;
       pb.add(y);
     }
-    RNN_TRY(count(h, launch_pack_batch(pb, h->bf16, s)));
+    RNN_LAYOUT(kClsPack, pack_bytes(pb, static_cast<int>(es)), count(h, launch_pack_batch(pb, h->bf16, s)));
     // hoisted input projection for every timestep and direction
     GemmArgs g;
     g.M = static_cast<int>(TB); g.N = D * 4 * H; g.K = Il;
@@ -598,8 +655,9 @@ rnn_status_t rnn_forward(rnn_handle_t h, const void* x, const void* hx, const vo
   }
   // y out (rows of slots 1..T)
   if (!y_direct)
-    RNN_TRY(count(h, launch_seq_transpose(layer_x, y, T, B, D * H, h->bf16, h->bf16, 0, h->bfirst, D * H, s,
-                                          h->has_len ? h->d_len : nullptr)));
+    RNN_LAYOUT(kClsSeq, seq_bytes(T, B, D * H, h->bf16, h->bf16),
+               count(h, launch_seq_transpose(layer_x, y, T, B, D * H, h->bf16, h->bf16, 0, h->bfirst, D * H, s,
+                                             h->has_len ? h->d_len : nullptr)));
   return cudaGetLastError() == cudaSuccess ? RNN_OK : RNN_CUDA_ERROR;
 }
 
@@ -623,7 +681,8 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
   slots_bwd_rec(h, sr);
   slots_fwd(h, sx);
   float* dyi = at<float>(workspace, h->w_dyi);
-  RNN_TRY(count(h, launch_seq_transpose(dy, dyi, T, B, D * H, h->bf16, 0, h->bfirst, 0, D * H, s)));
+  RNN_LAYOUT(kClsSeq, seq_bytes(T, B, D * H, h->bf16, 0),
+             count(h, launch_seq_transpose(dy, dyi, T, B, D * H, h->bf16, 0, h->bfirst, 0, D * H, s)));
   char* wb = static_cast<char*>(const_cast<void*>(w));
   for (int l = L - 1; l >= 0; --l) {
     const int Il = layer_in(h, l);
@@ -642,7 +701,7 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
       j.out = at<char>(workspace, h->w_wxt) + static_cast<size_t>(d) * 4 * H * es;
       pb.add(j);
     }
-    RNN_TRY(count(h, launch_pack_batch(pb, h->bf16, s)));
+    RNN_LAYOUT(kClsPack, pack_bytes(pb, static_cast<int>(es)), count(h, launch_pack_batch(pb, h->bf16, s)));
     PersistArgs a;
     a.mode = h->desc.mode; a.reset_after = h->ra; a.is_bf16 = h->bf16;
     a.T = T; a.B = B; a.H = H; a.D = D;
@@ -654,8 +713,10 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
       // buffer, idle in the backward pass (D*(T+1)*B*H*4 <= T*B*D*4H*es bytes)
       float* Cw = at<float>(workspace, h->w_p);
       const void* c0 = cx ? static_cast<const char*>(cx) + static_cast<size_t>(l) * D * B * H * es : nullptr;
-      RNN_TRY(count(h, launch_recompute_cells(a.gates, c0, Cw, T, B, H, D, h->bf16, h->has_len ? h->d_len : nullptr,
-                                              h->clip, h->clip_lo, h->clip_hi, s)));
+      RNN_LAYOUT(kClsRecompute, static_cast<double>(D) * T * B * H * (3.0 * es + 4.0),
+                 count(h, launch_recompute_cells(a.gates, c0, Cw, T, B, H, D, h->bf16,
+                                                 h->has_len ? h->d_len : nullptr, h->clip, h->clip_lo, h->clip_hi,
+                                                 s)));
       a.C = Cw;
     }
     a.WrT = at<char>(workspace, h->w_wrt);
@@ -688,8 +749,9 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
     RNN_TRY(run_gemm(h, g, s, 3));
   }
   if (h->bfirst)
-    RNN_TRY(count(h, launch_seq_transpose(at<char>(workspace, h->w_dx0), dx, T, B, h->I, h->bf16, h->bf16, 0, 1,
-                                          h->I, s)));
+    RNN_LAYOUT(kClsSeq, seq_bytes(T, B, h->I, h->bf16, h->bf16),
+               count(h, launch_seq_transpose(at<char>(workspace, h->w_dx0), dx, T, B, h->I, h->bf16, h->bf16, 0, 1,
+                                             h->I, s)));
   return cudaGetLastError() == cudaSuccess ? RNN_OK : RNN_CUDA_ERROR;
 }
 
@@ -710,8 +772,9 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
   trace(h, "backward weights");
   const void* x0 = x;
   if (h->bfirst) {
-    RNN_TRY(count(h, launch_seq_transpose(x, at<char>(workspace, h->w_xin), T, B, h->I, h->bf16, h->bf16, 1, 0,
-                                          h->I, s)));
+    RNN_LAYOUT(kClsSeq, seq_bytes(T, B, h->I, h->bf16, h->bf16),
+               count(h, launch_seq_transpose(x, at<char>(workspace, h->w_xin), T, B, h->I, h->bf16, h->bf16, 1, 0,
+                                             h->I, s)));
     x0 = at<char>(workspace, h->w_xin);
   }
   char* rs = static_cast<char*>(const_cast<void*>(reserve));
@@ -781,7 +844,7 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
       for (int k = 0; k < 4; ++k) j.map[k] = m_b[k];
       j.out = dwf + h->off_b[i];
       if (!scatter.add(j)) {
-        RNN_TRY(count(h, launch_pack_batch(scatter, 0, s)));
+        RNN_LAYOUT(kClsPack, pack_bytes(scatter, 4), count(h, launch_pack_batch(scatter, 0, s)));
         scatter.n = 0;
         scatter.add(j);
       }
@@ -789,14 +852,14 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
         for (int k = 0; k < 4; ++k) j.map[k] = m_bh[k];
         j.out = dwf + h->off_bh[i];
         if (!scatter.add(j)) {
-          RNN_TRY(count(h, launch_pack_batch(scatter, 0, s)));
+          RNN_LAYOUT(kClsPack, pack_bytes(scatter, 4), count(h, launch_pack_batch(scatter, 0, s)));
           scatter.n = 0;
           scatter.add(j);
         }
       }
     }
   }
-  RNN_TRY(count(h, launch_pack_batch(scatter, 0, s)));
+  RNN_LAYOUT(kClsPack, pack_bytes(scatter, 4), count(h, launch_pack_batch(scatter, 0, s)));
   return cudaGetLastError() == cudaSuccess ? RNN_OK : RNN_CUDA_ERROR;
 }
 

@@ -179,18 +179,6 @@ __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* m
          "r"(smem_u32(bar))
       : "memory");
 }
-// Multicast tiled load: the box lands at the same shared-memory offset in
-// every CTA of the cluster named in cta_mask, each completing the bytes on its
-// own mbarrier at the offset of ``bar``.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                                      int y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      :: "r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)),
-         "h"(cta_mask)
-      : "memory");
-}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -229,18 +217,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t start, uint32_t lbo, ui
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;   // descriptor version (sm_100 family)
   d |= static_cast<uint64_t>(2) << 61;   // swizzle mode: 128B
-  return d;
-}
-
-// Shared-memory matrix descriptor, 64-byte swizzle (K-major: 8-row atoms of
-// 64-byte rows, 512 bytes apart; +32 bytes per K=16 step inside the row).
-__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t start, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((start & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1) << 16;                          // leading byte offset (unused, 16 B)
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;                          // descriptor version (sm_100 family)
-  d |= static_cast<uint64_t>(4) << 61;                          // swizzle mode: 64B
   return d;
 }
 

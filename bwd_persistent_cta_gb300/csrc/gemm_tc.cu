@@ -425,11 +425,9 @@ int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev,
                    int* launches) {
   if (!gemm_tc_supported(g)) return 2;
   GemmPlan pl = plan_gemm(g, num_sms);
-  // tuning knob: RNN_GEMM_BN=128|256 forces the tile width (no K split)
-  if (const char* e = std::getenv("RNN_GEMM_BN")) {
-    const int v = std::atoi(e);
-    if (v == 128 || v == 256) pl = {v, 1};
-  }
+  // test hook: a forced tile width (no K split)
+  const int bn = plan_overrides().gemm_bn;
+  if (bn == 128 || bn == 256) pl = {bn, 1};
   if (launches) *launches = pl.S > 1 ? 2 : 1;
   return pl.BN == 256 ? launch_bn<256>(g, pl.S, s, num_sms, dev, timeout_ns)
                       : launch_bn<128>(g, pl.S, s, num_sms, dev, timeout_ns);

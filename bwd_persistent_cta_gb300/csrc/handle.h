@@ -33,7 +33,7 @@ struct rnn_handle_s {
   float clip_lo, clip_hi;
   bool trace;
   bool timing;
-  struct Ev { cudaEvent_t a, b; int cls; };
+  struct Ev { cudaEvent_t a, b; int cls; double bytes; };
   std::vector<Ev> events;      // recorded, not yet read
   std::vector<Ev> pool;        // created, free
   // weight offsets (elements), per layer and direction

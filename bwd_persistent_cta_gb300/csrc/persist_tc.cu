@@ -60,18 +60,11 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
   const int K = bwd ? 4 * H : H;
   const int nrg = bwd ? H / 128 : (4 * H) / 128;
   if (bwd ? (H % 128) : (H % 32)) return 0;
-  // tuning knobs: RNN_TC_MAX_KS_FWD / RNN_TC_MAX_KS_BWD cap the K split
-  // (1..16); RNN_TC_NB_FWD / RNN_TC_NB_BWD fix the batch parts (1, 2, 4)
+  // test hook: a K-split cap (1..16) and a fixed batch-part count (1, 2, 4)
+  const PlanOverrides ov = plan_overrides();
   int cap = kMaxKS;
-  if (const char* e = std::getenv(bwd ? "RNN_TC_MAX_KS_BWD" : "RNN_TC_MAX_KS_FWD")) {
-    const int v = std::atoi(e);
-    if (v >= 1 && v <= kMaxKS) cap = v;
-  }
-  int nb_only = 0;
-  if (const char* e = std::getenv(bwd ? "RNN_TC_NB_BWD" : "RNN_TC_NB_FWD")) {
-    const int v = std::atoi(e);
-    if (v == 1 || v == 2 || v == 4) nb_only = v;
-  }
+  if (const int v = bwd ? ov.max_ks_bwd : ov.max_ks_fwd) cap = v;
+  const int nb_only = bwd ? ov.nb_bwd : ov.nb_fwd;
   std::vector<std::pair<double, TcPlan>> cands;
   for (int NB = 1; NB <= kMaxBatchParts; NB *= 2) {
     // each batch part: Bp rows (at least 8; every part non-empty), the MMA N
@@ -173,10 +166,6 @@ struct PlanKey {
   bool operator<(const PlanKey& o) const { return std::lexicographical_compare(v, v + 12, o.v, o.v + 12); }
 };
 
-int env_cap(const char* name) {
-  const char* e = std::getenv(name);
-  return e ? std::atoi(e) : 0;
-}
 std::mutex g_plan_mu;
 std::map<PlanKey, std::pair<bool, TcPlan>> g_plans;
 std::map<std::pair<const void*, int>, int> g_smem_limit;
@@ -212,8 +201,8 @@ void trace_plan(int bwd, int H, int B, int ndir, int ext, const TcPlan* p) {
 bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext, TcPlan* chosen) {
   int dev = 0;
   cudaGetDevice(&dev);
-  const PlanKey key{{mode, bwd, H, B, ndir, num_sms, ext, dev, env_cap("RNN_TC_MAX_KS_FWD"),
-                     env_cap("RNN_TC_MAX_KS_BWD"), env_cap("RNN_TC_NB_FWD"), env_cap("RNN_TC_NB_BWD")}};
+  const PlanOverrides ov = plan_overrides();
+  const PlanKey key{{mode, bwd, H, B, ndir, num_sms, ext, dev, ov.max_ks_fwd, ov.max_ks_bwd, ov.nb_fwd, ov.nb_bwd}};
   std::lock_guard<std::mutex> lock(g_plan_mu);
   const auto hit = g_plans.find(key);
   if (hit != g_plans.end()) {

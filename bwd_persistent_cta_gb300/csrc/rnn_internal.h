@@ -43,9 +43,8 @@ struct DevArea {
   unsigned int pad[27];
 };
 
-enum KernelId : unsigned int { K_FWD_SIMT = 1, K_BWD_SIMT = 2, K_FWD_TC = 3, K_BWD_TC = 4, K_GEMM_TC = 5,
-                                K_FWD_CL = 6 };
-enum WaitKind : unsigned int { W_COUNTER = 1, W_TMA = 2, W_MMA = 3, W_PEER = 4 };
+enum KernelId : unsigned int { K_FWD_SIMT = 1, K_BWD_SIMT = 2, K_FWD_TC = 3, K_BWD_TC = 4, K_GEMM_TC = 5 };
+enum WaitKind : unsigned int { W_COUNTER = 1, W_TMA = 2, W_MMA = 3 };
 
 // C[row(m), n] = sum_k A(m, k) * B(n, k)  (+ bias[n]) (+ C_old if beta)
 //   A(m, k) = A[m*lda + k] (a_kmajor) or A[k*lda + m];  same for B with n.
@@ -132,9 +131,6 @@ constexpr int kMaxBatchParts = 4;
 bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms);
 // The forward kernel alone (a layer whose backward has no tensor-core plan).
 bool persist_tc_fwd_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms);
-// Cluster-resident forward (persist_cl.cu): returns 2 when the shape or the
-// options do not fit it (the caller then uses the tcgen05 persistent kernel).
-int launch_persist_fwd_cl(const PersistArgs& a, cudaStream_t s, int num_sms);
 int launch_persist_fwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms);
 int launch_persist_bwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms);
 
@@ -185,5 +181,13 @@ int launch_fill_zero(void* p, size_t bytes, cudaStream_t s);
 // PersistArgs.
 int launch_recompute_cells(const void* gates, const void* c0, float* C, int T, int B, int H, int D, int is_bf16,
                            const int* len, int clip, float lo, float hi, cudaStream_t s);
+
+// Plan overrides set by the rnn_debug_set_plan_overrides test hook (0 = the
+// planner's choice): K-split caps and batch parts of the tensor-core
+// persistent kernels, the tensor-core GEMM's tile width.
+struct PlanOverrides {
+  int max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn;
+};
+PlanOverrides plan_overrides();
 
 }  // namespace rnn

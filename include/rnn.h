@@ -65,18 +65,7 @@
  *                          shared memory), and the device status record
  *                          (kernel, block, step, wait) when rnn_sync_status
  *                          finds an error.
- *   RNN_TC_MAX_KS_FWD / RNN_TC_MAX_KS_BWD = 1..16
- *                          cap the tensor-core kernels' K split (CTAs per
- *                          cluster) in the forward / backward.
- *   RNN_TC_NB_FWD / RNN_TC_NB_BWD = 1, 2 or 4
- *                          fix their number of batch parts.
- *   RNN_GEMM_BN=128|256    force the tensor-core GEMM's tile width (no K split).
- *   RNN_CLUSTER_FWD=1      allow the cluster-resident forward for layers whose
- *                          gate rows fit one cluster (slower at the measured
- *                          shapes; off by default).
- * The status-record part of RNN_TRACE is fixed at rnn_create; the others are
- * read at every call (tensor-core plans are cached per shape and per value of
- * the four RNN_TC_ variables).
+ * The status-record part of RNN_TRACE is fixed at rnn_create.
  */
 #ifndef GB300_RNN_H
 #define GB300_RNN_H
@@ -292,22 +281,23 @@ int rnn_selected_algo(rnn_handle_t handle);
  * forward's two exchanges per step on the tensor cores). */
 int rnn_selected_fwd_algo(rnn_handle_t handle);
 
-/* Test hook for the timeout path: CTA ``cta`` (>= 0) of the next persistent
- * launches skips its per-step arrival, so its peers' bounded waits run out and
- * the call ends with RNN_TIMEOUT instead of hanging.  -1 (default) = off. */
-rnn_status_t rnn_debug_skip_arrival(rnn_handle_t handle, int cta);
-
 /* Per-kernel-class timing with CUDA events recorded on the launching stream
  * around every launch (off by default; costs two event records per launch).
  * Classes: 0 persistent forward, 1 persistent backward, 2 input-projection
  * GEMM, 3 input-gradient GEMM, 4 weight-gradient GEMMs (with their split-K
- * reduction), 5 reserved for the layout / pack kernels, which are not timed
- * (it reads 0).  rnn_get_timing waits for the recorded events, writes the summed
- * milliseconds (ms[6]) and launch counts (n[6]) since the last read, and
- * clears them.  Either output pointer may be NULL. */
-#define RNN_TIMING_CLASSES 6
+ * reduction), 5 sequence layout copies / casts (batch-first transposes, the
+ * upstream gradient's fp32 copy, y out), 6 weight / bias / state packing and
+ * the bias-gradient scatter, 7 the cell-state recomputation sweep.
+ * rnn_get_timing waits for the recorded events, writes the summed
+ * milliseconds (ms[8]) and launch counts (n[8]) since the last read, and
+ * clears them.  rnn_get_timing_ex also writes, per class, the algorithmic
+ * bytes of the timed launches (bytes[8]: every element read once and written
+ * once at its storage size; 0 for the classes that are bound by arithmetic,
+ * 0 to 4).  Any output pointer may be NULL. */
+#define RNN_TIMING_CLASSES 8
 rnn_status_t rnn_set_timing(rnn_handle_t handle, int enable);
 rnn_status_t rnn_get_timing(rnn_handle_t handle, double* ms, uint64_t* n);
+rnn_status_t rnn_get_timing_ex(rnn_handle_t handle, double* ms, uint64_t* n, double* bytes);
 
 /* Inference forward that allocates nothing on the device.
  *

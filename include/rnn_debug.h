@@ -1,7 +1,9 @@
 /*
  * rnn_debug.h - test hooks of librnn.so: the library's internal GEMM, run
- * directly so tests can check it element by element in isolation, and the
- * tensor-core planner's candidate ranking.
+ * directly so tests can check it element by element in isolation, the
+ * tensor-core planner's candidate ranking, plan overrides that force a kernel
+ * configuration, and a withheld arrival that exercises the timeout path.
+ * None of them is needed in normal use.
  *
  * C[row(m), n] = sum_k A(m,k) B(n,k) (+ bias[n]) (+ C if beta != 0)
  *   A(m,k) = A[m*lda + k] when a_kmajor, else A[k*lda + m] (same for B, n)
@@ -49,6 +51,24 @@ int rnn_debug_tc_plans(int mode, int bwd, int hidden, int batch, int ndir, int n
  * or 0 when the kernel cannot take the shape. */
 int rnn_debug_simt_plan(int mode, int reset_after, int is_bf16, int bwd, int hidden, int batch, int ndir,
                         int num_sms, int dwhh, int* out);
+
+/* Test hook for the timeout path: CTA ``cta`` (>= 0) of the next persistent
+ * launches of this handle skips its per-step arrival, so its peers' bounded
+ * waits run out and the call ends with RNN_TIMEOUT instead of hanging.
+ * -1 (default) = off.  RNN_BAD_PARAM for a NULL handle or cta < -1. */
+rnn_status_t rnn_debug_skip_arrival(rnn_handle_t handle, int cta);
+
+/* Test hook: process-wide overrides of the kernel plans, for tests that must
+ * reach a given configuration.  0 leaves a choice to the planner.
+ *   max_ks_fwd, max_ks_bwd  1..16: cap the tensor-core persistent kernels' K
+ *                           split (CTAs per cluster), forward / backward;
+ *   nb_fwd, nb_bwd          1, 2 or 4: fix their number of batch parts;
+ *   gemm_bn                 128 or 256: force the tensor-core GEMM's tile
+ *                           width (no K split).
+ * Other values are RNN_BAD_PARAM and change nothing.  Plans are cached per
+ * shape and per override set; set the overrides while no call of the library
+ * runs on another thread. */
+rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn);
 
 #ifdef __cplusplus
 }

@@ -1,5 +1,5 @@
 """Batch parts in the tensor-core persistent kernels: a row group's batch split
-over 1, 2 or 4 clusters (RNN_TC_NB_FWD / RNN_TC_NB_BWD force the count; by
+over 1, 2 or 4 clusters (the plan-override test hook forces the count; by
 default a per-step cost estimate chooses).  Against the fp64 oracle, tolerance
 2e-2 (bf16), and bit-identical results over repeated calls (the bias
 gradients of the parts are summed in part order)."""
@@ -25,9 +25,8 @@ def _wl(mode, ra, L, bidir, T, B, I, H, seed):
 @pytest.mark.parametrize("mode,ra,L,bidir,T,B,H", [("lstm", False, 1, False, 12, 64, 256),
                                                    ("gru", True, 2, True, 9, 40, 128),
                                                    ("lstm", False, 1, True, 8, 33, 128)])
-def test_batch_parts_parity(monkeypatch, nb, mode, ra, L, bidir, T, B, H):
-    monkeypatch.setenv("RNN_TC_NB_FWD", str(nb))
-    monkeypatch.setenv("RNN_TC_NB_BWD", str(nb))
+def test_batch_parts_parity(plan_overrides, nb, mode, ra, L, bidir, T, B, H):
+    plan_overrides(nb_fwd=nb, nb_bwd=nb)
     wl = _wl(mode, ra, L, bidir, T, B, 64, H, 800 + nb + B)
     inp = synth.make_inputs(wl)
     gpu = Hn.run_gpu(inp)
@@ -36,9 +35,8 @@ def test_batch_parts_parity(monkeypatch, nb, mode, ra, L, bidir, T, B, H):
 
 
 @pytest.mark.parametrize("nb", [2, 4])
-def test_batch_parts_with_lengths(monkeypatch, nb):
-    monkeypatch.setenv("RNN_TC_NB_FWD", str(nb))
-    monkeypatch.setenv("RNN_TC_NB_BWD", str(nb))
+def test_batch_parts_with_lengths(plan_overrides, nb):
+    plan_overrides(nb_fwd=nb, nb_bwd=nb)
     wl = _wl("lstm", False, 1, True, 10, 32, 64, 128, 810 + nb)
     lengths = np.array([10, 0, 1, 9, 5, 7, 10, 3] * 4)
     inp = dataclasses.replace(synth.make_inputs(wl), lengths=lengths)
@@ -49,8 +47,8 @@ def test_batch_parts_with_lengths(monkeypatch, nb):
 
 
 @pytest.mark.parametrize("nb", [2, 4])
-def test_batch_parts_reset_before_forward(monkeypatch, nb):
-    monkeypatch.setenv("RNN_TC_NB_FWD", str(nb))
+def test_batch_parts_reset_before_forward(plan_overrides, nb):
+    plan_overrides(nb_fwd=nb)
     wl = _wl("gru", False, 1, False, 8, 32, 64, 128, 820 + nb)
     inp = synth.make_inputs(wl)
     gpu = Hn.run_gpu(inp)
@@ -58,9 +56,8 @@ def test_batch_parts_reset_before_forward(monkeypatch, nb):
     Hn.compare(gpu, Hn.run_oracle(inp), wl)
 
 
-def test_batch_parts_repeatable(monkeypatch):
-    monkeypatch.setenv("RNN_TC_NB_FWD", "2")
-    monkeypatch.setenv("RNN_TC_NB_BWD", "4")
+def test_batch_parts_repeatable(plan_overrides):
+    plan_overrides(nb_fwd=2, nb_bwd=4)
     wl = _wl("gru", True, 1, False, 10, 64, 64, 256, 830)
     inp = synth.make_inputs(wl)
     a = Hn.run_gpu(inp)

@@ -33,7 +33,7 @@ def test_headline_flops_by_hand():
     assert fl["persist_fwd"] == fl["persist_bwd"] == 2 * 3 * 512 * 512 * 64 * 128
     assert fl["gemm_proj"] == fl["gemm_dx"] == 2 * 3 * 512 * 512 * 64 * 128
     assert fl["gemm_dw"] == 2 * fl["gemm_proj"]
-    assert fl["layout"] == 0.0
+    assert fl["layout_seq"] == fl["layout_pack"] == fl["recompute_cells"] == 0.0
 
 
 @pytest.mark.parametrize("name", sorted(synth.WORKLOADS))
@@ -97,10 +97,14 @@ def test_profiled_traffic_follows_the_sources(tmp_path, monkeypatch, sha_ok):
 
 
 def test_committed_profiles_name_a_traffic_and_a_sha():
+    import glob
+    found = 0
     for cls, path in bench.PROFILE_FOR_CLASS.items():
-        p = os.path.join(ROOT, path.format(workload=bench.DEFAULT_WORKLOAD))
-        keys = {ln.split(":", 1)[0].strip() for ln in open(p) if ":" in ln}
-        assert {"traffic-bytes-per-launch", "kernel-source-sha256"} <= keys, p
+        for p in glob.glob(os.path.join(ROOT, path.format(workload="*"))):
+            keys = {ln.split(":", 1)[0].strip() for ln in open(p) if ":" in ln}
+            assert {"traffic-bytes-per-launch", "kernel-source-sha256"} <= keys, p
+            found += 1
+    assert found >= 1
 
 
 # ---------------------------------------------------------------------------
@@ -160,3 +164,43 @@ def test_fp32_peak_derivation():
     # 152 SMs x 128 FP32 lanes x 2 flops per FMA x 2070 MHz
     assert bench.fp32_fma_tflops(152, 2070.0) == pytest.approx(80.54784)
     assert bench.load_peaks()["sm_max_mhz"] > 0
+
+
+# ---------------------------------------------------------------------------
+# layout kernels: achieved bandwidth = algorithmic bytes / event time, against
+# the HBM copy rate; classes with no launch are left out
+# ---------------------------------------------------------------------------
+def test_layout_report_bandwidth():
+    names = ("persist_fwd", "persist_bwd", "gemm_proj", "gemm_dx", "gemm_dw", "layout_seq", "layout_pack",
+             "recompute_cells")
+    ms = [5.0, 6.0, 1.0, 1.0, 1.0, 0.5, 0.1, 0.0]
+    n = [2, 2, 2, 2, 4, 2, 6, 0]
+    by = [0, 0, 0, 0, 0, 3.0e9, 2.0e8, 0]
+    rep = bench.layout_report(names, ms, n, by, 2, 6000.0)
+    assert set(rep) == {"layout_seq", "layout_pack"}
+    assert rep["layout_seq"]["achieved_gbs"] == pytest.approx(3.0e9 / 0.5e-3 / 1e9)
+    assert rep["layout_seq"]["frac_of_hbm"] == pytest.approx(6000.0 / 6000.0)
+    assert rep["layout_pack"]["bytes_per_step"] == pytest.approx(1.0e8)
+    assert rep["layout_pack"]["launches_per_step"] == 3
+
+
+def test_both_arms_share_the_config():
+    wl = synth.WORKLOADS[bench.DEFAULT_WORKLOAD]
+    a = bench.workload_config(wl, None, 1)
+    b = bench.workload_config(wl, synth.make_lengths(wl), 1)
+    assert a == b
+    assert a["workload"] == "lstm2bi_bf16_T512_B128_H1024"
+    assert "reserve_bytes" not in a
+
+
+def test_gpus_flag_starts_its_own_ranks():
+    # no WORLD_SIZE in the environment: bench.py starts 2 ranks itself
+    # (torch.distributed.run, gloo without a GPU) and rank 0 reports both
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--probe-ranks"],
+                       capture_output=True, text=True, env=env, cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    assert lines[0]["n_gpus"] == 2 and lines[0]["rank_sum"] == 3.0 and lines[0]["max_rank"] == 1.0

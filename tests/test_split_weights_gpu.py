@@ -3,7 +3,7 @@
 for K slices of more than 512 columns; and the automatic mixed choice, a
 tensor-core forward with the SIMT backward, for layers whose backward has no
 tensor-core plan (hidden 2048).  Against the fp64 oracle, tolerance 2e-2
-(bf16).  The K-split cap RNN_TC_MAX_KS_FWD=1 makes a hidden-1024 forward run
+(bf16).  A K-split cap of 1 (the plan-override test hook) makes a hidden-1024 forward run
 one 1024-column K slice per 128 gate rows, which takes the split tile."""
 import dataclasses
 
@@ -19,8 +19,8 @@ TC, SIMT = 1, 2
 
 
 @pytest.fixture
-def one_k_slice(monkeypatch):
-    monkeypatch.setenv("RNN_TC_MAX_KS_FWD", "1")
+def one_k_slice(plan_overrides):
+    plan_overrides(max_ks_fwd=1)
     yield
 
 
