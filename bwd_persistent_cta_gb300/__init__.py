@@ -68,6 +68,7 @@ _SIGS = {
     "rnn_get_timing_ex": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64),
                                          ctypes.POINTER(ctypes.c_double)]),
     "rnn_forward_noalloc": (ctypes.c_int, [ctypes.POINTER(rnn_desc_t)] + [_P] * 7 + [ctypes.c_int, _P]),
+    "rnn_noalloc_status": (ctypes.c_int, [_P]),
     "rnn_debug_gemm": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, ctypes.c_int64, ctypes.c_int,
                                       _P, ctypes.c_int64, ctypes.c_int, _P, ctypes.c_int64, ctypes.c_int, _P,
                                       ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int,
@@ -143,6 +144,12 @@ def rnn_forward_noalloc(desc: rnn_desc_t, x, hx, cx, w, y, hy, cy, sync: int = 1
     """Inference forward with no device allocation by the library (scratch is
     a fixed array inside librnn.so); see include/rnn.h."""
     return lib().rnn_forward_noalloc(ctypes.byref(desc), x, hx, cx, w, y, hy, cy, int(sync), stream)
+
+
+def rnn_noalloc_status(stream=None) -> int:
+    """Status of the last rnn_forward_noalloc call on the current device (waits
+    for ``stream`` and clears the status)."""
+    return lib().rnn_noalloc_status(stream)
 
 
 RNN_NOALLOC_SCRATCH_BYTES = 32 << 20

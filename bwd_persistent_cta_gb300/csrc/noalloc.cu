@@ -83,9 +83,25 @@ extern "C" rnn_status_t rnn_forward_noalloc(const rnn_desc_t* desc, const void* 
   if (cudaMemsetAsync(h.dev, 0, sizeof(rnn::DevArea), s) != cudaSuccess) return RNN_CUDA_ERROR;
   rs = rnn_forward(&h, x, hx, cx, w, y, hy, cy, static_cast<char*>(base) + area, nullptr, stream);
   if (rs != RNN_OK || !sync) return rs;
+  return rnn_noalloc_status(stream);
+}
+
+extern "C" rnn_status_t rnn_noalloc_status(void* stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RNN_CUDA_ERROR;
+  if (dev < 0 || dev >= kMaxDevices) return RNN_NOT_SUPPORTED;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    base = g_scratch_addr[dev];
+  }
+  if (!base) return RNN_OK;   // no call on this device yet
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return RNN_CUDA_ERROR;
+  rnn::DevArea* area = static_cast<rnn::DevArea*>(base);
   unsigned int code = 0;
-  if (cudaMemcpy(&code, &h.dev->status, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(&code, &area->status, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
     return RNN_CUDA_ERROR;
+  if (code != 0 && cudaMemset(&area->status, 0, sizeof(code)) != cudaSuccess) return RNN_CUDA_ERROR;
   return static_cast<rnn_status_t>(code);
 }

@@ -24,31 +24,43 @@ struct TcPlan {
   int KS = 0, Kc = 0, nsub = 0, R = 0, Npad = 0, UPC = 0, PP = 0, nrg = 0, w_tmem = 0;
   int NB = 1, Bp = 0;   // batch parts per row group, batch rows per part
   uint32_t tmem_cols = 0, off_ring = 0, off_recv = 0, off_bar = 0;
+  uint32_t wcol = 0;   // first TMEM column of the weight sub-tiles (w_tmem > 0)
   size_t smem = 0;
 };
 
 size_t a1k(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
-// Estimated per-step cost (us) of a plan's parts that differ between plans,
-// fitted to GB300 step traces and sweeps (T=128..512, B 32..128, H 512..1024):
-// MMA issue ~55 ns per K=16 instruction (issue-bound at N <= 128), the
-// DSMEM partial push ~33 ns per KB (51 in clusters of 16), the epilogue
-// ~0.35 us (forward) / 0.5 us (backward) per pair per thread, and the cluster
-// barrier by cluster size.  The counter exchange and TMA are about equal
-// across plans.  Examples it ranks as measured: GRU resetAfter B64 H512 takes
-// K split 4 / 2 batch parts forward (0.586 -> 0.477 ms) and 8 / 2 backward
-// (0.819 -> 0.606 ms); LSTM B32 H1024 keeps 4 / 1 and 8 / 1 (2 parts: 1.08 ->
-// 1.18 ms forward, 1.30 -> 1.56 ms backward); the 2-layer bidirectional LSTM
-// B128 H1024 backward takes 4 / 4 (17.8 -> 14.0 ms); GRU B128 H512 without
-// parts keeps a split of 16 over 8 (1.25 vs 1.35 ms).
+// Estimated per-step cost (us) of a plan, fitted to GB300 step-phase traces
+// (timestamps inside the kernels) of the LSTM at hidden 1024 with batch 32 and
+// 128 and the GRU at hidden 512:
+//   MMA      about 40 ns + 0.07 ns per batch column for each K=16 instruction
+//            (42 ns at N=32, 49 ns at N=128: a fixed cost per instruction
+//            dominates, so wide N is almost free);
+//   TMA      the step's K slice of the exchanged state, 0.3 us + 4 ns per KB;
+//   push     the K-split partials over distributed shared memory, 0.2 us +
+//            35 ns per KB (51 ns per KB in clusters of 16), none without a
+//            K split;
+//   cluster  the cluster barrier with the abort flags, about 0.6 us (1.6 us
+//            in clusters of 16);
+//   epilogue partial sums and cell math, about 0.15 us per (unit, batch row)
+//            pair each thread owns, and in the forward as much again for the
+//            stores after the step's release.
+// The counter wait and release (about 1.8 us) are the same for every plan.
+// Measured against these estimates: LSTM B128 H1024 forward, K split 2 x one
+// batch part, 9.2 us per step (both directions); backward, K split 4 x 4 batch
+// parts, 7.3 us per direction; LSTM B32 H1024 forward 4 x 1, 4.4 us; backward
+// 8 x 1, 5.3 us.
 double plan_cost(int bwd, int KS, int Kc, int Npad, int pairs) {
-  const double mma = 0.055 * (Kc / 16);
+  const double n_mma = Kc / 16;
+  const double mma = (0.040 + 0.00007 * Npad) * n_mma;
+  const double tma = 0.3 + 0.004 * (static_cast<double>(Kc) * Npad * 2 / 1024.0);
   const double push_kb = 128.0 * Npad * 4 * (KS - 1) / KS / 1024.0;
-  const double push = push_kb * (KS >= 16 ? 0.051 : 0.033);
+  const double push = KS > 1 ? 0.2 + push_kb * (KS >= 16 ? 0.051 : 0.035) : 0.1;
+  const double cl = KS >= 16 ? 1.6 : KS > 1 ? 0.62 : 0.05;
   const double per_thread = (pairs + kThreads - 1) / kThreads;
-  const double epi = (bwd ? 0.5 : 0.35) * per_thread;
-  const double cl = KS >= 16 ? 1.6 : KS >= 8 ? 0.8 : KS >= 4 ? 0.7 : KS >= 2 ? 0.6 : 0.2;
-  return mma + push + epi + cl;
+  const double epi = bwd ? 0.14 + 0.14 * per_thread : 0.09 + 0.15 * per_thread;
+  const double post = bwd ? 0.0 : 0.15 * per_thread;
+  return mma + tma + push + cl + epi + post;
 }
 
 // Candidate plans for one launch (K split x batch parts), cheapest first by
@@ -94,18 +106,23 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
         smem = a1k(wbytes) + a1k(R * rb) + a1k(recv) + a1k(sizeof(TcBars)) + 1024;
         if (smem <= kSmemCap) break;
       }
-      // else weight sub-tiles in TMEM columns [256, 512) (an even count, at
-      // most 8), the others in shared memory, and the whole K slice of the
-      // exchange operand in flight at once
+      // else the first wt weight sub-tiles (an even count) in tensor memory as
+      // the MMA A operand, in the columns the accumulator leaves free at the top
+      // (wcol = 512 - 32 * wt >= Npad), the others in shared memory, and the
+      // whole K slice of the exchange operand in flight at once; the fewest
+      // sub-tiles in tensor memory that fit
       int wt = 0;
       if (R < nsub && Npad <= 256) {
-        const int t = (nsub < 8 ? nsub : 8) & ~1;
-        const size_t sm2 = a1k(static_cast<size_t>(nsub - t) * kWSub) + a1k(static_cast<size_t>(nsub) * rb) +
-                           a1k(recv) + a1k(sizeof(TcBars)) + 1024;
-        if (t >= 2 && sm2 <= kSmemCap) {
-          wt = t;
-          R = nsub;
-          smem = sm2;
+        const int tmax = std::min(nsub, (512 - Npad) / 32) & ~1;
+        for (int t = 2; t <= tmax; t += 2) {
+          const size_t sm2 = a1k(static_cast<size_t>(nsub - t) * kWSub) + a1k(static_cast<size_t>(nsub) * rb) +
+                             a1k(recv) + a1k(sizeof(TcBars)) + 1024;
+          if (sm2 <= kSmemCap) {
+            wt = t;
+            R = nsub;
+            smem = sm2;
+            break;
+          }
         }
       }
       if (!wt && (R < 1 || (R < nsub && R < 2))) continue;
@@ -123,6 +140,7 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
       // second CTA off the SM
       const size_t floor = wt ? kOneCtaSmem : kMinSmem;
       p.smem = smem < floor ? floor : smem;
+      p.wcol = wt ? 512u - 32u * static_cast<uint32_t>(wt) : 0u;
       cands.emplace_back(plan_cost(bwd, KS, Kc, Npad, UPC * Bp), p);
     }
   }
@@ -304,7 +322,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   P.single = single;
   const uint64_t proj_bytes = static_cast<uint64_t>(a.T) * a.B * D * 4 * H * 2;
   P.prefetch = !bwd && proj_bytes > (32ull << 20);
-  P.wcol = 256;
+  P.wcol = pl.wcol;
   const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];

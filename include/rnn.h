@@ -313,7 +313,10 @@ rnn_status_t rnn_get_timing_ex(rnn_handle_t handle, double* ms, uint64_t* n, dou
  *   x, hx, cx, w, y, hy, cy  as for rnn_forward (caller-owned device memory)
  *   sync                  nonzero: synchronise ``stream`` and return the
  *                         device status (RNN_TIMEOUT when a spin-wait gave up);
- *                         zero: return once the work is queued
+ *                         zero: return once the work is queued - a device
+ *                         timeout of that call is then reported only by
+ *                         rnn_noalloc_status, which must run before the next
+ *                         call on the device (each call clears the status)
  * Returns RNN_NOT_SUPPORTED when the problem's workspace plus 256 bytes of
  * counters exceeds RNN_NOALLOC_SCRATCH_BYTES (nothing is launched then).
  * The first call on each device looks up the array's device address (with that
@@ -324,6 +327,14 @@ rnn_status_t rnn_get_timing_ex(rnn_handle_t handle, double* ms, uint64_t* n, dou
 #define RNN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 rnn_status_t rnn_forward_noalloc(const rnn_desc_t* desc, const void* x, const void* hx, const void* cx,
                                  const void* w, void* y, void* hy, void* cy, int sync, void* stream);
+
+/* Status of the last rnn_forward_noalloc call on the current device: waits
+ * for ``stream`` (the stream that call used), reads the device status word
+ * (RNN_OK, or RNN_TIMEOUT when a spin-wait of that call gave up, in which case
+ * its y / hy / cy are incomplete) and clears it.  Allocates nothing.
+ * RNN_OK when no call has run on this device yet; RNN_CUDA_ERROR when the
+ * stream cannot be synchronised. */
+rnn_status_t rnn_noalloc_status(void* stream);
 
 /* Static text for a status code. */
 const char* rnn_status_string(rnn_status_t status);
