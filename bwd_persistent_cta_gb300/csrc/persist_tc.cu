@@ -99,6 +99,9 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
       const size_t wbytes = static_cast<size_t>(nsub) * kWSub;
       const size_t rb = static_cast<size_t>(Npad) * 128;
       const size_t recv = static_cast<size_t>(Npad) * 128 * 4;
+      // without a K split the forward stages warp 0's post-step values (32 B
+      // per pair) in the receive buffer
+      if (KS == 1 && !bwd && recv < static_cast<size_t>(32) * PP * 32) continue;
       // weight tile in shared memory, with the deepest exchange ring that fits
       int R = nsub < kMaxRing ? nsub : kMaxRing;
       size_t smem = 0;

@@ -76,8 +76,16 @@ __device__ unsigned long long g_step_trace[2][2][1100][16];
         (step_) < 1100)                                                                          \
       g_step_trace[(kind_)][blockIdx.x == 0 ? 0 : 1][(step_)][(slot_)] = globaltimer_ns();       \
   } while (0)
+// the same, recorded by thread tid_ instead of thread 0
+#define RNN_TRACE_AT_T(tid_, slot_, kind_, step_)                                                  \
+  do {                                                                                          \
+    if (threadIdx.x == (tid_) && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1) && blockIdx.y == 0 && \
+        (step_) < 1100)                                                                          \
+      g_step_trace[(kind_)][blockIdx.x == 0 ? 0 : 1][(step_)][(slot_)] = globaltimer_ns();       \
+  } while (0)
 #else
 #define RNN_TRACE_AT(slot_, kind_, step_) do { } while (0)
+#define RNN_TRACE_AT_T(tid_, slot_, kind_, step_) do { } while (0)
 #endif
 
 constexpr int kThreads = 256;             // warps 0-3 read TMEM; all 8 run the cell epilogue
@@ -111,6 +119,9 @@ struct TcBars {
   uint64_t empty[kMaxRing];      // exchange sub-tile consumed (tcgen05.commit)
   int flags[2][kMaxKS];          // abort flags pushed by the peers, by step parity
   uint32_t tmem;
+  // forward: thread 0's post-step values (4 gates, h, c, y) per pair, stored
+  // by thread 32 during the next step while thread 0 drives the contraction
+  float stage[8][7];
 };
 
 // The forward requests the input projections of the step this many steps
@@ -230,7 +241,8 @@ __device__ __forceinline__ void push_partials(const TcPersistParams& P, uint32_t
   const int q = warp & 3, half = warp >> 2;
   const int row = q * 32 + lane;
   const int owner = row / P.RPC, lr = row - owner * P.RPC;
-  float* dst = peer_ptr(recv, owner) + static_cast<size_t>(ks) * P.Npad * P.RPC + lr;
+  // the rows this CTA owns itself go by local shared-memory stores
+  float* dst = (owner == ks ? recv : peer_ptr(recv, owner)) + static_cast<size_t>(ks) * P.Npad * P.RPC + lr;
   for (int c = half * 32; c < P.Npad; c += 64) {
     float v[32];
     tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
@@ -243,15 +255,29 @@ __device__ __forceinline__ void push_partials(const TcPersistParams& P, uint32_t
 // The per-step exchange and contraction, up to the point where this CTA's
 // units' summed pre-activations can be read from ``recv``.  Returns true when
 // the whole cluster may continue.
-__device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, const CUtensorMap* tmX4,
+// ``deferred`` runs on every thread while the step's contraction is under
+// way: on thread 0 after it has passed the counter wait and issued the step's
+// TMA and MMAs, on the others at once (the previous step's stores that no CTA
+// of this launch waits for, kept off the wait's critical path).
+struct NoDeferred {
+  __device__ void operator()() const {}
+};
+template <typename Deferred = NoDeferred>
+__device__ __forceinline__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, const CUtensorMap* tmX4,
                               uint8_t* ring, float* recv, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0,
                               int y4, int c2, int dir, uint32_t idesc,
                               uint64_t adesc0, bool do_contract, unsigned int wait_target, int s, int ks, int& n_mma,
-                              bool& w_waited, unsigned int kernel) {
+                              bool& w_waited, unsigned int kernel, const Deferred& deferred = Deferred()) {
   const PersistArgs& a = P.a;
   const int tk = kernel == K_BWD_TC ? 1 : 0;
   (void)tk;
   int ok = 1;
+  // warp 0's other lanes first: they would otherwise run their share only
+  // once thread 0 leaves its wait and issue (divergent paths of one warp)
+  if ((threadIdx.x >> 5) == 0) {
+    if (threadIdx.x != 0) deferred();
+    __syncwarp();
+  }
   if (threadIdx.x == 0) {
     if (wait_target > 0 && !wait_counter_geq(&a.dev->counters[a.dir0 + blockIdx.y], wait_target, a.timeout_ns)) {
       ok = 0;
@@ -267,6 +293,8 @@ __device__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, 
     }
     RNN_TRACE_AT(2, tk, s);
   }
+  if ((threadIdx.x >> 5) != 0) deferred();
+  RNN_TRACE_AT_T(32, 15, tk, s);
   ok = __syncthreads_and(ok);
   if (ok && do_contract) {
     const bool done = mbar_wait(&bars.mma, n_mma & 1, a.timeout_ns);
@@ -474,6 +502,111 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   uint32_t g = 0;
   int n_mma = 0;
   bool w_waited = false;
+  bool aborted = false;
+  // the step's new state and gate values: the state goes out before the
+  // step's release; the rest is stored during the next step's contraction
+  float hv[PP];
+  float gq[PP][4];
+  // stores of step sd that no CTA of this launch waits for (pair id: its 4
+  // gate values, the new state h, the LSTM cell c and the output y), and the
+  // L2 prefetch of a later step's projections
+  auto store_pair = [&](int sd, int id, const float (&g4)[4], float h, float c, float yv) {
+    const int t = dir ? TT - 1 - sd : sd;
+    const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
+    // one prefetch per 128-byte line of the projections (16 units)
+    if (P.prefetch && sd + kPrefetchSteps < TT && ((u & 15) == 0 || ul == 0)) {
+      const int tf = dir ? TT - 1 - (sd + kPrefetchSteps) : sd + kPrefetchSteps;
+      prefetch_l2(Pm + (static_cast<int64_t>(tf) * B + b) * ldP + dir * 4 * H + 4 * u);
+    }
+    if (G) Vec4<__nv_bfloat16>::store(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * 4 * H + 4 * u, g4);
+    if (lstm && a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = c;
+    if (a.y_out)
+      static_cast<__nv_bfloat16*>(a.y_out)[(static_cast<int64_t>(t) * B + b) * ldY + dir * H + u] =
+          __float2bfloat16_rn(yv);
+    if (sd == TT - 1) {
+      const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
+      if (a.hy) static_cast<__nv_bfloat16*>(a.hy)[o] = __float2bfloat16_rn(h);
+      if (lstm && a.cy) static_cast<__nv_bfloat16*>(a.cy)[o] = __float2bfloat16_rn(c);
+    }
+  };
+  auto y_of = [&](int sd, int p) {
+    float yv = hv[p];
+    if constexpr (EXT) {
+      const int t = dir ? TT - 1 - sd : sd;
+      if (t >= lenp[p]) yv = 0.f;
+    }
+    return yv;
+  };
+  // The stores of a step take about 0.15 us per pair a thread owns and must
+  // not delay thread 0, which drives the next step's wait, TMA and MMAs.
+  // Without a K split the receive buffer is idle from the end of a step until
+  // the next step's partials land: warp 0 stages all its pairs' values there
+  // (8 floats each: 4 gates, h, c, y) and warps 1-7 store them.  With a K
+  // split peers may write the receive buffer at any time: thread 0 alone
+  // stages its pairs (bars.stage) for thread 32, and warp 0's other lanes
+  // store theirs before thread 0 starts its wait.
+  constexpr bool kStageWarp0 = KS == 1;
+  float* const stage_w0 = recv;
+  auto post_stores = [&](int sd, bool own) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool mine = own || (kStageWarp0 ? warp != 0 : threadIdx.x != 0);
+    if (mine) {
+#pragma unroll
+      for (int p = 0; p < PP; ++p) {
+        const int id = threadIdx.x + p * kThreads;
+        if (id >= npairs) break;
+        store_pair(sd, id, gq[p], hv[p], st[p], y_of(sd, p));
+      }
+    }
+    if (own) return;
+    if constexpr (kStageWarp0) {
+      if (warp != 0) {
+        // staged entry j = warp-0 lane j % 32, pair j / 32
+        for (int j = (warp - 1) * 32 + lane; j < 32 * PP; j += 7 * 32) {
+          const int id = (j & 31) + (j >> 5) * kThreads;
+          if (id >= npairs) continue;
+          const float4 g = *reinterpret_cast<const float4*>(stage_w0 + 8 * j);
+          const float4 r = *reinterpret_cast<const float4*>(stage_w0 + 8 * j + 4);
+          const float g4[4] = {g.x, g.y, g.z, g.w};
+          store_pair(sd, id, g4, r.x, r.y, r.z);
+        }
+      }
+    } else if (threadIdx.x == 32) {
+#pragma unroll
+      for (int p = 0; p < PP; ++p) {
+        const int id = p * kThreads;
+        if (id >= npairs) break;
+        const float* v = bars.stage[p];
+        const float g4[4] = {v[0], v[1], v[2], v[3]};
+        store_pair(sd, id, g4, v[4], v[5], v[6]);
+      }
+    }
+  };
+  // the staging of step sd's values (ordered before the readers by the
+  // barrier of the step's release; without a K split after a barrier that
+  // ends every read of the step's partial sums)
+  auto stage_own = [&](int sd) {
+    if constexpr (kStageWarp0) {
+      __syncthreads();
+      if ((threadIdx.x >> 5) != 0) return;
+#pragma unroll
+      for (int p = 0; p < PP; ++p) {
+        if (static_cast<int>(threadIdx.x) + p * kThreads >= npairs) break;
+        float* v = stage_w0 + 8 * (threadIdx.x + 32 * p);
+        *reinterpret_cast<float4*>(v) = make_float4(gq[p][0], gq[p][1], gq[p][2], gq[p][3]);
+        *reinterpret_cast<float4*>(v + 4) = make_float4(hv[p], st[p], y_of(sd, p), 0.f);
+      }
+    } else {
+      if (threadIdx.x != 0) return;
+#pragma unroll
+      for (int p = 0; p < PP; ++p) {
+        if (p * kThreads >= npairs) break;
+        float* v = bars.stage[p];
+        v[0] = gq[p][0]; v[1] = gq[p][1]; v[2] = gq[p][2]; v[3] = gq[p][3];
+        v[4] = hv[p]; v[5] = st[p]; v[6] = y_of(sd, p);
+      }
+    }
+  };
   for (int s = 0; s < TT; ++s) {
     const int t = dir ? TT - 1 - s : s;
     const int sp = dir ? t + 2 : t;
@@ -488,11 +621,16 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       pq[p] = id < npairs ? ld_u2(Pm + (static_cast<int64_t>(t) * B + b) * ldP + dir * 4 * H + 4 * u) : make_uint2(0, 0);
     }
     const int ex = rbm ? 2 * s : s;   // exchanges (counter phases) before this step's first
+    auto deferred = [&]() {
+      if (s > 0) post_stores(s - 1, false);
+    };
     if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B + b0, sp * B + b0,
                        ks * P.nsub,
                        dir, idesc, adesc0, true, static_cast<unsigned int>(ex) * P.nblk_dir, ex, ks, n_mma, w_waited,
-                       K_FWD_TC))
+                       K_FWD_TC, deferred)) {
+      aborted = true;
       break;
+    }
     // partial sums of every pair first (all shared loads in flight), then the cell
     float4 acc[PP];
 #pragma unroll
@@ -512,8 +650,6 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       }
     }
     RNN_TRACE_AT(12, 0, s);
-    float hv[PP];
-    float gq[PP][4];
 #pragma unroll
     for (int p = 0; p < PP; ++p) {
       const int id = threadIdx.x + p * kThreads;
@@ -572,8 +708,10 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         step_arrive(a, skip, s, 0);
         if (!step_exchange(P, &tmR, &tmR4, ring, recv, bars, tmem, g, ks * P.Kc, (dir * TT + t) * B + b0, t * B + b0,
                            ks * P.nsub, dir, idesc, adesc0, true, static_cast<unsigned int>(ex + 1) * P.nblk_dir,
-                           ex + 1, ks, n_mma, w_waited, K_FWD_TC))
+                           ex + 1, ks, n_mma, w_waited, K_FWD_TC)) {
+          aborted = true;
           break;
+        }
 #pragma unroll
         for (int p = 0; p < PP; ++p) {
           const int id = threadIdx.x + p * kThreads;
@@ -597,42 +735,12 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       }
     }
     RNN_TRACE_AT(13, 0, s);
+    stage_own(s);
     RNN_TRACE_AT(5, 0, s);
     step_arrive(a, skip, s, 0);
     RNN_TRACE_AT(6, 0, s);
-    // stores nothing in this launch waits for, and the prefetch of later projections
-    if (P.prefetch && s + kPrefetchSteps < TT) {
-      const int tf = dir ? TT - 1 - (s + kPrefetchSteps) : s + kPrefetchSteps;
-#pragma unroll
-      for (int p = 0; p < PP; ++p) {
-        const int id = threadIdx.x + p * kThreads;
-        if (id >= npairs) break;
-        const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
-        prefetch_l2(Pm + (static_cast<int64_t>(tf) * B + b) * ldP + dir * 4 * H + 4 * u);
-      }
-    }
-#pragma unroll
-    for (int p = 0; p < PP; ++p) {
-      const int id = threadIdx.x + p * kThreads;
-      if (id >= npairs) break;
-      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
-      if (G) Vec4<__nv_bfloat16>::store(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * 4 * H + 4 * u, gq[p]);
-      if (lstm && a.C) a.C[((static_cast<int64_t>(dir) * (TT + 1) + (dir ? t : t + 1)) * B + b) * H + u] = st[p];
-      if (a.y_out) {
-        float yv = hv[p];
-        if constexpr (EXT) {
-          if (t >= lenp[p]) yv = 0.f;
-        }
-        static_cast<__nv_bfloat16*>(a.y_out)[(static_cast<int64_t>(t) * B + b) * ldY + dir * H + u] =
-            __float2bfloat16_rn(yv);
-      }
-      if (s == TT - 1) {
-        const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
-        if (a.hy) static_cast<__nv_bfloat16*>(a.hy)[o] = __float2bfloat16_rn(hv[p]);
-        if (lstm && a.cy) static_cast<__nv_bfloat16*>(a.cy)[o] = __float2bfloat16_rn(st[p]);
-      }
-    }
   }
+  if (!aborted) post_stores(TT - 1, true);
   teardown(P, bars);
 }
 
