@@ -13,9 +13,10 @@
 //   warp 0       TMA producer (one elected thread)
 //   warp 1       TMEM owner and MMA issuer (one elected thread); M=128, N=BN,
 //                K=16 per tcgen05.mma, 128-byte swizzled operands
-//   warps 2..5   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//                lanes 32*(w%4) .. +31 = tile rows), bias / accumulate / cast,
-//                global stores with the gate-slot row remap
+//   warps 2..9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//                lanes 32*(w%4) .. +31 = tile rows; warps 2-5 the first half
+//                of the tile's columns, warps 6-9 the second), bias /
+//                accumulate / cast, global stores with the gate-slot row remap
 // Two TMEM accumulators (2 x BN columns) let the epilogue of one tile overlap
 // the main loop of the next.  Operands may be K-major (row = M or N index, K
 // contiguous) or MN-major (K = row index, M or N contiguous); the descriptor
@@ -37,7 +38,8 @@ namespace rnn {
 namespace {
 
 constexpr int BM = 128, BK = 64;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int kMaxSplits = 16;
 
@@ -177,7 +179,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&sm.tfull[b], 1); mbar_init(&sm.tempty[b], 4); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&sm.tfull[b], 1); mbar_init(&sm.tempty[b], kEpiWarps); }
     sm.abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
@@ -255,6 +257,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     const int q = warp & 3;              // TMEM lane quarter of this warp
+    const int c_lo = (warp - 2) / 4 * (BN / 2), c_hi = c_lo + BN / 2;   // its half of the columns
     uint32_t acc = 0;
     for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++acc) {
       const int tile = item % ntiles, sp = item / ntiles;
@@ -277,7 +280,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (pm < 0) write = false;
         row = static_cast<int64_t>(pm) * p.rowmap_H + (m >> 2);
       }
-      for (int c = 0; c < BN; c += 32) {
+      for (int c = c_lo; c < c_hi; c += 32) {
         float v[32];
         tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c, v);
         if (write && n0 + c < p.N) {

@@ -102,7 +102,9 @@ struct TcPersistParams {
   int KS, Kc, nsub, R, Npad, UPC, RPC;
   int w_tmem;              // 64-column weight sub-tiles held in tensor memory (the A operand from TMEM):
                            // sub-tiles [0, w_tmem) there, [w_tmem, nsub) in shared memory
-  int single;              // the whole K slice arrives with one 4-D TMA per step (R == nsub)
+  int single;              // the whole K slice arrives with 4-D TMAs issued at the step's start (R == nsub)
+  int nchunk;              // single: that many 4-D TMAs of nsub / nchunk sub-tiles, each on its own
+                           // mbarrier, so the MMAs start when the first chunk lands
   int prefetch;            // forward: request later steps' projections into L2 (kPrefetchSteps)
   int nrg;                 // 128-row groups per direction
   int NB, Bp;              // batch parts per row group and batch rows per part (Npad = Bp rounded up to 16)
@@ -188,15 +190,20 @@ __device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, 
   if (P.single) {
     // the previous step's MMAs on the ring finished before this CTA released
     // that step, and every CTA's did before the counter let this load start
-    mbar_arrive_expect_tx(&bars.full[0], static_cast<uint32_t>(nsub) * rbytes);
-    tma_load_4d(ring, tmX4, &bars.full[0], 0, y4, c2, dir);
+    const int nc = P.nchunk, per = nsub / nc;
+    for (int c = 0; c < nc; ++c) {
+      mbar_arrive_expect_tx(&bars.full[c], static_cast<uint32_t>(per) * rbytes);
+      tma_load_4d(ring + static_cast<size_t>(c) * per * rbytes, tmX4, &bars.full[c], 0, y4, c2 + c * per, dir);
+    }
     RNN_TRACE_AT(1, tk, s);
     if (first_use_w && P.w_tmem < P.nsub && !mbar_wait(&bars.wbar, 0, to)) return false;
-    if (!mbar_wait(&bars.full[0], g & 1, to)) return false;
-    RNN_TRACE_AT(8, tk, s);
-    RNN_TRACE_AT(14, tk, s);
-    tc_fence_after();
-    for (int j = 0; j < nsub; ++j) mma_subtile(P, tmem, adesc0, bdesc0, rbytes, idesc, j, j);
+    for (int c = 0; c < nc; ++c) {
+      if (!mbar_wait(&bars.full[c], g & 1, to)) return false;
+      if (c == 0) RNN_TRACE_AT(8, tk, s);
+      if (c == nc - 1) RNN_TRACE_AT(14, tk, s);
+      tc_fence_after();
+      for (int j = c * per; j < (c + 1) * per; ++j) mma_subtile(P, tmem, adesc0, bdesc0, rbytes, idesc, j, j);
+    }
     mma_commit(&bars.mma);
     g += 1;
     return true;
