@@ -376,7 +376,7 @@ struct DeviceGuard {
 namespace rnn {
 namespace {
 std::mutex g_override_mu;
-PlanOverrides g_override{0, 0, 0, 0, 0};
+PlanOverrides g_override{0, 0, 0, 0, 0, 0};
 }  // namespace
 PlanOverrides plan_overrides() {
   std::lock_guard<std::mutex> lock(g_override_mu);
@@ -533,14 +533,15 @@ int rnn_selected_fwd_algo(rnn_handle_t h) {
   return h ? (h->fwd_tc ? RNN_ALGO_PERSIST_TC : h->algo) : 0;
 }
 
-rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn) {
+rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn,
+                                          int gemm_splits) {
   auto ks_ok = [](int v) { return v >= 0 && v <= 16; };
   auto nb_ok = [](int v) { return v == 0 || v == 1 || v == 2 || v == 4; };
   if (!ks_ok(max_ks_fwd) || !ks_ok(max_ks_bwd) || !nb_ok(nb_fwd) || !nb_ok(nb_bwd) ||
-      !(gemm_bn == 0 || gemm_bn == 128 || gemm_bn == 256))
+      !(gemm_bn == 0 || gemm_bn == 128 || gemm_bn == 256) || !ks_ok(gemm_splits))
     return RNN_BAD_PARAM;
   std::lock_guard<std::mutex> lock(rnn::g_override_mu);
-  rnn::g_override = {max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn};
+  rnn::g_override = {max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn, gemm_splits};
   return RNN_OK;
 }
 
@@ -799,6 +800,10 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
   for (int l = 0; l < L; ++l) {
     const int Il = layer_in(h, l);
     const void* Xl = l == 0 ? x0 : rs + h->r_y[l - 1] + static_cast<size_t>(B) * D * H * es;
+    // the layer's weight-gradient GEMMs (every direction, W_ih and W_hh):
+    // one grouped launch on the tensor cores, else one SIMT launch each
+    GemmArgs grp[6];
+    int ng = 0;
     for (int d = 0; d < D; ++d) {
       const int i = l * D + d;
       const char* dG = rs + h->r_dg[l] + static_cast<size_t>(d) * 4 * H * es;
@@ -809,12 +814,13 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
       // long K = T*B: the projection buffer (idle here) holds split-K partials
       g.split_ws = at<char>(workspace, h->w_p);
       g.split_ws_bytes = TB * D * 4 * H * es;
+      g.in_bf16 = h->bf16;
       // dW_ih = sum over (t, b) of dG x^T
       g.N = Il;
       g.B = Xl; g.ldb = Il; g.b_kmajor = 0;
       g.C = dwf + h->off_ih[i]; g.ldc = Il; g.c_bf16 = 0;
       for (int k = 0; k < 4; ++k) g.perm[k] = m_ih[k];
-      RNN_TRY(run_gemm(h, g, s, 4));
+      grp[ng++] = g;
       if (h->dw_bptt) {
         // accumulated by the backward-data pass, already in the caller's rows
         const size_t bytes = static_cast<size_t>(h->G) * H * H * 4;
@@ -829,14 +835,25 @@ rnn_status_t rnn_backward_weights(rnn_handle_t h, const void* x, const void* hx,
         g.B = hp; g.ldb = D * H; g.b_kmajor = 0;
         g.C = dwf + h->off_hh[i]; g.ldc = H;
         for (int k = 0; k < 4; ++k) g.perm[k] = m_hh[k];
-        RNN_TRY(run_gemm(h, g, s, 4));
+        grp[ng++] = g;
         if (h->rb) {
           // reset-before candidate rows: dW_hn = sum dn (r * h_prev)^T
           g.B = rs + h->r_rh[l] + static_cast<size_t>(d) * TB * H * es; g.ldb = H;
           g.perm[0] = -1; g.perm[1] = -1; g.perm[2] = pos[2]; g.perm[3] = -1;
-          RNN_TRY(run_gemm(h, g, s, 4));
+          grp[ng++] = g;
         }
       }
+    }
+    bool tc = h->bf16;
+    for (int k = 0; k < ng && tc; ++k) tc = gemm_tc_supported(grp[k]);
+    if (tc) {
+      TimeScope ts(h, 4, s);
+      RNN_TRY(count(h, launch_gemm_tc_grouped(grp, ng, s, h->num_sms, h->dev, h->timeout_ns)));
+    } else {
+      for (int k = 0; k < ng; ++k) RNN_TRY(run_gemm(h, grp[k], s, 4));
+    }
+    for (int d = 0; d < D; ++d) {
+      const int i = l * D + d;
       // bias gradients back to the caller's gate blocks (batched below)
       PackJob j;
       j.kind = SCATTER_DB; j.H = H;
@@ -889,7 +906,7 @@ extern "C" rnn_status_t rnn_debug_gemm(int M, int N, int K, const void* A, int64
   static void* ws = nullptr;
   static size_t ws_bytes = 0;
   if (!c_bf16 && use_tc) {
-    const size_t need = static_cast<size_t>(16) * M * N * sizeof(float);
+    const size_t need = gemm_tc_split_scratch_bytes(M, N);
     if (need > ws_bytes) {
       if (ws) cudaFree(ws);
       ws = nullptr;

@@ -22,10 +22,20 @@
 // contiguous) or MN-major (K = row index, M or N contiguous); the descriptor
 // major-ness bits select which.
 //
-// Split K (a long K with too few tiles to fill the GPU, i.e. the weight
-// gradients): work item (tile, s) covers K slice s of S and stores its raw
-// fp32 partial product to scratch; a second kernel sums the S partials of
-// every element in split order (deterministic) and applies the epilogue.
+// Groups: one launch may cover up to kMaxGroups GEMMs with the same K and
+// operand major-ness (the weight gradients of a layer: W_ih and W_hh of every
+// direction), each with its own operands, output and epilogue; their tiles
+// share the grid.
+//
+// Split K (a long K whose tiles fill the GPU in too few waves, i.e. the
+// weight gradients): work item (s, tile) covers K slice s of S, and items run
+// split by split (every split-0 item precedes every split-1 item in each
+// CTA's order).  Split s > 0 waits until every epilogue warp of split s - 1
+// of its tile has released the tile's counter, adds its accumulator to the
+// stored fp32 partial (fixed order: deterministic), and stores the sum back
+// (s < S - 1) or applies the epilogue (s = S - 1).  The wait always ends:
+// every CTA is resident (one per SM, grid <= SMs), and the item waited for
+// precedes the waiting one in the global order, which every CTA follows.
 // Every wait is bounded; on timeout the kernel records RNN_TIMEOUT in the
 // status word and leaves its loops.
 #include <atomic>
@@ -42,6 +52,7 @@ constexpr int kThreads = 320;
 constexpr int kEpiWarps = 8;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int kMaxSplits = 16;
+constexpr int kMaxGroups = 6;
 
 template <int BN>
 struct GemmCfg {
@@ -62,18 +73,31 @@ struct alignas(1024) GemmSmem {
   int abort_flag;
 };
 
-struct TcGemmParams {
-  int M, N, K;
-  int a_kmajor, b_kmajor;
+// One GEMM of a launch: C[row(m), n] = sum_k A(m, k) B(n, k) (+ bias) (+ C).
+struct GemmGroup {
+  int M, N, nt;               // nt: BN-wide column tiles
+  int tile0;                  // tiles of the groups before this one
   void* C; int64_t ldc; int c_bf16;
   const float* bias;
   int beta;
   int rowmap_H;
   int perm[4];
+};
+
+struct GemmMaps {
+  CUtensorMap a[kMaxGroups], b[kMaxGroups];
+};
+
+struct TcGemmParams {
+  int K;
+  int a_kmajor, b_kmajor;
+  int ngroups, ntiles;        // tiles over all groups
+  GemmGroup grp[kMaxGroups];
   DevArea* dev;
   uint64_t timeout_ns;
   int splits;                 // S >= 1
-  float* ws;                  // S > 1: partial products, [S][M][N] fp32
+  float* ws;                  // S > 1: one BM x BN fp32 partial per tile
+  unsigned int* flags;        // S > 1: per tile, epilogue-warp releases (zeroed before the launch)
 };
 
 __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kmajor, int kstep) {
@@ -99,9 +123,10 @@ __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* ma
 // 32 consecutive columns n0 .. n0+31 of one output row.  bias: added when
 // non-null; beta: C's previous value is added (read through L2: another SM may
 // have written it during this launch).
-__device__ __forceinline__ void store_chunk(const TcGemmParams& p, int64_t row, int n0, const float (&v)[32],
-                                            const float* bias, int beta) {
+__device__ __forceinline__ void store_chunk(const GemmGroup& p, int64_t row, int n0, const float (&v)[32]) {
   const bool full = n0 + 32 <= p.N;
+  const float* bias = p.bias;
+  const int beta = p.beta;
   if (p.c_bf16) {
     __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + n0;
     if (full && (p.ldc % 8 == 0) && !beta) {
@@ -150,40 +175,39 @@ __device__ __forceinline__ void store_chunk(const TcGemmParams& p, int64_t row, 
   }
 }
 
-// Raw fp32 partial product: 32 consecutive columns n0.. of row m of split s.
-__device__ __forceinline__ void store_partial(const TcGemmParams& p, int s, int m, int n0, const float (&v)[32]) {
-  float* W = p.ws + (static_cast<int64_t>(s) * p.M + m) * p.N + n0;
-  if (n0 + 32 <= p.N && p.N % 4 == 0) {
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(W + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-  } else {
-    for (int j = 0; j < 32 && n0 + j < p.N; ++j) W[j] = v[j];
-  }
+// Work item -> (split, group, tile within the group).
+__device__ __forceinline__ void decode_item(const TcGemmParams& p, int item, int& sp, int& g, int& tile, int& t) {
+  sp = item / p.ntiles;
+  t = item - sp * p.ntiles;
+  g = 0;
+  while (g + 1 < p.ngroups && t >= p.grp[g + 1].tile0) ++g;
+  tile = t - p.grp[g].tile0;
 }
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcGemmParams p) {
+gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ TcGemmParams p) {
   using Cfg = GemmCfg<BN>;
   constexpr int STAGES = Cfg::STAGES;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   GemmSmem<BN>& sm = *reinterpret_cast<GemmSmem<BN>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = (p.M + BM - 1) / BM, nt = (p.N + BN - 1) / BN;
-  const int ntiles = mt * nt;
-  const int nitems = ntiles * p.splits;
+  const int S = p.splits;
+  const int nitems = p.ntiles * S;
   const int nk = (p.K + BK - 1) / BK;
   // K blocks [kb_lo(s), kb_lo(s + 1)) belong to split s
-  auto kb_lo = [&](int s) { return static_cast<int>((static_cast<int64_t>(nk) * s) / p.splits); };
+  auto kb_lo = [&](int s) { return static_cast<int>((static_cast<int64_t>(nk) * s) / S); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&sm.tfull[b], 1); mbar_init(&sm.tempty[b], kEpiWarps); }
     sm.abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmB);
+    for (int g = 0; g < p.ngroups; ++g) {
+      prefetch_tmap(&maps.a[g]);
+      prefetch_tmap(&maps.b[g]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, Cfg::TMEM_COLS);
@@ -199,7 +223,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       uint32_t it = 0;
       for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
-        const int tile = item % ntiles, sp = item / ntiles;
+        int sp, g, tile, t;
+        decode_item(p, item, sp, g, tile, t);
+        const int nt = p.grp[g].nt;
         const int m0 = (tile / nt) * BM, n0 = (tile % nt) * BN;
         for (int kb = kb_lo(sp); kb < kb_lo(sp + 1); ++kb, ++it) {
           const int s = it % STAGES;
@@ -210,8 +236,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             goto producer_done;
           }
           mbar_arrive_expect_tx(&sm.full[s], Cfg::STAGE_BYTES);
-          load_operand<BM>(sm.stage[s], &tmA, &sm.full[s], p.a_kmajor, m0, kb * BK);
-          load_operand<BN>(sm.stage[s] + A_BYTES, &tmB, &sm.full[s], p.b_kmajor, n0, kb * BK);
+          load_operand<BM>(sm.stage[s], &maps.a[g], &sm.full[s], p.a_kmajor, m0, kb * BK);
+          load_operand<BN>(sm.stage[s] + A_BYTES, &maps.b[g], &sm.full[s], p.b_kmajor, n0, kb * BK);
         }
       }
     producer_done:;
@@ -220,7 +246,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       uint32_t it = 0, acc = 0;
       for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++acc) {
-        const int sp = item / ntiles;
+        const int sp = item / p.ntiles;
         const int buf = acc & 1;
         const uint32_t aph = (acc >> 1) & 1;
         if (!mbar_wait(&sm.tempty[buf], aph ^ 1, p.timeout_ns) || *(volatile int*)&sm.abort_flag) {
@@ -258,9 +284,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else {
     const int q = warp & 3;              // TMEM lane quarter of this warp
     const int c_lo = (warp - 2) / 4 * (BN / 2), c_hi = c_lo + BN / 2;   // its half of the columns
+    const int r = q * 32 + lane;         // row within the tile
     uint32_t acc = 0;
     for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++acc) {
-      const int tile = item % ntiles, sp = item / ntiles;
+      int sp, g, tile, t;
+      decode_item(p, item, sp, g, tile, t);
+      const GemmGroup& G = p.grp[g];
       const int buf = acc & 1;
       const uint32_t aph = (acc >> 1) & 1;
       int ok = 1;
@@ -270,25 +299,54 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) { report_status(p.dev, 4u, K_GEMM_TC, acc, W_MMA); sm.abort_flag = 1; }
         break;
       }
-      tc_fence_after();
-      const int m0 = (tile / nt) * BM, n0 = (tile % nt) * BN;
-      const int m = m0 + q * 32 + lane;
-      int64_t row = m;
-      bool write = m < p.M;
-      if (write && p.splits == 1 && p.rowmap_H > 0) {
-        const int pm = p.perm[m & 3];
-        if (pm < 0) write = false;
-        row = static_cast<int64_t>(pm) * p.rowmap_H + (m >> 2);
+      // split s > 0: the partial of splits 0 .. s - 1 is complete once all
+      // epilogue warps of split s - 1 have released the tile's counter
+      if (sp > 0) {
+        if (lane == 0) {
+          ok = wait_counter_geq(&p.flags[t], static_cast<unsigned int>(kEpiWarps * sp), p.timeout_ns) ? 1 : 0;
+          if (!ok) { report_status(p.dev, 4u, K_GEMM_TC, acc, W_COUNTER); sm.abort_flag = 1; }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
       }
+      tc_fence_after();
+      const int m0 = (tile / G.nt) * BM, n0 = (tile % G.nt) * BN;
+      const int m = m0 + r;
+      int64_t row = m;
+      bool write = m < G.M;
+      if (write && G.rowmap_H > 0) {
+        const int pm = G.perm[m & 3];
+        if (pm < 0) write = false;
+        row = static_cast<int64_t>(pm) * G.rowmap_H + (m >> 2);
+      }
+      float* part = S > 1 ? p.ws + (static_cast<int64_t>(t) * BM + r) * BN : nullptr;
       for (int c = c_lo; c < c_hi; c += 32) {
         float v[32];
         tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c, v);
-        if (write && n0 + c < p.N) {
-          if (p.splits > 1) store_partial(p, sp, m, n0 + c, v);
-          else store_chunk(p, row, n0 + c, v, p.bias, p.beta);
+        if (S > 1) {
+          if (sp > 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              const float4 o = __ldcg(reinterpret_cast<const float4*>(part + c + j));
+              v[j] = o.x + v[j]; v[j + 1] = o.y + v[j + 1]; v[j + 2] = o.z + v[j + 2]; v[j + 3] = o.w + v[j + 3];
+            }
+          }
+          if (sp < S - 1) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              __stcg(reinterpret_cast<float4*>(part + c + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+            continue;
+          }
         }
+        if (write && n0 + c < G.N) store_chunk(G, row, n0 + c, v);
       }
       tc_fence_before();
+      if (S > 1 && sp < S - 1) {
+        // this warp's share of the partial, visible at gpu scope, then released
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) red_release_gpu_add(&p.flags[t], 1u);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.tempty[buf]);
     }
@@ -303,95 +361,93 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 template <int BN>
 constexpr size_t smem_bytes() { return sizeof(GemmSmem<BN>) + 1024; }
 
-// C[row(m), n] = sum over s in order of ws[s][m][n] (+ bias[n]) (+ C if beta),
-// four consecutive columns per thread.
-__global__ void __launch_bounds__(256)
-gemm_split_reduce_kernel(const float* __restrict__ ws, int S, int M, int N, TcGemmParams p) {
-  const int nq = (N + 3) / 4;
-  const int64_t total = static_cast<int64_t>(M) * nq;
-  const int64_t plane = static_cast<int64_t>(M) * N;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int m = static_cast<int>(i / nq), n0 = static_cast<int>(i % nq) * 4;
-    int64_t row = m;
-    if (p.rowmap_H > 0) {
-      const int pm = p.perm[m & 3];
-      if (pm < 0) continue;
-      row = static_cast<int64_t>(pm) * p.rowmap_H + (m >> 2);
-    }
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
-    const float* w = ws + static_cast<int64_t>(m) * N + n0;
-    if (n0 + 4 <= N && N % 4 == 0) {
-      for (int s = 0; s < S; ++s) {
-        const float4 v = *reinterpret_cast<const float4*>(w + s * plane);
-        a[0] += v.x; a[1] += v.y; a[2] += v.z; a[3] += v.w;
-      }
-    } else {
-      for (int s = 0; s < S; ++s)
-        for (int j = 0; j < 4 && n0 + j < N; ++j) a[j] += w[s * plane + j];
-    }
-    for (int j = 0; j < 4 && n0 + j < N; ++j) {
-      float x = a[j];
-      if (p.bias) x += p.bias[n0 + j];
-      if (p.c_bf16) {
-        __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + n0 + j;
-        if (p.beta) x += __bfloat162float(*C);
-        *C = __float2bfloat16_rn(x);
-      } else {
-        float* C = static_cast<float*>(p.C) + row * p.ldc + n0 + j;
-        if (p.beta) x += *C;
-        *C = x;
-      }
-    }
-  }
-}
-
 struct GemmPlan { int BN, S; };
 
-// Tile width and K split.  Items run in waves of num_sms.  128 x 256 tiles
-// unless they would leave most SMs idle; then a long K is split when the
-// scratch allows and that saves at least a sixth of the waves per unit of
-// work, and otherwise 128-wide tiles double the tile count.
-GemmPlan plan_gemm(const GemmArgs& g, int num_sms) {
-  const int mt = (g.M + BM - 1) / BM;
-  const int t256 = mt * ((g.N + 255) / 256), t128 = mt * ((g.N + 127) / 128);
-  const int nk = (g.K + BK - 1) / BK;
-  if (t256 >= num_sms) return {256, 1};
-  const size_t plane = static_cast<size_t>(g.M) * g.N * 4;
-  if (g.split_ws && nk >= 32) {
+int tiles_of(const GemmArgs* gs, int n, int bn) {
+  int t = 0;
+  for (int i = 0; i < n; ++i) t += ((gs[i].M + BM - 1) / BM) * ((gs[i].N + bn - 1) / bn);
+  return t;
+}
+
+// Tile width and K split of a launch.  Items run in waves of num_sms.  K is
+// split (at most kMaxSplits, at least 16 K blocks of 64 per split, the
+// scratch holds one fp32 partial per tile) to the count with the fewest
+// waves x (K blocks per split + 48): each wave also pays about 48 K blocks'
+// time of pipeline fill, epilogue and split hand-over (fitted to GB300 runs
+// of the weight gradients: GRU hidden 512 x K 8192, 64 tiles, split 1 / 2 /
+// 4 / 8 = 63 / 53 / 75 / 130 us; the 2-layer bidirectional LSTM's 512 and
+// 768 tiles x K 65536, split 1 / 2 / 4 / 8 = 4.12 / 3.84 / 3.94 / 4.23 ms).
+// Equal costs keep the smaller split.  Without a split: 128 x 256 tiles,
+// unless they would leave most SMs idle; then 128-wide tiles double the tile
+// count.
+GemmPlan plan_gemm(const GemmArgs* gs, int n, int num_sms) {
+  const int t256 = tiles_of(gs, n, 256), t128 = tiles_of(gs, n, 128);
+  const int nk = (gs[0].K + BK - 1) / BK;
+  bool fp32_out = true;
+  for (int i = 0; i < n; ++i) fp32_out = fp32_out && !gs[i].c_bf16;
+  if (fp32_out && gs[0].split_ws && nk >= 32) {
+    const size_t need = static_cast<size_t>(t256) * BM * 256 * 4 + static_cast<size_t>(t256) * 4;
+    auto cost = [&](int S) {
+      const int64_t waves = (static_cast<int64_t>(t256) * S + num_sms - 1) / num_sms;
+      return static_cast<double>(waves) * ((nk + S - 1) / S + 48);
+    };
     int best = 1;
-    double best_cost = 1.0;
-    for (int S = 2; S <= kMaxSplits && nk / S >= 16 && S * plane <= g.split_ws_bytes; ++S) {
-      const double cost = static_cast<double>((t256 * S + num_sms - 1) / num_sms) / S;
-      if (cost < best_cost - 1e-9) { best_cost = cost; best = S; }
+    double best_cost = cost(1);
+    for (int S = 2; S <= kMaxSplits && nk / S >= 16 && need <= gs[0].split_ws_bytes; ++S) {
+      const double c = cost(S);
+      if (c < best_cost - 1e-9) { best_cost = c; best = S; }
     }
-    if (best > 1 && best_cost <= 5.0 / 6.0) return {256, best};
+    if (best > 1) return {256, best};
   }
+  if (t256 >= num_sms) return {256, 1};
   if (2 * t256 < num_sms && t128 > t256) return {128, 1};
   return {256, 1};
 }
 
 template <int BN>
-int launch_bn(const GemmArgs& g, int S, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns) {
-  CUtensorMap ta, tb;
-  int rc;
-  // A: rows = M; B: rows = N.
-  if (g.a_kmajor) rc = make_tmap_bf16_2d(&ta, g.A, g.K, g.M, g.lda, 64, BM);
-  else rc = make_tmap_bf16_2d(&ta, g.A, g.M, g.K, g.lda, 64, BK);
-  if (rc) return rc;
-  if (g.b_kmajor) rc = make_tmap_bf16_2d(&tb, g.B, g.K, g.N, g.ldb, 64, BN);
-  else rc = make_tmap_bf16_2d(&tb, g.B, g.N, g.K, g.ldb, 64, BK);
-  if (rc) return rc;
+int launch_bn(const GemmArgs* gs, int n, int S, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns) {
+  GemmMaps maps;
   TcGemmParams p;
-  p.M = g.M; p.N = g.N; p.K = g.K;
-  p.a_kmajor = g.a_kmajor; p.b_kmajor = g.b_kmajor;
-  p.C = g.C; p.ldc = g.ldc; p.c_bf16 = g.c_bf16;
-  p.bias = g.bias; p.beta = g.beta; p.rowmap_H = g.rowmap_H;
-  for (int i = 0; i < 4; ++i) p.perm[i] = g.perm[i];
+  p.K = gs[0].K;
+  p.a_kmajor = gs[0].a_kmajor; p.b_kmajor = gs[0].b_kmajor;
+  p.ngroups = n;
+  int tiles = 0;
+  for (int i = 0; i < n; ++i) {
+    const GemmArgs& g = gs[i];
+    int rc;
+    // A: rows = M; B: rows = N.
+    if (g.a_kmajor) rc = make_tmap_bf16_2d(&maps.a[i], g.A, g.K, g.M, g.lda, 64, BM);
+    else rc = make_tmap_bf16_2d(&maps.a[i], g.A, g.M, g.K, g.lda, 64, BK);
+    if (rc) return rc;
+    if (g.b_kmajor) rc = make_tmap_bf16_2d(&maps.b[i], g.B, g.K, g.N, g.ldb, 64, BN);
+    else rc = make_tmap_bf16_2d(&maps.b[i], g.B, g.N, g.K, g.ldb, 64, BK);
+    if (rc) return rc;
+    GemmGroup& G = p.grp[i];
+    G.M = g.M; G.N = g.N; G.nt = (g.N + BN - 1) / BN;
+    G.tile0 = tiles;
+    tiles += ((g.M + BM - 1) / BM) * G.nt;
+    G.C = g.C; G.ldc = g.ldc; G.c_bf16 = g.c_bf16;
+    G.bias = g.bias; G.beta = g.beta; G.rowmap_H = g.rowmap_H;
+    for (int k = 0; k < 4; ++k) G.perm[k] = g.perm[k];
+  }
+  for (int i = n; i < kMaxGroups; ++i) {
+    maps.a[i] = maps.a[0];
+    maps.b[i] = maps.b[0];
+    p.grp[i] = p.grp[0];
+    p.grp[i].tile0 = tiles;
+  }
+  p.ntiles = tiles;
   p.dev = dev;
   p.timeout_ns = timeout_ns;
   p.splits = S;
-  p.ws = static_cast<float*>(g.split_ws);
+  p.ws = static_cast<float*>(gs[0].split_ws);
+  p.flags = nullptr;
+  if (S > 1) {
+    const size_t part = static_cast<size_t>(tiles) * BM * BN * 4;
+    if (part + static_cast<size_t>(tiles) * 4 > gs[0].split_ws_bytes) return 2;
+    p.flags = reinterpret_cast<unsigned int*>(static_cast<char*>(gs[0].split_ws) + part);
+    if (cudaMemsetAsync(p.flags, 0, static_cast<size_t>(tiles) * 4, s) != cudaSuccess) return 3;
+  }
   // the shared-memory limit is a per-device attribute: set it once on each
   // device this instantiation launches on (any thread may get here first)
   static std::atomic<uint64_t> attr_set{0};
@@ -404,14 +460,10 @@ int launch_bn(const GemmArgs& g, int S, cudaStream_t s, int num_sms, DevArea* de
       return 3;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
-  const int items = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN) * S;
+  const int items = tiles * S;
   const int grid = items < num_sms ? items : num_sms;
-  gemm_tc_kernel<BN><<<grid, kThreads, smem_bytes<BN>(), s>>>(ta, tb, p);
+  gemm_tc_kernel<BN><<<grid, kThreads, smem_bytes<BN>(), s>>>(maps, p);
   if (cudaGetLastError() != cudaSuccess) return 3;
-  if (S > 1) {
-    gemm_split_reduce_kernel<<<4 * num_sms, 256, 0, s>>>(p.ws, S, g.M, g.N, p);
-    if (cudaGetLastError() != cudaSuccess) return 3;
-  }
   return 0;
 }
 
@@ -424,16 +476,37 @@ bool gemm_tc_supported(const GemmArgs& g) {
   return true;
 }
 
+size_t gemm_tc_split_scratch_bytes(int M, int N) {
+  const size_t tiles = static_cast<size_t>((M + BM - 1) / BM) * ((N + 127) / 128);
+  return tiles * BM * 128 * 4 + tiles * 4 + 4096;
+}
+
+int launch_gemm_tc_grouped(const GemmArgs* gs, int n, cudaStream_t s, int num_sms, DevArea* dev,
+                           uint64_t timeout_ns) {
+  if (n < 1 || n > kMaxGroups) return 2;
+  for (int i = 0; i < n; ++i) {
+    if (!gemm_tc_supported(gs[i])) return 2;
+    if (gs[i].K != gs[0].K || gs[i].a_kmajor != gs[0].a_kmajor || gs[i].b_kmajor != gs[0].b_kmajor) return 2;
+  }
+  GemmPlan pl = plan_gemm(gs, n, num_sms);
+  // test hooks: a forced tile width (no K split), a forced K split
+  const PlanOverrides ov = plan_overrides();
+  if (ov.gemm_bn == 128 || ov.gemm_bn == 256) pl = {ov.gemm_bn, 1};
+  if (ov.gemm_splits >= 1) {
+    bool fp32_out = gs[0].split_ws != nullptr;
+    for (int i = 0; i < n; ++i) fp32_out = fp32_out && !gs[i].c_bf16;
+    const int nk = (gs[0].K + BK - 1) / BK;
+    if (ov.gemm_splits == 1) pl.S = 1;
+    else if (fp32_out && nk / ov.gemm_splits >= 16) pl = {256, ov.gemm_splits};
+  }
+  return pl.BN == 256 ? launch_bn<256>(gs, n, pl.S, s, num_sms, dev, timeout_ns)
+                      : launch_bn<128>(gs, n, pl.S, s, num_sms, dev, timeout_ns);
+}
+
 int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns,
                    int* launches) {
-  if (!gemm_tc_supported(g)) return 2;
-  GemmPlan pl = plan_gemm(g, num_sms);
-  // test hook: a forced tile width (no K split)
-  const int bn = plan_overrides().gemm_bn;
-  if (bn == 128 || bn == 256) pl = {bn, 1};
-  if (launches) *launches = pl.S > 1 ? 2 : 1;
-  return pl.BN == 256 ? launch_bn<256>(g, pl.S, s, num_sms, dev, timeout_ns)
-                      : launch_bn<128>(g, pl.S, s, num_sms, dev, timeout_ns);
+  if (launches) *launches = 1;
+  return launch_gemm_tc_grouped(&g, 1, s, num_sms, dev, timeout_ns);
 }
 
 }  // namespace rnn

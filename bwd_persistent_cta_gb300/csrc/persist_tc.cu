@@ -25,6 +25,7 @@ struct TcPlan {
   int NB = 1, Bp = 0;   // batch parts per row group, batch rows per part
   uint32_t tmem_cols = 0, off_ring = 0, off_recv = 0, off_bar = 0;
   uint32_t wcol = 0;   // first TMEM column of the weight sub-tiles (w_tmem > 0)
+  uint32_t off_stage = 0;   // forward K split: warp 0's post-step stage (0: none)
   size_t smem = 0;
 };
 
@@ -139,6 +140,16 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
       p.off_ring = static_cast<uint32_t>(a1k(static_cast<size_t>(nsub - wt) * kWSub));
       p.off_recv = p.off_ring + static_cast<uint32_t>(a1k(R * rb));
       p.off_bar = p.off_recv + static_cast<uint32_t>(a1k(recv));
+      // forward with a K split: room for warp 0's post-step values (32 B per
+      // pair) after the barriers, when shared memory allows
+      p.off_stage = 0;
+      if (!bwd && KS > 1) {
+        const size_t st_bytes = static_cast<size_t>(32) * PP * 32;
+        if (smem + a1k(st_bytes) <= kSmemCap) {
+          p.off_stage = p.off_bar + static_cast<uint32_t>(a1k(sizeof(TcBars)));
+          smem += a1k(st_bytes);
+        }
+      }
       // all 512 TMEM columns: the shared-memory request alone must keep a
       // second CTA off the SM
       const size_t floor = wt ? kOneCtaSmem : kMinSmem;
@@ -287,9 +298,11 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   // direction), so that one box {64, Npad, nsub, 1} lands as nsub consecutive
   // swizzled 64-column sub-tiles
   int single = pl.R >= pl.nsub ? 1 : 0;
-  // the slice in two chunks of whole sub-tiles (each TMA issue costs about
-  // 0.1 us of the step: four chunks measured no faster)
-  const int nchunk = pl.nsub % 2 == 0 && pl.nsub >= 4 ? 2 : 1;
+  // a slice of 64 KB or more in two chunks of whole sub-tiles (each TMA issue
+  // costs about 0.1 us of the step: four chunks measured no faster, and a
+  // smaller slice lands too soon to gain)
+  const size_t slice_bytes = static_cast<size_t>(pl.nsub) * pl.Npad * 128;
+  const int nchunk = pl.nsub % 2 == 0 && pl.nsub >= 4 && slice_bytes >= (64u << 10) ? 2 : 1;
   if (single) {
     const uint64_t Kd = bwd ? 4ull * H : static_cast<uint64_t>(H);
     const uint64_t rows = bwd ? static_cast<uint64_t>(a.T) * a.B : static_cast<uint64_t>(a.T + 2) * a.B;
@@ -323,7 +336,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   P.NB = pl.NB;
   P.Bp = pl.Bp;
   P.tmem_cols = pl.tmem_cols;
-  P.off_ring = pl.off_ring; P.off_recv = pl.off_recv; P.off_bar = pl.off_bar;
+  P.off_ring = pl.off_ring; P.off_recv = pl.off_recv; P.off_bar = pl.off_bar; P.off_stage = pl.off_stage;
   P.w_tmem = pl.w_tmem;
   P.single = single;
   P.nchunk = nchunk;

@@ -112,6 +112,7 @@ struct TcPersistParams {
   unsigned int nblk_dir;   // CTAs per direction
   uint32_t tmem_cols;
   uint32_t off_ring, off_recv, off_bar;
+  uint32_t off_stage;      // forward with a K split: warp 0's post-step stage, 0 = none
 };
 
 struct TcBars {
@@ -546,14 +547,15 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   };
   // The stores of a step take about 0.15 us per pair a thread owns and must
   // not delay thread 0, which drives the next step's wait, TMA and MMAs.
-  // Without a K split the receive buffer is idle from the end of a step until
-  // the next step's partials land: warp 0 stages all its pairs' values there
-  // (8 floats each: 4 gates, h, c, y) and warps 1-7 store them.  With a K
-  // split peers may write the receive buffer at any time: thread 0 alone
-  // stages its pairs (bars.stage) for thread 32, and warp 0's other lanes
-  // store theirs before thread 0 starts its wait.
-  constexpr bool kStageWarp0 = KS == 1;
-  float* const stage_w0 = recv;
+  // Warp 0 stages all its pairs' values (8 floats each: 4 gates, h, c, y)
+  // and warps 1-7 store them: without a K split in the receive buffer, idle
+  // from the end of a step until the next step's partials land; with a K
+  // split (peers may write the receive buffer at any time) in a stage area of
+  // its own where shared memory allows.  Otherwise thread 0 alone stages its
+  // pairs (bars.stage) for thread 32, and warp 0's other lanes store theirs
+  // before thread 0 starts its wait.
+  float* const stage_w0 = KS == 1 ? recv : (P.off_stage ? reinterpret_cast<float*>(base + P.off_stage) : nullptr);
+  const bool kStageWarp0 = stage_w0 != nullptr;
   auto post_stores = [&](int sd, bool own) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool mine = own || (kStageWarp0 ? warp != 0 : threadIdx.x != 0);
@@ -566,7 +568,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       }
     }
     if (own) return;
-    if constexpr (kStageWarp0) {
+    if (kStageWarp0) {
       if (warp != 0) {
         // staged entry j = warp-0 lane j % 32, pair j / 32
         for (int j = (warp - 1) * 32 + lane; j < 32 * PP; j += 7 * 32) {
@@ -593,8 +595,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   // barrier of the step's release; without a K split after a barrier that
   // ends every read of the step's partial sums)
   auto stage_own = [&](int sd) {
-    if constexpr (kStageWarp0) {
-      __syncthreads();
+    if (kStageWarp0) {
+      if (KS == 1) __syncthreads();   // every read of the step's partial sums is done
       if ((threadIdx.x >> 5) != 0) return;
 #pragma unroll
       for (int p = 0; p < PP; ++p) {

@@ -60,8 +60,8 @@ struct GemmArgs {
   int rowmap_H = 0;
   int perm[4] = {0, 1, 2, 3};
   int in_bf16 = 1;            // operand element type (SIMT kernel takes fp32 too)
-  // scratch the tcgen05 kernel may use to split K across CTAs (fp32 partial
-  // products, reduced in a fixed order by a second kernel); null: no split
+  // scratch the tcgen05 kernel may use to split K across CTAs (one fp32
+  // partial per output tile, summed in split order); null: no split
   void* split_ws = nullptr;
   size_t split_ws_bytes = 0;
 };
@@ -116,6 +116,12 @@ int launch_gemm_simt(const GemmArgs& g, cudaStream_t s);
 int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns,
                    int* launches = nullptr);
 bool gemm_tc_supported(const GemmArgs& g);
+// Up to 6 GEMMs with the same K and operand major-ness in one launch (their
+// tiles share the grid); the split-K scratch of gs[0] serves all of them.
+int launch_gemm_tc_grouped(const GemmArgs* gs, int n, cudaStream_t s, int num_sms, DevArea* dev,
+                           uint64_t timeout_ns);
+// Scratch bytes that let the tensor-core GEMM split the K of an M x N output.
+size_t gemm_tc_split_scratch_bytes(int M, int N);
 
 int plan_persist_simt(const PersistArgs& a, int num_sms, int* nblk, size_t* smem);
 // Whether the SIMT backward kernel can accumulate dW_hh in its step loop for
@@ -184,9 +190,9 @@ int launch_recompute_cells(const void* gates, const void* c0, float* C, int T, i
 
 // Plan overrides set by the rnn_debug_set_plan_overrides test hook (0 = the
 // planner's choice): K-split caps and batch parts of the tensor-core
-// persistent kernels, the tensor-core GEMM's tile width.
+// persistent kernels, the tensor-core GEMM's tile width and K split.
 struct PlanOverrides {
-  int max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn;
+  int max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn, gemm_splits;
 };
 PlanOverrides plan_overrides();
 

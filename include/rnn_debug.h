@@ -64,11 +64,16 @@ rnn_status_t rnn_debug_skip_arrival(rnn_handle_t handle, int cta);
  *                           split (CTAs per cluster), forward / backward;
  *   nb_fwd, nb_bwd          1, 2 or 4: fix their number of batch parts;
  *   gemm_bn                 128 or 256: force the tensor-core GEMM's tile
- *                           width (no K split).
+ *                           width (no K split);
+ *   gemm_splits             1..16: force the K split of a tensor-core GEMM
+ *                           with fp32 output and split scratch (128 x 256
+ *                           tiles), where it has at least 16 K blocks of 64
+ *                           per split.
  * Other values are RNN_BAD_PARAM and change nothing.  Plans are cached per
  * shape and per override set; set the overrides while no call of the library
  * runs on another thread. */
-rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn);
+rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn,
+                                          int gemm_splits);
 
 #ifdef __cplusplus
 }

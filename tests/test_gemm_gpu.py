@@ -101,8 +101,11 @@ def test_gemm_split_k_rowmap_beta_bias():
     _case(512, 512, 8192, 0, 0, 1, bias=True, beta=True, rowmap=[1, -1, 0, 2], seed=11)
 
 
-def test_gemm_split_k_multiwave():
-    # more (tile, split) items than SMs: the split items run in several waves
+@pytest.mark.parametrize("splits", [2, 3])
+def test_gemm_split_k_multiwave(plan_overrides, splits):
+    # more (tile, split) items than SMs (a forced split): the split items run
+    # in several waves, each split of a tile after the one before it
+    plan_overrides(gemm_splits=splits)
     _case(6400, 512, 3072, 1, 1, 1, seed=12)
 
 

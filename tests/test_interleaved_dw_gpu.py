@@ -56,10 +56,15 @@ def test_interleaved_dw_parity(mode, ra, L, bidir, T, B, I, H, dtype):
         for d in range(2 if bidir else 1):
             a, b = on["dparams"][l][d]["W_hh"], off["dparams"][l][d]["W_hh"]
             assert Hn.max_rel_err(a, b) <= Hn.TOL[dtype]
-    # the reserve holds the accumulator; backward-weights runs one GEMM fewer per (layer, direction)
+    # the reserve holds the accumulator; backward-weights runs one GEMM fewer per (layer, direction):
+    # one launch fewer each on the fp32 path, while the bf16 path runs a layer's weight-gradient
+    # GEMMs as one grouped launch either way
     D = 2 if bidir else 1
     assert on["reserve_bytes"] - off["reserve_bytes"] == L * D * G * H * H * 4
-    assert on["launches"] / 2 < off["launches"]      # two calls on, one off
+    if dtype == "f32":
+        assert on["launches"] / 2 < off["launches"]      # two calls on, one off
+    else:
+        assert on["launches"] / 2 <= off["launches"]
 
 
 def test_interleaved_dw_with_lengths():
