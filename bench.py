@@ -232,21 +232,36 @@ KERNEL_SOURCES = ["bwd_persistent_cta_gb300/csrc/persist_tc_kernels.cuh", "bwd_p
                   "bwd_persistent_cta_gb300/csrc/common.cuh"]
 
 
+def code_only(text: str) -> str:
+    """C++ source without its comments and whitespace: what a profile's
+    counters depend on."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return re.sub(r"\s+", "", text)
+
+
+def kernel_sources_sha() -> str:
+    """Hash of the code (comments and whitespace removed) of the sources that
+    make the profiled kernels."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(code_only(open(os.path.join(ROOT, f)).read()).encode())
+    return h.hexdigest()[:16]
+
+
 def profiled_traffic(cls: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, or None when there is none or the kernel source has changed since
-    the counters were taken."""
-    import hashlib
+    workload, or None when there is none or the kernel code has changed since
+    the counters were taken (a comment edit does not count)."""
     path = PROFILE_FOR_CLASS.get(cls)
     if not path:
         return None
     path = os.path.join(ROOT, path.format(workload=workload))
     if not os.path.exists(path):
         return None
-    h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
-    sha = h.hexdigest()[:16]
+    sha = kernel_sources_sha()
     fields = {}
     for line in open(path):
         if ":" in line and line.split(":", 1)[0].strip() in ("traffic-bytes-per-launch", "kernel-source-sha256"):

@@ -11,8 +11,8 @@
 // Backward weights, per layer and direction: dW_ih = dG^T X and
 //   dW_hh = dG^T H_prev as long-K GEMMs writing straight into the caller's gate
 //   order, and the bias gradients scattered from the sums.
-// The split mirrors cudnnRNNForwardTraining / BackwardData / BackwardWeights as
-// SystemDS LibMatrixCuDNN.java calls them in ``lstm`` / ``lstmBackward``.
+// The split mirrors cuDNN's forward-training / backward-data / backward-weights
+// calls as the SystemDS LibMatrixCuDNN.java page's LSTM operators make them.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 

@@ -1,11 +1,11 @@
 // gemm_tc.cu - bf16 GEMM on the 5th-generation tensor cores (tcgen05), fp32
 // accumulation in tensor memory, operands fed by TMA.  Serves the three
 // contractions around the recurrence on the bf16 path:
-//   input projection  P  = X  * W_ih^T + b    (all timesteps at once; poplibs
-//                                              Lstm.cpp calcSequenceWeightedInputs)
-//   input gradient    dX = dG * W_ih          (Lstm.cpp backwardStepImpl, hoisted)
-//   weight gradients  dW = dG^T * [X | H_prev] (basicLstmParamUpdate /
-//                                              basicGruParamUpdate, one long-K GEMM)
+//   input projection  P  = X  * W_ih^T + b    (all timesteps at once: the popnn
+//                                              Lstm.cpp page's hoisted input weights)
+//   input gradient    dX = dG * W_ih          (its backward step's input side, hoisted)
+//   weight gradients  dW = dG^T * [X | H_prev] (the popnn Lstm.cpp / Gru.cpp pages'
+//                                              weight update, one long-K GEMM)
 //
 // Structure: a persistent kernel, one CTA per SM, 128 x BN output tiles
 // (BN = 256, or 128 when 256-wide tiles would leave most SMs idle), 64-deep K

@@ -6,9 +6,9 @@
 //   * sequence copies between seq-major [T,B,F] and batch-first [B,T,F], with
 //     fp32 <-> bf16 casts, vectorised by four elements;
 //   * placing h0 into the output buffer's boundary slot.
-// SystemDS LibMatrixCuDNN.java does the same job with separate layout kernels
-// (prepare_lstm_output, prepare_lstm_backward_gradients, prepare_lstm_dinput,
-// prepare_lstm_dweight) around the cuDNN calls in ``lstm`` / ``lstmBackward``.
+// The SystemDS LibMatrixCuDNN.java page does the same job with separate layout
+// kernels for the output, the upstream gradients, dx and dW around the cuDNN
+// calls of its LSTM forward and backward operators.
 #include "common.cuh"
 
 namespace rnn {
@@ -136,8 +136,8 @@ __global__ void seq_copy_kernel(const Ti* __restrict__ in, To* __restrict__ out,
 }
 
 // Recomputation of the LSTM cell states from the saved gate activations
-// (poplibs Lstm.cpp recomputeCellAndTanhImpl: prevCellState * forgetGate +
-// inputGate * candidate, before the backward pass): one thread per (direction,
+// (the popnn Lstm.cpp page's recomputation mode: previous cell state times the
+// forget gate plus input gate times candidate, before the backward pass): one thread per (direction,
 // sequence, unit) walks the direction's time order, c_t = f * clip(c_{t-1}) +
 // i * g (clip = identity without cell clipping; a masked step t >= len[b]
 // keeps c), and writes every c_t in the layout the forward kernels use,

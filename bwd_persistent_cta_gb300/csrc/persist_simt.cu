@@ -11,7 +11,7 @@
 // registers, writes its slice, and arrives on a gpu-scope step counter.
 // Before the next step every CTA waits - with a time limit - until all CTAs of
 // its direction have arrived.  This is the persistent-RNN structure of the
-// persistent backward-data kernel fragment (one launch for all steps,
+// persistent RNN backward-data kernel page (one launch for all steps,
 // register/shared-resident weights, a per-step exchange through global memory
 // between CTAs), with acquire/release counters in place of its -0.0 sentinel
 // polling.
@@ -26,11 +26,10 @@
 // contractions per step: r/z, then W_hn(r*h)) and its forward below batch 4,
 // and any shape the tensor-core kernels do not take.
 //
-// Cell math: Lstm.cpp lstmCellForwardPassCalcUnits / basicLstmCellForwardPass
-// and backwardStepImpl; Gru.cpp gruCellForwardPassCalcUnits,
-// gruCellForwardPassCalcUnitsResetAfter, backwardStepImpl and
-// backwardStepImplResetAfter; the LSTM and GRU branches of the persistent
-// backward-data kernel fragment.
+// Cell math: the popnn Lstm.cpp page's forward cell step and backward step;
+// the popnn Gru.cpp page's reset-before and resetAfter forward cell steps and
+// backward steps; the LSTM and GRU branches of the persistent RNN
+// backward-data kernel page.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -384,8 +383,8 @@ __device__ __forceinline__ void dwhh_stage(const PersistArgs& a, T* vs, int dir,
 }
 
 // dW_hh accumulation of one step (the weight update interleaved with the
-// backward pass: poplibs Lstm.cpp / Gru.cpp accumulate the weight gradients
-// inside the backward loop, "Interleaved weight update").  The CTA's rows are
+// backward pass: the popnn Lstm.cpp and Gru.cpp pages accumulate the weight
+// gradients inside the backward loop, their interleaved weight update).  The CTA's rows are
 // its units' 4 gate slots, row j = 4 * ul + slot; for column k
 //   acc[j][k] += sum_b dG_t[b][j] * v_b[k],
 // v = h_{t-1}, or r * h_{t-1} for the reset-before candidate (both staged in

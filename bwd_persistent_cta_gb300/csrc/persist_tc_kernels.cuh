@@ -46,13 +46,13 @@
 // cluster barrier, so no CTA exits while a peer may still touch its shared
 // memory).
 //
-// This is the persistent-RNN design of the persistent backward-data kernel
-// fragment (one launch for all steps, weights resident on chip, a per-step
+// This is the persistent-RNN design of the persistent RNN backward-data kernel
+// page (one launch for all steps, weights resident on chip, a per-step
 // exchange between CTAs through global memory) carried to tensor cores, TMA,
-// TMEM and thread-block clusters; the fragment polls its dgates buffer for a
+// TMEM and thread-block clusters; that kernel polls its dgates buffer for a
 // -0.0 sentinel where a release/acquire counter is used here.  Cell math:
-// Lstm.cpp lstmCellForwardPassCalcUnits / backwardStepImpl; Gru.cpp
-// gruCellForwardPassCalcUnitsResetAfter / backwardStepImplResetAfter.  The
+// the popnn Lstm.cpp page's forward cell step and backward step, and the popnn
+// Gru.cpp page's resetAfter forward cell step and backward step.  The
 // sigmoid and tanh of this bf16 path use the hardware tanh.approx.f32
 // instruction (sigma(x) = 1/2 + tanh(x/2)/2); its relative error (about 2^-11)
 // is below the bf16 storage rounding of the stored states.

@@ -5,26 +5,26 @@
  * RNN cells, run forward over a whole sequence and back-propagated through
  * time.  The
  * three-phase split (forward, backward-data, backward-weights) follows the
- * cuDNN RNN calls that SystemDS LibMatrixCuDNN.java makes in ``lstm`` and
- * ``lstmBackward`` (cudnnRNNForwardTraining, cudnnRNNBackwardData,
- * cudnnRNNBackwardWeights), and the Fwd / Bwd / WU entry points of poplibs
- * Lstm.cpp (lstmFwd, lstmBwd, lstmWU) and Gru.cpp (gruFwd, gruBwd, gruWU).
+ * SystemDS LibMatrixCuDNN.java page (its LSTM forward and backward operators
+ * run cuDNN's forward-training, backward-data and backward-weights calls) and
+ * the forward, backward and weight-update entry points of the popnn Lstm.cpp
+ * and Gru.cpp pages (Graphcore poplibs).
  *
  * Cell definitions (canonical gate order; sigma = logistic sigmoid):
- *   LSTM (Lstm.cpp lstmCellForwardPassCalcUnits / basicLstmCellForwardPass):
+ *   LSTM (the popnn Lstm.cpp page, forward cell step):
  *     a = W_ih x_t + W_hh h_{t-1} + b
  *     i = sigma(a_i), f = sigma(a_f), g = tanh(a_g), o = sigma(a_o)
  *     c_t = f c_{t-1} + i g,  h_t = o tanh(c_t)
- *   GRU resetAfter (Gru.cpp gruCellForwardPassCalcUnitsResetAfter):
+ *   GRU resetAfter (the popnn Gru.cpp page, resetAfter forward cell step):
  *     r = sigma(W_ir x + b_ir + W_hr h + b_hr), z = sigma(W_iz x + b_iz + W_hz h + b_hz)
  *     n = tanh(W_in x + b_in + r * (W_hn h + b_hn)),  h_t = (1 - z) n + z h_{t-1}
- *   GRU reset-before (Gru.cpp gruCellForwardPassCalcUnits / basicGruCellForwardPass):
+ *   GRU reset-before (the popnn Gru.cpp page, reset-before forward cell step):
  *     r, z as above with one bias b_r, b_z;  n = tanh(W_in x + b_n + W_hn (r * h_{t-1}))
  *     h_t = (1 - z) n + z h_{t-1}
- * Backward: the BPTT recurrences of Lstm.cpp / Gru.cpp backwardStepImpl and
- * backwardStepImplResetAfter (identical to the LSTM and GRU branches of the
- * persistent RNN backward-data kernel fragment), and the weight-gradient sums
- * of basicLstmParamUpdate / basicGruParamUpdate.
+ * Backward: the BPTT recurrences of the backward steps of the popnn Lstm.cpp
+ * and Gru.cpp pages (identical to the LSTM and GRU branches of the persistent
+ * RNN backward-data kernel page), and the weight-gradient sums of their weight
+ * updates.
  *
  * Conventions shared by every call
  *   - All pointers marked "device" are device memory owned by the caller; the
@@ -55,8 +55,9 @@
  *     bf16).  Accumulation and the cell state are always fp32.  dw is fp32.
  *   - State pointers may be NULL: NULL inputs (hx, cx, dhy, dcy) mean zero,
  *     NULL outputs (hy, cy, dhx, dcx) are skipped - the same convention as the
- *     ``cx == NULL`` / ``dhx != NULL`` tests of the persistent backward-data
- *     kernel fragment and the NULL dhy that SystemDS passes.
+ *     ``cx == NULL`` / ``dhx != NULL`` tests of the persistent RNN
+ *     backward-data kernel page and the absent final-state gradient of the
+ *     SystemDS LibMatrixCuDNN.java page's LSTM backward operator.
  *   - Every device pointer must be 16-byte aligned.
  *
  * Environment variables (read by the library; none is needed in normal use)
@@ -88,8 +89,8 @@ typedef enum {
 } rnn_status_t;
 
 /* RNN_RNN_RELU / RNN_RNN_TANH: the plain recurrent cell h' = act(W_ih x +
- * W_hh h + b) of the persistent backward-data kernel fragment's
- * CUDNN_RNN_RELU / CUDNN_RNN_TANH branch (one gate, G = 1). */
+ * W_hh h + b) of the persistent RNN backward-data kernel page's ReLU / tanh
+ * branch (one gate, G = 1). */
 typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_RNN_RELU = 2, RNN_RNN_TANH = 3 } rnn_mode_t;
 typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
 
@@ -186,8 +187,9 @@ rnn_status_t rnn_backward_data(rnn_handle_t handle, const void* y, const void* d
  * batch, written (overwritten, never accumulated) into dw: fp32, same layout
  * as w.  Needs the reserve after rnn_backward_data.  x (device, in, not NULL)
  * is read: it is the input operand of layer 0's dW_ih, and must be the x of
- * rnn_forward.  hx, y: accepted for symmetry with cudnnRNNBackwardWeights (may
- * be NULL); the reserve holds the states and gate gradients that are read. */
+ * rnn_forward.  hx, y: accepted for symmetry with cuDNN's backward-weights
+ * call (may be NULL); the reserve holds the states and gate gradients that are
+ * read. */
 rnn_status_t rnn_backward_weights(rnn_handle_t handle, const void* x, const void* hx,
                                   const void* y, void* workspace, const void* reserve,
                                   void* dw, void* stream);
@@ -200,8 +202,8 @@ rnn_status_t rnn_sync_status(rnn_handle_t handle, void* stream);
 /* Upper bound, in nanoseconds, of every device spin-wait (default 2 s). */
 rnn_status_t rnn_set_timeout_ns(rnn_handle_t handle, uint64_t ns);
 
-/* Variable sequence lengths (poplibs Gru.cpp / Lstm.cpp: the batchwise
- * time-step limit of the forward and backward loops).  ``lengths``: host
+/* Variable sequence lengths (the popnn Gru.cpp and Lstm.cpp pages: the
+ * batchwise time-step limit of the forward and backward loops).  ``lengths``: host
  * array of desc.batch ints, each in [0, seq_len]; sequence b then has
  * lengths[b] valid steps, and at every later step t >= lengths[b] (in time
  * order, for both directions) the step is masked: the state h (and c) is
@@ -217,7 +219,8 @@ rnn_status_t rnn_set_timeout_ns(rnn_handle_t handle, uint64_t ns);
  * outside [0, seq_len], RNN_CUDA_ERROR if the copy fails. */
 rnn_status_t rnn_set_seq_lengths(rnn_handle_t handle, const int* lengths);
 
-/* Recomputation (poplibs Lstm.cpp LstmRecomputationMode::CellAndTanh).
+/* Recomputation (the popnn Lstm.cpp page's recomputation mode that rebuilds
+ * the cell state and its tanh in the backward pass).
  * mode 1: the LSTM forward keeps no cell states in the reserve (smaller by
  * num_layers * D * (seq_len+1) * batch * hidden * 4 bytes); rnn_backward_data
  * recomputes them from the saved gate activations (c_t = f * c_{t-1} + i * g,
@@ -230,8 +233,8 @@ rnn_status_t rnn_set_seq_lengths(rnn_handle_t handle, const int* lengths);
  * modes. */
 rnn_status_t rnn_set_recomputation(rnn_handle_t handle, int mode);
 
-/* LSTM cell clipping (the clip / dclip of the persistent backward-data kernel
- * fragment's LSTM branch).  With enable != 0 and lo < hi the cell state stays
+/* LSTM cell clipping (the clip / dclip of the persistent RNN backward-data
+ * kernel page's LSTM branch).  With enable != 0 and lo < hi the cell state stays
  * the raw value c, and every use of it goes through clip(x) = min(max(x, lo),
  * hi) (a NaN stays NaN): c_t = f * clip(c_{t-1}) + i * g and
  * h_t = o * tanh(clip(c_t)); cy is the raw c_T; the backward uses
@@ -240,8 +243,8 @@ rnn_status_t rnn_set_recomputation(rnn_handle_t handle, int mode);
  * agree.  RNN_BAD_PARAM for a non-LSTM handle or lo >= hi. */
 rnn_status_t rnn_set_cell_clip(rnn_handle_t handle, int enable, double lo, double hi);
 
-/* Interleaved weight update (poplibs Lstm.cpp / Gru.cpp "Interleaved weight
- * update": the weight gradients accumulated inside the backward loop).
+/* Interleaved weight update (the popnn Lstm.cpp and Gru.cpp pages' interleaved
+ * weight update: the weight gradients accumulated inside the backward loop).
  * Where the SIMT persistent backward kernel runs the layers and its per-step
  * share of the recurrent weight gradient is small (units per CTA x hidden x
  * batch <= 16384 multiply-adds; small layers and batches), rnn_backward_data

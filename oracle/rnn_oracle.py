@@ -10,29 +10,26 @@ blocking, fusion or reordering.  Gate blocks are in canonical order
 (LSTM i, f, g, o; GRU r, z, n).  Sequences are seq-major [T, B, F]; states are
 [L*D, B, H] indexed l*D + d.
 
-Sources (titles and sections of the pages the method is taken from):
-  * poplibs popnn ``Lstm.cpp``: ``lstmCellForwardPassCalcUnits`` and
-    ``basicLstmCellForwardPass`` (forward cell), ``backwardStepImpl``
-    (backward step), ``basicLstmParamUpdate`` / ``basicLstmParamUpdateFinal``
-    (weight-gradient accumulation, zeroed accumulators).
-  * poplibs popnn ``Gru.cpp``: ``gruCellForwardPassCalcUnits`` and
-    ``basicGruCellForwardPass`` (reset-before cell),
-    ``gruCellForwardPassCalcUnitsResetAfter`` (resetAfter cell),
-    ``backwardStepImpl`` / ``backwardStepImplResetAfter`` (backward steps),
-    ``basicGruParamUpdate`` (weight-gradient accumulation).
-  * The persistent RNN backward-data kernel fragment (recovered file
-    f1556887768.txt): LSTM and GRU gate-gradient branches, the direction
-    mapping of the step loop, and the initial-state gradients at step zero.
-  * SystemDS ``LibMatrixCuDNN.java``: ``lstm`` / ``lstmBackward`` (the
-    forward / backward-data / backward-weights split, NULL final-state
-    gradient).
-  * Plain RNN cells (the fragment's CUDNN_RNN_RELU / CUDNN_RNN_TANH branch):
+Sources (the pages the method is taken from, by title, and the part of each):
+  * The popnn Lstm.cpp page (Graphcore poplibs LSTM): the forward cell step,
+    the backward step, and the weight update (weight-gradient accumulation
+    into zeroed accumulators).
+  * The popnn Gru.cpp page (Graphcore poplibs GRU): the reset-before and the
+    resetAfter forward cell steps, their backward steps, and the weight
+    update.
+  * The persistent RNN backward-data kernel page (a recovered CUDA listing):
+    the LSTM and GRU gate-gradient branches, the direction mapping of the
+    step loop, and the initial-state gradients at step zero.
+  * The SystemDS LibMatrixCuDNN.java page: the LSTM forward and backward
+    operators (the forward / backward-data / backward-weights split, the
+    absent final-state gradient).
+  * Plain RNN cells (the persistent kernel page's ReLU / tanh branch):
     h' = act(W_ih x + W_hh h + b) with one gate; its backward step multiplies
     the state gradient by the activation's derivative (ReLU: zero where the
     output is not positive; tanh: 1 - h'^2).
 
 Readings where the pages are silent:
-  * LSTM cell clipping (the fragment's clip / dclip on the cell state), when
+  * LSTM cell clipping (the persistent kernel page's clip / dclip on the cell state), when
     enabled with bounds lo < hi: the state is the raw c, and every use of it
     goes through clip(x) = min(max(x, lo), hi) (a NaN stays NaN):
     c_t = f clip(c_{t-1}) + i g, h_t = o tanh(clip(c_t)); cy is the raw c_T;
@@ -45,8 +42,8 @@ Readings where the pages are silent:
     n = tanh(W_in x + b_n + W_hn (r * h));
   * dhy / dcy default to zero; weight gradients overwrite (never accumulate
     across calls).
-  * variable sequence lengths (poplibs Gru.cpp / Lstm.cpp, the batchwise
-    time-step mask of the forward and backward loops): sequence b has
+  * variable sequence lengths (the popnn Gru.cpp and Lstm.cpp pages, the
+    batchwise time-step mask of the forward and backward loops): sequence b has
     len_b <= T valid steps; at a step t >= len_b the mask m = 0 holds the
     state (h, c carried unchanged, the latched final state) and zeroes the
     output, h_t = m h' + (1 - m) h_{t-1}, c_t = m c' + (1 - m) c_{t-1},
@@ -105,7 +102,7 @@ def _masks(T: int, B: int, lengths) -> np.ndarray:
 # LSTM, one direction of one layer
 # ----------------------------------------------------------------------------
 def lstm_forward_dir(x, p, h0, c0, reverse=False, lengths=None, clip=None):
-    """Lstm.cpp, lstmCellForwardPassCalcUnits / basicLstmCellForwardPass:
+    """The popnn Lstm.cpp page, forward cell step:
     a = W_ih x_t + W_hh h_{t-1} + b; i, f, o = sigmoid; g = tanh;
     c' = f c_{t-1} + i g; h' = o tanh(c').  With the step mask m:
     c_t = m c' + (1-m) c_{t-1}; h_t = m h' + (1-m) h_{t-1}; y_t = m h'.
@@ -137,18 +134,18 @@ def lstm_forward_dir(x, p, h0, c0, reverse=False, lengths=None, clip=None):
 
 
 def lstm_backward_dir(x, p, keep, dy, dhT, dcT, reverse=False):
-    """Lstm.cpp backwardStepImpl, identical to the LSTM branch of the
-    persistent backward-data kernel fragment:
+    """The popnn Lstm.cpp page, backward step, identical to the LSTM branch
+    of the persistent RNN backward-data kernel page:
       dh = dy_t + dh_rec
       dc = dh o (1 - tanh^2 c_t) + dc_next
       da_i = dc g i(1-i); da_f = dc c_{t-1} f(1-f); da_g = dc i (1-g^2);
       da_o = dh tanh(c_t) o(1-o)
       dh_rec <- W_hh^T da; dc_next <- dc f
-    Weight gradients (basicLstmParamUpdate): dW_ih = sum da x^T,
+    Weight gradients (the page's weight update): dW_ih = sum da x^T,
     dW_hh = sum da h_{t-1}^T, db = sum da.
     Masked step (m = 0): the gate gradients are zero and dh_rec, dc_next pass
     through unchanged; dy_t does not reach the state.  With cell clipping
-    (the fragment's LSTM branch): dc = dh o (1 - tanh^2 clip(c_t)) dclip(c_t)
+    (the persistent kernel page's LSTM branch): dc = dh o (1 - tanh^2 clip(c_t)) dclip(c_t)
     + dc_next, da_f uses clip(c_{t-1}), da_o uses tanh(clip(c_t)), and
     dc_next <- dc f dclip(c_{t-1})."""
     T, B, I = x.shape
@@ -182,7 +179,7 @@ def lstm_backward_dir(x, p, keep, dy, dhT, dcT, reverse=False):
 # GRU resetAfter, one direction of one layer
 # ----------------------------------------------------------------------------
 def gru_ra_forward_dir(x, p, h0, reverse=False, lengths=None):
-    """Gru.cpp, gruCellForwardPassCalcUnitsResetAfter:
+    """The popnn Gru.cpp page, resetAfter forward cell step:
     a^x = W_ih x + b_i; a^h = W_hh h + b_h; r = s(a^x_r + a^h_r);
     z = s(a^x_z + a^h_z); n = tanh(a^x_n + r a^h_n); h' = (1-z) n + z h.
     With the step mask m: h_t = m h' + (1-m) h_{t-1}; y_t = m h'."""
@@ -210,8 +207,8 @@ def gru_ra_forward_dir(x, p, h0, reverse=False, lengths=None):
 
 
 def gru_ra_backward_dir(x, p, keep, dy, dhT, reverse=False):
-    """Gru.cpp backwardStepImplResetAfter, identical to the GRU branch of the
-    persistent backward-data kernel fragment:
+    """The popnn Gru.cpp page, resetAfter backward step, identical to the GRU
+    branch of the persistent RNN backward-data kernel page:
       dh = dy_t + dh_rec
       dn = dh (1-z)(1-n^2); dz = dh (h_{t-1} - n) z(1-z); dr = dn a^h_n r(1-r)
       input side dA^x = [dr, dz, dn]; recurrent side dA^h = [dr, dz, dn r]
@@ -248,7 +245,7 @@ def gru_ra_backward_dir(x, p, keep, dy, dhT, reverse=False):
 # GRU reset-before, one direction of one layer
 # ----------------------------------------------------------------------------
 def gru_rb_forward_dir(x, p, h0, reverse=False, lengths=None):
-    """Gru.cpp, gruCellForwardPassCalcUnits / basicGruCellForwardPass:
+    """The popnn Gru.cpp page, reset-before forward cell step:
     [r, z] = s(W_{ih,rz} x + W_{hh,rz} h + b_rz);
     n = tanh(W_in x + W_hn (r * h) + b_n); h' = (1-z) n + z h.
     With the step mask m: h_t = m h' + (1-m) h_{t-1}; y_t = m h'."""
@@ -276,12 +273,12 @@ def gru_rb_forward_dir(x, p, h0, reverse=False, lengths=None):
 
 
 def gru_rb_backward_dir(x, p, keep, dy, dhT, reverse=False):
-    """Gru.cpp backwardStepImpl (reset-before):
+    """The popnn Gru.cpp page, reset-before backward step:
       dh = dy_t + dh_rec
       dn = dh (1-z)(1-n^2); dz = dh (h_{t-1} - n) z(1-z)
       d(rh) = W_hn^T dn; dr = d(rh) * h_{t-1} * r(1-r)
       dh_rec <- d(rh) * r + W_{hh,rz}^T [dr, dz] + dh z
-    Weight gradients (basicGruParamUpdate): dW_ih = sum [dr,dz,dn] x^T,
+    Weight gradients (the page's weight update): dW_ih = sum [dr,dz,dn] x^T,
     dW_{hh,rz} = sum [dr,dz] h_{t-1}^T, dW_hn = sum dn (r*h_{t-1})^T,
     db = sum [dr, dz, dn].
     Masked step (m = 0): zero gate gradients, dh_rec passes through."""
@@ -318,7 +315,7 @@ def _act(mode, a):
 
 
 def _dact_from_out(mode, h):
-    """Activation derivative expressed through its output, as the fragment's
+    """Activation derivative expressed through its output, as the persistent kernel page's
     backward branch does: ReLU 1 where h > 0 else 0; tanh 1 - h^2."""
     return (h > 0.0).astype(float) if mode == RNN_RELU else 1.0 - h * h
 
@@ -343,7 +340,7 @@ def rnn_plain_forward_dir(mode, x, p, h0, reverse=False, lengths=None):
 
 
 def rnn_plain_backward_dir(mode, x, p, keep, dy, dhT, reverse=False):
-    """The fragment's plain-RNN branch: da = (dy_t + dh_rec) act'(h'),
+    """The persistent kernel page's plain-RNN branch: da = (dy_t + dh_rec) act'(h'),
     dh_rec <- W_hh^T da (masked steps: da = 0, dh_rec passes through).
     Weight gradients dW_ih = sum da x^T, dW_hh = sum da h_{t-1}^T,
     db = sum da."""

@@ -80,8 +80,15 @@ def test_clock_summary_without_samples():
 def _sources_sha():
     h = hashlib.sha256()
     for f in bench.KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        h.update(bench.code_only(open(os.path.join(ROOT, f)).read()).encode())
     return h.hexdigest()[:16]
+
+
+def test_code_only_ignores_comments_and_whitespace():
+    a = "int f(int x) {  // the sum\n  return x + 1; /* one\n more */ }\n"
+    b = "int f(int x){return x+1;}"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(b.replace("+ 1", "+ 2").replace("+1", "+2"))
 
 
 @pytest.mark.parametrize("sha_ok", [True, False])

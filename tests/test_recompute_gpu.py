@@ -1,5 +1,6 @@
 """Recomputation mode (LSTM cell states recomputed from the saved gates in the
-backward pass, poplibs' CellAndTanh option) on the GPU, through the C ABI:
+backward pass, the popnn Lstm.cpp page's recomputation of the cell state and
+its tanh) on the GPU, through the C ABI:
 parity with the fp64 oracle (the mode changes storage, not the mathematics),
 the smaller reserve, and agreement with the storing mode.  Tolerances: 1e-5
 (fp32), 2e-2 (bf16)."""
