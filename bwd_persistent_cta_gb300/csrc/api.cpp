@@ -327,7 +327,10 @@ int init_handle_host(rnn_handle_s* h, const rnn_desc_t* desc) {
   h->timing = false;
   h->dev = nullptr;
   fill_layout(h);
-  const bool tc_ok = h->bf16 && persist_tc_supported(desc->mode, h->ra, h->H, h->B, 1, h->num_sms);
+  // GRU reset-before below batch kRbTcMinBatch keeps the SIMT kernels (its
+  // latency-mode forward is faster there)
+  const bool tc_ok = h->bf16 && (!h->rb || h->B >= kRbTcMinBatch) &&
+                     persist_tc_supported(desc->mode, h->ra, h->H, h->B, 1, h->num_sms);
   PersistArgs probe;
   probe.mode = desc->mode; probe.reset_after = h->ra; probe.is_bf16 = h->bf16;
   probe.T = h->T; probe.B = h->B; probe.H = h->H; probe.D = h->D; probe.ndir = 1;
@@ -731,6 +734,9 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
     a.clip = h->clip; a.clip_lo = h->clip_lo; a.clip_hi = h->clip_hi;
     a.dh0 = dhx ? static_cast<char*>(dhx) + so : nullptr;
     a.dc0 = (h->lstm && dcx) ? static_cast<char*>(dcx) + so : nullptr;
+    // the projection buffer, idle in the backward, holds the tensor-core
+    // reset-before backward's first-exchange operand [T, B, D*4H]
+    if (h->rb) a.XA = at<char>(workspace, h->w_p);
     if (h->dw_bptt) {
       a.dwhh = at<float>(reserve, h->r_dwhh[l]);
       for (int k = 0; k < 4; ++k) a.whh_map[k] = sr[k];

@@ -276,7 +276,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   // the extended kernel variant takes sequence lengths, cell clipping and the
   // GRU reset-before forward
   const bool rb = a.mode == 1 && !a.reset_after;
-  if (rb && (bwd || !a.RH)) return 2;
+  if (rb && (bwd ? a.XA == nullptr : a.RH == nullptr)) return 2;
   const int ext = (a.len != nullptr || a.clip || rb) ? 1 : 0;
   if (!choose_plan(a.mode, bwd, a.H, a.B, a.ndir, num_sms, ext, &pl)) return 2;
   const int H = a.H, D = a.D;
@@ -313,10 +313,23 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
     if (make_tmap_bf16_4d(&tmX4, bwd ? a.dG : a.Y, dims, strides, box) != 0) single = 0;
   }
   if (!single) tmX4 = tmX;
-  // reset-before: views of RH [D][T*B][H] for the second exchange of a step
-  // (whole K slice per TMA only)
+  // reset-before: views of RH [D][T*B][H] for the forward's second exchange
+  // of a step, of XA [T*B][D*4H] for the backward's first (whole K slice per
+  // TMA only)
   CUtensorMap tmR = tmX, tmR4 = tmX4;
-  if (rb) {
+  if (rb && bwd) {
+    if (!single) return 2;
+    const uint64_t TB = static_cast<uint64_t>(a.T) * a.B;
+    if (make_tmap_bf16_2d(&tmR, a.XA, static_cast<uint64_t>(D) * 4 * H, TB, static_cast<uint64_t>(D) * 4 * H, kSubK,
+                          pl.Npad) != 0)
+      return 2;
+    const uint64_t Kd = 4ull * H;
+    const uint64_t dims[4] = {static_cast<uint64_t>(kSubK), TB, Kd / kSubK, static_cast<uint64_t>(D)};
+    const uint64_t strides[3] = {static_cast<uint64_t>(D) * Kd * 2, static_cast<uint64_t>(kSubK) * 2, Kd * 2};
+    const uint32_t box[4] = {static_cast<uint32_t>(kSubK), static_cast<uint32_t>(pl.Npad),
+                             static_cast<uint32_t>(pl.nsub / nchunk), 1u};
+    if (make_tmap_bf16_4d(&tmR4, a.XA, dims, strides, box) != 0) return 2;
+  } else if (rb) {
     if (!single) return 2;
     const uint64_t TB = static_cast<uint64_t>(a.T) * a.B;
     if (make_tmap_bf16_2d(&tmR, a.RH, H, D * TB, H, kSubK, pl.Npad) != 0) return 2;
@@ -348,7 +361,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   cudaLaunchAttribute attr[1];
   fill_config(cfg, attr, pl, a.ndir, s);
   void* params_fwd[] = {&tmW, &tmX, &tmX4, &tmR, &tmR4, &P};
-  void* params_bwd[] = {&tmW, &tmX, &tmX4, &P};
+  void* params_bwd[] = {&tmW, &tmX, &tmX4, &tmR, &tmR4, &P};
   if (cudaLaunchKernelExC(&cfg, fn, bwd ? params_bwd : params_fwd) != cudaSuccess) return 3;
   return 0;
 }
@@ -357,9 +370,15 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
 
 
 bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms) {
-  if (!(mode == 0 || (mode == 1 && reset_after))) return false;
+  if (!(mode == 0 || mode == 1)) return false;
+  // GRU reset-before: the extended variant, two exchanges per step, each a
+  // whole K slice per TMA
+  const bool rb = mode == 1 && !reset_after;
+  const int ext = rb ? 1 : 0;
   TcPlan f, b;
-  return choose_plan(mode, 0, H, B, ndir, num_sms, 0, &f) && choose_plan(mode, 1, H, B, ndir, num_sms, 0, &b);
+  if (!choose_plan(mode, 0, H, B, ndir, num_sms, ext, &f) || !choose_plan(mode, 1, H, B, ndir, num_sms, ext, &b))
+    return false;
+  return !rb || (f.R >= f.nsub && b.R >= b.nsub);
 }
 
 bool persist_tc_fwd_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms) {

@@ -759,7 +759,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 template <int PP, int KS, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
 persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                      const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ TcPersistParams P) {
+                      const __grid_constant__ CUtensorMap tmX4, const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmA4, const __grid_constant__ TcPersistParams P) {
   RNN_TC_SMEM_VIEW;
   const PersistArgs& a = P.a;
   const int H = a.H, B = a.B, TT = a.T, D = a.D;
@@ -774,6 +775,15 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   constexpr int RPC = 128 / KS;
   const bool clip = EXT && a.clip;
   const float clo = a.clip_lo, chi = a.clip_hi;
+  // GRU reset-before (extended variant only): two exchanges per step.  Phase
+  // A publishes [0, 0, dn, 0] (XA), whose contraction with the resident
+  // W_hh^T is d(rh) = W_hn^T dn; phase B publishes dG = [dr, dz, dn, 0], whose
+  // contraction the next step reads: W_{h,rz}^T [dr, dz] + W_hn^T dn, so the
+  // carry adds d(rh) (r - 1) + dh z to give
+  //   dh_{t-1} = W_{h,rz}^T [dr, dz] + d(rh) r + dh z.
+  const bool rbm = EXT && a.mode == 1 && !a.reset_after;
+  const int ph = rbm ? 2 : 1;   // counter phases per step
+  __nv_bfloat16* XA = static_cast<__nv_bfloat16*>(a.XA);
 
   setup(P, &tmW, &tmX, &tmX4, wsm, bars, ks * P.Kc, dir * H + rg * 128, static_cast<const __nv_bfloat16*>(a.WrT),
         4 * H);
@@ -797,10 +807,12 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   // carry_h: LSTM dh passed over masked steps
   float carry[PP], carry_h[PP], db[PP][4];
   float cnext[PP];   // LSTM: the cell state the next step needs as c_t
+  float dhv[PP], dnv[PP], dzv[PP];   // reset-before: dh, dn, dz between the step's two phases
   int lenp[PP];
 #pragma unroll
   for (int p = 0; p < PP; ++p) {
     carry[p] = carry_h[p] = cnext[p] = 0.f;
+    dhv[p] = dnv[p] = dzv[p] = 0.f;
     lenp[p] = TT;
     db[p][0] = db[p][1] = db[p][2] = db[p][3] = 0.f;
     const int id = threadIdx.x + p * kThreads;
@@ -844,7 +856,8 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     }
     if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B + b0,
                        (s > 0 ? tp : 0) * B + b0,
-                       ks * P.nsub, dir, idesc, adesc0, s > 0, static_cast<unsigned int>(s) * P.nblk_dir, s, ks, n_mma, w_waited, K_BWD_TC)) {
+                       ks * P.nsub, dir, idesc, adesc0, s > 0, static_cast<unsigned int>(s * ph) * P.nblk_dir, s * ph,
+                       ks, n_mma, w_waited, K_BWD_TC)) {
       aborted = true;
       break;
     }
@@ -888,6 +901,25 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       float da[4] = {0.f, 0.f, 0.f, 0.f};
       bool live = true;
       if constexpr (EXT) live = t < lenp[p];
+      if (rbm) {
+        // phase A: dn, dz; [0, 0, dn, 0] to XA for the first exchange
+        const float gh = dhr + carry[p];
+        float dn = 0.f, dz = 0.f;
+        if (live) {
+          const float z = gv[1], n = gv[2], hp = e0[p];
+          const float dh = dyv[p] + gh;
+          dn = dh * (1.f - z) * (1.f - n * n);
+          dz = dh * (hp - n) * z * (1.f - z);
+          dhv[p] = dh;
+        } else {
+          dhv[p] = gh;
+        }
+        dnv[p] = dn;
+        dzv[p] = dz;
+        const float xa[4] = {0.f, 0.f, dn, 0.f};
+        Vec4<__nv_bfloat16>::store(XA + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u, xa);
+        continue;
+      }
       if (lstm) {
         const float gh = EXT ? dhr + carry_h[p] : dhr;
         if (live) {
@@ -934,6 +966,39 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 #pragma unroll
       for (int q = 0; q < 4; ++q) db[p][q] += da[q];
       Vec4<__nv_bfloat16>::store(dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u, da);
+    }
+    if constexpr (EXT) {
+      if (rbm && s < TT) {
+        // publish [0, 0, dn, 0], contract it: d(rh) = W_hn^T dn
+        step_arrive(a, skip, s, 1);
+        if (!step_exchange(P, &tmA, &tmA4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, t * B + b0, t * B + b0,
+                           ks * P.nsub, dir, idesc, adesc0, true, static_cast<unsigned int>(2 * s + 1) * P.nblk_dir,
+                           2 * s + 1, ks, n_mma, w_waited, K_BWD_TC)) {
+          aborted = true;
+          break;
+        }
+        // phase B: dr; dG = [dr, dz, dn, 0]; the carry to the step before
+#pragma unroll
+        for (int p = 0; p < PP; ++p) {
+          const int id = threadIdx.x + p * kThreads;
+          if (id >= npairs) break;
+          const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
+          const uint32_t ra = recv_s + static_cast<uint32_t>(((b - b0) * RPC + ul) * 4);
+          float drh = 0.f;
+#pragma unroll
+          for (int r = 0; r < KS; ++r) drh += lds_f1(ra + r * src_bytes);
+          float gv[4];
+          unpack4(gq[p], gv);
+          const float r = gv[0], z = gv[1];
+          const bool live = t < lenp[p];
+          const float dr = live ? drh * e0[p] * r * (1.f - r) : 0.f;
+          const float da[4] = {dr, dzv[p], dnv[p], 0.f};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) db[p][q] += da[q];
+          Vec4<__nv_bfloat16>::store(dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u, da);
+          carry[p] = live ? dhv[p] * z + drh * (r - 1.f) : dhv[p];
+        }
+      }
     }
     RNN_TRACE_AT(5, 1, s);
     if (s < TT) step_arrive(a, skip, s, 1);
@@ -983,7 +1048,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         int ok = 1;
         if (threadIdx.x == 0) {
           ok = wait_counter_geq(&a.dev->counters[a.dir0 + blockIdx.y],
-                                static_cast<unsigned int>(TT + 1) * P.nblk_dir, a.timeout_ns) ? 1 : 0;
+                                static_cast<unsigned int>(TT * ph + 1) * P.nblk_dir, a.timeout_ns) ? 1 : 0;
           if (!ok) report_status(a.dev, 4u, K_BWD_TC, static_cast<unsigned>(TT), W_COUNTER);
         }
         if (__syncthreads_and(ok)) {

@@ -98,6 +98,9 @@ struct PersistArgs {
   const void* dcT = nullptr;
   void* dh0 = nullptr;               // [D][B, H] slice of dhx
   void* dc0 = nullptr;
+  // tensor-core GRU reset-before backward: [T, B, D*4H] operand of the step's
+  // first exchange, rows [0, 0, dn, 0] per unit (the contraction W_hn^T dn)
+  void* XA = nullptr;
   // recurrent weight gradient accumulated inside the backward kernel (SIMT
   // kernel only): [D][G*H][H] fp32 in the caller's gate blocks, internal slot s
   // of unit u -> row whh_map[s] * H + u (-1: the slot is no W_hh row); the

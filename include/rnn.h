@@ -95,9 +95,10 @@ typedef enum { RNN_LSTM = 0, RNN_GRU = 1, RNN_RNN_RELU = 2, RNN_RNN_TANH = 3 } r
 typedef enum { RNN_F32 = 0, RNN_BF16 = 1 } rnn_dtype_t;
 
 /* Recurrent-kernel choice.  AUTO picks the tensor-core persistent kernels
- * (bf16 LSTM and GRU resetAfter whose W_hh slices fit on chip) and the SIMT
- * persistent kernels otherwise (every fp32 problem, plain RNN cells, GRU
- * reset-before, shapes the tensor-core kernels do not take); with AUTO the
+ * (bf16 LSTM and GRU whose W_hh slices fit on chip; GRU reset-before from
+ * batch 4) and the SIMT persistent kernels otherwise (every fp32 problem,
+ * plain RNN cells, GRU reset-before below batch 4, shapes the tensor-core
+ * kernels do not take); with AUTO the
  * forward alone may still run on the tensor cores (see
  * rnn_selected_fwd_algo).  The two explicit values force one kernel family
  * for both passes. */
@@ -278,10 +279,9 @@ int rnn_selected_algo(rnn_handle_t handle);
 /* Which recurrent kernel the forward runs (rnn_algo_t values).  Equal to
  * rnn_selected_algo except where the automatic choice runs the forward on the
  * tensor-core kernel and the backward on the SIMT kernel: a bf16 LSTM or GRU
- * resetAfter layer whose backward has no tensor-core plan (e.g. hidden 2048,
- * where the forward keeps part of its weight tile in tensor memory and the
- * rest in shared memory), and bf16 GRU reset-before from batch 4 (its
- * forward's two exchanges per step on the tensor cores). */
+ * layer whose backward has no tensor-core plan (e.g. hidden 2048, where the
+ * forward keeps part of its weight tile in tensor memory and the rest in
+ * shared memory, or a hidden size that is not a multiple of 128). */
 int rnn_selected_fwd_algo(rnn_handle_t handle);
 
 /* Per-kernel-class timing with CUDA events recorded on the launching stream

@@ -107,3 +107,29 @@ def test_sampled_columns():
     gpu["y"][:, 4] += 1.0                        # a sampled one
     with pytest.raises(AssertionError):
         Hn.compare(gpu, ref, wl, batch_idx=keep)
+
+
+def test_elementwise_error_definition():
+    # floor 1e-3 of the tensor's scale: 0.5 is held to itself, 1e-6 to 4e-3
+    r = np.array([4.0, 0.5, 1e-6])
+    g = r + np.array([0.0, 0.05, 0.0])
+    assert Hn.max_elem_rel_err(g, r) == pytest.approx(0.1)
+    g = r + np.array([0.0, 0.0, 4e-4])
+    assert Hn.max_elem_rel_err(g, r) == pytest.approx(0.1)
+    assert Hn.max_elem_rel_err(np.zeros(2), np.zeros(2)) == 0.0
+    assert Hn.max_elem_rel_err(np.ones(2), np.zeros(2)) == float("inf")
+
+
+def test_elementwise_bound_catches_a_small_element():
+    # an element near the floor (1e-3 of the tensor's scale) off by 1e-2 of
+    # the scale passes the norm-wise bound (2e-2) but not the elementwise one
+    # (about 10 > 6)
+    wl, _, ref = _case("lstm", False, "bf16")
+    gpu = _as_gpu(ref)
+    y = ref["y"]
+    scale = float(np.max(np.abs(y)))
+    idx = np.unravel_index(np.argmin(np.abs(np.abs(y) - 1e-3 * scale)), y.shape)
+    gpu["y"][idx] = y[idx] + 1e-2 * scale
+    assert Hn.max_rel_err(gpu["y"], y) <= Hn.TOL["bf16"]
+    with pytest.raises(AssertionError, match="elementwise"):
+        Hn.compare(gpu, ref, wl)
