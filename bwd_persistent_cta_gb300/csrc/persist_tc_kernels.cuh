@@ -198,12 +198,35 @@ __device__ bool contract_step(const TcPersistParams& P, const CUtensorMap* tmX, 
     }
     RNN_TRACE_AT(1, tk, s);
     if (first_use_w && P.w_tmem < P.nsub && !mbar_wait(&bars.wbar, 0, to)) return false;
+    // descriptors in registers, advanced per sub-tile: the issue loop does
+    // nothing but the MMAs (one K=16 instruction per 32 bytes of K)
+    const int wt = P.w_tmem;
+    const uint64_t bstep = static_cast<uint64_t>(rbytes >> 4);
+    uint64_t bd = bdesc0;
+    uint32_t at = tmem + P.wcol;
+    uint64_t ad = adesc0;
+    uint32_t acc = 0u;
     for (int c = 0; c < nc; ++c) {
       if (!mbar_wait(&bars.full[c], g & 1, to)) return false;
       if (c == 0) RNN_TRACE_AT(8, tk, s);
       if (c == nc - 1) RNN_TRACE_AT(14, tk, s);
       tc_fence_after();
-      for (int j = c * per; j < (c + 1) * per; ++j) mma_subtile(P, tmem, adesc0, bdesc0, rbytes, idesc, j, j);
+      const int j1 = (c + 1) * per;
+      int j = c * per;
+      for (; j < j1 && j < wt; ++j, at += kSubK / 2, bd += bstep) {
+        mma_bf16_ts(tmem, at, bd, idesc, acc);
+        mma_bf16_ts(tmem, at + 8, bd + 2, idesc, 1u);
+        mma_bf16_ts(tmem, at + 16, bd + 4, idesc, 1u);
+        mma_bf16_ts(tmem, at + 24, bd + 6, idesc, 1u);
+        acc = 1u;
+      }
+      for (; j < j1; ++j, ad += static_cast<uint64_t>(kWSub >> 4), bd += bstep) {
+        mma_bf16_ss(tmem, ad, bd, idesc, acc);
+        mma_bf16_ss(tmem, ad + 2, bd + 2, idesc, 1u);
+        mma_bf16_ss(tmem, ad + 4, bd + 4, idesc, 1u);
+        mma_bf16_ss(tmem, ad + 6, bd + 6, idesc, 1u);
+        acc = 1u;
+      }
     }
     mma_commit(&bars.mma);
     g += 1;
@@ -364,6 +387,95 @@ __device__ __forceinline__ void unpack4(uint2 q, float (&v)[4]) {
   __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&q.y);
   const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
   v[0] = fa.x; v[1] = fa.y; v[2] = fb.x; v[3] = fb.y;
+}
+
+// V (1, 2 or 4) consecutive values in one access: fp32, bf16 (widened to
+// fp32), and V units' 4-slot bf16 rows (as raw 32-bit words / from fp32).
+template <int V>
+__device__ __forceinline__ void ld_f32v(const float* p, float (&o)[V]) {
+  if constexpr (V == 4) {
+    const float4 q = *reinterpret_cast<const float4*>(p);
+    o[0] = q.x; o[1] = q.y; o[2] = q.z; o[3] = q.w;
+  } else if constexpr (V == 2) {
+    const float2 q = *reinterpret_cast<const float2*>(p);
+    o[0] = q.x; o[1] = q.y;
+  } else {
+    o[0] = *p;
+  }
+}
+template <int V>
+__device__ __forceinline__ void ld_bf16v(const __nv_bfloat16* p, float (&o)[V]) {
+  if constexpr (V == 4) {
+    float v[4];
+    unpack4(*reinterpret_cast<const uint2*>(p), v);
+    o[0] = v[0]; o[1] = v[1]; o[2] = v[2]; o[3] = v[3];
+  } else if constexpr (V == 2) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+    o[0] = f.x; o[1] = f.y;
+  } else {
+    o[0] = __bfloat162float(*p);
+  }
+}
+template <int V>
+__device__ __forceinline__ void st_bf16v(__nv_bfloat16* p, const float (&v)[V]) {
+  if constexpr (V == 4) {
+    Vec4<__nv_bfloat16>::store(p, v);
+  } else if constexpr (V == 2) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v[0], v[1]);
+  } else {
+    *p = __float2bfloat16_rn(v[0]);
+  }
+}
+template <int V>
+__device__ __forceinline__ void ld_rows(const __nv_bfloat16* p, uint32_t (&w)[2 * V]) {
+  if constexpr (V == 4) {
+    const uint4 a = reinterpret_cast<const uint4*>(p)[0], b = reinterpret_cast<const uint4*>(p)[1];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  } else if constexpr (V == 2) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  } else {
+    const uint2 a = *reinterpret_cast<const uint2*>(p);
+    w[0] = a.x; w[1] = a.y;
+  }
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <int V>
+__device__ __forceinline__ void st_rows(__nv_bfloat16* p, const float (&v)[V][4]) {
+  uint32_t w[2 * V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    w[2 * j] = pack_bf16x2(v[j][0], v[j][1]);
+    w[2 * j + 1] = pack_bf16x2(v[j][2], v[j][3]);
+  }
+  if constexpr (V == 4) {
+    reinterpret_cast<uint4*>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4*>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  } else if constexpr (V == 2) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+  }
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+  return v;
+}
+template <int V>
+__device__ __forceinline__ void lds_v(uint32_t a, float (&o)[V]) {
+  if constexpr (V == 4) {
+    const float4 q = lds_f4(a);
+    o[0] = q.x; o[1] = q.y; o[2] = q.z; o[3] = q.w;
+  } else if constexpr (V == 2) {
+    const float2 q = lds_f2(a);
+    o[0] = q.x; o[1] = q.y;
+  } else {
+    o[0] = lds_f1(a);
+  }
 }
 
 // Barriers, TMEM, and the resident weight tile: 128 rows from row wy0, K
@@ -798,29 +910,46 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   const int64_t ldY = static_cast<int64_t>(D) * H;
   const int64_t ldG = static_cast<int64_t>(D) * K4;
   const int UPC = P.UPC;
-  const int npairs = UPC * Bn;
   const int ubase = rg * 128 + ks * UPC;
   const uint32_t recv_s = smem_u32(recv);
   const uint32_t src_bytes = static_cast<uint32_t>(P.Npad) * RPC * 4;
+  // Pairs: each thread owns V consecutive units of NQ batch rows (V = 4 from
+  // 4 pairs per thread on), so every gate, state, gradient and partial-sum
+  // access of the epilogue is one vector access per V pairs.  Pair p = q V + j:
+  // unit ul0 + j of local batch row rl0 + q RPT.
+  constexpr int V = PP >= 4 ? 4 : PP;
+  constexpr int NQ = PP / V;
+  const int TPR = UPC / V;               // threads per batch row (UPC is a power of two >= 8)
+  const int RPT = kThreads / TPR;        // batch rows per round of the threads
+  const int ul0 = V * (static_cast<int>(threadIdx.x) % TPR);
+  const int u0 = ubase + ul0;
+  const int rl0 = static_cast<int>(threadIdx.x) / TPR;
 
   // carry: LSTM dc_next, GRU dh*z (or the whole dh over a masked step);
   // carry_h: LSTM dh passed over masked steps
   float carry[PP], carry_h[PP], db[PP][4];
   float cnext[PP];   // LSTM: the cell state the next step needs as c_t
   float dhv[PP], dnv[PP], dzv[PP];   // reset-before: dh, dn, dz between the step's two phases
-  int lenp[PP];
+  int lenq[NQ];
 #pragma unroll
   for (int p = 0; p < PP; ++p) {
     carry[p] = carry_h[p] = cnext[p] = 0.f;
     dhv[p] = dnv[p] = dzv[p] = 0.f;
-    lenp[p] = TT;
     db[p][0] = db[p][1] = db[p][2] = db[p][3] = 0.f;
-    const int id = threadIdx.x + p * kThreads;
-    if (id >= npairs) continue;
-    const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
-    if constexpr (EXT) lenp[p] = a.len ? a.len[b] : TT;   // clipping alone: no lengths
-    if (lstm && a.dcT)
-      carry[p] = __bfloat162float(static_cast<const __nv_bfloat16*>(a.dcT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
+  }
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    lenq[q] = TT;
+    const int rl = rl0 + q * RPT;
+    if (rl >= Bn) continue;
+    const int b = b0 + rl;
+    if constexpr (EXT) lenq[q] = a.len ? a.len[b] : TT;   // clipping alone: no lengths
+    if (lstm && a.dcT) {
+      float v[V];
+      ld_bf16v<V>(static_cast<const __nv_bfloat16*>(a.dcT) + (static_cast<int64_t>(dir) * B + b) * H + u0, v);
+#pragma unroll
+      for (int jj = 0; jj < V; ++jj) carry[q * V + jj] = v[jj];
+    }
   }
 
   const bool skip = a.skip_cta == static_cast<int>(blockIdx.x + gridDim.x * blockIdx.y);
@@ -835,23 +964,38 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     RNN_TRACE_AT(0, 1, s);
     // this step's saved forward values and upstream gradient: load before the exchange
     // (LSTM: c_t is the c_{t-1} the previous step loaded, only c_{t-1} is read)
-    uint2 gq[PP];
+    uint32_t gw[NQ][2 * V];
     float e0[PP], e1[PP], dyv[PP];
 #pragma unroll
-    for (int p = 0; p < PP; ++p) {
-      const int id = threadIdx.x + p * kThreads;
-      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
-      gq[p] = make_uint2(0, 0);
-      e0[p] = e1[p] = dyv[p] = 0.f;
-      if (id < npairs && s < TT) {
-        gq[p] = ld_u2(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * K4 + 4 * u);
-        dyv[p] = a.dYi[(static_cast<int64_t>(t) * B + b) * ldY + dir * H + u];
-        if (lstm) {
-          e0[p] = s == 0 ? Cb[(static_cast<int64_t>(dir ? t : t + 1) * B + b) * H + u] : cnext[p];
-          e1[p] = Cb[(static_cast<int64_t>(dir ? t + 1 : t) * B + b) * H + u];
+    for (int q = 0; q < NQ; ++q) {
+#pragma unroll
+      for (int k = 0; k < 2 * V; ++k) gw[q][k] = 0u;
+#pragma unroll
+      for (int jj = 0; jj < V; ++jj) e0[q * V + jj] = e1[q * V + jj] = dyv[q * V + jj] = 0.f;
+      const int rl = rl0 + q * RPT;
+      if (rl >= Bn || s >= TT) continue;
+      const int b = b0 + rl;
+      ld_rows<V>(G + ((static_cast<int64_t>(dir) * TT + t) * B + b) * K4 + 4 * u0, gw[q]);
+      float v[V];
+      ld_f32v<V>(a.dYi + (static_cast<int64_t>(t) * B + b) * ldY + dir * H + u0, v);
+#pragma unroll
+      for (int jj = 0; jj < V; ++jj) dyv[q * V + jj] = v[jj];
+      if (lstm) {
+        if (s == 0) {
+          ld_f32v<V>(Cb + (static_cast<int64_t>(dir ? t : t + 1) * B + b) * H + u0, v);
+#pragma unroll
+          for (int jj = 0; jj < V; ++jj) e0[q * V + jj] = v[jj];
         } else {
-          e0[p] = __bfloat162float(Y[(static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u]);
+#pragma unroll
+          for (int jj = 0; jj < V; ++jj) e0[q * V + jj] = cnext[q * V + jj];
         }
+        ld_f32v<V>(Cb + (static_cast<int64_t>(dir ? t + 1 : t) * B + b) * H + u0, v);
+#pragma unroll
+        for (int jj = 0; jj < V; ++jj) e1[q * V + jj] = v[jj];
+      } else {
+        ld_bf16v<V>(Y + (static_cast<int64_t>(sp) * B + b) * ldY + dir * H + u0, v);
+#pragma unroll
+        for (int jj = 0; jj < V; ++jj) e0[q * V + jj] = v[jj];
       }
     }
     if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B + b0,
@@ -864,108 +1008,127 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     // recurrent gradient of every pair first (all shared loads in flight)
     float dhs[PP];
 #pragma unroll
-    for (int p = 0; p < PP; ++p) {
-      const int id = threadIdx.x + p * kThreads;
-      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
-      dhs[p] = 0.f;
-      if (id < npairs) {
-        if (s == 0) {
-          if (a.dhT)
-            dhs[p] = __bfloat162float(
-                static_cast<const __nv_bfloat16*>(a.dhT)[(static_cast<int64_t>(dir) * B + b) * H + u]);
-        } else {
-          const uint32_t ra = recv_s + static_cast<uint32_t>(((b - b0) * RPC + ul) * 4);
-          float v[KS];
+    for (int q = 0; q < NQ; ++q) {
 #pragma unroll
-          for (int r = 0; r < KS; ++r) v[r] = lds_f1(ra + r * src_bytes);
+      for (int jj = 0; jj < V; ++jj) dhs[q * V + jj] = 0.f;
+      const int rl = rl0 + q * RPT;
+      if (rl >= Bn) continue;
+      if (s == 0) {
+        if (a.dhT) {
+          float v[V];
+          ld_bf16v<V>(static_cast<const __nv_bfloat16*>(a.dhT) + (static_cast<int64_t>(dir) * B + b0 + rl) * H + u0, v);
 #pragma unroll
-          for (int r = 0; r < KS; ++r) dhs[p] += v[r];
+          for (int jj = 0; jj < V; ++jj) dhs[q * V + jj] = v[jj];
+        }
+      } else {
+        const uint32_t ra = recv_s + static_cast<uint32_t>((rl * RPC + ul0) * 4);
+        float v[KS][V];
+#pragma unroll
+        for (int r = 0; r < KS; ++r) lds_v<V>(ra + r * src_bytes, v[r]);
+#pragma unroll
+        for (int r = 0; r < KS; ++r) {
+#pragma unroll
+          for (int jj = 0; jj < V; ++jj) dhs[q * V + jj] += v[r][jj];
         }
       }
     }
+    RNN_TRACE_AT(12, 1, s);
 #pragma unroll
-    for (int p = 0; p < PP; ++p) {
-      const int id = threadIdx.x + p * kThreads;
-      if (id >= npairs) break;
-      const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
-      const float dhr = dhs[p];
+    for (int q = 0; q < NQ; ++q) {
+      const int rl = rl0 + q * RPT;
+      if (rl >= Bn) break;
+      const int b = b0 + rl;
       if (s == TT) {
-        const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u;
-        if (a.dh0) static_cast<__nv_bfloat16*>(a.dh0)[o] = __float2bfloat16_rn(lstm ? dhr + (EXT ? carry_h[p] : 0.f)
-                                                                                   : dhr + carry[p]);
-        if (lstm && a.dc0) static_cast<__nv_bfloat16*>(a.dc0)[o] = __float2bfloat16_rn(carry[p]);
-        continue;
-      }
-      float gv[4];
-      unpack4(gq[p], gv);
-      float da[4] = {0.f, 0.f, 0.f, 0.f};
-      bool live = true;
-      if constexpr (EXT) live = t < lenp[p];
-      if (rbm) {
-        // phase A: dn, dz; [0, 0, dn, 0] to XA for the first exchange
-        const float gh = dhr + carry[p];
-        float dn = 0.f, dz = 0.f;
-        if (live) {
-          const float z = gv[1], n = gv[2], hp = e0[p];
-          const float dh = dyv[p] + gh;
-          dn = dh * (1.f - z) * (1.f - n * n);
-          dz = dh * (hp - n) * z * (1.f - z);
-          dhv[p] = dh;
-        } else {
-          dhv[p] = gh;
-        }
-        dnv[p] = dn;
-        dzv[p] = dz;
-        const float xa[4] = {0.f, 0.f, dn, 0.f};
-        Vec4<__nv_bfloat16>::store(XA + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u, xa);
-        continue;
-      }
-      if (lstm) {
-        const float gh = EXT ? dhr + carry_h[p] : dhr;
-        if (live) {
-          const float i = gv[0], f = gv[1], gg = gv[2], o = gv[3];
-          const float c = e0[p], cp = e1[p];
-          const float dh = dyv[p] + gh;
-          if (clip) {
-            const float tc = tanh_fast(clipv(c, clo, chi));
-            const float dc = dh * o * (1.f - tc * tc) * dclipv(c, clo, chi) + carry[p];
-            da[0] = dc * gg * i * (1.f - i);
-            da[1] = dc * clipv(cp, clo, chi) * f * (1.f - f);
-            da[2] = dc * i * (1.f - gg * gg);
-            da[3] = dh * tc * o * (1.f - o);
-            carry[p] = dc * f * dclipv(cp, clo, chi);
-          } else {
-            const float tc = tanh_fast(c);
-            const float dc = dh * o * (1.f - tc * tc) + carry[p];
-            da[0] = dc * gg * i * (1.f - i);
-            da[1] = dc * cp * f * (1.f - f);
-            da[2] = dc * i * (1.f - gg * gg);
-            da[3] = dh * tc * o * (1.f - o);
-            carry[p] = dc * f;
-          }
-          if constexpr (EXT) carry_h[p] = 0.f;
-        } else {
-          carry_h[p] = gh;
-        }
-        cnext[p] = e1[p];
-      } else {
-        const float gh = dhr + carry[p];
-        if (live) {
-          const float r = gv[0], z = gv[1], n = gv[2], hn = gv[3];
-          const float hp = e0[p];
-          const float dh = dyv[p] + gh;
-          const float dn = dh * (1.f - z) * (1.f - n * n);
-          const float dz = dh * (hp - n) * z * (1.f - z);
-          const float dr = dn * hn * r * (1.f - r);
-          da[0] = dr; da[1] = dz; da[2] = dn; da[3] = dn * r;
-          carry[p] = dh * z;
-        } else {
-          carry[p] = gh;
-        }
-      }
+        float h0v[V], c0v[V];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) db[p][q] += da[q];
-      Vec4<__nv_bfloat16>::store(dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u, da);
+        for (int jj = 0; jj < V; ++jj) {
+          const int p = q * V + jj;
+          h0v[jj] = lstm ? dhs[p] + (EXT ? carry_h[p] : 0.f) : dhs[p] + carry[p];
+          c0v[jj] = carry[p];
+        }
+        const int64_t o = (static_cast<int64_t>(dir) * B + b) * H + u0;
+        if (a.dh0) st_bf16v<V>(static_cast<__nv_bfloat16*>(a.dh0) + o, h0v);
+        if (lstm && a.dc0) st_bf16v<V>(static_cast<__nv_bfloat16*>(a.dc0) + o, c0v);
+        continue;
+      }
+      bool live = true;
+      if constexpr (EXT) live = t < lenq[q];
+      float da[V][4];
+      float xa[V][4];
+#pragma unroll
+      for (int jj = 0; jj < V; ++jj) {
+        const int p = q * V + jj;
+        const float dhr = dhs[p];
+        float gv[4];
+        unpack4(make_uint2(gw[q][2 * jj], gw[q][2 * jj + 1]), gv);
+        da[jj][0] = da[jj][1] = da[jj][2] = da[jj][3] = 0.f;
+        if (rbm) {
+          // phase A: dn, dz; [0, 0, dn, 0] to XA for the first exchange
+          const float gh = dhr + carry[p];
+          float dn = 0.f, dz = 0.f;
+          if (live) {
+            const float z = gv[1], n = gv[2], hp = e0[p];
+            const float dh = dyv[p] + gh;
+            dn = dh * (1.f - z) * (1.f - n * n);
+            dz = dh * (hp - n) * z * (1.f - z);
+            dhv[p] = dh;
+          } else {
+            dhv[p] = gh;
+          }
+          dnv[p] = dn;
+          dzv[p] = dz;
+          xa[jj][0] = 0.f; xa[jj][1] = 0.f; xa[jj][2] = dn; xa[jj][3] = 0.f;
+          continue;
+        }
+        if (lstm) {
+          const float gh = EXT ? dhr + carry_h[p] : dhr;
+          if (live) {
+            const float i = gv[0], f = gv[1], gg = gv[2], o = gv[3];
+            const float c = e0[p], cp = e1[p];
+            const float dh = dyv[p] + gh;
+            if (clip) {
+              const float tc = tanh_fast(clipv(c, clo, chi));
+              const float dc = dh * o * (1.f - tc * tc) * dclipv(c, clo, chi) + carry[p];
+              da[jj][0] = dc * gg * i * (1.f - i);
+              da[jj][1] = dc * clipv(cp, clo, chi) * f * (1.f - f);
+              da[jj][2] = dc * i * (1.f - gg * gg);
+              da[jj][3] = dh * tc * o * (1.f - o);
+              carry[p] = dc * f * dclipv(cp, clo, chi);
+            } else {
+              const float tc = tanh_fast(c);
+              const float dc = dh * o * (1.f - tc * tc) + carry[p];
+              da[jj][0] = dc * gg * i * (1.f - i);
+              da[jj][1] = dc * cp * f * (1.f - f);
+              da[jj][2] = dc * i * (1.f - gg * gg);
+              da[jj][3] = dh * tc * o * (1.f - o);
+              carry[p] = dc * f;
+            }
+            if constexpr (EXT) carry_h[p] = 0.f;
+          } else {
+            carry_h[p] = gh;
+          }
+          cnext[p] = e1[p];
+        } else {
+          const float gh = dhr + carry[p];
+          if (live) {
+            const float r = gv[0], z = gv[1], n = gv[2], hn = gv[3];
+            const float hp = e0[p];
+            const float dh = dyv[p] + gh;
+            const float dn = dh * (1.f - z) * (1.f - n * n);
+            const float dz = dh * (hp - n) * z * (1.f - z);
+            const float dr = dn * hn * r * (1.f - r);
+            da[jj][0] = dr; da[jj][1] = dz; da[jj][2] = dn; da[jj][3] = dn * r;
+            carry[p] = dh * z;
+          } else {
+            carry[p] = gh;
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) db[p][c] += da[jj][c];
+      }
+      const int64_t row = (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u0;
+      if (rbm) st_rows<V>(XA + row, xa);
+      else st_rows<V>(dG + row, da);
     }
     if constexpr (EXT) {
       if (rbm && s < TT) {
@@ -979,24 +1142,32 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         }
         // phase B: dr; dG = [dr, dz, dn, 0]; the carry to the step before
 #pragma unroll
-        for (int p = 0; p < PP; ++p) {
-          const int id = threadIdx.x + p * kThreads;
-          if (id >= npairs) break;
-          const int ul = id % UPC, b = b0 + id / UPC, u = ubase + ul;
-          const uint32_t ra = recv_s + static_cast<uint32_t>(((b - b0) * RPC + ul) * 4);
-          float drh = 0.f;
+        for (int q = 0; q < NQ; ++q) {
+          const int rl = rl0 + q * RPT;
+          if (rl >= Bn) break;
+          const int b = b0 + rl;
+          const uint32_t ra = recv_s + static_cast<uint32_t>((rl * RPC + ul0) * 4);
+          float v[KS][V];
 #pragma unroll
-          for (int r = 0; r < KS; ++r) drh += lds_f1(ra + r * src_bytes);
-          float gv[4];
-          unpack4(gq[p], gv);
-          const float r = gv[0], z = gv[1];
-          const bool live = t < lenp[p];
-          const float dr = live ? drh * e0[p] * r * (1.f - r) : 0.f;
-          const float da[4] = {dr, dzv[p], dnv[p], 0.f};
+          for (int r = 0; r < KS; ++r) lds_v<V>(ra + r * src_bytes, v[r]);
+          const bool live = t < lenq[q];
+          float da[V][4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) db[p][q] += da[q];
-          Vec4<__nv_bfloat16>::store(dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u, da);
-          carry[p] = live ? dhv[p] * z + drh * (r - 1.f) : dhv[p];
+          for (int jj = 0; jj < V; ++jj) {
+            const int p = q * V + jj;
+            float drh = 0.f;
+#pragma unroll
+            for (int r = 0; r < KS; ++r) drh += v[r][jj];
+            float gv[4];
+            unpack4(make_uint2(gw[q][2 * jj], gw[q][2 * jj + 1]), gv);
+            const float r = gv[0], z = gv[1];
+            const float dr = live ? drh * e0[p] * r * (1.f - r) : 0.f;
+            da[jj][0] = dr; da[jj][1] = dzv[p]; da[jj][2] = dnv[p]; da[jj][3] = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) db[p][c] += da[jj][c];
+            carry[p] = live ? dhv[p] * z + drh * (r - 1.f) : dhv[p];
+          }
+          st_rows<V>(dG + (static_cast<int64_t>(t) * B + b) * ldG + dir * K4 + 4 * u0, da);
         }
       }
     }
@@ -1007,40 +1178,36 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 
   if (!aborted) {
     // bias gradients: reduce each unit's four sums over the batch (reuses recv,
-    // after every peer has finished with it)
+    // after every peer has finished with it), one unit slot j of the threads'
+    // V units per pass.  Deterministic order throughout: each thread sums its
+    // batch rows in order, then unit V w + j adds threads w, w + TPR, ... in
+    // index order.
     tc_fence_before();
     if (KS > 1) cluster_sync(); else __syncthreads();
-    // Deterministic order throughout: UPC divides kThreads, so all pairs of
-    // thread t belong to unit t % UPC; each thread sums its pairs in order,
-    // then unit ul adds threads ul, ul + UPC, ... in index order.
     float* red = recv;
-    {
-      float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int p = 0; p < PP; ++p) {
-        const int id = threadIdx.x + p * kThreads;
-        if (id >= npairs) break;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) part[q] += db[p][q];
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) red[threadIdx.x * 4 + q] = part[q];
-    }
-    __syncthreads();
     // this batch part's sums to plane nb of db [NB][D][4H]; with several
     // parts, part 0 then adds planes 1.. in order once every CTA of the
     // direction has arrived once more
     float* plane = a.db + (static_cast<int64_t>(nb) * D + dir) * K4 + 4 * ubase;
-    float sums[2] = {0.f, 0.f};   // 4 * UPC <= 2 * kThreads values
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int i = threadIdx.x + k * kThreads;
-      if (i >= 4 * UPC) break;
-      const int ul = i >> 2, q = i & 3;
-      float v = 0.f;
-      for (int t2 = ul; t2 < kThreads; t2 += UPC) v += red[t2 * 4 + q];
-      sums[k] = v;
-      plane[i] = v;
+    for (int jj = 0; jj < V; ++jj) {
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (rl0 + q * RPT >= Bn) break;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) part[c] += db[q * V + jj][c];
+      }
+      if (jj > 0) __syncthreads();   // the previous pass's reads of red are done
+#pragma unroll
+      for (int c = 0; c < 4; ++c) red[threadIdx.x * 4 + c] = part[c];
+      __syncthreads();
+      for (int i = threadIdx.x; i < 4 * TPR; i += kThreads) {
+        const int w = i >> 2, c = i & 3;
+        float v = 0.f;
+        for (int t2 = w; t2 < kThreads; t2 += TPR) v += red[t2 * 4 + c];
+        plane[4 * (V * w + jj) + c] = v;
+      }
     }
     if (P.NB > 1) {
       step_arrive(a, skip, TT, 1);
@@ -1052,11 +1219,8 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
           if (!ok) report_status(a.dev, 4u, K_BWD_TC, static_cast<unsigned>(TT), W_COUNTER);
         }
         if (__syncthreads_and(ok)) {
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int i = threadIdx.x + k * kThreads;
-            if (i >= 4 * UPC) break;
-            float v = sums[k];
+          for (int i = threadIdx.x; i < 4 * UPC; i += kThreads) {
+            float v = __ldcg(plane + i);
             for (int q = 1; q < P.NB; ++q) v += __ldcg(a.db + (static_cast<int64_t>(q) * D + dir) * K4 + 4 * ubase + i);
             plane[i] = v;
           }
