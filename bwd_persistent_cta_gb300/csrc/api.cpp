@@ -217,7 +217,10 @@ int run_gemm(rnn_handle_s* h, GemmArgs g, cudaStream_t s, int cls) {
 }
 
 int reset_counters(rnn_handle_s* h, cudaStream_t s) {
-  return cudaMemsetAsync(h->dev->counters, 0, sizeof(h->dev->counters), s) == cudaSuccess ? 0 : 3;
+  return cudaMemsetAsync(h->dev->counters, 0, sizeof(h->dev->counters) + sizeof(h->dev->slice_ctr), s) ==
+                 cudaSuccess
+             ? 0
+             : 3;
 }
 
 // One persistent launch per layer (both directions), or one per direction

@@ -297,8 +297,9 @@ template <typename Deferred = NoDeferred>
 __device__ __forceinline__ bool step_exchange(const TcPersistParams& P, const CUtensorMap* tmX, const CUtensorMap* tmX4,
                               uint8_t* ring, float* recv, TcBars& bars, uint32_t tmem, uint32_t& g, int x0, int y0,
                               int y4, int c2, int dir, uint32_t idesc,
-                              uint64_t adesc0, bool do_contract, unsigned int wait_target, int s, int ks, int& n_mma,
-                              bool& w_waited, unsigned int kernel, const Deferred& deferred = Deferred()) {
+                              uint64_t adesc0, bool do_contract, unsigned int* ctr_in, unsigned int wait_target, int s,
+                              int ks, int& n_mma, bool& w_waited, unsigned int kernel,
+                              const Deferred& deferred = Deferred()) {
   const PersistArgs& a = P.a;
   const int tk = kernel == K_BWD_TC ? 1 : 0;
   (void)tk;
@@ -310,7 +311,7 @@ __device__ __forceinline__ bool step_exchange(const TcPersistParams& P, const CU
     __syncwarp();
   }
   if (threadIdx.x == 0) {
-    if (wait_target > 0 && !wait_counter_geq(&a.dev->counters[a.dir0 + blockIdx.y], wait_target, a.timeout_ns)) {
+    if (wait_target > 0 && !wait_counter_geq(ctr_in, wait_target, a.timeout_ns)) {
       ok = 0;
       report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_COUNTER);
     }
@@ -358,12 +359,22 @@ __device__ __forceinline__ bool step_exchange(const TcPersistParams& P, const CU
 // before the release add.  Fencing here, on the writer side, keeps the fence
 // off the reader's critical path, where it would also wait for the reader's
 // own outstanding prefetch loads.
-__device__ __forceinline__ void step_arrive(const PersistArgs& a, bool skip, int s, int tk) {
+__device__ __forceinline__ void step_arrive(unsigned int* ctr_out, bool skip, int s, int tk) {
   (void)s; (void)tk;
   fence_proxy_async_global();
   __syncthreads();
   RNN_TRACE_AT(11, tk, s);
-  if (threadIdx.x == 0 && !skip) red_release_gpu_add(&a.dev->counters[a.dir0 + blockIdx.y], 1u);
+  if (threadIdx.x == 0 && !skip) red_release_gpu_add(ctr_out, 1u);
+}
+
+// The step counter a CTA waits on (the K slice ks it contracts) or arrives on
+// (the K slice its outputs fall in), of its direction and batch part.  Each of
+// the KS slices of a batch part is written by exactly nrg CTAs: one CTA's
+// outputs (forward 32/KS units, backward 4 x 128/KS gate-gradient columns)
+// lie in one slice of H/KS units (forward) or 4H/KS columns (backward).
+__device__ __forceinline__ unsigned int* slice_counter(const TcPersistParams& P, int nbp, int slice) {
+  const int d = P.a.dir0 + static_cast<int>(blockIdx.y);
+  return &P.a.dev->slice_ctr[(d * P.NB + nbp) * P.KS + slice];
 }
 
 __device__ __forceinline__ uint2 ld_u2(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
@@ -618,6 +629,11 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     }
   }
 
+  // the step counters: in, the K slice this CTA contracts; out, the slice its
+  // units' new state falls in
+  const int nbp = static_cast<int>(blockIdx.x) / KS / P.nrg;
+  unsigned int* const ctr_in = slice_counter(P, nbp, ks);
+  unsigned int* const ctr_out = slice_counter(P, nbp, (rg * 32) / P.Kc);
   const bool skip = a.skip_cta == static_cast<int>(blockIdx.x + gridDim.x * blockIdx.y);
   uint32_t g = 0;
   int n_mma = 0;
@@ -746,9 +762,8 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       if (s > 0) post_stores(s - 1, false);
     };
     if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * H + ks * P.Kc, sp * B + b0, sp * B + b0,
-                       ks * P.nsub,
-                       dir, idesc, adesc0, true, static_cast<unsigned int>(ex) * P.nblk_dir, ex, ks, n_mma, w_waited,
-                       K_FWD_TC, deferred)) {
+                       ks * P.nsub, dir, idesc, adesc0, true, ctr_in, static_cast<unsigned int>(ex) * P.nrg, ex, ks,
+                       n_mma, w_waited, K_FWD_TC, deferred)) {
       aborted = true;
       break;
     }
@@ -826,9 +841,9 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     if constexpr (EXT) {
       if (rbm) {
         // reset-before, phase B: publish r * h_{t-1}, then n = tanh(W_in x + b_n + W_hn (r * h_{t-1}))
-        step_arrive(a, skip, s, 0);
+        step_arrive(ctr_out, skip, s, 0);
         if (!step_exchange(P, &tmR, &tmR4, ring, recv, bars, tmem, g, ks * P.Kc, (dir * TT + t) * B + b0, t * B + b0,
-                           ks * P.nsub, dir, idesc, adesc0, true, static_cast<unsigned int>(ex + 1) * P.nblk_dir,
+                           ks * P.nsub, dir, idesc, adesc0, true, ctr_in, static_cast<unsigned int>(ex + 1) * P.nrg,
                            ex + 1, ks, n_mma, w_waited, K_FWD_TC)) {
           aborted = true;
           break;
@@ -858,7 +873,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     RNN_TRACE_AT(13, 0, s);
     stage_own(s);
     RNN_TRACE_AT(5, 0, s);
-    step_arrive(a, skip, s, 0);
+    step_arrive(ctr_out, skip, s, 0);
     RNN_TRACE_AT(6, 0, s);
   }
   if (!aborted) post_stores(TT - 1, true);
@@ -952,6 +967,10 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     }
   }
 
+  // the step counters: in, the K slice this CTA contracts; out, the slice its
+  // units' gate gradients fall in
+  unsigned int* const ctr_in = slice_counter(P, nb, ks);
+  unsigned int* const ctr_out = slice_counter(P, nb, (4 * ubase) / P.Kc);
   const bool skip = a.skip_cta == static_cast<int>(blockIdx.x + gridDim.x * blockIdx.y);
   uint32_t g = 0;
   int n_mma = 0;
@@ -999,9 +1018,8 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       }
     }
     if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B + b0,
-                       (s > 0 ? tp : 0) * B + b0,
-                       ks * P.nsub, dir, idesc, adesc0, s > 0, static_cast<unsigned int>(s * ph) * P.nblk_dir, s * ph,
-                       ks, n_mma, w_waited, K_BWD_TC)) {
+                       (s > 0 ? tp : 0) * B + b0, ks * P.nsub, dir, idesc, adesc0, s > 0, ctr_in,
+                       static_cast<unsigned int>(s * ph) * P.nrg, s * ph, ks, n_mma, w_waited, K_BWD_TC)) {
       aborted = true;
       break;
     }
@@ -1133,9 +1151,9 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     if constexpr (EXT) {
       if (rbm && s < TT) {
         // publish [0, 0, dn, 0], contract it: d(rh) = W_hn^T dn
-        step_arrive(a, skip, s, 1);
+        step_arrive(ctr_out, skip, s, 1);
         if (!step_exchange(P, &tmA, &tmA4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, t * B + b0, t * B + b0,
-                           ks * P.nsub, dir, idesc, adesc0, true, static_cast<unsigned int>(2 * s + 1) * P.nblk_dir,
+                           ks * P.nsub, dir, idesc, adesc0, true, ctr_in, static_cast<unsigned int>(2 * s + 1) * P.nrg,
                            2 * s + 1, ks, n_mma, w_waited, K_BWD_TC)) {
           aborted = true;
           break;
@@ -1172,7 +1190,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       }
     }
     RNN_TRACE_AT(5, 1, s);
-    if (s < TT) step_arrive(a, skip, s, 1);
+    if (s < TT) step_arrive(ctr_out, skip, s, 1);
     RNN_TRACE_AT(6, 1, s);
   }
 
@@ -1210,12 +1228,13 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       }
     }
     if (P.NB > 1) {
-      step_arrive(a, skip, TT, 1);
+      // every CTA of the direction arrives once on the direction's counter
+      // after writing its plane; part 0 then sums the planes
+      step_arrive(&a.dev->counters[a.dir0 + blockIdx.y], skip, TT, 1);
       if (nb == 0) {
         int ok = 1;
         if (threadIdx.x == 0) {
-          ok = wait_counter_geq(&a.dev->counters[a.dir0 + blockIdx.y],
-                                static_cast<unsigned int>(TT * ph + 1) * P.nblk_dir, a.timeout_ns) ? 1 : 0;
+          ok = wait_counter_geq(&a.dev->counters[a.dir0 + blockIdx.y], P.nblk_dir, a.timeout_ns) ? 1 : 0;
           if (!ok) report_status(a.dev, 4u, K_BWD_TC, static_cast<unsigned>(TT), W_COUNTER);
         }
         if (__syncthreads_and(ok)) {

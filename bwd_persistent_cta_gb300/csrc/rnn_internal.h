@@ -37,11 +37,15 @@ namespace rnn {
 constexpr int kSlots = 4;
 
 struct DevArea {
-  unsigned int counters[32];   // step counters of the running persistent launch
+  unsigned int counters[32];   // step counters of the running persistent launch (per direction)
+  // tensor-core persistent kernels: per (direction, batch part, K slice), the
+  // arrivals of the CTAs whose outputs form that K slice of the exchanged state
+  unsigned int slice_ctr[128];
   unsigned int status;         // 0, or the first rnn_status_t a kernel reported
   unsigned int where[4];       // kernel id, block, step, wait kind of that report
-  unsigned int pad[27];
+  unsigned int pad[91];        // to 1 KB
 };
+static_assert(sizeof(DevArea) == 1024, "DevArea is 1 KB");
 
 enum KernelId : unsigned int { K_FWD_SIMT = 1, K_BWD_SIMT = 2, K_FWD_TC = 3, K_BWD_TC = 4, K_GEMM_TC = 5 };
 enum WaitKind : unsigned int { W_COUNTER = 1, W_TMA = 2, W_MMA = 3 };

@@ -320,7 +320,7 @@ rnn_status_t rnn_get_timing_ex(rnn_handle_t handle, double* ms, uint64_t* n, dou
  *                         timeout of that call is then reported only by
  *                         rnn_noalloc_status, which must run before the next
  *                         call on the device (each call clears the status)
- * Returns RNN_NOT_SUPPORTED when the problem's workspace plus 256 bytes of
+ * Returns RNN_NOT_SUPPORTED when the problem's workspace plus 1 KB of
  * counters exceeds RNN_NOALLOC_SCRATCH_BYTES (nothing is launched then).
  * The first call on each device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream

@@ -16,7 +16,7 @@ from tests import harness as Hn
 
 pytestmark = pytest.mark.gpu
 
-AREA = 256   # the counters and status word in front of the workspace
+AREA = 1024  # the counters and status word in front of the workspace
 
 
 def _desc(R, wl):
