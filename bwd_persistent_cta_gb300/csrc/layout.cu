@@ -1,6 +1,6 @@
 // layout.cu - the layout / cast / pack kernels around the recurrence:
 //   * weight packing into the unit-interleaved 4-slot order the GEMMs and the
-//     persistent kernels read (plain and transposed, 32x32 shared-memory tiles
+//     persistent kernels read (plain, and transposed through 64x64 shared-memory tiles
 //     so both sides stay coalesced);
 //   * bias packing and bias-gradient scatter back to the caller's gate order;
 //   * sequence copies between seq-major [T,B,F] and batch-first [B,T,F], with
@@ -9,6 +9,8 @@
 // The SystemDS LibMatrixCuDNN.java page does the same job with separate layout
 // kernels for the output, the upstream gradients, dx and dW around the cuDNN
 // calls of its LSTM forward and backward operators.
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace rnn {
@@ -18,7 +20,7 @@ namespace {
 // Several layout jobs in one launch: job j takes blocks [start[j], start[j+1])
 // and walks its elements with a stride of its block count.
 //   PACK_ROWS    out[(4u+s)*ld + k] = W[(map[s]*H + u)*K + k]   (zero for map -1)
-//   PACK_ROWS_T  out[k*ld + 4u+s]   = the same, through a 32x33 tile
+//   PACK_ROWS_T  out[k*ld + 4u+s]   = the same, through a 64x65 tile
 //   PACK_BIAS    out[4u+s] = b[map[s]*H + u]                     (fp32 out)
 //   SCATTER_DB   out[map[s]*H + u] = db[4u+s]                    (fp32)
 //   H0_TO_Y      Y[slot][b][dir*H + u] = h0[b][u], slot 0 (forward) / T+1 (reverse)
@@ -54,35 +56,64 @@ __device__ __forceinline__ void pack_job_rows(const PackJob& J, int blk, int nbl
   }
 }
 
+// Transposed packing through 64 x 64 tiles: every global access moves two
+// consecutive elements (4 bytes for bf16), on the read side along K, on the
+// write side along the packed rows (odd K, odd row stride or unaligned
+// bases: one element at a time).
 template <typename T>
-__device__ __forceinline__ void pack_job_rows_t(const PackJob& J, int blk, int nblk, float (*tile)[33]) {
+__device__ __forceinline__ void pack_job_rows_t(const PackJob& J, int blk, int nblk, float (*tile)[65]) {
   const T* W = static_cast<const T*>(J.in);
   T* out = static_cast<T*>(J.out);
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8
-  const int tk = (J.K + 31) / 32, tr = (4 * J.H + 31) / 32;
+  const int R = 4 * J.H;
+  const int tk = (J.K + 63) / 64, tr = (R + 63) / 64;
+  using T2 = typename std::conditional<std::is_same<T, float>::value, float2, __nv_bfloat162>::type;
+  const bool pair = J.K % 2 == 0 && J.ld_out % 2 == 0 && (reinterpret_cast<uintptr_t>(W) & 7) == 0 &&
+                    (reinterpret_cast<uintptr_t>(out) & 7) == 0;
   for (int tile_i = blk; tile_i < tk * tr; tile_i += nblk) {
-    const int k0 = (tile_i % tk) * 32, r0 = (tile_i / tk) * 32;
+    const int k0 = (tile_i % tk) * 64, r0 = (tile_i / tk) * 64;
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-      const int row = r0 + i, k = k0 + tx;
-      float v = 0.f;
-      if (row < 4 * J.H && k < J.K) {
-        const int sb = J.map[row & 3];
-        if (sb >= 0) v = to_f<T>(W[(static_cast<int64_t>(sb) * J.H + (row >> 2)) * J.K + k]);
+    // rows r0..r0+63 of the packed order, K columns k0..k0+63: tile[row][k]
+    for (int i = ty; i < 64; i += 8) {
+      const int row = r0 + i;
+      const int sb = row < R ? J.map[row & 3] : -1;
+      const T* src = sb >= 0 ? W + (static_cast<int64_t>(sb) * J.H + (row >> 2)) * J.K : nullptr;
+      const int k = k0 + 2 * tx;
+      float v0 = 0.f, v1 = 0.f;
+      if (src) {
+        if (pair && k + 1 < J.K) {
+          const T2 q = *reinterpret_cast<const T2*>(src + k);
+          if constexpr (std::is_same<T, float>::value) { v0 = q.x; v1 = q.y; }
+          else { const float2 f = __bfloat1622float2(q); v0 = f.x; v1 = f.y; }
+        } else {
+          if (k < J.K) v0 = to_f<T>(src[k]);
+          if (k + 1 < J.K) v1 = to_f<T>(src[k + 1]);
+        }
       }
-      tile[i][tx] = v;
+      tile[i][2 * tx] = v0;
+      tile[i][2 * tx + 1] = v1;
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-      const int k = k0 + i, row = r0 + tx;
-      if (k < J.K && row < 4 * J.H) out[static_cast<int64_t>(k) * J.ld_out + row] = from_f<T>(tile[tx][i]);
+    // out[k][r0..r0+63]: two consecutive packed rows per thread
+    for (int i = ty; i < 64; i += 8) {
+      const int k = k0 + i, row = r0 + 2 * tx;
+      if (k >= J.K) continue;
+      T* dst = out + static_cast<int64_t>(k) * J.ld_out + row;
+      const float v0 = tile[2 * tx][i], v1 = tile[2 * tx + 1][i];
+      if (pair && row + 1 < R) {
+        if constexpr (std::is_same<T, float>::value) *reinterpret_cast<float2*>(dst) = make_float2(v0, v1);
+        else *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(v0, v1);
+      } else {
+        if (row < R) dst[0] = from_f<T>(v0);
+        if (row + 1 < R) dst[1] = from_f<T>(v1);
+      }
     }
   }
 }
 
 template <typename T>
 __global__ void __launch_bounds__(256) pack_batch_kernel(PackBatchArgs P) {
-  __shared__ float tile[32][33];
+  __shared__ float tile[64][65];
   int j = 0;
   while (j < P.n - 1 && static_cast<int>(blockIdx.x) >= P.start[j + 1]) ++j;
   const PackJob& J = P.job[j];
@@ -239,7 +270,7 @@ int launch_pack_batch(const PackBatch& pb, int is_bf16, cudaStream_t s) {
     int64_t work;
     switch (J.kind) {
       case PACK_ROWS: work = (static_cast<int64_t>(4) * J.H * J.K + 1023) / 1024; break;
-      case PACK_ROWS_T: work = static_cast<int64_t>((J.K + 31) / 32) * ((4 * J.H + 31) / 32); break;
+      case PACK_ROWS_T: work = static_cast<int64_t>((J.K + 63) / 64) * ((4 * J.H + 63) / 64); break;
       case H0_TO_Y: work = (static_cast<int64_t>(J.B) * J.H + 255) / 256; break;
       default: work = (4 * J.H + 255) / 256;
     }
