@@ -382,7 +382,7 @@ struct DeviceGuard {
 namespace rnn {
 namespace {
 std::mutex g_override_mu;
-PlanOverrides g_override{0, 0, 0, 0, 0, 0};
+PlanOverrides g_override{0, 0, 0, 0, 0, 0, 0};
 }  // namespace
 PlanOverrides plan_overrides() {
   std::lock_guard<std::mutex> lock(g_override_mu);
@@ -540,14 +540,15 @@ int rnn_selected_fwd_algo(rnn_handle_t h) {
 }
 
 rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn,
-                                          int gemm_splits) {
+                                          int gemm_splits, int gemm_tm) {
   auto ks_ok = [](int v) { return v >= 0 && v <= 16; };
   auto nb_ok = [](int v) { return v == 0 || v == 1 || v == 2 || v == 4; };
   if (!ks_ok(max_ks_fwd) || !ks_ok(max_ks_bwd) || !nb_ok(nb_fwd) || !nb_ok(nb_bwd) ||
-      !(gemm_bn == 0 || gemm_bn == 128 || gemm_bn == 256) || !ks_ok(gemm_splits))
+      !(gemm_bn == 0 || gemm_bn == 128 || gemm_bn == 256) || !ks_ok(gemm_splits) ||
+      !(gemm_tm == 0 || gemm_tm == 128 || gemm_tm == 256) || (gemm_tm == 256 && gemm_bn == 128))
     return RNN_BAD_PARAM;
   std::lock_guard<std::mutex> lock(rnn::g_override_mu);
-  rnn::g_override = {max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn, gemm_splits};
+  rnn::g_override = {max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn, gemm_splits, gemm_tm};
   return RNN_OK;
 }
 

@@ -7,20 +7,29 @@
 //   weight gradients  dW = dG^T * [X | H_prev] (the popnn Lstm.cpp / Gru.cpp pages'
 //                                              weight update, one long-K GEMM)
 //
-// Structure: a persistent kernel, one CTA per SM, 128 x BN output tiles
-// (BN = 256, or 128 when 256-wide tiles would leave most SMs idle), 64-deep K
-// slices in a shared-memory ring (4 x 48 KB or 6 x 32 KB).
+// Structure: a persistent kernel, one CTA per SM, TM x BN output tiles
+// (128 x 256; 128 x 128 when 256-wide tiles would leave most SMs idle;
+// 256 x 256 for long K), 64-deep K slices in a shared-memory ring (4 x 48 KB,
+// 6 x 32 KB or 3 x 64 KB).
 //   warp 0       TMA producer (one elected thread)
 //   warp 1       TMEM owner and MMA issuer (one elected thread); M=128, N=BN,
-//                K=16 per tcgen05.mma, 128-byte swizzled operands
+//                K=16 per tcgen05.mma (two per K step for 256-row tiles, one
+//                per 128-row half, sharing the B operand), 128-byte swizzled
+//                operands
 //   warps 2..9   epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//                lanes 32*(w%4) .. +31 = tile rows; warps 2-5 the first half
-//                of the tile's columns, warps 6-9 the second), bias /
-//                accumulate / cast, global stores with the gate-slot row remap
-// Two TMEM accumulators (2 x BN columns) let the epilogue of one tile overlap
-// the main loop of the next.  Operands may be K-major (row = M or N index, K
-// contiguous) or MN-major (K = row index, M or N contiguous); the descriptor
-// major-ness bits select which.
+//                lanes 32*(w%4) .. +31 = tile rows; with 128-row tiles warps
+//                2-5 take the first half of the tile's columns and warps 6-9
+//                the second, with 256-row tiles they take the two row halves),
+//                32 x 32 blocks staged in shared memory and written by row
+//                segments (bias / accumulate / cast, gate-slot row remap)
+// With 128-row tiles two TMEM accumulators (2 x BN columns) let the epilogue
+// of one tile overlap the main loop of the next; a 256 x 256 tile fills the
+// 512 columns, so its epilogue releases the accumulator after its last
+// tcgen05.ld.  The 256-row tile loads a third fewer operand bytes per FLOP
+// (the 128 x 256 tile's main loop is bound by operand delivery from L2).
+// Operands may be K-major (row = M or N index, K contiguous) or MN-major
+// (K = row index, M or N contiguous); the descriptor major-ness bits select
+// which.
 //
 // Groups: one launch may cover up to kMaxGroups GEMMs with the same K and
 // operand major-ness (the weight gradients of a layer: W_ih and W_hh of every
@@ -54,19 +63,29 @@ constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int kMaxSplits = 16;
 constexpr int kMaxGroups = 6;
 
-template <int BN>
+// Tiles of TM x BN: TM = 128 (one M=128 accumulator, two of them in tensor
+// memory so the epilogue of a tile overlaps the next tile's main loop), or
+// TM = 256 with BN = 256 (two M=128 halves that share each B stage, in tensor
+// memory columns [0, 256) and [256, 512): a third fewer operand bytes per
+// FLOP, but one accumulator, so the epilogue does not overlap; taken for long
+// K, where the main loop dwarfs the epilogue).
+template <int BN, int TM>
 struct GemmCfg {
+  static_assert(TM == 128 || (TM == 256 && BN == 256), "tile shape");
+  static constexpr int A_BYTES_T = TM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int STAGE_BYTES = A_BYTES_T + B_BYTES;
+  static constexpr int STAGES = TM == 256 ? 3 : (BN == 256 ? 4 : 6);
+  static constexpr int NBUF = TM == 256 ? 1 : 2;   // accumulators in flight
+  static constexpr uint32_t TMEM_COLS = TM == 256 ? 512 : 2 * BN;
 };
 
-template <int BN>
+template <int BN, int TM>
 struct alignas(1024) GemmSmem {
-  uint8_t stage[GemmCfg<BN>::STAGES][GemmCfg<BN>::STAGE_BYTES];
-  uint64_t full[GemmCfg<BN>::STAGES];
-  uint64_t empty[GemmCfg<BN>::STAGES];
+  uint8_t stage[GemmCfg<BN, TM>::STAGES][GemmCfg<BN, TM>::STAGE_BYTES];
+  uint64_t full[GemmCfg<BN, TM>::STAGES];
+  uint64_t empty[GemmCfg<BN, TM>::STAGES];
+  float4 stg[kEpiWarps][256];   // per epilogue warp: a staged 32 x 32 fp32 block
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_base;
@@ -82,6 +101,7 @@ struct GemmGroup {
   int beta;
   int rowmap_H;
   int perm[4];
+  int vec;                    // C 16-byte aligned and ldc a multiple of 16 bytes
 };
 
 struct GemmMaps {
@@ -96,7 +116,7 @@ struct TcGemmParams {
   DevArea* dev;
   uint64_t timeout_ns;
   int splits;                 // S >= 1
-  float* ws;                  // S > 1: one BM x BN fp32 partial per tile
+  float* ws;                  // S > 1: one TM x BN fp32 partial per tile
   unsigned int* flags;        // S > 1: per tile, epilogue-warp releases (zeroed before the launch)
 };
 
@@ -120,56 +140,96 @@ __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* ma
   }
 }
 
-// 32 consecutive columns n0 .. n0+31 of one output row.  bias: added when
-// non-null; beta: C's previous value is added (read through L2: another SM may
-// have written it during this launch).
-__device__ __forceinline__ void store_chunk(const GemmGroup& p, int64_t row, int n0, const float (&v)[32]) {
-  const bool full = n0 + 32 <= p.N;
-  const float* bias = p.bias;
-  const int beta = p.beta;
-  if (p.c_bf16) {
-    __nv_bfloat16* C = static_cast<__nv_bfloat16*>(p.C) + row * p.ldc + n0;
-    if (full && (p.ldc % 8 == 0) && !beta) {
+// Output row of tile row m (the gate-slot remap: m -> perm[m % 4] * H + m / 4,
+// a negative slot drops the row); false when the row is not written.
+__device__ __forceinline__ bool out_row(const GemmGroup& G, int m, int64_t& row) {
+  row = m;
+  if (m >= G.M) return false;
+  if (G.rowmap_H > 0) {
+    const int pm = G.perm[m & 3];
+    if (pm < 0) return false;
+    row = static_cast<int64_t>(pm) * G.rowmap_H + (m >> 2);
+  }
+  return true;
+}
+
+// A warp's staged block (rows mb .. mb+31, columns nb .. nb+31; float4 j of
+// row r sits in slot j ^ (r % 8) of the row's 8, so that both the row-per-lane
+// writes and these reads are free of bank conflicts) written to C by row
+// segments: fp32 rows of 128 bytes, a float4 per lane, 4 rows per instruction;
+// bf16 rows of 64 bytes, 8 values per lane, 8 rows per instruction.  bias:
+// added when non-null; beta: C's previous value is added (read through L2:
+// another SM may have written it during this launch).
+__device__ __forceinline__ void store_staged(const GemmGroup& G, const float4* stg, int mb, int nb, int lane) {
+  const float* bias = G.bias;
+  if (G.c_bf16) {
+    const int jq = lane & 3;
+    const int n = nb + jq * 8;
 #pragma unroll
-      for (int j = 0; j < 32; j += 8) {
+    for (int i = 0; i < 4; ++i) {
+      const int rl = i * 8 + (lane >> 2);
+      int64_t row;
+      if (!out_row(G, mb + rl, row)) continue;
+      const float4 a = stg[rl * 8 + ((2 * jq) ^ (rl & 7))];
+      const float4 b = stg[rl * 8 + ((2 * jq + 1) ^ (rl & 7))];
+      float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      __nv_bfloat16* C = static_cast<__nv_bfloat16*>(G.C) + row * G.ldc + n;
+      if (G.vec && n + 8 <= G.N) {
+        if (bias) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] += bias[n + e];
+        }
+        if (G.beta) {
+          const uint4 o = __ldcg(reinterpret_cast<const uint4*>(C));
+          const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&o);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(oh[e]);
+            v[2 * e] += f.x; v[2 * e + 1] += f.y;
+          }
+        }
         uint4 q;
         uint32_t* w = reinterpret_cast<uint32_t*>(&q);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          float a0 = v[j + 2 * e], a1 = v[j + 2 * e + 1];
-          if (bias) { a0 += bias[n0 + j + 2 * e]; a1 += bias[n0 + j + 2 * e + 1]; }
-          __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+          __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
           w[e] = *reinterpret_cast<uint32_t*>(&h);
         }
-        *reinterpret_cast<uint4*>(C + j) = q;
-      }
-    } else {
-      for (int j = 0; j < 32 && n0 + j < p.N; ++j) {
-        float a = v[j];
-        if (bias) a += bias[n0 + j];
-        if (beta) a += __bfloat162float(__ldcg(C + j));
-        C[j] = __float2bfloat16_rn(a);
+        *reinterpret_cast<uint4*>(C) = q;
+      } else {
+        for (int e = 0; e < 8 && n + e < G.N; ++e) {
+          float x = v[e];
+          if (bias) x += bias[n + e];
+          if (G.beta) x += __bfloat162float(__ldcg(C + e));
+          C[e] = __float2bfloat16_rn(x);
+        }
       }
     }
   } else {
-    float* C = static_cast<float*>(p.C) + row * p.ldc + n0;
-    if (full && (p.ldc % 4 == 0)) {
+    const int jq = lane & 7;
+    const int n = nb + jq * 4;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        float4 q = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-        if (bias) { q.x += bias[n0 + j]; q.y += bias[n0 + j + 1]; q.z += bias[n0 + j + 2]; q.w += bias[n0 + j + 3]; }
-        if (beta) {
-          const float4 o = __ldcg(reinterpret_cast<const float4*>(C + j));
+    for (int i = 0; i < 8; ++i) {
+      const int rl = i * 4 + (lane >> 3);
+      int64_t row;
+      if (!out_row(G, mb + rl, row)) continue;
+      float4 q = stg[rl * 8 + (jq ^ (rl & 7))];
+      float* C = static_cast<float*>(G.C) + row * G.ldc + n;
+      if (G.vec && n + 4 <= G.N) {
+        if (bias) { q.x += bias[n]; q.y += bias[n + 1]; q.z += bias[n + 2]; q.w += bias[n + 3]; }
+        if (G.beta) {
+          const float4 o = __ldcg(reinterpret_cast<const float4*>(C));
           q.x += o.x; q.y += o.y; q.z += o.z; q.w += o.w;
         }
-        *reinterpret_cast<float4*>(C + j) = q;
-      }
-    } else {
-      for (int j = 0; j < 32 && n0 + j < p.N; ++j) {
-        float a = v[j];
-        if (bias) a += bias[n0 + j];
-        if (beta) a += __ldcg(C + j);
-        C[j] = a;
+        *reinterpret_cast<float4*>(C) = q;
+      } else {
+        const float v[4] = {q.x, q.y, q.z, q.w};
+        for (int e = 0; e < 4 && n + e < G.N; ++e) {
+          float x = v[e];
+          if (bias) x += bias[n + e];
+          if (G.beta) x += __ldcg(C + e);
+          C[e] = x;
+        }
       }
     }
   }
@@ -184,13 +244,14 @@ __device__ __forceinline__ void decode_item(const TcGemmParams& p, int item, int
   tile = t - p.grp[g].tile0;
 }
 
-template <int BN>
+template <int BN, int TM>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ TcGemmParams p) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg<BN, TM>;
   constexpr int STAGES = Cfg::STAGES;
+  constexpr int NBUF = Cfg::NBUF;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  GemmSmem<BN>& sm = *reinterpret_cast<GemmSmem<BN>*>(
+  GemmSmem<BN, TM>& sm = *reinterpret_cast<GemmSmem<BN, TM>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.splits;
@@ -217,7 +278,7 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ Tc
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t idesc = idesc_bf16(BM, BN, !p.a_kmajor, !p.b_kmajor);
+  const uint32_t idesc = idesc_bf16(128, BN, !p.a_kmajor, !p.b_kmajor);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -226,7 +287,7 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ Tc
         int sp, g, tile, t;
         decode_item(p, item, sp, g, tile, t);
         const int nt = p.grp[g].nt;
-        const int m0 = (tile / nt) * BM, n0 = (tile % nt) * BN;
+        const int m0 = (tile / nt) * TM, n0 = (tile % nt) * BN;
         for (int kb = kb_lo(sp); kb < kb_lo(sp + 1); ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1;
@@ -236,8 +297,8 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ Tc
             goto producer_done;
           }
           mbar_arrive_expect_tx(&sm.full[s], Cfg::STAGE_BYTES);
-          load_operand<BM>(sm.stage[s], &maps.a[g], &sm.full[s], p.a_kmajor, m0, kb * BK);
-          load_operand<BN>(sm.stage[s] + A_BYTES, &maps.b[g], &sm.full[s], p.b_kmajor, n0, kb * BK);
+          load_operand<TM>(sm.stage[s], &maps.a[g], &sm.full[s], p.a_kmajor, m0, kb * BK);
+          load_operand<BN>(sm.stage[s] + Cfg::A_BYTES_T, &maps.b[g], &sm.full[s], p.b_kmajor, n0, kb * BK);
         }
       }
     producer_done:;
@@ -247,8 +308,8 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ Tc
       uint32_t it = 0, acc = 0;
       for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++acc) {
         const int sp = item / p.ntiles;
-        const int buf = acc & 1;
-        const uint32_t aph = (acc >> 1) & 1;
+        const int buf = NBUF == 2 ? static_cast<int>(acc & 1) : 0;
+        const uint32_t aph = NBUF == 2 ? (acc >> 1) & 1 : acc & 1;
         if (!mbar_wait(&sm.tempty[buf], aph ^ 1, p.timeout_ns) || *(volatile int*)&sm.abort_flag) {
           report_status(p.dev, 4u, K_GEMM_TC, acc, W_MMA);
           sm.abort_flag = 1;
@@ -269,11 +330,13 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ Tc
           }
           tc_fence_after();
           const uint32_t abase = smem_u32(sm.stage[s]);
-          const uint32_t bbase = abase + A_BYTES;
+          const uint32_t bbase = abase + Cfg::A_BYTES_T;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            mma_bf16_ss(dt, operand_desc(abase, p.a_kmajor, k), operand_desc(bbase, p.b_kmajor, k), idesc,
-                        (kb > k0 || k > 0) ? 1u : 0u);
+#pragma unroll
+            for (int h = 0; h < TM / 128; ++h)   // row half h: A rows 128 h .., TMEM columns h BN ..
+              mma_bf16_ss(dt + static_cast<uint32_t>(h * BN), operand_desc(abase + h * A_BYTES, p.a_kmajor, k),
+                          operand_desc(bbase, p.b_kmajor, k), idesc, (kb > k0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&sm.empty[s]);
         }
@@ -283,15 +346,21 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ Tc
     }
   } else {
     const int q = warp & 3;              // TMEM lane quarter of this warp
-    const int c_lo = (warp - 2) / 4 * (BN / 2), c_hi = c_lo + BN / 2;   // its half of the columns
-    const int r = q * 32 + lane;         // row within the tile
+    // TM = 128: warps 2-5 / 6-9 take the first / second half of the columns;
+    // TM = 256: warps 2-5 / 6-9 take row half 0 / 1 (TMEM columns h BN ..), all columns
+    const int hw = (warp - 2) / 4;
+    const int c_lo = TM == 256 ? 0 : hw * (BN / 2), c_hi = TM == 256 ? BN : c_lo + BN / 2;
+    const int rh = TM == 256 ? hw : 0;   // row half
+    const uint32_t tcol0 = static_cast<uint32_t>(rh * BN);
+    const int r = rh * 128 + q * 32 + lane;   // row within the tile
+    const int r_lo = r - lane;                 // the warp's first row
     uint32_t acc = 0;
     for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++acc) {
       int sp, g, tile, t;
       decode_item(p, item, sp, g, tile, t);
       const GemmGroup& G = p.grp[g];
-      const int buf = acc & 1;
-      const uint32_t aph = (acc >> 1) & 1;
+      const int buf = NBUF == 2 ? static_cast<int>(acc & 1) : 0;
+      const uint32_t aph = NBUF == 2 ? (acc >> 1) & 1 : acc & 1;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&sm.tfull[buf], aph, p.timeout_ns) && !*(volatile int*)&sm.abort_flag;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -310,45 +379,60 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ Tc
         if (!ok) break;
       }
       tc_fence_after();
-      const int m0 = (tile / G.nt) * BM, n0 = (tile % G.nt) * BN;
-      const int m = m0 + r;
-      int64_t row = m;
-      bool write = m < G.M;
-      if (write && G.rowmap_H > 0) {
-        const int pm = G.perm[m & 3];
-        if (pm < 0) write = false;
-        row = static_cast<int64_t>(pm) * G.rowmap_H + (m >> 2);
-      }
-      float* part = S > 1 ? p.ws + (static_cast<int64_t>(t) * BM + r) * BN : nullptr;
-      for (int c = c_lo; c < c_hi; c += 32) {
+      const int m0 = (tile / G.nt) * TM, n0 = (tile % G.nt) * BN;
+      // the warp's 32 x BN block of the split partial, laid out so that each
+      // store / load instruction of the warp covers 512 contiguous bytes:
+      // float4 jj of chunk c of row (lane) at ((c / 32) * 8 + jj) * 32 + lane
+      float4* part = S > 1 ? reinterpret_cast<float4*>(p.ws + (static_cast<int64_t>(t) * TM + r_lo) * BN)
+                           : nullptr;
+      float4* stg = sm.stg[warp - 2];
+      // chunks past N are never read: the last one read releases the accumulator
+      const int c_end = min(c_hi, c_lo + ((G.N - n0 - c_lo + 31) / 32) * 32);
+      bool released = false;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + tcol0;
+      for (int c = c_lo; c < c_end; c += 32) {
         float v[32];
-        tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c, v);
+        tmem_ld_32x32b_x32(tbase + c, v);
+        if (c + 32 >= c_end) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.tempty[buf]);
+          released = true;
+        }
         if (S > 1) {
+          float4* pc = part + (c / 32) * 8 * 32 + lane;
           if (sp > 0) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 o = __ldcg(reinterpret_cast<const float4*>(part + c + j));
-              v[j] = o.x + v[j]; v[j + 1] = o.y + v[j + 1]; v[j + 2] = o.z + v[j + 2]; v[j + 3] = o.w + v[j + 3];
+            for (int j = 0; j < 8; ++j) {
+              const float4 o = __ldcg(pc + j * 32);
+              v[4 * j] += o.x; v[4 * j + 1] += o.y; v[4 * j + 2] += o.z; v[4 * j + 3] += o.w;
             }
           }
           if (sp < S - 1) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              __stcg(reinterpret_cast<float4*>(part + c + j), make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]));
+            for (int j = 0; j < 8; ++j)
+              __stcg(pc + j * 32, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
             continue;
           }
         }
-        if (write && n0 + c < G.N) store_chunk(G, row, n0 + c, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          stg[lane * 8 + (j ^ (lane & 7))] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        __syncwarp();
+        store_staged(G, stg, m0 + r_lo, n0 + c, lane);
+        __syncwarp();
       }
-      tc_fence_before();
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tempty[buf]);
+      }
       if (S > 1 && sp < S - 1) {
         // this warp's share of the partial, visible at gpu scope, then released
         __threadfence();
         __syncwarp();
         if (lane == 0) red_release_gpu_add(&p.flags[t], 1u);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.tempty[buf]);
     }
   }
 
@@ -358,53 +442,65 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ Tc
   if (warp == 1) tmem_dealloc(tmem, Cfg::TMEM_COLS);
 }
 
-template <int BN>
-constexpr size_t smem_bytes() { return sizeof(GemmSmem<BN>) + 1024; }
+template <int BN, int TM>
+constexpr size_t smem_bytes() { return sizeof(GemmSmem<BN, TM>) + 1024; }
+static_assert(smem_bytes<128, 128>() <= 232448 && smem_bytes<256, 128>() <= 232448 && smem_bytes<256, 256>() <= 232448,
+              "dynamic shared memory above 227 KB");
 
-struct GemmPlan { int BN, S; };
+struct GemmPlan { int BN, S, TM; };
 
-int tiles_of(const GemmArgs* gs, int n, int bn) {
+int tiles_of(const GemmArgs* gs, int n, int bn, int tm = BM) {
   int t = 0;
-  for (int i = 0; i < n; ++i) t += ((gs[i].M + BM - 1) / BM) * ((gs[i].N + bn - 1) / bn);
+  for (int i = 0; i < n; ++i) t += ((gs[i].M + tm - 1) / tm) * ((gs[i].N + bn - 1) / bn);
   return t;
 }
 
-// Tile width and K split of a launch.  Items run in waves of num_sms.  K is
-// split (at most kMaxSplits, at least 16 K blocks of 64 per split, the
-// scratch holds one fp32 partial per tile) to the count with the fewest
-// waves x (K blocks per split + 48): each wave also pays about 48 K blocks'
-// time of pipeline fill, epilogue and split hand-over (fitted to GB300 runs
-// of the weight gradients: GRU hidden 512 x K 8192, 64 tiles, split 1 / 2 /
-// 4 / 8 = 63 / 53 / 75 / 130 us; the 2-layer bidirectional LSTM's 512 and
-// 768 tiles x K 65536, split 1 / 2 / 4 / 8 = 4.12 / 3.84 / 3.94 / 4.23 ms).
-// Equal costs keep the smaller split.  Without a split: 128 x 256 tiles,
-// unless they would leave most SMs idle; then 128-wide tiles double the tile
-// count.
+// Tile shape and K split of a launch.  Items run in waves of num_sms; costs
+// are in units of one 128 x 256 x 64 K block.
+// 128-row tiles: K is split (at most kMaxSplits, at least 16 K blocks of 64
+// per split, the scratch holds one fp32 partial per tile) to the count with
+// the fewest waves x (K blocks per split + 48): each wave also pays about 48
+// K blocks' time of pipeline fill, epilogue and split hand-over (fitted to
+// GB300 runs of the weight gradients: GRU hidden 512 x K 8192, 64 tiles,
+// split 1 / 2 / 4 / 8 = 63 / 53 / 75 / 130 us; the 2-layer bidirectional
+// LSTM's 512 and 768 tiles x K 65536, split 1 / 2 / 4 / 8 = 4.12 / 3.84 /
+// 3.94 / 4.23 ms).  Equal costs keep the smaller split.  Without a split:
+// 128 x 256 tiles, unless they would leave most SMs idle; then 128-wide tiles
+// double the tile count.
+// 256 x 256 tiles (no split) for K of 4096 and more, where their waves x
+// (1.6 x K blocks + 48) is below that: a 256-row K block does twice the work
+// of a 128-row one in 1.6 times the time (GB300, K 8192 and 65536: 1.78 vs
+// 1.42 PFLOP/s), but its epilogue does not overlap the next tile, which
+// shorter K does not amortise (K 1024 / 2048 projections: 1.10 / 1.44 ms
+// against 0.80 / 1.39 ms with 128-row tiles).
 GemmPlan plan_gemm(const GemmArgs* gs, int n, int num_sms) {
   const int t256 = tiles_of(gs, n, 256), t128 = tiles_of(gs, n, 128);
   const int nk = (gs[0].K + BK - 1) / BK;
+  auto waves = [&](int64_t items) { return (items + num_sms - 1) / num_sms; };
+  GemmPlan pl{256, 1, BM};
+  double cost = static_cast<double>(waves(t256)) * (nk + 48);
   bool fp32_out = true;
   for (int i = 0; i < n; ++i) fp32_out = fp32_out && !gs[i].c_bf16;
   if (fp32_out && gs[0].split_ws && nk >= 32) {
     const size_t need = static_cast<size_t>(t256) * BM * 256 * 4 + static_cast<size_t>(t256) * 4;
-    auto cost = [&](int S) {
-      const int64_t waves = (static_cast<int64_t>(t256) * S + num_sms - 1) / num_sms;
-      return static_cast<double>(waves) * ((nk + S - 1) / S + 48);
-    };
-    int best = 1;
-    double best_cost = cost(1);
     for (int S = 2; S <= kMaxSplits && nk / S >= 16 && need <= gs[0].split_ws_bytes; ++S) {
-      const double c = cost(S);
-      if (c < best_cost - 1e-9) { best_cost = c; best = S; }
+      const double c = static_cast<double>(waves(static_cast<int64_t>(t256) * S)) * ((nk + S - 1) / S + 48);
+      if (c < cost - 1e-9) { cost = c; pl.S = S; }
     }
-    if (best > 1) return {256, best};
   }
-  if (t256 >= num_sms) return {256, 1};
-  if (2 * t256 < num_sms && t128 > t256) return {128, 1};
-  return {256, 1};
+  if (pl.S == 1 && t256 < num_sms && 2 * t256 < num_sms && t128 > t256) {
+    pl.BN = 128;
+    cost = static_cast<double>(waves(t128)) * (nk / 2.0 + 48);
+  }
+  if (nk >= 64) {
+    const int ttall = tiles_of(gs, n, 256, 256);
+    const double c = static_cast<double>(waves(ttall)) * (1.6 * nk + 48);
+    if (c < cost) pl = {256, 1, 256};
+  }
+  return pl;
 }
 
-template <int BN>
+template <int BN, int TM>
 int launch_bn(const GemmArgs* gs, int n, int S, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns) {
   GemmMaps maps;
   TcGemmParams p;
@@ -416,7 +512,7 @@ int launch_bn(const GemmArgs* gs, int n, int S, cudaStream_t s, int num_sms, Dev
     const GemmArgs& g = gs[i];
     int rc;
     // A: rows = M; B: rows = N.
-    if (g.a_kmajor) rc = make_tmap_bf16_2d(&maps.a[i], g.A, g.K, g.M, g.lda, 64, BM);
+    if (g.a_kmajor) rc = make_tmap_bf16_2d(&maps.a[i], g.A, g.K, g.M, g.lda, 64, TM);
     else rc = make_tmap_bf16_2d(&maps.a[i], g.A, g.M, g.K, g.lda, 64, BK);
     if (rc) return rc;
     if (g.b_kmajor) rc = make_tmap_bf16_2d(&maps.b[i], g.B, g.K, g.N, g.ldb, 64, BN);
@@ -425,9 +521,10 @@ int launch_bn(const GemmArgs* gs, int n, int S, cudaStream_t s, int num_sms, Dev
     GemmGroup& G = p.grp[i];
     G.M = g.M; G.N = g.N; G.nt = (g.N + BN - 1) / BN;
     G.tile0 = tiles;
-    tiles += ((g.M + BM - 1) / BM) * G.nt;
+    tiles += ((g.M + TM - 1) / TM) * G.nt;
     G.C = g.C; G.ldc = g.ldc; G.c_bf16 = g.c_bf16;
     G.bias = g.bias; G.beta = g.beta; G.rowmap_H = g.rowmap_H;
+    G.vec = (reinterpret_cast<uintptr_t>(g.C) % 16 == 0) && ((g.ldc * (g.c_bf16 ? 2 : 4)) % 16 == 0);
     for (int k = 0; k < 4; ++k) G.perm[k] = g.perm[k];
   }
   for (int i = n; i < kMaxGroups; ++i) {
@@ -443,7 +540,7 @@ int launch_bn(const GemmArgs* gs, int n, int S, cudaStream_t s, int num_sms, Dev
   p.ws = static_cast<float*>(gs[0].split_ws);
   p.flags = nullptr;
   if (S > 1) {
-    const size_t part = static_cast<size_t>(tiles) * BM * BN * 4;
+    const size_t part = static_cast<size_t>(tiles) * TM * BN * 4;
     if (part + static_cast<size_t>(tiles) * 4 > gs[0].split_ws_bytes) return 2;
     p.flags = reinterpret_cast<unsigned int*>(static_cast<char*>(gs[0].split_ws) + part);
     if (cudaMemsetAsync(p.flags, 0, static_cast<size_t>(tiles) * 4, s) != cudaSuccess) return 3;
@@ -455,14 +552,14 @@ int launch_bn(const GemmArgs* gs, int n, int S, cudaStream_t s, int num_sms, Dev
   if (cudaGetDevice(&cur) != cudaSuccess) return 3;
   const uint64_t bit = cur < 64 ? (1ull << cur) : 0ull;
   if (!bit || !(attr_set.load(std::memory_order_acquire) & bit)) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<BN>())) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_tc_kernel<BN, TM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<BN, TM>())) != cudaSuccess)
       return 3;
     attr_set.fetch_or(bit, std::memory_order_release);
   }
   const int items = tiles * S;
   const int grid = items < num_sms ? items : num_sms;
-  gemm_tc_kernel<BN><<<grid, kThreads, smem_bytes<BN>(), s>>>(maps, p);
+  gemm_tc_kernel<BN, TM><<<grid, kThreads, smem_bytes<BN, TM>(), s>>>(maps, p);
   if (cudaGetLastError() != cudaSuccess) return 3;
   return 0;
 }
@@ -477,8 +574,12 @@ bool gemm_tc_supported(const GemmArgs& g) {
 }
 
 size_t gemm_tc_split_scratch_bytes(int M, int N) {
-  const size_t tiles = static_cast<size_t>((M + BM - 1) / BM) * ((N + 127) / 128);
-  return tiles * BM * 128 * 4 + tiles * 4 + 4096;
+  // the larger of the 128 x 128 and the 256 x 256 tilings (one fp32 partial
+  // and one counter per tile)
+  const size_t t128 = static_cast<size_t>((M + 127) / 128) * ((N + 127) / 128);
+  const size_t t256 = static_cast<size_t>((M + 255) / 256) * ((N + 255) / 256);
+  const size_t a = t128 * 128 * 128 * 4 + t128 * 4, b = t256 * 256 * 256 * 4 + t256 * 4;
+  return (a > b ? a : b) + 4096;
 }
 
 int launch_gemm_tc_grouped(const GemmArgs* gs, int n, cudaStream_t s, int num_sms, DevArea* dev,
@@ -489,18 +590,22 @@ int launch_gemm_tc_grouped(const GemmArgs* gs, int n, cudaStream_t s, int num_sm
     if (gs[i].K != gs[0].K || gs[i].a_kmajor != gs[0].a_kmajor || gs[i].b_kmajor != gs[0].b_kmajor) return 2;
   }
   GemmPlan pl = plan_gemm(gs, n, num_sms);
-  // test hooks: a forced tile width (no K split), a forced K split
+  // test hooks: a forced tile width (128-row tiles, no K split), a forced K
+  // split, forced tile rows (256 rows: 256-wide tiles)
   const PlanOverrides ov = plan_overrides();
-  if (ov.gemm_bn == 128 || ov.gemm_bn == 256) pl = {ov.gemm_bn, 1};
+  if (ov.gemm_bn == 128 || ov.gemm_bn == 256) pl = {ov.gemm_bn, 1, BM};
   if (ov.gemm_splits >= 1) {
     bool fp32_out = gs[0].split_ws != nullptr;
     for (int i = 0; i < n; ++i) fp32_out = fp32_out && !gs[i].c_bf16;
     const int nk = (gs[0].K + BK - 1) / BK;
     if (ov.gemm_splits == 1) pl.S = 1;
-    else if (fp32_out && nk / ov.gemm_splits >= 16) pl = {256, ov.gemm_splits};
+    else if (fp32_out && nk / ov.gemm_splits >= 16) pl = {256, ov.gemm_splits, pl.TM};
   }
-  return pl.BN == 256 ? launch_bn<256>(gs, n, pl.S, s, num_sms, dev, timeout_ns)
-                      : launch_bn<128>(gs, n, pl.S, s, num_sms, dev, timeout_ns);
+  if (ov.gemm_tm == 128) pl.TM = 128;
+  if (ov.gemm_tm == 256 && ov.gemm_bn != 128) { pl.TM = 256; pl.BN = 256; }
+  if (pl.TM == 256) return launch_bn<256, 256>(gs, n, pl.S, s, num_sms, dev, timeout_ns);
+  return pl.BN == 256 ? launch_bn<256, 128>(gs, n, pl.S, s, num_sms, dev, timeout_ns)
+                      : launch_bn<128, 128>(gs, n, pl.S, s, num_sms, dev, timeout_ns);
 }
 
 int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns,

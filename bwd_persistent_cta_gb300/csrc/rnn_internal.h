@@ -199,7 +199,7 @@ int launch_recompute_cells(const void* gates, const void* c0, float* C, int T, i
 // planner's choice): K-split caps and batch parts of the tensor-core
 // persistent kernels, the tensor-core GEMM's tile width and K split.
 struct PlanOverrides {
-  int max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn, gemm_splits;
+  int max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn, gemm_splits, gemm_tm;
 };
 PlanOverrides plan_overrides();
 

@@ -66,14 +66,17 @@ rnn_status_t rnn_debug_skip_arrival(rnn_handle_t handle, int cta);
  *   gemm_bn                 128 or 256: force the tensor-core GEMM's tile
  *                           width (no K split);
  *   gemm_splits             1..16: force the K split of a tensor-core GEMM
- *                           with fp32 output and split scratch (128 x 256
+ *                           with fp32 output and split scratch (256-wide
  *                           tiles), where it has at least 16 K blocks of 64
- *                           per split.
+ *                           per split;
+ *   gemm_tm                 128 or 256: force the tensor-core GEMM's tile
+ *                           rows (256 rows go with 256-wide tiles, so 256
+ *                           together with gemm_bn 128 is rejected).
  * Other values are RNN_BAD_PARAM and change nothing.  Plans are cached per
  * shape and per override set; set the overrides while no call of the library
  * runs on another thread. */
 rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn,
-                                          int gemm_splits);
+                                          int gemm_splits, int gemm_tm);
 
 #ifdef __cplusplus
 }
