@@ -20,8 +20,12 @@
 //                lanes 32*(w%4) .. +31 = tile rows; with 128-row tiles warps
 //                2-5 take the first half of the tile's columns and warps 6-9
 //                the second, with 256-row tiles they take the two row halves),
-//                32 x 32 blocks staged in shared memory and written by row
-//                segments (bias / accumulate / cast, gate-slot row remap)
+//                blocks staged in shared memory and written by whole 128-byte
+//                row segments (bias / accumulate / cast, gate-slot row remap):
+//                32 x 32 fp32, or 32 x 64 already rounded for bf16 output
+//                without accumulate (GB300: 64-byte half-line segments wrote
+//                bf16 at 2.0 TB/s, whole lines at 3.1 TB/s; a plain fill
+//                reaches 4.0)
 // With 128-row tiles two TMEM accumulators (2 x BN columns) let the epilogue
 // of one tile overlap the main loop of the next; a 256 x 256 tile fills the
 // 512 columns, so its epilogue releases the accumulator after its last
@@ -102,6 +106,7 @@ struct GemmGroup {
   int rowmap_H;
   int perm[4];
   int vec;                    // C 16-byte aligned and ldc a multiple of 16 bytes
+  int bias_vec;               // bias 16-byte aligned
 };
 
 struct GemmMaps {
@@ -142,6 +147,11 @@ __device__ __forceinline__ void load_operand(uint8_t* dst, const CUtensorMap* ma
 
 // Output row of tile row m (the gate-slot remap: m -> perm[m % 4] * H + m / 4,
 // a negative slot drops the row); false when the row is not written.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 __device__ __forceinline__ bool out_row(const GemmGroup& G, int m, int64_t& row) {
   row = m;
   if (m >= G.M) return false;
@@ -390,7 +400,67 @@ gemm_tc_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ Tc
       const int c_end = min(c_hi, c_lo + ((G.N - n0 - c_lo + 31) / 32) * 32);
       bool released = false;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + tcol0;
-      for (int c = c_lo; c < c_end; c += 32) {
+      // bf16 output without accumulate: 64 columns per chunk, rounded to bf16
+      // before staging, so that every row segment written is a whole 128-byte line
+      const bool wide = G.c_bf16 && !G.beta && S == 1;
+      const int c_end64 = wide ? min(c_hi, c_lo + ((G.N - n0 - c_lo + 63) / 64) * 64) : c_lo;
+      for (int c = c_lo; c < c_end64; c += 64) {
+        float v[32], w[32];
+        tmem_ld_32x32b_x32(tbase + c, v);
+        tmem_ld_32x32b_x32(tbase + c + 32, w);
+        if (c + 64 >= c_end64) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.tempty[buf]);
+          released = true;
+        }
+        const float* bias = G.bias;
+        uint4* sb = reinterpret_cast<uint4*>(stg);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float e[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) e[i] = j < 4 ? v[8 * j + i] : w[8 * (j - 4) + i];
+          if (bias) {
+            const int nb = n0 + c + 8 * j;
+            if (G.bias_vec && nb + 8 <= G.N) {
+              // the same 32 bytes for every lane: broadcast loads
+              const float4 b0 = __ldg(reinterpret_cast<const float4*>(bias + nb));
+              const float4 b1 = __ldg(reinterpret_cast<const float4*>(bias + nb + 4));
+              e[0] += b0.x; e[1] += b0.y; e[2] += b0.z; e[3] += b0.w;
+              e[4] += b1.x; e[5] += b1.y; e[6] += b1.z; e[7] += b1.w;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) e[i] += nb + i < G.N ? bias[nb + i] : 0.f;
+            }
+          }
+          uint4 qv;
+          qv.x = pack_bf16(e[0], e[1]); qv.y = pack_bf16(e[2], e[3]);
+          qv.z = pack_bf16(e[4], e[5]); qv.w = pack_bf16(e[6], e[7]);
+          sb[lane * 8 + (j ^ (lane & 7))] = qv;
+        }
+        __syncwarp();
+        {
+          const int jq = lane & 7;
+          const int n = n0 + c + jq * 8;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rl = i * 4 + (lane >> 3);
+            int64_t row;
+            if (!out_row(G, m0 + r_lo + rl, row)) continue;
+            const uint4 qv = sb[rl * 8 + (jq ^ (rl & 7))];
+            __nv_bfloat16* C = static_cast<__nv_bfloat16*>(G.C) + row * G.ldc + n;
+            if (G.vec && n + 8 <= G.N) {
+              *reinterpret_cast<uint4*>(C) = qv;
+            } else {
+              const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&qv);
+              for (int e2 = 0; e2 < 8 && n + e2 < G.N; ++e2) C[e2] = h[e2];
+            }
+          }
+        }
+        __syncwarp();
+      }
+      for (int c = wide ? c_end : c_lo; c < c_end; c += 32) {
         float v[32];
         tmem_ld_32x32b_x32(tbase + c, v);
         if (c + 32 >= c_end) {
@@ -469,10 +539,11 @@ int tiles_of(const GemmArgs* gs, int n, int bn, int tm = BM) {
 // double the tile count.
 // 256 x 256 tiles (no split) for K of 4096 and more, where their waves x
 // (1.6 x K blocks + 48) is below that: a 256-row K block does twice the work
-// of a 128-row one in 1.6 times the time (GB300, K 8192 and 65536: 1.78 vs
-// 1.42 PFLOP/s), but its epilogue does not overlap the next tile, which
-// shorter K does not amortise (K 1024 / 2048 projections: 1.10 / 1.44 ms
-// against 0.80 / 1.39 ms with 128-row tiles).
+// of a 128-row one in 1.6 times the time (GB300, K 65536 weight gradients:
+// 1.81 vs 1.42 PFLOP/s), but its epilogue does not overlap the next tile,
+// which shorter K does not amortise (GB300, bf16 output with bias, 65536 x
+// 8192: K 1024 1.05 ms against 0.77 ms with 128-row tiles, K 2048 1.55
+// against 1.37 ms).
 GemmPlan plan_gemm(const GemmArgs* gs, int n, int num_sms) {
   const int t256 = tiles_of(gs, n, 256), t128 = tiles_of(gs, n, 128);
   const int nk = (gs[0].K + BK - 1) / BK;
@@ -525,6 +596,7 @@ int launch_bn(const GemmArgs* gs, int n, int S, cudaStream_t s, int num_sms, Dev
     G.C = g.C; G.ldc = g.ldc; G.c_bf16 = g.c_bf16;
     G.bias = g.bias; G.beta = g.beta; G.rowmap_H = g.rowmap_H;
     G.vec = (reinterpret_cast<uintptr_t>(g.C) % 16 == 0) && ((g.ldc * (g.c_bf16 ? 2 : 4)) % 16 == 0);
+    G.bias_vec = reinterpret_cast<uintptr_t>(g.bias) % 16 == 0;
     for (int k = 0; k < 4; ++k) G.perm[k] = g.perm[k];
   }
   for (int i = n; i < kMaxGroups; ++i) {

@@ -156,3 +156,14 @@ def test_gemm_tall_tiles_split_k(plan_overrides, splits):
     plan_overrides(gemm_tm=256, gemm_splits=splits)
     _case(12800, 768, 3072, 1, 1, 1, seed=43 + splits)
     _case(512, 512, 8192, 0, 0, 1, bias=True, beta=True, rowmap=[1, -1, 0, 2], seed=47)
+
+
+@pytest.mark.parametrize("tm", [128, 256])
+@pytest.mark.parametrize("M,N,K", [(300, 200, 128), (260, 196, 96), (384, 520, 4096)])
+def test_gemm_bf16_output_ragged_rows(plan_overrides, tm, M, N, K):
+    # bf16 output without accumulate (whole 128-byte row segments, a scalar
+    # tail where N ends inside a segment or rows are not 16-byte aligned)
+    plan_overrides(gemm_tm=tm)
+    _case(M, N, K, 1, 1, 1, bias=True, c_bf16=True, seed=M + N)
+    # MN-major A where its rows stay 16-byte aligned (M a multiple of 8)
+    _case(M, N, K, int(M % 8 != 0), 1, 1, c_bf16=True, rowmap=[1, 3, -1, 0], seed=M + N + 1)
