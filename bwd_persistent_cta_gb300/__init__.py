@@ -58,7 +58,7 @@ _SIGS = {
     "rnn_selected_algo": (ctypes.c_int, [_P]),
     "rnn_selected_fwd_algo": (ctypes.c_int, [_P]),
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
-    "rnn_debug_set_plan_overrides": (ctypes.c_int, [ctypes.c_int] * 7),
+    "rnn_debug_set_plan_overrides": (ctypes.c_int, [ctypes.c_int] * 8),
     "rnn_debug_tc_plans": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "rnn_debug_simt_plan": (ctypes.c_int, [ctypes.c_int] * 9 + [ctypes.POINTER(ctypes.c_int)]),
@@ -253,9 +253,10 @@ def rnn_debug_skip_arrival(handle, cta: int) -> int:
 
 
 def rnn_debug_set_plan_overrides(max_ks_fwd: int = 0, max_ks_bwd: int = 0, nb_fwd: int = 0, nb_bwd: int = 0,
-                                 gemm_bn: int = 0, gemm_splits: int = 0, gemm_tm: int = 0) -> int:
+                                 gemm_bn: int = 0, gemm_splits: int = 0, gemm_tm: int = 0,
+                                 bwd_global_ks: int = 0) -> int:
     return lib().rnn_debug_set_plan_overrides(int(max_ks_fwd), int(max_ks_bwd), int(nb_fwd), int(nb_bwd),
-                                              int(gemm_bn), int(gemm_splits), int(gemm_tm))
+                                              int(gemm_bn), int(gemm_splits), int(gemm_tm), int(bwd_global_ks))
 
 
 def rnn_debug_gemm(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, C, ldc, c_bf16, bias, beta, rowmap_H, perm,

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include <cstddef>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -121,6 +122,15 @@ void fill_layout(rnn_handle_s* h) {
   h->w_y1 = w.take(static_cast<size_t>(T + 2) * B * D * H * es);
   h->w_rh = h->rb ? w.take(static_cast<size_t>(D) * TB * H * es) : 0;
   h->w_g = 0;
+  // the backward's K-split partials where its plan runs without clusters
+  // (both directions in one launch, or one at a time)
+  h->gk_bytes = 0;
+  if (h->algo == RNN_ALGO_PERSIST_TC) {
+    const size_t a = persist_tc_bwd_gk_bytes(h->desc.mode, h->ra, H, B, D, h->num_sms);
+    const size_t b = D > 1 ? persist_tc_bwd_gk_bytes(h->desc.mode, h->ra, H, B, 1, h->num_sms) : 0;
+    h->gk_bytes = a > b ? a : b;
+  }
+  h->w_gk = h->gk_bytes ? w.take(h->gk_bytes) : 0;
   h->workspace_bytes = w.off;
 }
 
@@ -217,10 +227,8 @@ int run_gemm(rnn_handle_s* h, GemmArgs g, cudaStream_t s, int cls) {
 }
 
 int reset_counters(rnn_handle_s* h, cudaStream_t s) {
-  return cudaMemsetAsync(h->dev->counters, 0, sizeof(h->dev->counters) + sizeof(h->dev->slice_ctr), s) ==
-                 cudaSuccess
-             ? 0
-             : 3;
+  // counters, slice counters, the global-K-split counters and abort flag
+  return cudaMemsetAsync(h->dev->counters, 0, offsetof(DevArea, status), s) == cudaSuccess ? 0 : 3;
 }
 
 // One persistent launch per layer (both directions), or one per direction
@@ -382,7 +390,7 @@ struct DeviceGuard {
 namespace rnn {
 namespace {
 std::mutex g_override_mu;
-PlanOverrides g_override{0, 0, 0, 0, 0, 0, 0};
+PlanOverrides g_override{0, 0, 0, 0, 0, 0, 0, 0};
 }  // namespace
 PlanOverrides plan_overrides() {
   std::lock_guard<std::mutex> lock(g_override_mu);
@@ -540,15 +548,16 @@ int rnn_selected_fwd_algo(rnn_handle_t h) {
 }
 
 rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn,
-                                          int gemm_splits, int gemm_tm) {
+                                          int gemm_splits, int gemm_tm, int bwd_global_ks) {
   auto ks_ok = [](int v) { return v >= 0 && v <= 16; };
   auto nb_ok = [](int v) { return v == 0 || v == 1 || v == 2 || v == 4; };
   if (!ks_ok(max_ks_fwd) || !ks_ok(max_ks_bwd) || !nb_ok(nb_fwd) || !nb_ok(nb_bwd) ||
       !(gemm_bn == 0 || gemm_bn == 128 || gemm_bn == 256) || !ks_ok(gemm_splits) ||
-      !(gemm_tm == 0 || gemm_tm == 128 || gemm_tm == 256) || (gemm_tm == 256 && gemm_bn == 128))
+      !(gemm_tm == 0 || gemm_tm == 128 || gemm_tm == 256) || (gemm_tm == 256 && gemm_bn == 128) ||
+      !(bwd_global_ks == 0 || bwd_global_ks == 1))
     return RNN_BAD_PARAM;
   std::lock_guard<std::mutex> lock(rnn::g_override_mu);
-  rnn::g_override = {max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn, gemm_splits, gemm_tm};
+  rnn::g_override = {max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn, gemm_splits, gemm_tm, bwd_global_ks};
   return RNN_OK;
 }
 
@@ -746,6 +755,7 @@ rnn_status_t rnn_backward_data(rnn_handle_t h, const void* y, const void* dy, co
       for (int k = 0; k < 4; ++k) a.whh_map[k] = sr[k];
       a.RH = h->rb ? at<char>(reserve, h->r_rh[l]) : nullptr;
     }
+    a.gk_buf = h->gk_bytes ? at<float>(workspace, h->w_gk) : nullptr;
     RNN_TRY(run_persist(h, a, true, s));
     // input gradient dX = dG * W_ih (both directions summed through K)
     GemmArgs g;

@@ -44,6 +44,7 @@ struct rnn_handle_s {
   size_t reserve_bytes;
   // workspace offsets (bytes)
   size_t w_p, w_xin, w_dyi, w_dx0, w_wx, w_wxt, w_wr, w_wrt, w_bx, w_bh, w_y0, w_y1, w_rh, w_g;
+  size_t w_gk, gk_bytes;       // tensor-core backward: K-split partials through global memory (0: none)
   size_t workspace_bytes;
 };
 

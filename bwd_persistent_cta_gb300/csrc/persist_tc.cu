@@ -27,6 +27,7 @@ struct TcPlan {
   uint32_t wcol = 0;   // first TMEM column of the weight sub-tiles (w_tmem > 0)
   uint32_t off_stage = 0;   // forward K split: warp 0's post-step stage (0: none)
   size_t smem = 0;
+  int gk = 0;               // backward: K-split partials through global memory, no clusters
 };
 
 size_t a1k(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
@@ -51,13 +52,21 @@ size_t a1k(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 // batch part, 9.2 us per step (both directions); backward, K split 4 x 4 batch
 // parts, 7.3 us per direction; LSTM B32 H1024 forward 4 x 1, 4.4 us; backward
 // 8 x 1, 5.3 us.
-double plan_cost(int bwd, int KS, int Kc, int Npad, int pairs) {
+// A K split exchanged through global memory instead (gk) is estimated at
+// 0.3 us + 30 ns per KB to write the partials, a counter round trip of about
+// 1.5 us, and 0.3 us + 30 ns per KB to read the owned rows back.
+double plan_cost(int bwd, int KS, int Kc, int Npad, int pairs, int gk = 0) {
   const double n_mma = Kc / 16;
   const double mma = (0.040 + 0.00007 * Npad) * n_mma;
   const double tma = 0.3 + 0.004 * (static_cast<double>(Kc) * Npad * 2 / 1024.0);
   const double push_kb = 128.0 * Npad * 4 * (KS - 1) / KS / 1024.0;
-  const double push = KS > 1 ? 0.2 + push_kb * (KS >= 16 ? 0.051 : 0.035) : 0.1;
-  const double cl = KS >= 16 ? 1.6 : KS > 1 ? 0.62 : 0.05;
+  double push = KS > 1 ? 0.2 + push_kb * (KS >= 16 ? 0.051 : 0.035) : 0.1;
+  double cl = KS >= 16 ? 1.6 : KS > 1 ? 0.62 : 0.05;
+  if (gk && KS > 1) {
+    const double kb = 128.0 * Npad * 4 / 1024.0;
+    push = 0.6 + 0.06 * kb;
+    cl = 1.5;
+  }
   const double per_thread = (pairs + kThreads - 1) / kThreads;
   const double epi = bwd ? 0.14 + 0.14 * per_thread : 0.09 + 0.15 * per_thread;
   const double post = bwd ? 0.0 : 0.15 * per_thread;
@@ -67,8 +76,11 @@ double plan_cost(int bwd, int KS, int Kc, int Npad, int pairs) {
 // Candidate plans for one launch (K split x batch parts), cheapest first by
 // plan_cost.  Whether their clusters can all be resident at once is checked
 // at launch.
-int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int max_out) {
+// gk: backward plans whose K split is exchanged through global memory (no
+// clusters; at most 64 row-group counters over directions and batch parts).
+int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* out, int max_out, int gk = 0) {
   (void)mode;
+  if (gk && !bwd) return 0;
   if (B < 1 || B > 256 * kMaxBatchParts) return 0;
   const int K = bwd ? 4 * H : H;
   const int nrg = bwd ? H / 128 : (4 * H) / 128;
@@ -97,6 +109,7 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
       const int PP = pp_for(UPC * Bp);
       if (PP == 0) continue;
       if (nrg * KS * NB * ndir > num_sms) continue;
+      if (gk && (KS == 1 || ndir * NB * nrg > 64)) continue;
       const size_t wbytes = static_cast<size_t>(nsub) * kWSub;
       const size_t rb = static_cast<size_t>(Npad) * 128;
       const size_t recv = static_cast<size_t>(Npad) * 128 * 4;
@@ -155,7 +168,8 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
       const size_t floor = wt ? kOneCtaSmem : kMinSmem;
       p.smem = smem < floor ? floor : smem;
       p.wcol = wt ? 512u - 32u * static_cast<uint32_t>(wt) : 0u;
-      cands.emplace_back(plan_cost(bwd, KS, Kc, Npad, UPC * Bp), p);
+      p.gk = gk;
+      cands.emplace_back(plan_cost(bwd, KS, Kc, Npad, UPC * Bp, gk), p);
     }
   }
   std::stable_sort(cands.begin(), cands.end(),
@@ -181,7 +195,7 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPla
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = pl.KS;
+  attr[0].val.clusterDim.x = pl.gk ? 1 : pl.KS;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -194,8 +208,8 @@ void fill_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, const TcPla
 // of microseconds of host time, which the GPU would otherwise wait for at the
 // start of every persistent launch.
 struct PlanKey {
-  int v[12];
-  bool operator<(const PlanKey& o) const { return std::lexicographical_compare(v, v + 12, o.v, o.v + 12); }
+  int v[13];
+  bool operator<(const PlanKey& o) const { return std::lexicographical_compare(v, v + 13, o.v, o.v + 13); }
 };
 
 std::mutex g_plan_mu;
@@ -224,17 +238,18 @@ void trace_plan(int bwd, int H, int B, int ndir, int ext, const TcPlan* p) {
     return;
   }
   std::fprintf(stderr,
-               "[rnn] tensor-core %s H=%d B=%d dirs=%d%s: K split %d, %d batch part(s) of %d rows, %d CTAs, "
+               "[rnn] tensor-core %s H=%d B=%d dirs=%d%s: K split %d%s, %d batch part(s) of %d rows, %d CTAs, "
                "%d pair(s) per thread, %d weight sub-tiles in tensor memory, %zu B shared memory\n",
-               pass, H, B, ndir, ext ? " (extended)" : "", p->KS, p->NB, p->Bp, p->nrg * p->KS * p->NB * ndir, p->PP,
-               p->w_tmem, p->smem);
+               pass, H, B, ndir, ext ? " (extended)" : "", p->KS, p->gk ? " (through global memory)" : "", p->NB,
+               p->Bp, p->nrg * p->KS * p->NB * ndir, p->PP, p->w_tmem, p->smem);
 }
 
 bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext, TcPlan* chosen) {
   int dev = 0;
   cudaGetDevice(&dev);
   const PlanOverrides ov = plan_overrides();
-  const PlanKey key{{mode, bwd, H, B, ndir, num_sms, ext, dev, ov.max_ks_fwd, ov.max_ks_bwd, ov.nb_fwd, ov.nb_bwd}};
+  const PlanKey key{{mode, bwd, H, B, ndir, num_sms, ext, dev, ov.max_ks_fwd, ov.max_ks_bwd, ov.nb_fwd, ov.nb_bwd,
+                     ov.bwd_global_ks}};
   std::lock_guard<std::mutex> lock(g_plan_mu);
   const auto hit = g_plans.find(key);
   if (hit != g_plans.end()) {
@@ -242,7 +257,8 @@ bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext
     return hit->second.first;
   }
   TcPlan plans[12];
-  const int n = make_plans(mode, bwd, H, B, ndir, num_sms, plans, 12);
+  // test hook: the backward's K split through global memory only
+  const int n = bwd && ov.bwd_global_ks ? 0 : make_plans(mode, bwd, H, B, ndir, num_sms, plans, 12);
   for (int i = 0; i < n; ++i) {
     const TcPlan& pl = plans[i];
     const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
@@ -266,6 +282,25 @@ bool choose_plan(int mode, int bwd, int H, int B, int ndir, int num_sms, int ext
       return true;
     }
   }
+  // no cluster plan can be resident: the backward's K split through global
+  // memory, every CTA of the grid resident at once (one per SM)
+  const int ng = bwd ? make_plans(mode, bwd, H, B, ndir, num_sms, plans, 12, 1) : 0;
+  for (int i = 0; i < ng; ++i) {
+    const TcPlan& pl = plans[i];
+    const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
+    if (!raise_smem_limit(fn, dev, static_cast<int>(pl.smem))) continue;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, pl.smem) != cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    if (per_sm >= 1 && pl.nrg * pl.KS * pl.NB * ndir <= num_sms) {
+      *chosen = pl;
+      g_plans[key] = {true, pl};
+      trace_plan(bwd, H, B, ndir, ext, &pl);
+      return true;
+    }
+  }
   g_plans[key] = {false, TcPlan()};
   trace_plan(bwd, H, B, ndir, ext, nullptr);
   return false;
@@ -279,6 +314,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   if (rb && (bwd ? a.XA == nullptr : a.RH == nullptr)) return 2;
   const int ext = (a.len != nullptr || a.clip || rb) ? 1 : 0;
   if (!choose_plan(a.mode, bwd, a.H, a.B, a.ndir, num_sms, ext, &pl)) return 2;
+  if (pl.gk && !a.gk_buf) return 2;
   const int H = a.H, D = a.D;
   CUtensorMap tmW, tmX, tmX4;
   int rc;
@@ -356,6 +392,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   const uint64_t proj_bytes = static_cast<uint64_t>(a.T) * a.B * D * 4 * H * 2;
   P.prefetch = !bwd && proj_bytes > (32ull << 20);
   P.wcol = pl.wcol;
+  P.gk = pl.gk;
   const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
@@ -379,6 +416,20 @@ bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int
   if (!choose_plan(mode, 0, H, B, ndir, num_sms, ext, &f) || !choose_plan(mode, 1, H, B, ndir, num_sms, ext, &b))
     return false;
   return !rb || (f.R >= f.nsub && b.R >= b.nsub);
+}
+
+size_t persist_tc_bwd_gk_bytes(int mode, int reset_after, int H, int B, int ndir, int num_sms) {
+  if (!(mode == 0 || mode == 1)) return 0;
+  size_t most = 0;
+  for (int ext = 0; ext <= 1; ++ext) {
+    TcPlan b;
+    if (!choose_plan(mode, 1, H, B, ndir, num_sms, ext, &b) || !b.gk) continue;
+    // two exchange parities x row groups x KS sources x Npad columns x 128 rows
+    const size_t bytes = static_cast<size_t>(2) * ndir * b.NB * b.nrg * b.KS * b.Npad * 128 * 4;
+    most = std::max(most, bytes);
+  }
+  (void)reset_after;
+  return most;
 }
 
 bool persist_tc_fwd_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms) {

@@ -113,6 +113,7 @@ struct TcPersistParams {
   uint32_t tmem_cols;
   uint32_t off_ring, off_recv, off_bar;
   uint32_t off_stage;      // forward with a K split: warp 0's post-step stage, 0 = none
+  int gk;                  // backward: the K-split partials go through global memory (a.gk_buf), no cluster
 };
 
 struct TcBars {
@@ -283,6 +284,34 @@ __device__ __forceinline__ void push_partials(const TcPersistParams& P, uint32_t
   }
 }
 
+// The K split of a row group exchanged through global memory instead of
+// distributed shared memory (a grid without clusters: shapes whose clusters
+// cannot all be resident).  ctr: the group's arrival counter; buf: its
+// partials, two exchange parities of [owner][source][column][row in owner],
+// so an owner's rows from every source are one contiguous block laid out as
+// the receive buffer.
+struct GkGroup {
+  unsigned int* ctr = nullptr;
+  float* buf = nullptr;
+};
+
+// TMEM accumulator rows -> the group's partials in global memory (plain
+// stores; published by the caller's fence and release).
+__device__ __forceinline__ void push_partials_global(const TcPersistParams& P, uint32_t tmem, float* buf, int ks) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3, half = warp >> 2;
+  const int row = q * 32 + lane;
+  const int owner = row / P.RPC, lr = row - owner * P.RPC;
+  float* dst = buf + (static_cast<size_t>(owner) * P.KS + ks) * P.Npad * P.RPC + lr;
+  for (int c = half * 32; c < P.Npad; c += 64) {
+    float v[32];
+    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (c + j < P.Npad) dst[(c + j) * P.RPC] = v[j];
+  }
+}
+
 // The per-step exchange and contraction, up to the point where this CTA's
 // units' summed pre-activations can be read from ``recv``.  Returns true when
 // the whole cluster may continue.
@@ -299,7 +328,7 @@ __device__ __forceinline__ bool step_exchange(const TcPersistParams& P, const CU
                               int y4, int c2, int dir, uint32_t idesc,
                               uint64_t adesc0, bool do_contract, unsigned int* ctr_in, unsigned int wait_target, int s,
                               int ks, int& n_mma, bool& w_waited, unsigned int kernel,
-                              const Deferred& deferred = Deferred()) {
+                              const Deferred& deferred = Deferred(), const GkGroup& gk = GkGroup()) {
   const PersistArgs& a = P.a;
   const int tk = kernel == K_BWD_TC ? 1 : 0;
   (void)tk;
@@ -336,10 +365,42 @@ __device__ __forceinline__ bool step_exchange(const TcPersistParams& P, const CU
     ok = __syncthreads_and(done ? 1 : 0);
     if (ok) {
       tc_fence_after();
-      push_partials(P, tmem, recv, ks);
+      if (P.gk) push_partials_global(P, tmem, gk.buf + static_cast<size_t>(s & 1) * P.KS * P.Npad * 128, ks);
+      else push_partials(P, tmem, recv, ks);
     }
   }
   RNN_TRACE_AT(9, tk, s);
+  if (P.gk) {
+    // publish the partials (or this CTA's failure), then wait for the KS CTAs
+    // of the row group: exchange s completes at s + 1 arrivals each
+    const float* pbuf = gk.buf + static_cast<size_t>(s & 1) * P.KS * P.Npad * 128;
+    __threadfence();
+    tc_fence_before();
+    const int all_ok = __syncthreads_and(ok);
+    int pass = 1;
+    if (threadIdx.x == 0) {
+      if (!all_ok) atomicExch(&a.dev->gk_abort, 1u);
+      red_release_gpu_add(gk.ctr, 1u);
+      if (!wait_counter_geq(gk.ctr, static_cast<unsigned int>(s + 1) * P.KS, a.timeout_ns)) {
+        pass = 0;
+        report_status(a.dev, 4u, kernel, static_cast<unsigned>(s), W_COUNTER);
+      } else {
+        pass = all_ok && *reinterpret_cast<volatile unsigned int*>(&a.dev->gk_abort) == 0u;
+      }
+    }
+    pass = __syncthreads_and(pass);
+    tc_fence_after();
+    if (pass && do_contract) {
+      // this CTA's rows from every source, as the receive buffer lays them out
+      const float4* src = reinterpret_cast<const float4*>(pbuf + static_cast<size_t>(ks) * P.KS * P.Npad * P.RPC);
+      float4* dst = reinterpret_cast<float4*>(recv);
+      const int n4 = P.Npad * 128 / 4;
+      for (int i = threadIdx.x; i < n4; i += kThreads) dst[i] = __ldcg(src + i);
+      __syncthreads();
+    }
+    RNN_TRACE_AT(4, tk, s);
+    return pass != 0;
+  }
   if (static_cast<int>(threadIdx.x) < P.KS) *peer_ptr(&bars.flags[s & 1][ks], threadIdx.x) = ok ? 0 : 1;
   tc_fence_before();
   if (P.KS > 1) cluster_sync(); else __syncthreads();
@@ -543,7 +604,7 @@ __device__ __forceinline__ void setup(const TcPersistParams& P, const CUtensorMa
 
 __device__ __forceinline__ void teardown(const TcPersistParams& P, TcBars& bars) {
   tc_fence_before();
-  if (P.KS > 1) cluster_sync(); else __syncthreads();
+  if (P.KS > 1 && !P.gk) cluster_sync(); else __syncthreads();
   tc_fence_after();
   if ((threadIdx.x >> 5) == 0) tmem_dealloc(bars.tmem, P.tmem_cols);
 }
@@ -972,6 +1033,13 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   unsigned int* const ctr_in = slice_counter(P, nb, ks);
   unsigned int* const ctr_out = slice_counter(P, nb, (4 * ubase) / P.Kc);
   const bool skip = a.skip_cta == static_cast<int>(blockIdx.x + gridDim.x * blockIdx.y);
+  // K split through global memory: this row group's counter and partials
+  GkGroup gkg;
+  if (P.gk) {
+    const int grp = (static_cast<int>(blockIdx.y) * P.NB + nb) * P.nrg + rg;
+    gkg.ctr = &a.dev->gk_ctr[grp];
+    gkg.buf = a.gk_buf + static_cast<size_t>(grp) * 2 * KS * P.Npad * 128;
+  }
   uint32_t g = 0;
   int n_mma = 0;
   bool w_waited = false;
@@ -1019,7 +1087,8 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     }
     if (!step_exchange(P, &tmX, &tmX4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, (s > 0 ? tp : 0) * B + b0,
                        (s > 0 ? tp : 0) * B + b0, ks * P.nsub, dir, idesc, adesc0, s > 0, ctr_in,
-                       static_cast<unsigned int>(s * ph) * P.nrg, s * ph, ks, n_mma, w_waited, K_BWD_TC)) {
+                       static_cast<unsigned int>(s * ph) * P.nrg, s * ph, ks, n_mma, w_waited, K_BWD_TC,
+                       NoDeferred(), gkg)) {
       aborted = true;
       break;
     }
@@ -1154,7 +1223,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         step_arrive(ctr_out, skip, s, 1);
         if (!step_exchange(P, &tmA, &tmA4, ring, recv, bars, tmem, g, dir * K4 + ks * P.Kc, t * B + b0, t * B + b0,
                            ks * P.nsub, dir, idesc, adesc0, true, ctr_in, static_cast<unsigned int>(2 * s + 1) * P.nrg,
-                           2 * s + 1, ks, n_mma, w_waited, K_BWD_TC)) {
+                           2 * s + 1, ks, n_mma, w_waited, K_BWD_TC, NoDeferred(), gkg)) {
           aborted = true;
           break;
         }
@@ -1201,7 +1270,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     // batch rows in order, then unit V w + j adds threads w, w + TPR, ... in
     // index order.
     tc_fence_before();
-    if (KS > 1) cluster_sync(); else __syncthreads();
+    if (KS > 1 && !P.gk) cluster_sync(); else __syncthreads();
     float* red = recv;
     // this batch part's sums to plane nb of db [NB][D][4H]; with several
     // parts, part 0 then adds planes 1.. in order once every CTA of the

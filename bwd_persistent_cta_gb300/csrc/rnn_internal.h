@@ -41,9 +41,14 @@ struct DevArea {
   // tensor-core persistent kernels: per (direction, batch part, K slice), the
   // arrivals of the CTAs whose outputs form that K slice of the exchanged state
   unsigned int slice_ctr[128];
+  // tensor-core backward with its K split exchanged through global memory
+  // (no cluster): per (direction, batch part, row group) the arrivals of its
+  // KS CTAs, and a flag any of them sets when it gives up
+  unsigned int gk_ctr[64];
+  unsigned int gk_abort;
   unsigned int status;         // 0, or the first rnn_status_t a kernel reported
   unsigned int where[4];       // kernel id, block, step, wait kind of that report
-  unsigned int pad[91];        // to 1 KB
+  unsigned int pad[26];        // to 1 KB
 };
 static_assert(sizeof(DevArea) == 1024, "DevArea is 1 KB");
 
@@ -112,6 +117,9 @@ struct PersistArgs {
   // gradient is left to the GEMM of the backward-weights call
   float* dwhh = nullptr;
   int whh_map[4] = {-1, -1, -1, -1};
+  // tensor-core backward without clusters: the K-split partials of every
+  // row group, two exchange parities (persist_tc_bwd_gk_bytes)
+  float* gk_buf = nullptr;
   DevArea* dev = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int skip_cta = -1;
@@ -146,6 +154,9 @@ bool persist_tc_supported(int mode, int reset_after, int H, int B, int ndir, int
 bool persist_tc_fwd_supported(int mode, int reset_after, int H, int B, int ndir, int num_sms);
 int launch_persist_fwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms);
 int launch_persist_bwd_tc(const PersistArgs& a, cudaStream_t s, int num_sms);
+// Bytes of PersistArgs::gk_buf the tensor-core backward needs for this shape:
+// 0 when its plan exchanges the K split within clusters.
+size_t persist_tc_bwd_gk_bytes(int mode, int reset_after, int H, int B, int ndir, int num_sms);
 
 // TMA tensor map (CUtensorMap, 128 bytes) over a bf16 row-major matrix
 // ptr[j * ld + i], i < dim0, j < dim1, box box0 x box1, 128-byte swizzle.
@@ -200,6 +211,7 @@ int launch_recompute_cells(const void* gates, const void* c0, float* C, int T, i
 // persistent kernels, the tensor-core GEMM's tile width and K split.
 struct PlanOverrides {
   int max_ks_fwd, max_ks_bwd, nb_fwd, nb_bwd, gemm_bn, gemm_splits, gemm_tm;
+  int bwd_global_ks;           // 1: the tensor-core backward exchanges its K split through global memory
 };
 PlanOverrides plan_overrides();
 

@@ -71,12 +71,18 @@ rnn_status_t rnn_debug_skip_arrival(rnn_handle_t handle, int cta);
  *                           per split;
  *   gemm_tm                 128 or 256: force the tensor-core GEMM's tile
  *                           rows (256 rows go with 256-wide tiles, so 256
- *                           together with gemm_bn 128 is rejected).
+ *                           together with gemm_bn 128 is rejected);
+ *   bwd_global_ks           1: the tensor-core backward exchanges its K-split
+ *                           partials through global memory (no thread-block
+ *                           clusters), as it does by itself only where no
+ *                           cluster plan can be resident.  Takes effect for
+ *                           handles created after it is set (the workspace
+ *                           size depends on it).
  * Other values are RNN_BAD_PARAM and change nothing.  Plans are cached per
  * shape and per override set; set the overrides while no call of the library
  * runs on another thread. */
 rnn_status_t rnn_debug_set_plan_overrides(int max_ks_fwd, int max_ks_bwd, int nb_fwd, int nb_bwd, int gemm_bn,
-                                          int gemm_splits, int gemm_tm);
+                                          int gemm_splits, int gemm_tm, int bwd_global_ks);
 
 #ifdef __cplusplus
 }

@@ -196,11 +196,11 @@ def test_null_arguments(lib):
     assert lib.rnn_get_timing(None, None, None) == bad
     assert lib.rnn_debug_skip_arrival(None, 0) == bad
     # plan overrides: out-of-range values are rejected and change nothing
-    for args in ((17, 0, 0, 0, 0, 0, 0), (-1, 0, 0, 0, 0, 0, 0), (0, 0, 3, 0, 0, 0, 0), (0, 0, 0, 8, 0, 0, 0),
-                 (0, 0, 0, 0, 64, 0, 0), (0, 0, 0, 0, 0, 17, 0), (0, 0, 0, 0, 0, 0, 64),
-                 (0, 0, 0, 0, 128, 0, 256)):
+    for args in ((17, 0, 0, 0, 0, 0, 0, 0), (-1, 0, 0, 0, 0, 0, 0, 0), (0, 0, 3, 0, 0, 0, 0, 0),
+                 (0, 0, 0, 8, 0, 0, 0, 0), (0, 0, 0, 0, 64, 0, 0, 0), (0, 0, 0, 0, 0, 17, 0, 0),
+                 (0, 0, 0, 0, 0, 0, 64, 0), (0, 0, 0, 0, 128, 0, 256, 0), (0, 0, 0, 0, 0, 0, 0, 2)):
         assert lib.rnn_debug_set_plan_overrides(*args) == bad, args
-    assert lib.rnn_debug_set_plan_overrides(0, 0, 0, 0, 0, 0, 0) == 0
+    assert lib.rnn_debug_set_plan_overrides(0, 0, 0, 0, 0, 0, 0, 0) == 0
     for q in ("rnn_interleaved_dw_active", "rnn_launch_count", "rnn_selected_algo", "rnn_selected_fwd_algo"):
         assert getattr(lib, q)(None) == 0, q
 

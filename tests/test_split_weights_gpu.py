@@ -1,8 +1,9 @@
 """The tensor-core forward with its weight tile split between tensor memory
 (8 sub-tiles of 64 columns, the MMA A operand) and shared memory (the rest),
-for K slices of more than 512 columns; and the automatic mixed choice, a
-tensor-core forward with the SIMT backward, for layers whose backward has no
-tensor-core plan (hidden 2048).  Against the fp64 oracle, tolerance 2e-2
+for K slices of more than 512 columns, at hidden 2048 with the tensor-core
+backward; and the automatic mixed choice, a tensor-core forward with the SIMT
+backward, for layers whose backward has no tensor-core plan (hidden not a
+multiple of 128).  Against the fp64 oracle, tolerance 2e-2
 (bf16).  A K-split cap of 1 (the plan-override test hook) makes a hidden-1024 forward run
 one 1024-column K slice per 128 gate rows, which takes the split tile."""
 import dataclasses
@@ -50,8 +51,21 @@ def test_split_weight_tile_forward_with_lengths_and_clip(one_k_slice):
 
 
 @pytest.mark.parametrize("mode,ra", [("lstm", False), ("gru", True)])
-def test_hidden_2048_tensor_core_forward_simt_backward(mode, ra):
+def test_hidden_2048_tensor_core_forward_and_backward(mode, ra):
+    # the backward's K split of 8 goes through global memory (16 clusters of
+    # 8 cannot all be resident)
     wl = _wl(mode, ra, 1, False, 6, 4, 64, 2048, 612)
+    inp = synth.make_inputs(wl)
+    gpu = Hn.run_gpu(inp)
+    assert gpu["fwd_algo"] == TC and gpu["algo"] == TC
+    Hn.compare(gpu, Hn.run_oracle(inp), wl)
+
+
+@pytest.mark.parametrize("mode,ra", [("lstm", False), ("gru", True)])
+def test_tensor_core_forward_simt_backward(mode, ra):
+    # hidden 320: the forward's 64-column K slices fit, the backward's
+    # 128-unit row groups do not; the automatic choice mixes the two
+    wl = _wl(mode, ra, 1, False, 6, 8, 64, 320, 614)
     inp = synth.make_inputs(wl)
     gpu = Hn.run_gpu(inp)
     assert gpu["fwd_algo"] == TC and gpu["algo"] == SIMT
