@@ -279,9 +279,10 @@ int rnn_selected_algo(rnn_handle_t handle);
 /* Which recurrent kernel the forward runs (rnn_algo_t values).  Equal to
  * rnn_selected_algo except where the automatic choice runs the forward on the
  * tensor-core kernel and the backward on the SIMT kernel: a bf16 LSTM or GRU
- * layer whose backward has no tensor-core plan (e.g. hidden 2048, where the
- * forward keeps part of its weight tile in tensor memory and the rest in
- * shared memory, or a hidden size that is not a multiple of 128). */
+ * layer whose backward has no tensor-core plan (a hidden size that is a
+ * multiple of 64 but not of 128: the forward's K slices fit, the backward's
+ * 128-unit row groups do not).  Hidden 2048 runs both on tensor cores (the
+ * backward exchanging its K split through global memory). */
 int rnn_selected_fwd_algo(rnn_handle_t handle);
 
 /* Per-kernel-class timing with CUDA events recorded on the launching stream
