@@ -137,6 +137,18 @@ def test_full_lstm2bi_bf16_T512_B128_H1024_sampled():
     Hn.compare(gpu, ref, wl, batch_idx=keep)
 
 
+@pytest.mark.parametrize("name,keep", [("lstm_bf16_T1024_B8_H2048", [3, 6]), ("gru_rb_bf16_T1024_B8_H2048", [0, 7])])
+def test_full_hidden_2048_training_sampled(name, keep):
+    # the latency workloads' shapes trained: tensor-core forward and backward
+    # (the backward's K split through global memory)
+    wl = synth.WORKLOADS[name]
+    full = Hn.masked_dy(synth.make_inputs(wl), keep)
+    gpu = Hn.run_gpu(full)
+    assert gpu["algo"] == 1 and gpu["fwd_algo"] == 1
+    ref = Hn.run_oracle(synth.make_inputs(wl, batch_subset=keep))
+    Hn.compare(gpu, ref, wl, batch_idx=keep)
+
+
 # ---------------------------------------------------------------------------
 # weights that do not fit on chip: the SIMT kernels stream them from L2
 # ---------------------------------------------------------------------------
