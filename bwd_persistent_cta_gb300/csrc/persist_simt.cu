@@ -66,7 +66,7 @@ template <typename T> __host__ __device__ inline int row_pad() { return sizeof(T
 __device__ __forceinline__ float ldcg_f(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ float ldcg_f(const __nv_bfloat16* p) { return __bfloat162float(__ldcg(p)); }
 
-// thread 0 waits on the counter; the verdict is shared with the whole CTA.
+// thread 0 waits on the counter; the outcome is shared with the whole CTA.
 // A direction run by one CTA needs no counter: the block barrier orders its
 // own global writes before its reads.
 __device__ __forceinline__ bool cta_wait(const PersistArgs& a, const unsigned int* ctr, unsigned int target,
