@@ -426,7 +426,8 @@ def run_ours(args):
     Ke = max(3, K // 2)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # dy is needed only by the backward: its upload runs on a copy stream
-    # during the forward (started after e0, waited for before the backward)
+    # during the forward (started once x is in, so the two uploads do not share
+    # the host link; waited for before the backward)
     copy_stream = torch.cuda.Stream(device=dev)
     started, dy_in = torch.cuda.Event(), torch.cuda.Event()
     main = torch.cuda.current_stream()
@@ -434,8 +435,8 @@ def run_ours(args):
     for _ in range(Ke):
         flush.zero_()
         e0.record()
-        started.record()
         x.copy_(xh, non_blocking=True)
+        started.record()
         if wl.forward_only:
             step()
         else:
