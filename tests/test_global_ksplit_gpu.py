@@ -33,6 +33,26 @@ def test_hidden_2048_backward_on_tensor_cores(mode, ra):
     Hn.compare(gpu, Hn.run_oracle(inp), wl)
 
 
+@pytest.mark.parametrize("B", [32, 64])
+def test_hidden_2048_backward_wider_batch(B):
+    # N = 32 / 64 per MMA (one batch part), 2 or 4 pairs per thread
+    wl = _wl("lstm", False, 1, False, 4, B, 64, 2048, 903 + B)
+    inp = synth.make_inputs(wl)
+    gpu = Hn.run_gpu(inp)
+    assert gpu["algo"] == TC
+    Hn.compare(gpu, Hn.run_oracle(inp), wl)
+
+
+def test_hidden_2048_bidirectional_one_direction_per_launch():
+    # both directions need 256 CTAs: the layer runs as one launch per
+    # direction, each with its K split through global memory
+    wl = _wl("gru", True, 1, True, 4, 8, 64, 2048, 905)
+    inp = synth.make_inputs(wl)
+    gpu = Hn.run_gpu(inp)
+    assert gpu["algo"] == TC
+    Hn.compare(gpu, Hn.run_oracle(inp), wl)
+
+
 @pytest.mark.parametrize("mode,ra,L,bidir,T,B,H", [("lstm", False, 2, True, 7, 16, 256),
                                                    ("gru", True, 1, True, 6, 33, 128),
                                                    ("gru", False, 2, False, 5, 8, 256),
