@@ -28,6 +28,7 @@ struct TcPlan {
   uint32_t off_stage = 0;   // forward K split: warp 0's post-step stage (0: none)
   size_t smem = 0;
   int gk = 0;               // backward: K-split partials through global memory, no clusters
+  int recv2 = 0;            // K split over a cluster: one receive buffer per exchange parity
 };
 
 size_t a1k(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
@@ -112,10 +113,15 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
       if (gk && (KS == 1 || ndir * NB * nrg > 64)) continue;
       const size_t wbytes = static_cast<size_t>(nsub) * kWSub;
       const size_t rb = static_cast<size_t>(Npad) * 128;
-      const size_t recv = static_cast<size_t>(Npad) * 128 * 4;
+      // a K split over a cluster receives into one buffer per exchange
+      // parity: a peer may push the next exchange's partials while this CTA
+      // still reads the current ones (it can push the one after only once this
+      // CTA has passed the next cluster barrier, after those reads)
+      const size_t recv1 = static_cast<size_t>(Npad) * 128 * 4;
+      const size_t recv = (KS > 1 && !gk) ? 2 * recv1 : recv1;
       // without a K split the forward stages warp 0's post-step values (32 B
       // per pair) in the receive buffer
-      if (KS == 1 && !bwd && recv < static_cast<size_t>(32) * PP * 32) continue;
+      if (KS == 1 && !bwd && recv1 < static_cast<size_t>(32) * PP * 32) continue;
       // weight tile in shared memory, with the deepest exchange ring that fits
       int R = nsub < kMaxRing ? nsub : kMaxRing;
       size_t smem = 0;
@@ -169,6 +175,7 @@ int make_plans(int mode, int bwd, int H, int B, int ndir, int num_sms, TcPlan* o
       p.smem = smem < floor ? floor : smem;
       p.wcol = wt ? 512u - 32u * static_cast<uint32_t>(wt) : 0u;
       p.gk = gk;
+      p.recv2 = (KS > 1 && !gk) ? 1 : 0;
       cands.emplace_back(plan_cost(bwd, KS, Kc, Npad, UPC * Bp, gk), p);
     }
   }
@@ -393,6 +400,7 @@ int launch(const PersistArgs& a, int bwd, cudaStream_t s, int num_sms) {
   P.prefetch = !bwd && proj_bytes > (32ull << 20);
   P.wcol = pl.wcol;
   P.gk = pl.gk;
+  P.recv2 = pl.recv2;
   const void* fn = kernel_for(bwd, pl.PP, pl.KS, ext);
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];

@@ -114,7 +114,14 @@ struct TcPersistParams {
   uint32_t off_ring, off_recv, off_bar;
   uint32_t off_stage;      // forward with a K split: warp 0's post-step stage, 0 = none
   int gk;                  // backward: the K-split partials go through global memory (a.gk_buf), no cluster
+  int recv2;               // K split over a cluster: receive buffer (exchange index & 1); else one buffer
 };
+
+// Byte offset of exchange e's receive buffer: with a K split over a cluster
+// a peer may push exchange e + 1's partials while this CTA still reads e's.
+__device__ __forceinline__ uint32_t recv_off(const TcPersistParams& P, int e) {
+  return (P.recv2 && (e & 1)) ? static_cast<uint32_t>(P.Npad) * 128 * 4 : 0u;
+}
 
 struct TcBars {
   uint64_t wbar;                 // resident weight tile landed (TMA)
@@ -366,7 +373,7 @@ __device__ __forceinline__ bool step_exchange(const TcPersistParams& P, const CU
     if (ok) {
       tc_fence_after();
       if (P.gk) push_partials_global(P, tmem, gk.buf + static_cast<size_t>(s & 1) * P.KS * P.Npad * 128, ks);
-      else push_partials(P, tmem, recv, ks);
+      else push_partials(P, tmem, recv + recv_off(P, s) / 4, ks);
     }
   }
   RNN_TRACE_AT(9, tk, s);
@@ -836,7 +843,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       const int ul = id % UPC, bl = id / UPC;
       acc[p] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (id < npairs) {
-        const uint32_t ra = recv_s + static_cast<uint32_t>((bl * RPC + 4 * ul) * 4);
+        const uint32_t ra = recv_s + recv_off(P, ex) + static_cast<uint32_t>((bl * RPC + 4 * ul) * 4);
         float4 v[KS];
 #pragma unroll
         for (int r = 0; r < KS; ++r) v[r] = lds_f4(ra + r * src_bytes);
@@ -914,7 +921,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
           const int id = threadIdx.x + p * kThreads;
           if (id >= npairs) break;
           const int ul = id % UPC, bl = id / UPC, b = b0 + bl, u = ubase + ul;
-          const uint32_t ra = recv_s + static_cast<uint32_t>((bl * RPC + 4 * ul + 2) * 4);
+          const uint32_t ra = recv_s + recv_off(P, ex + 1) + static_cast<uint32_t>((bl * RPC + 4 * ul + 2) * 4);
           float sn = 0.f;
 #pragma unroll
           for (int r = 0; r < KS; ++r) sn += lds_f1(ra + r * src_bytes);
@@ -1108,7 +1115,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
           for (int jj = 0; jj < V; ++jj) dhs[q * V + jj] = v[jj];
         }
       } else {
-        const uint32_t ra = recv_s + static_cast<uint32_t>((rl * RPC + ul0) * 4);
+        const uint32_t ra = recv_s + recv_off(P, s * ph) + static_cast<uint32_t>((rl * RPC + ul0) * 4);
         float v[KS][V];
 #pragma unroll
         for (int r = 0; r < KS; ++r) lds_v<V>(ra + r * src_bytes, v[r]);
@@ -1233,7 +1240,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
           const int rl = rl0 + q * RPT;
           if (rl >= Bn) break;
           const int b = b0 + rl;
-          const uint32_t ra = recv_s + static_cast<uint32_t>((rl * RPC + ul0) * 4);
+          const uint32_t ra = recv_s + recv_off(P, 2 * s + 1) + static_cast<uint32_t>((rl * RPC + ul0) * 4);
           float v[KS][V];
 #pragma unroll
           for (int r = 0; r < KS; ++r) lds_v<V>(ra + r * src_bytes, v[r]);
