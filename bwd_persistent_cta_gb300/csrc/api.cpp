@@ -237,6 +237,27 @@ int run_persist(rnn_handle_s* h, PersistArgs a, bool bwd, cudaStream_t s) {
   a.dev = h->dev;
   a.timeout_ns = h->timeout_ns;
   a.skip_cta = h->skip_cta;
+#ifdef RNN_CHECKS
+  // checking builds: every buffer the steps exchange through starts as 0xFF
+  // bytes (a NaN no kernel writes), so a slice read before its producers
+  // wrote it shows (the kernels scan each landed slice).  Once per layer,
+  // before the first launch: per-direction launches share the buffers.
+  {
+    const size_t es = h->bf16 ? 2 : 4;
+    const size_t TB = static_cast<size_t>(a.T) * a.B;
+    const size_t slot = static_cast<size_t>(a.B) * a.D * a.H * es;   // one step of Y
+    auto poison = [&](void* p, size_t bytes) { return !p || cudaMemsetAsync(p, 0xFF, bytes, s) == cudaSuccess; };
+    bool ok = true;
+    if (!bwd) {
+      ok = poison(static_cast<char*>(a.Y) + slot, slot * a.T) && ok;   // slots 1 .. T (0 and T + 1 hold h0)
+      if (a.mode == 1 && !a.reset_after && a.RH) ok = poison(a.RH, TB * a.D * a.H * es) && ok;
+    } else {
+      ok = poison(a.dG, TB * a.D * 4 * a.H * es) && ok;
+      if (a.XA) ok = poison(a.XA, TB * a.D * 4 * a.H * es) && ok;
+    }
+    if (!ok) return 3;
+  }
+#endif
   auto go = [&](PersistArgs& x) -> int {
     int rc = reset_counters(h, s);
     if (rc) return rc;

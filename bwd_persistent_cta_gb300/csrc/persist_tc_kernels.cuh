@@ -421,6 +421,35 @@ __device__ __forceinline__ bool step_exchange(const TcPersistParams& P, const CU
   return any == 0;
 }
 
+// Checking builds (-DRNN_CHECKS): the host fills the buffers the step
+// exchanges go through with 0xFF bytes (bf16 0xFFFF, a NaN no kernel writes)
+// before each persistent launch; after every contraction, all threads scan
+// the slice that landed in shared memory (whole K slice per TMA only) for the
+// pattern in this CTA's batch rows and record RNN_INTERNAL / W_CHECK with the
+// step in the status word: a slice read before its producers wrote it.
+__device__ __forceinline__ void check_slice(const TcPersistParams& P, const uint8_t* ring, int rows,
+                                            unsigned int kernel, int s) {
+#ifdef RNN_CHECKS
+  if (!P.single) return;
+  const int per_sub = P.Npad * 8;          // 16-byte pieces per sub-tile (Npad rows of 128 bytes)
+  const int n16 = P.nsub * per_sub;
+  const uint32_t rbytes = static_cast<uint32_t>(P.Npad) * 128;
+  int bad = 0;
+  for (int i = threadIdx.x; i < n16; i += kThreads) {
+    const int j = i / per_sub, rem = i - j * per_sub;
+    if (rem / 8 >= rows) continue;
+    const uint4 q = *reinterpret_cast<const uint4*>(ring + j * rbytes + rem * 16);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) bad |= ((w[e] & 0xFFFFu) == 0xFFFFu) || ((w[e] >> 16) == 0xFFFFu);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0)
+    report_status(P.a.dev, 6u /* RNN_INTERNAL */, kernel, static_cast<unsigned>(s), W_CHECK);
+#else
+  (void)P; (void)ring; (void)rows; (void)kernel; (void)s;
+#endif
+}
+
 // After the exchange-critical stores of a step.  Each thread orders its own
 // generic-proxy stores before the TMA (async-proxy) reads that other CTAs issue
 // once they observe the counter; the barrier orders every thread's stores
@@ -835,6 +864,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       aborted = true;
       break;
     }
+    check_slice(P, ring, Bn, K_FWD_TC, s);
     // partial sums of every pair first (all shared loads in flight), then the cell
     float4 acc[PP];
 #pragma unroll
@@ -916,6 +946,7 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
           aborted = true;
           break;
         }
+        check_slice(P, ring, Bn, K_FWD_TC, s);
 #pragma unroll
         for (int p = 0; p < PP; ++p) {
           const int id = threadIdx.x + p * kThreads;
@@ -1099,6 +1130,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
       aborted = true;
       break;
     }
+    if (s > 0) check_slice(P, ring, Bn, K_BWD_TC, s);
     // recurrent gradient of every pair first (all shared loads in flight)
     float dhs[PP];
 #pragma unroll
@@ -1234,6 +1266,7 @@ persist_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
           aborted = true;
           break;
         }
+        check_slice(P, ring, Bn, K_BWD_TC, s);
         // phase B: dr; dG = [dr, dz, dn, 0]; the carry to the step before
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {

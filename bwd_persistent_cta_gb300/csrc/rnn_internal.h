@@ -53,7 +53,9 @@ struct DevArea {
 static_assert(sizeof(DevArea) == 1024, "DevArea is 1 KB");
 
 enum KernelId : unsigned int { K_FWD_SIMT = 1, K_BWD_SIMT = 2, K_FWD_TC = 3, K_BWD_TC = 4, K_GEMM_TC = 5 };
-enum WaitKind : unsigned int { W_COUNTER = 1, W_TMA = 2, W_MMA = 3 };
+// W_CHECK (checking builds, -DRNN_CHECKS): an exchanged slice held the poison
+// pattern, i.e. it was read before its producer wrote it.
+enum WaitKind : unsigned int { W_COUNTER = 1, W_TMA = 2, W_MMA = 3, W_CHECK = 4 };
 
 // C[row(m), n] = sum_k A(m, k) * B(n, k)  (+ bias[n]) (+ C_old if beta)
 //   A(m, k) = A[m*lda + k] (a_kmajor) or A[k*lda + m];  same for B with n.
