@@ -1,50 +1,60 @@
 // persist_tc_kernels.cuh - persistent recurrent kernels on the tcgen05 tensor cores
 // (bf16 operands, fp32 accumulation in tensor memory), forward and backward
-// through time, for LSTM and GRU resetAfter (and the GRU reset-before
-// forward, in the extended variant).
+// through time, for LSTM, GRU resetAfter and GRU reset-before (the latter in
+// the extended variant).
 //
 // Work split.  The per-step recurrent contraction is swapped so that the
 // weights are the M=128 operand and the batch is N:
 //   forward   S^T[4H, B]  = W_hh[4H, H] . h_{t-1}^T[H, B]
 //   backward  dh^T[H, B]  = W_hh^T[H, 4H] . dG^T_{t+1}[4H, B]
-// A cluster of KS CTAs owns one 128-row block of the weight operand and one
-// batch part (NB parts of Bp rows split the batch); CTA rank ks owns the K
-// slice [ks*K/KS, (ks+1)*K/KS) and keeps that 128 x K/KS bf16 tile resident
-// for the whole sequence - in shared memory (loaded once by TMA), in tensor
-// memory as the MMA A operand, or split between the two - and owns the
-// 128/KS rows [ks*128/KS, (ks+1)*128/KS) of the result for its batch part.
+// KS CTAs own one 128-row block of the weight operand and one batch part (NB
+// parts of Bp rows split the batch); CTA ks owns the K slice
+// [ks*K/KS, (ks+1)*K/KS) and keeps that 128 x K/KS bf16 tile resident for the
+// whole sequence - in shared memory (loaded once by TMA), in tensor memory as
+// the MMA A operand, or split between the two - and owns the 128/KS rows
+// [ks*128/KS, (ks+1)*128/KS) of the result for its batch part.  The KS CTAs
+// are one thread-block cluster, or, for a backward whose clusters cannot all
+// be resident, a group that exchanges through global memory.
 //
 // Each step a CTA
-//   1. waits (bounded) until every CTA of its direction finished the previous
-//      step: one gpu-scope counter per direction, release add / acquire poll;
-//   2. streams its K slice of the previous state (h_{t-1} rows of the layer
-//      output, or the gate gradients of the step after) with TMA through a
-//      ring of 64-column sub-tiles, issuing tcgen05.mma (M=128, N=B rounded up
-//      to 16, K=16) into a TMEM accumulator as sub-tiles land;
-//   3. pushes each accumulator row (tcgen05.ld) straight into the shared
-//      memory of the cluster peer that owns that row (posted distributed
-//      shared-memory stores), together with its abort flag;
-//   4. after one cluster barrier sums the KS partial rows of its own units
-//      from local shared memory, applies the cell (forward) or its derivative
-//      (backward) in registers - the LSTM cell state, the GRU state and the
-//      backward carries never leave registers - stores the exchanged values,
-//      arrives on the counter, and only then stores what no CTA of this
-//      launch waits for.
+//   1. waits (bounded) on the step counter of the K slice it contracts: one
+//      gpu-scope counter per (direction, batch part, K slice), advanced by
+//      the CTAs whose outputs form that slice (release add / acquire poll);
+//   2. brings its K slice of the previous state (h_{t-1} rows of the layer
+//      output, or the gate gradients of the step after) into shared memory
+//      with TMA (4-D boxes for the whole slice, or a ring of 64-column
+//      sub-tiles), issuing tcgen05.mma (M=128, N=B rounded up to 16, K=16)
+//      into a TMEM accumulator as the pieces land;
+//   3. pushes each accumulator row (tcgen05.ld) into the shared memory of the
+//      cluster peer that owns that row (posted distributed shared-memory
+//      stores, one receive buffer per exchange parity), together with its
+//      abort flag - or, without a cluster, writes them to the group's buffer
+//      in global memory and copies its own rows back after the group's
+//      counter says every peer has written;
+//   4. after one cluster barrier sums the KS partial rows of its own units,
+//      applies the cell (forward) or its derivative (backward) in registers -
+//      the LSTM cell state, the GRU state and the backward carries never leave
+//      registers - stores the exchanged values and arrives on the counter of
+//      the slice they form.  The forward stores what no CTA of the launch
+//      waits for (gates, c, the caller's y) during the next step's
+//      contraction instead.
 // Extended variant (template flag EXT, used when sequence lengths or LSTM cell
-// clipping are set, and for the GRU reset-before forward; the plain variant
-// compiles without them):
+// clipping are set, and for GRU reset-before; the plain variant compiles
+// without them):
 //  * variable sequence lengths: at a step t >= len[b] the pair (u, b) keeps
 //    its state (h, c) and stores it unchanged, and the backward step writes
 //    zero gate gradients and passes the state gradients on (LSTM: an extra
 //    register carries dh past such steps);
 //  * LSTM cell clipping: every use of the raw cell state goes through
 //    clip = min(max(c, lo), hi), and the backward multiplies by dclip;
-//  * GRU reset-before forward: two exchanges per step, the second over
-//    r * h_{t-1}, which each CTA stores for its units in between.
+//  * GRU reset-before: two exchanges per step.  Forward: the second is over
+//    r * h_{t-1}, which each CTA stores for its units in between.  Backward:
+//    the first contracts [0, 0, dn, 0] (d(rh) = W_hn^T dn), the second the
+//    gate gradients [dr, dz, dn, 0].
 // Cluster-uniform abort: every CTA reads the same set of flags after the same
 // barrier, so all CTAs of a cluster leave at the same step (after one more
 // cluster barrier, so no CTA exits while a peer may still touch its shared
-// memory).
+// memory); a group without a cluster shares one abort flag in global memory.
 //
 // This is the persistent-RNN design of the persistent RNN backward-data kernel
 // page (one launch for all steps, weights resident on chip, a per-step
