@@ -59,6 +59,8 @@ _SIGS = {
     "rnn_selected_fwd_algo": (ctypes.c_int, [_P]),
     "rnn_debug_skip_arrival": (ctypes.c_int, [_P, ctypes.c_int]),
     "rnn_debug_set_plan_overrides": (ctypes.c_int, [ctypes.c_int] * 8),
+    "rnn_debug_gemm_plan": (ctypes.c_int, [ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_size_t,
+                                            ctypes.c_int, _P]),
     "rnn_debug_tc_plans": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "rnn_debug_simt_plan": (ctypes.c_int, [ctypes.c_int] * 9 + [ctypes.POINTER(ctypes.c_int)]),
@@ -227,6 +229,18 @@ def rnn_get_timing_ex(handle):
     if rc != RNN_OK:
         raise RnnError(rc, "rnn_get_timing_ex")
     return list(ms), [int(v) for v in n], list(by)
+
+
+def rnn_debug_gemm_plan(shapes, K: int, fp32_out: bool, ws_bytes: int, num_sms: int):
+    """(tile width, K split, tile rows) the tensor-core GEMM planner picks for
+    one grouped launch of GEMMs [(M, N), ...] of depth K (host arithmetic)."""
+    n = len(shapes)
+    Ms = (ctypes.c_int * n)(*[int(m) for m, _ in shapes])
+    Ns = (ctypes.c_int * n)(*[int(nn) for _, nn in shapes])
+    out = (ctypes.c_int * 3)()
+    if not lib().rnn_debug_gemm_plan(n, Ms, Ns, int(K), int(bool(fp32_out)), int(ws_bytes), int(num_sms), out):
+        raise ValueError("invalid GEMM plan query")
+    return tuple(out)
 
 
 def rnn_debug_tc_plans(mode: int, bwd: int, hidden: int, batch: int, ndir: int, num_sms: int, max_out: int = 16):

@@ -680,6 +680,26 @@ int launch_gemm_tc_grouped(const GemmArgs* gs, int n, cudaStream_t s, int num_sm
                       : launch_bn<128, 128>(gs, n, pl.S, s, num_sms, dev, timeout_ns);
 }
 
+// Planner hook (host arithmetic only): the plan of a grouped launch of n
+// GEMMs (sizes M[i] x N[i], common K), fp32 outputs with split scratch of
+// ws_bytes when fp32_out, else bf16.  out = {tile width, K split, tile rows}.
+extern "C" int rnn_debug_gemm_plan(int n, const int* M, const int* N, int K, int fp32_out, size_t ws_bytes,
+                                   int num_sms, int* out) {
+  if (n < 1 || n > kMaxGroups || !M || !N || !out || K <= 0 || num_sms <= 0) return 0;
+  GemmArgs gs[kMaxGroups];
+  static char dummy;
+  for (int i = 0; i < n; ++i) {
+    if (M[i] <= 0 || N[i] <= 0) return 0;
+    gs[i].M = M[i]; gs[i].N = N[i]; gs[i].K = K;
+    gs[i].c_bf16 = fp32_out ? 0 : 1;
+    gs[i].split_ws = fp32_out && ws_bytes ? &dummy : nullptr;
+    gs[i].split_ws_bytes = ws_bytes;
+  }
+  const GemmPlan pl = plan_gemm(gs, n, num_sms);
+  out[0] = pl.BN; out[1] = pl.S; out[2] = pl.TM;
+  return 1;
+}
+
 int launch_gemm_tc(const GemmArgs& g, cudaStream_t s, int num_sms, DevArea* dev, uint64_t timeout_ns,
                    int* launches) {
   if (launches) *launches = 1;

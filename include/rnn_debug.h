@@ -43,6 +43,14 @@ rnn_status_t rnn_debug_gemm(int M, int N, int K, const void* A, int64_t lda, int
  * written (at most max_out). */
 int rnn_debug_tc_plans(int mode, int bwd, int hidden, int batch, int ndir, int num_sms, int* out, int max_out);
 
+/* Planner hook: the tensor-core GEMM's plan for one grouped launch (host
+ * arithmetic only): n GEMMs (1..6) of M[i] x N[i] with the common depth K;
+ * fp32_out != 0: fp32 outputs with ws_bytes of split-K scratch (0: no K
+ * split), else bf16 outputs.  out[0..2] = {tile width (128 or 256), K split,
+ * tile rows (128 or 256)}.  Returns 1, or 0 for invalid arguments. */
+int rnn_debug_gemm_plan(int n, const int* M, const int* N, int K, int fp32_out, size_t ws_bytes, int num_sms,
+                        int* out);
+
 /* Planner hook: the SIMT persistent kernel's plan for one launch shape (host
  * arithmetic only).  dwhh != 0 plans with the interleaved dW_hh accumulator.
  * out[0..6] = {units per CTA, CTAs per direction, pairs per thread, weights

@@ -1,8 +1,9 @@
-"""Host logic of the tensor-core planner (no GPU): the candidate ranking by the
-per-step cost estimate, followed by the co-residency filter the launch applies
-(emulated here with the limits measured on the 152-SM GB300: 7 clusters of 16
-CTAs, 15 of 8, 36 of 4 at one CTA per SM).  Each pinned choice is the plan
-measured fastest for that shape."""
+"""Host logic of the tensor-core planners (no GPU): the persistent kernels'
+candidate ranking by the per-step cost estimate, followed by the co-residency
+filter the launch applies (emulated here with the limits measured on the
+152-SM GB300: 7 clusters of 16 CTAs, 15 of 8, 36 of 4 at one CTA per SM), and
+the GEMM's tile shape and K split.  Each pinned choice is the plan measured
+fastest for that shape."""
 import os
 import sys
 
@@ -172,3 +173,37 @@ def test_simt_plan_invariants_sweep(R, mode, ra, bf16, bwd):
                 if bwd and q is not None:
                     assert q["nu"] * H * B <= 16384 and not q["stream"] and q["smem"] <= 200 * 1024
     assert planned > 0
+
+
+# ---------------------------------------------------------------------------
+# tensor-core GEMM planner (host arithmetic): tile width, K split, tile rows
+# ---------------------------------------------------------------------------
+GIB = 1 << 30
+
+
+@pytest.mark.parametrize("shapes,K,fp32,ws,expect", [
+    # 2-layer bidirectional LSTM H1024 weight gradients (one launch per layer): 256-row tiles, no split
+    ([(4096, 1024)] * 4, 65536, True, GIB, (256, 1, 256)),
+    ([(4096, 2048), (4096, 1024)] * 2, 65536, True, GIB, (256, 1, 256)),
+    # its dX (K = 8192) and projections (K = 1024 / 2048, bf16 output)
+    ([(65536, 1024)], 8192, False, 0, (256, 1, 256)),
+    ([(65536, 8192)], 1024, False, 0, (256, 1, 128)),
+    ([(65536, 8192)], 2048, False, 0, (256, 1, 128)),
+    # GRU H512 T128 B64 weight gradients: 64 tiles of 128 x 256 split in two
+    ([(2048, 512)] * 2, 8192, True, 32 << 20, (256, 2, 128)),
+    # without split scratch the same launch cannot split: 128-wide tiles double the tile count
+    ([(2048, 512)] * 2, 8192, True, 0, (128, 1, 128)),
+    # LSTM H1024 T256 B32 weight gradients: 128 tiles of 256 x 256 fill one wave
+    ([(4096, 1024)] * 2, 8192, True, 64 << 20, (256, 1, 256)),
+    # a small GEMM: 128-wide tiles double the tile count
+    ([(256, 256)], 64, False, 0, (128, 1, 128)),
+])
+def test_gemm_plan(R, shapes, K, fp32, ws, expect):
+    assert R.rnn_debug_gemm_plan(shapes, K, fp32, ws, SMS) == expect
+
+
+def test_gemm_plan_rejects_bad_queries(R):
+    with pytest.raises(ValueError):
+        R.rnn_debug_gemm_plan([(0, 16)], 64, False, 0, SMS)
+    with pytest.raises(ValueError):
+        R.rnn_debug_gemm_plan([(16, 16)] * 7, 64, False, 0, SMS)
