@@ -750,6 +750,11 @@ persist_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
   // step's release; the rest is stored during the next step's contraction
   float hv[PP];
   float gq[PP][4];
+#pragma unroll
+  for (int p = 0; p < PP; ++p) {
+    hv[p] = 0.f;
+    gq[p][0] = gq[p][1] = gq[p][2] = gq[p][3] = 0.f;
+  }
   // stores of step sd that no CTA of this launch waits for (pair id: its 4
   // gate values, the new state h, the LSTM cell c and the output y), and the
   // L2 prefetch of a later step's projections
